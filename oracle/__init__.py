@@ -1,0 +1,247 @@
+"""fp64 CPU oracle for decode attention with KV append, GQA, window and sinks.
+
+TEST INFRASTRUCTURE: only the tests, the smoke check and the benchmark's CPU
+baseline leg use this package. It shares no code with the CUDA path.
+
+The arithmetic lives in ``oracle.c`` (see its header for the definition and the
+passage it follows: SimpleLLM README, changes table, rows "one decode-attention
+kernel for sinks, sliding window, GQA and the KV append", "paged KV cache for
+full-attention layers" and "ring buffer for sliding-window layers"). This module
+only marshals numpy arrays into it. bf16 tensors travel as their raw 16-bit
+patterns (``numpy.uint16``).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        c_int, c_double = ctypes.c_int, ctypes.c_double
+        lib.oracle_decode_paged.argtypes = [
+            _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _f32p, c_int, c_double, _f64p,
+            c_int, c_int, c_int, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_decode_ring.argtypes = [
+            _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _f32p, c_int, c_double, _f64p,
+            c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_decode_contig.argtypes = [
+            _u16p, _u16p, _u16p, _i32p, c_int, _f32p, c_int, c_double, _f64p,
+            c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_kv_append_paged.argtypes = [
+            _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, c_int, c_int, c_int, c_int, c_int, c_int]
+        lib.oracle_kv_append_ring.argtypes = [
+            _u16p, _u16p, _u16p, _u16p, _i32p, c_int, c_int, c_int, c_int]
+        lib.oracle_scatter_paged.argtypes = [
+            _u16p, _u16p, _i32p, c_int, _i32p, _u16p, _u16p, c_int, c_int, c_int, c_int, c_int,
+            c_int]
+        lib.oracle_scatter_ring.argtypes = [
+            _u16p, _u16p, _i32p, c_int, c_int, _u16p, _u16p, c_int, c_int, c_int]
+        for name in ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
+                     "oracle_kv_append_paged", "oracle_kv_append_ring",
+                     "oracle_scatter_paged", "oracle_scatter_ring"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def load_library(path):
+    """Point this wrapper at another build of the oracle (used by the tests
+    that plant mistakes in a copy of oracle.c). Returns the previous handle."""
+    global _lib
+    prev = _lib
+    ref = _load()
+    lib = ctypes.CDLL(path)
+    for fn in ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
+               "oracle_kv_append_paged", "oracle_kv_append_ring",
+               "oracle_scatter_paged", "oracle_scatter_ring"):
+        f_new, f_ref = getattr(lib, fn), getattr(ref, fn)
+        f_new.argtypes, f_new.restype = f_ref.argtypes, f_ref.restype
+    _lib = lib
+    return prev
+
+
+def restore_library(prev):
+    global _lib
+    _lib = prev
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count())
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctype)
+
+
+def _u16(a, name):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"{name}: expected uint16 bf16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _items(items):
+    if items is None:
+        return None, 0
+    arr = np.ascontiguousarray(np.asarray(items, dtype=np.int32).reshape(-1, 2))
+    return arr, arr.shape[0]
+
+
+def _check(status, what):
+    if status != 0:
+        raise ValueError(f"{what}: oracle returned {status} (bad argument or index)")
+
+
+def decode_paged(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window, scale,
+                 page_size, items=None, nthreads=None):
+    """Attention output in fp64, shape [B, Hq, D] (or [n_items, D] for sampled items).
+
+    q: [B, Hq, D] u16; k_new/v_new: [B, Hkv, D] u16 or None (no append: token p
+    is read from the cache); k_cache/v_cache: [num_pages, Hkv, P, D] u16;
+    block_table: [B, max_pages] int32; seq_lens: [B] int32 (post-append);
+    sinks: [Hq] float32 or None; window: 0 = full attention.
+    """
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    k_cache, v_cache = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_cache.shape
+    assert D2 == D and P == page_size and v_cache.shape == k_cache.shape
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_paged(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(k_cache, _u16p),
+        _ptr(v_cache, _u16p), _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(sk, _f32p), int(window),
+        float(scale), _ptr(out, _f64p), B, Hq, Hkv, D, P, bt.shape[1], num_pages,
+        _ptr(it, _i32p), n_items, nthreads or default_threads())
+    _check(st, "decode_paged")
+    return out
+
+
+def decode_ring(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, window, scale, items=None,
+                nthreads=None):
+    """Attention over a ring cache k_cache [B, Hkv, W, D] (W = window = capacity)."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    k_cache, v_cache = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    sl, sk = _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    B2, Hkv, W, D2 = k_cache.shape
+    assert B2 == B and D2 == D and W == window
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_ring(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(k_cache, _u16p),
+        _ptr(v_cache, _u16p), _ptr(sl, _i32p), _ptr(sk, _f32p), int(window), float(scale),
+        _ptr(out, _f64p), B, Hq, Hkv, D, _ptr(it, _i32p), n_items,
+        nthreads or default_threads())
+    _check(st, "decode_ring")
+    return out
+
+
+def decode_contig(q, hist_k, hist_v, seq_lens, sinks, window, scale, items=None, nthreads=None):
+    """Attention over a contiguous history hist [B, Tmax, Hkv, D] that already
+    holds the new token at position L - 1. window = 0 means full attention."""
+    lib = _load()
+    q, hist_k, hist_v = _u16(q, "q"), _u16(hist_k, "hist_k"), _u16(hist_v, "hist_v")
+    sl, sk = _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    B2, Tmax, Hkv, D2 = hist_k.shape
+    assert B2 == B and D2 == D
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_contig(
+        _ptr(q, _u16p), _ptr(hist_k, _u16p), _ptr(hist_v, _u16p), _ptr(sl, _i32p), Tmax,
+        _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D,
+        _ptr(it, _i32p), n_items, nthreads or default_threads())
+    _check(st, "decode_contig")
+    return out
+
+
+def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, seq_lens):
+    """Return copies of the paged caches with each active sequence's new token written."""
+    lib = _load()
+    k_new, v_new = _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    kc, vc = np.array(k_cache, dtype=np.uint16, copy=True), np.array(v_cache, dtype=np.uint16,
+                                                                      copy=True)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    num_pages, Hkv, P, D = kc.shape
+    st = lib.oracle_kv_append_paged(
+        _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(kc, _u16p), _ptr(vc, _u16p),
+        _ptr(bt, _i32p), _ptr(sl, _i32p), sl.shape[0], Hkv, D, P, bt.shape[1], num_pages)
+    _check(st, "kv_append_paged")
+    return kc, vc
+
+
+def kv_append_ring(k_new, v_new, k_cache, v_cache, seq_lens, window):
+    """Return copies of the ring caches with each active sequence's new token written."""
+    lib = _load()
+    k_new, v_new = _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    kc, vc = np.array(k_cache, dtype=np.uint16, copy=True), np.array(v_cache, dtype=np.uint16,
+                                                                      copy=True)
+    sl = _i32(seq_lens)
+    B, Hkv, W, D = kc.shape
+    assert W == window
+    st = lib.oracle_kv_append_ring(
+        _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(kc, _u16p), _ptr(vc, _u16p),
+        _ptr(sl, _i32p), int(window), B, Hkv, D)
+    _check(st, "kv_append_ring")
+    return kc, vc
+
+
+def scatter_paged(hist_k, hist_v, n_tokens, block_table, k_cache, v_cache):
+    """Write tokens 0..n[b]-1 of each history into (copies of) the paged caches."""
+    lib = _load()
+    hist_k, hist_v = _u16(hist_k, "hist_k"), _u16(hist_v, "hist_v")
+    kc, vc = np.array(k_cache, dtype=np.uint16, copy=True), np.array(v_cache, dtype=np.uint16,
+                                                                      copy=True)
+    n, bt = _i32(n_tokens), _i32(block_table)
+    B, Tmax, Hkv, D = hist_k.shape
+    num_pages, Hkv2, P, D2 = kc.shape
+    assert Hkv2 == Hkv and D2 == D
+    st = lib.oracle_scatter_paged(
+        _ptr(hist_k, _u16p), _ptr(hist_v, _u16p), _ptr(n, _i32p), Tmax, _ptr(bt, _i32p),
+        _ptr(kc, _u16p), _ptr(vc, _u16p), B, Hkv, D, P, bt.shape[1], num_pages)
+    _check(st, "scatter_paged")
+    return kc, vc
+
+
+def scatter_ring(hist_k, hist_v, n_tokens, window, k_cache, v_cache):
+    """Write the ring state after n[b] tokens into (copies of) the ring caches."""
+    lib = _load()
+    hist_k, hist_v = _u16(hist_k, "hist_k"), _u16(hist_v, "hist_v")
+    kc, vc = np.array(k_cache, dtype=np.uint16, copy=True), np.array(v_cache, dtype=np.uint16,
+                                                                      copy=True)
+    n = _i32(n_tokens)
+    B, Tmax, Hkv, D = hist_k.shape
+    st = lib.oracle_scatter_ring(
+        _ptr(hist_k, _u16p), _ptr(hist_v, _u16p), _ptr(n, _i32p), Tmax, int(window),
+        _ptr(kc, _u16p), _ptr(vc, _u16p), B, Hkv, D)
+    _check(st, "scatter_ring")
+    return kc, vc

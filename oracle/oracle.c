@@ -1,0 +1,337 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for one decode step of attention with a
+ * KV append, grouped-query heads, an optional sliding window and a per-head
+ * attention-sink logit, over three cache layouts (paged, ring, contiguous).
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark load this library. The CUDA path shares no
+ * code, header, table or helper with it, and never calls it.
+ *
+ * What is computed (SimpleLLM README, changes table, row "one decode-attention
+ * kernel for sinks, sliding window, GQA and the KV append"; the paged cache
+ * and the ring buffer come from the rows "paged KV cache for full-attention
+ * layers" and "ring buffer for sliding-window layers" of the same table). The
+ * pages print no formula, so the definition below is the plain reading:
+ *
+ *   for each active sequence b (seq_lens[b] = L > 0, the length *after* the
+ *   new token is appended; the new token sits at position p = L - 1),
+ *   each query head h, and KV head g = h / (Hq / Hkv)   (grouped-query):
+ *     J      = positions j with lo <= j < L, lo = max(0, L - W) when a window
+ *              W > 0 applies, else lo = 0        (window includes token p)
+ *     s_j    = scale * sum_d q[b,h,d] * k_j[g,d]
+ *     M      = max(sigma_h, max_j s_j)            (sigma_h = sink logit, or
+ *                                                  -inf when there is none)
+ *     out    = sum_j e^(s_j - M) v_j[g,:] / (e^(sigma_h - M) + sum_j e^(s_j - M))
+ *   and out = 0 for an inactive sequence (L = 0).
+ *
+ * Token j < p is read from the cache through the layout's address map; token
+ * p is k_new / v_new (when given) -- the append happens before attention.
+ *
+ * Layouts (element = bf16, given as raw 16-bit patterns):
+ *   paged : k_cache[num_pages][Hkv][P][D]; token j of b lives in page
+ *           block_table[b][j / P], slot j % P.
+ *   ring  : k_cache[B][Hkv][W][D]; token j of b lives in cell j % W.
+ *   contig: hist[B][Tmax][Hkv][D]; token j of b is hist[b][j] (includes p).
+ *
+ * Every bf16 input is widened exactly to double; all arithmetic is fp64 with
+ * libm exp(). Work is split over (b, h) pairs across POSIX threads; each pair
+ * is computed exactly as written above, no blocking or reordering.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_OK 0
+#define OR_BAD_ARG (-1)
+#define OR_BAD_INDEX (-2)
+#define OR_NOMEM (-3)
+
+static double bf16_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------ */
+/* Layout descriptions: each maps (b, g, position j) to a key/value row. */
+
+enum layout_kind { LAYOUT_PAGED = 0, LAYOUT_RING = 1, LAYOUT_CONTIG = 2 };
+
+typedef struct {
+    int kind;
+    const uint16_t *q;      /* [B][Hq][D] */
+    const uint16_t *k_new;  /* [B][Hkv][D] or NULL */
+    const uint16_t *v_new;
+    const uint16_t *k_src;  /* cache or history, per kind */
+    const uint16_t *v_src;
+    const int32_t *block_table; /* paged: [B][max_pages] */
+    const int32_t *seq_lens;    /* [B] */
+    const float *sinks;         /* [Hq] or NULL */
+    int window;                 /* 0 = no window (paged / contig); ring capacity (ring) */
+    double scale;
+    int B, Hq, Hkv, D;
+    int P, max_pages, num_pages; /* paged */
+    int Tmax;                    /* contig */
+    const int32_t *items;        /* NULL = every (b, h); else n_items pairs (b, h) */
+    int n_items;
+    double *out;                 /* [B][Hq][D] or [n_items][D] */
+    int status;                  /* first error seen, 0 if none */
+} problem;
+
+/* Address of the key (or value, when v != 0) row of position j, KV head g,
+ * sequence b, taken from the cache (j < p) or from k_new/v_new (j == p).
+ * Returns NULL when the address map leaves the buffers (bad input). */
+static const uint16_t *token_row(const problem *pr, int b, int g, int j, int v) {
+    const int L = pr->seq_lens[b];
+    const int D = pr->D, Hkv = pr->Hkv;
+    if (j == L - 1 && pr->k_new != NULL && pr->kind != LAYOUT_CONTIG) {
+        const uint16_t *src = v ? pr->v_new : pr->k_new;
+        return src + ((size_t)b * Hkv + g) * D;
+    }
+    const uint16_t *base = v ? pr->v_src : pr->k_src;
+    if (pr->kind == LAYOUT_PAGED) {
+        int slot_in_table = j / pr->P;
+        if (slot_in_table >= pr->max_pages) return NULL;
+        int32_t page = pr->block_table[(size_t)b * pr->max_pages + slot_in_table];
+        if (page < 0 || page >= pr->num_pages) return NULL;
+        return base + (((size_t)page * Hkv + g) * pr->P + (size_t)(j % pr->P)) * D;
+    }
+    if (pr->kind == LAYOUT_RING) {
+        int cell = j % pr->window;
+        return base + (((size_t)b * Hkv + g) * pr->window + (size_t)cell) * D;
+    }
+    /* contig */
+    if (j >= pr->Tmax) return NULL;
+    return base + (((size_t)b * pr->Tmax + j) * Hkv + g) * D;
+}
+
+/* One (b, h) output row, straight from the definition in the file header. */
+static int attend_one(const problem *pr, int b, int h, double *out) {
+    const int D = pr->D;
+    const int L = pr->seq_lens[b];
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (L <= 0) return OR_OK; /* inactive slot: output 0 */
+
+    const int G = pr->Hq / pr->Hkv;
+    const int g = h / G;
+    int W = 0;
+    if (pr->kind == LAYOUT_RING) W = pr->window;            /* ring: window = capacity */
+    else if (pr->window > 0) W = pr->window;                /* paged / contig windowed */
+    const int lo = (W > 0 && L - W > 0) ? L - W : 0;
+    const int n = L - lo;
+
+    const uint16_t *qrow = pr->q + ((size_t)b * pr->Hq + h) * D;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!s) return OR_NOMEM;
+
+    const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;
+    double M = sigma;
+    for (int i = 0; i < n; ++i) {
+        const uint16_t *krow = token_row(pr, b, g, lo + i, 0);
+        if (!krow) { free(s); return OR_BAD_INDEX; }
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+        s[i] = pr->scale * dot;
+        if (s[i] > M) M = s[i];
+    }
+    double den = isinf(sigma) && sigma < 0 ? 0.0 : exp(sigma - M);
+    for (int i = 0; i < n; ++i) {
+        const uint16_t *vrow = token_row(pr, b, g, lo + i, 1);
+        if (!vrow) { free(s); return OR_BAD_INDEX; }
+        double w = exp(s[i] - M);
+        den += w;
+        for (int d = 0; d < D; ++d) out[d] += w * bf16_to_f64(vrow[d]);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= den;
+    free(s);
+    return OR_OK;
+}
+
+typedef struct {
+    problem *pr;
+    int tid, nthreads;
+    int status;
+} worker_arg;
+
+static void *worker(void *p) {
+    worker_arg *a = (worker_arg *)p;
+    problem *pr = a->pr;
+    const int total = pr->items ? pr->n_items : pr->B * pr->Hq;
+    for (int w = a->tid; w < total; w += a->nthreads) {
+        int b, h;
+        if (pr->items) { b = pr->items[2 * w]; h = pr->items[2 * w + 1]; }
+        else { b = w / pr->Hq; h = w % pr->Hq; }
+        if (b < 0 || b >= pr->B || h < 0 || h >= pr->Hq) { a->status = OR_BAD_ARG; continue; }
+        int st = attend_one(pr, b, h, pr->out + (size_t)w * pr->D);
+        if (st != OR_OK && a->status == OR_OK) a->status = st;
+    }
+    return NULL;
+}
+
+static int run(problem *pr, int nthreads) {
+    if (pr->B < 0 || pr->Hq <= 0 || pr->Hkv <= 0 || pr->D <= 0 || pr->Hq % pr->Hkv != 0)
+        return OR_BAD_ARG;
+    if (!pr->q || !pr->seq_lens || !pr->out) return OR_BAD_ARG;
+    if ((pr->k_new == NULL) != (pr->v_new == NULL)) return OR_BAD_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    worker_arg args[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        args[t].pr = pr; args[t].tid = t; args[t].nthreads = nthreads; args[t].status = OR_OK;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, worker, &args[t]) != 0) break;
+        started = t;
+    }
+    /* threads that failed to start: run their share here */
+    for (int t = started + 1; t < nthreads; ++t) worker(&args[t]);
+    worker(&args[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    int st = OR_OK;
+    for (int t = 0; t < nthreads; ++t) if (args[t].status != OR_OK) { st = args[t].status; break; }
+    return st;
+}
+
+/* ------------------------------------------------------------------ */
+/* Public entry points.                                                */
+
+int oracle_decode_paged(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                        const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                        int window, double scale, double *out,
+                        int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                        const int32_t *items, int n_items, int nthreads) {
+    if (page_size <= 0 || max_pages <= 0 || num_pages <= 0 || window < 0 || !block_table)
+        return OR_BAD_ARG;
+    problem pr;
+    memset(&pr, 0, sizeof pr);
+    pr.kind = LAYOUT_PAGED;
+    pr.q = q; pr.k_new = k_new; pr.v_new = v_new; pr.k_src = k_cache; pr.v_src = v_cache;
+    pr.block_table = block_table; pr.seq_lens = seq_lens; pr.sinks = sinks;
+    pr.window = window; pr.scale = scale; pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.D = D;
+    pr.P = page_size; pr.max_pages = max_pages; pr.num_pages = num_pages;
+    pr.items = items; pr.n_items = n_items; pr.out = out;
+    return run(&pr, nthreads);
+}
+
+int oracle_decode_ring(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                       const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *seq_lens, const float *sinks,
+                       int window, double scale, double *out, int B, int Hq, int Hkv, int D,
+                       const int32_t *items, int n_items, int nthreads) {
+    if (window <= 0) return OR_BAD_ARG;
+    problem pr;
+    memset(&pr, 0, sizeof pr);
+    pr.kind = LAYOUT_RING;
+    pr.q = q; pr.k_new = k_new; pr.v_new = v_new; pr.k_src = k_cache; pr.v_src = v_cache;
+    pr.seq_lens = seq_lens; pr.sinks = sinks; pr.window = window; pr.scale = scale;
+    pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.D = D;
+    pr.items = items; pr.n_items = n_items; pr.out = out;
+    return run(&pr, nthreads);
+}
+
+int oracle_decode_contig(const uint16_t *q, const uint16_t *hist_k, const uint16_t *hist_v,
+                         const int32_t *seq_lens, int Tmax, const float *sinks,
+                         int window, double scale, double *out, int B, int Hq, int Hkv, int D,
+                         const int32_t *items, int n_items, int nthreads) {
+    if (window < 0 || Tmax < 0) return OR_BAD_ARG;
+    problem pr;
+    memset(&pr, 0, sizeof pr);
+    pr.kind = LAYOUT_CONTIG;
+    pr.q = q; pr.k_src = hist_k; pr.v_src = hist_v;
+    pr.seq_lens = seq_lens; pr.Tmax = Tmax; pr.sinks = sinks; pr.window = window;
+    pr.scale = scale; pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.D = D;
+    pr.items = items; pr.n_items = n_items; pr.out = out;
+    return run(&pr, nthreads);
+}
+
+/* Append (bit copy) of the new token of every active sequence into a paged
+ * cache: position p = L - 1 goes to page block_table[b][p / P], slot p % P. */
+int oracle_kv_append_paged(const uint16_t *k_new, const uint16_t *v_new,
+                           uint16_t *k_cache, uint16_t *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int B, int Hkv, int D, int page_size, int max_pages, int num_pages) {
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        if (L <= 0) continue;
+        int p = L - 1;
+        if (p / page_size >= max_pages) return OR_BAD_INDEX;
+        int32_t page = block_table[(size_t)b * max_pages + p / page_size];
+        if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
+        for (int g = 0; g < Hkv; ++g) {
+            size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;
+            size_t src = ((size_t)b * Hkv + g) * D;
+            memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
+            memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return OR_OK;
+}
+
+/* Append into a ring of capacity W: position p goes to cell p % W. */
+int oracle_kv_append_ring(const uint16_t *k_new, const uint16_t *v_new,
+                          uint16_t *k_cache, uint16_t *v_cache, const int32_t *seq_lens,
+                          int window, int B, int Hkv, int D) {
+    if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens || window <= 0) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        if (L <= 0) continue;
+        int cell = (L - 1) % window;
+        for (int g = 0; g < Hkv; ++g) {
+            size_t dst = (((size_t)b * Hkv + g) * window + (size_t)cell) * D;
+            size_t src = ((size_t)b * Hkv + g) * D;
+            memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
+            memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return OR_OK;
+}
+
+/* Materialise the first n[b] tokens of a contiguous history hist[B][Tmax][Hkv][D]
+ * into a paged cache through the block table. Other cells are left untouched. */
+int oracle_scatter_paged(const uint16_t *hist_k, const uint16_t *hist_v, const int32_t *n_tokens,
+                         int Tmax, const int32_t *block_table, uint16_t *k_cache, uint16_t *v_cache,
+                         int B, int Hkv, int D, int page_size, int max_pages, int num_pages) {
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < n_tokens[b]; ++j) {
+            if (j >= Tmax || j / page_size >= max_pages) return OR_BAD_INDEX;
+            int32_t page = block_table[(size_t)b * max_pages + j / page_size];
+            if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
+            for (int g = 0; g < Hkv; ++g) {
+                size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(j % page_size)) * D;
+                size_t src = (((size_t)b * Tmax + j) * Hkv + g) * D;
+                memcpy(k_cache + dst, hist_k + src, sizeof(uint16_t) * (size_t)D);
+                memcpy(v_cache + dst, hist_v + src, sizeof(uint16_t) * (size_t)D);
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* Materialise the ring state after n[b] tokens: tokens max(0, n - W) .. n - 1
+ * sit in cells j % W; older tokens have been overwritten. */
+int oracle_scatter_ring(const uint16_t *hist_k, const uint16_t *hist_v, const int32_t *n_tokens,
+                        int Tmax, int window, uint16_t *k_cache, uint16_t *v_cache,
+                        int B, int Hkv, int D) {
+    if (window <= 0) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        int n = n_tokens[b];
+        int lo = n - window > 0 ? n - window : 0;
+        for (int j = lo; j < n; ++j) {
+            if (j >= Tmax) return OR_BAD_INDEX;
+            for (int g = 0; g < Hkv; ++g) {
+                size_t dst = (((size_t)b * Hkv + g) * window + (size_t)(j % window)) * D;
+                size_t src = (((size_t)b * Tmax + j) * Hkv + g) * D;
+                memcpy(k_cache + dst, hist_k + src, sizeof(uint16_t) * (size_t)D);
+                memcpy(v_cache + dst, hist_v + src, sizeof(uint16_t) * (size_t)D);
+            }
+        }
+    }
+    return OR_OK;
+}

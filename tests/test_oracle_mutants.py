@@ -1,0 +1,86 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that at least one pin in test_oracle.py catches each of them. This is what
+makes the pins trustworthy: a dropped term, a wrong sign, a wrong index or a
+transposed operand anywhere in the oracle must fail something."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("drop_sink", "double den = isinf(sigma) && sigma < 0 ? 0.0 : exp(sigma - M);",
+     "double den = 0.0;"),
+    ("sink_scaled", "const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;",
+     "const double sigma = pr->sinks ? pr->scale * (double)pr->sinks[h] : -INFINITY;"),
+    ("gqa_modulo", "const int g = h / G;", "const int g = h % pr->Hkv;"),
+    ("window_one_short", "const int lo = (W > 0 && L - W > 0) ? L - W : 0;",
+     "const int lo = (W > 0 && L - W + 1 > 0) ? L - W + 1 : 0;"),
+    ("window_one_long", "const int lo = (W > 0 && L - W > 0) ? L - W : 0;",
+     "const int lo = (W > 0 && L - W - 1 > 0) ? L - W - 1 : 0;"),
+    ("ignore_new_token", "if (j == L - 1 && pr->k_new != NULL && pr->kind != LAYOUT_CONTIG) {",
+     "if (0) {"),
+    ("page_slot_swapped",
+     "return base + (((size_t)page * Hkv + g) * pr->P + (size_t)(j % pr->P)) * D;",
+     "return base + (((size_t)page * Hkv + g) * pr->P + (size_t)((j / pr->P) % pr->P)) * D;"),
+    ("page_head_token_swapped",
+     "return base + (((size_t)page * Hkv + g) * pr->P + (size_t)(j % pr->P)) * D;",
+     "return base + (((size_t)page * pr->P + (size_t)(j % pr->P)) * Hkv + g) * D;"),
+    ("ring_cell_shift", "int cell = j % pr->window;", "int cell = (j + 1) % pr->window;"),
+    ("no_scale", "s[i] = pr->scale * dot;", "s[i] = dot;"),
+    ("exp_sign", "double w = exp(s[i] - M);", "double w = exp(M - s[i]);"),
+    ("value_is_key", "const uint16_t *vrow = token_row(pr, b, g, lo + i, 1);",
+     "const uint16_t *vrow = token_row(pr, b, g, lo + i, 0);"),
+    ("q_transposed", "const uint16_t *qrow = pr->q + ((size_t)b * pr->Hq + h) * D;",
+     "const uint16_t *qrow = pr->q + ((size_t)h * pr->B + b) * D;"),
+    ("append_wrong_cell",
+     "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
+     "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(L % page_size)) * D;"),
+]
+
+PIN_CALLS = [
+    lambda: pins.test_brute_force_matches_all_layouts(11, 2, 4, 2, 8, [5, 17], 0),
+    lambda: pins.test_brute_force_matches_all_layouts(12, 3, 6, 3, 4, [1, 16, 33], 7),
+    lambda: pins.test_no_sink_equals_torch_sdpa_fp64(9),
+    pins.test_single_token_is_sigmoid_weighted_value,
+    pins.test_zero_query_is_windowed_mean_with_sink,
+    pins.test_equal_keys_equal_values_closed_form,
+    pins.test_window_at_or_beyond_length_equals_full,
+    lambda: pins.test_ring_paged_contig_agree(13),
+    pins.test_gqa_equals_mha_on_repeated_kv,
+    pins.test_append_is_bit_exact_and_touches_only_target_cells,
+    pins.test_hand_worked_example,
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutant {name}: anchor text not found in oracle.c"
+    mutated = src.replace(old, new, 1)
+    c_path = tmp_path / f"{name}.c"
+    so_path = tmp_path / f"lib{name}.so"
+    c_path.write_text(mutated)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", str(c_path),
+                    "-o", str(so_path), "-lm"], check=True)
+    return str(so_path)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    so = _build_mutant(tmp_path, name, old, new)
+    prev = oracle.load_library(so)
+    caught = []
+    try:
+        for call in PIN_CALLS:
+            try:
+                call()
+            except (AssertionError, ValueError):
+                caught.append(call)
+    finally:
+        oracle.restore_library(prev)
+    assert caught, f"no pin caught the planted mistake {name!r}"
