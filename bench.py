@@ -1,0 +1,426 @@
+"""Benchmark of the fused decode-attention step on GB300.
+
+A step is one decode step of attention for one full-attention layer (paged KV
+cache, page 16) and one sliding-window layer (ring of 128 cells), each with
+its fused 1-token KV append, for the gpt-oss head shape (64 query heads, 8 KV
+heads, head dim 64). Default workload: batch 64, lengths uniform in
+[1024, 8192]. Prints one JSON line.
+
+  value     achieved HBM GB/s of the step (algorithmic bytes / device time),
+            summed over all ranks (replicas; the path needs no exchange)
+  roofline  the paged kernel's own GB/s against the measured HBM copy peak
+  e2e       the same metric end to end through the public API, with the
+            step's inputs copied from pinned host memory and outputs read back
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/call and achieved HBM GB/s (% of GB300 peak) per config"
+UNIT = "GB/s"
+KERNEL_SRC = os.path.join(ROOT, "paged_decode_attention_kv_gb300", "csrc", "decode_attn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- bytes the method must move
+def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W):
+    """Per call: cached K+V of the attended tokens (except the new one), k_new/v_new read
+    and written, q read, out written, block-table entries read, seq_lens, sinks."""
+    total = 0
+    for L in lens:
+        if L <= 0:
+            continue
+        if kind == "paged_full":
+            n, tiles = L, math.ceil(L / P)
+        elif kind == "paged_window":
+            lo = max(0, L - W)
+            n, tiles = L - lo, (L - 1) // P - lo // P + 1
+        else:  # ring
+            n, tiles = min(L, W), 0
+        total += (n - 1) * 4 * Hkv * D + 2 * 2 * Hkv * D + 2 * 2 * Hkv * D + 2 * Hq * D \
+            + 2 * Hq * D + 4 * tiles
+    return total + 4 * len(lens) + 4 * Hq
+
+
+# ---------------------------------------------------------------- environment helpers
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload, kind):
+    """DRAM bytes per launch from an ncu capture, if taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload \
+                        and parts[1] == kind and parts[2] == source_hash():
+                    return float(parts[3])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 8:
+                    continue
+                if self.uuid and self.uuid not in p[0]:
+                    continue
+                rows.append(p)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- workload construction
+class StepInputs:
+    """One independent copy of a step's inputs and caches on the device."""
+
+    def __init__(self, name, device, seed_offset=0):
+        import torch
+        from paged_decode_attention_kv_gb300 import workloads as wl
+        cfg = wl.config(name)
+        self.cfg = cfg
+        self.lens = wl.seq_lens(name)
+        seed = cfg["seed"] + seed_offset
+        gen = wl.cpu_generator(seed)
+        vgen = torch.Generator(device=device)
+        vgen.manual_seed(seed)
+        B, Hq, Hkv, D, P, W = (cfg[k] for k in ("B", "Hq", "Hkv", "D", "page_size", "window"))
+        self.inp = wl.draw_decode_inputs(B, Hq, Hkv, D, self.lens, gen)
+        self.pool = wl.draw_paged_pool(wl.pool_size(name, self.lens), Hkv, P, D, self.lens,
+                                       wl.max_pages_per_seq(name, self.lens), gen, device=device,
+                                       value_gen=vgen)
+        self.ring = wl.draw_ring_pool(B, Hkv, W, D, vgen, device=device)
+        d = lambda t: t.to(device).contiguous()
+        self.q, self.k_new, self.v_new = d(self.inp.q), d(self.inp.k_new), d(self.inp.v_new)
+        self.seq_lens, self.sinks = d(self.inp.seq_lens), d(self.inp.sinks)
+        self.out_full = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.out_ring = torch.empty_like(self.out_full)
+
+    def nbytes(self):
+        ts = [self.pool.k_cache, self.pool.v_cache, self.ring.k_cache, self.ring.v_cache]
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+def step_bytes(name, lens):
+    from paged_decode_attention_kv_gb300 import workloads as wl
+    c = wl.config(name)
+    args = (c["Hq"], c["Hkv"], c["D"], c["page_size"], c["window"])
+    return algorithmic_bytes(lens, "paged_full", *args), algorithmic_bytes(lens, "ring", *args)
+
+
+# ---------------------------------------------------------------- the CPU oracle on a sample
+def oracle_sample(name, s: "StepInputs", budget_s):
+    """Time the fp64 oracle on whole sequences (all heads, both layers) of this workload,
+    adding sequences until about budget_s of CPU work. Returns (GB/s, cores, description)."""
+    import numpy as np
+    import oracle
+    from paged_decode_attention_kv_gb300 import workloads as wl
+    c = s.cfg
+    Hq, P, W = c["Hq"], c["page_size"], c["window"]
+    kp, vp = wl.bits(s.pool.k_cache), wl.bits(s.pool.v_cache)
+    rk, rv = wl.bits(s.ring.k_cache), wl.bits(s.ring.v_cache)
+    q, kn, vn = wl.bits(s.inp.q), wl.bits(s.inp.k_new), wl.bits(s.inp.v_new)
+    bt = s.pool.block_table.cpu().numpy()
+    lens = np.asarray(s.lens, np.int32)
+    sinks = s.inp.sinks.numpy()
+    cores = oracle.default_threads()
+    done_bytes, elapsed, seqs = 0, 0.0, 0
+    order = [b for b in range(len(lens)) if lens[b] > 0]
+    for b in order:
+        items = [(b, h) for h in range(Hq)]
+        t0 = time.perf_counter()
+        oracle.decode_paged(q, kn, vn, kp, vp, bt, lens, sinks, 0, s.inp.scale, P, items=items,
+                            nthreads=cores)
+        oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
+                           nthreads=cores)
+        elapsed += time.perf_counter() - t0
+        pb, rb = step_bytes(name, [int(lens[b])])
+        done_bytes += pb + rb
+        seqs += 1
+        if elapsed >= budget_s:
+            break
+    desc = (f"{seqs} of {len(order)} active sequences, all {Hq} heads, full + ring layer; "
+            f"{elapsed:.1f} s on {cores} threads")
+    return done_bytes / elapsed / 1e9, cores, desc
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    import torch
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    s = StepInputs(args.workload, device)
+    # each step is a bounded sample: calibrate so that warmup+steps fit ~90 s
+    per_step = max(0.02, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, s, per_step)
+    vals, descs = [], []
+    for _ in range(args.steps):
+        v, cores, desc = oracle_sample(args.workload, s, per_step)
+        vals.append(v)
+        descs.append(desc)
+    value = statistics.median(vals)
+    pbytes, rbytes = step_bytes(args.workload, s.lens)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round((pbytes + rbytes) / (value * 1e9) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(args.workload, s),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": descs[-1]},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def workload_config(name, s):
+    c = s.cfg
+    lens = [L for L in s.lens if L > 0]
+    return {"workload": name, "batch": c["B"], "active": len(lens), "q_heads": c["Hq"],
+            "kv_heads": c["Hkv"], "head_dim": c["D"], "page_size": c["page_size"],
+            "window": c["window"], "mean_len": round(sum(lens) / max(1, len(lens)), 1),
+            "max_len": max(lens) if lens else 0,
+            "layers_per_step": ["paged full attention", f"ring window {c['window']}"],
+            "parallelism": "replicas"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_decode_attention_kv_gb300 as da
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    first = StepInputs(args.workload, dev)
+    set_bytes = first.nbytes()
+    n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
+    sets = [first] + [StepInputs(args.workload, dev, seed_offset=i) for i in range(1, n_sets)]
+    cfg = first.cfg
+    B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
+    da.decode_attn_reserve(da.decode_attn_workspace_bytes(B, Hq, Hkv, D))
+    pbytes, rbytes = step_bytes(args.workload, first.lens)
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        da.decode_attn_paged(s.q, s.k_new, s.v_new, s.pool.k_cache, s.pool.v_cache,
+                             s.pool.block_table, s.seq_lens, s.sinks, 0, s.inp.scale, s.out_full)
+        da.decode_attn_ring(s.q, s.k_new, s.v_new, s.ring.k_cache, s.ring.v_cache, s.seq_lens,
+                            s.sinks, s.inp.scale, s.out_ring)
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    ev_p0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_p1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        s = sets[i % n_sets]
+        ev_p0[i].record(stream)
+        da.decode_attn_paged(s.q, s.k_new, s.v_new, s.pool.k_cache, s.pool.v_cache,
+                             s.pool.block_table, s.seq_lens, s.sinks, 0, s.inp.scale, s.out_full)
+        ev_p1[i].record(stream)
+        da.decode_attn_ring(s.q, s.k_new, s.v_new, s.ring.k_cache, s.ring.v_cache, s.seq_lens,
+                            s.sinks, s.inp.scale, s.out_ring)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    paged_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p0, ev_p1)) / args.steps
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    assert da.decode_attn_device_status() == 0
+    value = world * (pbytes + rbytes) / (ms_step * 1e-3) / 1e9
+    ring_ms = ms_step - paged_ms
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, first, pbytes + rbytes, dev)
+
+    peak, peak_kind = measured_hbm_peak()
+    achieved = pbytes / (paged_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload, "paged")
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(workload_config(args.workload, first),
+                       l2=("inputs larger than L2: %.0f MB per step" % (set_bytes / 1e6))
+                       if n_sets == 1 else f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB > 2x L2"),
+        "us_per_call": {"paged_full": round(paged_ms * 1e3, 2), "ring": round(ring_ms * 1e3, 2)},
+        "gb_per_s_per_call": {"paged_full": round(achieved, 1),
+                              "ring": round(rbytes / (ring_ms * 1e-3) / 1e9, 1)},
+        "algorithmic_bytes_per_step": {"paged_full": pbytes, "ring": rbytes},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "traffic": traffic, "kernel": "decode_attn_kernel (paged, full attention)"},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, desc = oracle_sample(args.workload, first, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores,
+                                  "kind": "oracle", "sample": desc}
+    return result
+
+
+def run_e2e(args, s, step_bytes_total, dev):
+    """Per step: H2D of q, k_new, v_new, seq_lens, block table, sinks from pinned host
+    memory; both layer calls; D2H of both outputs. Wall clock around the whole loop."""
+    import torch
+    import paged_decode_attention_kv_gb300 as da
+    host = {k: getattr(s, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "seq_lens", "sinks")}
+    host["block_table"] = s.pool.block_table.cpu().pin_memory()
+    outs = [torch.empty(s.out_full.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dst = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    n = max(3, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        for k, v in host.items():
+            dst[k].copy_(v, non_blocking=True)
+        da.decode_attn_paged(dst["q"], dst["k_new"], dst["v_new"], s.pool.k_cache,
+                             s.pool.v_cache, dst["block_table"], dst["seq_lens"], dst["sinks"], 0,
+                             s.inp.scale, s.out_full)
+        da.decode_attn_ring(dst["q"], dst["k_new"], dst["v_new"], s.ring.k_cache, s.ring.v_cache,
+                            dst["seq_lens"], dst["sinks"], s.inp.scale, s.out_ring)
+        outs[0].copy_(s.out_full, non_blocking=True)
+        outs[1].copy_(s.out_ring, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(step_bytes_total * n / dt / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "us_per_step": round(dt / n * 1e6, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="b64",
+                    choices=["tiny", "b1", "b64", "long1", "long8", "serve"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+
+    if args.impl == "reference":
+        result = run_reference(args, rank, world)
+    else:
+        result = run_ours(args, rank, world, local_rank)
+    if rank == 0 and result is not None:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

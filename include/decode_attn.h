@@ -1,0 +1,150 @@
+/*
+ * decode_attn.h -- C ABI of the fused decode-step attention library for GB300
+ * (sm_103a): KV append + grouped-query attention over a paged KV cache or a
+ * sliding-window ring buffer + per-head attention-sink logits.
+ *
+ * The operation (SimpleLLM README, changes table):
+ *   row "one decode-attention kernel for sinks, sliding window, GQA and the KV
+ *        append (replaces four ops)"           -> decode_attn_paged / _ring
+ *   row "paged KV cache for full-attention layers" -> the paged layout
+ *   row "ring buffer for sliding-window layers"    -> the ring layout
+ *   row "CUDA graphs for any set of active slots"  -> every call is
+ *        capturable: no host read of seq_lens, no allocation once reserved.
+ * The pages print no formula; the definition used is, for every active
+ * sequence b (L = seq_lens[b] > 0, the length AFTER this step's append; the
+ * new token has position p = L - 1), query head h and KV head g = h / (Hq/Hkv):
+ *     J   = { j : lo <= j < L },  lo = max(0, L - W) if a window W applies, else 0
+ *     s_j = scale * <q[b,h,:], k_j[g,:]>
+ *     out[b,h,:] = sum_j e^{s_j} v_j[g,:] / (e^{sink[h]} + sum_j e^{s_j})
+ * and out[b] = 0 when L == 0 (inactive slot). The sink is a raw logit (not
+ * multiplied by scale) and carries no value vector.
+ *
+ * Conventions for every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *     16-byte aligned. The library keeps none of them after the call returns.
+ *   - bf16 tensors: q, k_new, v_new, k_cache, v_cache, out. int32: block_table,
+ *     seq_lens. fp32: sinks.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream). A return of 0 means "validated and
+ *     launched"; faults found by the kernel itself (a bad length or page id)
+ *     are recorded in a device status word, see decode_attn_device_status().
+ *   - Return value: 0 on success, else a negative DA_ERR_* code; nothing is
+ *     launched when a code is returned.
+ *   - Supported now: head_dim 64, page_size 16, query heads per KV head
+ *     (G = Hq/Hkv) in {1, 2, 4, 8, 16}, batch <= 1024, batch*Hkv <= 65536,
+ *     ring capacity >= 16. Anything else returns DA_ERR_UNSUPPORTED.
+ *   - The attention entry points use a library-owned workspace per device
+ *     (split partials and arrival counters). It is allocated on first use or
+ *     by decode_attn_reserve(); during stream capture a call that would need
+ *     a larger workspace returns DA_ERR_WORKSPACE instead of allocating.
+ *     Calls that run concurrently on different streams of one device share
+ *     this workspace and must not overlap.
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DA_API __attribute__((visibility("default")))
+#else
+#define DA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DA_OK 0
+#define DA_ERR_INVALID_ARG (-1) /* null pointer, misalignment, Hq % Hkv != 0, bad size */
+#define DA_ERR_UNSUPPORTED (-2) /* a shape outside the supported set above */
+#define DA_ERR_WORKSPACE (-3)   /* workspace too small while the stream is capturing */
+#define DA_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed */
+
+/* Bits of the device status word (decode_attn_device_status). */
+#define DA_STATUS_BAD_SEQ_LEN 1u /* seq_lens[b] < 0, or beyond max_seq_len / the block table row;
+                                    the slot is treated as inactive (output 0, no append) */
+#define DA_STATUS_BAD_PAGE 2u    /* a block-table entry outside [0, num_pages); that tile reads
+                                    zeros and the append into it is skipped */
+#define DA_STATUS_TIMEOUT 4u     /* a bounded wait on a tile copy expired; output is garbage */
+
+typedef struct {
+    int batch;        /* B: number of sequence slots */
+    int num_q_heads;  /* Hq */
+    int num_kv_heads; /* Hkv; Hq % Hkv == 0 */
+    int head_dim;     /* D (64) */
+} da_shape;
+
+/*
+ * decode_attn_paged -- one decode step of attention for a full-attention (or
+ * windowed) layer whose KV cache is paged. Fuses the KV append: the new
+ * token's k_new/v_new are written into the cache AND used for this step.
+ *
+ *   q          [B, Hq, D]                    query of the new token
+ *   k_new,v_new[B, Hkv, D]                   its key / value; both NULL = no append
+ *                                            (token p is then read from the cache)
+ *   k_cache,   [num_pages, Hkv, page_size, D] paged pool; token j of sequence b sits in
+ *   v_cache                                   page block_table[b][j / 16], slot j % 16.
+ *                                            Written only at token p's cell.
+ *   block_table[B, max_pages_per_seq]        physical page per logical page
+ *   seq_lens   [B]                           post-append lengths, 0 = inactive slot
+ *   sinks      [Hq] or NULL                  sink logits (NULL = no sink)
+ *   window     0 = full attention, W > 0 = attend to the last W positions (incl. p)
+ *   scale      multiplier of q.k (1/sqrt(D) for gpt-oss)
+ *   out        [B, Hq, D]                    written for every slot (0 for inactive)
+ *   max_seq_len upper bound of seq_lens (<= max_pages_per_seq * page_size)
+ * Distinct active sequences must not share the page that receives their append.
+ */
+DA_API int decode_attn_paged(const void *q, const void *k_new, const void *v_new,
+                      void *k_cache, void *v_cache,
+                      const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                      int window, float scale, void *out,
+                      da_shape s, int page_size, int max_pages_per_seq, int num_pages,
+                      int max_seq_len, void *stream);
+
+/*
+ * decode_attn_ring -- one decode step for a sliding-window layer whose KV
+ * lives in a per-sequence ring of `window` cells: k_cache/v_cache are
+ * [B, Hkv, window, D] and token j of sequence b sits in cell j % window.
+ * Attends to the last min(L, window) tokens; the append overwrites cell
+ * p % window (which held token p - window, now outside the window).
+ * Other arguments as in decode_attn_paged.
+ */
+DA_API int decode_attn_ring(const void *q, const void *k_new, const void *v_new,
+                     void *k_cache, void *v_cache,
+                     const int32_t *seq_lens, const float *sinks,
+                     int window, float scale, void *out, da_shape s, void *stream);
+
+/*
+ * kv_append -- the append alone: bit-copies k_new/v_new [B, Hkv, D] of every
+ * active sequence into the cell of position p = seq_lens[b] - 1.
+ * block_table != NULL: paged cache (page_size, max_pages_per_seq, num_pages as
+ * above; window ignored). block_table == NULL: ring cache [B, Hkv, window, D].
+ */
+DA_API int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+              const int32_t *block_table, const int32_t *seq_lens,
+              int window, da_shape s, int page_size, int max_pages_per_seq,
+              int num_pages, void *stream);
+
+/* Workspace the attention calls need on the current device for this shape. */
+DA_API size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len);
+
+/* Make sure the current device's workspace holds at least `bytes` (allocates
+ * and zeroes synchronously). Call before capturing a CUDA graph. */
+DA_API int decode_attn_reserve(size_t bytes);
+
+/* Wait for `stream`, then return the device status word (DA_STATUS_* bits, 0
+ * if clean) of the current device and clear it; negative DA_ERR_CUDA on
+ * failure. */
+DA_API int decode_attn_device_status(void *stream);
+
+/* Text for a return code; for DA_ERR_CUDA it includes the last CUDA error of
+ * the calling thread. The pointer stays valid until the thread's next call. */
+DA_API const char *decode_attn_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */

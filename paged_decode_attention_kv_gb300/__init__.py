@@ -1,0 +1,176 @@
+"""Fused decode-step attention for GB300: KV append + GQA over a paged cache or a
+sliding-window ring + per-head attention sinks.
+
+A thin ctypes binding over the C ABI in ``include/decode_attn.h`` (library
+``libdecode_attn.so`` next to this file, built by ``build.py``). Every step of
+the computation runs in the library's CUDA kernels; this module only turns
+torch tensors into device pointers, sizes and the current CUDA stream, and
+turns error codes into exceptions. There is no CPU fallback: if the library
+is missing, every call raises.
+
+Tensor layouts (all contiguous, bf16 unless noted):
+  q, out            [B, Hq, D]
+  k_new, v_new      [B, Hkv, D]
+  paged caches      [num_pages, Hkv, page_size, D]
+  ring caches       [B, Hkv, window, D]
+  block_table       [B, max_pages_per_seq] int32
+  seq_lens          [B] int32, length after this step's append (0 = inactive)
+  sinks             [Hq] float32, or None
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "da_shape",
+    "DecodeAttnError", "decode_attn_paged", "decode_attn_ring", "kv_append",
+    "decode_attn_workspace_bytes", "decode_attn_reserve", "decode_attn_device_status",
+    "decode_attn_error_string", "library_path", "load_library",
+    "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libdecode_attn.so"
+
+DA_OK = 0
+DA_ERR_INVALID_ARG = -1
+DA_ERR_UNSUPPORTED = -2
+DA_ERR_WORKSPACE = -3
+DA_ERR_CUDA = -4
+DA_STATUS_BAD_SEQ_LEN = 1
+DA_STATUS_BAD_PAGE = 2
+DA_STATUS_TIMEOUT = 4
+
+
+class da_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("num_q_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int)]
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, code, message):
+        super().__init__(f"decode_attn error {code}: {message}")
+        self.code = code
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load_library():
+    """Load the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    c_int, c_float = ctypes.c_int, ctypes.c_float
+    lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, f32p, c_int, c_float, vp,
+                                      da_shape, c_int, c_int, c_int, c_int, vp]
+    lib.decode_attn_ring.argtypes = [vp, vp, vp, vp, vp, i32p, f32p, c_int, c_float, vp,
+                                     da_shape, vp]
+    lib.kv_append.argtypes = [vp, vp, vp, vp, i32p, i32p, c_int, da_shape, c_int, c_int, c_int, vp]
+    lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
+    lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
+    lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
+    lib.decode_attn_device_status.argtypes = [vp]
+    lib.decode_attn_error_string.argtypes = [c_int]
+    lib.decode_attn_error_string.restype = ctypes.c_char_p
+    for fn in (lib.decode_attn_paged, lib.decode_attn_ring, lib.kv_append, lib.decode_attn_reserve,
+               lib.decode_attn_device_status):
+        fn.restype = c_int
+    _lib = lib
+    return lib
+
+
+def decode_attn_error_string(code: int) -> str:
+    return load_library().decode_attn_error_string(int(code)).decode()
+
+
+def _check(code):
+    if code != 0:
+        raise DecodeAttnError(code, decode_attn_error_string(code))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shape(q, k_cache_heads):
+    B, Hq, D = q.shape
+    return da_shape(B, Hq, k_cache_heads, D)
+
+
+def decode_attn_paged(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window,
+                      scale, out, max_seq_len=None, stream=None):
+    """One decode step over a paged cache, with the KV append fused in.
+
+    k_new/v_new None = no append. window 0 = full attention. max_seq_len
+    defaults to the block table's capacity (max_pages_per_seq * page_size).
+    """
+    num_pages, Hkv, P, _ = k_cache.shape
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * P
+    lib = load_library()
+    _check(lib.decode_attn_paged(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(sinks), int(window), float(scale), _ptr(out), _shape(q, Hkv), P,
+        max_pages, num_pages, int(max_seq_len), _stream(stream)))
+    return out
+
+
+def decode_attn_ring(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, scale, out,
+                     stream=None):
+    """One decode step over a sliding-window ring [B, Hkv, W, D] (W = its capacity)."""
+    B, Hkv, W, _ = k_cache.shape
+    lib = load_library()
+    _check(lib.decode_attn_ring(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        _ptr(sinks), int(W), float(scale), _ptr(out), _shape(q, Hkv), _stream(stream)))
+    return out
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, seq_lens, block_table=None, stream=None):
+    """Append alone: paged when block_table is given, else ring [B, Hkv, W, D]."""
+    B, Hkv, D = k_new.shape
+    lib = load_library()
+    if block_table is not None:
+        num_pages, _, P, _ = k_cache.shape
+        args = (0, da_shape(B, Hkv, Hkv, D), P, block_table.shape[1], num_pages)
+    else:
+        W = k_cache.shape[2]
+        args = (W, da_shape(B, Hkv, Hkv, D), 0, 0, 0)
+    _check(lib.kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                         _ptr(block_table), _ptr(seq_lens), *args, _stream(stream)))
+
+
+def decode_attn_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim=64, max_seq_len=0):
+    return int(load_library().decode_attn_workspace_bytes(
+        da_shape(batch, num_q_heads, num_kv_heads, head_dim), int(max_seq_len)))
+
+
+def decode_attn_reserve(nbytes: int):
+    _check(load_library().decode_attn_reserve(int(nbytes)))
+
+
+def decode_attn_device_status(stream=None) -> int:
+    """Wait for the stream, return and clear the device status bits."""
+    rc = load_library().decode_attn_device_status(_stream(stream))
+    if rc < 0:
+        _check(rc)
+    return rc

@@ -1,0 +1,1194 @@
+// decode_attn.cu -- fused decode-step attention for GB300 (sm_103a).
+//
+// One launch per call does the whole step described in the SimpleLLM README,
+// changes table, row "one decode-attention kernel for sinks, sliding window,
+// GQA and the KV append": it appends the new token's K/V into a paged cache
+// (row "paged KV cache for full-attention layers") or a ring buffer (row "ring
+// buffer for sliding-window layers"), attends with all query heads of a KV
+// head at once (GQA), and folds the per-head sink logit into the softmax
+// denominator when the per-split partials are combined.
+//
+// Work decomposition (graph-capturable, no host read of seq_lens):
+//   * unit = one 16-token tile (one page) of one (sequence b, KV head g);
+//     units are ordered (b, g, tile), so a "segment" (b, g) is a contiguous
+//     run of units. Every CTA recomputes the prefix of units over b from
+//     seq_lens in shared memory.
+//   * the grid is one CTA per SM, 8 warps each; every warp is a worker that
+//     takes an equal contiguous share of all units (split-KV with perfect
+//     balance, whatever the length mix). A warp streams its tiles through a
+//     private TMA/mbarrier pipeline and keeps an online-softmax state (running
+//     max m, sum l, accumulator acc) per segment in registers.
+//   * a segment a warp owns entirely is finished by that warp (sink + 1/den +
+//     bf16 store). Segments shared by several warps are merged in shared
+//     memory; segments shared by several CTAs leave one fp32 partial per CTA
+//     in the workspace, and the last CTA to arrive (atomic ticket, no waiting)
+//     combines them with the sink.
+//   * the QK^T and PV products of a 16-token tile run on tensor cores
+//     (mma.sync m16n8k16 bf16 -> fp32): keys are the M dimension and the G <= 8
+//     query heads of the group the N dimension, so nothing is padded; the
+//     probabilities are moved from the accumulator layout into the B-operand
+//     layout with movmatrix.
+//   * K/V tiles (2 KiB each) arrive by TMA with 128-byte swizzle, so the
+//     ldmatrix reads are free of bank conflicts.
+#include <cuda.h>  // CUtensorMap and its enums (types only; resolved at run time)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "decode_attn.h"
+
+namespace {
+
+constexpr int kD = 64;             // head dim
+constexpr int kPage = 16;          // tokens per page = per tile
+constexpr int kWarps = 8;          // workers per CTA
+constexpr int kThreads = kWarps * 32;
+#ifndef DA_STAGES
+#define DA_STAGES 4
+#endif
+constexpr int kStages = DA_STAGES; // tiles in flight per warp
+#ifndef DA_MIN_TILES
+#define DA_MIN_TILES 4
+#endif
+constexpr int kMinTilesPerWorker = DA_MIN_TILES;
+constexpr int kTileBytes = kPage * kD * 2;  // 2048 B of K (or V) per tile
+constexpr int kMaxBatch = 1024;
+constexpr int kMaxSegments = 65536;         // B * Hkv
+constexpr int kCounterBytes = kMaxSegments * 4;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per tile wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ unsigned int g_status;  // DA_STATUS_* bits, read and cleared by the host
+
+struct Params {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    __nv_bfloat16 *k_cache;
+    __nv_bfloat16 *v_cache;
+    const int *block_table;
+    const int *seq_lens;
+    const float *sinks;
+    __nv_bfloat16 *out;
+    float *part;     // [gridDim.x][2][slot floats] CTA partials
+    int *counters;   // [B*Hkv] arrival tickets, zero at rest
+    int B, Hq, Hkv, G, window, max_pages, num_pages, max_seq_len;
+    float scale_log2;  // scale * log2(e)
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void flag_status(unsigned bits) { atomicOr(&g_status, bits); }
+
+// ------------------------------------------------------------------ layout helpers
+template <bool RING>
+__device__ __forceinline__ int tiles_of(int L, int window) {
+    if (L <= 0) return 0;
+    if (RING) {
+        const int n = L < window ? L : window;
+        return (n + kPage - 1) / kPage;
+    }
+    const int lo = (window > 0 && L > window) ? L - window : 0;
+    return ((L - 1) / kPage) - (lo / kPage) + 1;
+}
+
+// Largest b in [0, B) with pre[b] <= x (pre is non-decreasing, x < pre[B]).
+__device__ __forceinline__ int find_seq(const int *pre, int B, int x) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Worker boundaries: worker w owns units [wstart(w), wstart(w+1)).
+__device__ __forceinline__ int wstart(long long w, long long U, long long nw) {
+    return static_cast<int>((w * U) / nw);
+}
+__device__ __forceinline__ int worker_of(long long x, long long U, long long nw) {
+    return static_cast<int>(((x + 1) * nw - 1) / U);
+}
+
+template <int NT>
+struct SegState {
+    float acc[NT][4][4];  // O^T fragments: [n-tile][d m-tile][c0..c3]
+    float m[NT][2];       // running max (log2 units) of heads 2(lane%4), +1
+    float l[NT][2];       // running sum, this lane's token rows only until reduced
+};
+
+template <int NT>
+__device__ __forceinline__ void state_reset(SegState<NT> &s) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) s.acc[n][mt][k] = 0.f;
+        s.m[n][0] = s.m[n][1] = -INFINITY;
+        s.l[n][0] = s.l[n][1] = 0.f;
+    }
+}
+
+// Sum the per-lane l over the 8 lanes holding the same heads (token rows).
+template <int NT>
+__device__ __forceinline__ void state_reduce_l(SegState<NT> &s) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float v = s.l[n][j];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            s.l[n][j] = v;
+        }
+}
+
+// Slot in shared memory holding one warp's partial state of a segment.
+template <int NT>
+struct Slot {
+    static constexpr int GP = NT * 8;
+    static constexpr int LD = kD + 4;  // padded row: conflict-free fragment stores
+    float m[GP];
+    float l[GP];
+    float acc[GP][LD];
+};
+
+template <int NT>
+__device__ __forceinline__ void state_to_slot(const SegState<NT> &s, Slot<NT> *slot, int lane) {
+    const int r = lane >> 2, c = (lane & 3) * 2;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        if (lane < 4) {
+            slot->m[n * 8 + c] = s.m[n][0];
+            slot->m[n * 8 + c + 1] = s.m[n][1];
+            slot->l[n * 8 + c] = s.l[n][0];
+            slot->l[n * 8 + c + 1] = s.l[n][1];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            slot->acc[n * 8 + c][mt * 16 + r] = s.acc[n][mt][0];
+            slot->acc[n * 8 + c + 1][mt * 16 + r] = s.acc[n][mt][1];
+            slot->acc[n * 8 + c][mt * 16 + r + 8] = s.acc[n][mt][2];
+            slot->acc[n * 8 + c + 1][mt * 16 + r + 8] = s.acc[n][mt][3];
+        }
+    }
+}
+
+// Final output of a segment finished by one warp: sink, normalise, bf16, store.
+template <int NT>
+__device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&sig)[NT][2],
+                                                __nv_bfloat16 *out_bg, int G, int lane) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        float f[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float M = fmaxf(s.m[n][j], sig[n][j]);
+            const float a = fast_exp2(s.m[n][j] - M);
+            const float den = s.l[n][j] * a + fast_exp2(sig[n][j] - M);
+            f[j] = a / den;
+        }
+        const int head = n * 8 + (lane >> 2);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t lo = movmatrix_t(pack_bf16(s.acc[n][mt][0] * f[0], s.acc[n][mt][1] * f[1]));
+            const uint32_t hi = movmatrix_t(pack_bf16(s.acc[n][mt][2] * f[0], s.acc[n][mt][3] * f[1]));
+            if (head < G) {
+                uint32_t *row = reinterpret_cast<uint32_t *>(out_bg + head * kD);
+                row[(mt * 16 + (lane & 3) * 2) >> 1] = lo;
+                row[(mt * 16 + 8 + (lane & 3) * 2) >> 1] = hi;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int NT, bool RING>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                       const Params p) {
+    constexpr int GP = NT * 8;
+    constexpr int kQBytes = GP * kD * 2;
+    constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
+    constexpr int kWarpBytes = kStages * kStageBytes;
+    static_assert(kWarpBytes % 1024 == 0, "tile buffers must stay 1024-byte aligned");
+    static_assert(2 * sizeof(Slot<NT>) <= kWarpBytes, "merge slots must fit a drained warp area");
+    constexpr int kSlotFloats = 2 * GP + GP * kD;  // global partial: m, l, acc
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * kWarpBytes);
+    int4 *meta = reinterpret_cast<int4 *>(bars + kWarps * kStages);
+    int *s_pre = reinterpret_cast<int *>(meta + kWarps * kStages);  // [B + 1]
+    int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
+    int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
+    int *s_winfo = s_wsum + kWarps;                                   // [kWarps][8]
+    int *s_flag = s_winfo + kWarps * 8;                               // [4]
+
+    const int B = p.B, Hkv = p.Hkv;
+
+    // ---- 1. lengths, validation, prefix of units over sequences
+    {
+        int v[4], tsum = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int b = tid * 4 + k;
+            int L = 0;
+            if (b < B) {
+                L = __ldg(p.seq_lens + b);
+                bool bad = L < 0;
+                if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
+                if (bad) {
+                    if (blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+                    L = 0;
+                }
+                s_len[b] = L;
+            }
+            v[k] = tiles_of<RING>(L, p.window) * Hkv;
+            tsum += v[k];
+        }
+        int incl = tsum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int woff = 0;
+        for (int w = 0; w < warp; ++w) woff += s_wsum[w];
+        int run = woff + incl - tsum;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int b = tid * 4 + k;
+            if (b < B) s_pre[b] = run;
+            run += v[k];
+        }
+        if (tid == kThreads - 1) s_pre[B] = run;  // total (all later b are beyond B)
+        __syncthreads();
+    }
+    const int U = s_pre[B];
+
+    // ---- 2. inactive slots get a zero output
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        if (s_len[b] != 0) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(b) * p.Hq * kD);
+        const int n16 = p.Hq * kD * 2 / 16;
+        for (int i = tid; i < n16; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (U == 0) return;
+
+    // ---- 3. workers and their unit ranges
+    const long long nwork =
+        min(static_cast<long long>(gridDim.x) * kWarps,
+            static_cast<long long>((U + kMinTilesPerWorker - 1) / kMinTilesPerWorker));
+    if (static_cast<long long>(blockIdx.x) * kWarps >= nwork) return;  // whole CTA idle
+    const long long wid = static_cast<long long>(blockIdx.x) * kWarps + warp;
+    const bool active = wid < nwork;
+    const int ua = active ? wstart(wid, U, nwork) : 0;
+    const int ue = active ? wstart(wid + 1, U, nwork) : 0;
+    const int n_tiles = ue - ua;
+
+    uint8_t *wbase = smem + warp * kWarpBytes;
+    const uint32_t wbase_s = smem_addr(wbase);
+    auto k_tile = [&](int st) { return wbase_s + st * kTileBytes; };
+    auto v_tile = [&](int st) { return wbase_s + (kStages + st) * kTileBytes; };
+    auto q_tile = [&](int st) { return wbase_s + 2 * kStages * kTileBytes + st * kQBytes; };
+    const uint32_t bar0 = smem_addr(bars + warp * kStages);
+    int4 *wmeta = meta + warp * kStages;
+
+    // per-lane ldmatrix offsets inside a swizzled 16 x 128 B tile
+    const int lj = lane & 7, lmi = lane >> 3;
+    const uint32_t k_row = ((lj + ((lmi & 1) << 3)) * 128);
+    const int k_cb = lmi >> 1;
+    const uint32_t v_row = ((lj + ((lmi >> 1) << 3)) * 128);
+    const int v_cb = lmi & 1;
+
+    SegState<NT> st;       // running state of the current segment
+    SegState<NT> head;     // saved state of the warp's first segment when shared
+    float sig[NT][2];      // sink logits (log2 units) of this lane's heads
+    uint32_t qf[NT][4][2]; // Q as mma B operand
+    int head_seg = -1, tail_seg = -1;
+    bool failed = false;
+
+    if (active) {
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+        const uint64_t policy = evict_first_policy();
+
+        // address batches: lane l describes unit ua + 32*k + l
+        int cb = 0, cg = 0, ct = 0, cp = 0, nb = 0, ng = 0, ntl = 0, np = 0;
+        auto load_batch = [&](int k, int &ob, int &og, int &ot, int &op) {
+            const int x = ua + 32 * k + lane;
+            ob = og = ot = op = 0;
+            if (x < ue) {
+                const int b = find_seq(s_pre, B, x);
+                const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
+                const int r = x - s_pre[b];
+                ob = b;
+                og = r / tiles;
+                ot = r - og * tiles;
+                if (!RING) {
+                    const int L = s_len[b];
+                    const int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+                    op = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + lo / kPage + ot);
+                }
+            }
+        };
+        load_batch(0, cb, cg, ct, cp);
+        if (n_tiles > 32) load_batch(1, nb, ng, ntl, np);
+        int cur_batch = 0;
+
+        auto issue = [&](int i) {
+            if ((i >> 5) != cur_batch) {  // advance to the next batch, prefetch the one after
+                cb = nb; cg = ng; ct = ntl; cp = np;
+                cur_batch = i >> 5;
+                if (n_tiles > 32 * (cur_batch + 1)) load_batch(cur_batch + 1, nb, ng, ntl, np);
+            }
+            const int src = i & 31;
+            const int tb = __shfl_sync(0xffffffffu, cb, src);
+            const int tg = __shfl_sync(0xffffffffu, cg, src);
+            const int tt = __shfl_sync(0xffffffffu, ct, src);
+            int tp = __shfl_sync(0xffffffffu, cp, src);
+            if (lane == 0) {
+                const int stg = i % kStages;
+                if (!RING && (tp < 0 || tp >= p.num_pages)) {
+                    flag_status(DA_STATUS_BAD_PAGE);
+                    tp = -1;  // TMA reads zeros out of bounds
+                }
+                const bool newseg = (i == 0) || (tt == 0);
+                wmeta[stg] = make_int4(tb, tg, tt, tp);
+                const uint32_t bar = bar0 + 8 * stg;
+                mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0));
+                int c1, c2;
+                if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
+                else { c1 = 0; c2 = tp * Hkv + tg; }
+                tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
+                tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
+                if (newseg)
+                    bulk_load(q_tile(stg),
+                              p.q + (static_cast<size_t>(tb) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
+                              p.G * kD * 2, bar);
+            }
+        };
+
+        const int pro = n_tiles < kStages ? n_tiles : kStages;
+        for (int i = 0; i < pro; ++i) issue(i);
+
+        // segment context
+        int sb = -1, sgk = -1;  // current segment (b, g)
+        int seg_first_unit = 0, seg_end_unit = 0;
+        int L = 0, lo = 0, ft = 0, nvalid = 0, app_tile = -1, app_row = 0;
+        uint32_t knew = 0, vnew = 0;
+        const bool do_append = p.k_new != nullptr;
+
+        int i = 0;
+        for (; i < n_tiles; ++i) {
+            const int stg = i % kStages;
+            if (!mbar_wait_bounded(bar0 + 8 * stg, (i / kStages) & 1)) {
+                failed = true;
+                break;
+            }
+            const int4 md = wmeta[stg];
+            const int tb = md.x, tg = md.y, tt = md.z, tp = md.w;
+            if (i == 0 || tt == 0) {
+                // close the previous segment
+                if (i > 0) {
+                    state_reduce_l(st);
+                    if (seg_first_unit < ua) {  // shared with earlier workers: keep for merge
+                        head = st;
+                        head_seg = sb * Hkv + sgk;
+                    } else {
+                        state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD,
+                                        p.G, lane);
+                    }
+                }
+                sb = tb; sgk = tg;
+                L = s_len[sb];
+                const int tiles = (s_pre[sb + 1] - s_pre[sb]) / Hkv;
+                seg_first_unit = s_pre[sb] + sgk * tiles;
+                seg_end_unit = seg_first_unit + tiles;
+                if (RING) {
+                    nvalid = L < p.window ? L : p.window;
+                    const int cell = (L - 1) % p.window;
+                    app_tile = cell / kPage;
+                    app_row = cell % kPage;
+                } else {
+                    lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+                    ft = lo / kPage;
+                    app_tile = (L - 1) / kPage - ft;
+                    app_row = (L - 1) % kPage;
+                }
+                if (do_append) {
+                    const size_t off = (static_cast<size_t>(sb) * Hkv + sgk) * kD + 2 * lane;
+                    knew = __ldg(reinterpret_cast<const uint32_t *>(p.k_new + off));
+                    vnew = __ldg(reinterpret_cast<const uint32_t *>(p.v_new + off));
+                }
+                // Q fragments (B operand): q[head = lane/4][d = 16ks + 2(lane%4) (+8)]
+                const uint8_t *qs = wbase + 2 * kStages * kTileBytes + stg * kQBytes;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const int hq = n * 8 + (lane >> 2);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        if (hq < p.G) {
+                            const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + hq * kD * 2);
+                            qf[n][ks][0] = row[ks * 8 + (lane & 3)];
+                            qf[n][ks][1] = row[ks * 8 + 4 + (lane & 3)];
+                        } else {
+                            qf[n][ks][0] = qf[n][ks][1] = 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int hs = n * 8 + (lane & 3) * 2 + j;
+                        sig[n][j] = (p.sinks != nullptr && hs < p.G)
+                                        ? __ldg(p.sinks + sgk * p.G + hs) * kLog2e
+                                        : -INFINITY;
+                    }
+                }
+                state_reset(st);
+            }
+
+            const uint32_t sK = k_tile(stg), sV = v_tile(stg);
+            uint8_t *gK = wbase + stg * kTileBytes;
+            uint8_t *gV = wbase + (kStages + stg) * kTileBytes;
+
+            // fused append: this tile holds position p = L - 1
+            if (do_append && tt == app_tile) {
+                const uint32_t off = app_row * 128 + ((((lane >> 2) ^ (app_row & 7))) << 4) + (lane & 3) * 4;
+                *reinterpret_cast<uint32_t *>(gK + off) = knew;
+                *reinterpret_cast<uint32_t *>(gV + off) = vnew;
+                size_t cell;
+                bool ok = true;
+                if (RING) {
+                    cell = (static_cast<size_t>(sb) * Hkv + sgk) * p.window + (tt * kPage + app_row);
+                } else {
+                    ok = tp >= 0;
+                    cell = (static_cast<size_t>(tp) * Hkv + sgk) * kPage + app_row;
+                }
+                if (ok) {
+                    reinterpret_cast<uint32_t *>(p.k_cache + cell * kD)[lane] = knew;
+                    reinterpret_cast<uint32_t *>(p.v_cache + cell * kD)[lane] = vnew;
+                }
+                __syncwarp();
+            }
+
+            // token validity of this lane's rows
+            int t0, lo_v, hi_v;
+            if (RING) { t0 = tt * kPage; lo_v = 0; hi_v = nvalid; }
+            else { t0 = (ft + tt) * kPage; lo_v = lo; hi_v = L; }
+            const bool partial = (t0 < lo_v) || (t0 + kPage > hi_v);
+            const int r0 = t0 + (lane >> 2);
+            const bool ok_lo = r0 >= lo_v && r0 < hi_v;
+            const bool ok_hi = (r0 + 8) >= lo_v && (r0 + 8) < hi_v;
+
+            // S^T = K Q^T  (16 tokens x 8 heads per n-tile)
+            uint32_t ka[4][4];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3]);
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(sc, ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3], qf[n][ks][0], qf[n][ks][1]);
+                float s0 = ok_lo ? sc[0] * p.scale_log2 : -INFINITY;
+                float s1 = ok_lo ? sc[1] * p.scale_log2 : -INFINITY;
+                float s2 = ok_hi ? sc[2] * p.scale_log2 : -INFINITY;
+                float s3 = ok_hi ? sc[3] * p.scale_log2 : -INFINITY;
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 8));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 8));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
+                const float mn0 = fmaxf(st.m[n][0], mx0), mn1 = fmaxf(st.m[n][1], mx1);
+                const float a0 = fast_exp2(st.m[n][0] - mn0), a1 = fast_exp2(st.m[n][1] - mn1);
+                const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+                const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+                st.l[n][0] = st.l[n][0] * a0 + (p0 + p2);
+                st.l[n][1] = st.l[n][1] * a1 + (p1 + p3);
+                st.m[n][0] = mn0;
+                st.m[n][1] = mn1;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    st.acc[n][mt][0] *= a0;
+                    st.acc[n][mt][1] *= a1;
+                    st.acc[n][mt][2] *= a0;
+                    st.acc[n][mt][3] *= a1;
+                }
+                pb[n][0] = movmatrix_t(pack_bf16(p0, p1));  // tokens 2(lane%4)+{0,1}
+                pb[n][1] = movmatrix_t(pack_bf16(p2, p3));  // tokens 8+2(lane%4)+{0,1}
+            }
+
+            // O^T += V^T P^T  (64 d x 8 heads per n-tile)
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (partial) {
+                const int tv = t0 + (lane & 3) * 2;
+                vm0 = ((tv >= lo_v && tv < hi_v) ? 0x0000ffffu : 0u) |
+                      ((tv + 1 >= lo_v && tv + 1 < hi_v) ? 0xffff0000u : 0u);
+                vm1 = ((tv + 8 >= lo_v && tv + 8 < hi_v) ? 0x0000ffffu : 0u) |
+                      ((tv + 9 >= lo_v && tv + 9 < hi_v) ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), a0, a1, a2, a3);
+                a0 &= vm0; a1 &= vm0; a2 &= vm1; a3 &= vm1;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma_bf16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+            }
+
+            __syncwarp();
+            if (i + kStages < n_tiles) {
+                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(i + kStages);
+            }
+        }
+
+        if (failed) {
+            flag_status(DA_STATUS_TIMEOUT);
+            // let the copies still in flight land before the buffers are reused
+            for (int j = i + 1; j < n_tiles && j < i + kStages; ++j)
+                mbar_wait_bounded(bar0 + 8 * (j % kStages), (j / kStages) & 1);
+        }
+        __syncwarp();
+
+        // close the last segment
+        state_reduce_l(st);
+        const bool last_shared = failed || seg_first_unit < ua || seg_end_unit > ue;
+        if (last_shared) {
+            tail_seg = sb * Hkv + sgk;
+        } else {
+            state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD, p.G, lane);
+        }
+        // partial states -> this warp's (drained) buffer area
+        Slot<NT> *slots = reinterpret_cast<Slot<NT> *>(wbase);
+        if (head_seg >= 0) state_to_slot(head, &slots[0], lane);
+        if (tail_seg >= 0) state_to_slot(st, &slots[1], lane);
+    }
+    if (lane == 0) {
+        int *wi = s_winfo + warp * 8;
+        wi[0] = ua; wi[1] = ue; wi[2] = head_seg; wi[3] = tail_seg; wi[4] = active ? 1 : 0;
+    }
+    __syncthreads();
+
+    // ---- 4. merge segments shared between warps of this CTA
+    const long long cta_w0 = static_cast<long long>(blockIdx.x) * kWarps;
+    const long long cta_w1 = min(cta_w0 + kWarps, nwork);
+    const int R0 = wstart(cta_w0, U, nwork), R1 = wstart(cta_w1, U, nwork);
+    const int nw_cta = static_cast<int>(cta_w1 - cta_w0);
+    auto seg_range = [&](int seg, int &s0, int &s1) {
+        const int b = seg / Hkv, g = seg - b * Hkv;
+        const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
+        s0 = s_pre[b] + g * tiles;
+        s1 = s0 + tiles;
+    };
+    // the CTA's first segment (global partial slot 0); any other boundary segment uses slot 1
+    int cta_first_seg;
+    {
+        const int b = find_seq(s_pre, B, R0);
+        const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
+        cta_first_seg = b * Hkv + (R0 - s_pre[b]) / tiles;
+    }
+    if (warp < nw_cta) {
+        const int *wi = s_winfo + warp * 8;
+        const int my_a = wi[0];
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+            const int seg = wi[2 + which];
+            if (seg < 0) continue;
+            int s0, s1;
+            seg_range(seg, s0, s1);
+            if (!(warp == 0 || s0 >= my_a)) continue;  // an earlier warp of this CTA leads
+            // contributors: this warp and the following warps that start inside the segment
+            int w_end = warp;
+            while (w_end + 1 < nw_cta && s_winfo[(w_end + 1) * 8] < s1) ++w_end;
+            const bool internal = s0 >= R0 && s1 <= R1;
+            const int b = seg / Hkv, g = seg - b * Hkv;
+            // lane -> (head n, 16 d values)
+            for (int item = lane; item < GP * 4; item += 32) {
+                const int n = item >> 2, d0 = (item & 3) * 16;
+                float M = -INFINITY;
+                for (int w = warp; w <= w_end; ++w) {
+                    const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
+                                         ((s_winfo[w * 8 + 3] == seg) ? 1 : 0);
+                    M = fmaxf(M, sl->m[n]);
+                }
+                float sg = -INFINITY;
+                if (internal && p.sinks != nullptr && n < p.G) sg = __ldg(p.sinks + g * p.G + n) * kLog2e;
+                const float Mf = internal ? fmaxf(M, sg) : M;
+                float den = internal ? fast_exp2(sg - Mf) : 0.f;
+                float acc[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+                for (int w = warp; w <= w_end; ++w) {
+                    const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
+                                         ((s_winfo[w * 8 + 3] == seg) ? 1 : 0);
+                    const float wgt = fast_exp2(sl->m[n] - Mf);
+                    den += sl->l[n] * wgt;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) acc[k] += sl->acc[n][d0 + k] * wgt;
+                }
+                if (internal) {
+                    if (n < p.G) {
+                        const float inv = 1.f / den;
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            p.out + (static_cast<size_t>(b) * p.Hq + g * p.G + n) * kD + d0);
+                        uint4 o0, o1;
+                        o0.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                        o0.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                        o0.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+                        o0.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+                        o1.x = pack_bf16(acc[8] * inv, acc[9] * inv);
+                        o1.y = pack_bf16(acc[10] * inv, acc[11] * inv);
+                        o1.z = pack_bf16(acc[12] * inv, acc[13] * inv);
+                        o1.w = pack_bf16(acc[14] * inv, acc[15] * inv);
+                        dst[0] = o0;
+                        dst[1] = o1;
+                    }
+                } else {
+                    float *gp = p.part + (static_cast<size_t>(blockIdx.x) * 2 + (seg == cta_first_seg ? 0 : 1)) *
+                                             kSlotFloats;
+                    if (d0 == 0) {
+                        gp[n] = M;
+                        gp[GP + n] = den;
+                    }
+                    float4 *ga = reinterpret_cast<float4 *>(gp + 2 * GP + n * kD + d0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ga[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+                }
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+
+    // ---- 5. segments shared with other CTAs: ticket, and the last CTA combines
+    if (tid == 0) {
+        s_flag[0] = s_flag[1] = -1;
+        int cand[2] = {cta_first_seg, -1};
+        {
+            const int b = find_seq(s_pre, B, R1 - 1);
+            const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
+            const int last = b * Hkv + (R1 - 1 - s_pre[b]) / tiles;
+            if (last != cta_first_seg) cand[1] = last;
+        }
+        for (int k = 0; k < 2; ++k) {
+            const int seg = cand[k];
+            if (seg < 0) continue;
+            int s0, s1;
+            seg_range(seg, s0, s1);
+            if (s0 >= R0 && s1 <= R1) continue;  // finished inside this CTA
+            const int c_lo = worker_of(s0, U, nwork) / kWarps;
+            const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+            const int ticket = atomicAdd(p.counters + seg, 1);
+            if (ticket == c_hi - c_lo) {
+                __threadfence();
+                s_flag[k] = seg;
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+        const int seg = s_flag[k];
+        if (seg < 0) continue;
+        int s0, s1;
+        seg_range(seg, s0, s1);
+        const int c_lo = worker_of(s0, U, nwork) / kWarps;
+        const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+        // the first contributing CTA may have started before this segment (slot 1)
+        const int lo_slot = (wstart(static_cast<long long>(c_lo) * kWarps, U, nwork) < s0) ? 1 : 0;
+        const int b = seg / Hkv, g = seg - b * Hkv;
+        constexpr int kPer = GP * kD / kThreads;  // 2 (G<=8) or 4 (G=16) outputs per thread
+        const int n = tid / (kD / kPer), d0 = (tid % (kD / kPer)) * kPer;
+        float M = -INFINITY, den = 0.f, acc[kPer];
+#pragma unroll
+        for (int k2 = 0; k2 < kPer; ++k2) acc[k2] = 0.f;
+#pragma unroll 4
+        for (int c = c_lo; c <= c_hi; ++c) {
+            const float *gp = p.part + (static_cast<size_t>(c) * 2 + (c == c_lo ? lo_slot : 0)) * kSlotFloats;
+            const float mc = __ldcg(gp + n), lc = __ldcg(gp + GP + n);
+            float v[kPer];
+            if constexpr (kPer == 2) {
+                const float2 t = __ldcg(reinterpret_cast<const float2 *>(gp + 2 * GP + n * kD + d0));
+                v[0] = t.x; v[1] = t.y;
+            } else {
+                const float4 t = __ldcg(reinterpret_cast<const float4 *>(gp + 2 * GP + n * kD + d0));
+                v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+            }
+            const float Mn = fmaxf(M, mc);
+            const float a = fast_exp2(M - Mn), w = fast_exp2(mc - Mn);
+            den = den * a + lc * w;
+#pragma unroll
+            for (int k2 = 0; k2 < kPer; ++k2) acc[k2] = acc[k2] * a + v[k2] * w;
+            M = Mn;
+        }
+        const float sg = (p.sinks != nullptr && n < p.G) ? __ldg(p.sinks + g * p.G + n) * kLog2e : -INFINITY;
+        const float Mf = fmaxf(M, sg);
+        const float a = fast_exp2(M - Mf);
+        den = den * a + fast_exp2(sg - Mf);
+        const float f = a / den;
+        if (n < p.G) {
+            __nv_bfloat16 *dst = p.out + (static_cast<size_t>(b) * p.Hq + g * p.G + n) * kD + d0;
+#pragma unroll
+            for (int k2 = 0; k2 < kPer; k2 += 2)
+                *reinterpret_cast<uint32_t *>(dst + k2) = pack_bf16(acc[k2] * f, acc[k2 + 1] * f);
+        }
+        if (tid == 0) p.counters[seg] = 0;  // ready for the next call
+    }
+}
+
+// ------------------------------------------------------------------ standalone append
+__global__ void kv_append_kernel(const __nv_bfloat16 *__restrict__ k_new,
+                                 const __nv_bfloat16 *__restrict__ v_new, __nv_bfloat16 *k_cache,
+                                 __nv_bfloat16 *v_cache, const int *__restrict__ block_table,
+                                 const int *__restrict__ seq_lens, int Hkv, int D, int window,
+                                 int page_size, int max_pages, int num_pages) {
+    const int b = blockIdx.x;
+    const int L = __ldg(seq_lens + b);
+    if (L <= 0) {
+        if (L < 0 && threadIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+        return;
+    }
+    const int pos = L - 1;
+    size_t base;  // element offset of (head 0, the cell of pos) in the caches
+    size_t head_stride;
+    if (block_table != nullptr) {
+        if (pos / page_size >= max_pages) {
+            if (threadIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+            return;
+        }
+        const int page = __ldg(block_table + static_cast<size_t>(b) * max_pages + pos / page_size);
+        if (page < 0 || page >= num_pages) {
+            if (threadIdx.x == 0) flag_status(DA_STATUS_BAD_PAGE);
+            return;
+        }
+        base = (static_cast<size_t>(page) * Hkv * page_size + pos % page_size) * D;
+        head_stride = static_cast<size_t>(page_size) * D;
+    } else {
+        base = (static_cast<size_t>(b) * Hkv * window + pos % window) * D;
+        head_stride = static_cast<size_t>(window) * D;
+    }
+    const int chunks = D / 8;  // 16-byte chunks per row
+    for (int i = threadIdx.x; i < Hkv * chunks; i += blockDim.x) {
+        const int g = i / chunks, c = i % chunks;
+        const size_t src = (static_cast<size_t>(b) * Hkv + g) * D + c * 8;
+        const size_t dst = base + g * head_stride + c * 8;
+        *reinterpret_cast<uint4 *>(k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+        *reinterpret_cast<uint4 *>(v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+    }
+}
+
+// ------------------------------------------------------------------ host side
+thread_local char t_err[256];
+
+int set_cuda_error(cudaError_t e) {
+    snprintf(t_err, sizeof t_err, "CUDA error: %s", cudaGetErrorString(e));
+    return DA_ERR_CUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 3-D map over a bf16 cache viewed as [slices][rows][64]; box = 16 rows x 64.
+bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), rows, slices};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, rows * kD * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kPage), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    int sm_count = 0;
+    bool attr_set[4] = {false, false, false, false};
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (*dev < 0 || *dev >= kMaxDevices) return DA_ERR_UNSUPPORTED;
+    return DA_OK;
+}
+
+int sm_count(int dev) {
+    if (g_dev[dev].sm_count == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        g_dev[dev].sm_count = n;
+    }
+    return g_dev[dev].sm_count;
+}
+
+size_t slot_floats(int G) {
+    const int gp = G <= 8 ? 8 : 16;
+    return static_cast<size_t>(2 * gp + gp * kD);
+}
+
+size_t workspace_for(int G, int ctas) {
+    return kCounterBytes + static_cast<size_t>(ctas) * 2 * slot_floats(G) * sizeof(float);
+}
+
+int reserve_locked(int dev, size_t bytes) {
+    DeviceState &d = g_dev[dev];
+    if (d.ws_bytes >= bytes) return DA_OK;
+    if (d.ws) {
+        cudaError_t e = cudaFree(d.ws);
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+        if (e != cudaSuccess) return set_cuda_error(e);
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    e = cudaMemset(p, 0, bytes);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return set_cuda_error(e);
+    }
+    d.ws = p;
+    d.ws_bytes = bytes;
+    return DA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const da_shape &s) {
+    if (s.batch < 0 || s.num_q_heads <= 0 || s.num_kv_heads <= 0 || s.head_dim <= 0) return DA_ERR_INVALID_ARG;
+    if (s.num_q_heads % s.num_kv_heads != 0) return DA_ERR_INVALID_ARG;
+    const int G = s.num_q_heads / s.num_kv_heads;
+    if (s.head_dim != kD) return DA_ERR_UNSUPPORTED;
+    if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return DA_ERR_UNSUPPORTED;
+    if (s.batch > kMaxBatch) return DA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(s.batch) * s.num_kv_heads > kMaxSegments) return DA_ERR_UNSUPPORTED;
+    return DA_OK;
+}
+
+template <int NT, bool RING>
+int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
+    constexpr int GP = NT * 8;
+    constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2);
+    const size_t smem = 1024 + static_cast<size_t>(kWarps) * kWarpBytes + kWarps * kStages * (8 + 16) +
+                        (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * sizeof(int);
+    auto kern = decode_attn_kernel<NT, RING>;
+    const int idx = (NT - 1) * 2 + (RING ? 1 : 0);
+    if (!g_dev[dev].attr_set[idx]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return set_cuda_error(e);
+        g_dev[dev].attr_set[idx] = true;
+    }
+    kern<<<sm_count(dev), kThreads, smem, stream>>>(mk, mv, prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return DA_OK;
+}
+
+int prepare_workspace(int dev, int G, cudaStream_t stream, float **part, int **counters) {
+    const size_t need = workspace_for(G, sm_count(dev));
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].ws_bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
+        int rc = reserve_locked(dev, need);
+        if (rc != DA_OK) return rc;
+    }
+    *counters = static_cast<int *>(g_dev[dev].ws);
+    *part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws) + kCounterBytes);
+    return DA_OK;
+}
+
+int run_attention(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                  const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
+                  float scale, void *out, const da_shape &s, int page_size, int max_pages, int num_pages,
+                  int max_seq_len, void *stream_v) {
+    int rc = check_shape(s);
+    if (rc != DA_OK) return rc;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return DA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return DA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return DA_ERR_INVALID_ARG;
+    const int G = s.num_q_heads / s.num_kv_heads;
+    if (ring) {
+        if (window < kPage) return window <= 0 ? DA_ERR_INVALID_ARG : DA_ERR_UNSUPPORTED;
+    } else {
+        if (!block_table || window < 0 || max_pages <= 0 || num_pages <= 0 || max_seq_len < 0)
+            return DA_ERR_INVALID_ARG;
+        if (page_size != kPage) return DA_ERR_UNSUPPORTED;
+        if (static_cast<long long>(max_pages) * kPage < max_seq_len) return DA_ERR_INVALID_ARG;
+        if (static_cast<long long>(num_pages) * s.num_kv_heads > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+    }
+    if (s.batch == 0) return DA_OK;
+    int dev;
+    rc = current_device(&dev);
+    if (rc != DA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+    Params prm;
+    prm.q = static_cast<const __nv_bfloat16 *>(q);
+    prm.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    prm.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+    prm.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
+    prm.block_table = block_table;
+    prm.seq_lens = seq_lens;
+    prm.sinks = sinks;
+    prm.out = static_cast<__nv_bfloat16 *>(out);
+    prm.B = s.batch;
+    prm.Hq = s.num_q_heads;
+    prm.Hkv = s.num_kv_heads;
+    prm.G = G;
+    prm.window = window;
+    prm.max_pages = ring ? 0 : max_pages;
+    prm.num_pages = ring ? 0 : num_pages;
+    prm.max_seq_len = ring ? 0 : max_seq_len;
+    prm.scale_log2 = scale * kLog2e;
+    rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
+    if (rc != DA_OK) return rc;
+
+    CUtensorMap mk, mv;
+    const uint64_t rows = ring ? static_cast<uint64_t>(window) : static_cast<uint64_t>(kPage);
+    const uint64_t slices = ring ? static_cast<uint64_t>(s.batch) * s.num_kv_heads
+                                 : static_cast<uint64_t>(num_pages) * s.num_kv_heads;
+    if (!make_kv_map(&mk, k_cache, rows, slices) || !make_kv_map(&mv, v_cache, rows, slices)) {
+        snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
+        return DA_ERR_CUDA;
+    }
+    if (G <= 8) return ring ? launch_attn<1, true>(mk, mv, prm, dev, stream) : launch_attn<1, false>(mk, mv, prm, dev, stream);
+    return ring ? launch_attn<2, true>(mk, mv, prm, dev, stream) : launch_attn<2, false>(mk, mv, prm, dev, stream);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+int decode_attn_paged(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                      const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
+                      float scale, void *out, da_shape s, int page_size, int max_pages_per_seq, int num_pages,
+                      int max_seq_len, void *stream) {
+    return run_attention(false, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window, scale,
+                         out, s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream);
+}
+
+int decode_attn_ring(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                     const int32_t *seq_lens, const float *sinks, int window, float scale, void *out, da_shape s,
+                     void *stream) {
+    return run_attention(true, q, k_new, v_new, k_cache, v_cache, nullptr, seq_lens, sinks, window, scale, out, s,
+                         kPage, 0, 0, 0, stream);
+}
+
+int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, const int32_t *block_table,
+              const int32_t *seq_lens, int window, da_shape s, int page_size, int max_pages_per_seq, int num_pages,
+              void *stream) {
+    if (s.batch < 0 || s.num_kv_heads <= 0 || s.head_dim <= 0) return DA_ERR_INVALID_ARG;
+    if (s.head_dim % 8 != 0) return DA_ERR_UNSUPPORTED;
+    if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens) return DA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return DA_ERR_INVALID_ARG;
+    if (block_table) {
+        if (page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0) return DA_ERR_INVALID_ARG;
+    } else if (window <= 0) {
+        return DA_ERR_INVALID_ARG;
+    }
+    if (s.batch == 0) return DA_OK;
+    kv_append_kernel<<<s.batch, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new),
+        static_cast<__nv_bfloat16 *>(k_cache), static_cast<__nv_bfloat16 *>(v_cache), block_table, seq_lens,
+        s.num_kv_heads, s.head_dim, window, page_size, max_pages_per_seq, num_pages);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DA_OK : set_cuda_error(e);
+}
+
+size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len) {
+    (void)max_seq_len;
+    if (check_shape(s) != DA_OK) return 0;
+    int dev;
+    if (current_device(&dev) != DA_OK) return 0;
+    return workspace_for(s.num_q_heads / s.num_kv_heads, sm_count(dev));
+}
+
+int decode_attn_reserve(size_t bytes) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc != DA_OK) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return reserve_locked(dev, bytes);
+}
+
+int decode_attn_device_status(void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int h = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_status, sizeof h, 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return static_cast<int>(h & 0x7fffffffu);
+}
+
+const char *decode_attn_error_string(int code) {
+    switch (code) {
+        case DA_OK: return "ok";
+        case DA_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size, Hq % Hkv != 0)";
+        case DA_ERR_UNSUPPORTED: return "unsupported shape (needs head_dim 64, page 16, G in {1,2,4,8,16}, batch <= 1024, ring window >= 16)";
+        case DA_ERR_WORKSPACE: return "workspace too small during stream capture: call decode_attn_reserve() first";
+        case DA_ERR_CUDA: return t_err[0] ? t_err : "CUDA error";
+        default: return "unknown error code";
+    }
+}
+
+}  // extern "C"

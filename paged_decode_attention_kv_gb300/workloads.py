@@ -16,7 +16,7 @@ query heads, 8 KV heads, head dim 64, page 16, window 128):
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 import torch
 
