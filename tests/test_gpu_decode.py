@@ -67,13 +67,14 @@ def pre(c):
     return np.maximum(c.lens - 1, 0)
 
 
-def paged_setup(c, seed, spare=5):
-    kp, vp, bt = paged_identity(c, pre(c))
+def paged_setup(c, seed, spare=5, appended=False):
+    """Pools before this step's append (fused calls) or after it (calls without k_new)."""
+    kp, vp, bt = paged_identity(c, c.lens if appended else pre(c))
     return shuffle_pages(kp, vp, bt, seed, spare=spare)
 
 
 def check_paged(c, window, seed=0, fused=True, sinks=True):
-    kp, vp, bt = paged_setup(c, seed)
+    kp, vp, bt = paged_setup(c, seed, appended=not fused)
     got, ak, av = run_paged(c, kp, vp, bt, window, fused=fused, sinks=sinks)
     ref = oracle.decode_paged(c.q, c.k_new if fused else None, c.v_new if fused else None, kp, vp,
                               bt, c.lens, c.sinks if sinks else None, window, c.scale, c.P)
@@ -88,7 +89,7 @@ def check_paged(c, window, seed=0, fused=True, sinks=True):
 
 
 def check_ring(c, W, fused=True, sinks=True):
-    kr, vr = ring_from_history(c, pre(c), W)
+    kr, vr = ring_from_history(c, pre(c) if fused else c.lens, W)
     got, ak, av = run_ring(c, kr, vr, W, fused=fused, sinks=sinks)
     ref = oracle.decode_ring(c.q, c.k_new if fused else None, c.v_new if fused else None, kr, vr,
                              c.lens, c.sinks if sinks else None, W, c.scale)
