@@ -147,12 +147,13 @@ def cpu_cores():
 class StepInputs:
     """One independent copy of a step's inputs and caches on the device."""
 
-    def __init__(self, name, device, seed_offset=0):
+    def __init__(self, name, device, seed_offset=0, batch_limit=None):
         import torch
         from paged_decode_attention_kv_gb300 import workloads as wl
         cfg = wl.config(name)
+        self.lens = wl.seq_lens(name)[:batch_limit]
+        cfg["B"] = len(self.lens)
         self.cfg = cfg
-        self.lens = wl.seq_lens(name)
         seed = cfg["seed"] + seed_offset
         gen = wl.cpu_generator(seed)
         vgen = torch.Generator(device=device)
@@ -199,21 +200,24 @@ def oracle_sample(name, s: "StepInputs", budget_s):
     cores = oracle.default_threads()
     done_bytes, elapsed, seqs = 0, 0.0, 0
     order = [b for b in range(len(lens)) if lens[b] > 0]
-    for b in order:
-        items = [(b, h) for h in range(Hq)]
-        t0 = time.perf_counter()
-        oracle.decode_paged(q, kn, vn, kp, vp, bt, lens, sinks, 0, s.inp.scale, P, items=items,
-                            nthreads=cores)
-        oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
-                           nthreads=cores)
-        elapsed += time.perf_counter() - t0
-        pb, rb = step_bytes(name, [int(lens[b])])
-        done_bytes += pb + rb
-        seqs += 1
-        if elapsed >= budget_s:
-            break
-    desc = (f"{seqs} of {len(order)} active sequences, all {Hq} heads, full + ring layer; "
-            f"{elapsed:.1f} s on {cores} threads")
+    passes = 0
+    while elapsed < budget_s and order:
+        for b in order:
+            items = [(b, h) for h in range(Hq)]
+            t0 = time.perf_counter()
+            oracle.decode_paged(q, kn, vn, kp, vp, bt, lens, sinks, 0, s.inp.scale, P,
+                                items=items, nthreads=cores)
+            oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
+                               nthreads=cores)
+            elapsed += time.perf_counter() - t0
+            pb, rb = step_bytes(name, [int(lens[b])])
+            done_bytes += pb + rb
+            seqs += 1
+            if elapsed >= budget_s:
+                break
+        passes += 1
+    desc = (f"{seqs} sequence-steps ({passes} pass(es) over the {len(order)} active sequences), "
+            f"all {Hq} heads, full + ring layer; {elapsed:.1f} s on {cores} threads")
     return done_bytes / elapsed / 1e9, cores, desc
 
 
@@ -224,7 +228,7 @@ def run_reference(args, rank, world):
         return None
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    s = StepInputs(args.workload, device)
+    s = StepInputs(args.workload, device, batch_limit=args.batch_limit)
     # each step is a bounded sample: calibrate so that warmup+steps fit ~90 s
     per_step = max(0.02, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -257,7 +261,7 @@ def workload_config(name, s):
             "window": c["window"], "mean_len": round(sum(lens) / max(1, len(lens)), 1),
             "max_len": max(lens) if lens else 0,
             "layers_per_step": ["paged full attention", f"ring window {c['window']}"],
-            "parallelism": "replicas"}
+            "parallelism": "replicas", **({"note": c["workload_note"]} if "workload_note" in c else {})}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -267,14 +271,17 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    first = StepInputs(args.workload, dev)
+    first = StepInputs(args.workload, dev, batch_limit=args.batch_limit)
     set_bytes = first.nbytes()
     n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
-    sets = [first] + [StepInputs(args.workload, dev, seed_offset=i) for i in range(1, n_sets)]
+    sets = [first] + [StepInputs(args.workload, dev, seed_offset=i, batch_limit=args.batch_limit)
+                      for i in range(1, n_sets)]
     cfg = first.cfg
     B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
     da.decode_attn_reserve(da.decode_attn_workspace_bytes(B, Hq, Hkv, D))
     pbytes, rbytes = step_bytes(args.workload, first.lens)
+    if args.batch_limit is not None:
+        first.cfg["workload_note"] = f"first {args.batch_limit} sequences only"
     stream = torch.cuda.current_stream()
 
     def step(s):
@@ -398,6 +405,8 @@ def main():
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--batch-limit", type=int, default=None,
+                    help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
