@@ -31,7 +31,7 @@
  *   - Return value: 0 on success, else a negative DA_ERR_* code; nothing is
  *     launched when a code is returned.
  *   - Supported now: head_dim 64, page_size 16, query heads per KV head
- *     (G = Hq/Hkv) in {1, 2, 4, 8, 16}, batch <= 1024, batch*Hkv <= 65536,
+ *     (G = Hq/Hkv) in {1, 2, 4, 8, 16}, batch <= 1024, Hq <= 1024, batch*Hkv <= 65536,
  *     ring capacity >= 16. Anything else returns DA_ERR_UNSUPPORTED.
  *   - The attention entry points use a library-owned workspace per device
  *     (split partials and arrival counters). It is allocated on first use or

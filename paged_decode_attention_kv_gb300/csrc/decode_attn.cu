@@ -58,6 +58,7 @@ constexpr int kMinTilesPerWorker = DA_MIN_TILES;
 constexpr int kTileBytes = kPage * kD * 2;  // 2048 B of K (or V) per tile
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxSegments = 65536;         // B * Hkv
+constexpr int kMaxQHeads = 1024;
 constexpr int kCounterBytes = kMaxSegments * 4;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per tile wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
     constexpr int GP = NT * 8;
-    constexpr int kQBytes = GP * kD * 2;
+    constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2;  // the group's q rows, then k_new, v_new
     constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
     constexpr int kWarpBytes = kStages * kStageBytes;
     static_assert(kWarpBytes % 1024 == 0, "tile buffers must stay 1024-byte aligned");
@@ -338,11 +339,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
     int *s_winfo = s_wsum + kWarps;                                   // [kWarps][8]
     int *s_flag = s_winfo + kWarps * 8;                               // [4]
+    float *s_sink = reinterpret_cast<float *>(s_flag + 4);            // [Hq], log2 units
+
+    if (tid == 0) {  // descriptor fetch overlaps the length loads below
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
 
     const int B = p.B, Hkv = p.Hkv;
 
     // ---- 1. lengths, validation, prefix of units over sequences
     {
+        for (int h = tid; h < p.Hq; h += kThreads)
+            s_sink[h] = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
         int v[4], tsum = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -476,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool newseg = (i == 0) || (tt == 0);
                 wmeta[stg] = make_int4(tb, tg, tt, tp);
                 const uint32_t bar = bar0 + 8 * stg;
-                mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0));
+                const bool rows = newseg && p.k_new != nullptr;
+                mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0));
                 int c1, c2;
                 if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
                 else { c1 = 0; c2 = tp * Hkv + tg; }
@@ -486,6 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_load(q_tile(stg),
                               p.q + (static_cast<size_t>(tb) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
                               p.G * kD * 2, bar);
+                if (rows) {
+                    const size_t off = (static_cast<size_t>(tb) * Hkv + tg) * kD;
+                    bulk_load(q_tile(stg) + GP * kD * 2, p.k_new + off, kD * 2, bar);
+                    bulk_load(q_tile(stg) + GP * kD * 2 + kD * 2, p.v_new + off, kD * 2, bar);
+                }
             }
         };
 
@@ -536,13 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     app_tile = (L - 1) / kPage - ft;
                     app_row = (L - 1) % kPage;
                 }
-                if (do_append) {
-                    const size_t off = (static_cast<size_t>(sb) * Hkv + sgk) * kD + 2 * lane;
-                    knew = __ldg(reinterpret_cast<const uint32_t *>(p.k_new + off));
-                    vnew = __ldg(reinterpret_cast<const uint32_t *>(p.v_new + off));
-                }
                 // Q fragments (B operand): q[head = lane/4][d = 16ks + 2(lane%4) (+8)]
                 const uint8_t *qs = wbase + 2 * kStages * kTileBytes + stg * kQBytes;
+                if (do_append) {  // the new token's k/v rows arrived with this tile
+                    knew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2)[lane];
+                    vnew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2 + kD * 2)[lane];
+                }
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     const int hq = n * 8 + (lane >> 2);
@@ -559,9 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int hs = n * 8 + (lane & 3) * 2 + j;
-                        sig[n][j] = (p.sinks != nullptr && hs < p.G)
-                                        ? __ldg(p.sinks + sgk * p.G + hs) * kLog2e
-                                        : -INFINITY;
+                        sig[n][j] = hs < p.G ? s_sink[sgk * p.G + hs] : -INFINITY;
                     }
                 }
                 state_reset(st);
@@ -736,8 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          ((s_winfo[w * 8 + 3] == seg) ? 1 : 0);
                     M = fmaxf(M, sl->m[n]);
                 }
-                float sg = -INFINITY;
-                if (internal && p.sinks != nullptr && n < p.G) sg = __ldg(p.sinks + g * p.G + n) * kLog2e;
+                const float sg = (internal && n < p.G) ? s_sink[g * p.G + n] : -INFINITY;
                 const float Mf = internal ? fmaxf(M, sg) : M;
                 float den = internal ? fast_exp2(sg - Mf) : 0.f;
                 float acc[16];
@@ -781,9 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ga[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
                 }
             }
+            if (!internal) __threadfence();  // partial visible before this CTA takes a ticket
         }
     }
-    __threadfence();
     __syncthreads();
 
     // ---- 5. segments shared with other CTAs: ticket, and the last CTA combines
@@ -847,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k2 = 0; k2 < kPer; ++k2) acc[k2] = acc[k2] * a + v[k2] * w;
             M = Mn;
         }
-        const float sg = (p.sinks != nullptr && n < p.G) ? __ldg(p.sinks + g * p.G + n) * kLog2e : -INFINITY;
+        const float sg = n < p.G ? s_sink[g * p.G + n] : -INFINITY;
         const float Mf = fmaxf(M, sg);
         const float a = fast_exp2(M - Mf);
         den = den * a + fast_exp2(sg - Mf);
@@ -1009,7 +1020,7 @@ int check_shape(const da_shape &s) {
     const int G = s.num_q_heads / s.num_kv_heads;
     if (s.head_dim != kD) return DA_ERR_UNSUPPORTED;
     if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return DA_ERR_UNSUPPORTED;
-    if (s.batch > kMaxBatch) return DA_ERR_UNSUPPORTED;
+    if (s.batch > kMaxBatch || s.num_q_heads > kMaxQHeads) return DA_ERR_UNSUPPORTED;
     if (static_cast<long long>(s.batch) * s.num_kv_heads > kMaxSegments) return DA_ERR_UNSUPPORTED;
     return DA_OK;
 }
@@ -1017,13 +1028,16 @@ int check_shape(const da_shape &s) {
 template <int NT, bool RING>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
     constexpr int GP = NT * 8;
-    constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2);
+    constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2 + 2 * kD * 2);
     const size_t smem = 1024 + static_cast<size_t>(kWarps) * kWarpBytes + kWarps * kStages * (8 + 16) +
-                        (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * sizeof(int);
+                        (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * sizeof(int) +
+                        static_cast<size_t>(prm.Hq) * sizeof(float);
+    const size_t smem_max = smem + static_cast<size_t>(kMaxQHeads - prm.Hq) * sizeof(float);
     auto kern = decode_attn_kernel<NT, RING>;
     const int idx = (NT - 1) * 2 + (RING ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
         if (e != cudaSuccess) return set_cuda_error(e);
         g_dev[dev].attr_set[idx] = true;
     }
