@@ -47,10 +47,15 @@ constexpr int kD = 64;             // head dim
 constexpr int kPage = 16;          // tokens per page = per tile
 constexpr int kWarps = 8;          // workers per CTA
 constexpr int kThreads = kWarps * 32;
-#ifndef DA_STAGES
-#define DA_STAGES 4
+// tiles in flight per warp: the deepest pipeline the 227 KiB of shared memory allows
+#ifndef DA_STAGES_G8
+#define DA_STAGES_G8 5
 #endif
-constexpr int kStages = DA_STAGES; // tiles in flight per warp
+#ifndef DA_STAGES_G16
+#define DA_STAGES_G16 4
+#endif
+template <int NT>
+__host__ __device__ constexpr int stages_for() { return NT == 1 ? DA_STAGES_G8 : DA_STAGES_G16; }
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
 #endif
@@ -60,7 +65,8 @@ constexpr int kMaxBatch = 1024;
 constexpr int kMaxSegments = 65536;         // B * Hkv
 constexpr int kMaxQHeads = 1024;
 constexpr int kCounterBytes = kMaxSegments * 4;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per tile wait
+constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s of SM clock per tile wait
+constexpr int kMaxSmem = 232448;                       // opt-in shared memory per block
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ unsigned int g_status;  // DA_STATUS_* bits, read and cleared by the host
@@ -107,19 +113,13 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs.
+// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
+    const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
     }
 }
 
@@ -320,11 +320,11 @@ template <int NT, bool RING>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
+    constexpr int kStages = stages_for<NT>();
     constexpr int GP = NT * 8;
     constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2;  // the group's q rows, then k_new, v_new
-    constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
-    constexpr int kWarpBytes = kStages * kStageBytes;
-    static_assert(kWarpBytes % 1024 == 0, "tile buffers must stay 1024-byte aligned");
+    constexpr int kWarpBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
+    static_assert(kTileBytes % 1024 == 0, "tile buffers must stay 1024-byte aligned");
     static_assert(2 * sizeof(Slot<NT>) <= kWarpBytes, "merge slots must fit a drained warp area");
     constexpr int kSlotFloats = 2 * GP + GP * kD;  // global partial: m, l, acc
 
@@ -332,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * kWarpBytes);
+    uint8_t *qarea = smem + kWarps * kWarpBytes;  // [kWarps][kStages] q / k_new / v_new slots
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qarea + kWarps * kStages * kQBytes);
     int4 *meta = reinterpret_cast<int4 *>(bars + kWarps * kStages);
     int *s_pre = reinterpret_cast<int *>(meta + kWarps * kStages);  // [B + 1]
     int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
@@ -416,7 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t wbase_s = smem_addr(wbase);
     auto k_tile = [&](int st) { return wbase_s + st * kTileBytes; };
     auto v_tile = [&](int st) { return wbase_s + (kStages + st) * kTileBytes; };
-    auto q_tile = [&](int st) { return wbase_s + 2 * kStages * kTileBytes + st * kQBytes; };
+    uint8_t *wq = qarea + warp * kStages * kQBytes;
+    const uint32_t wq_s = smem_addr(wq);
+    auto q_tile = [&](int st) { return wq_s + st * kQBytes; };
     const uint32_t bar0 = smem_addr(bars + warp * kStages);
     int4 *wmeta = meta + warp * kStages;
 
@@ -552,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     app_row = (L - 1) % kPage;
                 }
                 // Q fragments (B operand): q[head = lane/4][d = 16ks + 2(lane%4) (+8)]
-                const uint8_t *qs = wbase + 2 * kStages * kTileBytes + stg * kQBytes;
+                const uint8_t *qs = wq + stg * kQBytes;
                 if (do_append) {  // the new token's k/v rows arrived with this tile
                     knew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2)[lane];
                     vnew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2 + kD * 2)[lane];
@@ -1027,12 +1030,17 @@ int check_shape(const da_shape &s) {
 
 template <int NT, bool RING>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
+    constexpr int kStages = stages_for<NT>();
     constexpr int GP = NT * 8;
-    constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2 + 2 * kD * 2);
+    constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2 + 2 * kD * 2);  // tiles + q slots
     const size_t smem = 1024 + static_cast<size_t>(kWarps) * kWarpBytes + kWarps * kStages * (8 + 16) +
                         (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * sizeof(int) +
                         static_cast<size_t>(prm.Hq) * sizeof(float);
     const size_t smem_max = smem + static_cast<size_t>(kMaxQHeads - prm.Hq) * sizeof(float);
+    static_assert(1024 + kWarps * kWarpBytes + kWarps * kStages * 24 +
+                          (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * 4 + kMaxQHeads * 4 <=
+                      kMaxSmem,
+                  "shared memory budget");
     auto kern = decode_attn_kernel<NT, RING>;
     const int idx = (NT - 1) * 2 + (RING ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
