@@ -342,10 +342,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *s_flag = s_winfo + kWarps * 8;                               // [4]
     float *s_sink = reinterpret_cast<float *>(s_flag + 4);            // [Hq], log2 units
 
-    if (tid == 0) {  // descriptor fetch overlaps the length loads below
+    // Set-up that reads no input: it overlaps the previous kernel in the stream when this
+    // grid is launched as a programmatic dependent.
+    if (tid == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
+    const uint32_t bar0 = smem_addr(bars + warp * kStages);
+    if (lane == 0) {
+        for (int st = 0; st < kStages; ++st) mbar_init(bar0 + 8 * st, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < 2) s_flag[tid] = -1;
+    // Inputs may come from the previous kernel: wait for it before the first read.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int B = p.B, Hkv = p.Hkv;
 
@@ -420,7 +430,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *wq = qarea + warp * kStages * kQBytes;
     const uint32_t wq_s = smem_addr(wq);
     auto q_tile = [&](int st) { return wq_s + st * kQBytes; };
-    const uint32_t bar0 = smem_addr(bars + warp * kStages);
     int4 *wmeta = meta + warp * kStages;
 
     // per-lane ldmatrix offsets inside a swizzled 16 x 128 B tile
@@ -438,10 +447,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
 
     if (active) {
-        if (lane == 0) {
-            for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
         __syncwarp();
         const uint64_t policy = evict_first_policy();
 
@@ -708,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wi[0] = ua; wi[1] = ue; wi[2] = head_seg; wi[3] = tail_seg; wi[4] = active ? 1 : 0;
     }
     __syncthreads();
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 4. merge segments shared between warps of this CTA
     const long long cta_w0 = static_cast<long long>(blockIdx.x) * kWarps;
@@ -795,37 +801,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ga[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
                 }
             }
-            if (!internal) __threadfence();  // partial visible before this CTA takes a ticket
-        }
-    }
-    __syncthreads();
-
-    // ---- 5. segments shared with other CTAs: ticket, and the last CTA combines
-    if (tid == 0) {
-        s_flag[0] = s_flag[1] = -1;
-        int cand[2] = {cta_first_seg, -1};
-        {
-            const int b = find_seq(s_pre, B, R1 - 1);
-            const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
-            const int last = b * Hkv + (R1 - 1 - s_pre[b]) / tiles;
-            if (last != cta_first_seg) cand[1] = last;
-        }
-        for (int k = 0; k < 2; ++k) {
-            const int seg = cand[k];
-            if (seg < 0) continue;
-            int s0, s1;
-            seg_range(seg, s0, s1);
-            if (s0 >= R0 && s1 <= R1) continue;  // finished inside this CTA
-            const int c_lo = worker_of(s0, U, nwork) / kWarps;
-            const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
-            const int ticket = atomicAdd(p.counters + seg, 1);
-            if (ticket == c_hi - c_lo) {
+            if (!internal) {
+                // publish this CTA's partial, then take a ticket; the last CTA combines
                 __threadfence();
-                s_flag[k] = seg;
+                __syncwarp();
+                if (lane == 0) {
+                    const int c_lo = worker_of(s0, U, nwork) / kWarps;
+                    const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+                    if (atomicAdd(p.counters + seg, 1) == c_hi - c_lo) {
+                        __threadfence();
+                        s_flag[seg == cta_first_seg ? 0 : 1] = seg;
+                    }
+                }
             }
         }
     }
     __syncthreads();
+
+    // ---- 5. segments shared with other CTAs: the last CTA to arrive combines them
 #pragma unroll 1
     for (int k = 0; k < 2; ++k) {
         const int seg = s_flag[k];
@@ -945,7 +938,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D map over a bf16 cache viewed as [slices][rows][64]; box = 16 rows x 64.
-bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
+bool encode_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), rows, slices};
@@ -955,6 +948,37 @@ bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encoding a map costs host time on every call; the map depends only on the
+// address and the extents, so recent ones are kept.
+struct MapCacheEntry {
+    void *base = nullptr;
+    uint64_t rows = 0, slices = 0;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 32;
+MapCacheEntry g_maps[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
+bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < kMapCache; ++i) {
+        const MapCacheEntry &e = g_maps[i];
+        if (e.base == base && e.rows == rows && e.slices == slices) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!encode_kv_map(map, base, rows, slices)) return false;
+    MapCacheEntry &e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.base = base;
+    e.rows = rows;
+    e.slices = slices;
+    e.map = *map;
+    return true;
 }
 
 constexpr int kMaxDevices = 64;
@@ -1049,8 +1073,21 @@ int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm,
         if (e != cudaSuccess) return set_cuda_error(e);
         g_dev[dev].attr_set[idx] = true;
     }
-    kern<<<sm_count(dev), kThreads, smem, stream>>>(mk, mv, prm);
-    cudaError_t e = cudaGetLastError();
+    // Programmatic dependent launch: the grid may start (and run its input-free set-up)
+    // while the previous kernel of the stream drains; it waits for that kernel before
+    // touching memory (griddepcontrol.wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sm_count(dev));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mk, mv, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e);
     return DA_OK;
 }
