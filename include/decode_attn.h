@@ -61,6 +61,7 @@ extern "C" {
 #define DA_ERR_UNSUPPORTED (-2) /* a shape outside the supported set above */
 #define DA_ERR_WORKSPACE (-3)   /* workspace too small while the stream is capturing */
 #define DA_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed */
+#define DA_ERR_SCRATCH_LIMIT (-5) /* decode_attn_paged_noalloc: shape beyond its fixed scratch */
 
 /* Bits of the device status word (decode_attn_device_status). */
 #define DA_STATUS_BAD_SEQ_LEN 1u /* seq_lens[b] < 0, or beyond max_seq_len / the block table row;
@@ -126,6 +127,32 @@ DA_API int kv_append(const void *k_new, const void *v_new, void *k_cache, void *
               const int32_t *block_table, const int32_t *seq_lens,
               int window, da_shape s, int page_size, int max_pages_per_seq,
               int num_pages, void *stream);
+
+/*
+ * decode_attn_paged_noalloc -- decode_attn_paged for callers that cannot allocate
+ * device memory when they call it (a serving runtime that owns every byte of the GPU
+ * through its own pool, a plugin host that forbids cudaMalloc, or code that must not
+ * risk the device-wide synchronisation cudaMalloc/cudaFree can cause). Same arguments,
+ * layouts and results as decode_attn_paged. The pages describe nothing like it: it is
+ * an interface choice of this library, not part of the method.
+ *
+ * Instead of the library workspace it uses one fixed array compiled into the library
+ * (1.3 MiB of device memory on every GPU that loads the library, held until the
+ * process exits). It never calls cudaMalloc, cudaFree or any allocating routine.
+ *   - Limits: batch * num_kv_heads <= 4096 and a GPU with at most 160 SMs; beyond
+ *     that it returns DA_ERR_SCRATCH_LIMIT and launches nothing.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array (it clears the arrival counters it
+ *     needs at the start of each call), so calls that overlap on the GPU, e.g. on two
+ *     streams at once, race and give wrong results. Serialise them.
+ */
+DA_API int decode_attn_paged_noalloc(const void *q, const void *k_new, const void *v_new,
+                                     void *k_cache, void *v_cache,
+                                     const int32_t *block_table, const int32_t *seq_lens,
+                                     const float *sinks, int window, float scale, void *out,
+                                     da_shape s, int page_size, int max_pages_per_seq,
+                                     int num_pages, int max_seq_len, void *stream);
 
 /* Workspace the attention calls need on the current device for this shape. */
 DA_API size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len);

@@ -1170,6 +1170,104 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     return ring ? launch_attn<2, true>(mk, mv, prm, dev, stream) : launch_attn<2, false>(mk, mv, prm, dev, stream);
 }
 
+// ------------------------------------------------------------------ allocation-free variant
+// Some callers cannot allocate device memory at the point where they run decode
+// attention: a runtime whose memory is handed out up front by its own pool, a plugin
+// that is not allowed to call cudaMalloc, or code that must not synchronise the device
+// (cudaMalloc/cudaFree may). For them, decode_attn_paged_noalloc keeps its scratch (the
+// split partials and the arrival counters) in the fixed array below instead of the
+// library workspace. The array is part of the module image: every GPU that loads this
+// library holds its 1.3 MiB until the process exits.
+constexpr int kNoAllocMaxCtas = 160;        // one CTA per SM; GB300 has 152 SMs
+constexpr int kNoAllocMaxSegments = 4096;   // batch * KV heads
+constexpr size_t kNoAllocCounterBytes = static_cast<size_t>(kNoAllocMaxSegments) * sizeof(int);
+constexpr size_t kNoAllocPartialFloats = 2 * 16 + 16 * kD;  // one partial slot at 16 heads per group
+constexpr size_t kNoAllocScratchBytes =
+    kNoAllocCounterBytes + static_cast<size_t>(kNoAllocMaxCtas) * 2 * kNoAllocPartialFloats * sizeof(float);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void *g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+std::mutex g_noalloc_mu;
+
+// The array's name means nothing to host code; its device address is looked up once
+// per device, with that device current.
+int noalloc_scratch(int dev, void **addr) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        g_noalloc_addr[dev] = ptr;
+    }
+    *addr = g_noalloc_addr[dev];
+    return DA_OK;
+}
+
+int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                      const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
+                      float scale, void *out, const da_shape &s, int page_size, int max_pages, int num_pages,
+                      int max_seq_len, void *stream_v) {
+    int rc = check_shape(s);
+    if (rc != DA_OK) return rc;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out || !block_table) return DA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return DA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return DA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return DA_ERR_INVALID_ARG;
+    if (window < 0 || max_pages <= 0 || num_pages <= 0 || max_seq_len < 0) return DA_ERR_INVALID_ARG;
+    if (page_size != kPage) return DA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_pages) * kPage < max_seq_len) return DA_ERR_INVALID_ARG;
+    if (static_cast<long long>(num_pages) * s.num_kv_heads > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(s.batch) * s.num_kv_heads > kNoAllocMaxSegments) return DA_ERR_SCRATCH_LIMIT;
+    if (s.batch == 0) return DA_OK;
+    int dev;
+    rc = current_device(&dev);
+    if (rc != DA_OK) return rc;
+    if (sm_count(dev) > kNoAllocMaxCtas) return DA_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    rc = noalloc_scratch(dev, &scratch);
+    if (rc != DA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+    Params prm;
+    prm.q = static_cast<const __nv_bfloat16 *>(q);
+    prm.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    prm.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+    prm.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
+    prm.block_table = block_table;
+    prm.seq_lens = seq_lens;
+    prm.sinks = sinks;
+    prm.out = static_cast<__nv_bfloat16 *>(out);
+    prm.B = s.batch;
+    prm.Hq = s.num_q_heads;
+    prm.Hkv = s.num_kv_heads;
+    prm.G = s.num_q_heads / s.num_kv_heads;
+    prm.window = window;
+    prm.max_pages = max_pages;
+    prm.num_pages = num_pages;
+    prm.max_seq_len = max_seq_len;
+    prm.scale_log2 = scale * kLog2e;
+    prm.counters = static_cast<int *>(scratch);
+    prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
+    // The array keeps whatever the previous call left: the arrival counters this call
+    // uses must start at zero. (The partials need no clearing; each is written before
+    // it is read.)
+    cudaError_t e = cudaMemsetAsync(prm.counters, 0, static_cast<size_t>(s.batch) * s.num_kv_heads * sizeof(int),
+                                    stream);
+    if (e != cudaSuccess) return set_cuda_error(e);
+
+    CUtensorMap mk, mv;
+    const uint64_t slices = static_cast<uint64_t>(num_pages) * s.num_kv_heads;
+    if (!make_kv_map(&mk, k_cache, kPage, slices) || !make_kv_map(&mv, v_cache, kPage, slices)) {
+        snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
+        return DA_ERR_CUDA;
+    }
+    return prm.G <= 8 ? launch_attn<1, false>(mk, mv, prm, dev, stream) : launch_attn<2, false>(mk, mv, prm, dev, stream);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI
@@ -1212,6 +1310,14 @@ int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache
     return e == cudaSuccess ? DA_OK : set_cuda_error(e);
 }
 
+int decode_attn_paged_noalloc(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                              const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
+                              float scale, void *out, da_shape s, int page_size, int max_pages_per_seq,
+                              int num_pages, int max_seq_len, void *stream) {
+    return run_paged_noalloc(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window, scale, out,
+                             s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream);
+}
+
 size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len) {
     (void)max_seq_len;
     if (check_shape(s) != DA_OK) return 0;
@@ -1246,6 +1352,8 @@ const char *decode_attn_error_string(int code) {
         case DA_ERR_UNSUPPORTED: return "unsupported shape (needs head_dim 64, page 16, G in {1,2,4,8,16}, batch <= 1024, ring window >= 16)";
         case DA_ERR_WORKSPACE: return "workspace too small during stream capture: call decode_attn_reserve() first";
         case DA_ERR_CUDA: return t_err[0] ? t_err : "CUDA error";
+        case DA_ERR_SCRATCH_LIMIT:
+            return "beyond the fixed scratch of the allocation-free call (batch * kv_heads <= 4096, at most 160 SMs)";
         default: return "unknown error code";
     }
 }
