@@ -34,6 +34,7 @@ UNIT = "GB/s"
 KERNEL_SRC = os.path.join(ROOT, "paged_decode_attention_kv_gb300", "csrc", "decode_attn.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 FALLBACK_HBM_GBS = 6800.0
+HBM_BUS_BITS = 8192  # 8 HBM3e stacks x 1024 bits
 
 
 # ---------------------------------------------------------------- bytes the method must move
@@ -65,6 +66,25 @@ def measured_hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def nominal_hbm_peak():
+    """Memory clock x 2 (double data rate) x bus width, for context next to the measured peak."""
+    mhz = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("mem_max_mhz") or 0) or None
+    except Exception:
+        pass
+    if mhz is None:
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.memory",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=10).stdout.split()
+            mhz = float(out[0])
+        except Exception:
+            return None
+    return mhz * 1e6 * 2 * HBM_BUS_BITS / 8 / 1e9
 
 
 def source_hash():
@@ -342,6 +362,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = run_e2e(args, first, pbytes + rbytes, dev)
 
     peak, peak_kind = measured_hbm_peak()
+    nominal = nominal_hbm_peak()
     achieved = pbytes / (paged_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload, "paged")
     result = {
@@ -359,7 +380,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": traffic, "kernel": "decode_attn_kernel (paged, full attention)"},
+                     "traffic": traffic, "kernel": "decode_attn_kernel (paged, full attention)",
+                     "nominal_peak": round(nominal, 1) if nominal else None,
+                     "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
