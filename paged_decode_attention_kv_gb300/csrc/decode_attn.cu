@@ -64,6 +64,7 @@ constexpr int kTileBytes = kPage * kD * 2;  // 2048 B of K (or V) per tile
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxSegments = 65536;         // B * Hkv
 constexpr int kMaxQHeads = 1024;
+constexpr int kWinfo = 12;     // ints of per-warp bookkeeping in shared memory
 constexpr int kCounterBytes = kMaxSegments * 4;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s of SM clock per tile wait
 constexpr int kMaxSmem = 232448;                       // opt-in shared memory per block
@@ -149,7 +150,7 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+    asm("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr)
                  : "memory");
@@ -157,7 +158,7 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r
 
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                           uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+    asm("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr)
                  : "memory");
@@ -165,8 +166,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -174,7 +174,7 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
 }
 
@@ -338,9 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *s_pre = reinterpret_cast<int *>(meta + kWarps * kStages);  // [B + 1]
     int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
     int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
-    int *s_winfo = s_wsum + kWarps;                                   // [kWarps][8]
-    int *s_flag = s_winfo + kWarps * 8;                               // [4]
-    float *s_sink = reinterpret_cast<float *>(s_flag + 4);            // [Hq], log2 units
+    int *s_winfo = s_wsum + kWarps;                                   // [kWarps][kWinfo]
+    int *s_flag = s_winfo + kWarps * kWinfo;                          // [8]
+    float *s_sink = reinterpret_cast<float *>(s_flag + 8);            // [Hq], log2 units
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
     // grid is launched as a programmatic dependent.
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int st = 0; st < kStages; ++st) mbar_init(bar0 + 8 * st, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < 2) s_flag[tid] = -1;
+    if (tid < 4) s_flag[tid] = -1;  // [0,1] segments this CTA combines; [2,3] its boundary segments
     // Inputs may come from the previous kernel: wait for it before the first read.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sig[NT][2];      // sink logits (log2 units) of this lane's heads
     uint32_t qf[NT][4][2]; // Q as mma B operand
     int head_seg = -1, tail_seg = -1;
+    int head_s0 = 0, head_s1 = 0, tail_s0 = 0, tail_s1 = 0;  // unit ranges of those segments
     bool failed = false;
 
     if (active) {
@@ -538,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (seg_first_unit < ua) {  // shared with earlier workers: keep for merge
                         head = st;
                         head_seg = sb * Hkv + sgk;
+                        head_s0 = seg_first_unit;
+                        head_s1 = seg_end_unit;
                     } else {
                         state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD,
                                         p.G, lane);
@@ -620,18 +623,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok_lo = r0 >= lo_v && r0 < hi_v;
             const bool ok_hi = (r0 + 8) >= lo_v && (r0 + 8) < hi_v;
 
-            // S^T = K Q^T  (16 tokens x 8 heads per n-tile)
-            uint32_t ka[4][4];
+            // K fragments, and the V fragments too: they do not depend on the softmax, so
+            // their shared-memory latency overlaps the QK products
+            uint32_t ka[4][4], va[4][4];
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3]);
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+                ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+            // S^T = K Q^T  (16 tokens x 8 heads per n-tile), as two independent MMA chains
             uint32_t pb[NT][2];
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[n][0][0], qf[n][0][1]);
+                mma_bf16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[n][1][0], qf[n][1][1]);
+                mma_bf16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[n][2][0], qf[n][2][1]);
+                mma_bf16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[n][3][0], qf[n][3][1]);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(sc, ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3], qf[n][ks][0], qf[n][ks][1]);
+                for (int k = 0; k < 4; ++k) sc[k] += sd[k];
                 float s0 = ok_lo ? sc[0] * p.scale_log2 : -INFINITY;
                 float s1 = ok_lo ? sc[1] * p.scale_log2 : -INFINITY;
                 float s2 = ok_hi ? sc[2] * p.scale_log2 : -INFINITY;
@@ -673,9 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), a0, a1, a2, a3);
-                a0 &= vm0; a1 &= vm0; a2 &= vm1; a3 &= vm1;
+                const uint32_t a0 = va[mt][0] & vm0, a1 = va[mt][1] & vm0;
+                const uint32_t a2 = va[mt][2] & vm1, a3 = va[mt][3] & vm1;
 #pragma unroll
                 for (int n = 0; n < NT; ++n) mma_bf16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
             }
@@ -700,6 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool last_shared = failed || seg_first_unit < ua || seg_end_unit > ue;
         if (last_shared) {
             tail_seg = sb * Hkv + sgk;
+            tail_s0 = seg_first_unit;
+            tail_s1 = seg_end_unit;
         } else {
             state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD, p.G, lane);
         }
@@ -709,52 +721,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tail_seg >= 0) state_to_slot(st, &slots[1], lane);
     }
     if (lane == 0) {
-        int *wi = s_winfo + warp * 8;
+        int *wi = s_winfo + warp * kWinfo;
         wi[0] = ua; wi[1] = ue; wi[2] = head_seg; wi[3] = tail_seg; wi[4] = active ? 1 : 0;
+        wi[5] = head_s0; wi[6] = head_s1; wi[7] = tail_s0; wi[8] = tail_s1;
     }
     __syncthreads();
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // ---- 4. merge segments shared between warps of this CTA
+    // ---- 4. merge segments shared between warps of this CTA (all threads take part)
     const long long cta_w0 = static_cast<long long>(blockIdx.x) * kWarps;
     const long long cta_w1 = min(cta_w0 + kWarps, nwork);
     const int R0 = wstart(cta_w0, U, nwork), R1 = wstart(cta_w1, U, nwork);
     const int nw_cta = static_cast<int>(cta_w1 - cta_w0);
-    auto seg_range = [&](int seg, int &s0, int &s1) {
-        const int b = seg / Hkv, g = seg - b * Hkv;
-        const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
-        s0 = s_pre[b] + g * tiles;
-        s1 = s0 + tiles;
-    };
-    // the CTA's first segment (global partial slot 0); any other boundary segment uses slot 1
-    int cta_first_seg;
-    {
-        const int b = find_seq(s_pre, B, R0);
-        const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
-        cta_first_seg = b * Hkv + (R0 - s_pre[b]) / tiles;
-    }
+    // Segments shared by several warps: the first warp of this CTA touching one merges it
+    // (warps merge their segments concurrently). A segment that also crosses into another
+    // CTA becomes this CTA's fp32 partial; slot 0 if it holds the CTA's first unit, else 1.
+    bool wrote_partial = false;
     if (warp < nw_cta) {
-        const int *wi = s_winfo + warp * 8;
-        const int my_a = wi[0];
+        const int *wi = s_winfo + warp * kWinfo;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
             const int seg = wi[2 + which];
-            if (seg < 0) continue;
-            int s0, s1;
-            seg_range(seg, s0, s1);
-            if (!(warp == 0 || s0 >= my_a)) continue;  // an earlier warp of this CTA leads
-            // contributors: this warp and the following warps that start inside the segment
+            const int s0 = wi[5 + 2 * which], s1 = wi[6 + 2 * which];
+            if (seg < 0 || !(warp == 0 || s0 >= wi[0])) continue;
             int w_end = warp;
-            while (w_end + 1 < nw_cta && s_winfo[(w_end + 1) * 8] < s1) ++w_end;
+            while (w_end + 1 < nw_cta && s_winfo[(w_end + 1) * kWinfo] < s1) ++w_end;
             const bool internal = s0 >= R0 && s1 <= R1;
+            const int slot_k = s0 <= R0 ? 0 : 1;
             const int b = seg / Hkv, g = seg - b * Hkv;
-            // lane -> (head n, 16 d values)
+            if (!internal && lane == 0) {
+                s_flag[2 + slot_k] = seg;
+                s_flag[4 + 2 * slot_k] = s0;
+                s_flag[5 + 2 * slot_k] = s1;
+            }
+            // lane -> (head n, 16 d values); the contributor loops issue independent loads
             for (int item = lane; item < GP * 4; item += 32) {
                 const int n = item >> 2, d0 = (item & 3) * 16;
                 float M = -INFINITY;
                 for (int w = warp; w <= w_end; ++w) {
                     const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
-                                         ((s_winfo[w * 8 + 3] == seg) ? 1 : 0);
+                                         ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
                     M = fmaxf(M, sl->m[n]);
                 }
                 const float sg = (internal && n < p.G) ? s_sink[g * p.G + n] : -INFINITY;
@@ -762,14 +768,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float den = internal ? fast_exp2(sg - Mf) : 0.f;
                 float acc[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+                for (int j = 0; j < 16; ++j) acc[j] = 0.f;
                 for (int w = warp; w <= w_end; ++w) {
                     const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
-                                         ((s_winfo[w * 8 + 3] == seg) ? 1 : 0);
+                                         ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
                     const float wgt = fast_exp2(sl->m[n] - Mf);
                     den += sl->l[n] * wgt;
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) acc[k] += sl->acc[n][d0 + k] * wgt;
+                    for (int j = 0; j < 16; ++j) acc[j] += sl->acc[n][d0 + j] * wgt;
                 }
                 if (internal) {
                     if (n < p.G) {
@@ -789,81 +795,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[1] = o1;
                     }
                 } else {
-                    float *gp = p.part + (static_cast<size_t>(blockIdx.x) * 2 + (seg == cta_first_seg ? 0 : 1)) *
-                                             kSlotFloats;
+                    float *gp = p.part + (static_cast<size_t>(blockIdx.x) * 2 + slot_k) * kSlotFloats;
                     if (d0 == 0) {
                         gp[n] = M;
                         gp[GP + n] = den;
                     }
                     float4 *ga = reinterpret_cast<float4 *>(gp + 2 * GP + n * kD + d0);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        ga[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-                }
-            }
-            if (!internal) {
-                // publish this CTA's partial, then take a ticket; the last CTA combines
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) {
-                    const int c_lo = worker_of(s0, U, nwork) / kWarps;
-                    const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
-                    if (atomicAdd(p.counters + seg, 1) == c_hi - c_lo) {
-                        __threadfence();
-                        s_flag[seg == cta_first_seg ? 0 : 1] = seg;
-                    }
+                    for (int j = 0; j < 4; ++j)
+                        ga[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    wrote_partial = true;
                 }
             }
         }
     }
+    if (wrote_partial) __threadfence();  // partials visible before the tickets below
     __syncthreads();
 
     // ---- 5. segments shared with other CTAs: the last CTA to arrive combines them
+    if (tid == 0) {
+        const int cand0 = s_flag[2], cand1 = s_flag[3];
+        // both tickets in flight together
+        const int t0 = cand0 >= 0 ? atomicAdd(p.counters + cand0, 1) : 0;
+        const int t1 = cand1 >= 0 ? atomicAdd(p.counters + cand1, 1) : 0;
+        auto last_of = [&](int seg, int ticket, int s0, int s1) {
+            if (seg < 0) return -1;
+            const int c_lo = worker_of(s0, U, nwork) / kWarps;
+            const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+            return ticket == c_hi - c_lo ? seg : -1;
+        };
+        s_flag[0] = last_of(cand0, t0, s_flag[4], s_flag[5]);
+        s_flag[1] = last_of(cand1, t1, s_flag[6], s_flag[7]);
+        if (s_flag[0] >= 0 || s_flag[1] >= 0) __threadfence();
+    }
+    __syncthreads();
+    // One pass, no barrier: every thread owns kPer outputs of one head and folds the
+    // partials in batches of 8 contributors whose loads are all in flight together.
+    constexpr int kPer = GP * kD / kThreads;  // outputs per thread: 2 (G <= 8) or 4 (G = 16)
+    const int cn = tid / (kD / kPer), cd0 = (tid % (kD / kPer)) * kPer;
 #pragma unroll 1
     for (int k = 0; k < 2; ++k) {
         const int seg = s_flag[k];
         if (seg < 0) continue;
-        int s0, s1;
-        seg_range(seg, s0, s1);
+        const int s0 = s_flag[4 + 2 * k], s1 = s_flag[5 + 2 * k];
         const int c_lo = worker_of(s0, U, nwork) / kWarps;
         const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
-        // the first contributing CTA may have started before this segment (slot 1)
+        const int nc = c_hi - c_lo + 1;
+        // the first contributing CTA may have started before this segment (its slot 1)
         const int lo_slot = (wstart(static_cast<long long>(c_lo) * kWarps, U, nwork) < s0) ? 1 : 0;
         const int b = seg / Hkv, g = seg - b * Hkv;
-        constexpr int kPer = GP * kD / kThreads;  // 2 (G<=8) or 4 (G=16) outputs per thread
-        const int n = tid / (kD / kPer), d0 = (tid % (kD / kPer)) * kPer;
         float M = -INFINITY, den = 0.f, acc[kPer];
 #pragma unroll
-        for (int k2 = 0; k2 < kPer; ++k2) acc[k2] = 0.f;
-#pragma unroll 4
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const float *gp = p.part + (static_cast<size_t>(c) * 2 + (c == c_lo ? lo_slot : 0)) * kSlotFloats;
-            const float mc = __ldcg(gp + n), lc = __ldcg(gp + GP + n);
-            float v[kPer];
-            if constexpr (kPer == 2) {
-                const float2 t = __ldcg(reinterpret_cast<const float2 *>(gp + 2 * GP + n * kD + d0));
-                v[0] = t.x; v[1] = t.y;
-            } else {
-                const float4 t = __ldcg(reinterpret_cast<const float4 *>(gp + 2 * GP + n * kD + d0));
-                v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-            }
-            const float Mn = fmaxf(M, mc);
-            const float a = fast_exp2(M - Mn), w = fast_exp2(mc - Mn);
-            den = den * a + lc * w;
+        for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < nc; c0 += 8) {
+            float mc[8], lc[8], v[8][kPer];
 #pragma unroll
-            for (int k2 = 0; k2 < kPer; ++k2) acc[k2] = acc[k2] * a + v[k2] * w;
+            for (int j = 0; j < 8; ++j) {
+                mc[j] = -INFINITY;
+                lc[j] = 0.f;
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) v[j][t] = 0.f;
+                if (c0 + j < nc) {
+                    const int c = c0 + j;
+                    const float *gp =
+                        p.part + (static_cast<size_t>(c_lo + c) * 2 + (c == 0 ? lo_slot : 0)) * kSlotFloats;
+                    mc[j] = __ldcg(gp + cn);
+                    lc[j] = __ldcg(gp + GP + cn);
+                    if constexpr (kPer == 2) {
+                        const float2 t2 = __ldcg(reinterpret_cast<const float2 *>(gp + 2 * GP + cn * kD + cd0));
+                        v[j][0] = t2.x; v[j][1] = t2.y;
+                    } else {
+                        const float4 t4 = __ldcg(reinterpret_cast<const float4 *>(gp + 2 * GP + cn * kD + cd0));
+                        v[j][0] = t4.x; v[j][1] = t4.y; v[j][2] = t4.z; v[j][3] = t4.w;
+                    }
+                }
+            }
+            float Mn = M;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mc[j]);
+            const float a = fast_exp2(M - Mn);  // 0 on the first batch (M = -inf)
+            den *= a;
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) acc[t] *= a;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = fast_exp2(mc[j] - Mn);  // 0 for the padding entries
+                den += lc[j] * w;
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) acc[t] += v[j][t] * w;
+            }
             M = Mn;
         }
-        const float sg = n < p.G ? s_sink[g * p.G + n] : -INFINITY;
+        const float sg = cn < p.G ? s_sink[g * p.G + cn] : -INFINITY;
         const float Mf = fmaxf(M, sg);
         const float a = fast_exp2(M - Mf);
         den = den * a + fast_exp2(sg - Mf);
         const float f = a / den;
-        if (n < p.G) {
-            __nv_bfloat16 *dst = p.out + (static_cast<size_t>(b) * p.Hq + g * p.G + n) * kD + d0;
+        if (cn < p.G) {
+            __nv_bfloat16 *dst = p.out + (static_cast<size_t>(b) * p.Hq + g * p.G + cn) * kD + cd0;
 #pragma unroll
-            for (int k2 = 0; k2 < kPer; k2 += 2)
-                *reinterpret_cast<uint32_t *>(dst + k2) = pack_bf16(acc[k2] * f, acc[k2 + 1] * f);
+            for (int t = 0; t < kPer; t += 2)
+                *reinterpret_cast<uint32_t *>(dst + t) = pack_bf16(acc[t] * f, acc[t + 1] * f);
         }
         if (tid == 0) p.counters[seg] = 0;  // ready for the next call
     }
@@ -1058,11 +1091,12 @@ int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm,
     constexpr int GP = NT * 8;
     constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2 + 2 * kD * 2);  // tiles + q slots
     const size_t smem = 1024 + static_cast<size_t>(kWarps) * kWarpBytes + kWarps * kStages * (8 + 16) +
-                        (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * sizeof(int) +
-                        static_cast<size_t>(prm.Hq) * sizeof(float);
-    const size_t smem_max = smem + static_cast<size_t>(kMaxQHeads - prm.Hq) * sizeof(float);
+                        (2 * kMaxBatch + 1 + kWarps + kWarps * kWinfo + 8) * sizeof(int) +
+                        static_cast<size_t>(kMaxQHeads) * sizeof(float) + 2 * kWarps * sizeof(int4) + 16;
+    const size_t smem_max = smem;
     static_assert(1024 + kWarps * kWarpBytes + kWarps * kStages * 24 +
-                          (2 * kMaxBatch + 1 + kWarps + kWarps * 8 + 4) * 4 + kMaxQHeads * 4 <=
+                          (2 * kMaxBatch + 1 + kWarps + kWarps * kWinfo + 8) * 4 + kMaxQHeads * 4 +
+                          2 * kWarps * 16 + 16 <=
                       kMaxSmem,
                   "shared memory budget");
     auto kern = decode_attn_kernel<NT, RING>;
