@@ -57,6 +57,24 @@ def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W):
     return total + 4 * len(lens) + 4 * Hq
 
 
+# ---------------------------------------------------------------- ranks (replicas)
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's value (all ranks get it); x itself on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job throughput: every rank moves the same bytes per step (weak scaling),
+    divided by the slowest rank's time per step."""
+    return world * bytes_per_step_per_rank / (ms_per_step_max * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- environment helpers
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -349,13 +367,9 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     paged_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p0, ev_p1)) / args.steps
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, dev)
     assert da.decode_attn_device_status() == 0
-    value = world * (pbytes + rbytes) / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(pbytes + rbytes, ms_step, world)
     ring_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p1, ev_r1)) / args.steps
 
     # end to end through the public API with host buffers
