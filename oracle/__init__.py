@@ -18,6 +18,10 @@ import numpy as np
 from . import build as _build
 
 _lib = None
+_FUNCS = ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
+          "oracle_kv_append_paged", "oracle_kv_append_ring", "oracle_scatter_paged",
+          "oracle_scatter_ring", "oracle_rope_q64", "oracle_rope_k", "oracle_decode_paged_rope",
+          "oracle_decode_ring_rope")
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -49,9 +53,16 @@ def _load():
             c_int]
         lib.oracle_scatter_ring.argtypes = [
             _u16p, _u16p, _i32p, c_int, c_int, _u16p, _u16p, c_int, c_int, c_int]
-        for name in ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
-                     "oracle_kv_append_paged", "oracle_kv_append_ring",
-                     "oracle_scatter_paged", "oracle_scatter_ring"):
+        lib.oracle_rope_q64.argtypes = [_u16p, _i32p, _f32p, _f32p, c_int, c_int, c_int, c_int,
+                                        _f64p]
+        lib.oracle_rope_k.argtypes = [_u16p, _i32p, _f32p, _f32p, c_int, c_int, c_int, c_int, _u16p]
+        lib.oracle_decode_paged_rope.argtypes = [
+            _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _f32p, _f32p, _f32p, c_int, c_int,
+            c_double, _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_decode_ring_rope.argtypes = [
+            _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _f32p, _f32p, _f32p, c_int, c_int, c_double,
+            _f64p, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        for name in _FUNCS:
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -64,9 +75,7 @@ def load_library(path):
     prev = _lib
     ref = _load()
     lib = ctypes.CDLL(path)
-    for fn in ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
-               "oracle_kv_append_paged", "oracle_kv_append_ring",
-               "oracle_scatter_paged", "oracle_scatter_ring"):
+    for fn in _FUNCS:
         f_new, f_ref = getattr(lib, fn), getattr(ref, fn)
         f_new.argtypes, f_new.restype = f_ref.argtypes, f_ref.restype
     _lib = lib
@@ -245,3 +254,82 @@ def scatter_ring(hist_k, hist_v, n_tokens, window, k_cache, v_cache):
         _ptr(kc, _u16p), _ptr(vc, _u16p), B, Hkv, D)
     _check(st, "scatter_ring")
     return kc, vc
+
+
+# ---------------------------------------------------------------- rotary position embedding
+def _tables(rope_cos, rope_sin, D):
+    c = np.ascontiguousarray(rope_cos, dtype=np.float32)
+    sn = np.ascontiguousarray(rope_sin, dtype=np.float32)
+    assert c.shape == sn.shape and c.ndim == 2 and c.shape[1] == D // 2
+    return c, sn, c.shape[0]
+
+
+def rope_q64(q, seq_lens, rope_cos, rope_sin):
+    """Queries rotated to position L - 1, fp64 [B, Hq, D] (rotate-half pairs (i, i + D/2))."""
+    lib = _load()
+    q = _u16(q, "q")
+    sl = _i32(seq_lens)
+    B, Hq, D = q.shape
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    out = np.zeros((B, Hq, D), np.float64)
+    _check(lib.oracle_rope_q64(_ptr(q, _u16p), _ptr(sl, _i32p), _ptr(c, _f32p), _ptr(sn, _f32p),
+                               maxpos, B, Hq, D, _ptr(out, _f64p)), "rope_q64")
+    return out
+
+
+def rope_k(k_new, seq_lens, rope_cos, rope_sin):
+    """New keys rotated to position L - 1 as stored in a bf16 cache (fp32 arithmetic,
+    round to nearest even), uint16 [B, Hkv, D]."""
+    lib = _load()
+    k = _u16(k_new, "k_new")
+    sl = _i32(seq_lens)
+    B, Hkv, D = k.shape
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    out = np.zeros_like(k)
+    _check(lib.oracle_rope_k(_ptr(k, _u16p), _ptr(sl, _i32p), _ptr(c, _f32p), _ptr(sn, _f32p),
+                             maxpos, B, Hkv, D, _ptr(out, _u16p)), "rope_k")
+    return out
+
+
+def decode_paged_rope(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, rope_cos,
+                      rope_sin, window, scale, page_size, items=None, nthreads=None):
+    """decode_paged with q and k_new rotated to position L - 1 first."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    k_cache, v_cache = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, _ = k_cache.shape
+    assert P == page_size
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_paged_rope(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(k_cache, _u16p),
+        _ptr(v_cache, _u16p), _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(sk, _f32p), _ptr(c, _f32p),
+        _ptr(sn, _f32p), maxpos, int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D, P,
+        bt.shape[1], num_pages, _ptr(it, _i32p), n_items, nthreads or default_threads())
+    _check(st, "decode_paged_rope")
+    return out
+
+
+def decode_ring_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, rope_cos, rope_sin,
+                     window, scale, items=None, nthreads=None):
+    """decode_ring with q and k_new rotated to position L - 1 first."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    k_cache, v_cache = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    sl, sk = _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    _, Hkv, W, _ = k_cache.shape
+    assert W == window
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_ring_rope(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(k_cache, _u16p),
+        _ptr(v_cache, _u16p), _ptr(sl, _i32p), _ptr(sk, _f32p), _ptr(c, _f32p), _ptr(sn, _f32p),
+        maxpos, int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D, _ptr(it, _i32p),
+        n_items, nthreads or default_threads())
+    _check(st, "decode_ring_rope")
+    return out

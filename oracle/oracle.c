@@ -63,6 +63,7 @@ enum layout_kind { LAYOUT_PAGED = 0, LAYOUT_RING = 1, LAYOUT_CONTIG = 2 };
 typedef struct {
     int kind;
     const uint16_t *q;      /* [B][Hq][D] */
+    const double *q64;      /* [B][Hq][D] rotated queries in fp64, used instead of q when set */
     const uint16_t *k_new;  /* [B][Hkv][D] or NULL */
     const uint16_t *v_new;
     const uint16_t *k_src;  /* cache or history, per kind */
@@ -124,6 +125,7 @@ static int attend_one(const problem *pr, int b, int h, double *out) {
     const int n = L - lo;
 
     const uint16_t *qrow = pr->q + ((size_t)b * pr->Hq + h) * D;
+    const double *q64row = pr->q64 ? pr->q64 + ((size_t)b * pr->Hq + h) * D : NULL;
     double *s = (double *)malloc(sizeof(double) * (size_t)n);
     if (!s) return OR_NOMEM;
 
@@ -133,7 +135,10 @@ static int attend_one(const problem *pr, int b, int h, double *out) {
         const uint16_t *krow = token_row(pr, b, g, lo + i, 0);
         if (!krow) { free(s); return OR_BAD_INDEX; }
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+        if (q64row)
+            for (int d = 0; d < D; ++d) dot += q64row[d] * bf16_to_f64(krow[d]);
+        else
+            for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
         s[i] = pr->scale * dot;
         if (s[i] > M) M = s[i];
     }
@@ -174,7 +179,7 @@ static void *worker(void *p) {
 static int run(problem *pr, int nthreads) {
     if (pr->B < 0 || pr->Hq <= 0 || pr->Hkv <= 0 || pr->D <= 0 || pr->Hq % pr->Hkv != 0)
         return OR_BAD_ARG;
-    if (!pr->q || !pr->seq_lens || !pr->out) return OR_BAD_ARG;
+    if ((!pr->q && !pr->q64) || !pr->seq_lens || !pr->out) return OR_BAD_ARG;
     if ((pr->k_new == NULL) != (pr->v_new == NULL)) return OR_BAD_ARG;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
@@ -334,4 +339,161 @@ int oracle_scatter_ring(const uint16_t *hist_k, const uint16_t *hist_v, const in
         }
     }
     return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Rotary position embedding of the new token (SimpleLLM README, changes
+ * table, row "RoPE as one fused kernel at every batch size"). The pages give
+ * no formula; the reading is the rotate-half form used by gpt-oss: for
+ * i < D/2 the pair (x_i, x_{i+D/2}) of a query or key vector at position pos
+ * is rotated by the table angle of (pos, i):
+ *     x_i'       = x_i c - x_{i+D/2} s
+ *     x_{i+D/2}' = x_{i+D/2} c + x_i s,        c = cos[pos][i], s = sin[pos][i]
+ * with the cos/sin tables (fp32, [max_position][D/2]) supplied by the caller,
+ * so any frequency scaling lives in the tables. pos = L - 1 for the new token;
+ * cached keys are stored already rotated; values are not rotated.
+ *
+ * Queries are rotated exactly (fp64). The new key is stored in a bf16 cache, so
+ * its rotation decides bits: it is computed the way the kernel computes it --
+ * each product and the difference/sum rounded to fp32 (no fused multiply-add),
+ * then rounded to bf16 to nearest, ties to even. */
+
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays NaN */
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static void rope_row_f64(const uint16_t *x, const float *c, const float *sn, int D, double *out) {
+    const int h = D / 2;
+    for (int i = 0; i < h; ++i) {
+        const double x1 = bf16_to_f64(x[i]), x2 = bf16_to_f64(x[i + h]);
+        out[i] = x1 * (double)c[i] - x2 * (double)sn[i];
+        out[i + h] = x2 * (double)c[i] + x1 * (double)sn[i];
+    }
+}
+
+static void rope_row_bf16(const uint16_t *x, const float *c, const float *sn, int D, uint16_t *out) {
+    const int h = D / 2;
+    for (int i = 0; i < h; ++i) {
+        const float x1 = bf16_to_f32(x[i]), x2 = bf16_to_f32(x[i + h]);
+        const float a = x1 * c[i], b = x2 * sn[i];
+        const float e = x2 * c[i], f = x1 * sn[i];
+        out[i] = f32_to_bf16_rne(a - b);
+        out[i + h] = f32_to_bf16_rne(e + f);
+    }
+}
+
+/* Rotated queries, fp64, [B][Hq][D]; rows of inactive slots are left zero. */
+int oracle_rope_q64(const uint16_t *q, const int32_t *seq_lens, const float *rope_cos,
+                    const float *rope_sin, int max_position, int B, int Hq, int D, double *out) {
+    if (!q || !seq_lens || !rope_cos || !rope_sin || !out || D % 2 || max_position <= 0)
+        return OR_BAD_ARG;
+    const int h = D / 2;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        for (int hq = 0; hq < Hq; ++hq) {
+            double *o = out + ((size_t)b * Hq + hq) * D;
+            if (L <= 0) { for (int d = 0; d < D; ++d) o[d] = 0.0; continue; }
+            if (L - 1 >= max_position) return OR_BAD_INDEX;
+            const size_t row = (size_t)(L - 1) * h;
+            rope_row_f64(q + ((size_t)b * Hq + hq) * D, rope_cos + row, rope_sin + row, D, o);
+        }
+    }
+    return OR_OK;
+}
+
+/* Rotated new keys as stored in the cache, bf16 bits, [B][Hkv][D]. */
+int oracle_rope_k(const uint16_t *k_new, const int32_t *seq_lens, const float *rope_cos,
+                  const float *rope_sin, int max_position, int B, int Hkv, int D, uint16_t *out) {
+    if (!k_new || !seq_lens || !rope_cos || !rope_sin || !out || D % 2 || max_position <= 0)
+        return OR_BAD_ARG;
+    const int h = D / 2;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        for (int g = 0; g < Hkv; ++g) {
+            const size_t off = ((size_t)b * Hkv + g) * D;
+            if (L <= 0) { memcpy(out + off, k_new + off, sizeof(uint16_t) * (size_t)D); continue; }
+            if (L - 1 >= max_position) return OR_BAD_INDEX;
+            const size_t row = (size_t)(L - 1) * h;
+            rope_row_bf16(k_new + off, rope_cos + row, rope_sin + row, D, out + off);
+        }
+    }
+    return OR_OK;
+}
+
+/* Decode steps with the fused RoPE: rotate q (fp64) and k_new (bf16, as stored), then
+ * append and attend exactly as oracle_decode_paged / oracle_decode_ring. */
+static int rope_inputs(const uint16_t *q, const uint16_t *k_new, const int32_t *seq_lens,
+                       const float *rope_cos, const float *rope_sin, int max_position, int B, int Hq,
+                       int Hkv, int D, double **q64, uint16_t **krot) {
+    *q64 = (double *)malloc(sizeof(double) * (size_t)B * Hq * D + 1);
+    *krot = k_new ? (uint16_t *)malloc(sizeof(uint16_t) * (size_t)B * Hkv * D + 1) : NULL;
+    if (!*q64 || (k_new && !*krot)) return OR_NOMEM;
+    int st = oracle_rope_q64(q, seq_lens, rope_cos, rope_sin, max_position, B, Hq, D, *q64);
+    if (st == OR_OK && k_new)
+        st = oracle_rope_k(k_new, seq_lens, rope_cos, rope_sin, max_position, B, Hkv, D, *krot);
+    return st;
+}
+
+int oracle_decode_paged_rope(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                             const uint16_t *k_cache, const uint16_t *v_cache,
+                             const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                             const float *rope_cos, const float *rope_sin, int max_position,
+                             int window, double scale, double *out,
+                             int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                             const int32_t *items, int n_items, int nthreads) {
+    if (page_size <= 0 || max_pages <= 0 || num_pages <= 0 || window < 0 || !block_table)
+        return OR_BAD_ARG;
+    double *q64 = NULL;
+    uint16_t *krot = NULL;
+    int st = rope_inputs(q, k_new, seq_lens, rope_cos, rope_sin, max_position, B, Hq, Hkv, D, &q64, &krot);
+    if (st == OR_OK) {
+        problem pr;
+        memset(&pr, 0, sizeof pr);
+        pr.kind = LAYOUT_PAGED;
+        pr.q = q; pr.q64 = q64; pr.k_new = krot; pr.v_new = v_new; pr.k_src = k_cache; pr.v_src = v_cache;
+        pr.block_table = block_table; pr.seq_lens = seq_lens; pr.sinks = sinks;
+        pr.window = window; pr.scale = scale; pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.D = D;
+        pr.P = page_size; pr.max_pages = max_pages; pr.num_pages = num_pages;
+        pr.items = items; pr.n_items = n_items; pr.out = out;
+        st = run(&pr, nthreads);
+    }
+    free(q64);
+    free(krot);
+    return st;
+}
+
+int oracle_decode_ring_rope(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                            const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *seq_lens, const float *sinks,
+                            const float *rope_cos, const float *rope_sin, int max_position,
+                            int window, double scale, double *out, int B, int Hq, int Hkv, int D,
+                            const int32_t *items, int n_items, int nthreads) {
+    if (window <= 0) return OR_BAD_ARG;
+    double *q64 = NULL;
+    uint16_t *krot = NULL;
+    int st = rope_inputs(q, k_new, seq_lens, rope_cos, rope_sin, max_position, B, Hq, Hkv, D, &q64, &krot);
+    if (st == OR_OK) {
+        problem pr;
+        memset(&pr, 0, sizeof pr);
+        pr.kind = LAYOUT_RING;
+        pr.q = q; pr.q64 = q64; pr.k_new = krot; pr.v_new = v_new; pr.k_src = k_cache; pr.v_src = v_cache;
+        pr.seq_lens = seq_lens; pr.sinks = sinks; pr.window = window; pr.scale = scale;
+        pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.D = D;
+        pr.items = items; pr.n_items = n_items; pr.out = out;
+        st = run(&pr, nthreads);
+    }
+    free(q64);
+    free(krot);
+    return st;
 }

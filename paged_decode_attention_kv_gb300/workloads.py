@@ -206,3 +206,15 @@ def from_bits(a, device="cpu") -> torch.Tensor:
     """bf16 tensor from a numpy uint16 array of raw patterns."""
     import numpy as np
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def rope_tables(max_position: int, D: int, base: float = 150000.0):
+    """cos/sin tables [max_position, D/2] fp32 of the plain rotary schedule
+    angle(pos, i) = pos * base^(-2i/D), computed in fp64 and rounded once. These
+    are caller inputs (the model's frequency schedule; a scaled schedule such as
+    YaRN would be folded into the same tables)."""
+    import numpy as np
+    pos = np.arange(max_position, dtype=np.float64)[:, None]
+    inv = base ** (-np.arange(0, D, 2, dtype=np.float64) / D)[None, :]
+    ang = pos * inv
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_rope as rope_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -38,6 +39,17 @@ MUTANTS = [
      "const uint16_t *vrow = token_row(pr, b, g, lo + i, 0);"),
     ("q_transposed", "const uint16_t *qrow = pr->q + ((size_t)b * pr->Hq + h) * D;",
      "const uint16_t *qrow = pr->q + ((size_t)h * pr->B + b) * D;"),
+    ("rope_sign", "out[i] = x1 * (double)c[i] - x2 * (double)sn[i];",
+     "out[i] = x1 * (double)c[i] + x2 * (double)sn[i];"),
+    ("rope_mirror_pairs", "const double x1 = bf16_to_f64(x[i]), x2 = bf16_to_f64(x[i + h]);",
+     "const double x1 = bf16_to_f64(x[i]), x2 = bf16_to_f64(x[D - 1 - i]);"),
+    ("rope_q_position", "            const size_t row = (size_t)(L - 1) * h;\n            rope_row_f64",
+     "            const size_t row = (size_t)(L % max_position) * h;\n            rope_row_f64"),
+    ("rope_q_unrotated", "pr.q = q; pr.q64 = q64; pr.k_new = krot; pr.v_new = v_new; pr.k_src = k_cache; "
+     "pr.v_src = v_cache;\n        pr.block_table",
+     "pr.q = q; pr.q64 = NULL; pr.k_new = krot; pr.v_new = v_new; pr.k_src = k_cache; "
+     "pr.v_src = v_cache;\n        pr.block_table"),
+    ("rope_key_truncated", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;"),
     ("append_wrong_cell",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(L % page_size)) * D;"),
@@ -55,6 +67,12 @@ PIN_CALLS = [
     pins.test_gqa_equals_mha_on_repeated_kv,
     pins.test_append_is_bit_exact_and_touches_only_target_cells,
     pins.test_hand_worked_example,
+    rope_pins.test_identity_tables_change_nothing,
+    rope_pins.test_quarter_turn_is_a_signed_half_swap,
+    rope_pins.test_position_zero_is_the_identity,
+    rope_pins.test_rotation_keeps_norms,
+    rope_pins.test_stored_key_rounding_is_fp32_then_bf16_nearest_even,
+    lambda: rope_pins.test_attention_depends_only_on_relative_positions(37),
 ]
 
 
@@ -65,7 +83,7 @@ def _build_mutant(tmp_path, name, old, new):
     c_path = tmp_path / f"{name}.c"
     so_path = tmp_path / f"lib{name}.so"
     c_path.write_text(mutated)
-    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", str(c_path),
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", str(c_path),
                     "-o", str(so_path), "-lm"], check=True)
     return str(so_path)
 
