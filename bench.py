@@ -207,10 +207,44 @@ class StepInputs:
         self.seq_lens, self.sinks = d(self.inp.seq_lens), d(self.inp.sinks)
         self.out_full = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
         self.out_ring = torch.empty_like(self.out_full)
+        cs, sn = wl.rope_tables(max(self.lens) + 1, D)
+        self.rope_cos = torch.from_numpy(cs).to(device)
+        self.rope_sin = torch.from_numpy(sn).to(device)
 
     def nbytes(self):
         ts = [self.pool.k_cache, self.pool.v_cache, self.ring.k_cache, self.ring.v_cache]
         return sum(t.numel() * t.element_size() for t in ts)
+
+
+def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=None):
+    import paged_decode_attention_kv_gb300 as da
+    q = s.q if q is None else q
+    k_new = s.k_new if k_new is None else k_new
+    v_new = s.v_new if v_new is None else v_new
+    bt = s.pool.block_table if bt is None else bt
+    sl = s.seq_lens if sl is None else sl
+    sinks = s.sinks if sinks is None else sinks
+    if rope:
+        da.decode_attn_paged_rope(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks,
+                                  s.rope_cos, s.rope_sin, 0, s.inp.scale, s.out_full)
+    else:
+        da.decode_attn_paged(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks, 0,
+                             s.inp.scale, s.out_full)
+
+
+def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
+    import paged_decode_attention_kv_gb300 as da
+    q = s.q if q is None else q
+    k_new = s.k_new if k_new is None else k_new
+    v_new = s.v_new if v_new is None else v_new
+    sl = s.seq_lens if sl is None else sl
+    sinks = s.sinks if sinks is None else sinks
+    if rope:
+        da.decode_attn_ring_rope(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
+                                 s.rope_cos, s.rope_sin, s.inp.scale, s.out_ring)
+    else:
+        da.decode_attn_ring(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
+                            s.inp.scale, s.out_ring)
 
 
 def step_bytes(name, lens):
@@ -243,10 +277,17 @@ def oracle_sample(name, s: "StepInputs", budget_s):
         for b in order:
             items = [(b, h) for h in range(Hq)]
             t0 = time.perf_counter()
-            oracle.decode_paged(q, kn, vn, kp, vp, bt, lens, sinks, 0, s.inp.scale, P,
-                                items=items, nthreads=cores)
-            oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
-                               nthreads=cores)
+            if getattr(s, "rope", False):
+                cs, sn = s.rope_cos.cpu().numpy(), s.rope_sin.cpu().numpy()
+                oracle.decode_paged_rope(q, kn, vn, kp, vp, bt, lens, sinks, cs, sn, 0,
+                                         s.inp.scale, P, items=items, nthreads=cores)
+                oracle.decode_ring_rope(q, kn, vn, rk, rv, lens, sinks, cs, sn, W, s.inp.scale,
+                                        items=items, nthreads=cores)
+            else:
+                oracle.decode_paged(q, kn, vn, kp, vp, bt, lens, sinks, 0, s.inp.scale, P,
+                                    items=items, nthreads=cores)
+                oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
+                                   nthreads=cores)
             elapsed += time.perf_counter() - t0
             pb, rb = step_bytes(name, [int(lens[b])])
             done_bytes += pb + rb
@@ -267,6 +308,7 @@ def run_reference(args, rank, world):
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
     s = StepInputs(args.workload, device, batch_limit=args.batch_limit)
+    s.rope = args.rope
     # each step is a bounded sample: calibrate so that warmup+steps fit ~90 s
     per_step = max(0.02, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -299,6 +341,7 @@ def workload_config(name, s):
             "window": c["window"], "mean_len": round(sum(lens) / max(1, len(lens)), 1),
             "max_len": max(lens) if lens else 0,
             "layers_per_step": ["paged full attention", f"ring window {c['window']}"],
+            "rope": bool(getattr(s, "rope", False)),
             "parallelism": "replicas", **({"note": c["workload_note"]} if "workload_note" in c else {})}
 
 
@@ -310,6 +353,7 @@ def run_ours(args, rank, world, local_rank):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     first = StepInputs(args.workload, dev, batch_limit=args.batch_limit)
+    first.rope = args.rope
     set_bytes = first.nbytes()
     n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
     sets = [first] + [StepInputs(args.workload, dev, seed_offset=i, batch_limit=args.batch_limit)
@@ -323,10 +367,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step(s):
-        da.decode_attn_paged(s.q, s.k_new, s.v_new, s.pool.k_cache, s.pool.v_cache,
-                             s.pool.block_table, s.seq_lens, s.sinks, 0, s.inp.scale, s.out_full)
-        da.decode_attn_ring(s.q, s.k_new, s.v_new, s.ring.k_cache, s.ring.v_cache, s.seq_lens,
-                            s.sinks, s.inp.scale, s.out_ring)
+        call_paged(s, args.rope)
+        call_ring(s, args.rope)
 
     for i in range(args.warmup):
         step(sets[i % n_sets])
@@ -357,11 +399,9 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.steps):
         s = sets[i % n_sets]
         ev_p0[i].record(stream)
-        da.decode_attn_paged(s.q, s.k_new, s.v_new, s.pool.k_cache, s.pool.v_cache,
-                             s.pool.block_table, s.seq_lens, s.sinks, 0, s.inp.scale, s.out_full)
+        call_paged(s, args.rope)
         ev_p1[i].record(stream)
-        da.decode_attn_ring(s.q, s.k_new, s.v_new, s.ring.k_cache, s.ring.v_cache, s.seq_lens,
-                            s.sinks, s.inp.scale, s.out_ring)
+        call_ring(s, args.rope)
         ev_r1[i].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -427,11 +467,9 @@ def run_e2e(args, s, step_bytes_total, dev):
     for _ in range(n):
         for k, v in host.items():
             dst[k].copy_(v, non_blocking=True)
-        da.decode_attn_paged(dst["q"], dst["k_new"], dst["v_new"], s.pool.k_cache,
-                             s.pool.v_cache, dst["block_table"], dst["seq_lens"], dst["sinks"], 0,
-                             s.inp.scale, s.out_full)
-        da.decode_attn_ring(dst["q"], dst["k_new"], dst["v_new"], s.ring.k_cache, s.ring.v_cache,
-                            dst["seq_lens"], dst["sinks"], s.inp.scale, s.out_ring)
+        call_paged(s, args.rope, dst["q"], dst["k_new"], dst["v_new"], dst["block_table"],
+                   dst["seq_lens"], dst["sinks"])
+        call_ring(s, args.rope, dst["q"], dst["k_new"], dst["v_new"], dst["seq_lens"], dst["sinks"])
         outs[0].copy_(s.out_full, non_blocking=True)
         outs[1].copy_(s.out_ring, non_blocking=True)
     torch.cuda.synchronize()
@@ -453,6 +491,8 @@ def main():
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--rope", action="store_true",
+                    help="fuse the rotary embedding of position L-1 (q and the new key) into both calls")
     ap.add_argument("--batch-limit", type=int, default=None,
                     help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()

@@ -69,6 +69,7 @@ extern "C" {
 #define DA_STATUS_BAD_PAGE 2u    /* a block-table entry outside [0, num_pages); that tile reads
                                     zeros and the append into it is skipped */
 #define DA_STATUS_TIMEOUT 4u     /* a bounded wait on a tile copy expired; output is garbage */
+#define DA_STATUS_BAD_POSITION 8u /* a position L - 1 beyond the rotary tables; row 0 was used */
 
 typedef struct {
     int batch;        /* B: number of sequence slots */
@@ -116,6 +117,36 @@ DA_API int decode_attn_ring(const void *q, const void *k_new, const void *v_new,
                      void *k_cache, void *v_cache,
                      const int32_t *seq_lens, const float *sinks,
                      int window, float scale, void *out, da_shape s, void *stream);
+
+/*
+ * decode_attn_paged_rope / decode_attn_ring_rope -- the same steps with the rotary
+ * position embedding fused in front of the append (SimpleLLM README, changes table,
+ * row "RoPE as one fused kernel at every batch size"). The query and the new key are
+ * rotated to position p = L - 1 before the new key is stored and before the scores:
+ * for i < D/2 the pair (x_i, x_{i+D/2}) becomes
+ *     (x_i c - x_{i+D/2} s,  x_{i+D/2} c + x_i s),   c = rope_cos[p][i], s = rope_sin[p][i]
+ * (the rotate-half form of gpt-oss). v is not rotated; cached keys are expected to be
+ * stored rotated already.
+ *   rope_cos, rope_sin  [max_position, D/2] fp32 device tables, 16-byte aligned; any
+ *                       frequency scaling (e.g. YaRN) is the caller's, folded into them
+ *   max_position        rows of the tables; a position beyond them sets
+ *                       DA_STATUS_BAD_POSITION and uses row 0
+ * The new key is rotated in fp32 (each product, sum and difference rounded separately)
+ * and stored rounded to bf16, nearest even; the query is rounded to bf16 for the scores.
+ * Other arguments as in decode_attn_paged / decode_attn_ring.
+ */
+DA_API int decode_attn_paged_rope(const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  const float *sinks, const float *rope_cos, const float *rope_sin,
+                                  int max_position, int window, float scale, void *out,
+                                  da_shape s, int page_size, int max_pages_per_seq, int num_pages,
+                                  int max_seq_len, void *stream);
+DA_API int decode_attn_ring_rope(const void *q, const void *k_new, const void *v_new,
+                                 void *k_cache, void *v_cache, const int32_t *seq_lens,
+                                 const float *sinks, const float *rope_cos, const float *rope_sin,
+                                 int max_position, int window, float scale, void *out, da_shape s,
+                                 void *stream);
 
 /*
  * kv_append -- the append alone: bit-copies k_new/v_new [B, Hkv, D] of every

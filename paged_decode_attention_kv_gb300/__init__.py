@@ -27,7 +27,8 @@ __all__ = [
     "DecodeAttnError", "decode_attn_paged", "decode_attn_ring", "kv_append",
     "decode_attn_workspace_bytes", "decode_attn_reserve", "decode_attn_device_status",
     "decode_attn_error_string", "library_path", "load_library",
-    "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT",
+    "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT", "DA_STATUS_BAD_POSITION",
+    "decode_attn_paged_rope", "decode_attn_ring_rope",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,6 +42,7 @@ DA_ERR_CUDA = -4
 DA_STATUS_BAD_SEQ_LEN = 1
 DA_STATUS_BAD_PAGE = 2
 DA_STATUS_TIMEOUT = 4
+DA_STATUS_BAD_POSITION = 8
 
 
 class da_shape(ctypes.Structure):
@@ -78,6 +80,11 @@ def load_library():
     lib.decode_attn_ring.argtypes = [vp, vp, vp, vp, vp, i32p, f32p, c_int, c_float, vp,
                                      da_shape, vp]
     lib.kv_append.argtypes = [vp, vp, vp, vp, i32p, i32p, c_int, da_shape, c_int, c_int, c_int, vp]
+    lib.decode_attn_paged_rope.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, f32p, f32p, f32p, c_int,
+                                           c_int, c_float, vp, da_shape, c_int, c_int, c_int, c_int,
+                                           vp]
+    lib.decode_attn_ring_rope.argtypes = [vp, vp, vp, vp, vp, i32p, f32p, f32p, f32p, c_int, c_int,
+                                          c_float, vp, da_shape, vp]
     lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
@@ -85,7 +92,7 @@ def load_library():
     lib.decode_attn_error_string.argtypes = [c_int]
     lib.decode_attn_error_string.restype = ctypes.c_char_p
     for fn in (lib.decode_attn_paged, lib.decode_attn_ring, lib.kv_append, lib.decode_attn_reserve,
-               lib.decode_attn_device_status):
+               lib.decode_attn_device_status, lib.decode_attn_paged_rope, lib.decode_attn_ring_rope):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -142,6 +149,35 @@ def decode_attn_ring(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, scale, 
     _check(lib.decode_attn_ring(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
         _ptr(sinks), int(W), float(scale), _ptr(out), _shape(q, Hkv), _stream(stream)))
+    return out
+
+
+def decode_attn_paged_rope(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks,
+                           rope_cos, rope_sin, window, scale, out, max_seq_len=None, stream=None):
+    """decode_attn_paged with the rotary embedding of position L - 1 applied to q and k_new
+    first; rope_cos/rope_sin are fp32 [max_position, D/2] device tables."""
+    num_pages, Hkv, P, _ = k_cache.shape
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * P
+    lib = load_library()
+    _check(lib.decode_attn_paged_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(sinks), _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]),
+        int(window), float(scale), _ptr(out), _shape(q, Hkv), P, max_pages, num_pages,
+        int(max_seq_len), _stream(stream)))
+    return out
+
+
+def decode_attn_ring_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, rope_cos, rope_sin,
+                          scale, out, stream=None):
+    """decode_attn_ring with the rotary embedding of position L - 1 applied first."""
+    B, Hkv, W, _ = k_cache.shape
+    lib = load_library()
+    _check(lib.decode_attn_ring_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        _ptr(sinks), _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]), int(W), float(scale),
+        _ptr(out), _shape(q, Hkv), _stream(stream)))
     return out
 
 

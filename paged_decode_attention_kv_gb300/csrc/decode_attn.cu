@@ -49,7 +49,7 @@ constexpr int kWarps = 8;          // workers per CTA
 constexpr int kThreads = kWarps * 32;
 // tiles in flight per warp: the deepest pipeline the 227 KiB of shared memory allows
 #ifndef DA_STAGES_G8
-#define DA_STAGES_G8 5
+#define DA_STAGES_G8 4
 #endif
 #ifndef DA_STAGES_G16
 #define DA_STAGES_G16 4
@@ -86,6 +86,9 @@ struct Params {
     int *counters;   // [B*Hkv] arrival tickets, zero at rest
     int B, Hq, Hkv, G, window, max_pages, num_pages, max_seq_len;
     float scale_log2;  // scale * log2(e)
+    const float *rope_cos;  // [max_position][D/2] fp32, or null: no rotary embedding
+    const float *rope_sin;
+    int max_position;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -190,6 +193,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __device__ __forceinline__ void flag_status(unsigned bits) { atomicOr(&g_status, bits); }
+
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v));
+}
+
+// Rotate two element pairs (x1 = elements d, d+1; x2 = elements d+32, d+33) by the
+// table angles of d, d+1: x1' = x1 c - x2 s, x2' = x2 c + x1 s, every operation
+// rounded to fp32 separately (no fused multiply-add), results rounded to bf16.
+__device__ __forceinline__ void rope_pair(uint32_t &x1, uint32_t &x2, const float *c, const float *s) {
+    const float2 a = unpack_bf16(x1), b = unpack_bf16(x2);
+    const float o1x = __fsub_rn(__fmul_rn(a.x, c[0]), __fmul_rn(b.x, s[0]));
+    const float o1y = __fsub_rn(__fmul_rn(a.y, c[1]), __fmul_rn(b.y, s[1]));
+    const float o2x = __fadd_rn(__fmul_rn(b.x, c[0]), __fmul_rn(a.x, s[0]));
+    const float o2y = __fadd_rn(__fmul_rn(b.y, c[1]), __fmul_rn(a.y, s[1]));
+    x1 = pack_bf16(o1x, o1y);
+    x2 = pack_bf16(o2x, o2y);
+}
+
+// One half of the rotation: `mine` holds elements d, d+1 and `other` their partners
+// d +- 32; the first half gets mine*c - other*s, the second half mine*c + other*s.
+__device__ __forceinline__ uint32_t rope_half(uint32_t mine, uint32_t other, const float *c, const float *s,
+                                              bool first_half) {
+    const float2 a = unpack_bf16(mine), b = unpack_bf16(other);
+    float ox, oy;
+    if (first_half) {
+        ox = __fsub_rn(__fmul_rn(a.x, c[0]), __fmul_rn(b.x, s[0]));
+        oy = __fsub_rn(__fmul_rn(a.y, c[1]), __fmul_rn(b.y, s[1]));
+    } else {
+        ox = __fadd_rn(__fmul_rn(a.x, c[0]), __fmul_rn(b.x, s[0]));
+        oy = __fadd_rn(__fmul_rn(a.y, c[1]), __fmul_rn(b.y, s[1]));
+    }
+    return pack_bf16(ox, oy);
+}
 
 // ------------------------------------------------------------------ layout helpers
 template <bool RING>
@@ -322,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const Params p) {
     constexpr int kStages = stages_for<NT>();
     constexpr int GP = NT * 8;
-    constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2;  // the group's q rows, then k_new, v_new
+    // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin rows
+    constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + 2 * (kD / 2) * 4;
     constexpr int kWarpBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
     static_assert(kTileBytes % 1024 == 0, "tile buffers must stay 1024-byte aligned");
     static_assert(2 * sizeof(Slot<NT>) <= kWarpBytes, "merge slots must fit a drained warp area");
@@ -495,7 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wmeta[stg] = make_int4(tb, tg, tt, tp);
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = newseg && p.k_new != nullptr;
-                mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0));
+                const bool rope = newseg && p.rope_cos != nullptr;
+                mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
+                                        (rope ? 4 * kD : 0));
                 int c1, c2;
                 if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
                 else { c1 = 0; c2 = tp * Hkv + tg; }
@@ -509,6 +548,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const size_t off = (static_cast<size_t>(tb) * Hkv + tg) * kD;
                     bulk_load(q_tile(stg) + GP * kD * 2, p.k_new + off, kD * 2, bar);
                     bulk_load(q_tile(stg) + GP * kD * 2 + kD * 2, p.v_new + off, kD * 2, bar);
+                }
+                if (rope) {  // cos/sin rows of the new token's position
+                    int pos = s_len[tb] - 1;
+                    if (pos >= p.max_position) {
+                        flag_status(DA_STATUS_BAD_POSITION);
+                        pos = 0;
+                    }
+                    const size_t row = static_cast<size_t>(pos) * (kD / 2);
+                    bulk_load(q_tile(stg) + GP * kD * 2 + 4 * kD, p.rope_cos + row, kD * 2, bar);
+                    bulk_load(q_tile(stg) + GP * kD * 2 + 6 * kD, p.rope_sin + row, kD * 2, bar);
                 }
             }
         };
@@ -585,6 +634,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 2; ++j) {
                         const int hs = n * 8 + (lane & 3) * 2 + j;
                         sig[n][j] = hs < p.G ? s_sink[sgk * p.G + hs] : -INFINITY;
+                    }
+                }
+                if (p.rope_cos != nullptr) {
+                    // rotary embedding of the new token (rotate-half pairs (i, i + 32)); each
+                    // product and the sum/difference rounded to fp32, then to bf16 (nearest even)
+                    const float *cr = reinterpret_cast<const float *>(qs + GP * kD * 2 + 4 * kD);
+                    const float *sr = cr + kD / 2;
+                    // queries: the partner of element d (< 32) is d + 32, two k-steps further
+#pragma unroll
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const int d = ks * 16 + r * 8 + (lane & 3) * 2;
+                                rope_pair(qf[n][ks][r], qf[n][ks + 2][r], cr + d, sr + d);
+                            }
+                    if (do_append) {  // the new key: element 2*lane pairs with lane ^ 16
+                        const uint32_t other = __shfl_xor_sync(0xffffffffu, knew, 16);
+                        const int d = (2 * lane) & 31;
+                        knew = rope_half(knew, other, cr + d, sr + d, lane < 16);
                     }
                 }
                 state_reset(st);
@@ -1145,7 +1215,8 @@ int prepare_workspace(int dev, int G, cudaStream_t stream, float **part, int **c
 int run_attention(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                   const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
                   float scale, void *out, const da_shape &s, int page_size, int max_pages, int num_pages,
-                  int max_seq_len, void *stream_v) {
+                  int max_seq_len, void *stream_v, const float *rope_cos = nullptr,
+                  const float *rope_sin = nullptr, int max_position = 0) {
     int rc = check_shape(s);
     if (rc != DA_OK) return rc;
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
@@ -1154,6 +1225,8 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
         (k_new && (!aligned16(k_new) || !aligned16(v_new))))
         return DA_ERR_INVALID_ARG;
     if (!(scale == scale)) return DA_ERR_INVALID_ARG;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr)) return DA_ERR_INVALID_ARG;
+    if (rope_cos && (max_position <= 0 || !aligned16(rope_cos) || !aligned16(rope_sin))) return DA_ERR_INVALID_ARG;
     const int G = s.num_q_heads / s.num_kv_heads;
     if (ring) {
         if (window < kPage) return window <= 0 ? DA_ERR_INVALID_ARG : DA_ERR_UNSUPPORTED;
@@ -1189,6 +1262,9 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.num_pages = ring ? 0 : num_pages;
     prm.max_seq_len = ring ? 0 : max_seq_len;
     prm.scale_log2 = scale * kLog2e;
+    prm.rope_cos = rope_cos;
+    prm.rope_sin = rope_sin;
+    prm.max_position = max_position;
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
@@ -1284,6 +1360,9 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.num_pages = num_pages;
     prm.max_seq_len = max_seq_len;
     prm.scale_log2 = scale * kLog2e;
+    prm.rope_cos = nullptr;
+    prm.rope_sin = nullptr;
+    prm.max_position = 0;
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call
@@ -1320,6 +1399,26 @@ int decode_attn_ring(const void *q, const void *k_new, const void *v_new, void *
                      void *stream) {
     return run_attention(true, q, k_new, v_new, k_cache, v_cache, nullptr, seq_lens, sinks, window, scale, out, s,
                          kPage, 0, 0, 0, stream);
+}
+
+int decode_attn_paged_rope(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                           const float *rope_cos, const float *rope_sin, int max_position, int window,
+                           float scale, void *out, da_shape s, int page_size, int max_pages_per_seq,
+                           int num_pages, int max_seq_len, void *stream) {
+    if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
+    return run_attention(false, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window, scale,
+                         out, s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream, rope_cos, rope_sin,
+                         max_position);
+}
+
+int decode_attn_ring_rope(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                          const int32_t *seq_lens, const float *sinks, const float *rope_cos,
+                          const float *rope_sin, int max_position, int window, float scale, void *out,
+                          da_shape s, void *stream) {
+    if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
+    return run_attention(true, q, k_new, v_new, k_cache, v_cache, nullptr, seq_lens, sinks, window, scale, out, s,
+                         kPage, 0, 0, 0, stream, rope_cos, rope_sin, max_position);
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, const int32_t *block_table,
