@@ -351,17 +351,39 @@ __device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&s
     }
 }
 
+// Shared-memory layout of decode_attn_kernel<NT, .>: byte offsets from a 1024-byte
+// aligned base. The kernel carves its buffers from these offsets and the launch
+// requests `bytes`, so the two cannot drift apart.
+template <int NT>
+struct SmemLayout {
+    static constexpr int kStages = stages_for<NT>();
+    static constexpr int GP = NT * 8;
+    // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin rows
+    static constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + 2 * (kD / 2) * 4;
+    static constexpr int kWarpTileBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
+    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8;
+    static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
+    static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
+    static constexpr size_t meta = bars + static_cast<size_t>(kWarps) * kStages * 8;
+    static constexpr size_t ints = meta + static_cast<size_t>(kWarps) * kStages * 16;
+    static constexpr size_t sinks = ints + static_cast<size_t>(kInts) * 4;
+    static constexpr size_t end = sinks + static_cast<size_t>(kMaxQHeads) * 4;
+    static constexpr size_t bytes = 1024 + end;  // plus the slack to align the base
+    static_assert(kTileBytes % 1024 == 0 && kWarpTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
+    static_assert(kQBytes % 16 == 0 && meta % 16 == 0, "bulk copies and int4 need 16-byte alignment");
+    static_assert(bytes <= kMaxSmem, "shared memory budget");
+};
+
 // ------------------------------------------------------------------ the kernel
 template <int NT, bool RING>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
-    constexpr int kStages = stages_for<NT>();
-    constexpr int GP = NT * 8;
-    // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin rows
-    constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + 2 * (kD / 2) * 4;
-    constexpr int kWarpBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
-    static_assert(kTileBytes % 1024 == 0, "tile buffers must stay 1024-byte aligned");
+    using Lay = SmemLayout<NT>;
+    constexpr int kStages = Lay::kStages;
+    constexpr int GP = Lay::GP;
+    constexpr int kQBytes = Lay::kQBytes;
+    constexpr int kWarpBytes = Lay::kWarpTileBytes;
     static_assert(2 * sizeof(Slot<NT>) <= kWarpBytes, "merge slots must fit a drained warp area");
     constexpr int kSlotFloats = 2 * GP + GP * kD;  // global partial: m, l, acc
 
@@ -369,15 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    uint8_t *qarea = smem + kWarps * kWarpBytes;  // [kWarps][kStages] q / k_new / v_new slots
-    uint64_t *bars = reinterpret_cast<uint64_t *>(qarea + kWarps * kStages * kQBytes);
-    int4 *meta = reinterpret_cast<int4 *>(bars + kWarps * kStages);
-    int *s_pre = reinterpret_cast<int *>(meta + kWarps * kStages);  // [B + 1]
+    uint8_t *qarea = smem + Lay::qarea;  // [kWarps][kStages] q / k_new / v_new / cos / sin slots
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bars);
+    int4 *meta = reinterpret_cast<int4 *>(smem + Lay::meta);
+    int *s_pre = reinterpret_cast<int *>(smem + Lay::ints);  // [B + 1]
     int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
     int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
     int *s_winfo = s_wsum + kWarps;                                   // [kWarps][kWinfo]
     int *s_flag = s_winfo + kWarps * kWinfo;                          // [8]
-    float *s_sink = reinterpret_cast<float *>(s_flag + 8);            // [Hq], log2 units
+    float *s_sink = reinterpret_cast<float *>(smem + Lay::sinks);     // [Hq], log2 units
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
     // grid is launched as a programmatic dependent.
@@ -1157,18 +1179,8 @@ int check_shape(const da_shape &s) {
 
 template <int NT, bool RING>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
-    constexpr int kStages = stages_for<NT>();
-    constexpr int GP = NT * 8;
-    constexpr int kWarpBytes = kStages * (2 * kTileBytes + GP * kD * 2 + 2 * kD * 2);  // tiles + q slots
-    const size_t smem = 1024 + static_cast<size_t>(kWarps) * kWarpBytes + kWarps * kStages * (8 + 16) +
-                        (2 * kMaxBatch + 1 + kWarps + kWarps * kWinfo + 8) * sizeof(int) +
-                        static_cast<size_t>(kMaxQHeads) * sizeof(float) + 2 * kWarps * sizeof(int4) + 16;
+    const size_t smem = SmemLayout<NT>::bytes;
     const size_t smem_max = smem;
-    static_assert(1024 + kWarps * kWarpBytes + kWarps * kStages * 24 +
-                          (2 * kMaxBatch + 1 + kWarps + kWarps * kWinfo + 8) * 4 + kMaxQHeads * 4 +
-                          2 * kWarps * 16 + 16 <=
-                      kMaxSmem,
-                  "shared memory budget");
     auto kern = decode_attn_kernel<NT, RING>;
     const int idx = (NT - 1) * 2 + (RING ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
