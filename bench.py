@@ -352,28 +352,49 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    first = StepInputs(args.workload, dev, batch_limit=args.batch_limit)
+    # one set = the layer pairs of one step (each pair: a full layer and a ring layer with
+    # their own caches); more sets rotate when one step's inputs would fit in L2
+    def make_set(k):
+        return [StepInputs(args.workload, dev, seed_offset=k * 10007 + 101 * li,
+                           batch_limit=args.batch_limit) for li in range(args.layers)]
+    sets = [make_set(0)]
+    first = sets[0][0]
     first.rope = args.rope
-    set_bytes = first.nbytes()
+    set_bytes = sum(l.nbytes() for l in sets[0])
     n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
-    sets = [first] + [StepInputs(args.workload, dev, seed_offset=i, batch_limit=args.batch_limit)
-                      for i in range(1, n_sets)]
+    sets += [make_set(k) for k in range(1, n_sets)]
     cfg = first.cfg
     B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
     da.decode_attn_reserve(da.decode_attn_workspace_bytes(B, Hq, Hkv, D))
     pbytes, rbytes = step_bytes(args.workload, first.lens)
+    pbytes_call, rbytes_call = pbytes, rbytes
+    pbytes, rbytes = pbytes * args.layers, rbytes * args.layers
     if args.batch_limit is not None:
         first.cfg["workload_note"] = f"first {args.batch_limit} sequences only"
     stream = torch.cuda.current_stream()
 
-    def step(s):
-        call_paged(s, args.rope)
-        call_ring(s, args.rope)
+    def step(layer_set):
+        for s in layer_set:
+            call_paged(s, args.rope)
+            call_ring(s, args.rope)
 
     for i in range(args.warmup):
         step(sets[i % n_sets])
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
+    graphs = None
+    if args.graph:  # the whole step captured once per input set
+        from paged_decode_attention_kv_gb300.graph import DecodeStepGraph
+        graphs = []
+        for st in sets:
+            calls = []
+            for s in st:
+                calls.append(lambda s=s: call_paged(s, args.rope))
+                calls.append(lambda s=s: call_ring(s, args.rope))
+            graphs.append(DecodeStepGraph(calls, (B, Hq, Hkv, D), dev).capture())
+        for i in range(args.warmup):
+            graphs[i % n_sets].replay()
+        torch.cuda.synchronize()
 
     uuid = str(getattr(props, "uuid", "") or "")
     sampler = ClockSampler(uuid)
@@ -385,7 +406,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        step(sets[i % n_sets])
+        if graphs is not None:
+            graphs[i % n_sets].replay()
+        else:
+            step(sets[i % n_sets])
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -397,7 +421,7 @@ def run_ours(args, rank, world, local_rank):
     ev_p1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_r1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.steps):
-        s = sets[i % n_sets]
+        s = sets[i % n_sets][0]
         ev_p0[i].record(stream)
         call_paged(s, args.rope)
         ev_p1[i].record(stream)
@@ -413,11 +437,11 @@ def run_ours(args, rank, world, local_rank):
     ring_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p1, ev_r1)) / args.steps
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, first, pbytes + rbytes, dev)
+    e2e = run_e2e(args, first, pbytes_call + rbytes_call, dev)
 
     peak, peak_kind = measured_hbm_peak()
     nominal = nominal_hbm_peak()
-    achieved = pbytes / (paged_ms * 1e-3) / 1e9
+    achieved = pbytes_call / (paged_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload, "paged")
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -429,8 +453,9 @@ def run_ours(args, rank, world, local_rank):
                        if n_sets == 1 else f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB > 2x L2"),
         "us_per_call": {"paged_full": round(paged_ms * 1e3, 2), "ring": round(ring_ms * 1e3, 2)},
         "gb_per_s_per_call": {"paged_full": round(achieved, 1),
-                              "ring": round(rbytes / (ring_ms * 1e-3) / 1e9, 1)},
+                              "ring": round(rbytes_call / (ring_ms * 1e-3) / 1e9, 1)},
         "algorithmic_bytes_per_step": {"paged_full": pbytes, "ring": rbytes},
+        "layers_per_step": 2 * args.layers, "graph_replay": bool(args.graph),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
@@ -438,7 +463,7 @@ def run_ours(args, rank, world, local_rank):
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * args.layers * args.steps,
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
                    "events around every launch in a second pass (includes the launch gap)"),
         "clocks": clocks,
@@ -491,6 +516,10 @@ def main():
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--layers", type=int, default=1,
+                    help="full+ring layer pairs per step, each with its own caches")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the whole step once as a CUDA graph and time its replays")
     ap.add_argument("--rope", action="store_true",
                     help="fuse the rotary embedding of position L-1 (q and the new key) into both calls")
     ap.add_argument("--batch-limit", type=int, default=None,
