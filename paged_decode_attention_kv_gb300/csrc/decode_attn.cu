@@ -49,7 +49,7 @@ constexpr int kWarps = 8;          // workers per CTA
 constexpr int kThreads = kWarps * 32;
 // tiles in flight per warp: the deepest pipeline the 227 KiB of shared memory allows
 #ifndef DA_STAGES_G8
-#define DA_STAGES_G8 5
+#define DA_STAGES_G8 4
 #endif
 #ifndef DA_STAGES_G16
 #define DA_STAGES_G16 4
@@ -351,21 +351,6 @@ __device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&s
     }
 }
 
-// Length of sequence b as used everywhere in the kernel: a negative length, or one
-// beyond max_seq_len or the block-table row (paged), counts as an inactive slot.
-// (Read through the read-only cache; every use applies the same rule.)
-template <bool RING>
-__device__ __forceinline__ int valid_len(const Params &p, int b) {
-    const int L = __ldg(p.seq_lens + b);
-    bool bad = L < 0;
-    if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
-    return bad ? 0 : L;
-}
-
-__device__ __forceinline__ float sink_log2(const Params &p, int h) {
-    return p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
-}
-
 // Shared-memory layout of decode_attn_kernel<NT, .>: byte offsets from a 1024-byte
 // aligned base. The kernel carves its buffers from these offsets and the launch
 // requests `bytes`, so the two cannot drift apart.
@@ -376,12 +361,13 @@ struct SmemLayout {
     // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin rows
     static constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + 2 * (kD / 2) * 4;
     static constexpr int kWarpTileBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
-    static constexpr int kInts = (kMaxBatch + 1) + kWarps + kWarps * kWinfo + 8;
+    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8;
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
     static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
     static constexpr size_t meta = bars + static_cast<size_t>(kWarps) * kStages * 8;
     static constexpr size_t ints = meta + static_cast<size_t>(kWarps) * kStages * 16;
-    static constexpr size_t end = ints + static_cast<size_t>(kInts) * 4;
+    static constexpr size_t sinks = ints + static_cast<size_t>(kInts) * 4;
+    static constexpr size_t end = sinks + static_cast<size_t>(kMaxQHeads) * 4;
     static constexpr size_t bytes = 1024 + end;  // plus the slack to align the base
     static_assert(kTileBytes % 1024 == 0 && kWarpTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
     static_assert(kQBytes % 16 == 0 && meta % 16 == 0, "bulk copies and int4 need 16-byte alignment");
@@ -409,9 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bars);
     int4 *meta = reinterpret_cast<int4 *>(smem + Lay::meta);
     int *s_pre = reinterpret_cast<int *>(smem + Lay::ints);  // [B + 1]
-    int *s_wsum = s_pre + (kMaxBatch + 1);                            // [kWarps]
+    int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
+    int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
     int *s_winfo = s_wsum + kWarps;                                   // [kWarps][kWinfo]
     int *s_flag = s_winfo + kWarps * kWinfo;                          // [8]
+    float *s_sink = reinterpret_cast<float *>(smem + Lay::sinks);     // [Hq], log2 units
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
     // grid is launched as a programmatic dependent.
@@ -432,14 +420,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- 1. lengths, validation, prefix of units over sequences
     {
+        for (int h = tid; h < p.Hq; h += kThreads)
+            s_sink[h] = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
         int v[4], tsum = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int b = tid * 4 + k;
             int L = 0;
             if (b < B) {
-                L = valid_len<RING>(p, b);
-                if (L == 0 && blockIdx.x == 0 && __ldg(p.seq_lens + b) != 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+                L = __ldg(p.seq_lens + b);
+                bool bad = L < 0;
+                if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
+                if (bad) {
+                    if (blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+                    L = 0;
+                }
+                s_len[b] = L;
             }
             v[k] = tiles_of<RING>(L, p.window) * Hkv;
             tsum += v[k];
@@ -468,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- 2. inactive slots get a zero output
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        if (valid_len<RING>(p, b) != 0) continue;
+        if (s_len[b] != 0) continue;
         uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(b) * p.Hq * kD);
         const int n16 = p.Hq * kD * 2 / 16;
         for (int i = tid; i < n16; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
@@ -527,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 og = r / tiles;
                 ot = r - og * tiles;
                 if (!RING) {
-                    const int L = valid_len<RING>(p, b);
+                    const int L = s_len[b];
                     const int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
                     op = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + lo / kPage + ot);
                 }
@@ -576,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_load(q_tile(stg) + GP * kD * 2 + kD * 2, p.v_new + off, kD * 2, bar);
                 }
                 if (rope) {  // cos/sin rows of the new token's position
-                    int pos = valid_len<RING>(p, tb) - 1;
+                    int pos = s_len[tb] - 1;
                     if (pos >= p.max_position) {
                         flag_status(DA_STATUS_BAD_POSITION);
                         pos = 0;
@@ -622,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 sb = tb; sgk = tg;
-                L = valid_len<RING>(p, sb);
+                L = s_len[sb];
                 const int tiles = (s_pre[sb + 1] - s_pre[sb]) / Hkv;
                 seg_first_unit = s_pre[sb] + sgk * tiles;
                 seg_end_unit = seg_first_unit + tiles;
@@ -659,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int hs = n * 8 + (lane & 3) * 2 + j;
-                        sig[n][j] = hs < p.G ? sink_log2(p, sgk * p.G + hs) : -INFINITY;
+                        sig[n][j] = hs < p.G ? s_sink[sgk * p.G + hs] : -INFINITY;
                     }
                 }
                 if (p.rope_cos != nullptr) {
@@ -859,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
                     M = fmaxf(M, sl->m[n]);
                 }
-                const float sg = (internal && n < p.G) ? sink_log2(p, g * p.G + n) : -INFINITY;
+                const float sg = (internal && n < p.G) ? s_sink[g * p.G + n] : -INFINITY;
                 const float Mf = internal ? fmaxf(M, sg) : M;
                 float den = internal ? fast_exp2(sg - Mf) : 0.f;
                 float acc[16];
@@ -983,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             M = Mn;
         }
-        const float sg = cn < p.G ? sink_log2(p, g * p.G + cn) : -INFINITY;
+        const float sg = cn < p.G ? s_sink[g * p.G + cn] : -INFINITY;
         const float Mf = fmaxf(M, sg);
         const float a = fast_exp2(M - Mf);
         den = den * a + fast_exp2(sg - Mf);
