@@ -49,13 +49,18 @@ constexpr int kWarps = 8;          // workers per CTA
 constexpr int kThreads = kWarps * 32;
 // tiles in flight per warp: the deepest pipeline the 227 KiB of shared memory allows
 #ifndef DA_STAGES_G8
-#define DA_STAGES_G8 4
+#define DA_STAGES_G8 5
+#endif
+#ifndef DA_STAGES_G8_ROPE
+#define DA_STAGES_G8_ROPE 4
 #endif
 #ifndef DA_STAGES_G16
 #define DA_STAGES_G16 4
 #endif
-template <int NT>
-__host__ __device__ constexpr int stages_for() { return NT == 1 ? DA_STAGES_G8 : DA_STAGES_G16; }
+template <int NT, bool ROPE>
+__host__ __device__ constexpr int stages_for() {
+    return NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16;
+}
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
 #endif
@@ -351,15 +356,15 @@ __device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&s
     }
 }
 
-// Shared-memory layout of decode_attn_kernel<NT, .>: byte offsets from a 1024-byte
+// Shared-memory layout of decode_attn_kernel<NT, ., ROPE>: byte offsets from a 1024-byte
 // aligned base. The kernel carves its buffers from these offsets and the launch
 // requests `bytes`, so the two cannot drift apart.
-template <int NT>
+template <int NT, bool ROPE>
 struct SmemLayout {
-    static constexpr int kStages = stages_for<NT>();
+    static constexpr int kStages = stages_for<NT, ROPE>();
     static constexpr int GP = NT * 8;
     // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin rows
-    static constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + 2 * (kD / 2) * 4;
+    static constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + (ROPE ? 2 * (kD / 2) * 4 : 0);
     static constexpr int kWarpTileBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
     static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8;
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
@@ -375,11 +380,11 @@ struct SmemLayout {
 };
 
 // ------------------------------------------------------------------ the kernel
-template <int NT, bool RING>
+template <int NT, bool RING, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
-    using Lay = SmemLayout<NT>;
+    using Lay = SmemLayout<NT, ROPE>;
     constexpr int kStages = Lay::kStages;
     constexpr int GP = Lay::GP;
     constexpr int kQBytes = Lay::kQBytes;
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wmeta[stg] = make_int4(tb, tg, tt, tp);
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = newseg && p.k_new != nullptr;
-                const bool rope = newseg && p.rope_cos != nullptr;
+                const bool rope = ROPE && newseg;
                 mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
                                         (rope ? 4 * kD : 0));
                 int c1, c2;
@@ -658,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sig[n][j] = hs < p.G ? s_sink[sgk * p.G + hs] : -INFINITY;
                     }
                 }
-                if (p.rope_cos != nullptr) {
+                if constexpr (ROPE) {
                     // rotary embedding of the new token (rotate-half pairs (i, i + 32)); each
                     // product and the sum/difference rounded to fp32, then to bf16 (nearest even)
                     const float *cr = reinterpret_cast<const float *>(qs + GP * kD * 2 + 4 * kD);
@@ -1112,7 +1117,7 @@ struct DeviceState {
     void *ws = nullptr;
     size_t ws_bytes = 0;
     int sm_count = 0;
-    bool attr_set[4] = {false, false, false, false};
+    bool attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -1177,12 +1182,12 @@ int check_shape(const da_shape &s) {
     return DA_OK;
 }
 
-template <int NT, bool RING>
+template <int NT, bool RING, bool ROPE>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
-    const size_t smem = SmemLayout<NT>::bytes;
+    const size_t smem = SmemLayout<NT, ROPE>::bytes;
     const size_t smem_max = smem;
-    auto kern = decode_attn_kernel<NT, RING>;
-    const int idx = (NT - 1) * 2 + (RING ? 1 : 0);
+    auto kern = decode_attn_kernel<NT, RING, ROPE>;
+    const int idx = (NT - 1) * 4 + (RING ? 2 : 0) + (ROPE ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
@@ -1288,8 +1293,18 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
         snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
         return DA_ERR_CUDA;
     }
-    if (G <= 8) return ring ? launch_attn<1, true>(mk, mv, prm, dev, stream) : launch_attn<1, false>(mk, mv, prm, dev, stream);
-    return ring ? launch_attn<2, true>(mk, mv, prm, dev, stream) : launch_attn<2, false>(mk, mv, prm, dev, stream);
+    if (rope_cos != nullptr) {
+        if (G <= 8)
+            return ring ? launch_attn<1, true, true>(mk, mv, prm, dev, stream)
+                        : launch_attn<1, false, true>(mk, mv, prm, dev, stream);
+        return ring ? launch_attn<2, true, true>(mk, mv, prm, dev, stream)
+                    : launch_attn<2, false, true>(mk, mv, prm, dev, stream);
+    }
+    if (G <= 8)
+        return ring ? launch_attn<1, true, false>(mk, mv, prm, dev, stream)
+                    : launch_attn<1, false, false>(mk, mv, prm, dev, stream);
+    return ring ? launch_attn<2, true, false>(mk, mv, prm, dev, stream)
+                : launch_attn<2, false, false>(mk, mv, prm, dev, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free variant
@@ -1390,7 +1405,8 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
         snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
         return DA_ERR_CUDA;
     }
-    return prm.G <= 8 ? launch_attn<1, false>(mk, mv, prm, dev, stream) : launch_attn<2, false>(mk, mv, prm, dev, stream);
+    return prm.G <= 8 ? launch_attn<1, false, false>(mk, mv, prm, dev, stream)
+                      : launch_attn<2, false, false>(mk, mv, prm, dev, stream);
 }
 
 }  // namespace
