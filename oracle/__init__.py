@@ -21,12 +21,15 @@ _lib = None
 _FUNCS = ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
           "oracle_kv_append_paged", "oracle_kv_append_ring", "oracle_scatter_paged",
           "oracle_scatter_ring", "oracle_rope_q64", "oracle_rope_k", "oracle_decode_paged_rope",
-          "oracle_decode_ring_rope")
+          "oracle_decode_ring_rope", "oracle_e4m3_decode", "oracle_e4m3_encode",
+          "oracle_quantise_rows", "oracle_decode_paged_fp8", "oracle_decode_ring_fp8",
+          "oracle_kv_append_fp8", "oracle_scatter_fp8")
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 def _load():
@@ -62,6 +65,21 @@ def _load():
         lib.oracle_decode_ring_rope.argtypes = [
             _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _f32p, _f32p, _f32p, c_int, c_int, c_double,
             _f64p, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_e4m3_decode.argtypes = [_u8p, c_int, _f64p]
+        lib.oracle_e4m3_encode.argtypes = [_f32p, c_int, _u8p]
+        lib.oracle_quantise_rows.argtypes = [_u16p, c_int, c_int, _u8p, _f32p]
+        lib.oracle_decode_paged_fp8.argtypes = [
+            _u16p, _u16p, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, _i32p, _f32p, c_int, c_double,
+            _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_decode_ring_fp8.argtypes = [
+            _u16p, _u16p, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, _f32p, c_int, c_double, _f64p,
+            c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_kv_append_fp8.argtypes = [
+            _u16p, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, _i32p, c_int, c_int, c_int, c_int, c_int,
+            c_int, c_int]
+        lib.oracle_scatter_fp8.argtypes = [
+            _u16p, _u16p, _i32p, c_int, _i32p, c_int, _u8p, _u8p, _f32p, _f32p, c_int, c_int, c_int,
+            c_int, c_int, c_int]
         for name in _FUNCS:
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -332,4 +350,129 @@ def decode_ring_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, rope_co
         maxpos, int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D, _ptr(it, _i32p),
         n_items, nthreads or default_threads())
     _check(st, "decode_ring_rope")
+    return out
+
+
+# ---------------------------------------------------------------- fp8 (e4m3) KV cache
+def e4m3_decode(codes):
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.shape, np.float64)
+    lib.oracle_e4m3_decode(_ptr(c, _u8p), c.size, _ptr(out, _f64p))
+    return out
+
+
+def e4m3_encode(x):
+    lib = _load()
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.zeros(f.shape, np.uint8)
+    lib.oracle_e4m3_encode(_ptr(f, _f32p), f.size, _ptr(out, _u8p))
+    return out
+
+
+def quantise_rows(rows):
+    """bf16 rows [..., D] -> (e4m3 codes [..., D], fp32 scales [...])."""
+    lib = _load()
+    r = _u16(rows, "rows")
+    D = r.shape[-1]
+    n = r.size // D
+    codes = np.zeros(r.shape, np.uint8)
+    scales = np.zeros(r.shape[:-1], np.float32)
+    lib.oracle_quantise_rows(_ptr(r, _u16p), n, D, _ptr(codes, _u8p), _ptr(scales, _f32p))
+    return codes, scales
+
+
+class Fp8Cache:
+    """fp8 cache arrays: K codes, V^T codes, K scales, V scales (numpy)."""
+
+    def __init__(self, k, vt, ks, vs):
+        self.k, self.vt, self.ks, self.vs = k, vt, ks, vs
+
+    @staticmethod
+    def empty_paged(num_pages, Hkv, P, D, fill_code=0x7F, fill_scale=np.nan):
+        return Fp8Cache(np.full((num_pages, Hkv, P, D), fill_code, np.uint8),
+                        np.full((num_pages, Hkv, D, P), fill_code, np.uint8),
+                        np.full((num_pages, Hkv, P), fill_scale, np.float32),
+                        np.full((num_pages, Hkv, P), fill_scale, np.float32))
+
+    @staticmethod
+    def empty_ring(B, Hkv, W, D, fill_code=0x7F, fill_scale=np.nan):
+        return Fp8Cache(np.full((B, Hkv, W, D), fill_code, np.uint8),
+                        np.full((B, Hkv, D, W), fill_code, np.uint8),
+                        np.full((B, Hkv, W), fill_scale, np.float32),
+                        np.full((B, Hkv, W), fill_scale, np.float32))
+
+    def copy(self):
+        return Fp8Cache(self.k.copy(), self.vt.copy(), self.ks.copy(), self.vs.copy())
+
+    def ptrs(self):
+        return (_ptr(self.k, _u8p), _ptr(self.vt, _u8p), _ptr(self.ks, _f32p), _ptr(self.vs, _f32p))
+
+
+def scatter_fp8(hist_k, hist_v, n_tokens, cache, block_table=None, window=0):
+    """Quantise tokens 0..n[b]-1 of each history into (a copy of) an fp8 cache: paged when a
+    block table is given, else the ring state of capacity `window`."""
+    lib = _load()
+    hk, hv = _u16(hist_k, "hist_k"), _u16(hist_v, "hist_v")
+    n = _i32(n_tokens)
+    out = cache.copy()
+    B, Tmax, Hkv, D = hk.shape
+    if block_table is not None:
+        bt = _i32(block_table)
+        P, maxp, npages = out.k.shape[2], bt.shape[1], out.k.shape[0]
+    else:
+        bt, P, maxp, npages = None, 16, 0, 0
+    _check(lib.oracle_scatter_fp8(_ptr(hk, _u16p), _ptr(hv, _u16p), _ptr(n, _i32p), Tmax,
+                                  _ptr(bt, _i32p), int(window), *out.ptrs(), B, Hkv, D, P, maxp,
+                                  npages), "scatter_fp8")
+    return out
+
+
+def kv_append_fp8(k_new, v_new, cache, seq_lens, block_table=None, window=0):
+    lib = _load()
+    kn, vn = _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    sl = _i32(seq_lens)
+    out = cache.copy()
+    B, Hkv, D = kn.shape
+    if block_table is not None:
+        bt = _i32(block_table)
+        P, maxp, npages = out.k.shape[2], bt.shape[1], out.k.shape[0]
+    else:
+        bt, P, maxp, npages = None, 16, 0, 0
+    _check(lib.oracle_kv_append_fp8(_ptr(kn, _u16p), _ptr(vn, _u16p), *out.ptrs(), _ptr(bt, _i32p),
+                                    _ptr(sl, _i32p), int(window), B, Hkv, D, P, maxp, npages),
+           "kv_append_fp8")
+    return out
+
+
+def decode_paged_fp8(q, k_new, v_new, cache, block_table, seq_lens, sinks, window, scale,
+                     items=None, nthreads=None):
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, _ = cache.k.shape
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_paged_fp8(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), *cache.ptrs(), _ptr(bt, _i32p),
+        _ptr(sl, _i32p), _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv,
+        D, P, bt.shape[1], num_pages, _ptr(it, _i32p), n_items, nthreads or default_threads()),
+        "decode_paged_fp8")
+    return out
+
+
+def decode_ring_fp8(q, k_new, v_new, cache, seq_lens, sinks, window, scale, items=None,
+                    nthreads=None):
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    sl, sk = _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    Hkv = cache.k.shape[1]
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_ring_fp8(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), *cache.ptrs(), _ptr(sl, _i32p),
+        _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D,
+        _ptr(it, _i32p), n_items, nthreads or default_threads()), "decode_ring_fp8")
     return out

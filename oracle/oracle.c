@@ -497,3 +497,302 @@ int oracle_decode_ring_rope(const uint16_t *q, const uint16_t *k_new, const uint
     free(krot);
     return st;
 }
+
+/* ------------------------------------------------------------------ */
+/* fp8 KV cache (reading of "quantised KV pages": the pages name quantisation
+ * only as a topic). Every cached K or V row of one token and one KV head is
+ * stored as 64 OCP e4m3 codes (the FN variant: sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits, no infinities, largest finite 448, NaN = 0x7F / 0xFF)
+ * and one fp32 scale; its value is decode(code) * scale.
+ * Quantising a row when it is appended: amax = max |x_d| (x widened exactly
+ * from bf16), scale = amax / 448 in fp32 (scale = 1 when amax = 0), code_d =
+ * the e4m3 value nearest to x_d / scale (fp32 division), ties to even,
+ * saturating at +-448. The kernel takes the same fp32 decisions.
+ * Layouts: paged K codes [num_pages][Hkv][P][D], paged V codes transposed
+ * [num_pages][Hkv][D][P] (V^T per page), scales [num_pages][Hkv][P];
+ * ring K [B][Hkv][W][D], ring V^T [B][Hkv][D][W], scales [B][Hkv][W]. */
+
+static double e4m3_decode(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* nearest e4m3 value to f (ties to even mantissa), saturating at 448; f finite */
+static uint8_t e4m3_encode(float f) {
+    if (f != f) return 0x7F;
+    const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7E;
+    /* candidates are k * 2^(e-3) on the grid of the binade of a (subnormal grid 2^-9) */
+    int ex;
+    frexp(a, &ex);                 /* a = frac * 2^ex, frac in [0.5, 1) */
+    int e_unb = ex - 1;            /* a in [2^e_unb, 2^(e_unb+1)) */
+    if (e_unb < -6) e_unb = -6;    /* subnormal range shares the grid of binade -6 */
+    const double step = ldexp(1.0, e_unb - 3);
+    double k = floor(a / step);
+    const double rem = a - k * step;
+    if (rem > step / 2 || (rem == step / 2 && fmod(k, 2.0) == 1.0)) k += 1.0;
+    const double v = k * step;     /* may reach the next binade: still representable */
+    if (v >= 448.0) return sign | 0x7E;
+    if (v == 0.0) return sign;
+    int ev;
+    frexp(v, &ev);
+    int eu = ev - 1;
+    if (eu < -6) { /* subnormal: v = m * 2^-9 */
+        return sign | (uint8_t)(v / ldexp(1.0, -9));
+    }
+    const int mant = (int)((v / ldexp(1.0, eu) - 1.0) * 8.0 + 0.5);
+    return sign | (uint8_t)(((eu + 7) << 3) | mant);
+}
+
+/* quantise one row of D bf16 values: codes[D] and its scale */
+static void quantise_row(const uint16_t *x, int D, uint8_t *codes, float *scale_out) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        const float v = fabsf(bf16_to_f32(x[d]));
+        if (v > amax) amax = v;
+    }
+    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int d = 0; d < D; ++d) codes[d] = e4m3_encode(bf16_to_f32(x[d]) / scale);
+    *scale_out = scale;
+}
+
+int oracle_e4m3_decode(const uint8_t *codes, int n, double *out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_decode(codes[i]);
+    return OR_OK;
+}
+
+int oracle_e4m3_encode(const float *x, int n, uint8_t *out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+    return OR_OK;
+}
+
+/* rows [n][D] bf16 -> codes [n][D], scales [n] */
+int oracle_quantise_rows(const uint16_t *x, int n, int D, uint8_t *codes, float *scales) {
+    for (int i = 0; i < n; ++i) quantise_row(x + (size_t)i * D, D, codes + (size_t)i * D, scales + i);
+    return OR_OK;
+}
+
+typedef struct {
+    int ring;                    /* 0 paged, 1 ring */
+    const uint16_t *q;
+    const uint16_t *k_new, *v_new; /* bf16 [B][Hkv][D], quantised on append, or NULL */
+    const uint8_t *kc, *vct;     /* K codes, V^T codes */
+    const float *ks, *vs;        /* scales */
+    const int32_t *block_table, *seq_lens;
+    const float *sinks;
+    int window; double scale;
+    int B, Hq, Hkv, D, P, max_pages, num_pages;
+    const int32_t *items; int n_items;
+    double *out;
+} problem8;
+
+/* dequantised key and value rows of position j (cache or, for j = L-1, the quantised new token) */
+static int token_rows8(const problem8 *pr, int b, int g, int j, double *k, double *v) {
+    const int L = pr->seq_lens[b], D = pr->D;
+    if (j == L - 1 && pr->k_new) {
+        uint8_t ck[256], cv[256];
+        float sk, sv;
+        if (D > 256) return OR_BAD_ARG;
+        quantise_row(pr->k_new + ((size_t)b * pr->Hkv + g) * D, D, ck, &sk);
+        quantise_row(pr->v_new + ((size_t)b * pr->Hkv + g) * D, D, cv, &sv);
+        for (int d = 0; d < D; ++d) { k[d] = e4m3_decode(ck[d]) * sk; v[d] = e4m3_decode(cv[d]) * sv; }
+        return OR_OK;
+    }
+    size_t krow, vbase, srow; int vstride;
+    if (!pr->ring) {
+        if (j / pr->P >= pr->max_pages) return OR_BAD_INDEX;
+        const int32_t page = pr->block_table[(size_t)b * pr->max_pages + j / pr->P];
+        if (page < 0 || page >= pr->num_pages) return OR_BAD_INDEX;
+        const size_t ph = (size_t)page * pr->Hkv + g;
+        const int slot = j % pr->P;
+        krow = (ph * pr->P + slot) * D;
+        vbase = ph * (size_t)D * pr->P + slot; vstride = pr->P;
+        srow = ph * pr->P + slot;
+    } else {
+        const int W = pr->window, cell = j % W;
+        const size_t bh = (size_t)b * pr->Hkv + g;
+        krow = (bh * W + cell) * D;
+        vbase = bh * (size_t)D * W + cell; vstride = W;
+        srow = bh * W + cell;
+    }
+    const double sk = pr->ks[srow], sv = pr->vs[srow];
+    for (int d = 0; d < D; ++d) {
+        k[d] = e4m3_decode(pr->kc[krow + d]) * sk;
+        v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]) * sv;
+    }
+    return OR_OK;
+}
+
+static int attend_one8(const problem8 *pr, int b, int h, double *out) {
+    const int D = pr->D, L = pr->seq_lens[b];
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (L <= 0) return OR_OK;
+    const int g = h / (pr->Hq / pr->Hkv);
+    const int W = pr->ring ? pr->window : pr->window;
+    const int lo = (W > 0 && L - W > 0) ? L - W : 0, n = L - lo;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double *kv = (double *)malloc(sizeof(double) * 2 * (size_t)D);
+    if (!s || !kv) { free(s); free(kv); return OR_NOMEM; }
+    const uint16_t *qrow = pr->q + ((size_t)b * pr->Hq + h) * D;
+    const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;
+    double M = sigma;
+    int st = OR_OK;
+    for (int i = 0; i < n && st == OR_OK; ++i) {
+        st = token_rows8(pr, b, g, lo + i, kv, kv + D);
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * kv[d];
+        s[i] = pr->scale * dot;
+        if (s[i] > M) M = s[i];
+    }
+    double den = isinf(sigma) && sigma < 0 ? 0.0 : exp(sigma - M);
+    for (int i = 0; i < n && st == OR_OK; ++i) {
+        st = token_rows8(pr, b, g, lo + i, kv, kv + D);
+        const double w = exp(s[i] - M);
+        den += w;
+        for (int d = 0; d < D; ++d) out[d] += w * kv[D + d];
+    }
+    if (st == OR_OK) for (int d = 0; d < D; ++d) out[d] /= den;
+    free(s); free(kv);
+    return st;
+}
+
+typedef struct { problem8 *pr; int tid, nthreads, status; } worker8_arg;
+
+static void *worker8(void *p) {
+    worker8_arg *a = (worker8_arg *)p;
+    problem8 *pr = a->pr;
+    const int total = pr->items ? pr->n_items : pr->B * pr->Hq;
+    for (int w = a->tid; w < total; w += a->nthreads) {
+        int b = pr->items ? pr->items[2 * w] : w / pr->Hq;
+        int h = pr->items ? pr->items[2 * w + 1] : w % pr->Hq;
+        if (b < 0 || b >= pr->B || h < 0 || h >= pr->Hq) { a->status = OR_BAD_ARG; continue; }
+        int st = attend_one8(pr, b, h, pr->out + (size_t)w * pr->D);
+        if (st != OR_OK && a->status == OR_OK) a->status = st;
+    }
+    return NULL;
+}
+
+static int run8(problem8 *pr, int nthreads) {
+    if (pr->B < 0 || pr->Hq <= 0 || pr->Hkv <= 0 || pr->Hq % pr->Hkv || pr->D <= 0 || pr->D > 256)
+        return OR_BAD_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    worker8_arg args[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) { args[t].pr = pr; args[t].tid = t; args[t].nthreads = nthreads; args[t].status = OR_OK; }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, worker8, &args[t]) != 0) break;
+        started = t;
+    }
+    for (int t = started + 1; t < nthreads; ++t) worker8(&args[t]);
+    worker8(&args[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    for (int t = 0; t < nthreads; ++t) if (args[t].status != OR_OK) return args[t].status;
+    return OR_OK;
+}
+
+int oracle_decode_paged_fp8(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                            const uint8_t *k_codes, const uint8_t *vt_codes, const float *k_scale,
+                            const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                            const float *sinks, int window, double scale, double *out,
+                            int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                            const int32_t *items, int n_items, int nthreads) {
+    if (!q || !k_codes || !vt_codes || !k_scale || !v_scale || !block_table || !seq_lens || !out ||
+        page_size <= 0 || max_pages <= 0 || num_pages <= 0 || window < 0 || ((k_new == NULL) != (v_new == NULL)))
+        return OR_BAD_ARG;
+    problem8 pr = {0, q, k_new, v_new, k_codes, vt_codes, k_scale, v_scale, block_table, seq_lens, sinks,
+                   window, scale, B, Hq, Hkv, D, page_size, max_pages, num_pages, items, n_items, out};
+    return run8(&pr, nthreads);
+}
+
+int oracle_decode_ring_fp8(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                           const uint8_t *k_codes, const uint8_t *vt_codes, const float *k_scale,
+                           const float *v_scale, const int32_t *seq_lens, const float *sinks, int window,
+                           double scale, double *out, int B, int Hq, int Hkv, int D,
+                           const int32_t *items, int n_items, int nthreads) {
+    if (!q || !k_codes || !vt_codes || !k_scale || !v_scale || !seq_lens || !out || window <= 0 ||
+        ((k_new == NULL) != (v_new == NULL)))
+        return OR_BAD_ARG;
+    problem8 pr = {1, q, k_new, v_new, k_codes, vt_codes, k_scale, v_scale, NULL, seq_lens, sinks,
+                   window, scale, B, Hq, Hkv, D, 16, 0, 0, items, n_items, out};
+    return run8(&pr, nthreads);
+}
+
+/* Write token rows (bf16 [n][Hkv][D] per sequence b at positions pos[b] .. ) quantised into an
+ * fp8 cache: the append of the new tokens (positions L-1), or the materialisation of a history. */
+static void put8(int ring, uint8_t *kc, uint8_t *vct, float *ks, float *vs, int b, int g, int j,
+                 const uint16_t *krow, const uint16_t *vrow, int Hkv, int D, int P, int W,
+                 int32_t page) {
+    uint8_t ck[256], cv[256];
+    float sk, sv;
+    quantise_row(krow, D, ck, &sk);
+    quantise_row(vrow, D, cv, &sv);
+    size_t kbase, vbase, srow; int vstride;
+    if (!ring) {
+        const size_t ph = (size_t)page * Hkv + g;
+        const int slot = j % P;
+        kbase = (ph * P + slot) * D; vbase = ph * (size_t)D * P + slot; vstride = P; srow = ph * P + slot;
+    } else {
+        const size_t bh = (size_t)b * Hkv + g;
+        const int cell = j % W;
+        kbase = (bh * W + cell) * D; vbase = bh * (size_t)D * W + cell; vstride = W; srow = bh * W + cell;
+    }
+    for (int d = 0; d < D; ++d) { kc[kbase + d] = ck[d]; vct[vbase + (size_t)d * vstride] = cv[d]; }
+    ks[srow] = sk; vs[srow] = sv;
+}
+
+int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_codes, uint8_t *vt_codes,
+                         float *k_scale, float *v_scale, const int32_t *block_table /* NULL = ring */,
+                         const int32_t *seq_lens, int window, int B, int Hkv, int D, int page_size,
+                         int max_pages, int num_pages) {
+    if (D > 256) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        if (L <= 0) continue;
+        const int p = L - 1;
+        int32_t page = 0;
+        if (block_table) {
+            if (p / page_size >= max_pages) return OR_BAD_INDEX;
+            page = block_table[(size_t)b * max_pages + p / page_size];
+            if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
+        }
+        for (int g = 0; g < Hkv; ++g) {
+            const size_t src = ((size_t)b * Hkv + g) * D;
+            put8(block_table == NULL, k_codes, vt_codes, k_scale, v_scale, b, g, p, k_new + src, v_new + src,
+                 Hkv, D, page_size, window, page);
+        }
+    }
+    return OR_OK;
+}
+
+/* Materialise the first n[b] tokens of hist [B][Tmax][Hkv][D] into an fp8 cache (paged when a
+ * block table is given, else the ring state of capacity `window`). */
+int oracle_scatter_fp8(const uint16_t *hist_k, const uint16_t *hist_v, const int32_t *n_tokens, int Tmax,
+                       const int32_t *block_table, int window, uint8_t *k_codes, uint8_t *vt_codes,
+                       float *k_scale, float *v_scale, int B, int Hkv, int D, int page_size, int max_pages,
+                       int num_pages) {
+    if (D > 256) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int n = n_tokens[b];
+        const int lo = (!block_table && n - window > 0) ? n - window : 0;
+        for (int j = lo; j < n; ++j) {
+            if (j >= Tmax) return OR_BAD_INDEX;
+            int32_t page = 0;
+            if (block_table) {
+                if (j / page_size >= max_pages) return OR_BAD_INDEX;
+                page = block_table[(size_t)b * max_pages + j / page_size];
+                if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
+            }
+            for (int g = 0; g < Hkv; ++g) {
+                const size_t src = (((size_t)b * Tmax + j) * Hkv + g) * D;
+                put8(block_table == NULL, k_codes, vt_codes, k_scale, v_scale, b, g, j, hist_k + src,
+                     hist_v + src, Hkv, D, page_size, window, page);
+            }
+        }
+    }
+    return OR_OK;
+}

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_fp8 as fp8_pins
 import test_oracle_rope as rope_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -50,6 +51,14 @@ MUTANTS = [
      "pr.q = q; pr.q64 = NULL; pr.k_new = krot; pr.v_new = v_new; pr.k_src = k_cache; "
      "pr.v_src = v_cache;\n        pr.block_table"),
     ("rope_key_truncated", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;"),
+    ("e4m3_bias", "ldexp(1.0 + m / 8.0, e - 7);", "ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3_ties_away", "if (rem > step / 2 || (rem == step / 2 && fmod(k, 2.0) == 1.0)) k += 1.0;",
+     "if (rem >= step / 2) k += 1.0;"),
+    ("fp8_vt_stride", "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]) * sv;",
+     "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d]) * sv;"),
+    ("fp8_no_vscale", "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]) * sv;",
+     "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]);"),
+    ("fp8_scale_rule", "amax / 448.0f", "amax / 447.0f"),
     ("append_wrong_cell",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(L % page_size)) * D;"),
@@ -73,6 +82,11 @@ PIN_CALLS = [
     rope_pins.test_rotation_keeps_norms,
     rope_pins.test_stored_key_rounding_is_fp32_then_bf16_nearest_even,
     lambda: rope_pins.test_attention_depends_only_on_relative_positions(37),
+    fp8_pins.test_decode_every_code_like_torch,
+    fp8_pins.test_encode_rounds_to_nearest_even_like_torch,
+    fp8_pins.test_quantisation_rule_closed_form,
+    lambda: fp8_pins.test_fp8_equals_bf16_on_values_exact_in_both(0),
+    fp8_pins.test_paged_and_ring_agree_and_append_is_fused,
 ]
 
 
