@@ -38,9 +38,11 @@ HBM_BUS_BITS = 8192  # 8 HBM3e stacks x 1024 bits
 
 
 # ---------------------------------------------------------------- bytes the method must move
-def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W):
+def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W, kv="bf16"):
     """Per call: cached K+V of the attended tokens (except the new one), k_new/v_new read
-    and written, q read, out written, block-table entries read, seq_lens, sinks."""
+    and written, q read, out written, block-table entries read, seq_lens, sinks. A cached
+    token costs 2*2*D bytes per KV head in bf16, or 2*D codes + two fp32 scales in fp8."""
+    tok = 4 * D if kv == "bf16" else 2 * D + 8
     total = 0
     for L in lens:
         if L <= 0:
@@ -52,7 +54,7 @@ def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W):
             n, tiles = L - lo, (L - 1) // P - lo // P + 1
         else:  # ring
             n, tiles = min(L, W), 0
-        total += (n - 1) * 4 * Hkv * D + 2 * 2 * Hkv * D + 2 * 2 * Hkv * D + 2 * Hq * D \
+        total += (n - 1) * tok * Hkv + 2 * 2 * Hkv * D + tok * Hkv + 2 * Hq * D \
             + 2 * Hq * D + 4 * tiles
     return total + 4 * len(lens) + 4 * Hq
 
@@ -185,7 +187,7 @@ def cpu_cores():
 class StepInputs:
     """One independent copy of a step's inputs and caches on the device."""
 
-    def __init__(self, name, device, seed_offset=0, batch_limit=None):
+    def __init__(self, name, device, seed_offset=0, batch_limit=None, kv="bf16"):
         import torch
         from paged_decode_attention_kv_gb300 import workloads as wl
         cfg = wl.config(name)
@@ -197,11 +199,21 @@ class StepInputs:
         vgen = torch.Generator(device=device)
         vgen.manual_seed(seed)
         B, Hq, Hkv, D, P, W = (cfg[k] for k in ("B", "Hq", "Hkv", "D", "page_size", "window"))
+        self.kv = kv
         self.inp = wl.draw_decode_inputs(B, Hq, Hkv, D, self.lens, gen)
-        self.pool = wl.draw_paged_pool(wl.pool_size(name, self.lens), Hkv, P, D, self.lens,
-                                       wl.max_pages_per_seq(name, self.lens), gen, device=device,
-                                       value_gen=vgen)
-        self.ring = wl.draw_ring_pool(B, Hkv, W, D, vgen, device=device)
+        npages = wl.pool_size(name, self.lens)
+        if kv == "bf16":
+            self.pool = wl.draw_paged_pool(npages, Hkv, P, D, self.lens,
+                                           wl.max_pages_per_seq(name, self.lens), gen,
+                                           device=device, value_gen=vgen)
+            self.ring = wl.draw_ring_pool(B, Hkv, W, D, vgen, device=device)
+            self.block_table = self.pool.block_table
+        else:
+            self.block_table = wl.draw_block_table(self.lens, P, npages,
+                                                   wl.max_pages_per_seq(name, self.lens),
+                                                   gen).to(device)
+            self.pool = wl.draw_fp8_paged_pool(npages, Hkv, P, D, vgen, device=device)
+            self.ring = wl.draw_fp8_ring_pool(B, Hkv, W, D, vgen, device=device)
         d = lambda t: t.to(device).contiguous()
         self.q, self.k_new, self.v_new = d(self.inp.q), d(self.inp.k_new), d(self.inp.v_new)
         self.seq_lens, self.sinks = d(self.inp.seq_lens), d(self.inp.sinks)
@@ -211,9 +223,14 @@ class StepInputs:
         self.rope_cos = torch.from_numpy(cs).to(device)
         self.rope_sin = torch.from_numpy(sn).to(device)
 
+    def cache_tensors(self):
+        if self.kv == "bf16":
+            return [self.pool.k_cache, self.pool.v_cache, self.ring.k_cache, self.ring.v_cache]
+        return [getattr(c, a) for c in (self.pool, self.ring)
+                for a in ("k_cache", "vt_cache", "k_scale", "v_scale")]
+
     def nbytes(self):
-        ts = [self.pool.k_cache, self.pool.v_cache, self.ring.k_cache, self.ring.v_cache]
-        return sum(t.numel() * t.element_size() for t in ts)
+        return sum(t.numel() * t.element_size() for t in self.cache_tensors())
 
 
 def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=None):
@@ -221,10 +238,14 @@ def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=
     q = s.q if q is None else q
     k_new = s.k_new if k_new is None else k_new
     v_new = s.v_new if v_new is None else v_new
-    bt = s.pool.block_table if bt is None else bt
+    bt = s.block_table if bt is None else bt
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
-    if rope:
+    if s.kv == "fp8":
+        p = s.pool
+        da.decode_attn_paged_fp8(q, k_new, v_new, p.k_cache, p.vt_cache, p.k_scale, p.v_scale, bt,
+                                 sl, sinks, 0, s.inp.scale, s.out_full)
+    elif rope:
         da.decode_attn_paged_rope(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks,
                                   s.rope_cos, s.rope_sin, 0, s.inp.scale, s.out_full)
     else:
@@ -239,7 +260,11 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
     v_new = s.v_new if v_new is None else v_new
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
-    if rope:
+    if s.kv == "fp8":
+        r = s.ring
+        da.decode_attn_ring_fp8(q, k_new, v_new, r.k_cache, r.vt_cache, r.k_scale, r.v_scale, sl,
+                                sinks, s.inp.scale, s.out_ring)
+    elif rope:
         da.decode_attn_ring_rope(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
                                  s.rope_cos, s.rope_sin, s.inp.scale, s.out_ring)
     else:
@@ -247,11 +272,12 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
                             s.inp.scale, s.out_ring)
 
 
-def step_bytes(name, lens):
+def step_bytes(name, lens, kv="bf16"):
     from paged_decode_attention_kv_gb300 import workloads as wl
     c = wl.config(name)
     args = (c["Hq"], c["Hkv"], c["D"], c["page_size"], c["window"])
-    return algorithmic_bytes(lens, "paged_full", *args), algorithmic_bytes(lens, "ring", *args)
+    return (algorithmic_bytes(lens, "paged_full", *args, kv=kv),
+            algorithmic_bytes(lens, "ring", *args, kv=kv))
 
 
 # ---------------------------------------------------------------- the CPU oracle on a sample
@@ -263,10 +289,15 @@ def oracle_sample(name, s: "StepInputs", budget_s):
     from paged_decode_attention_kv_gb300 import workloads as wl
     c = s.cfg
     Hq, P, W = c["Hq"], c["page_size"], c["window"]
-    kp, vp = wl.bits(s.pool.k_cache), wl.bits(s.pool.v_cache)
-    rk, rv = wl.bits(s.ring.k_cache), wl.bits(s.ring.v_cache)
+    if s.kv == "bf16":
+        kp, vp = wl.bits(s.pool.k_cache), wl.bits(s.pool.v_cache)
+        rk, rv = wl.bits(s.ring.k_cache), wl.bits(s.ring.v_cache)
+    else:
+        host = lambda p: oracle.Fp8Cache(*[t.cpu().numpy() for t in
+                                           (p.k_cache, p.vt_cache, p.k_scale, p.v_scale)])
+        pool8, ring8 = host(s.pool), host(s.ring)
     q, kn, vn = wl.bits(s.inp.q), wl.bits(s.inp.k_new), wl.bits(s.inp.v_new)
-    bt = s.pool.block_table.cpu().numpy()
+    bt = s.block_table.cpu().numpy()
     lens = np.asarray(s.lens, np.int32)
     sinks = s.inp.sinks.numpy()
     cores = oracle.default_threads()
@@ -277,7 +308,12 @@ def oracle_sample(name, s: "StepInputs", budget_s):
         for b in order:
             items = [(b, h) for h in range(Hq)]
             t0 = time.perf_counter()
-            if getattr(s, "rope", False):
+            if s.kv == "fp8":
+                oracle.decode_paged_fp8(q, kn, vn, pool8, bt, lens, sinks, 0, s.inp.scale,
+                                        items=items, nthreads=cores)
+                oracle.decode_ring_fp8(q, kn, vn, ring8, lens, sinks, W, s.inp.scale,
+                                       items=items, nthreads=cores)
+            elif getattr(s, "rope", False):
                 cs, sn = s.rope_cos.cpu().numpy(), s.rope_sin.cpu().numpy()
                 oracle.decode_paged_rope(q, kn, vn, kp, vp, bt, lens, sinks, cs, sn, 0,
                                          s.inp.scale, P, items=items, nthreads=cores)
@@ -289,7 +325,7 @@ def oracle_sample(name, s: "StepInputs", budget_s):
                 oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
                                    nthreads=cores)
             elapsed += time.perf_counter() - t0
-            pb, rb = step_bytes(name, [int(lens[b])])
+            pb, rb = step_bytes(name, [int(lens[b])], s.kv)
             done_bytes += pb + rb
             seqs += 1
             if elapsed >= budget_s:
@@ -307,7 +343,7 @@ def run_reference(args, rank, world):
         return None
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    s = StepInputs(args.workload, device, batch_limit=args.batch_limit)
+    s = StepInputs(args.workload, device, batch_limit=args.batch_limit, kv=args.kv)
     s.rope = args.rope
     # each step is a bounded sample: calibrate so that warmup+steps fit ~90 s
     per_step = max(0.02, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
@@ -319,7 +355,7 @@ def run_reference(args, rank, world):
         vals.append(v)
         descs.append(desc)
     value = statistics.median(vals)
-    pbytes, rbytes = step_bytes(args.workload, s.lens)
+    pbytes, rbytes = step_bytes(args.workload, s.lens, args.kv)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -342,6 +378,7 @@ def workload_config(name, s):
             "max_len": max(lens) if lens else 0,
             "layers_per_step": ["paged full attention", f"ring window {c['window']}"],
             "rope": bool(getattr(s, "rope", False)),
+            "kv_cache": "bf16" if s.kv == "bf16" else "fp8 e4m3 codes + per-token fp32 scales",
             "parallelism": "replicas", **({"note": c["workload_note"]} if "workload_note" in c else {})}
 
 
@@ -356,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
     # their own caches); more sets rotate when one step's inputs would fit in L2
     def make_set(k):
         return [StepInputs(args.workload, dev, seed_offset=k * 10007 + 101 * li,
-                           batch_limit=args.batch_limit) for li in range(args.layers)]
+                           batch_limit=args.batch_limit, kv=args.kv) for li in range(args.layers)]
     sets = [make_set(0)]
     first = sets[0][0]
     first.rope = args.rope
@@ -366,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
     cfg = first.cfg
     B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
     da.decode_attn_reserve(da.decode_attn_workspace_bytes(B, Hq, Hkv, D))
-    pbytes, rbytes = step_bytes(args.workload, first.lens)
+    pbytes, rbytes = step_bytes(args.workload, first.lens, args.kv)
     pbytes_call, rbytes_call = pbytes, rbytes
     pbytes, rbytes = pbytes * args.layers, rbytes * args.layers
     if args.batch_limit is not None:
@@ -442,11 +479,12 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_hbm_peak()
     nominal = nominal_hbm_peak()
     achieved = pbytes_call / (paged_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload, "paged")
+    traffic = recorded_traffic(args.workload, "paged" if args.kv == "bf16" else "paged_fp8")
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.kv == "bf16" else "fp8 e4m3 cache, f16 mma, fp32 softmax",
         "data": "synthetic",
         "config": dict(workload_config(args.workload, first),
                        l2=("inputs larger than L2: %.0f MB per step" % (set_bytes / 1e6))
@@ -459,7 +497,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": traffic, "kernel": "decode_attn_kernel (paged, full attention)",
+                     "traffic": traffic,
+                     "kernel": "decode_attn_kernel (paged, full attention%s)" % (
+                         "" if args.kv == "bf16" else ", fp8 cache"),
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
@@ -481,7 +521,7 @@ def run_e2e(args, s, step_bytes_total, dev):
     import torch
     import paged_decode_attention_kv_gb300 as da
     host = {k: getattr(s, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "seq_lens", "sinks")}
-    host["block_table"] = s.pool.block_table.cpu().pin_memory()
+    host["block_table"] = s.block_table.cpu().pin_memory()
     outs = [torch.empty(s.out_full.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     dst = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -522,11 +562,15 @@ def main():
                     help="capture the whole step once as a CUDA graph and time its replays")
     ap.add_argument("--rope", action="store_true",
                     help="fuse the rotary embedding of position L-1 (q and the new key) into both calls")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="cache storage: bf16, or e4m3 codes with per-token scales (quantised on append)")
     ap.add_argument("--batch-limit", type=int, default=None,
                     help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.kv == "fp8" and args.rope:
+        ap.error("--rope is not available with --kv fp8")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

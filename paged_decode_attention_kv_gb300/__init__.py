@@ -28,7 +28,7 @@ __all__ = [
     "decode_attn_workspace_bytes", "decode_attn_reserve", "decode_attn_device_status",
     "decode_attn_error_string", "library_path", "load_library",
     "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT", "DA_STATUS_BAD_POSITION",
-    "decode_attn_paged_rope", "decode_attn_ring_rope",
+    "decode_attn_paged_rope", "decode_attn_ring_rope", "decode_attn_paged_fp8", "decode_attn_ring_fp8",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +85,10 @@ def load_library():
                                            vp]
     lib.decode_attn_ring_rope.argtypes = [vp, vp, vp, vp, vp, i32p, f32p, f32p, f32p, c_int, c_int,
                                           c_float, vp, da_shape, vp]
+    lib.decode_attn_paged_fp8.argtypes = [vp, vp, vp, vp, vp, f32p, f32p, i32p, i32p, f32p, c_int,
+                                          c_float, vp, da_shape, c_int, c_int, c_int, c_int, vp]
+    lib.decode_attn_ring_fp8.argtypes = [vp, vp, vp, vp, vp, f32p, f32p, i32p, f32p, c_int, c_float,
+                                         vp, da_shape, vp]
     lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
@@ -92,7 +96,8 @@ def load_library():
     lib.decode_attn_error_string.argtypes = [c_int]
     lib.decode_attn_error_string.restype = ctypes.c_char_p
     for fn in (lib.decode_attn_paged, lib.decode_attn_ring, lib.kv_append, lib.decode_attn_reserve,
-               lib.decode_attn_device_status, lib.decode_attn_paged_rope, lib.decode_attn_ring_rope):
+               lib.decode_attn_device_status, lib.decode_attn_paged_rope, lib.decode_attn_ring_rope,
+               lib.decode_attn_paged_fp8, lib.decode_attn_ring_fp8):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -178,6 +183,35 @@ def decode_attn_ring_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, ro
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
         _ptr(sinks), _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]), int(W), float(scale),
         _ptr(out), _shape(q, Hkv), _stream(stream)))
+    return out
+
+
+def decode_attn_paged_fp8(q, k_new, v_new, k_cache, vt_cache, k_scale, v_scale, block_table,
+                          seq_lens, sinks, window, scale, out, max_seq_len=None, stream=None):
+    """decode_attn_paged over an fp8 cache: k_cache [num_pages, Hkv, 16, 64] and vt_cache
+    [num_pages, Hkv, 64, 16] uint8 e4m3 codes, k_scale/v_scale [num_pages, Hkv, 16] fp32."""
+    num_pages, Hkv, P, _ = k_cache.shape
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * P
+    lib = load_library()
+    _check(lib.decode_attn_paged_fp8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(vt_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(sinks), int(window), float(scale),
+        _ptr(out), _shape(q, Hkv), P, max_pages, num_pages, int(max_seq_len), _stream(stream)))
+    return out
+
+
+def decode_attn_ring_fp8(q, k_new, v_new, k_cache, vt_cache, k_scale, v_scale, seq_lens, sinks,
+                         scale, out, stream=None):
+    """decode_attn_ring over an fp8 ring: k_cache [B, Hkv, W, 64], vt_cache [B, Hkv, 64, W]
+    uint8 e4m3 codes, k_scale/v_scale [B, Hkv, W] fp32; W % 16 == 0."""
+    B, Hkv, W, _ = k_cache.shape
+    lib = load_library()
+    _check(lib.decode_attn_ring_fp8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(vt_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(seq_lens), _ptr(sinks), int(W), float(scale), _ptr(out),
+        _shape(q, Hkv), _stream(stream)))
     return out
 
 

@@ -32,6 +32,8 @@
 //     ldmatrix reads are free of bank conflicts.
 #include <cuda.h>  // CUtensorMap and its enums (types only; resolved at run time)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -57,9 +59,10 @@ constexpr int kThreads = kWarps * 32;
 #ifndef DA_STAGES_G16
 #define DA_STAGES_G16 4
 #endif
-template <int NT, bool ROPE>
+template <int NT, bool ROPE, bool KV8>
 __host__ __device__ constexpr int stages_for() {
-    return NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16;
+    // fp8 tiles are half the size: more of them in flight for the same bytes
+    return KV8 ? (NT == 1 ? 7 : 6) : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16);
 }
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
@@ -94,6 +97,8 @@ struct Params {
     const float *rope_cos;  // [max_position][D/2] fp32, or null: no rotary embedding
     const float *rope_sin;
     int max_position;
+    float *k_scale;  // fp8 caches: per-token fp32 scales of K and V, laid out like the token rows
+    float *v_scale;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -297,6 +302,16 @@ __device__ __forceinline__ void state_reduce_l(SegState<NT> &s) {
         }
 }
 
+template <int NT>
+__device__ __forceinline__ void state_scale_acc(SegState<NT> &s, float f) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) s.acc[n][mt][k] *= f;
+}
+
 // Slot in shared memory holding one warp's partial state of a segment.
 template <int NT>
 struct Slot {
@@ -356,16 +371,58 @@ __device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&s
     }
 }
 
+// ---- fp8 (e4m3) helpers
+// Four e4m3 codes (bytes 0..3 of w) to two fp16 pairs: bytes 0,1 -> lo, bytes 2,3 -> hi
+// (lower byte to the lower half). Exact: every e4m3 value is an fp16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    const float2 f = unpack_bf16(v);
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two values to e4m3 codes (nearest, ties to even, saturating at +-448), low byte first.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Token held by row g (< 8) of a 16-token fp8 K tile in the QK product; row g + 8 holds
+// that token + 2. The permutation makes the transposed probabilities of each lane
+// cover the four consecutive tokens 4t..4t+3 that one 32-bit word of a V^T row holds.
+__device__ __forceinline__ int fp8_row_token(int g) { return 4 * (g >> 1) + (g & 1); }
+
 // Shared-memory layout of decode_attn_kernel<NT, ., ROPE>: byte offsets from a 1024-byte
 // aligned base. The kernel carves its buffers from these offsets and the launch
 // requests `bytes`, so the two cannot drift apart.
-template <int NT, bool ROPE>
+template <int NT, bool ROPE, bool KV8>
 struct SmemLayout {
-    static constexpr int kStages = stages_for<NT, ROPE>();
+    static constexpr int kStages = stages_for<NT, ROPE, KV8>();
     static constexpr int GP = NT * 8;
-    // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin rows
-    static constexpr int kQBytes = GP * kD * 2 + 2 * kD * 2 + (ROPE ? 2 * (kD / 2) * 4 : 0);
-    static constexpr int kWarpTileBytes = kStages * 2 * kTileBytes;  // K and V tiles of one warp
+    static constexpr int kTile = KV8 ? kTileBytes / 2 : kTileBytes;  // one K (or V) tile
+    // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin
+    // rows, the fp8 tile's K and V scale rows
+    static constexpr int kRopeOff = GP * kD * 2 + 2 * kD * 2;
+    static constexpr int kScaleOff = kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
+    static constexpr int kQBytes = kScaleOff + (KV8 ? 2 * kPage * 4 : 0);
+    static constexpr int kWarpTileBytes = kStages * 2 * kTile;  // K and V tiles of one warp
     static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8;
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
     static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
@@ -374,17 +431,18 @@ struct SmemLayout {
     static constexpr size_t sinks = ints + static_cast<size_t>(kInts) * 4;
     static constexpr size_t end = sinks + static_cast<size_t>(kMaxQHeads) * 4;
     static constexpr size_t bytes = 1024 + end;  // plus the slack to align the base
-    static_assert(kTileBytes % 1024 == 0 && kWarpTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
+    static_assert(kTile % 1024 == 0 && kWarpTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
     static_assert(kQBytes % 16 == 0 && meta % 16 == 0, "bulk copies and int4 need 16-byte alignment");
     static_assert(bytes <= kMaxSmem, "shared memory budget");
 };
 
 // ------------------------------------------------------------------ the kernel
-template <int NT, bool RING, bool ROPE>
+template <int NT, bool RING, bool ROPE, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
-    using Lay = SmemLayout<NT, ROPE>;
+    using Lay = SmemLayout<NT, ROPE, KV8>;
+    constexpr int kTileB = Lay::kTile;
     constexpr int kStages = Lay::kStages;
     constexpr int GP = Lay::GP;
     constexpr int kQBytes = Lay::kQBytes;
@@ -489,8 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint8_t *wbase = smem + warp * kWarpBytes;
     const uint32_t wbase_s = smem_addr(wbase);
-    auto k_tile = [&](int st) { return wbase_s + st * kTileBytes; };
-    auto v_tile = [&](int st) { return wbase_s + (kStages + st) * kTileBytes; };
+    auto k_tile = [&](int st) { return wbase_s + st * kTileB; };
+    auto v_tile = [&](int st) { return wbase_s + (kStages + st) * kTileB; };
     uint8_t *wq = qarea + warp * kStages * kQBytes;
     const uint32_t wq_s = smem_addr(wq);
     auto q_tile = [&](int st) { return wq_s + st * kQBytes; };
@@ -560,13 +618,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = newseg && p.k_new != nullptr;
                 const bool rope = ROPE && newseg;
-                mbar_expect_tx(bar, 2 * kTileBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
-                                        (rope ? 4 * kD : 0));
+                mbar_expect_tx(bar, 2 * kTileB + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
+                                        (rope ? 4 * kD : 0) + (KV8 ? 2 * kPage * 4 : 0));
                 int c1, c2;
                 if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
                 else { c1 = 0; c2 = tp * Hkv + tg; }
                 tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
-                tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
+                if (KV8 && RING) tma_load_3d(v_tile(stg), &tmv, c1, 0, c2, bar, policy);  // V^T: cells inner
+                else tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
+                if constexpr (KV8) {  // the tile's per-token K and V scales
+                    size_t srow;
+                    if (RING) srow = (static_cast<size_t>(tb) * Hkv + tg) * p.window + tt * kPage;
+                    else srow = (static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg) * kPage;
+                    bulk_load(q_tile(stg) + Lay::kScaleOff, p.k_scale + srow, kPage * 4, bar);
+                    bulk_load(q_tile(stg) + Lay::kScaleOff + kPage * 4, p.v_scale + srow, kPage * 4, bar);
+                }
                 if (newseg)
                     bulk_load(q_tile(stg),
                               p.q + (static_cast<size_t>(tb) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
@@ -596,7 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sb = -1, sgk = -1;  // current segment (b, g)
         int seg_first_unit = 0, seg_end_unit = 0;
         int L = 0, lo = 0, ft = 0, nvalid = 0, app_tile = -1, app_row = 0;
-        uint32_t knew = 0, vnew = 0;
+        uint32_t knew = 0, vnew = 0;           // new token's k/v (bf16 pair, or 2 e4m3 codes)
+        float knew_scale = 1.f, vnew_scale = 1.f;  // fp8: their scales
         const bool do_append = p.k_new != nullptr;
 
         int i = 0;
@@ -612,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // close the previous segment
                 if (i > 0) {
                     state_reduce_l(st);
+                    if constexpr (KV8) state_scale_acc(st, 1.f / 256.f);
                     if (seg_first_unit < ua) {  // shared with earlier workers: keep for merge
                         head = st;
                         head_seg = sb * Hkv + sgk;
@@ -651,8 +719,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 4; ++ks) {
                         if (hq < p.G) {
                             const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + hq * kD * 2);
-                            qf[n][ks][0] = row[ks * 8 + (lane & 3)];
-                            qf[n][ks][1] = row[ks * 8 + 4 + (lane & 3)];
+                            if constexpr (KV8) {
+                                // fp16 operands; k-step ks takes d = 16t + 4ks .. +3, the bytes
+                                // one lane reads from an fp8 K row (see the QK product)
+                                qf[n][ks][0] = bf16x2_to_f16x2(row[8 * (lane & 3) + 2 * ks]);
+                                qf[n][ks][1] = bf16x2_to_f16x2(row[8 * (lane & 3) + 2 * ks + 1]);
+                            } else {
+                                qf[n][ks][0] = row[ks * 8 + (lane & 3)];
+                                qf[n][ks][1] = row[ks * 8 + 4 + (lane & 3)];
+                            }
                         } else {
                             qf[n][ks][0] = qf[n][ks][1] = 0u;
                         }
@@ -684,66 +759,148 @@ __global__ void __launch_bounds__(kThreads, 1)
                         knew = rope_half(knew, other, cr + d, sr + d, lane < 16);
                     }
                 }
+                if constexpr (KV8) {
+                    if (do_append) {  // quantise the new token: per row amax / 448, e4m3 codes
+                        const float2 kf = unpack_bf16(knew), vf = unpack_bf16(vnew);
+                        float ka = fmaxf(fabsf(kf.x), fabsf(kf.y)), va = fmaxf(fabsf(vf.x), fabsf(vf.y));
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) {
+                            ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, off));
+                            va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, off));
+                        }
+                        knew_scale = ka > 0.f ? __fdiv_rn(ka, 448.f) : 1.f;
+                        vnew_scale = va > 0.f ? __fdiv_rn(va, 448.f) : 1.f;
+                        knew = f32x2_to_e4m3x2(__fdiv_rn(kf.x, knew_scale), __fdiv_rn(kf.y, knew_scale));
+                        vnew = f32x2_to_e4m3x2(__fdiv_rn(vf.x, vnew_scale), __fdiv_rn(vf.y, vnew_scale));
+                    }
+                }
                 state_reset(st);
             }
 
             const uint32_t sK = k_tile(stg), sV = v_tile(stg);
-            uint8_t *gK = wbase + stg * kTileBytes;
-            uint8_t *gV = wbase + (kStages + stg) * kTileBytes;
+            uint8_t *gK = wbase + stg * kTileB;
+            uint8_t *gV = wbase + (kStages + stg) * kTileB;
 
             // fused append: this tile holds position p = L - 1
             if (do_append && tt == app_tile) {
-                const uint32_t off = app_row * 128 + ((((lane >> 2) ^ (app_row & 7))) << 4) + (lane & 3) * 4;
-                *reinterpret_cast<uint32_t *>(gK + off) = knew;
-                *reinterpret_cast<uint32_t *>(gV + off) = vnew;
-                size_t cell;
+                size_t slice, cell;  // (KV head) slice of the cache and the token's cell in it
                 bool ok = true;
                 if (RING) {
-                    cell = (static_cast<size_t>(sb) * Hkv + sgk) * p.window + (tt * kPage + app_row);
+                    slice = static_cast<size_t>(sb) * Hkv + sgk;
+                    cell = tt * kPage + app_row;
                 } else {
                     ok = tp >= 0;
-                    cell = (static_cast<size_t>(tp) * Hkv + sgk) * kPage + app_row;
+                    slice = static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + sgk;
+                    cell = app_row;
                 }
-                if (ok) {
-                    reinterpret_cast<uint32_t *>(p.k_cache + cell * kD)[lane] = knew;
-                    reinterpret_cast<uint32_t *>(p.v_cache + cell * kD)[lane] = vnew;
+                if constexpr (KV8) {
+                    // K row of codes, one column of the transposed V tile, both scales
+                    const int rows = RING ? p.window : kPage;
+                    *reinterpret_cast<uint16_t *>(gK + app_row * kD + 2 * lane) = static_cast<uint16_t>(knew);
+                    gV[(2 * lane) * kPage + app_row] = static_cast<uint8_t>(vnew);
+                    gV[(2 * lane + 1) * kPage + app_row] = static_cast<uint8_t>(vnew >> 8);
+                    float *ssr = reinterpret_cast<float *>(wq + stg * kQBytes + Lay::kScaleOff);
+                    if (lane == 0) {
+                        ssr[app_row] = knew_scale;
+                        ssr[kPage + app_row] = vnew_scale;
+                    }
+                    if (ok) {
+                        uint8_t *kc = reinterpret_cast<uint8_t *>(p.k_cache);
+                        uint8_t *vt = reinterpret_cast<uint8_t *>(p.v_cache);
+                        *reinterpret_cast<uint16_t *>(kc + (slice * rows + cell) * kD + 2 * lane) =
+                            static_cast<uint16_t>(knew);
+                        vt[slice * kD * rows + (2 * lane) * rows + cell] = static_cast<uint8_t>(vnew);
+                        vt[slice * kD * rows + (2 * lane + 1) * rows + cell] = static_cast<uint8_t>(vnew >> 8);
+                        if (lane == 0) {
+                            p.k_scale[slice * rows + cell] = knew_scale;
+                            p.v_scale[slice * rows + cell] = vnew_scale;
+                        }
+                    }
+                } else {
+                    const uint32_t off = app_row * 128 + ((((lane >> 2) ^ (app_row & 7))) << 4) + (lane & 3) * 4;
+                    *reinterpret_cast<uint32_t *>(gK + off) = knew;
+                    *reinterpret_cast<uint32_t *>(gV + off) = vnew;
+                    if (ok) {
+                        const size_t c = slice * (RING ? p.window : kPage) + cell;
+                        reinterpret_cast<uint32_t *>(p.k_cache + c * kD)[lane] = knew;
+                        reinterpret_cast<uint32_t *>(p.v_cache + c * kD)[lane] = vnew;
+                    }
                 }
                 __syncwarp();
             }
 
-            // token validity of this lane's rows
+            // token validity of this lane's rows (fp8 tiles: rows are permuted tokens)
             int t0, lo_v, hi_v;
             if (RING) { t0 = tt * kPage; lo_v = 0; hi_v = nvalid; }
             else { t0 = (ft + tt) * kPage; lo_v = lo; hi_v = L; }
             const bool partial = (t0 < lo_v) || (t0 + kPage > hi_v);
-            const int r0 = t0 + (lane >> 2);
+            const int row_tok = KV8 ? fp8_row_token(lane >> 2) : (lane >> 2);
+            const int r0 = t0 + row_tok;
+            const int r8 = r0 + (KV8 ? 2 : 8);
             const bool ok_lo = r0 >= lo_v && r0 < hi_v;
-            const bool ok_hi = (r0 + 8) >= lo_v && (r0 + 8) < hi_v;
+            const bool ok_hi = r8 >= lo_v && r8 < hi_v;
 
             // K fragments, and the V fragments too: they do not depend on the softmax, so
             // their shared-memory latency overlaps the QK products
             uint32_t ka[4][4], va[4][4];
+            float ks_lo = 1.f, ks_hi = 1.f, vs_lo = 1.f, vs_hi = 1.f;  // fp8 per-token scales
+            if constexpr (KV8) {
+                // K rows row_tok and row_tok + 2: bytes 16t..16t+15 (d), 4 per k-step
+                const uint4 klo = *reinterpret_cast<const uint4 *>(gK + row_tok * kD + 16 * (lane & 3));
+                const uint4 khi = *reinterpret_cast<const uint4 *>(gK + (row_tok + 2) * kD + 16 * (lane & 3));
+                const uint32_t wl[4] = {klo.x, klo.y, klo.z, klo.w}, wh[4] = {khi.x, khi.y, khi.z, khi.w};
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3]);
+                for (int ks = 0; ks < 4; ++ks) {
+                    e4m3x4_to_f16x2x2(wl[ks], ka[ks][0], ka[ks][2]);
+                    e4m3x4_to_f16x2x2(wh[ks], ka[ks][1], ka[ks][3]);
+                }
+                // V^T rows d and d + 8: tokens 4t..4t+3 in one word
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-                ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+                for (int mt = 0; mt < 4; ++mt) {
+                    const uint32_t vl = *reinterpret_cast<const uint32_t *>(gV + (16 * mt + (lane >> 2)) * kPage + 4 * (lane & 3));
+                    const uint32_t vh = *reinterpret_cast<const uint32_t *>(gV + (16 * mt + 8 + (lane >> 2)) * kPage + 4 * (lane & 3));
+                    e4m3x4_to_f16x2x2(vl, va[mt][0], va[mt][2]);
+                    e4m3x4_to_f16x2x2(vh, va[mt][1], va[mt][3]);
+                }
+                const float *ssr = reinterpret_cast<const float *>(wq + stg * kQBytes + Lay::kScaleOff);
+                ks_lo = ssr[row_tok];
+                ks_hi = ssr[row_tok + 2];
+                // V scales carry a factor 2^8 so that the fp16 probabilities stay normal;
+                // it is taken out when the segment closes
+                // (a row outside the attended range may hold a garbage scale: select 0)
+                vs_lo = ok_lo ? ssr[kPage + row_tok] * 256.f : 0.f;
+                vs_hi = ok_hi ? ssr[kPage + row_tok + 2] * 256.f : 0.f;
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3]);
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)
+                    ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+            }
             // S^T = K Q^T  (16 tokens x 8 heads per n-tile), as two independent MMA chains
             uint32_t pb[NT][2];
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_bf16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[n][0][0], qf[n][0][1]);
-                mma_bf16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[n][1][0], qf[n][1][1]);
-                mma_bf16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[n][2][0], qf[n][2][1]);
-                mma_bf16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[n][3][0], qf[n][3][1]);
+                if constexpr (KV8) {
+                    mma_f16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[n][0][0], qf[n][0][1]);
+                    mma_f16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[n][1][0], qf[n][1][1]);
+                    mma_f16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[n][2][0], qf[n][2][1]);
+                    mma_f16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[n][3][0], qf[n][3][1]);
+                } else {
+                    mma_bf16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[n][0][0], qf[n][0][1]);
+                    mma_bf16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[n][1][0], qf[n][1][1]);
+                    mma_bf16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[n][2][0], qf[n][2][1]);
+                    mma_bf16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[n][3][0], qf[n][3][1]);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) sc[k] += sd[k];
-                float s0 = ok_lo ? sc[0] * p.scale_log2 : -INFINITY;
-                float s1 = ok_lo ? sc[1] * p.scale_log2 : -INFINITY;
-                float s2 = ok_hi ? sc[2] * p.scale_log2 : -INFINITY;
-                float s3 = ok_hi ? sc[3] * p.scale_log2 : -INFINITY;
+                const float sl_lo = p.scale_log2 * ks_lo, sl_hi = p.scale_log2 * ks_hi;
+                float s0 = ok_lo ? sc[0] * sl_lo : -INFINITY;
+                float s1 = ok_lo ? sc[1] * sl_lo : -INFINITY;
+                float s2 = ok_hi ? sc[2] * sl_hi : -INFINITY;
+                float s3 = ok_hi ? sc[3] * sl_hi : -INFINITY;
                 float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
@@ -766,25 +923,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st.acc[n][mt][2] *= a0;
                     st.acc[n][mt][3] *= a1;
                 }
-                pb[n][0] = movmatrix_t(pack_bf16(p0, p1));  // tokens 2(lane%4)+{0,1}
-                pb[n][1] = movmatrix_t(pack_bf16(p2, p3));  // tokens 8+2(lane%4)+{0,1}
+                if constexpr (KV8) {  // probabilities times the tokens' V scales, fp16
+                    pb[n][0] = movmatrix_t(pack_f16(p0 * vs_lo, p1 * vs_lo));  // tokens 4t, 4t+1
+                    pb[n][1] = movmatrix_t(pack_f16(p2 * vs_hi, p3 * vs_hi));  // tokens 4t+2, 4t+3
+                } else {
+                    pb[n][0] = movmatrix_t(pack_bf16(p0, p1));  // tokens 2(lane%4)+{0,1}
+                    pb[n][1] = movmatrix_t(pack_bf16(p2, p3));  // tokens 8+2(lane%4)+{0,1}
+                }
             }
 
             // O^T += V^T P^T  (64 d x 8 heads per n-tile)
-            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
             if (partial) {
-                const int tv = t0 + (lane & 3) * 2;
-                vm0 = ((tv >= lo_v && tv < hi_v) ? 0x0000ffffu : 0u) |
-                      ((tv + 1 >= lo_v && tv + 1 < hi_v) ? 0xffff0000u : 0u);
-                vm1 = ((tv + 8 >= lo_v && tv + 8 < hi_v) ? 0x0000ffffu : 0u) |
-                      ((tv + 9 >= lo_v && tv + 9 < hi_v) ? 0xffff0000u : 0u);
+                // zero the V values of tokens outside the range (they may hold NaN): this
+                // lane's V^T fragment halves carry tokens 2t, 2t+1 / 2t+8, 2t+9 (bf16 tiles);
+                // 4t, 4t+1 / 4t+2, 4t+3 (fp8 tiles)
+                const int tv = t0 + (lane & 3) * (KV8 ? 4 : 2);
+                const int tw = tv + (KV8 ? 2 : 8);
+                const uint32_t vm0 = ((tv >= lo_v && tv < hi_v) ? 0x0000ffffu : 0u) |
+                                     ((tv + 1 >= lo_v && tv + 1 < hi_v) ? 0xffff0000u : 0u);
+                const uint32_t vm1 = ((tw >= lo_v && tw < hi_v) ? 0x0000ffffu : 0u) |
+                                     ((tw + 1 >= lo_v && tw + 1 < hi_v) ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    va[mt][0] &= vm0;
+                    va[mt][1] &= vm0;
+                    va[mt][2] &= vm1;
+                    va[mt][3] &= vm1;
+                }
             }
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
-                const uint32_t a0 = va[mt][0] & vm0, a1 = va[mt][1] & vm0;
-                const uint32_t a2 = va[mt][2] & vm1, a3 = va[mt][3] & vm1;
+                const uint32_t a0 = va[mt][0], a1 = va[mt][1];
+                const uint32_t a2 = va[mt][2], a3 = va[mt][3];
 #pragma unroll
-                for (int n = 0; n < NT; ++n) mma_bf16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+                for (int n = 0; n < NT; ++n) {
+                    if constexpr (KV8) mma_f16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+                    else mma_bf16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+                }
             }
 
             __syncwarp();
@@ -804,6 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // close the last segment
         state_reduce_l(st);
+        if constexpr (KV8) state_scale_acc(st, 1.f / 256.f);
         const bool last_shared = failed || seg_first_unit < ua || seg_end_unit > ue;
         if (last_shared) {
             tail_seg = sb * Hkv + sgk;
@@ -1067,16 +1243,38 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D map over a bf16 cache viewed as [slices][rows][64]; box = 16 rows x 64.
-bool encode_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
+// Kinds of cache views a tile is copied from:
+//   kMapBf16: bf16 [slices][rows][64], box 16 rows x 64, 128-byte swizzle (K and V tiles)
+//   kMapFp8K: e4m3 [slices][rows][64], box 16 rows x 64 bytes (fp8 K tiles)
+//   kMapFp8V: e4m3 [slices][64][rows], box 64 rows x 16 bytes (fp8 transposed V tiles)
+// rows = tokens per slice (16 per page, or the ring capacity).
+enum MapKind { kMapBf16 = 0, kMapFp8K = 1, kMapFp8V = 2 };
+
+bool encode_kv_map(CUtensorMap *map, void *base, int kind, uint64_t rows, uint64_t slices) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), rows, slices};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, rows * kD * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kPage), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (kind == kMapBf16) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), rows, slices};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, rows * kD * 2};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kPage), 1};
+        return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (kind == kMapFp8K) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), rows, slices};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), rows * kD};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kPage), 1};
+        return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const cuuint64_t dims[3] = {rows, static_cast<cuuint64_t>(kD), slices};
+    const cuuint64_t strides[2] = {rows, rows * kD};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kPage), static_cast<cuuint32_t>(kD), 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1084,6 +1282,7 @@ bool encode_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices)
 // address and the extents, so recent ones are kept.
 struct MapCacheEntry {
     void *base = nullptr;
+    int kind = 0;
     uint64_t rows = 0, slices = 0;
     CUtensorMap map;
 };
@@ -1092,19 +1291,20 @@ MapCacheEntry g_maps[kMapCache];
 int g_map_next = 0;
 std::mutex g_map_mu;
 
-bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices) {
+bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices, int kind = kMapBf16) {
     std::lock_guard<std::mutex> lk(g_map_mu);
     for (int i = 0; i < kMapCache; ++i) {
         const MapCacheEntry &e = g_maps[i];
-        if (e.base == base && e.rows == rows && e.slices == slices) {
+        if (e.base == base && e.kind == kind && e.rows == rows && e.slices == slices) {
             *map = e.map;
             return true;
         }
     }
-    if (!encode_kv_map(map, base, rows, slices)) return false;
+    if (!encode_kv_map(map, base, kind, rows, slices)) return false;
     MapCacheEntry &e = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % kMapCache;
     e.base = base;
+    e.kind = kind;
     e.rows = rows;
     e.slices = slices;
     e.map = *map;
@@ -1117,7 +1317,7 @@ struct DeviceState {
     void *ws = nullptr;
     size_t ws_bytes = 0;
     int sm_count = 0;
-    bool attr_set[8] = {false, false, false, false, false, false, false, false};
+    bool attr_set[16] = {};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -1182,12 +1382,12 @@ int check_shape(const da_shape &s) {
     return DA_OK;
 }
 
-template <int NT, bool RING, bool ROPE>
+template <int NT, bool RING, bool ROPE, bool KV8 = false>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
-    const size_t smem = SmemLayout<NT, ROPE>::bytes;
+    const size_t smem = SmemLayout<NT, ROPE, KV8>::bytes;
     const size_t smem_max = smem;
-    auto kern = decode_attn_kernel<NT, RING, ROPE>;
-    const int idx = (NT - 1) * 4 + (RING ? 2 : 0) + (ROPE ? 1 : 0);
+    auto kern = decode_attn_kernel<NT, RING, ROPE, KV8>;
+    const int idx = (NT - 1) * 8 + (RING ? 4 : 0) + (ROPE ? 2 : 0) + (KV8 ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
@@ -1233,7 +1433,9 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
                   const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
                   float scale, void *out, const da_shape &s, int page_size, int max_pages, int num_pages,
                   int max_seq_len, void *stream_v, const float *rope_cos = nullptr,
-                  const float *rope_sin = nullptr, int max_position = 0) {
+                  const float *rope_sin = nullptr, int max_position = 0, float *k_scale = nullptr,
+                  float *v_scale = nullptr) {
+    const bool kv8 = k_scale != nullptr;
     int rc = check_shape(s);
     if (rc != DA_OK) return rc;
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
@@ -1243,6 +1445,9 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
         return DA_ERR_INVALID_ARG;
     if (!(scale == scale)) return DA_ERR_INVALID_ARG;
     if ((rope_cos == nullptr) != (rope_sin == nullptr)) return DA_ERR_INVALID_ARG;
+    if (kv8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return DA_ERR_INVALID_ARG;
+    if (kv8 && rope_cos) return DA_ERR_UNSUPPORTED;
+    if (kv8 && ring && window % kPage != 0) return DA_ERR_UNSUPPORTED;
     if (rope_cos && (max_position <= 0 || !aligned16(rope_cos) || !aligned16(rope_sin))) return DA_ERR_INVALID_ARG;
     const int G = s.num_q_heads / s.num_kv_heads;
     if (ring) {
@@ -1282,6 +1487,8 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.rope_cos = rope_cos;
     prm.rope_sin = rope_sin;
     prm.max_position = max_position;
+    prm.k_scale = k_scale;
+    prm.v_scale = v_scale;
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
@@ -1289,9 +1496,17 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     const uint64_t rows = ring ? static_cast<uint64_t>(window) : static_cast<uint64_t>(kPage);
     const uint64_t slices = ring ? static_cast<uint64_t>(s.batch) * s.num_kv_heads
                                  : static_cast<uint64_t>(num_pages) * s.num_kv_heads;
-    if (!make_kv_map(&mk, k_cache, rows, slices) || !make_kv_map(&mv, v_cache, rows, slices)) {
+    if (!make_kv_map(&mk, k_cache, rows, slices, kv8 ? kMapFp8K : kMapBf16) ||
+        !make_kv_map(&mv, v_cache, rows, slices, kv8 ? kMapFp8V : kMapBf16)) {
         snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
         return DA_ERR_CUDA;
+    }
+    if (kv8) {
+        if (G <= 8)
+            return ring ? launch_attn<1, true, false, true>(mk, mv, prm, dev, stream)
+                        : launch_attn<1, false, false, true>(mk, mv, prm, dev, stream);
+        return ring ? launch_attn<2, true, false, true>(mk, mv, prm, dev, stream)
+                    : launch_attn<2, false, false, true>(mk, mv, prm, dev, stream);
     }
     if (rope_cos != nullptr) {
         if (G <= 8)
@@ -1390,6 +1605,8 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.rope_cos = nullptr;
     prm.rope_sin = nullptr;
     prm.max_position = 0;
+    prm.k_scale = nullptr;
+    prm.v_scale = nullptr;
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call
@@ -1447,6 +1664,24 @@ int decode_attn_ring_rope(const void *q, const void *k_new, const void *v_new, v
     if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
     return run_attention(true, q, k_new, v_new, k_cache, v_cache, nullptr, seq_lens, sinks, window, scale, out, s,
                          kPage, 0, 0, 0, stream, rope_cos, rope_sin, max_position);
+}
+
+int decode_attn_paged_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache, void *vt_cache,
+                          float *k_scale, float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                          const float *sinks, int window, float scale, void *out, da_shape s, int page_size,
+                          int max_pages_per_seq, int num_pages, int max_seq_len, void *stream) {
+    if (!k_scale || !v_scale) return DA_ERR_INVALID_ARG;
+    return run_attention(false, q, k_new, v_new, k_cache, vt_cache, block_table, seq_lens, sinks, window, scale,
+                         out, s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream, nullptr, nullptr, 0,
+                         k_scale, v_scale);
+}
+
+int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache, void *vt_cache,
+                         float *k_scale, float *v_scale, const int32_t *seq_lens, const float *sinks, int window,
+                         float scale, void *out, da_shape s, void *stream) {
+    if (!k_scale || !v_scale) return DA_ERR_INVALID_ARG;
+    return run_attention(true, q, k_new, v_new, k_cache, vt_cache, nullptr, seq_lens, sinks, window, scale, out,
+                         s, kPage, 0, 0, 0, stream, nullptr, nullptr, 0, k_scale, v_scale);
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, const int32_t *block_table,

@@ -11,7 +11,9 @@ query heads, 8 KV heads, head dim 64, page 16, window 128):
   * block tables hand out pages from a shuffled free list; unused table entries
     are -1;
   * pools are either fully random (benchmark) or NaN-filled (tests, where the
-    oracle writes the live tokens in and every dead cell stays NaN).
+    oracle writes the live tokens in and every dead cell stays NaN);
+  * fp8 pools (benchmark) hold uniform random finite e4m3 codes and per-token
+    scales uniform in [2/448, 3/448).
 """
 from __future__ import annotations
 
@@ -189,6 +191,46 @@ def draw_ring_pool(B, Hkv, W, D, gen, device="cpu", fill="randn") -> RingPool:
     else:
         raise ValueError(fill)
     return RingPool(k, v, W)
+
+
+@dataclass
+class Fp8Pool:
+    """fp8 (e4m3) cache arrays: K codes [.., Hkv, rows, D], V^T codes [.., Hkv, D, rows]
+    (uint8), per-token scales [.., Hkv, rows] fp32. `rows` is the page size (paged)
+    or the window (ring)."""
+    k_cache: torch.Tensor
+    vt_cache: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+
+
+def draw_fp8_codes(shape, gen, device="cpu") -> torch.Tensor:
+    """Uniform random e4m3 byte patterns with the two NaN patterns (0x7F, 0xFF)
+    redrawn as their neighbours 0x7E / 0xFE: every finite code, both signs."""
+    c = torch.randint(0, 256, shape, generator=gen, dtype=torch.int32, device=device)
+    c = torch.where((c & 0x7F) == 0x7F, c - 1, c)
+    return c.to(torch.uint8)
+
+
+def draw_fp8_scales(shape, gen, device="cpu") -> torch.Tensor:
+    """Per-token scales in [2/448, 3/448): what a row of N(0,1) values with an
+    absolute maximum of 2 to 3 would get."""
+    u = torch.rand(shape, generator=gen, dtype=torch.float32, device=device)
+    return (2.0 + u) / 448.0
+
+
+def draw_fp8_paged_pool(num_pages, Hkv, P, D, gen, device="cpu") -> Fp8Pool:
+    return Fp8Pool(draw_fp8_codes((num_pages, Hkv, P, D), gen, device),
+                   draw_fp8_codes((num_pages, Hkv, D, P), gen, device),
+                   draw_fp8_scales((num_pages, Hkv, P), gen, device),
+                   draw_fp8_scales((num_pages, Hkv, P), gen, device))
+
+
+def draw_fp8_ring_pool(B, Hkv, W, D, gen, device="cpu") -> Fp8Pool:
+    return Fp8Pool(draw_fp8_codes((B, Hkv, W, D), gen, device),
+                   draw_fp8_codes((B, Hkv, D, W), gen, device),
+                   draw_fp8_scales((B, Hkv, W), gen, device),
+                   draw_fp8_scales((B, Hkv, W), gen, device))
 
 
 def draw_history(B, Tmax, Hkv, D, gen, device="cpu"):

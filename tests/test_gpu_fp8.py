@@ -1,0 +1,140 @@
+"""GPU parity of the fp8 KV-cache path (decode_attn_paged_fp8 / _ring_fp8) against
+the fp64 oracle over the same e4m3 codes and scales: attention within
+4e-3 + 1e-2 |oracle|; the quantised append (K row, transposed V column, both
+scales) bit-exact; dead cells hold NaN codes and NaN scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_decode_attention_kv_gb300 as da
+from cases import make_case, paged_identity, shuffle_pages
+from paged_decode_attention_kv_gb300 import workloads as wl
+from test_gpu_decode import DEV, assert_close, dev, dev_bits, sample_items
+
+pytestmark = pytest.mark.gpu
+
+
+def pre(c):
+    return np.maximum(c.lens - 1, 0)
+
+
+def to_dev(cache):
+    return [torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (cache.k, cache.vt, cache.ks, cache.vs)]
+
+
+def from_dev(ts):
+    return oracle.Fp8Cache(*[t.cpu().numpy() for t in ts])
+
+
+def check_paged_fp8(c, window, seed, fused=True):
+    kp, vp, bt = paged_identity(c, c.lens if not fused else pre(c))
+    kp, vp, bt = shuffle_pages(kp, vp, bt, seed, spare=4)
+    blank = oracle.Fp8Cache.empty_paged(kp.shape[0], c.Hkv, 16, c.D)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, c.lens if not fused else pre(c), blank,
+                               block_table=bt)
+    kc, vt, ks, vs = to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_paged_fp8(dev_bits(c.q), dev_bits(c.k_new) if fused else None,
+                             dev_bits(c.v_new) if fused else None, kc, vt, ks, vs, dev(bt),
+                             dev(c.lens), dev(c.sinks), window, c.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_paged_fp8(c.q, c.k_new if fused else None, c.v_new if fused else None,
+                                  cache, bt, c.lens, c.sinks, window, c.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"paged fp8 window={window}")
+    got = from_dev((kc, vt, ks, vs))
+    want = oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, block_table=bt) if fused else cache
+    np.testing.assert_array_equal(got.k, want.k)
+    np.testing.assert_array_equal(got.vt, want.vt)
+    np.testing.assert_array_equal(got.ks.view(np.uint32), want.ks.view(np.uint32))
+    np.testing.assert_array_equal(got.vs.view(np.uint32), want.vs.view(np.uint32))
+
+
+EDGE = [1, 2, 15, 16, 17, 31, 33, 100, 257, 1000]
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (8, 8), (16, 1), (32, 4)])
+@pytest.mark.parametrize("window", [0, 7, 100])
+def test_paged_fp8_matches_oracle(Hq, Hkv, window):
+    c = make_case(700 + Hq + Hkv + window, len(EDGE), Hq, Hkv, 64, EDGE)
+    check_paged_fp8(c, window, seed=window + 1)
+
+
+def test_paged_fp8_without_append_and_long_sequences():
+    c = make_case(720, 3, 64, 8, 64, [40, 5000, 12000])
+    check_paged_fp8(c, 0, seed=3, fused=False)
+    check_paged_fp8(c, 0, seed=4, fused=True)
+
+
+@pytest.mark.parametrize("W", [16, 128])
+def test_ring_fp8_matches_oracle(W):
+    lens = [1, 15, 16, 17, W - 1, W, W + 1, 3 * W + 5, 0]
+    c = make_case(730 + W, len(lens), 64, 8, 64, lens)
+    blank = oracle.Fp8Cache.empty_ring(c.B, c.Hkv, W, c.D)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c), blank, window=W)
+    kc, vt, ks, vs = to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_ring_fp8(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kc, vt, ks, vs,
+                            dev(c.lens), dev(c.sinks), c.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_ring_fp8(c.q, c.k_new, c.v_new, cache, c.lens, c.sinks, W, c.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"ring fp8 W={W}")
+    got = from_dev((kc, vt, ks, vs))
+    want = oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, window=W)
+    np.testing.assert_array_equal(got.k, want.k)
+    np.testing.assert_array_equal(got.vt, want.vt)
+    np.testing.assert_array_equal(got.ks.view(np.uint32), want.ks.view(np.uint32))
+    np.testing.assert_array_equal(got.vs.view(np.uint32), want.vs.view(np.uint32))
+
+
+def test_paged_fp8_inactive_slots():
+    c = make_case(740, 6, 64, 8, 64, [0, 50, 0, 0, 17, 0])
+    check_paged_fp8(c, 0, seed=5)
+    check_paged_fp8(c, 128, seed=6)
+    c0 = make_case(741, 3, 64, 8, 64, [0, 0, 0])
+    check_paged_fp8(c0, 0, seed=7)
+
+
+def test_paged_fp8_many_segments_across_ctas():
+    rng = np.random.default_rng(9)
+    lens = list(rng.integers(1, 70, size=200)) + [3000, 700, 1]
+    c = make_case(742, len(lens), 64, 8, 64, lens)
+    check_paged_fp8(c, 0, seed=8)
+
+
+@pytest.mark.parametrize("name", ["b64", "long1"])
+def test_full_size_fp8(name):
+    """Benchmark-size fp8 pools of random codes and scales; sampled heads against the
+    oracle, the appended rows and scales bit-exact."""
+    cfg = wl.config(name)
+    lens = wl.seq_lens(name)
+    gen = wl.cpu_generator(cfg["seed"])
+    vgen = torch.Generator(device=DEV)
+    vgen.manual_seed(cfg["seed"])
+    B, Hq, Hkv, D, P = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["page_size"]
+    inp = wl.draw_decode_inputs(B, Hq, Hkv, D, lens, gen)
+    npages = wl.pool_size(name, lens)
+    bt = wl.draw_block_table(lens, P, npages, wl.max_pages_per_seq(name, lens), gen)
+    pool = wl.draw_fp8_paged_pool(npages, Hkv, P, D, vgen, device=DEV)
+    before = oracle.Fp8Cache(*[t.cpu().numpy() for t in (pool.k_cache, pool.vt_cache,
+                                                         pool.k_scale, pool.v_scale)])
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
+    sl = np.asarray(lens, np.int32)
+    da.decode_attn_paged_fp8(dev(inp.q), dev(inp.k_new), dev(inp.v_new), pool.k_cache,
+                             pool.vt_cache, pool.k_scale, pool.v_scale, dev(bt), dev(sl),
+                             dev(inp.sinks), 0, inp.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    items = sample_items(lens, Hq, 32, 13)
+    ref = oracle.decode_paged_fp8(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), before,
+                                  bt.numpy(), sl, inp.sinks.numpy(), 0, inp.scale, items=items)
+    got = out.double().cpu().numpy()
+    assert_close(np.stack([got[b, h] for b, h in items]), ref, f"{name} paged fp8")
+    want = oracle.kv_append_fp8(wl.bits(inp.k_new), wl.bits(inp.v_new), before, sl,
+                                block_table=bt.numpy())
+    after = from_dev((pool.k_cache, pool.vt_cache, pool.k_scale, pool.v_scale))
+    assert np.array_equal(after.k, want.k) and np.array_equal(after.vt, want.vt)
+    assert np.array_equal(after.ks.view(np.uint32), want.ks.view(np.uint32))
+    assert np.array_equal(after.vs.view(np.uint32), want.vs.view(np.uint32))
