@@ -226,8 +226,7 @@ class StepInputs:
     def cache_tensors(self):
         if self.kv == "bf16":
             return [self.pool.k_cache, self.pool.v_cache, self.ring.k_cache, self.ring.v_cache]
-        return [getattr(c, a) for c in (self.pool, self.ring)
-                for a in ("k_cache", "vt_cache", "k_scale", "v_scale")]
+        return [self.pool, self.ring]
 
     def nbytes(self):
         return sum(t.numel() * t.element_size() for t in self.cache_tensors())
@@ -242,9 +241,7 @@ def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
     if s.kv == "fp8":
-        p = s.pool
-        da.decode_attn_paged_fp8(q, k_new, v_new, p.k_cache, p.vt_cache, p.k_scale, p.v_scale, bt,
-                                 sl, sinks, 0, s.inp.scale, s.out_full)
+        da.decode_attn_paged_fp8(q, k_new, v_new, s.pool, bt, sl, sinks, 0, s.inp.scale, s.out_full)
     elif rope:
         da.decode_attn_paged_rope(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks,
                                   s.rope_cos, s.rope_sin, 0, s.inp.scale, s.out_full)
@@ -261,9 +258,7 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
     if s.kv == "fp8":
-        r = s.ring
-        da.decode_attn_ring_fp8(q, k_new, v_new, r.k_cache, r.vt_cache, r.k_scale, r.v_scale, sl,
-                                sinks, s.inp.scale, s.out_ring)
+        da.decode_attn_ring_fp8(q, k_new, v_new, s.ring, sl, sinks, s.inp.scale, s.out_ring)
     elif rope:
         da.decode_attn_ring_rope(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
                                  s.rope_cos, s.rope_sin, s.inp.scale, s.out_ring)
@@ -293,9 +288,7 @@ def oracle_sample(name, s: "StepInputs", budget_s):
         kp, vp = wl.bits(s.pool.k_cache), wl.bits(s.pool.v_cache)
         rk, rv = wl.bits(s.ring.k_cache), wl.bits(s.ring.v_cache)
     else:
-        host = lambda p: oracle.Fp8Cache(*[t.cpu().numpy() for t in
-                                           (p.k_cache, p.vt_cache, p.k_scale, p.v_scale)])
-        pool8, ring8 = host(s.pool), host(s.ring)
+        pool8, ring8 = oracle.Fp8Cache(s.pool.cpu().numpy()), oracle.Fp8Cache(s.ring.cpu().numpy())
     q, kn, vn = wl.bits(s.inp.q), wl.bits(s.inp.k_new), wl.bits(s.inp.v_new)
     bt = s.block_table.cpu().numpy()
     lens = np.asarray(s.lens, np.int32)

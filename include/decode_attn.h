@@ -150,30 +150,36 @@ DA_API int decode_attn_ring_rope(const void *q, const void *k_new, const void *v
 
 /*
  * decode_attn_paged_fp8 / decode_attn_ring_fp8 -- the same decode step over an fp8 KV
- * cache (half the bytes of bf16 per cached token). The pages only name quantisation; the
+ * cache (17/32 of the bytes of bf16 per cached token). The pages only name quantisation; the
  * format here: every cached K or V row of one token and KV head is 64 OCP e4m3 codes
  * (FN variant: no infinities, largest finite 448) and one fp32 scale; its value is
- * e4m3(code) * scale.
- *   paged: k_cache  [num_pages, Hkv, 16, 64] e4m3 codes (K rows)
- *          vt_cache [num_pages, Hkv, 64, 16] e4m3 codes (V stored transposed per page)
- *          k_scale, v_scale [num_pages, Hkv, 16] fp32 (one per token and head)
- *   ring:  k_cache [B, Hkv, W, 64], vt_cache [B, Hkv, 64, W], scales [B, Hkv, W]; W % 16 == 0
+ * e4m3(code) * scale. The cache is an array of 2176-byte blocks, one per 16 tokens of one
+ * KV head, each holding (byte offsets):
+ *      0  K codes [16][64]      (row t = token t of the block)
+ *   1024  V codes [64][16]      (transposed: row d holds the 16 tokens' element d)
+ *   2048  K scales [16] fp32
+ *   2112  V scales [16] fp32
+ *   paged: kv_cache [num_pages, Hkv, 2176] bytes; block (page, g) holds the page's tokens.
+ *   ring:  kv_cache [B, Hkv, W / 16, 2176] bytes; cell c = p % W of (b, g) is token c % 16
+ *          of block c / 16; W % 16 == 0.
+ * One block is one contiguous copy. kv_cache must be 16-byte aligned; it is read, and the
+ * new token's bytes written, in place.
  * The new token is quantised when it is appended: scale = max_d |x_d| / 448 in fp32 (1 when
  * the row is all zero), code_d = the e4m3 value nearest to x_d / scale (fp32 division),
  * ties to even, saturating at +-448; its K row, V column and both scales are written.
  * Scores and the PV product run in fp16 on tensor cores: |q| must stay below 65504.
- * No rotary embedding on this path yet. Other arguments as in decode_attn_paged / _ring.
+ * No rotary embedding on this path yet (DA_ERR_UNSUPPORTED). Other arguments, the status
+ * and the error behaviour as in decode_attn_paged / _ring.
  */
 DA_API int decode_attn_paged_fp8(const void *q, const void *k_new, const void *v_new,
-                                 void *k_cache, void *vt_cache, float *k_scale, float *v_scale,
-                                 const int32_t *block_table, const int32_t *seq_lens,
-                                 const float *sinks, int window, float scale, void *out, da_shape s,
-                                 int page_size, int max_pages_per_seq, int num_pages,
-                                 int max_seq_len, void *stream);
+                                 void *kv_cache, const int32_t *block_table,
+                                 const int32_t *seq_lens, const float *sinks, int window,
+                                 float scale, void *out, da_shape s, int page_size,
+                                 int max_pages_per_seq, int num_pages, int max_seq_len,
+                                 void *stream);
 DA_API int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_new,
-                                void *k_cache, void *vt_cache, float *k_scale, float *v_scale,
-                                const int32_t *seq_lens, const float *sinks, int window,
-                                float scale, void *out, da_shape s, void *stream);
+                                void *kv_cache, const int32_t *seq_lens, const float *sinks,
+                                int window, float scale, void *out, da_shape s, void *stream);
 
 /*
  * kv_append -- the append alone: bit-copies k_new/v_new [B, Hkv, D] of every

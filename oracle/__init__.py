@@ -69,17 +69,16 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [_f32p, c_int, _u8p]
         lib.oracle_quantise_rows.argtypes = [_u16p, c_int, c_int, _u8p, _f32p]
         lib.oracle_decode_paged_fp8.argtypes = [
-            _u16p, _u16p, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, _i32p, _f32p, c_int, c_double,
+            _u16p, _u16p, _u16p, _u8p, _i32p, _i32p, _f32p, c_int, c_double,
             _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
         lib.oracle_decode_ring_fp8.argtypes = [
-            _u16p, _u16p, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, _f32p, c_int, c_double, _f64p,
+            _u16p, _u16p, _u16p, _u8p, _i32p, _f32p, c_int, c_double, _f64p,
             c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
         lib.oracle_kv_append_fp8.argtypes = [
-            _u16p, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, _i32p, c_int, c_int, c_int, c_int, c_int,
-            c_int, c_int]
+            _u16p, _u16p, _u8p, _i32p, _i32p, c_int, c_int, c_int, c_int, c_int, c_int, c_int]
         lib.oracle_scatter_fp8.argtypes = [
-            _u16p, _u16p, _i32p, c_int, _i32p, c_int, _u8p, _u8p, _f32p, _f32p, c_int, c_int, c_int,
-            c_int, c_int, c_int]
+            _u16p, _u16p, _i32p, c_int, _i32p, c_int, _u8p, c_int, c_int, c_int, c_int, c_int,
+            c_int]
         for name in _FUNCS:
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -383,30 +382,68 @@ def quantise_rows(rows):
 
 
 class Fp8Cache:
-    """fp8 cache arrays: K codes, V^T codes, K scales, V scales (numpy)."""
+    """An fp8 cache: numpy uint8 blocks [..., 2*P*D + 8*P], one per P = 16 tokens of one KV
+    head (paged: [num_pages, Hkv, bytes]; ring of capacity W: [B, Hkv, W / P, bytes]), each
+    K codes [P][D], V codes transposed [D][P], K scales [P] and V scales [P] (fp32). The
+    properties k, vt, ks, vs are views of those parts."""
 
-    def __init__(self, k, vt, ks, vs):
-        self.k, self.vt, self.ks, self.vs = k, vt, ks, vs
+    def __init__(self, blocks, P=16, D=64):
+        assert blocks.dtype == np.uint8 and blocks.shape[-1] == 2 * P * D + 8 * P
+        self.blocks, self.P, self.D = blocks, P, D
+
+    @property
+    def k(self):
+        P, D = self.P, self.D
+        return self.blocks[..., :P * D].reshape(self.blocks.shape[:-1] + (P, D))
+
+    @property
+    def vt(self):
+        P, D = self.P, self.D
+        return self.blocks[..., P * D:2 * P * D].reshape(self.blocks.shape[:-1] + (D, P))
+
+    @property
+    def ks(self):
+        o = 2 * self.P * self.D
+        return self.blocks[..., o:o + 4 * self.P].view(np.float32)
+
+    @property
+    def vs(self):
+        o = 2 * self.P * self.D + 4 * self.P
+        return self.blocks[..., o:o + 4 * self.P].view(np.float32)
+
+    @staticmethod
+    def _filled(lead, P, D, fill_code, fill_scale):
+        c = Fp8Cache(np.full(tuple(lead) + (2 * P * D + 8 * P,), fill_code, np.uint8), P, D)
+        c.ks[...] = fill_scale
+        c.vs[...] = fill_scale
+        return c
 
     @staticmethod
     def empty_paged(num_pages, Hkv, P, D, fill_code=0x7F, fill_scale=np.nan):
-        return Fp8Cache(np.full((num_pages, Hkv, P, D), fill_code, np.uint8),
-                        np.full((num_pages, Hkv, D, P), fill_code, np.uint8),
-                        np.full((num_pages, Hkv, P), fill_scale, np.float32),
-                        np.full((num_pages, Hkv, P), fill_scale, np.float32))
+        return Fp8Cache._filled((num_pages, Hkv), P, D, fill_code, fill_scale)
 
     @staticmethod
-    def empty_ring(B, Hkv, W, D, fill_code=0x7F, fill_scale=np.nan):
-        return Fp8Cache(np.full((B, Hkv, W, D), fill_code, np.uint8),
-                        np.full((B, Hkv, D, W), fill_code, np.uint8),
-                        np.full((B, Hkv, W), fill_scale, np.float32),
-                        np.full((B, Hkv, W), fill_scale, np.float32))
+    def empty_ring(B, Hkv, W, D, fill_code=0x7F, fill_scale=np.nan, P=16):
+        assert W % P == 0, "the fp8 ring capacity is a multiple of 16"
+        return Fp8Cache._filled((B, Hkv, W // P), P, D, fill_code, fill_scale)
+
+    @staticmethod
+    def from_parts(k, vt, ks, vs):
+        """Pack K codes [..., P, D], V^T codes [..., D, P] and scales [..., P] into blocks."""
+        P, D = k.shape[-2], k.shape[-1]
+        c = Fp8Cache._filled(k.shape[:-2], P, D, 0, 0.0)
+        c.k[...] = k
+        c.vt[...] = vt
+        c.ks[...] = ks
+        c.vs[...] = vs
+        return c
 
     def copy(self):
-        return Fp8Cache(self.k.copy(), self.vt.copy(), self.ks.copy(), self.vs.copy())
+        return Fp8Cache(self.blocks.copy(), self.P, self.D)
 
-    def ptrs(self):
-        return (_ptr(self.k, _u8p), _ptr(self.vt, _u8p), _ptr(self.ks, _f32p), _ptr(self.vs, _f32p))
+    def ptr(self):
+        assert self.blocks.flags.c_contiguous
+        return _ptr(self.blocks, _u8p)
 
 
 def scatter_fp8(hist_k, hist_v, n_tokens, cache, block_table=None, window=0):
@@ -419,11 +456,11 @@ def scatter_fp8(hist_k, hist_v, n_tokens, cache, block_table=None, window=0):
     B, Tmax, Hkv, D = hk.shape
     if block_table is not None:
         bt = _i32(block_table)
-        P, maxp, npages = out.k.shape[2], bt.shape[1], out.k.shape[0]
+        maxp, npages = bt.shape[1], out.blocks.shape[0]
     else:
-        bt, P, maxp, npages = None, 16, 0, 0
+        bt, maxp, npages = None, 0, 0
     _check(lib.oracle_scatter_fp8(_ptr(hk, _u16p), _ptr(hv, _u16p), _ptr(n, _i32p), Tmax,
-                                  _ptr(bt, _i32p), int(window), *out.ptrs(), B, Hkv, D, P, maxp,
+                                  _ptr(bt, _i32p), int(window), out.ptr(), B, Hkv, D, out.P, maxp,
                                   npages), "scatter_fp8")
     return out
 
@@ -436,11 +473,11 @@ def kv_append_fp8(k_new, v_new, cache, seq_lens, block_table=None, window=0):
     B, Hkv, D = kn.shape
     if block_table is not None:
         bt = _i32(block_table)
-        P, maxp, npages = out.k.shape[2], bt.shape[1], out.k.shape[0]
+        maxp, npages = bt.shape[1], out.blocks.shape[0]
     else:
-        bt, P, maxp, npages = None, 16, 0, 0
-    _check(lib.oracle_kv_append_fp8(_ptr(kn, _u16p), _ptr(vn, _u16p), *out.ptrs(), _ptr(bt, _i32p),
-                                    _ptr(sl, _i32p), int(window), B, Hkv, D, P, maxp, npages),
+        bt, maxp, npages = None, 0, 0
+    _check(lib.oracle_kv_append_fp8(_ptr(kn, _u16p), _ptr(vn, _u16p), out.ptr(), _ptr(bt, _i32p),
+                                    _ptr(sl, _i32p), int(window), B, Hkv, D, out.P, maxp, npages),
            "kv_append_fp8")
     return out
 
@@ -451,13 +488,13 @@ def decode_paged_fp8(q, k_new, v_new, cache, block_table, seq_lens, sinks, windo
     q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
     bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
     B, Hq, D = q.shape
-    num_pages, Hkv, P, _ = cache.k.shape
+    num_pages, Hkv = cache.blocks.shape[:2]
     it, n_items = _items(items)
     out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
     _check(lib.oracle_decode_paged_fp8(
-        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), *cache.ptrs(), _ptr(bt, _i32p),
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), cache.ptr(), _ptr(bt, _i32p),
         _ptr(sl, _i32p), _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv,
-        D, P, bt.shape[1], num_pages, _ptr(it, _i32p), n_items, nthreads or default_threads()),
+        D, cache.P, bt.shape[1], num_pages, _ptr(it, _i32p), n_items, nthreads or default_threads()),
         "decode_paged_fp8")
     return out
 
@@ -468,11 +505,11 @@ def decode_ring_fp8(q, k_new, v_new, cache, seq_lens, sinks, window, scale, item
     q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
     sl, sk = _i32(seq_lens), _f32(sinks)
     B, Hq, D = q.shape
-    Hkv = cache.k.shape[1]
+    Hkv = cache.blocks.shape[1]
     it, n_items = _items(items)
     out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
     _check(lib.oracle_decode_ring_fp8(
-        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), *cache.ptrs(), _ptr(sl, _i32p),
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), cache.ptr(), _ptr(sl, _i32p),
         _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D,
         _ptr(it, _i32p), n_items, nthreads or default_threads()), "decode_ring_fp8")
     return out

@@ -508,9 +508,31 @@ int oracle_decode_ring_rope(const uint16_t *q, const uint16_t *k_new, const uint
  * from bf16), scale = amax / 448 in fp32 (scale = 1 when amax = 0), code_d =
  * the e4m3 value nearest to x_d / scale (fp32 division), ties to even,
  * saturating at +-448. The kernel takes the same fp32 decisions.
- * Layouts: paged K codes [num_pages][Hkv][P][D], paged V codes transposed
- * [num_pages][Hkv][D][P] (V^T per page), scales [num_pages][Hkv][P];
- * ring K [B][Hkv][W][D], ring V^T [B][Hkv][D][W], scales [B][Hkv][W]. */
+ * Layout: the cache is an array of blocks, one per P = 16 tokens of one KV head,
+ * each 2PD + 8P bytes: K codes [P][D] (row per token), V codes transposed [D][P],
+ * K scales [P] and V scales [P] as fp32 in native byte order. Paged: the block of
+ * (page, g) is number page * Hkv + g, slot j % P. Ring of capacity W (a multiple
+ * of P): cell c = j % W lives in block (b * Hkv + g) * (W / P) + c / P, slot c % P. */
+
+static size_t blk8_bytes(int P, int D) { return 2 * (size_t)P * D + 8 * (size_t)P; }
+
+static float f32_at(const uint8_t *p) { float f; memcpy(&f, p, sizeof f); return f; }
+static void f32_put(uint8_t *p, float f) { memcpy(p, &f, sizeof f); }
+
+/* block number holding position j of (b, g), and its slot; -1 for a bad page */
+static long long blk8_of(int ring, int b, int g, int j, int Hkv, int P, int W, const int32_t *block_table,
+                         int max_pages, int num_pages, int *slot) {
+    if (!ring) {
+        if (j / P >= max_pages) return -1;
+        const int32_t page = block_table[(size_t)b * max_pages + j / P];
+        if (page < 0 || page >= num_pages) return -1;
+        *slot = j % P;
+        return (long long)page * Hkv + g;
+    }
+    const int cell = j % W;
+    *slot = cell % P;
+    return ((long long)b * Hkv + g) * (W / P) + cell / P;
+}
 
 static double e4m3_decode(uint8_t c) {
     const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
@@ -579,8 +601,7 @@ typedef struct {
     int ring;                    /* 0 paged, 1 ring */
     const uint16_t *q;
     const uint16_t *k_new, *v_new; /* bf16 [B][Hkv][D], quantised on append, or NULL */
-    const uint8_t *kc, *vct;     /* K codes, V^T codes */
-    const float *ks, *vs;        /* scales */
+    const uint8_t *blocks;       /* the cache blocks */
     const int32_t *block_table, *seq_lens;
     const float *sinks;
     int window; double scale;
@@ -601,27 +622,17 @@ static int token_rows8(const problem8 *pr, int b, int g, int j, double *k, doubl
         for (int d = 0; d < D; ++d) { k[d] = e4m3_decode(ck[d]) * sk; v[d] = e4m3_decode(cv[d]) * sv; }
         return OR_OK;
     }
-    size_t krow, vbase, srow; int vstride;
-    if (!pr->ring) {
-        if (j / pr->P >= pr->max_pages) return OR_BAD_INDEX;
-        const int32_t page = pr->block_table[(size_t)b * pr->max_pages + j / pr->P];
-        if (page < 0 || page >= pr->num_pages) return OR_BAD_INDEX;
-        const size_t ph = (size_t)page * pr->Hkv + g;
-        const int slot = j % pr->P;
-        krow = (ph * pr->P + slot) * D;
-        vbase = ph * (size_t)D * pr->P + slot; vstride = pr->P;
-        srow = ph * pr->P + slot;
-    } else {
-        const int W = pr->window, cell = j % W;
-        const size_t bh = (size_t)b * pr->Hkv + g;
-        krow = (bh * W + cell) * D;
-        vbase = bh * (size_t)D * W + cell; vstride = W;
-        srow = bh * W + cell;
-    }
-    const double sk = pr->ks[srow], sv = pr->vs[srow];
+    const int P = pr->P;
+    int slot = 0;
+    const long long bi = blk8_of(pr->ring, b, g, j, pr->Hkv, P, pr->window, pr->block_table, pr->max_pages,
+                                 pr->num_pages, &slot);
+    if (bi < 0) return OR_BAD_INDEX;
+    const uint8_t *blk = pr->blocks + (size_t)bi * blk8_bytes(P, D);
+    const double sk = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)slot);
+    const double sv = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)(P + slot));
     for (int d = 0; d < D; ++d) {
-        k[d] = e4m3_decode(pr->kc[krow + d]) * sk;
-        v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]) * sv;
+        k[d] = e4m3_decode(blk[(size_t)slot * D + d]) * sk;
+        v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d * P + slot]) * sv;
     }
     return OR_OK;
 }
@@ -696,74 +707,63 @@ static int run8(problem8 *pr, int nthreads) {
 }
 
 int oracle_decode_paged_fp8(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
-                            const uint8_t *k_codes, const uint8_t *vt_codes, const float *k_scale,
-                            const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                            const uint8_t *blocks, const int32_t *block_table, const int32_t *seq_lens,
                             const float *sinks, int window, double scale, double *out,
                             int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
                             const int32_t *items, int n_items, int nthreads) {
-    if (!q || !k_codes || !vt_codes || !k_scale || !v_scale || !block_table || !seq_lens || !out ||
-        page_size <= 0 || max_pages <= 0 || num_pages <= 0 || window < 0 || ((k_new == NULL) != (v_new == NULL)))
+    if (!q || !blocks || !block_table || !seq_lens || !out || page_size <= 0 || max_pages <= 0 ||
+        num_pages <= 0 || window < 0 || ((k_new == NULL) != (v_new == NULL)))
         return OR_BAD_ARG;
-    problem8 pr = {0, q, k_new, v_new, k_codes, vt_codes, k_scale, v_scale, block_table, seq_lens, sinks,
+    problem8 pr = {0, q, k_new, v_new, blocks, block_table, seq_lens, sinks,
                    window, scale, B, Hq, Hkv, D, page_size, max_pages, num_pages, items, n_items, out};
     return run8(&pr, nthreads);
 }
 
 int oracle_decode_ring_fp8(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
-                           const uint8_t *k_codes, const uint8_t *vt_codes, const float *k_scale,
-                           const float *v_scale, const int32_t *seq_lens, const float *sinks, int window,
+                           const uint8_t *blocks, const int32_t *seq_lens, const float *sinks, int window,
                            double scale, double *out, int B, int Hq, int Hkv, int D,
                            const int32_t *items, int n_items, int nthreads) {
-    if (!q || !k_codes || !vt_codes || !k_scale || !v_scale || !seq_lens || !out || window <= 0 ||
+    if (!q || !blocks || !seq_lens || !out || window <= 0 || window % 16 != 0 ||
         ((k_new == NULL) != (v_new == NULL)))
         return OR_BAD_ARG;
-    problem8 pr = {1, q, k_new, v_new, k_codes, vt_codes, k_scale, v_scale, NULL, seq_lens, sinks,
+    problem8 pr = {1, q, k_new, v_new, blocks, NULL, seq_lens, sinks,
                    window, scale, B, Hq, Hkv, D, 16, 0, 0, items, n_items, out};
     return run8(&pr, nthreads);
 }
 
 /* Write token rows (bf16 [n][Hkv][D] per sequence b at positions pos[b] .. ) quantised into an
  * fp8 cache: the append of the new tokens (positions L-1), or the materialisation of a history. */
-static void put8(int ring, uint8_t *kc, uint8_t *vct, float *ks, float *vs, int b, int g, int j,
-                 const uint16_t *krow, const uint16_t *vrow, int Hkv, int D, int P, int W,
-                 int32_t page) {
+static int put8(int ring, uint8_t *blocks, int b, int g, int j, const uint16_t *krow, const uint16_t *vrow,
+                int Hkv, int D, int P, int W, const int32_t *block_table, int max_pages, int num_pages) {
     uint8_t ck[256], cv[256];
     float sk, sv;
+    int slot = 0;
+    const long long bi = blk8_of(ring, b, g, j, Hkv, P, W, block_table, max_pages, num_pages, &slot);
+    if (bi < 0) return OR_BAD_INDEX;
     quantise_row(krow, D, ck, &sk);
     quantise_row(vrow, D, cv, &sv);
-    size_t kbase, vbase, srow; int vstride;
-    if (!ring) {
-        const size_t ph = (size_t)page * Hkv + g;
-        const int slot = j % P;
-        kbase = (ph * P + slot) * D; vbase = ph * (size_t)D * P + slot; vstride = P; srow = ph * P + slot;
-    } else {
-        const size_t bh = (size_t)b * Hkv + g;
-        const int cell = j % W;
-        kbase = (bh * W + cell) * D; vbase = bh * (size_t)D * W + cell; vstride = W; srow = bh * W + cell;
+    uint8_t *blk = blocks + (size_t)bi * blk8_bytes(P, D);
+    for (int d = 0; d < D; ++d) {
+        blk[(size_t)slot * D + d] = ck[d];
+        blk[(size_t)P * D + (size_t)d * P + slot] = cv[d];
     }
-    for (int d = 0; d < D; ++d) { kc[kbase + d] = ck[d]; vct[vbase + (size_t)d * vstride] = cv[d]; }
-    ks[srow] = sk; vs[srow] = sv;
+    f32_put(blk + 2 * (size_t)P * D + 4 * (size_t)slot, sk);
+    f32_put(blk + 2 * (size_t)P * D + 4 * (size_t)(P + slot), sv);
+    return OR_OK;
 }
 
-int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_codes, uint8_t *vt_codes,
-                         float *k_scale, float *v_scale, const int32_t *block_table /* NULL = ring */,
-                         const int32_t *seq_lens, int window, int B, int Hkv, int D, int page_size,
-                         int max_pages, int num_pages) {
-    if (D > 256) return OR_BAD_ARG;
+int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *blocks,
+                         const int32_t *block_table /* NULL = ring */, const int32_t *seq_lens, int window,
+                         int B, int Hkv, int D, int page_size, int max_pages, int num_pages) {
+    if (D > 256 || (!block_table && (window <= 0 || window % page_size != 0))) return OR_BAD_ARG;
     for (int b = 0; b < B; ++b) {
         const int L = seq_lens[b];
         if (L <= 0) continue;
-        const int p = L - 1;
-        int32_t page = 0;
-        if (block_table) {
-            if (p / page_size >= max_pages) return OR_BAD_INDEX;
-            page = block_table[(size_t)b * max_pages + p / page_size];
-            if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
-        }
         for (int g = 0; g < Hkv; ++g) {
             const size_t src = ((size_t)b * Hkv + g) * D;
-            put8(block_table == NULL, k_codes, vt_codes, k_scale, v_scale, b, g, p, k_new + src, v_new + src,
-                 Hkv, D, page_size, window, page);
+            const int st = put8(block_table == NULL, blocks, b, g, L - 1, k_new + src, v_new + src, Hkv, D,
+                                page_size, window, block_table, max_pages, num_pages);
+            if (st != OR_OK) return st;
         }
     }
     return OR_OK;
@@ -772,25 +772,19 @@ int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *
 /* Materialise the first n[b] tokens of hist [B][Tmax][Hkv][D] into an fp8 cache (paged when a
  * block table is given, else the ring state of capacity `window`). */
 int oracle_scatter_fp8(const uint16_t *hist_k, const uint16_t *hist_v, const int32_t *n_tokens, int Tmax,
-                       const int32_t *block_table, int window, uint8_t *k_codes, uint8_t *vt_codes,
-                       float *k_scale, float *v_scale, int B, int Hkv, int D, int page_size, int max_pages,
-                       int num_pages) {
-    if (D > 256) return OR_BAD_ARG;
+                       const int32_t *block_table, int window, uint8_t *blocks, int B, int Hkv, int D,
+                       int page_size, int max_pages, int num_pages) {
+    if (D > 256 || (!block_table && (window <= 0 || window % page_size != 0))) return OR_BAD_ARG;
     for (int b = 0; b < B; ++b) {
         const int n = n_tokens[b];
         const int lo = (!block_table && n - window > 0) ? n - window : 0;
         for (int j = lo; j < n; ++j) {
             if (j >= Tmax) return OR_BAD_INDEX;
-            int32_t page = 0;
-            if (block_table) {
-                if (j / page_size >= max_pages) return OR_BAD_INDEX;
-                page = block_table[(size_t)b * max_pages + j / page_size];
-                if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
-            }
             for (int g = 0; g < Hkv; ++g) {
                 const size_t src = (((size_t)b * Tmax + j) * Hkv + g) * D;
-                put8(block_table == NULL, k_codes, vt_codes, k_scale, v_scale, b, g, j, hist_k + src,
-                     hist_v + src, Hkv, D, page_size, window, page);
+                const int st = put8(block_table == NULL, blocks, b, g, j, hist_k + src, hist_v + src, Hkv, D,
+                                    page_size, window, block_table, max_pages, num_pages);
+                if (st != OR_OK) return st;
             }
         }
     }

@@ -85,10 +85,10 @@ def load_library():
                                            vp]
     lib.decode_attn_ring_rope.argtypes = [vp, vp, vp, vp, vp, i32p, f32p, f32p, f32p, c_int, c_int,
                                           c_float, vp, da_shape, vp]
-    lib.decode_attn_paged_fp8.argtypes = [vp, vp, vp, vp, vp, f32p, f32p, i32p, i32p, f32p, c_int,
-                                          c_float, vp, da_shape, c_int, c_int, c_int, c_int, vp]
-    lib.decode_attn_ring_fp8.argtypes = [vp, vp, vp, vp, vp, f32p, f32p, i32p, f32p, c_int, c_float,
-                                         vp, da_shape, vp]
+    lib.decode_attn_paged_fp8.argtypes = [vp, vp, vp, vp, i32p, i32p, f32p, c_int, c_float, vp,
+                                          da_shape, c_int, c_int, c_int, c_int, vp]
+    lib.decode_attn_ring_fp8.argtypes = [vp, vp, vp, vp, i32p, f32p, c_int, c_float, vp, da_shape,
+                                         vp]
     lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
@@ -186,32 +186,36 @@ def decode_attn_ring_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, ro
     return out
 
 
-def decode_attn_paged_fp8(q, k_new, v_new, k_cache, vt_cache, k_scale, v_scale, block_table,
-                          seq_lens, sinks, window, scale, out, max_seq_len=None, stream=None):
-    """decode_attn_paged over an fp8 cache: k_cache [num_pages, Hkv, 16, 64] and vt_cache
-    [num_pages, Hkv, 64, 16] uint8 e4m3 codes, k_scale/v_scale [num_pages, Hkv, 16] fp32."""
-    num_pages, Hkv, P, _ = k_cache.shape
+FP8_BLOCK_BYTES = 2176  # 16 tokens of one KV head: K codes, V^T codes, K and V scales
+
+
+def decode_attn_paged_fp8(q, k_new, v_new, kv_cache, block_table, seq_lens, sinks, window, scale,
+                          out, max_seq_len=None, stream=None):
+    """decode_attn_paged over an fp8 cache: kv_cache uint8 [num_pages, Hkv, 2176], one block
+    per page and KV head (K codes [16][64], V codes [64][16], K scales [16], V scales [16])."""
+    num_pages, Hkv, nb = kv_cache.shape
+    if nb != FP8_BLOCK_BYTES:
+        raise ValueError(f"kv_cache blocks must be {FP8_BLOCK_BYTES} bytes, got {nb}")
     max_pages = block_table.shape[1]
     if max_seq_len is None:
-        max_seq_len = max_pages * P
+        max_seq_len = max_pages * 16
     lib = load_library()
     _check(lib.decode_attn_paged_fp8(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(vt_cache), _ptr(k_scale),
-        _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(sinks), int(window), float(scale),
-        _ptr(out), _shape(q, Hkv), P, max_pages, num_pages, int(max_seq_len), _stream(stream)))
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(sinks), int(window), float(scale), _ptr(out), _shape(q, Hkv), 16, max_pages,
+        num_pages, int(max_seq_len), _stream(stream)))
     return out
 
 
-def decode_attn_ring_fp8(q, k_new, v_new, k_cache, vt_cache, k_scale, v_scale, seq_lens, sinks,
-                         scale, out, stream=None):
-    """decode_attn_ring over an fp8 ring: k_cache [B, Hkv, W, 64], vt_cache [B, Hkv, 64, W]
-    uint8 e4m3 codes, k_scale/v_scale [B, Hkv, W] fp32; W % 16 == 0."""
-    B, Hkv, W, _ = k_cache.shape
+def decode_attn_ring_fp8(q, k_new, v_new, kv_cache, seq_lens, sinks, scale, out, stream=None):
+    """decode_attn_ring over an fp8 ring: kv_cache uint8 [B, Hkv, W / 16, 2176]."""
+    B, Hkv, nblk, nb = kv_cache.shape
+    if nb != FP8_BLOCK_BYTES:
+        raise ValueError(f"kv_cache blocks must be {FP8_BLOCK_BYTES} bytes, got {nb}")
     lib = load_library()
     _check(lib.decode_attn_ring_fp8(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(vt_cache), _ptr(k_scale),
-        _ptr(v_scale), _ptr(seq_lens), _ptr(sinks), int(W), float(scale), _ptr(out),
-        _shape(q, Hkv), _stream(stream)))
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _ptr(seq_lens), _ptr(sinks),
+        int(nblk * 16), float(scale), _ptr(out), _shape(q, Hkv), _stream(stream)))
     return out
 
 

@@ -40,6 +40,7 @@
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
+#include <type_traits>
 
 #include "decode_attn.h"
 
@@ -64,11 +65,22 @@ __host__ __device__ constexpr int stages_for() {
     // fp8 tiles are half the size: more of them in flight for the same bytes
     return KV8 ? (NT == 1 ? 7 : 6) : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16);
 }
+#ifndef DA_PAIR_BF16
+#define DA_PAIR_BF16 1
+#endif
+#ifndef DA_PAIR_FP8
+#define DA_PAIR_FP8 1
+#endif
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
 #endif
 constexpr int kMinTilesPerWorker = DA_MIN_TILES;
 constexpr int kTileBytes = kPage * kD * 2;  // 2048 B of K (or V) per tile
+// fp8 cache block: 16 tokens of one KV head, K codes [16][64], V codes transposed [64][16],
+// K scales [16] and V scales [16] (fp32)
+constexpr int kBlk8V = kPage * kD;            // offset of the V^T codes
+constexpr int kBlk8S = 2 * kPage * kD;        // offset of the K scales (V scales follow)
+constexpr int kBlk8Bytes = kBlk8S + 8 * kPage;  // 2176
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxSegments = 65536;         // B * Hkv
 constexpr int kMaxQHeads = 1024;
@@ -97,8 +109,6 @@ struct Params {
     const float *rope_cos;  // [max_position][D/2] fp32, or null: no rotary embedding
     const float *rope_sin;
     int max_position;
-    float *k_scale;  // fp8 caches: per-token fp32 scales of K and V, laid out like the token rows
-    float *v_scale;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -143,6 +153,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -416,13 +435,14 @@ template <int NT, bool ROPE, bool KV8>
 struct SmemLayout {
     static constexpr int kStages = stages_for<NT, ROPE, KV8>();
     static constexpr int GP = NT * 8;
-    static constexpr int kTile = KV8 ? kTileBytes / 2 : kTileBytes;  // one K (or V) tile
+    // a stage holds a K and a V tile (bf16: 2 KiB each, kept 1024-byte aligned for the
+    // 128-byte swizzle; all K tiles first, then all V tiles) or one fp8 block
+    static constexpr int kStageBytes = KV8 ? kBlk8Bytes : 2 * kTileBytes;
     // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin
     // rows, the fp8 tile's K and V scale rows
     static constexpr int kRopeOff = GP * kD * 2 + 2 * kD * 2;
-    static constexpr int kScaleOff = kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
-    static constexpr int kQBytes = kScaleOff + (KV8 ? 2 * kPage * 4 : 0);
-    static constexpr int kWarpTileBytes = kStages * 2 * kTile;  // K and V tiles of one warp
+    static constexpr int kQBytes = kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
+    static constexpr int kWarpTileBytes = kStages * kStageBytes;  // the tiles of one warp
     static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8;
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
     static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
@@ -431,7 +451,8 @@ struct SmemLayout {
     static constexpr size_t sinks = ints + static_cast<size_t>(kInts) * 4;
     static constexpr size_t end = sinks + static_cast<size_t>(kMaxQHeads) * 4;
     static constexpr size_t bytes = 1024 + end;  // plus the slack to align the base
-    static_assert(kTile % 1024 == 0 && kWarpTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
+    static_assert(KV8 || kWarpTileBytes % 1024 == 0, "bf16 tiles stay 1024-byte aligned");
+    static_assert(kWarpTileBytes % 16 == 0 && kStageBytes % 16 == 0, "bulk copies need 16-byte alignment");
     static_assert(kQBytes % 16 == 0 && meta % 16 == 0, "bulk copies and int4 need 16-byte alignment");
     static_assert(bytes <= kMaxSmem, "shared memory budget");
 };
@@ -442,13 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
     using Lay = SmemLayout<NT, ROPE, KV8>;
-    constexpr int kTileB = Lay::kTile;
+    constexpr int kTileB = KV8 ? kBlk8V : kTileBytes;  // bytes of one K (or V) tile
     constexpr int kStages = Lay::kStages;
     constexpr int GP = Lay::GP;
     constexpr int kQBytes = Lay::kQBytes;
     constexpr int kWarpBytes = Lay::kWarpTileBytes;
     static_assert(2 * sizeof(Slot<NT>) <= kWarpBytes, "merge slots must fit a drained warp area");
     constexpr int kSlotFloats = 2 * GP + GP * kD;  // global partial: m, l, acc
+    // two tiles per loop pass (single 8-head n-tile only: the registers of two 16-head passes
+    // would not fit)
+    constexpr bool kPair = NT == 1 && (KV8 ? DA_PAIR_FP8 : DA_PAIR_BF16);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -466,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
     // grid is launched as a programmatic dependent.
-    if (tid == 0) {
+    if (!KV8 && tid == 0) {  // fp8 blocks are plain bulk copies: no tensor maps
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
@@ -547,8 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint8_t *wbase = smem + warp * kWarpBytes;
     const uint32_t wbase_s = smem_addr(wbase);
-    auto k_tile = [&](int st) { return wbase_s + st * kTileB; };
-    auto v_tile = [&](int st) { return wbase_s + (kStages + st) * kTileB; };
+    // offsets of a stage's K tile, V tile and (fp8) scale rows in the warp's area
+    auto k_off = [&](int st) { return KV8 ? st * kBlk8Bytes : st * kTileB; };
+    auto v_off = [&](int st) { return KV8 ? st * kBlk8Bytes + kBlk8V : (kStages + st) * kTileB; };
+    auto s_off = [&](int st) { return st * kBlk8Bytes + kBlk8S; };
+    auto k_tile = [&](int st) { return wbase_s + k_off(st); };
+    auto v_tile = [&](int st) { return wbase_s + v_off(st); };
     uint8_t *wq = qarea + warp * kStages * kQBytes;
     const uint32_t wq_s = smem_addr(wq);
     auto q_tile = [&](int st) { return wq_s + st * kQBytes; };
@@ -618,20 +646,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = newseg && p.k_new != nullptr;
                 const bool rope = ROPE && newseg;
-                mbar_expect_tx(bar, 2 * kTileB + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
-                                        (rope ? 4 * kD : 0) + (KV8 ? 2 * kPage * 4 : 0));
-                int c1, c2;
-                if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
-                else { c1 = 0; c2 = tp * Hkv + tg; }
-                tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
-                if (KV8 && RING) tma_load_3d(v_tile(stg), &tmv, c1, 0, c2, bar, policy);  // V^T: cells inner
-                else tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
-                if constexpr (KV8) {  // the tile's per-token K and V scales
-                    size_t srow;
-                    if (RING) srow = (static_cast<size_t>(tb) * Hkv + tg) * p.window + tt * kPage;
-                    else srow = (static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg) * kPage;
-                    bulk_load(q_tile(stg) + Lay::kScaleOff, p.k_scale + srow, kPage * 4, bar);
-                    bulk_load(q_tile(stg) + Lay::kScaleOff + kPage * 4, p.v_scale + srow, kPage * 4, bar);
+                mbar_expect_tx(bar, Lay::kStageBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
+                                        (rope ? 4 * kD : 0));
+                if constexpr (KV8) {  // the whole block in one copy (a bad page reads block 0)
+                    const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
+                                            : static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg;
+                    bulk_load_hint(k_tile(stg), reinterpret_cast<const uint8_t *>(p.k_cache) + blk * kBlk8Bytes,
+                                   kBlk8Bytes, bar, policy);
+                } else {
+                    int c1, c2;
+                    if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
+                    else { c1 = 0; c2 = tp * Hkv + tg; }
+                    tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
+                    tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
                 }
                 if (newseg)
                     bulk_load(q_tile(stg),
@@ -666,15 +693,255 @@ __global__ void __launch_bounds__(kThreads, 1)
         float knew_scale = 1.f, vnew_scale = 1.f;  // fp8: their scales
         const bool do_append = p.k_new != nullptr;
 
-        int i = 0;
-        for (; i < n_tiles; ++i) {
+        int i = 0;  // first tile of the current pass
+        // One pass over UT (1 or 2) consecutive tiles i .. i + UT - 1 of the current segment.
+        // Two tiles give each warp two independent load / convert / MMA chains and one
+        // online-softmax update per 32 tokens.
+        auto tiles_step = [&](auto ut_c) {
+            constexpr int UT = decltype(ut_c)::value;
+            int stgs[UT], tts[UT], tps[UT];
+#pragma unroll
+            for (int u = 0; u < UT; ++u) {
+                stgs[u] = (i + u) % kStages;
+                const int4 m = wmeta[stgs[u]];
+                tts[u] = m.z;
+                tps[u] = m.w;
+            }
+#pragma unroll
+            for (int u = 0; u < UT; ++u) {
+                const int stg = stgs[u], tt = tts[u], tp = tps[u];
+                uint8_t *gK = wbase + k_off(stg);
+                uint8_t *gV = wbase + v_off(stg);
+                // fused append: this tile holds position p = L - 1
+                if (do_append && tt == app_tile) {
+                    size_t slice, cell;  // (KV head) slice of the cache and the token's cell in it
+                    bool ok = true;
+                    if (RING) {
+                        slice = static_cast<size_t>(sb) * Hkv + sgk;
+                        cell = tt * kPage + app_row;
+                    } else {
+                        ok = tp >= 0;
+                        slice = static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + sgk;
+                        cell = app_row;
+                    }
+                    if constexpr (KV8) {
+                        // K row of codes, one column of the transposed V tile and both scales, in
+                        // the staged block and in the cache block (the same bytes)
+                        auto put = [&](uint8_t *blk) {
+                            *reinterpret_cast<uint16_t *>(blk + app_row * kD + 2 * lane) = static_cast<uint16_t>(knew);
+                            blk[kBlk8V + (2 * lane) * kPage + app_row] = static_cast<uint8_t>(vnew);
+                            blk[kBlk8V + (2 * lane + 1) * kPage + app_row] = static_cast<uint8_t>(vnew >> 8);
+                            if (lane == 0) {
+                                reinterpret_cast<float *>(blk + kBlk8S)[app_row] = knew_scale;
+                                reinterpret_cast<float *>(blk + kBlk8S)[kPage + app_row] = vnew_scale;
+                            }
+                        };
+                        put(gK);
+                        if (ok) {
+                            const size_t blk = RING ? slice * (p.window / kPage) + tt : slice;
+                            put(reinterpret_cast<uint8_t *>(p.k_cache) + blk * kBlk8Bytes);
+                        }
+                    } else {
+                        const uint32_t off = app_row * 128 + ((((lane >> 2) ^ (app_row & 7))) << 4) + (lane & 3) * 4;
+                        *reinterpret_cast<uint32_t *>(gK + off) = knew;
+                        *reinterpret_cast<uint32_t *>(gV + off) = vnew;
+                        if (ok) {
+                            const size_t c = slice * (RING ? p.window : kPage) + cell;
+                            reinterpret_cast<uint32_t *>(p.k_cache + c * kD)[lane] = knew;
+                            reinterpret_cast<uint32_t *>(p.v_cache + c * kD)[lane] = vnew;
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+
+            // token validity of this lane's rows (fp8 tiles: rows are permuted tokens)
+            const int lo_v = RING ? 0 : lo, hi_v = RING ? nvalid : L;
+            const int row_tok = KV8 ? fp8_row_token(lane >> 2) : (lane >> 2);
+            int t0[UT];
+            bool partial[UT], ok_lo[UT], ok_hi[UT];
+#pragma unroll
+            for (int u = 0; u < UT; ++u) {
+                t0[u] = (RING ? tts[u] : ft + tts[u]) * kPage;
+                partial[u] = (t0[u] < lo_v) || (t0[u] + kPage > hi_v);
+                const int r0 = t0[u] + row_tok;
+                const int r8 = r0 + (KV8 ? 2 : 8);
+                ok_lo[u] = r0 >= lo_v && r0 < hi_v;
+                ok_hi[u] = r8 >= lo_v && r8 < hi_v;
+            }
+
+            // K fragments, and the V fragments too: they do not depend on the softmax, so
+            // their shared-memory latency overlaps the QK products
+            uint32_t ka[UT][4][4], va[UT][4][4];
+            float ks_lo[UT], ks_hi[UT], vs_lo[UT], vs_hi[UT];  // fp8 per-token scales
+#pragma unroll
+            for (int u = 0; u < UT; ++u) {
+                ks_lo[u] = ks_hi[u] = vs_lo[u] = vs_hi[u] = 1.f;
+                if constexpr (KV8) {
+                    const uint8_t *gK = wbase + k_off(stgs[u]);
+                    const uint8_t *gV = wbase + v_off(stgs[u]);
+                    // K rows row_tok and row_tok + 2: bytes 16t..16t+15 (d), 4 per k-step
+                    const uint4 klo = *reinterpret_cast<const uint4 *>(gK + row_tok * kD + 16 * (lane & 3));
+                    const uint4 khi = *reinterpret_cast<const uint4 *>(gK + (row_tok + 2) * kD + 16 * (lane & 3));
+                    const uint32_t wl[4] = {klo.x, klo.y, klo.z, klo.w}, wh[4] = {khi.x, khi.y, khi.z, khi.w};
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        e4m3x4_to_f16x2x2(wl[ks], ka[u][ks][0], ka[u][ks][2]);
+                        e4m3x4_to_f16x2x2(wh[ks], ka[u][ks][1], ka[u][ks][3]);
+                    }
+                    // V^T rows d and d + 8: tokens 4t..4t+3 in one word
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        const uint32_t vl = *reinterpret_cast<const uint32_t *>(gV + (16 * mt + (lane >> 2)) * kPage + 4 * (lane & 3));
+                        const uint32_t vh = *reinterpret_cast<const uint32_t *>(gV + (16 * mt + 8 + (lane >> 2)) * kPage + 4 * (lane & 3));
+                        e4m3x4_to_f16x2x2(vl, va[u][mt][0], va[u][mt][2]);
+                        e4m3x4_to_f16x2x2(vh, va[u][mt][1], va[u][mt][3]);
+                    }
+                    const float *ssr = reinterpret_cast<const float *>(wbase + s_off(stgs[u]));
+                    ks_lo[u] = ssr[row_tok];
+                    ks_hi[u] = ssr[row_tok + 2];
+                    // V scales carry a factor 2^8 so that the fp16 probabilities stay normal;
+                    // it is taken out when the segment closes
+                    vs_lo[u] = ssr[kPage + row_tok] * 256.f;
+                    vs_hi[u] = ssr[kPage + row_tok + 2] * 256.f;
+                    if (partial[u]) {  // a row outside the attended range may hold a garbage scale
+                        vs_lo[u] = ok_lo[u] ? vs_lo[u] : 0.f;
+                        vs_hi[u] = ok_hi[u] ? vs_hi[u] : 0.f;
+                    }
+                } else {
+                    const uint32_t sK = k_tile(stgs[u]), sV = v_tile(stgs[u]);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[u][ks][0], ka[u][ks][1], ka[u][ks][2], ka[u][ks][3]);
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt)
+                        ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), va[u][mt][0], va[u][mt][1], va[u][mt][2], va[u][mt][3]);
+                }
+            }
+            // S^T = K Q^T  (16 tokens x 8 heads per n-tile and tile), two MMA chains per tile
+            uint32_t pb[UT][NT][2];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                float sv[UT][4];
+#pragma unroll
+                for (int u = 0; u < UT; ++u) {
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (KV8) {
+                        mma_f16(sc, ka[u][0][0], ka[u][0][1], ka[u][0][2], ka[u][0][3], qf[n][0][0], qf[n][0][1]);
+                        mma_f16(sd, ka[u][1][0], ka[u][1][1], ka[u][1][2], ka[u][1][3], qf[n][1][0], qf[n][1][1]);
+                        mma_f16(sc, ka[u][2][0], ka[u][2][1], ka[u][2][2], ka[u][2][3], qf[n][2][0], qf[n][2][1]);
+                        mma_f16(sd, ka[u][3][0], ka[u][3][1], ka[u][3][2], ka[u][3][3], qf[n][3][0], qf[n][3][1]);
+                    } else {
+                        mma_bf16(sc, ka[u][0][0], ka[u][0][1], ka[u][0][2], ka[u][0][3], qf[n][0][0], qf[n][0][1]);
+                        mma_bf16(sd, ka[u][1][0], ka[u][1][1], ka[u][1][2], ka[u][1][3], qf[n][1][0], qf[n][1][1]);
+                        mma_bf16(sc, ka[u][2][0], ka[u][2][1], ka[u][2][2], ka[u][2][3], qf[n][2][0], qf[n][2][1]);
+                        mma_bf16(sd, ka[u][3][0], ka[u][3][1], ka[u][3][2], ka[u][3][3], qf[n][3][0], qf[n][3][1]);
+                    }
+                    const float sl_lo = KV8 ? p.scale_log2 * ks_lo[u] : p.scale_log2;
+                    const float sl_hi = KV8 ? p.scale_log2 * ks_hi[u] : p.scale_log2;
+                    sv[u][0] = (sc[0] + sd[0]) * sl_lo;
+                    sv[u][1] = (sc[1] + sd[1]) * sl_lo;
+                    sv[u][2] = (sc[2] + sd[2]) * sl_hi;
+                    sv[u][3] = (sc[3] + sd[3]) * sl_hi;
+                    if (partial[u]) {
+                        if (!ok_lo[u]) sv[u][0] = sv[u][1] = -INFINITY;
+                        if (!ok_hi[u]) sv[u][2] = sv[u][3] = -INFINITY;
+                    }
+                }
+                float mx0 = fmaxf(sv[0][0], sv[0][2]), mx1 = fmaxf(sv[0][1], sv[0][3]);
+#pragma unroll
+                for (int u = 1; u < UT; ++u) {
+                    mx0 = fmaxf(mx0, fmaxf(sv[u][0], sv[u][2]));
+                    mx1 = fmaxf(mx1, fmaxf(sv[u][1], sv[u][3]));
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 8));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 8));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
+                const float mn0 = fmaxf(st.m[n][0], mx0), mn1 = fmaxf(st.m[n][1], mx1);
+                const float a0 = fast_exp2(st.m[n][0] - mn0), a1 = fast_exp2(st.m[n][1] - mn1);
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < UT; ++u) {
+                    const float p0 = fast_exp2(sv[u][0] - mn0), p1 = fast_exp2(sv[u][1] - mn1);
+                    const float p2 = fast_exp2(sv[u][2] - mn0), p3 = fast_exp2(sv[u][3] - mn1);
+                    ls0 += p0 + p2;
+                    ls1 += p1 + p3;
+                    if constexpr (KV8) {  // probabilities times the tokens' V scales, fp16
+                        pb[u][n][0] = movmatrix_t(pack_f16(p0 * vs_lo[u], p1 * vs_lo[u]));  // tokens 4t, 4t+1
+                        pb[u][n][1] = movmatrix_t(pack_f16(p2 * vs_hi[u], p3 * vs_hi[u]));  // tokens 4t+2, 4t+3
+                    } else {
+                        pb[u][n][0] = movmatrix_t(pack_bf16(p0, p1));  // tokens 2(lane%4)+{0,1}
+                        pb[u][n][1] = movmatrix_t(pack_bf16(p2, p3));  // tokens 8+2(lane%4)+{0,1}
+                    }
+                }
+                st.l[n][0] = st.l[n][0] * a0 + ls0;
+                st.l[n][1] = st.l[n][1] * a1 + ls1;
+                st.m[n][0] = mn0;
+                st.m[n][1] = mn1;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    st.acc[n][mt][0] *= a0;
+                    st.acc[n][mt][1] *= a1;
+                    st.acc[n][mt][2] *= a0;
+                    st.acc[n][mt][3] *= a1;
+                }
+            }
+
+            // O^T += V^T P^T  (64 d x 8 heads per n-tile)
+#pragma unroll
+            for (int u = 0; u < UT; ++u) {
+                if (partial[u]) {
+                    // zero the V values of tokens outside the range (they may hold NaN): this
+                    // lane's V^T fragment halves carry tokens 2t, 2t+1 / 2t+8, 2t+9 (bf16 tiles);
+                    // 4t, 4t+1 / 4t+2, 4t+3 (fp8 tiles)
+                    const int tv = t0[u] + (lane & 3) * (KV8 ? 4 : 2);
+                    const int tw = tv + (KV8 ? 2 : 8);
+                    const uint32_t vm0 = ((tv >= lo_v && tv < hi_v) ? 0x0000ffffu : 0u) |
+                                         ((tv + 1 >= lo_v && tv + 1 < hi_v) ? 0xffff0000u : 0u);
+                    const uint32_t vm1 = ((tw >= lo_v && tw < hi_v) ? 0x0000ffffu : 0u) |
+                                         ((tw + 1 >= lo_v && tw + 1 < hi_v) ? 0xffff0000u : 0u);
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        va[u][mt][0] &= vm0;
+                        va[u][mt][1] &= vm0;
+                        va[u][mt][2] &= vm1;
+                        va[u][mt][3] &= vm1;
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int u = 0; u < UT; ++u)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        if constexpr (KV8)
+                            mma_f16(st.acc[n][mt], va[u][mt][0], va[u][mt][1], va[u][mt][2], va[u][mt][3], pb[u][n][0], pb[u][n][1]);
+                        else
+                            mma_bf16(st.acc[n][mt], va[u][mt][0], va[u][mt][1], va[u][mt][2], va[u][mt][3], pb[u][n][0], pb[u][n][1]);
+                    }
+
+            __syncwarp();
+            // refill the stages just read
+            if (i + kStages < n_tiles) {
+                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+                for (int u = 0; u < UT; ++u)
+                    if (i + u + kStages < n_tiles) issue(i + u + kStages);
+            }
+        };
+
+        while (i < n_tiles) {
             const int stg = i % kStages;
             if (!mbar_wait_bounded(bar0 + 8 * stg, (i / kStages) & 1)) {
                 failed = true;
                 break;
             }
             const int4 md = wmeta[stg];
-            const int tb = md.x, tg = md.y, tt = md.z, tp = md.w;
+            const int tb = md.x, tg = md.y, tt = md.z;
             if (i == 0 || tt == 0) {
                 // close the previous segment
                 if (i > 0) {
@@ -776,199 +1043,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 state_reset(st);
             }
-
-            const uint32_t sK = k_tile(stg), sV = v_tile(stg);
-            uint8_t *gK = wbase + stg * kTileB;
-            uint8_t *gV = wbase + (kStages + stg) * kTileB;
-
-            // fused append: this tile holds position p = L - 1
-            if (do_append && tt == app_tile) {
-                size_t slice, cell;  // (KV head) slice of the cache and the token's cell in it
-                bool ok = true;
-                if (RING) {
-                    slice = static_cast<size_t>(sb) * Hkv + sgk;
-                    cell = tt * kPage + app_row;
-                } else {
-                    ok = tp >= 0;
-                    slice = static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + sgk;
-                    cell = app_row;
-                }
-                if constexpr (KV8) {
-                    // K row of codes, one column of the transposed V tile, both scales
-                    const int rows = RING ? p.window : kPage;
-                    *reinterpret_cast<uint16_t *>(gK + app_row * kD + 2 * lane) = static_cast<uint16_t>(knew);
-                    gV[(2 * lane) * kPage + app_row] = static_cast<uint8_t>(vnew);
-                    gV[(2 * lane + 1) * kPage + app_row] = static_cast<uint8_t>(vnew >> 8);
-                    float *ssr = reinterpret_cast<float *>(wq + stg * kQBytes + Lay::kScaleOff);
-                    if (lane == 0) {
-                        ssr[app_row] = knew_scale;
-                        ssr[kPage + app_row] = vnew_scale;
+            // the next tile continues this segment: take both in one pass
+            if constexpr (kPair) {
+                if (i + 1 < n_tiles && ua + i + 1 < seg_end_unit) {
+                    if (!mbar_wait_bounded(bar0 + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1)) {
+                        failed = true;
+                        break;
                     }
-                    if (ok) {
-                        uint8_t *kc = reinterpret_cast<uint8_t *>(p.k_cache);
-                        uint8_t *vt = reinterpret_cast<uint8_t *>(p.v_cache);
-                        *reinterpret_cast<uint16_t *>(kc + (slice * rows + cell) * kD + 2 * lane) =
-                            static_cast<uint16_t>(knew);
-                        vt[slice * kD * rows + (2 * lane) * rows + cell] = static_cast<uint8_t>(vnew);
-                        vt[slice * kD * rows + (2 * lane + 1) * rows + cell] = static_cast<uint8_t>(vnew >> 8);
-                        if (lane == 0) {
-                            p.k_scale[slice * rows + cell] = knew_scale;
-                            p.v_scale[slice * rows + cell] = vnew_scale;
-                        }
-                    }
-                } else {
-                    const uint32_t off = app_row * 128 + ((((lane >> 2) ^ (app_row & 7))) << 4) + (lane & 3) * 4;
-                    *reinterpret_cast<uint32_t *>(gK + off) = knew;
-                    *reinterpret_cast<uint32_t *>(gV + off) = vnew;
-                    if (ok) {
-                        const size_t c = slice * (RING ? p.window : kPage) + cell;
-                        reinterpret_cast<uint32_t *>(p.k_cache + c * kD)[lane] = knew;
-                        reinterpret_cast<uint32_t *>(p.v_cache + c * kD)[lane] = vnew;
-                    }
-                }
-                __syncwarp();
-            }
-
-            // token validity of this lane's rows (fp8 tiles: rows are permuted tokens)
-            int t0, lo_v, hi_v;
-            if (RING) { t0 = tt * kPage; lo_v = 0; hi_v = nvalid; }
-            else { t0 = (ft + tt) * kPage; lo_v = lo; hi_v = L; }
-            const bool partial = (t0 < lo_v) || (t0 + kPage > hi_v);
-            const int row_tok = KV8 ? fp8_row_token(lane >> 2) : (lane >> 2);
-            const int r0 = t0 + row_tok;
-            const int r8 = r0 + (KV8 ? 2 : 8);
-            const bool ok_lo = r0 >= lo_v && r0 < hi_v;
-            const bool ok_hi = r8 >= lo_v && r8 < hi_v;
-
-            // K fragments, and the V fragments too: they do not depend on the softmax, so
-            // their shared-memory latency overlaps the QK products
-            uint32_t ka[4][4], va[4][4];
-            float ks_lo = 1.f, ks_hi = 1.f, vs_lo = 1.f, vs_hi = 1.f;  // fp8 per-token scales
-            if constexpr (KV8) {
-                // K rows row_tok and row_tok + 2: bytes 16t..16t+15 (d), 4 per k-step
-                const uint4 klo = *reinterpret_cast<const uint4 *>(gK + row_tok * kD + 16 * (lane & 3));
-                const uint4 khi = *reinterpret_cast<const uint4 *>(gK + (row_tok + 2) * kD + 16 * (lane & 3));
-                const uint32_t wl[4] = {klo.x, klo.y, klo.z, klo.w}, wh[4] = {khi.x, khi.y, khi.z, khi.w};
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    e4m3x4_to_f16x2x2(wl[ks], ka[ks][0], ka[ks][2]);
-                    e4m3x4_to_f16x2x2(wh[ks], ka[ks][1], ka[ks][3]);
-                }
-                // V^T rows d and d + 8: tokens 4t..4t+3 in one word
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-                    const uint32_t vl = *reinterpret_cast<const uint32_t *>(gV + (16 * mt + (lane >> 2)) * kPage + 4 * (lane & 3));
-                    const uint32_t vh = *reinterpret_cast<const uint32_t *>(gV + (16 * mt + 8 + (lane >> 2)) * kPage + 4 * (lane & 3));
-                    e4m3x4_to_f16x2x2(vl, va[mt][0], va[mt][2]);
-                    e4m3x4_to_f16x2x2(vh, va[mt][1], va[mt][3]);
-                }
-                const float *ssr = reinterpret_cast<const float *>(wq + stg * kQBytes + Lay::kScaleOff);
-                ks_lo = ssr[row_tok];
-                ks_hi = ssr[row_tok + 2];
-                // V scales carry a factor 2^8 so that the fp16 probabilities stay normal;
-                // it is taken out when the segment closes
-                // (a row outside the attended range may hold a garbage scale: select 0)
-                vs_lo = ok_lo ? ssr[kPage + row_tok] * 256.f : 0.f;
-                vs_hi = ok_hi ? ssr[kPage + row_tok + 2] * 256.f : 0.f;
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3]);
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt)
-                    ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
-            }
-            // S^T = K Q^T  (16 tokens x 8 heads per n-tile), as two independent MMA chains
-            uint32_t pb[NT][2];
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (KV8) {
-                    mma_f16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[n][0][0], qf[n][0][1]);
-                    mma_f16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[n][1][0], qf[n][1][1]);
-                    mma_f16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[n][2][0], qf[n][2][1]);
-                    mma_f16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[n][3][0], qf[n][3][1]);
-                } else {
-                    mma_bf16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[n][0][0], qf[n][0][1]);
-                    mma_bf16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[n][1][0], qf[n][1][1]);
-                    mma_bf16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[n][2][0], qf[n][2][1]);
-                    mma_bf16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[n][3][0], qf[n][3][1]);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) sc[k] += sd[k];
-                const float sl_lo = p.scale_log2 * ks_lo, sl_hi = p.scale_log2 * ks_hi;
-                float s0 = ok_lo ? sc[0] * sl_lo : -INFINITY;
-                float s1 = ok_lo ? sc[1] * sl_lo : -INFINITY;
-                float s2 = ok_hi ? sc[2] * sl_hi : -INFINITY;
-                float s3 = ok_hi ? sc[3] * sl_hi : -INFINITY;
-                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 8));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 8));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
-                const float mn0 = fmaxf(st.m[n][0], mx0), mn1 = fmaxf(st.m[n][1], mx1);
-                const float a0 = fast_exp2(st.m[n][0] - mn0), a1 = fast_exp2(st.m[n][1] - mn1);
-                const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-                const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
-                st.l[n][0] = st.l[n][0] * a0 + (p0 + p2);
-                st.l[n][1] = st.l[n][1] * a1 + (p1 + p3);
-                st.m[n][0] = mn0;
-                st.m[n][1] = mn1;
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-                    st.acc[n][mt][0] *= a0;
-                    st.acc[n][mt][1] *= a1;
-                    st.acc[n][mt][2] *= a0;
-                    st.acc[n][mt][3] *= a1;
-                }
-                if constexpr (KV8) {  // probabilities times the tokens' V scales, fp16
-                    pb[n][0] = movmatrix_t(pack_f16(p0 * vs_lo, p1 * vs_lo));  // tokens 4t, 4t+1
-                    pb[n][1] = movmatrix_t(pack_f16(p2 * vs_hi, p3 * vs_hi));  // tokens 4t+2, 4t+3
-                } else {
-                    pb[n][0] = movmatrix_t(pack_bf16(p0, p1));  // tokens 2(lane%4)+{0,1}
-                    pb[n][1] = movmatrix_t(pack_bf16(p2, p3));  // tokens 8+2(lane%4)+{0,1}
+                    tiles_step(std::integral_constant<int, 2>{});
+                    i += 2;
+                    continue;
                 }
             }
-
-            // O^T += V^T P^T  (64 d x 8 heads per n-tile)
-            if (partial) {
-                // zero the V values of tokens outside the range (they may hold NaN): this
-                // lane's V^T fragment halves carry tokens 2t, 2t+1 / 2t+8, 2t+9 (bf16 tiles);
-                // 4t, 4t+1 / 4t+2, 4t+3 (fp8 tiles)
-                const int tv = t0 + (lane & 3) * (KV8 ? 4 : 2);
-                const int tw = tv + (KV8 ? 2 : 8);
-                const uint32_t vm0 = ((tv >= lo_v && tv < hi_v) ? 0x0000ffffu : 0u) |
-                                     ((tv + 1 >= lo_v && tv + 1 < hi_v) ? 0xffff0000u : 0u);
-                const uint32_t vm1 = ((tw >= lo_v && tw < hi_v) ? 0x0000ffffu : 0u) |
-                                     ((tw + 1 >= lo_v && tw + 1 < hi_v) ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-                    va[mt][0] &= vm0;
-                    va[mt][1] &= vm0;
-                    va[mt][2] &= vm1;
-                    va[mt][3] &= vm1;
-                }
-            }
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const uint32_t a0 = va[mt][0], a1 = va[mt][1];
-                const uint32_t a2 = va[mt][2], a3 = va[mt][3];
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    if constexpr (KV8) mma_f16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
-                    else mma_bf16(st.acc[n][mt], a0, a1, a2, a3, pb[n][0], pb[n][1]);
-                }
-            }
-
-            __syncwarp();
-            if (i + kStages < n_tiles) {
-                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(i + kStages);
-            }
+            tiles_step(std::integral_constant<int, 1>{});
+            i += 1;
         }
-
         if (failed) {
             flag_status(DA_STATUS_TIMEOUT);
             // let the copies still in flight land before the buffers are reused
@@ -1243,12 +1332,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Kinds of cache views a tile is copied from:
-//   kMapBf16: bf16 [slices][rows][64], box 16 rows x 64, 128-byte swizzle (K and V tiles)
-//   kMapFp8K: e4m3 [slices][rows][64], box 16 rows x 64 bytes (fp8 K tiles)
-//   kMapFp8V: e4m3 [slices][64][rows], box 64 rows x 16 bytes (fp8 transposed V tiles)
-// rows = tokens per slice (16 per page, or the ring capacity).
-enum MapKind { kMapBf16 = 0, kMapFp8K = 1, kMapFp8V = 2 };
+// The cache view a bf16 tile is copied from: [slices][rows][64], box 16 rows x 64,
+// 128-byte swizzle (K and V tiles); rows = tokens per slice (16 per page, or the ring
+// capacity). fp8 blocks need no map: they are contiguous.
+enum MapKind { kMapBf16 = 0 };
 
 bool encode_kv_map(CUtensorMap *map, void *base, int kind, uint64_t rows, uint64_t slices) {
     EncodeTiledFn enc = encode_fn();
@@ -1262,20 +1349,7 @@ bool encode_kv_map(CUtensorMap *map, void *base, int kind, uint64_t rows, uint64
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
-    if (kind == kMapFp8K) {
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), rows, slices};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), rows * kD};
-        const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kPage), 1};
-        return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
-    const cuuint64_t dims[3] = {rows, static_cast<cuuint64_t>(kD), slices};
-    const cuuint64_t strides[2] = {rows, rows * kD};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kPage), static_cast<cuuint32_t>(kD), 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return false;
 }
 
 // Encoding a map costs host time on every call; the map depends only on the
@@ -1433,19 +1507,16 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
                   const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
                   float scale, void *out, const da_shape &s, int page_size, int max_pages, int num_pages,
                   int max_seq_len, void *stream_v, const float *rope_cos = nullptr,
-                  const float *rope_sin = nullptr, int max_position = 0, float *k_scale = nullptr,
-                  float *v_scale = nullptr) {
-    const bool kv8 = k_scale != nullptr;
+                  const float *rope_sin = nullptr, int max_position = 0, bool kv8 = false) {
     int rc = check_shape(s);
     if (rc != DA_OK) return rc;
-    if (!q || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
+    if (!q || !k_cache || (!kv8 && !v_cache) || !seq_lens || !out) return DA_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return DA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+    if (!aligned16(q) || !aligned16(k_cache) || (!kv8 && !aligned16(v_cache)) || !aligned16(out) ||
         (k_new && (!aligned16(k_new) || !aligned16(v_new))))
         return DA_ERR_INVALID_ARG;
     if (!(scale == scale)) return DA_ERR_INVALID_ARG;
     if ((rope_cos == nullptr) != (rope_sin == nullptr)) return DA_ERR_INVALID_ARG;
-    if (kv8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return DA_ERR_INVALID_ARG;
     if (kv8 && rope_cos) return DA_ERR_UNSUPPORTED;
     if (kv8 && ring && window % kPage != 0) return DA_ERR_UNSUPPORTED;
     if (rope_cos && (max_position <= 0 || !aligned16(rope_cos) || !aligned16(rope_sin))) return DA_ERR_INVALID_ARG;
@@ -1487,19 +1558,21 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.rope_cos = rope_cos;
     prm.rope_sin = rope_sin;
     prm.max_position = max_position;
-    prm.k_scale = k_scale;
-    prm.v_scale = v_scale;
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
     CUtensorMap mk, mv;
-    const uint64_t rows = ring ? static_cast<uint64_t>(window) : static_cast<uint64_t>(kPage);
-    const uint64_t slices = ring ? static_cast<uint64_t>(s.batch) * s.num_kv_heads
-                                 : static_cast<uint64_t>(num_pages) * s.num_kv_heads;
-    if (!make_kv_map(&mk, k_cache, rows, slices, kv8 ? kMapFp8K : kMapBf16) ||
-        !make_kv_map(&mv, v_cache, rows, slices, kv8 ? kMapFp8V : kMapBf16)) {
-        snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
-        return DA_ERR_CUDA;
+    if (kv8) {  // contiguous blocks, copied without tensor maps
+        memset(&mk, 0, sizeof mk);
+        memset(&mv, 0, sizeof mv);
+    } else {
+        const uint64_t rows = ring ? static_cast<uint64_t>(window) : static_cast<uint64_t>(kPage);
+        const uint64_t slices = ring ? static_cast<uint64_t>(s.batch) * s.num_kv_heads
+                                     : static_cast<uint64_t>(num_pages) * s.num_kv_heads;
+        if (!make_kv_map(&mk, k_cache, rows, slices) || !make_kv_map(&mv, v_cache, rows, slices)) {
+            snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
+            return DA_ERR_CUDA;
+        }
     }
     if (kv8) {
         if (G <= 8)
@@ -1605,8 +1678,6 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.rope_cos = nullptr;
     prm.rope_sin = nullptr;
     prm.max_position = 0;
-    prm.k_scale = nullptr;
-    prm.v_scale = nullptr;
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call
@@ -1666,22 +1737,20 @@ int decode_attn_ring_rope(const void *q, const void *k_new, const void *v_new, v
                          kPage, 0, 0, 0, stream, rope_cos, rope_sin, max_position);
 }
 
-int decode_attn_paged_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache, void *vt_cache,
-                          float *k_scale, float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
-                          const float *sinks, int window, float scale, void *out, da_shape s, int page_size,
-                          int max_pages_per_seq, int num_pages, int max_seq_len, void *stream) {
-    if (!k_scale || !v_scale) return DA_ERR_INVALID_ARG;
-    return run_attention(false, q, k_new, v_new, k_cache, vt_cache, block_table, seq_lens, sinks, window, scale,
+int decode_attn_paged_fp8(const void *q, const void *k_new, const void *v_new, void *kv_cache,
+                          const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
+                          float scale, void *out, da_shape s, int page_size, int max_pages_per_seq, int num_pages,
+                          int max_seq_len, void *stream) {
+    return run_attention(false, q, k_new, v_new, kv_cache, nullptr, block_table, seq_lens, sinks, window, scale,
                          out, s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream, nullptr, nullptr, 0,
-                         k_scale, v_scale);
+                         true);
 }
 
-int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache, void *vt_cache,
-                         float *k_scale, float *v_scale, const int32_t *seq_lens, const float *sinks, int window,
-                         float scale, void *out, da_shape s, void *stream) {
-    if (!k_scale || !v_scale) return DA_ERR_INVALID_ARG;
-    return run_attention(true, q, k_new, v_new, k_cache, vt_cache, nullptr, seq_lens, sinks, window, scale, out,
-                         s, kPage, 0, 0, 0, stream, nullptr, nullptr, 0, k_scale, v_scale);
+int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_new, void *kv_cache,
+                         const int32_t *seq_lens, const float *sinks, int window, float scale, void *out,
+                         da_shape s, void *stream) {
+    return run_attention(true, q, k_new, v_new, kv_cache, nullptr, nullptr, seq_lens, sinks, window, scale, out,
+                         s, kPage, 0, 0, 0, stream, nullptr, nullptr, 0, true);
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, const int32_t *block_table,

@@ -12,8 +12,8 @@ query heads, 8 KV heads, head dim 64, page 16, window 128):
     are -1;
   * pools are either fully random (benchmark) or NaN-filled (tests, where the
     oracle writes the live tokens in and every dead cell stays NaN);
-  * fp8 pools (benchmark) hold uniform random finite e4m3 codes and per-token
-    scales uniform in [2/448, 3/448).
+  * fp8 pools (benchmark) are 2176-byte blocks of uniform random finite e4m3
+    codes and per-token scales uniform in [2/448, 3/448).
 """
 from __future__ import annotations
 
@@ -193,15 +193,7 @@ def draw_ring_pool(B, Hkv, W, D, gen, device="cpu", fill="randn") -> RingPool:
     return RingPool(k, v, W)
 
 
-@dataclass
-class Fp8Pool:
-    """fp8 (e4m3) cache arrays: K codes [.., Hkv, rows, D], V^T codes [.., Hkv, D, rows]
-    (uint8), per-token scales [.., Hkv, rows] fp32. `rows` is the page size (paged)
-    or the window (ring)."""
-    k_cache: torch.Tensor
-    vt_cache: torch.Tensor
-    k_scale: torch.Tensor
-    v_scale: torch.Tensor
+FP8_BLOCK_BYTES = 2176  # 16 tokens of one KV head: K codes, V^T codes, K and V scales
 
 
 def draw_fp8_codes(shape, gen, device="cpu") -> torch.Tensor:
@@ -219,18 +211,22 @@ def draw_fp8_scales(shape, gen, device="cpu") -> torch.Tensor:
     return (2.0 + u) / 448.0
 
 
-def draw_fp8_paged_pool(num_pages, Hkv, P, D, gen, device="cpu") -> Fp8Pool:
-    return Fp8Pool(draw_fp8_codes((num_pages, Hkv, P, D), gen, device),
-                   draw_fp8_codes((num_pages, Hkv, D, P), gen, device),
-                   draw_fp8_scales((num_pages, Hkv, P), gen, device),
-                   draw_fp8_scales((num_pages, Hkv, P), gen, device))
+def draw_fp8_blocks(lead, gen, P=16, D=64, device="cpu") -> torch.Tensor:
+    """fp8 cache blocks [*lead, 2PD + 8P] bytes: random codes (K rows, V^T) then random
+    per-token K and V scales."""
+    codes = draw_fp8_codes(tuple(lead) + (2 * P * D,), gen, device)
+    scales = draw_fp8_scales(tuple(lead) + (2 * P,), gen, device)
+    return torch.cat([codes, scales.view(torch.uint8)], dim=-1).contiguous()
 
 
-def draw_fp8_ring_pool(B, Hkv, W, D, gen, device="cpu") -> Fp8Pool:
-    return Fp8Pool(draw_fp8_codes((B, Hkv, W, D), gen, device),
-                   draw_fp8_codes((B, Hkv, D, W), gen, device),
-                   draw_fp8_scales((B, Hkv, W), gen, device),
-                   draw_fp8_scales((B, Hkv, W), gen, device))
+def draw_fp8_paged_pool(num_pages, Hkv, P, D, gen, device="cpu") -> torch.Tensor:
+    """[num_pages, Hkv, 2176]: one block per page and KV head."""
+    return draw_fp8_blocks((num_pages, Hkv), gen, P, D, device)
+
+
+def draw_fp8_ring_pool(B, Hkv, W, D, gen, device="cpu", P=16) -> torch.Tensor:
+    """[B, Hkv, W / 16, 2176]: the ring of capacity W as blocks of 16 cells."""
+    return draw_fp8_blocks((B, Hkv, W // P), gen, P, D, device)
 
 
 def draw_history(B, Tmax, Hkv, D, gen, device="cpu"):

@@ -1,7 +1,8 @@
 """GPU parity of the fp8 KV-cache path (decode_attn_paged_fp8 / _ring_fp8) against
 the fp64 oracle over the same e4m3 codes and scales: attention within
 4e-3 + 1e-2 |oracle|; the quantised append (K row, transposed V column, both
-scales) bit-exact; dead cells hold NaN codes and NaN scales."""
+scales) bit-exact, every other byte of the 2176-byte blocks untouched; dead
+cells hold NaN codes and NaN scales."""
 import numpy as np
 import pytest
 import torch
@@ -20,11 +21,16 @@ def pre(c):
 
 
 def to_dev(cache):
-    return [torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (cache.k, cache.vt, cache.ks, cache.vs)]
+    return torch.from_numpy(cache.blocks.copy()).to(DEV)
 
 
-def from_dev(ts):
-    return oracle.Fp8Cache(*[t.cpu().numpy() for t in ts])
+def from_dev(t):
+    return oracle.Fp8Cache(t.cpu().numpy())
+
+
+def assert_blocks_equal(got, want):
+    """Bit-exact: every byte of every block (codes, and the scales' bit patterns)."""
+    np.testing.assert_array_equal(got.blocks, want.blocks)
 
 
 def check_paged_fp8(c, window, seed, fused=True):
@@ -33,22 +39,18 @@ def check_paged_fp8(c, window, seed, fused=True):
     blank = oracle.Fp8Cache.empty_paged(kp.shape[0], c.Hkv, 16, c.D)
     cache = oracle.scatter_fp8(c.hist_k, c.hist_v, c.lens if not fused else pre(c), blank,
                                block_table=bt)
-    kc, vt, ks, vs = to_dev(cache)
+    kv = to_dev(cache)
     out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
     da.decode_attn_paged_fp8(dev_bits(c.q), dev_bits(c.k_new) if fused else None,
-                             dev_bits(c.v_new) if fused else None, kc, vt, ks, vs, dev(bt),
+                             dev_bits(c.v_new) if fused else None, kv, dev(bt),
                              dev(c.lens), dev(c.sinks), window, c.scale, out)
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
     ref = oracle.decode_paged_fp8(c.q, c.k_new if fused else None, c.v_new if fused else None,
                                   cache, bt, c.lens, c.sinks, window, c.scale)
     assert_close(out.double().cpu().numpy(), ref, f"paged fp8 window={window}")
-    got = from_dev((kc, vt, ks, vs))
     want = oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, block_table=bt) if fused else cache
-    np.testing.assert_array_equal(got.k, want.k)
-    np.testing.assert_array_equal(got.vt, want.vt)
-    np.testing.assert_array_equal(got.ks.view(np.uint32), want.ks.view(np.uint32))
-    np.testing.assert_array_equal(got.vs.view(np.uint32), want.vs.view(np.uint32))
+    assert_blocks_equal(from_dev(kv), want)
 
 
 EDGE = [1, 2, 15, 16, 17, 31, 33, 100, 257, 1000]
@@ -73,20 +75,16 @@ def test_ring_fp8_matches_oracle(W):
     c = make_case(730 + W, len(lens), 64, 8, 64, lens)
     blank = oracle.Fp8Cache.empty_ring(c.B, c.Hkv, W, c.D)
     cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c), blank, window=W)
-    kc, vt, ks, vs = to_dev(cache)
+    kv = to_dev(cache)
     out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
-    da.decode_attn_ring_fp8(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kc, vt, ks, vs,
+    da.decode_attn_ring_fp8(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kv,
                             dev(c.lens), dev(c.sinks), c.scale, out)
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
     ref = oracle.decode_ring_fp8(c.q, c.k_new, c.v_new, cache, c.lens, c.sinks, W, c.scale)
     assert_close(out.double().cpu().numpy(), ref, f"ring fp8 W={W}")
-    got = from_dev((kc, vt, ks, vs))
     want = oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, window=W)
-    np.testing.assert_array_equal(got.k, want.k)
-    np.testing.assert_array_equal(got.vt, want.vt)
-    np.testing.assert_array_equal(got.ks.view(np.uint32), want.ks.view(np.uint32))
-    np.testing.assert_array_equal(got.vs.view(np.uint32), want.vs.view(np.uint32))
+    assert_blocks_equal(from_dev(kv), want)
 
 
 def test_paged_fp8_inactive_slots():
@@ -118,12 +116,10 @@ def test_full_size_fp8(name):
     npages = wl.pool_size(name, lens)
     bt = wl.draw_block_table(lens, P, npages, wl.max_pages_per_seq(name, lens), gen)
     pool = wl.draw_fp8_paged_pool(npages, Hkv, P, D, vgen, device=DEV)
-    before = oracle.Fp8Cache(*[t.cpu().numpy() for t in (pool.k_cache, pool.vt_cache,
-                                                         pool.k_scale, pool.v_scale)])
+    before = from_dev(pool)
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
     sl = np.asarray(lens, np.int32)
-    da.decode_attn_paged_fp8(dev(inp.q), dev(inp.k_new), dev(inp.v_new), pool.k_cache,
-                             pool.vt_cache, pool.k_scale, pool.v_scale, dev(bt), dev(sl),
+    da.decode_attn_paged_fp8(dev(inp.q), dev(inp.k_new), dev(inp.v_new), pool, dev(bt), dev(sl),
                              dev(inp.sinks), 0, inp.scale, out)
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
@@ -134,7 +130,4 @@ def test_full_size_fp8(name):
     assert_close(np.stack([got[b, h] for b, h in items]), ref, f"{name} paged fp8")
     want = oracle.kv_append_fp8(wl.bits(inp.k_new), wl.bits(inp.v_new), before, sl,
                                 block_table=bt.numpy())
-    after = from_dev((pool.k_cache, pool.vt_cache, pool.k_scale, pool.v_scale))
-    assert np.array_equal(after.k, want.k) and np.array_equal(after.vt, want.vt)
-    assert np.array_equal(after.ks.view(np.uint32), want.ks.view(np.uint32))
-    assert np.array_equal(after.vs.view(np.uint32), want.vs.view(np.uint32))
+    assert_blocks_equal(from_dev(pool), want)

@@ -1,7 +1,8 @@
 """Pins for the oracle's fp8 (e4m3) KV cache: the codec against torch's
 float8_e4m3fn, the per-row quantisation rule in closed form, exact agreement
 with the bf16 oracle when every stored value is representable in both, layouts
-(paged with transposed V pages, ring) agreeing, and the quantised append."""
+(paged and ring blocks of 16 tokens: K rows, transposed V, scales) agreeing,
+the block layout byte by byte, and the quantised append."""
 import numpy as np
 import pytest
 import torch
@@ -76,7 +77,7 @@ def _exact_fp8_cache(seed, num_pages, Hkv, P, D):
         rng.integers(0, 2, size=k.shape, dtype=np.uint8) << 7)
     ks = (2.0 ** rng.integers(-6, -2, size=(num_pages, Hkv, P))).astype(np.float32)
     vs = (2.0 ** rng.integers(-6, -2, size=(num_pages, Hkv, P))).astype(np.float32)
-    cache = oracle.Fp8Cache(k, np.ascontiguousarray(vcodes.transpose(0, 1, 3, 2)), ks, vs)
+    cache = oracle.Fp8Cache.from_parts(k, vcodes.transpose(0, 1, 3, 2), ks, vs)
     kdeq = oracle.e4m3_decode(k) * ks[..., None]
     vdeq = oracle.e4m3_decode(vcodes) * vs[..., None]
     from cases import f64_to_bf16_bits
@@ -124,3 +125,40 @@ def test_paged_and_ring_agree_and_append_is_fused():
     # the fp8 step is close to the bf16 step on the same (unquantised) history
     bf = oracle.decode_paged(c.q, c.k_new, c.v_new, kp, vp, bt, c.lens, c.sinks, 0, c.scale, 16)
     assert np.all(np.abs(a - bf) <= 0.1 * np.abs(bf) + 0.1)   # loose: e4m3 keeps 3 mantissa bits
+
+
+def test_block_layout_byte_by_byte():
+    """One token written into an empty cache lands at the documented bytes: K codes at
+    slot * 64, V codes at 1024 + d * 16 + slot, K scale at 2048 + 4 slot, V scale at
+    2112 + 4 slot of block page * Hkv + g (paged) or (b * Hkv + g) * W/16 + cell/16 (ring)."""
+    c = make_case(604, 2, 4, 2, 64, [21, 37])
+    x = c.hist_k[1, 36, 1]                       # token 36 of sequence 1, head 1
+    y = c.hist_v[1, 36, 1]
+    kc, ksc = oracle.quantise_rows(x[None])
+    vc, vsc = oracle.quantise_rows(y[None])
+    bt = np.array([[5, 0, -1], [3, 1, 2]], np.int32)   # token 36 -> page bt[1][2] = 2, slot 4
+    paged = oracle.kv_append_fp8(c.k_new, c.v_new, oracle.Fp8Cache.empty_paged(6, 2, 16, 64),
+                                 c.lens, block_table=bt)
+    blk = paged.blocks[2, 1]
+    np.testing.assert_array_equal(blk[4 * 64:5 * 64], kc[0])
+    np.testing.assert_array_equal(blk[1024 + np.arange(64) * 16 + 4], vc[0])
+    assert blk[2048 + 16:2048 + 20].view(np.float32)[0] == ksc[0]
+    assert blk[2112 + 16:2112 + 20].view(np.float32)[0] == vsc[0]
+    # every other byte of the pool is untouched (the fill code, NaN scales): the append
+    # writes slot 4 of page 2 (sequence 1, token 36) and of page 0 (sequence 0, token 20)
+    touched = np.zeros(paged.blocks.shape, bool)
+    for page in (2, 0):
+        for g in range(2):
+            t = touched[page, g]
+            t[4 * 64:5 * 64] = True
+            t[1024 + np.arange(64) * 16 + 4] = True
+            t[2064:2068] = t[2128:2132] = True
+    empty = oracle.Fp8Cache.empty_paged(6, 2, 16, 64).blocks
+    np.testing.assert_array_equal(paged.blocks[~touched], empty[~touched])
+    # ring of capacity 32: token 36 sits in cell 4 = block 0 of (1, 1), slot 4
+    ring = oracle.kv_append_fp8(c.k_new, c.v_new, oracle.Fp8Cache.empty_ring(2, 2, 32, 64), c.lens,
+                                window=32)
+    rb = ring.blocks[1, 1, 0]
+    np.testing.assert_array_equal(rb[4 * 64:5 * 64], kc[0])
+    np.testing.assert_array_equal(rb[1024 + np.arange(64) * 16 + 4], vc[0])
+    assert rb[2064:2068].view(np.float32)[0] == ksc[0] and rb[2128:2132].view(np.float32)[0] == vsc[0]

@@ -54,10 +54,14 @@ MUTANTS = [
     ("e4m3_bias", "ldexp(1.0 + m / 8.0, e - 7);", "ldexp(1.0 + m / 8.0, e - 8);"),
     ("e4m3_ties_away", "if (rem > step / 2 || (rem == step / 2 && fmod(k, 2.0) == 1.0)) k += 1.0;",
      "if (rem >= step / 2) k += 1.0;"),
-    ("fp8_vt_stride", "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]) * sv;",
-     "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d]) * sv;"),
-    ("fp8_no_vscale", "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]) * sv;",
-     "v[d] = e4m3_decode(pr->vct[vbase + (size_t)d * vstride]);"),
+    ("fp8_vt_stride", "v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d * P + slot]) * sv;",
+     "v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d + slot]) * sv;"),
+    ("fp8_no_vscale", "v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d * P + slot]) * sv;",
+     "v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d * P + slot]);"),
+    ("fp8_scales_swapped", "const double sk = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)slot);",
+     "const double sk = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)(P + slot));"),
+    ("fp8_ring_block", "return ((long long)b * Hkv + g) * (W / P) + cell / P;",
+     "return ((long long)g * 64 + b) * (W / P) + cell / P;"),
     ("fp8_scale_rule", "amax / 448.0f", "amax / 447.0f"),
     ("append_wrong_cell",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
@@ -87,6 +91,7 @@ PIN_CALLS = [
     fp8_pins.test_quantisation_rule_closed_form,
     lambda: fp8_pins.test_fp8_equals_bf16_on_values_exact_in_both(0),
     fp8_pins.test_paged_and_ring_agree_and_append_is_fused,
+    fp8_pins.test_block_layout_byte_by_byte,
 ]
 
 
