@@ -624,24 +624,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n_tiles > 32) load_batch(1, nb, ng, ntl, np);
         int cur_batch = 0;
 
-        auto issue = [&](int i) {
-            if ((i >> 5) != cur_batch) {  // advance to the next batch, prefetch the one after
+        // Copies of tiles j0 .. j0 + cnt - 1 (cnt <= kStages, calls in increasing order): lane u
+        // issues tile j0 + u into stage (stg0 + u) mod kStages, so several tiles go out at once.
+        auto issue_n = [&](int j0, int cnt, int stg0) {
+            if ((j0 >> 5) != cur_batch) {  // advance to the next batch, prefetch the one after
                 cb = nb; cg = ng; ct = ntl; cp = np;
-                cur_batch = i >> 5;
+                ++cur_batch;
                 if (n_tiles > 32 * (cur_batch + 1)) load_batch(cur_batch + 1, nb, ng, ntl, np);
             }
-            const int src = i & 31;
-            const int tb = __shfl_sync(0xffffffffu, cb, src);
-            const int tg = __shfl_sync(0xffffffffu, cg, src);
-            const int tt = __shfl_sync(0xffffffffu, ct, src);
+            const int j = j0 + (lane < cnt ? lane : 0);
+            const int src = j & 31;
+            int tb = __shfl_sync(0xffffffffu, cb, src);
+            int tg = __shfl_sync(0xffffffffu, cg, src);
+            int tt = __shfl_sync(0xffffffffu, ct, src);
             int tp = __shfl_sync(0xffffffffu, cp, src);
-            if (lane == 0) {
-                const int stg = i % kStages;
+            const bool nxt = (j >> 5) != cur_batch;  // this lane's tile is in the prefetched batch
+            if (__any_sync(0xffffffffu, nxt)) {
+                const int b2 = __shfl_sync(0xffffffffu, nb, src);
+                const int g2 = __shfl_sync(0xffffffffu, ng, src);
+                const int t2 = __shfl_sync(0xffffffffu, ntl, src);
+                const int p2 = __shfl_sync(0xffffffffu, np, src);
+                if (nxt) { tb = b2; tg = g2; tt = t2; tp = p2; }
+            }
+            if (lane < cnt) {
+                const int stg = stg0 + lane < kStages ? stg0 + lane : stg0 + lane - kStages;
                 if (!RING && (tp < 0 || tp >= p.num_pages)) {
                     flag_status(DA_STATUS_BAD_PAGE);
                     tp = -1;  // TMA reads zeros out of bounds
                 }
-                const bool newseg = (i == 0) || (tt == 0);
+                const bool newseg = (j == 0) || (tt == 0);
                 wmeta[stg] = make_int4(tb, tg, tt, tp);
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = newseg && p.k_new != nullptr;
@@ -682,8 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        const int pro = n_tiles < kStages ? n_tiles : kStages;
-        for (int i = 0; i < pro; ++i) issue(i);
+        issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0);
 
         // segment context
         int sb = -1, sgk = -1;  // current segment (b, g)
@@ -697,12 +707,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One pass over UT (1 or 2) consecutive tiles i .. i + UT - 1 of the current segment.
         // Two tiles give each warp two independent load / convert / MMA chains and one
         // online-softmax update per 32 tokens.
-        auto tiles_step = [&](auto ut_c) {
+        auto tiles_step = [&](auto ut_c, int st0, int st1) {
             constexpr int UT = decltype(ut_c)::value;
             int stgs[UT], tts[UT], tps[UT];
 #pragma unroll
             for (int u = 0; u < UT; ++u) {
-                stgs[u] = (i + u) % kStages;
+                stgs[u] = u == 0 ? st0 : st1;
                 const int4 m = wmeta[stgs[u]];
                 tts[u] = m.z;
                 tps[u] = m.w;
@@ -925,18 +935,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 
             __syncwarp();
-            // refill the stages just read
-            if (i + kStages < n_tiles) {
-                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-#pragma unroll
-                for (int u = 0; u < UT; ++u)
-                    if (i + u + kStages < n_tiles) issue(i + u + kStages);
+            // refill the stages just read (tile i + u + kStages goes where tile i + u was)
+            const int nref = min(UT, n_tiles - (i + kStages));
+            if (nref > 0) {
+                if (lane < nref) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_n(i + kStages, nref, st0);
             }
         };
 
+        int stg = 0;       // stage of tile i
+        uint32_t ph = 0;   // parity of its barrier phase
         while (i < n_tiles) {
-            const int stg = i % kStages;
-            if (!mbar_wait_bounded(bar0 + 8 * stg, (i / kStages) & 1)) {
+            if (!mbar_wait_bounded(bar0 + 8 * stg, ph)) {
                 failed = true;
                 break;
             }
@@ -1044,19 +1054,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 state_reset(st);
             }
             // the next tile continues this segment: take both in one pass
+            int stg1 = stg + 1;
+            uint32_t ph1 = ph;
+            if (stg1 == kStages) { stg1 = 0; ph1 ^= 1u; }
             if constexpr (kPair) {
                 if (i + 1 < n_tiles && ua + i + 1 < seg_end_unit) {
-                    if (!mbar_wait_bounded(bar0 + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1)) {
+                    if (!mbar_wait_bounded(bar0 + 8 * stg1, ph1)) {
                         failed = true;
                         break;
                     }
-                    tiles_step(std::integral_constant<int, 2>{});
+                    tiles_step(std::integral_constant<int, 2>{}, stg, stg1);
                     i += 2;
+                    stg = stg1 + 1;
+                    ph = ph1;
+                    if (stg == kStages) { stg = 0; ph ^= 1u; }
                     continue;
                 }
             }
-            tiles_step(std::integral_constant<int, 1>{});
+            tiles_step(std::integral_constant<int, 1>{}, stg, stg);
             i += 1;
+            stg = stg1;
+            ph = ph1;
         }
         if (failed) {
             flag_status(DA_STATUS_TIMEOUT);
