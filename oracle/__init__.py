@@ -23,7 +23,8 @@ _FUNCS = ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
           "oracle_scatter_ring", "oracle_rope_q64", "oracle_rope_k", "oracle_decode_paged_rope",
           "oracle_decode_ring_rope", "oracle_e4m3_decode", "oracle_e4m3_encode",
           "oracle_quantise_rows", "oracle_decode_paged_fp8", "oracle_decode_ring_fp8",
-          "oracle_kv_append_fp8", "oracle_scatter_fp8")
+          "oracle_kv_append_fp8", "oracle_scatter_fp8", "oracle_decode_multi",
+          "oracle_kv_append_multi")
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -79,6 +80,12 @@ def _load():
         lib.oracle_scatter_fp8.argtypes = [
             _u16p, _u16p, _i32p, c_int, _i32p, c_int, _u8p, c_int, c_int, c_int, c_int, c_int,
             c_int]
+        lib.oracle_decode_multi.argtypes = [
+            c_int, _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _f32p, c_int, c_double,
+            _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int]
+        lib.oracle_kv_append_multi.argtypes = [
+            c_int, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, c_int, c_int, c_int, c_int,
+            c_int, c_int, c_int, c_int]
         for name in _FUNCS:
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -513,3 +520,44 @@ def decode_ring_fp8(q, k_new, v_new, cache, seq_lens, sinks, window, scale, item
         _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D,
         _ptr(it, _i32p), n_items, nthreads or default_threads()), "decode_ring_fp8")
     return out
+
+
+# ---------------------------------------------------------------- several query tokens
+def decode_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, window, scale,
+                 block_table=None, q_lens=None, page_size=16, nthreads=None):
+    """q [B, T, Hq, D], k_new / v_new [B, T, Hkv, D] (bf16 bits); caches hold the history
+    before the step (paged when a block table is given, else the ring of capacity `window`).
+    Returns out [B, T, Hq, D] float64."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    kc, vc = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    sl, ql, sk = _i32(seq_lens), _i32(q_lens), _f32(sinks)
+    B, T, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    ring = block_table is None
+    bt = None if ring else _i32(block_table)
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_multi(
+        int(ring), _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(kc, _u16p),
+        _ptr(vc, _u16p), _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(ql, _i32p), _ptr(sk, _f32p),
+        int(window), float(scale), _ptr(out, _f64p), B, T, Hq, Hkv, D, page_size,
+        0 if ring else bt.shape[1], 0 if ring else kc.shape[0], nthreads or default_threads()),
+        "decode_multi")
+    return out
+
+
+def kv_append_multi(k_new, v_new, k_cache, v_cache, seq_lens, window=0, block_table=None,
+                    q_lens=None, page_size=16):
+    """Copies of the caches with the step's n = q_lens[b] (or T) new tokens appended."""
+    lib = _load()
+    kn, vn = _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    kc, vc = _u16(k_cache, "k_cache").copy(), _u16(v_cache, "v_cache").copy()
+    sl, ql = _i32(seq_lens), _i32(q_lens)
+    B, T, Hkv, D = kn.shape
+    ring = block_table is None
+    bt = None if ring else _i32(block_table)
+    _check(lib.oracle_kv_append_multi(
+        int(ring), _ptr(kn, _u16p), _ptr(vn, _u16p), _ptr(kc, _u16p), _ptr(vc, _u16p),
+        _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(ql, _i32p), int(window), B, T, Hkv, D, page_size,
+        0 if ring else bt.shape[1], 0 if ring else kc.shape[0]), "kv_append_multi")
+    return kc, vc

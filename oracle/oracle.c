@@ -790,3 +790,171 @@ int oracle_scatter_fp8(const uint16_t *hist_k, const uint16_t *hist_v, const int
     }
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* Several query tokens per sequence in one step (reading of the chapters "Chunked
+ * Prefill" and "Speculative Decoding" named in the teaching repo's table "The files",
+ * page "Run it locally": both run attention for a run of new tokens over the cached
+ * history, each new token seeing the history and the new tokens before it).
+ *
+ *   n = q_lens[b] (T when q_lens is NULL) new tokens, at positions base .. L-1 with
+ *   L = seq_lens[b] and base = L - n (n <= T, n <= L). Query row (t, h), t < n, sits at
+ *   p = base + t and attends the positions j with lo <= j <= p (causal), lo = max(0,
+ *   p - W + 1) when a window W > 0 applies (always for the ring), else 0. Position
+ *   j >= base is new token j - base (k_new / v_new [B][T][Hkv][D]); j < base comes from
+ *   the cache. Rows t >= n, and every row of an inactive slot (L = 0), are zero.
+ *   q / out are [B][T][Hq][D].
+ *
+ * The cache holds the history before this step: the ring of capacity W holds positions
+ * max(0, base - W) .. base - 1 (cell j % W). The n new tokens are appended afterwards
+ * (oracle_kv_append_multi); the ring's early queries still see the cells that the later
+ * new tokens overwrite, so the append cannot come first. */
+
+typedef struct {
+    int ring;
+    const uint16_t *q, *k_new, *v_new, *k_cache, *v_cache;
+    const int32_t *block_table, *seq_lens, *q_lens;
+    const float *sinks;
+    int window; double scale;
+    int B, T, Hq, Hkv, D, P, max_pages, num_pages;
+    double *out;
+} problemM;
+
+static int q_count(const int32_t *q_lens, int T, int b) { return q_lens ? q_lens[b] : T; }
+
+/* key (v = 0) or value (v = 1) row of position j for (b, g); NULL for a bad page */
+static const uint16_t *rowM(const problemM *pr, int b, int g, int j, int v) {
+    const int L = pr->seq_lens[b], base = L - q_count(pr->q_lens, pr->T, b), D = pr->D;
+    if (j >= base) {
+        const int t = j - base;
+        return (v ? pr->v_new : pr->k_new) + (((size_t)b * pr->T + t) * pr->Hkv + g) * D;
+    }
+    const uint16_t *cache = v ? pr->v_cache : pr->k_cache;
+    if (pr->ring) {
+        const int cell = j % pr->window;
+        return cache + (((size_t)b * pr->Hkv + g) * pr->window + cell) * D;
+    }
+    if (j / pr->P >= pr->max_pages) return NULL;
+    const int32_t page = pr->block_table[(size_t)b * pr->max_pages + j / pr->P];
+    if (page < 0 || page >= pr->num_pages) return NULL;
+    return cache + (((size_t)page * pr->Hkv + g) * pr->P + j % pr->P) * D;
+}
+
+static int attend_oneM(const problemM *pr, int b, int t, int h, double *out) {
+    const int D = pr->D, L = pr->seq_lens[b], n = q_count(pr->q_lens, pr->T, b);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (L <= 0 || t >= n) return OR_OK;
+    const int g = h / (pr->Hq / pr->Hkv);
+    const int p = L - n + t;
+    const int W = pr->window;
+    const int lo = (W > 0 && p - W + 1 > 0) ? p - W + 1 : 0;
+    const int cnt = p - lo + 1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)cnt);
+    if (!s) return OR_NOMEM;
+    const uint16_t *qrow = pr->q + (((size_t)b * pr->T + t) * pr->Hq + h) * D;
+    const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;
+    double M = sigma;
+    for (int i = 0; i < cnt; ++i) {
+        const uint16_t *krow = rowM(pr, b, g, lo + i, 0);
+        if (!krow) { free(s); return OR_BAD_INDEX; }
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+        s[i] = pr->scale * dot;
+        if (s[i] > M) M = s[i];
+    }
+    double den = isinf(sigma) && sigma < 0 ? 0.0 : exp(sigma - M);
+    for (int i = 0; i < cnt; ++i) {
+        const uint16_t *vrow = rowM(pr, b, g, lo + i, 1);
+        const double w = exp(s[i] - M);
+        den += w;
+        for (int d = 0; d < D; ++d) out[d] += w * bf16_to_f64(vrow[d]);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= den;
+    free(s);
+    return OR_OK;
+}
+
+typedef struct { problemM *pr; int tid, nthreads, status; } workerM_arg;
+
+static void *workerM(void *arg) {
+    workerM_arg *a = (workerM_arg *)arg;
+    problemM *pr = a->pr;
+    const long long total = (long long)pr->B * pr->T * pr->Hq;
+    for (long long w = a->tid; w < total; w += a->nthreads) {
+        const int h = (int)(w % pr->Hq), t = (int)((w / pr->Hq) % pr->T), b = (int)(w / ((long long)pr->Hq * pr->T));
+        const int st = attend_oneM(pr, b, t, h, pr->out + (size_t)w * pr->D);
+        if (st != OR_OK && a->status == OR_OK) a->status = st;
+    }
+    return NULL;
+}
+
+static int check_counts(const int32_t *seq_lens, const int32_t *q_lens, int B, int T) {
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b], n = q_count(q_lens, T, b);
+        if (L < 0 || n < 0 || n > T || (L > 0 && n > L)) return OR_BAD_ARG;
+    }
+    return OR_OK;
+}
+
+int oracle_decode_multi(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                        const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_table,
+                        const int32_t *seq_lens, const int32_t *q_lens, const float *sinks, int window,
+                        double scale, double *out, int B, int T, int Hq, int Hkv, int D, int page_size,
+                        int max_pages, int num_pages, int nthreads) {
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !out || B < 0 || T <= 0 || Hq <= 0 ||
+        Hkv <= 0 || Hq % Hkv || D <= 0 || window < 0 || (ring && window <= 0) ||
+        (!ring && (!block_table || page_size <= 0 || max_pages <= 0 || num_pages <= 0)))
+        return OR_BAD_ARG;
+    if (check_counts(seq_lens, q_lens, B, T) != OR_OK) return OR_BAD_ARG;
+    problemM pr = {ring, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks, window, scale,
+                   B, T, Hq, Hkv, D, page_size, max_pages, num_pages, out};
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    workerM_arg args[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) { args[t].pr = &pr; args[t].tid = t; args[t].nthreads = nthreads; args[t].status = OR_OK; }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, workerM, &args[t]) != 0) break;
+        started = t;
+    }
+    for (int t = started + 1; t < nthreads; ++t) workerM(&args[t]);
+    workerM(&args[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    for (int t = 0; t < nthreads; ++t) if (args[t].status != OR_OK) return args[t].status;
+    return OR_OK;
+}
+
+/* The append of a multi-token step: new token t < n of b goes to position L - n + t (paged:
+ * its page and slot; ring of capacity W: cell (L - n + t) % W). */
+int oracle_kv_append_multi(int ring, const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_cache,
+                           uint16_t *v_cache, const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *q_lens, int window, int B, int T, int Hkv, int D, int page_size,
+                           int max_pages, int num_pages) {
+    if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens || (ring && window <= 0) ||
+        (!ring && (!block_table || page_size <= 0 || max_pages <= 0)))
+        return OR_BAD_ARG;
+    if (check_counts(seq_lens, q_lens, B, T) != OR_OK) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b], n = q_count(q_lens, T, b);
+        if (L <= 0) continue;
+        for (int t = 0; t < n; ++t) {
+            const int pos = L - n + t;
+            for (int g = 0; g < Hkv; ++g) {
+                size_t dst;
+                if (ring) {
+                    dst = (((size_t)b * Hkv + g) * window + pos % window) * D;
+                } else {
+                    if (pos / page_size >= max_pages) return OR_BAD_INDEX;
+                    const int32_t page = block_table[(size_t)b * max_pages + pos / page_size];
+                    if (page < 0 || page >= num_pages) return OR_BAD_INDEX;
+                    dst = (((size_t)page * Hkv + g) * page_size + pos % page_size) * D;
+                }
+                const size_t src = (((size_t)b * T + t) * Hkv + g) * D;
+                memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
+                memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+            }
+        }
+    }
+    return OR_OK;
+}

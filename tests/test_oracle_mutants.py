@@ -10,6 +10,7 @@ import pytest
 import oracle
 import test_oracle as pins
 import test_oracle_fp8 as fp8_pins
+import test_oracle_multi as multi_pins
 import test_oracle_rope as rope_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -63,6 +64,16 @@ MUTANTS = [
     ("fp8_ring_block", "return ((long long)b * Hkv + g) * (W / P) + cell / P;",
      "return ((long long)g * 64 + b) * (W / P) + cell / P;"),
     ("fp8_scale_rule", "amax / 448.0f", "amax / 447.0f"),
+    ("multi_not_causal_self", "const int cnt = p - lo + 1;", "const int cnt = p - lo;"),
+    ("multi_position_shift", "const int p = L - n + t;", "const int p = L - n + t - 1;"),
+    ("multi_new_token_index", "const int t = j - base;", "const int t = j - base + 1;"),
+    ("multi_window_one_long", "const int lo = (W > 0 && p - W + 1 > 0) ? p - W + 1 : 0;",
+     "const int lo = (W > 0 && p - W > 0) ? p - W : 0;"),
+    ("multi_q_lens_ignored", "static int q_count(const int32_t *q_lens, int T, int b) { return q_lens ? q_lens[b] : T; }",
+     "static int q_count(const int32_t *q_lens, int T, int b) { (void)q_lens; (void)b; return T; }"),
+    ("multi_append_shift", "const int pos = L - n + t;", "const int pos = L - n + t + 1;"),
+    ("multi_q_token_stride", "const uint16_t *qrow = pr->q + (((size_t)b * pr->T + t) * pr->Hq + h) * D;",
+     "const uint16_t *qrow = pr->q + (((size_t)t * pr->B + b) * pr->Hq + h) * D;"),
     ("append_wrong_cell",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(L % page_size)) * D;"),
@@ -92,6 +103,13 @@ PIN_CALLS = [
     lambda: fp8_pins.test_fp8_equals_bf16_on_values_exact_in_both(0),
     fp8_pins.test_paged_and_ring_agree_and_append_is_fused,
     fp8_pins.test_block_layout_byte_by_byte,
+    lambda: multi_pins.test_multi_brute_force_paged(0, 3),
+    lambda: multi_pins.test_multi_brute_force_ring(1, 16),
+    multi_pins.test_multi_equals_torch_sdpa_with_causal_mask,
+    multi_pins.test_one_token_equals_the_single_token_step,
+    multi_pins.test_rows_beyond_q_lens_and_inactive_slots_are_zero,
+    lambda: multi_pins.test_append_is_bit_exact_and_touches_only_the_new_cells(True),
+    lambda: multi_pins.test_append_is_bit_exact_and_touches_only_the_new_cells(False),
 ]
 
 
