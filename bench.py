@@ -108,8 +108,13 @@ def nominal_hbm_peak():
 
 
 def source_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of the kernel sources (every .cu / .cuh of csrc, in name order)."""
+    h = hashlib.sha256()
+    csrc = os.path.dirname(KERNEL_SRC)
+    for name in sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload, kind):

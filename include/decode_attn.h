@@ -182,6 +182,49 @@ DA_API int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_
                                 int window, float scale, void *out, da_shape s, void *stream);
 
 /*
+ * decode_attn_paged_multi / decode_attn_ring_multi -- several query tokens per sequence in
+ * one call: speculative verification (draft tokens checked in one step) and chunked
+ * prefill appending a run of tokens into pages (the teaching repo's chapters "Speculative
+ * Decoding" and "Chunked Prefill", table "The files" on the page "Run it locally", name
+ * both; the plain causal reading is used).
+ *   q_tokens = T; n_b = q_lens[b] (T when q_lens == NULL), 0 <= n_b <= T, n_b <= seq_lens[b];
+ *   seq_lens[b] = L counts the cached tokens plus the n_b new ones (0 = inactive slot).
+ *   New token t < n_b sits at position p = L - n_b + t. Query row (t, h) attends the
+ *   positions lo..p (causal), lo = max(0, p - W + 1) under a window (paged: window > 0;
+ *   ring: always, W = its capacity), else 0; GQA, sinks and scale as in decode_attn_paged.
+ *   Positions >= L - n_b are the new tokens, read from k_new / v_new; the others come from
+ *   the cache, which holds the history before the call. Afterwards the n_b new tokens are
+ *   written into their cells (paged: their pages; ring: cell p % W, the last W of them).
+ *   Rows t >= n_b and inactive slots are written as zero.
+ *   q, out        [B, T, Hq, 64] bf16 (device)
+ *   k_new, v_new  [B, T, Hkv, 64] bf16 (device, required), rows t >= n_b ignored
+ *   q_lens        [B] int32 (device) or NULL
+ *   caches, block_table, sinks, page_size, max_pages_per_seq, num_pages, max_seq_len:
+ *                 as in decode_attn_paged / decode_attn_ring (the ring's W >= 16).
+ * Two kernels on `stream`: the attention, then the append (the ring's early query tokens
+ * still read the cells the later new tokens overwrite). Split partials and counters live
+ * in a second library workspace (decode_attn_multi_workspace_bytes / _reserve); it is
+ * allocated on first use outside graph capture, else DA_ERR_WORKSPACE. T <= 4096.
+ * Bad lengths (n_b > T, n_b > L, L beyond the block table) set DA_STATUS_BAD_SEQ_LEN and
+ * the slot is treated as inactive.
+ */
+DA_API int decode_attn_paged_multi(const void *q, const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *block_table,
+                                   const int32_t *seq_lens, const int32_t *q_lens,
+                                   const float *sinks, int window, float scale, void *out,
+                                   da_shape s, int q_tokens, int page_size, int max_pages_per_seq,
+                                   int num_pages, int max_seq_len, void *stream);
+DA_API int decode_attn_ring_multi(const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const int32_t *seq_lens,
+                                  const int32_t *q_lens, const float *sinks, int window,
+                                  float scale, void *out, da_shape s, int q_tokens, void *stream);
+/* Bytes of the multi-token workspace for a shape, T, the ring capacity (0 for paged calls)
+ * and the longest sequence; decode_attn_multi_reserve allocates it (call before capture). */
+DA_API size_t decode_attn_multi_workspace_bytes(da_shape s, int q_tokens, int ring_window,
+                                                int max_seq_len);
+DA_API int decode_attn_multi_reserve(size_t bytes);
+
+/*
  * kv_append -- the append alone: bit-copies k_new/v_new [B, Hkv, D] of every
  * active sequence into the cell of position p = seq_lens[b] - 1.
  * block_table != NULL: paged cache (page_size, max_pages_per_seq, num_pages as

@@ -29,6 +29,8 @@ __all__ = [
     "decode_attn_error_string", "library_path", "load_library",
     "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT", "DA_STATUS_BAD_POSITION",
     "decode_attn_paged_rope", "decode_attn_ring_rope", "decode_attn_paged_fp8", "decode_attn_ring_fp8",
+    "decode_attn_paged_multi", "decode_attn_ring_multi", "decode_attn_multi_workspace_bytes",
+    "decode_attn_multi_reserve",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -89,6 +91,14 @@ def load_library():
                                           da_shape, c_int, c_int, c_int, c_int, vp]
     lib.decode_attn_ring_fp8.argtypes = [vp, vp, vp, vp, i32p, f32p, c_int, c_float, vp, da_shape,
                                          vp]
+    lib.decode_attn_paged_multi.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, i32p, f32p, c_int,
+                                            c_float, vp, da_shape, c_int, c_int, c_int, c_int,
+                                            c_int, vp]
+    lib.decode_attn_ring_multi.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, f32p, c_int, c_float,
+                                           vp, da_shape, c_int, vp]
+    lib.decode_attn_multi_workspace_bytes.argtypes = [da_shape, c_int, c_int, c_int]
+    lib.decode_attn_multi_workspace_bytes.restype = ctypes.c_size_t
+    lib.decode_attn_multi_reserve.argtypes = [ctypes.c_size_t]
     lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
@@ -97,7 +107,8 @@ def load_library():
     lib.decode_attn_error_string.restype = ctypes.c_char_p
     for fn in (lib.decode_attn_paged, lib.decode_attn_ring, lib.kv_append, lib.decode_attn_reserve,
                lib.decode_attn_device_status, lib.decode_attn_paged_rope, lib.decode_attn_ring_rope,
-               lib.decode_attn_paged_fp8, lib.decode_attn_ring_fp8):
+               lib.decode_attn_paged_fp8, lib.decode_attn_ring_fp8, lib.decode_attn_paged_multi,
+               lib.decode_attn_ring_multi, lib.decode_attn_multi_reserve):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -231,6 +242,49 @@ def kv_append(k_new, v_new, k_cache, v_cache, seq_lens, block_table=None, stream
         args = (W, da_shape(B, Hkv, Hkv, D), 0, 0, 0)
     _check(lib.kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                          _ptr(block_table), _ptr(seq_lens), *args, _stream(stream)))
+
+
+def decode_attn_paged_multi(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window,
+                            scale, out, q_lens=None, max_seq_len=None, stream=None):
+    """Several query tokens per sequence: q / out [B, T, Hq, 64], k_new / v_new [B, T, Hkv, 64]
+    bf16; seq_lens counts the cached tokens plus the q_lens[b] (or T) new ones. Attention is
+    causal over the cache and the new tokens, which are then appended to the pages."""
+    B, T, Hq, D = q.shape
+    num_pages, Hkv = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * 16
+    lib = load_library()
+    _check(lib.decode_attn_paged_multi(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(q_lens), _ptr(sinks), int(window), float(scale), _ptr(out),
+        da_shape(B, Hq, Hkv, D), T, 16, max_pages, num_pages, int(max_seq_len), _stream(stream)))
+    return out
+
+
+def decode_attn_ring_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, scale, out,
+                           q_lens=None, stream=None):
+    """decode_attn_paged_multi over a ring of capacity W = k_cache.shape[2]; the ring holds
+    the window of the history before the step."""
+    B, T, Hq, D = q.shape
+    Hkv, W = k_cache.shape[1], k_cache.shape[2]
+    lib = load_library()
+    _check(lib.decode_attn_ring_multi(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        _ptr(q_lens), _ptr(sinks), int(W), float(scale), _ptr(out), da_shape(B, Hq, Hkv, D), T,
+        _stream(stream)))
+    return out
+
+
+def decode_attn_multi_workspace_bytes(batch, num_q_heads, num_kv_heads, q_tokens, ring_window=0,
+                                      max_seq_len=0, head_dim=64):
+    return int(load_library().decode_attn_multi_workspace_bytes(
+        da_shape(batch, num_q_heads, num_kv_heads, head_dim), int(q_tokens), int(ring_window),
+        int(max_seq_len)))
+
+
+def decode_attn_multi_reserve(nbytes: int):
+    _check(load_library().decode_attn_multi_reserve(int(nbytes)))
 
 
 def decode_attn_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim=64, max_seq_len=0):

@@ -1,6 +1,6 @@
 """Build the CUDA library libdecode_attn.so in-tree for GB300 (sm_103a).
 
-One translation unit, nvcc, static CUDA runtime; the driver API entry used
+One translation unit (decode_attn.cu, which includes multi_attn.cuh), nvcc, static CUDA runtime; the driver API entry used
 for tensor maps is resolved at run time, so the library loads on a machine
 without a GPU (for the ABI checks) and needs no libcuda at link time.
 """
@@ -23,7 +23,9 @@ def nvcc() -> str:
 
 def build(force: bool = False, extra_flags=(), out: str = LIB, verbose: bool = False) -> str:
     """Compile the library unless it is newer than its sources."""
-    newest = max(os.path.getmtime(SRC), os.path.getmtime(HDR))
+    csrc = os.path.dirname(SRC)
+    deps = [os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))] + [HDR]
+    newest = max(os.path.getmtime(f) for f in deps)
     if not force and not extra_flags and os.path.exists(out) and os.path.getmtime(out) >= newest:
         return out
     tmp = out + f".tmp{os.getpid()}"

@@ -36,6 +36,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <stdint.h>
 #include <stdio.h>
@@ -1342,6 +1343,9 @@ __global__ void kv_append_kernel(const __nv_bfloat16 *__restrict__ k_new,
     }
 }
 
+// ------------------------------------------------------------------ several query tokens
+#include "multi_attn.cuh"
+
 // ------------------------------------------------------------------ host side
 thread_local char t_err[256];
 
@@ -1427,8 +1431,11 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     void *ws = nullptr;
     size_t ws_bytes = 0;
+    void *ws_multi = nullptr;  // multi-token calls: counters + split partials
+    size_t ws_multi_bytes = 0;
     int sm_count = 0;
     bool attr_set[16] = {};
+    bool multi_attr_set[2] = {};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -1632,6 +1639,202 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
                 : launch_attn<2, false, false>(mk, mv, prm, dev, stream);
 }
 
+// ------------------------------------------------------------------ several query tokens: host side
+// k_new / v_new [B][T][Hkv][64] bf16 seen as tiles of 16 tokens of one KV head:
+// dims {64, Hkv, T, B}, box {64, 1, 16, 1}, 128-byte swizzle (the cache tiles' layout).
+bool make_new_map(CUtensorMap *map, const void *base, int Hkv, int T, int B) {
+    const int kind = 1000 + Hkv;  // cache key: never equal to a cache view's kind
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < kMapCache; ++i) {
+        const MapCacheEntry &e = g_maps[i];
+        if (e.base == base && e.kind == kind && e.rows == static_cast<uint64_t>(T) &&
+            e.slices == static_cast<uint64_t>(B)) {
+            *map = e.map;
+            return true;
+        }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Hkv),
+                                static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(Hkv) * kD * 2,
+                                   static_cast<cuuint64_t>(T) * Hkv * kD * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kD), 1, static_cast<cuuint32_t>(kPage), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    MapCacheEntry &e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.base = const_cast<void *>(base);
+    e.kind = kind;
+    e.rows = static_cast<uint64_t>(T);
+    e.slices = static_cast<uint64_t>(B);
+    e.map = *map;
+    return true;
+}
+
+// How a multi-token call is cut: warps per CTA, query-row blocks, key splits and tiles per
+// split. A function of the shape, T, the window or longest sequence and the SM count only
+// (never of the lengths), so the workspace can be sized ahead and the call captured.
+struct MultiPlan {
+    long long groups;  // (sequence, KV head, query-row block) triples, one counter each
+    int nw, rows, row_blocks, splits, chunk;
+    size_t counter_bytes, part_bytes;
+};
+
+MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_seq_len, int sms) {
+    MultiPlan m;
+    const int G = s.num_q_heads / s.num_kv_heads;
+    const long long TG = static_cast<long long>(T) * G;
+    m.nw = static_cast<int>(std::min<long long>(kMWarps, (TG + 15) / 16));
+    m.rows = 16 * m.nw;
+    m.row_blocks = static_cast<int>((TG + m.rows - 1) / m.rows);
+    const long long cached = ring ? (window + kPage - 1) / kPage : (max_seq_len + kPage - 1) / kPage;
+    const long long max_tiles = cached + (T + kPage - 1) / kPage + 1;
+    const long long groups = static_cast<long long>(s.batch) * s.num_kv_heads * m.row_blocks;
+    const long long target = 4LL * sms;  // two CTAs per SM, two waves
+    long long sp = std::max<long long>(1, (target + groups - 1) / std::max<long long>(1, groups));
+    sp = std::min(sp, max_tiles);
+    m.chunk = static_cast<int>((max_tiles + sp - 1) / sp);
+    m.splits = static_cast<int>((max_tiles + m.chunk - 1) / m.chunk);
+    // the counters sit in a fixed region: a later call with more groups must find zeros
+    // there, not the partials of an earlier call with fewer
+    m.groups = groups;
+    m.counter_bytes = static_cast<size_t>(kMMaxGroups) * sizeof(int);
+    m.part_bytes =
+        m.splits > 1 ? static_cast<size_t>(groups) * m.splits * m.rows * kMSlotFloats * sizeof(float) : 0;
+    return m;
+}
+
+int reserve_multi_locked(int dev, size_t bytes) {
+    DeviceState &d = g_dev[dev];
+    if (d.ws_multi_bytes >= bytes) return DA_OK;
+    if (d.ws_multi) {
+        cudaError_t e = cudaFree(d.ws_multi);
+        d.ws_multi = nullptr;
+        d.ws_multi_bytes = 0;
+        if (e != cudaSuccess) return set_cuda_error(e);
+    }
+    void *ptr = nullptr;
+    cudaError_t e = cudaMalloc(&ptr, bytes);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    e = cudaMemset(ptr, 0, bytes);
+    if (e != cudaSuccess) {
+        cudaFree(ptr);
+        return set_cuda_error(e);
+    }
+    d.ws_multi = ptr;
+    d.ws_multi_bytes = bytes;
+    return DA_OK;
+}
+
+int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+              const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens, const float *sinks,
+              int window, float scale, void *out, const da_shape &s, int T, int page_size, int max_pages,
+              int num_pages, int max_seq_len, void *stream_v) {
+    int rc = check_shape(s);
+    if (rc != DA_OK) return rc;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(out))
+        return DA_ERR_INVALID_ARG;
+    if (!(scale == scale) || T <= 0) return DA_ERR_INVALID_ARG;
+    if (T > kMMaxTokens) return DA_ERR_UNSUPPORTED;
+    if (ring) {
+        if (window < kPage) return window <= 0 ? DA_ERR_INVALID_ARG : DA_ERR_UNSUPPORTED;
+    } else {
+        if (!block_table || window < 0 || max_pages <= 0 || num_pages <= 0 || max_seq_len < 0)
+            return DA_ERR_INVALID_ARG;
+        if (page_size != kPage) return DA_ERR_UNSUPPORTED;
+        if (static_cast<long long>(max_pages) * kPage < max_seq_len) return DA_ERR_INVALID_ARG;
+        if (static_cast<long long>(num_pages) * s.num_kv_heads > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+    }
+    if (s.batch == 0) return DA_OK;
+    int dev;
+    rc = current_device(&dev);
+    if (rc != DA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const MultiPlan m = multi_plan(s, T, ring, window, max_seq_len, sm_count(dev));
+    if (static_cast<long long>(m.splits) * m.row_blocks > 0x7fffffffLL || m.groups > kMMaxGroups)
+        return DA_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const size_t need = m.counter_bytes + m.part_bytes;
+        if (g_dev[dev].ws_multi_bytes < need) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+            if (e != cudaSuccess) return set_cuda_error(e);
+            if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
+            rc = reserve_multi_locked(dev, need);
+            if (rc != DA_OK) return rc;
+        }
+    }
+    MultiParams prm;
+    prm.q = static_cast<const __nv_bfloat16 *>(q);
+    prm.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    prm.out = static_cast<__nv_bfloat16 *>(out);
+    prm.block_table = block_table;
+    prm.seq_lens = seq_lens;
+    prm.q_lens = q_lens;
+    prm.sinks = sinks;
+    prm.scale_log2 = scale * kLog2e;
+    prm.B = s.batch;
+    prm.Hq = s.num_q_heads;
+    prm.Hkv = s.num_kv_heads;
+    prm.G = s.num_q_heads / s.num_kv_heads;
+    prm.T = T;
+    prm.window = window;
+    prm.max_pages = ring ? 0 : max_pages;
+    prm.num_pages = ring ? 0 : num_pages;
+    prm.max_seq_len = ring ? 0 : max_seq_len;
+    prm.row_blocks = m.row_blocks;
+    prm.splits = m.splits;
+    prm.chunk = m.chunk;
+    prm.counters = static_cast<int *>(g_dev[dev].ws_multi);
+    prm.part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws_multi) + m.counter_bytes);
+
+    CUtensorMap mk, mv, nk, nv;
+    const uint64_t rows = ring ? static_cast<uint64_t>(window) : static_cast<uint64_t>(kPage);
+    const uint64_t slices = ring ? static_cast<uint64_t>(s.batch) * s.num_kv_heads
+                                 : static_cast<uint64_t>(num_pages) * s.num_kv_heads;
+    if (!make_kv_map(&mk, k_cache, rows, slices) || !make_kv_map(&mv, v_cache, rows, slices) ||
+        !make_new_map(&nk, k_new, s.num_kv_heads, T, s.batch) ||
+        !make_new_map(&nv, v_new, s.num_kv_heads, T, s.batch)) {
+        snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
+        return DA_ERR_CUDA;
+    }
+    auto kern = ring ? multi_attn_kernel<true> : multi_attn_kernel<false>;
+    if (!g_dev[dev].multi_attr_set[ring ? 1 : 0]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMSmem);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        g_dev[dev].multi_attr_set[ring ? 1 : 0] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(m.splits * m.row_blocks), static_cast<unsigned>(s.num_kv_heads),
+                       static_cast<unsigned>(s.batch));
+    cfg.blockDim = dim3(32 * m.nw);
+    cfg.dynamicSmemBytes = kMSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mk, mv, nk, nv, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e);
+    // the append, after every read of the cache (an ordinary launch: it waits for the kernel)
+    kv_append_multi_kernel<<<s.batch, 256, 0, stream>>>(
+        prm.k_new, prm.v_new, static_cast<__nv_bfloat16 *>(k_cache), static_cast<__nv_bfloat16 *>(v_cache),
+        ring ? nullptr : block_table, seq_lens, q_lens, T, s.num_kv_heads, ring ? window : 0, prm.max_pages,
+        prm.num_pages, prm.max_seq_len);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? DA_OK : set_cuda_error(e);
+}
+
 // ------------------------------------------------------------------ allocation-free variant
 // Some callers cannot allocate device memory at the point where they run decode
 // attention: a runtime whose memory is handed out up front by its own pool, a plugin
@@ -1818,6 +2021,38 @@ int decode_attn_paged_noalloc(const void *q, const void *k_new, const void *v_ne
                               int num_pages, int max_seq_len, void *stream) {
     return run_paged_noalloc(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks, window, scale, out,
                              s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream);
+}
+
+int decode_attn_paged_multi(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                            const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                            const float *sinks, int window, float scale, void *out, da_shape s, int q_tokens,
+                            int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, void *stream) {
+    return run_multi(false, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks, window, scale,
+                     out, s, q_tokens, page_size, max_pages_per_seq, num_pages, max_seq_len, stream);
+}
+
+int decode_attn_ring_multi(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           const int32_t *seq_lens, const int32_t *q_lens, const float *sinks, int window,
+                           float scale, void *out, da_shape s, int q_tokens, void *stream) {
+    return run_multi(true, q, k_new, v_new, k_cache, v_cache, nullptr, seq_lens, q_lens, sinks, window, scale, out,
+                     s, q_tokens, kPage, 0, 0, 0, stream);
+}
+
+size_t decode_attn_multi_workspace_bytes(da_shape s, int q_tokens, int ring_window, int max_seq_len) {
+    if (check_shape(s) != DA_OK || q_tokens <= 0 || q_tokens > kMMaxTokens || max_seq_len < 0 || ring_window < 0)
+        return 0;
+    int dev;
+    if (current_device(&dev) != DA_OK) return 0;
+    const MultiPlan m = multi_plan(s, q_tokens, ring_window > 0, ring_window, max_seq_len, sm_count(dev));
+    return m.counter_bytes + m.part_bytes;
+}
+
+int decode_attn_multi_reserve(size_t bytes) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc != DA_OK) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return reserve_multi_locked(dev, bytes);
 }
 
 size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len) {

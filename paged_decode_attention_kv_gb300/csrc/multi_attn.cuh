@@ -1,0 +1,484 @@
+// Several query tokens per sequence in one call: speculative verification (the draft
+// tokens and the bonus token checked in one step) and chunked prefill appending a run of
+// tokens into pages (the teaching repo's chapters "Speculative Decoding" and "Chunked
+// Prefill", table "The files" on the page "Run it locally", name both; the plain causal
+// reading is used).
+//
+//   n = q_lens[b] (T when q_lens is null) new tokens at positions base = L - n .. L - 1,
+//   L = seq_lens[b]. Query row (t, h), t < n, at position p = base + t attends the
+//   positions lo .. p (causal), lo = max(0, p - W + 1) under a window W, else 0.
+//   Positions >= base are the new tokens, read from k_new / v_new [B][T][Hkv][64]; the
+//   rest come from the cache, which holds the history before the step. Rows t >= n and
+//   inactive slots are zero. The new tokens are appended by a second kernel after the
+//   attention: in a W-cell ring the early query tokens still read the cells that the later
+//   new tokens overwrite.
+//
+// Included into decode_attn.cu (inside its anonymous namespace): one translation unit,
+// sharing the PTX helpers, the status word and the online-softmax state.
+//
+// Work split: one CTA per (sequence b, KV head g, block of 16 * warps query rows, key
+// split). Query rows of (b, g) are ordered (t, head): row r = t * G + (h - g * G). Each warp
+// owns 16 rows (two 8-row n-tiles of the same mma.sync shapes as the decode kernel). The
+// CTA streams the key tiles of its split through one TMA pipeline that every warp reads:
+// cached tiles first (pages, or 16-cell groups of the ring), then tiles of 16 new tokens
+// copied straight out of k_new / v_new by a 4-D tensor map. Splits of the same rows leave
+// fp32 partials; the CTA that takes the last ticket combines them with the sink.
+
+constexpr int kMWarps = 4;                        // query-row warps per CTA at most
+constexpr int kMStages = 8;                       // K/V tile pairs in flight per CTA
+constexpr int kMStageBytes = 2 * kTileBytes;      // K tile, then V tile
+constexpr int kMSmem = 1024 + kMStages * kMStageBytes + 2 * kMStages * 8;
+constexpr int kMSlotFloats = 4 + kD;              // per query row: m, l (log2 units), 2 pad, acc[64]
+constexpr int kMAccOff = 4;                       // acc starts 16-byte aligned
+constexpr int kMMaxTokens = 4096;                 // query tokens per sequence per call
+constexpr int kMMaxGroups = 1 << 18;              // (b, g, row block) counters: a fixed 1 MiB
+
+struct MultiParams {
+    const __nv_bfloat16 *q, *k_new, *v_new;  // [B][T][Hq][64], [B][T][Hkv][64]
+    __nv_bfloat16 *out;                      // [B][T][Hq][64]
+    const int32_t *block_table, *seq_lens, *q_lens;
+    const float *sinks;
+    float scale_log2;
+    int B, Hq, Hkv, G, T, window, max_pages, num_pages, max_seq_len;
+    int row_blocks, splits, chunk;  // query-row blocks per (b, g); key splits; tiles per split
+    float *part;                    // [B * Hkv * row_blocks][splits][rows per CTA][kMSlotFloats]
+    int *counters;                  // [B * Hkv * row_blocks], zero at rest
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <bool RING>
+__global__ void __launch_bounds__(kMWarps * 32, 2)
+    multi_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                      const __grid_constant__ CUtensorMap tnk, const __grid_constant__ CUtensorMap tnv,
+                      const MultiParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t tiles_s = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kMStages * kMStageBytes);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kMStages);
+    __shared__ int s_ticket;
+    __shared__ int s_failed;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int nw = blockDim.x >> 5;
+    const int RB = nw * 16;  // query rows per CTA
+    const int split = blockIdx.x % p.splits, rb = blockIdx.x / p.splits;
+    const int g = blockIdx.y, b = blockIdx.z;
+
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tnk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tnv)) : "memory");
+        for (int s = 0; s < kMStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, nw);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_failed = 0;
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- this sequence's counts and the block's key tiles
+    int L = __ldg(p.seq_lens + b);
+    int n = p.q_lens != nullptr ? __ldg(p.q_lens + b) : p.T;
+    bool bad = L < 0 || n < 0 || n > p.T || (L > 0 && n > L);
+    if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
+    if (bad) {
+        if (tid == 0 && g == 0 && blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+        L = 0;
+    }
+    if (L == 0) n = 0;
+    const int base = L - n;
+    const int W = p.window;
+    const int TG = p.T * p.G;
+    const int r0 = rb * RB;
+    const int r_end = min(r0 + RB, TG);
+    const int t0 = r0 / p.G;                             // first query token of the block
+    const int t1 = min(n - 1, (r_end - 1) / p.G);         // last valid one (< t0: none)
+    int ncache = 0, pt_lo = 0, nvalid = 0, nt_base = 0, ntiles = 0;
+    if (t1 >= t0) {
+        const int lo_min = W > 0 ? max(0, base + t0 - W + 1) : 0;
+        if (base > lo_min) {  // cached keys
+            if (RING) {
+                nvalid = min(base, W);
+                ncache = (nvalid + kPage - 1) / kPage;
+            } else {
+                pt_lo = lo_min / kPage;
+                ncache = (base - 1) / kPage - pt_lo + 1;
+            }
+        }
+        nt_base = max(0, lo_min - base) / kPage;  // first tile of new tokens (16 per tile)
+        ntiles = ncache + t1 / kPage - nt_base + 1;
+    }
+    const int kb = split * p.chunk;
+    const int ke = min(kb + p.chunk, ntiles);
+    const int nsplit = (ntiles + p.chunk - 1) / p.chunk;
+    const size_t bg = static_cast<size_t>(b) * p.Hkv + g;
+    auto row_off = [&](int r) {  // element offset of query row r of (b, g) in q and out
+        const int t = r / p.G, hl = r - t * p.G;
+        return ((static_cast<size_t>(b) * p.T + t) * p.Hq + g * p.G + hl) * kD;
+    };
+    auto out_row = [&](int r) { return p.out + row_off(r); };
+    if (kb >= ke) {
+        if (ntiles == 0 && split == 0)  // no valid query row here: zeros
+            for (int i = tid; i < (r_end - r0) * (kD / 8); i += blockDim.x)
+                *reinterpret_cast<uint4 *>(out_row(r0 + i / (kD / 8)) + (i % (kD / 8)) * 8) = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const int cnt = ke - kb;
+
+    // ---- producer (thread 0): tile k into stage s
+    const uint64_t policy = evict_first_policy();
+    auto issue = [&](int k, int s) {
+        const uint32_t fb = full0 + 8 * s;
+        const uint32_t dk = tiles_s + s * kMStageBytes, dv = dk + kTileBytes;
+        mbar_expect_tx(fb, kMStageBytes);
+        if (k < ncache) {
+            if (RING) {
+                tma_load_3d(dk, &tmk, 0, k * kPage, static_cast<int>(bg), fb, policy);
+                tma_load_3d(dv, &tmv, 0, k * kPage, static_cast<int>(bg), fb, policy);
+            } else {
+                int page = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pt_lo + k);
+                if (page < 0 || page >= p.num_pages) {
+                    flag_status(DA_STATUS_BAD_PAGE);
+                    page = -1;  // out of the map: the copy reads zeros
+                }
+                tma_load_3d(dk, &tmk, 0, 0, page * p.Hkv + g, fb, policy);
+                tma_load_3d(dv, &tmv, 0, 0, page * p.Hkv + g, fb, policy);
+            }
+        } else {
+            const int tt = (nt_base + k - ncache) * kPage;  // first new token of the tile
+            tma_load_4d(dk, &tnk, 0, g, tt, b, fb, policy);
+            tma_load_4d(dv, &tnv, 0, g, tt, b, fb, policy);
+        }
+    };
+    int issued = 0;  // tiles issued so far (thread 0)
+    if (tid == 0) {
+        for (; issued < cnt && issued < kMStages; ++issued) issue(kb + issued, issued);
+    }
+
+    // ---- this lane's query rows: n-tile j, column c -> row r0 + 16 warp + 8 j + 2 (lane % 4) + c
+    int rp[2][2], rlo[2][2];  // position and window start of the row (invalid row: no key passes)
+    float sig[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int r = r0 + 16 * warp + 8 * j + 2 * (lane & 3) + c;
+            const int t = r / p.G;
+            const bool ok = r < r_end && t < n;
+            rp[j][c] = ok ? base + t : -1;
+            rlo[j][c] = ok && W > 0 ? max(0, base + t - W + 1) : 0;
+            const int h = g * p.G + (r - t * p.G);
+            sig[j][c] = ok && p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+        }
+    // query fragments (B operand): row r0 + 16 warp + 8 j + lane / 4, d = 16 ks + 2 (lane % 4) (+ 8)
+    uint32_t qf[2][4][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int r = r0 + 16 * warp + 8 * j + (lane >> 2);
+        const int t = r / p.G;
+        const bool ok = r < r_end && t < n;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) qf[j][ks][0] = qf[j][ks][1] = 0u;
+        if (ok) {
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(p.q + row_off(r));
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                qf[j][ks][0] = __ldg(row + ks * 8 + (lane & 3));
+                qf[j][ks][1] = __ldg(row + ks * 8 + 4 + (lane & 3));
+            }
+        }
+    }
+
+    // per-lane ldmatrix offsets inside a swizzled 16 x 128 B tile (as in the decode kernel)
+    const int lj = lane & 7, lmi = lane >> 3;
+    const uint32_t k_row = ((lj + ((lmi & 1) << 3)) * 128);
+    const int k_cb = lmi >> 1;
+    const uint32_t v_row = ((lj + ((lmi >> 1) << 3)) * 128);
+    const int v_cb = lmi & 1;
+
+    // position of key row kr of tile k, and whether it is a real key
+    auto key_at = [&](int k, int kr, int &j) -> bool {
+        if (k < ncache) {
+            if (RING) {
+                const int c = k * kPage + kr;
+                if (c >= nvalid) return false;
+                j = base - 1 - (base - 1 - c) % W;  // the newest cached position in cell c
+                return true;
+            }
+            j = (pt_lo + k) * kPage + kr;
+            return j < base;
+        }
+        const int tn = (nt_base + k - ncache) * kPage + kr;
+        j = base + tn;
+        return tn < n;
+    };
+
+    SegState<2> st;
+    state_reset(st);
+    bool failed = false;
+    int s = 0;
+    uint32_t ph = 0;
+    int i = 0;
+    for (; i < cnt; ++i) {
+        // producer: refill the stage of tile i - 1 (its readers are most likely done)
+        if (tid == 0 && i >= 1 && issued < cnt) {
+            const int sp = s == 0 ? kMStages - 1 : s - 1;
+            const uint32_t pp = s == 0 ? ph ^ 1u : ph;
+            if (!mbar_wait_bounded(empty0 + 8 * sp, pp)) {
+                failed = true;
+                break;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(kb + issued, sp);
+            ++issued;
+        }
+        if (!mbar_wait_bounded(full0 + 8 * s, ph)) {
+            failed = true;
+            break;
+        }
+        const int k = kb + i;
+        int jS[2];
+        bool okS[2];
+        okS[0] = key_at(k, lane >> 2, jS[0]);
+        okS[1] = key_at(k, (lane >> 2) + 8, jS[1]);
+        int jlast;
+        const bool full_tile = key_at(k, kPage - 1, jlast);  // keys only end at a tile's top
+
+        const uint32_t sK = tiles_s + s * kMStageBytes, sV = sK + kTileBytes;
+        uint32_t ka[4][4], va[4][4];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            ldsm_x4(sK + k_row + (((2 * ks + k_cb) ^ lj) << 4), ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3]);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+            ldsm_x4_t(sV + v_row + (((2 * mt + v_cb) ^ lj) << 4), va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+        if (!full_tile) {  // zero the V values of keys that do not exist (they may hold NaN)
+            int jj;
+            const int kv = 2 * (lane & 3);
+            const uint32_t vm0 = (key_at(k, kv, jj) ? 0x0000ffffu : 0u) | (key_at(k, kv + 1, jj) ? 0xffff0000u : 0u);
+            const uint32_t vm1 = (key_at(k, kv + 8, jj) ? 0x0000ffffu : 0u) | (key_at(k, kv + 9, jj) ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                va[mt][0] &= vm0;
+                va[mt][1] &= vm0;
+                va[mt][2] &= vm1;
+                va[mt][3] &= vm1;
+            }
+        }
+        uint32_t pb[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[j][0][0], qf[j][0][1]);
+            mma_bf16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[j][1][0], qf[j][1][1]);
+            mma_bf16(sc, ka[2][0], ka[2][1], ka[2][2], ka[2][3], qf[j][2][0], qf[j][2][1]);
+            mma_bf16(sd, ka[3][0], ka[3][1], ka[3][2], ka[3][3], qf[j][3][0], qf[j][3][1]);
+            // [key lane/4 | lane/4 + 8][row 2(lane%4) | + 1], causal and window masks per row
+            auto keep = [&](int kk, int c) { return okS[kk] && jS[kk] >= rlo[j][c] && jS[kk] <= rp[j][c]; };
+            const float s00 = keep(0, 0) ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
+            const float s01 = keep(0, 1) ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
+            const float s10 = keep(1, 0) ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
+            const float s11 = keep(1, 1) ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 8));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 8));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
+            const float mn0 = fmaxf(st.m[j][0], mx0), mn1 = fmaxf(st.m[j][1], mx1);
+            // a row with no key so far keeps m = -inf: subtract 0 instead (every term is 0)
+            const float mr0 = mn0 == -INFINITY ? 0.f : mn0, mr1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float a0 = fast_exp2(st.m[j][0] - mr0), a1 = fast_exp2(st.m[j][1] - mr1);
+            const float p00 = fast_exp2(s00 - mr0), p01 = fast_exp2(s01 - mr1);
+            const float p10 = fast_exp2(s10 - mr0), p11 = fast_exp2(s11 - mr1);
+            st.l[j][0] = st.l[j][0] * a0 + (p00 + p10);
+            st.l[j][1] = st.l[j][1] * a1 + (p01 + p11);
+            st.m[j][0] = mn0;
+            st.m[j][1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                st.acc[j][mt][0] *= a0;
+                st.acc[j][mt][1] *= a1;
+                st.acc[j][mt][2] *= a0;
+                st.acc[j][mt][3] *= a1;
+            }
+            pb[j][0] = movmatrix_t(pack_bf16(p00, p01));  // keys 2(lane%4), +1
+            pb[j][1] = movmatrix_t(pack_bf16(p10, p11));  // keys 2(lane%4) + 8, + 9
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                mma_bf16(st.acc[j][mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb[j][0], pb[j][1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (++s == kMStages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    if (failed) {
+        flag_status(DA_STATUS_TIMEOUT);
+        s_failed = 1;
+    }
+    __syncthreads();
+    if (tid == 0 && s_failed) {  // let the copies still in flight land before the CTA leaves
+        for (int j = i; j < issued; ++j) mbar_wait_bounded(full0 + 8 * (j % kMStages), (j / kMStages) & 1);
+    }
+    state_reduce_l(st);
+
+    // ---- finish: one split writes the rows, several leave partials for the last to combine
+    auto finish_row = [&](float m, float l, float sg, float &f) {  // f: factor on acc; false: zero row
+        const float M = fmaxf(m, sg);
+        if (M == -INFINITY) {
+            f = 0.f;
+            return;
+        }
+        const float den = l * exp2f(m - M) + (sg == -INFINITY ? 0.f : exp2f(sg - M));
+        f = den > 0.f ? exp2f(m - M) / den : 0.f;
+    };
+    if (nsplit == 1) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = r0 + 16 * warp + 8 * j + 2 * (lane & 3) + c;
+                if (r >= r_end) continue;
+                float f = 0.f;
+                if (rp[j][c] >= 0) finish_row(st.m[j][c], st.l[j][c], sig[j][c], f);
+                __nv_bfloat16 *o = out_row(r);
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    o[mt * 16 + (lane >> 2)] = __float2bfloat16_rn(st.acc[j][mt][c] * f);
+                    o[mt * 16 + (lane >> 2) + 8] = __float2bfloat16_rn(st.acc[j][mt][c + 2] * f);
+                }
+            }
+        return;
+    }
+    const size_t slot0 = ((bg * p.row_blocks + rb) * p.splits) * static_cast<size_t>(RB);
+    float *mine = p.part + (slot0 + static_cast<size_t>(split) * RB) * kMSlotFloats;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int rl = 16 * warp + 8 * j + 2 * (lane & 3) + c;
+            float *o = mine + static_cast<size_t>(rl) * kMSlotFloats;
+            if (lane < 4) {
+                o[0] = st.m[j][c];
+                o[1] = st.l[j][c];
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                o[kMAccOff + mt * 16 + (lane >> 2)] = st.acc[j][mt][c];
+                o[kMAccOff + mt * 16 + (lane >> 2) + 8] = st.acc[j][mt][c + 2];
+            }
+        }
+    __threadfence();
+    __syncthreads();
+    int *ctr = p.counters + bg * p.row_blocks + rb;
+    if (tid == 0) s_ticket = atomicAdd(ctr, 1);
+    __syncthreads();
+    if (s_ticket != nsplit - 1) return;
+    __threadfence();
+    // the last split: rows x 16 quarter-rows of 4 outputs
+    const float *all = p.part + slot0 * kMSlotFloats;
+    for (int idx = tid; idx < RB * (kD / 4); idx += blockDim.x) {
+        const int rl = idx / (kD / 4), d0 = (idx % (kD / 4)) * 4;
+        const int r = r0 + rl;
+        if (r >= r_end) continue;
+        const int t = r / p.G;
+        __nv_bfloat16 *o = out_row(r) + d0;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < n) {
+            const int h = g * p.G + (r - t * p.G);
+            const float sg = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+            float M = sg;
+            for (int sp = 0; sp < nsplit; ++sp)
+                M = fmaxf(M, __ldcg(all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats));
+            if (M != -INFINITY) {
+                float den = sg == -INFINITY ? 0.f : exp2f(sg - M);
+                for (int sp = 0; sp < nsplit; ++sp) {
+                    const float *src = all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats;
+                    const float m = __ldcg(src);
+                    if (m == -INFINITY) continue;
+                    const float w = exp2f(m - M);
+                    den += __ldcg(src + 1) * w;
+                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + kMAccOff + d0));
+                    acc4[0] += a.x * w;
+                    acc4[1] += a.y * w;
+                    acc4[2] += a.z * w;
+                    acc4[3] += a.w * w;
+                }
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc4[e] *= inv;
+            }
+        }
+        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc4[0], acc4[1]);
+        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc4[2], acc4[3]);
+        uint2 v;
+        v.x = *reinterpret_cast<const uint32_t *>(&lo2);
+        v.y = *reinterpret_cast<const uint32_t *>(&hi2);
+        *reinterpret_cast<uint2 *>(o) = v;
+    }
+    if (tid == 0) *ctr = 0;  // ready for the next call
+}
+
+// The append of a multi-token step: new token t < n of b goes to position L - n + t. In a
+// ring only the last W of them survive (one write per cell).
+__global__ void kv_append_multi_kernel(const __nv_bfloat16 *__restrict__ k_new,
+                                       const __nv_bfloat16 *__restrict__ v_new, __nv_bfloat16 *k_cache,
+                                       __nv_bfloat16 *v_cache, const int *__restrict__ block_table,
+                                       const int *__restrict__ seq_lens, const int *__restrict__ q_lens, int T,
+                                       int Hkv, int window, int max_pages, int num_pages, int max_seq_len) {
+    const int b = blockIdx.x;
+    const int L = __ldg(seq_lens + b);
+    const int n = q_lens != nullptr ? __ldg(q_lens + b) : T;
+    bool bad = L < 0 || n < 0 || n > T || (L > 0 && n > L);
+    if (block_table != nullptr) bad = bad || L > max_seq_len || L > max_pages * kPage;
+    if (bad) {
+        if (threadIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+        return;
+    }
+    if (L == 0 || n == 0) return;
+    const int base = L - n;
+    const int first = block_table == nullptr && n > window ? n - window : 0;  // ring: last W only
+    constexpr int kChunks = kD / 8;  // 16-byte pieces per row
+    for (int i = threadIdx.x; i < (n - first) * Hkv * kChunks; i += blockDim.x) {
+        const int t = first + i / (Hkv * kChunks);
+        const int g = (i / kChunks) % Hkv, c = i % kChunks;
+        const int pos = base + t;
+        size_t dst;
+        if (block_table != nullptr) {
+            const int page = __ldg(block_table + static_cast<size_t>(b) * max_pages + pos / kPage);
+            if (page < 0 || page >= num_pages) {
+                flag_status(DA_STATUS_BAD_PAGE);
+                continue;
+            }
+            dst = ((static_cast<size_t>(page) * Hkv + g) * kPage + pos % kPage) * kD + c * 8;
+        } else {
+            dst = ((static_cast<size_t>(b) * Hkv + g) * window + pos % window) * kD + c * 8;
+        }
+        const size_t src = ((static_cast<size_t>(b) * T + t) * Hkv + g) * kD + c * 8;
+        *reinterpret_cast<uint4 *>(k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+        *reinterpret_cast<uint4 *>(v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+    }
+}

@@ -87,6 +87,39 @@ def test_ring_argument_validation(lib):
     assert ring(lib, s=_shape(B=0)) == 0
 
 
+def multi(lib, ring_=False, **kw):
+    a = dict(q=P, k_new=P, v_new=P, kc=P, vc=P, bt=P, sl=P, ql=None, sinks=P, window=0,
+             scale=0.125, out=P, s=_shape(), T=4, page=16, maxp=16, npages=64, maxlen=200,
+             stream=None)
+    if ring_:
+        a["window"] = 128
+    a.update(kw)
+    if ring_:
+        return lib.decode_attn_ring_multi(a["q"], a["k_new"], a["v_new"], a["kc"], a["vc"], a["sl"],
+                                          a["ql"], a["sinks"], a["window"], a["scale"], a["out"],
+                                          a["s"], a["T"], a["stream"])
+    return lib.decode_attn_paged_multi(a["q"], a["k_new"], a["v_new"], a["kc"], a["vc"], a["bt"],
+                                       a["sl"], a["ql"], a["sinks"], a["window"], a["scale"], a["out"],
+                                       a["s"], a["T"], a["page"], a["maxp"], a["npages"], a["maxlen"],
+                                       a["stream"])
+
+
+def test_multi_argument_validation(lib):
+    assert multi(lib, k_new=None) == -1                # the new tokens are required
+    assert multi(lib, v_new=None) == -1
+    assert multi(lib, T=0) == -1
+    assert multi(lib, T=5000) == -2                    # beyond 4096 query tokens
+    assert multi(lib, q=BAD) == -1
+    assert multi(lib, bt=None) == -1
+    assert multi(lib, page=32) == -2
+    assert multi(lib, maxlen=16 * 16 + 1) == -1
+    assert multi(lib, s=_shape(Hq=24, Hkv=1)) == -2
+    assert multi(lib, s=_shape(B=0)) == 0
+    assert multi(lib, ring_=True, window=8) == -2
+    assert multi(lib, ring_=True, window=0) == -1
+    assert multi(lib, ring_=True, s=_shape(B=0)) == 0
+
+
 def test_append_argument_validation(lib):
     s = _shape()
     assert lib.kv_append(None, P, P, P, P, P, 0, s, 16, 16, 64, None) == -1

@@ -1,0 +1,191 @@
+"""GPU parity of the multi-token step (decode_attn_paged_multi / _ring_multi) against the
+fp64 oracle: every output row within 4e-3 + 1e-2 |oracle| (rows beyond q_lens and
+inactive slots exactly zero), and the caches after the call bit-exact against the
+oracle's append, whole pools compared. Dead cache cells and the padding rows of
+k_new / v_new hold NaN, so reading any of them shows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_decode_attention_kv_gb300 as da
+from paged_decode_attention_kv_gb300 import workloads as wl
+from test_gpu_decode import DEV, assert_close, dev, dev_bits
+from test_oracle_multi import Multi
+
+pytestmark = pytest.mark.gpu
+
+
+def run_paged(m, window, seed=1, q_lens=True, sinks=True):
+    kp, vp, bt = m.paged(seed)
+    kd, vd = dev_bits(kp), dev_bits(vp)
+    c = m.c
+    out = torch.full((c.B, m.T, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_paged_multi(dev_bits(m.q), dev_bits(m.k_new), dev_bits(m.v_new), kd, vd, dev(bt),
+                               dev(m.lens), dev(m.sinks) if sinks else None, window, c.scale, out,
+                               q_lens=dev(m.n) if q_lens else None)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_multi(m.q, m.k_new, m.v_new, kp, vp, m.lens, m.sinks if sinks else None,
+                              window, c.scale, block_table=bt, q_lens=m.n if q_lens else None)
+    assert_close(out.double().cpu().numpy(), ref, f"paged multi window={window}")
+    ek, ev = oracle.kv_append_multi(m.k_new, m.v_new, kp, vp, m.lens, block_table=bt,
+                                    q_lens=m.n if q_lens else None)
+    np.testing.assert_array_equal(wl.bits(kd), ek)
+    np.testing.assert_array_equal(wl.bits(vd), ev)
+
+
+def run_ring(m, W, q_lens=True):
+    kr, vr = m.ring(W)
+    kd, vd = dev_bits(kr), dev_bits(vr)
+    c = m.c
+    out = torch.full((c.B, m.T, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_ring_multi(dev_bits(m.q), dev_bits(m.k_new), dev_bits(m.v_new), kd, vd,
+                              dev(m.lens), dev(m.sinks), c.scale, out,
+                              q_lens=dev(m.n) if q_lens else None)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_multi(m.q, m.k_new, m.v_new, kr, vr, m.lens, m.sinks, W, c.scale,
+                              q_lens=m.n if q_lens else None)
+    assert_close(out.double().cpu().numpy(), ref, f"ring multi W={W}")
+    ek, ev = oracle.kv_append_multi(m.k_new, m.v_new, kr, vr, m.lens, window=W,
+                                    q_lens=m.n if q_lens else None)
+    np.testing.assert_array_equal(wl.bits(kd), ek)
+    np.testing.assert_array_equal(wl.bits(vd), ev)
+
+
+LENS = [1, 4, 15, 16, 17, 33, 100, 257, 0]
+
+
+def counts(T, lens, seed):
+    """Per-sequence new-token counts in [0, min(T, L)], with T itself and 1 present."""
+    rng = np.random.default_rng(seed)
+    n = [int(rng.integers(0, min(T, L) + 1)) if L > 0 else 0 for L in lens]
+    for i, L in enumerate(lens):
+        if L >= T:
+            n[i] = T
+            break
+    for i, L in enumerate(lens):
+        if L > 0 and n[i] == 0:
+            n[i] = 1
+            break
+    return n
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (8, 8), (16, 1), (32, 4)])
+@pytest.mark.parametrize("T", [2, 5, 16])
+@pytest.mark.parametrize("window", [0, 7, 100])
+def test_paged_multi_matches_oracle(Hq, Hkv, T, window):
+    n = counts(T, LENS, Hq + T + window)
+    m = Multi(800 + Hq + T + window, Hq, Hkv, LENS, n, T)
+    run_paged(m, window, seed=T + 1)
+
+
+@pytest.mark.parametrize("W", [16, 128])
+@pytest.mark.parametrize("T", [3, 16, 40])
+def test_ring_multi_matches_oracle(W, T):
+    lens = [1, 15, 16, 17, W - 1, W, W + 1, 3 * W + 5, 60, 0]
+    n = counts(T, lens, W + T)
+    m = Multi(850 + W + T, 64, 8, lens, n, T)
+    run_ring(m, W)
+
+
+def test_all_rows_new_without_q_lens_and_no_sinks():
+    m = Multi(870, 64, 8, [8, 40, 300], [8, 8, 8], 8)
+    run_paged(m, 0, q_lens=False)
+    run_paged(m, 0, sinks=False)
+    run_ring(m, 32, q_lens=False)
+
+
+def test_chunked_prefill_sized_step():
+    """A run of 200 tokens appended behind a 1000-token history, and a first chunk (no
+    history at all): many query-row blocks per KV head."""
+    m = Multi(871, 64, 8, [1200, 200], [200, 200], 200)
+    run_paged(m, 0)
+    run_paged(m, 128)
+    run_ring(m, 128)
+
+
+def test_long_history_uses_many_splits():
+    """One sequence of 20k tokens and 4 draft tokens: the keys are split over many CTAs
+    and the last one combines."""
+    m = Multi(872, 64, 8, [20000, 3000], [4, 3], 4)
+    run_paged(m, 0)
+    run_paged(m, 1000)
+
+
+def test_repeated_calls_are_identical_and_counters_return_to_zero():
+    m = Multi(873, 64, 8, [5000, 70], [4, 4], 4)
+    kp, vp, bt = m.paged(2)
+    outs = []
+    for _ in range(3):
+        kd, vd = dev_bits(kp), dev_bits(vp)
+        out = torch.empty((m.c.B, m.T, m.c.Hq, m.c.D), dtype=torch.bfloat16, device=DEV)
+        da.decode_attn_paged_multi(dev_bits(m.q), dev_bits(m.k_new), dev_bits(m.v_new), kd, vd,
+                                   dev(bt), dev(m.lens), dev(m.sinks), 0, m.c.scale, out,
+                                   q_lens=dev(m.n))
+        outs.append(out.cpu())
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))
+
+
+def test_bad_counts_are_reported_not_faulted():
+    m = Multi(874, 8, 8, [10, 20], [2, 2], 2)
+    kp, vp, bt = m.paged(1)
+    out = torch.empty((2, 2, 8, 64), dtype=torch.bfloat16, device=DEV)
+    bad_q = torch.tensor([3, 2], dtype=torch.int32, device=DEV)   # 3 > T
+    da.decode_attn_paged_multi(dev_bits(m.q), dev_bits(m.k_new), dev_bits(m.v_new), dev_bits(kp),
+                               dev_bits(vp), dev(bt), dev(m.lens), dev(m.sinks), 0, m.c.scale, out,
+                               q_lens=bad_q)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() & da.DA_STATUS_BAD_SEQ_LEN
+    assert torch.all(out[0].float() == 0)                          # treated as inactive
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_full_size_speculative_step(T):
+    """The batch-64 workload with T draft tokens per sequence (lengths from the benchmark
+    recipe, random pools): a sample of sequences against the oracle, the append
+    bit-exact over the whole pool."""
+    cfg = wl.config("b64")
+    lens = [L + T for L in wl.seq_lens("b64")]
+    B, Hq, Hkv, D, P = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["page_size"]
+    gen = wl.cpu_generator(cfg["seed"])
+    vgen = torch.Generator(device=DEV)
+    vgen.manual_seed(cfg["seed"])
+    npages = sum(-(-L // P) for L in lens) + 64
+    maxp = max(-(-L // P) for L in lens)
+    pool = wl.draw_paged_pool(npages, Hkv, P, D, lens, maxp, gen, device=DEV, value_gen=vgen)
+    q = wl.randn_bf16((B, T, Hq, D), gen)
+    kn = wl.randn_bf16((B, T, Hkv, D), gen)
+    vn = wl.randn_bf16((B, T, Hkv, D), gen)
+    sinks = torch.randn((Hq,), generator=gen, dtype=torch.float32)
+    sl = np.asarray(lens, np.int32)
+    k_pre, v_pre = wl.bits(pool.k_cache), wl.bits(pool.v_cache)
+    out = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_paged_multi(dev(q), dev(kn), dev(vn), pool.k_cache, pool.v_cache,
+                               pool.block_table, dev(sl), dev(sinks), 0, wl.SCALE, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    bt = pool.block_table.cpu().numpy()
+    pick = sorted({0, int(np.argmax(lens)), int(np.argmin(lens)), 17, 40})
+    ref = oracle.decode_multi(wl.bits(q)[pick], wl.bits(kn)[pick], wl.bits(vn)[pick], k_pre, v_pre,
+                              sl[pick], sinks.numpy(), 0, wl.SCALE, block_table=bt[pick])
+    assert_close(out.double().cpu().numpy()[pick], ref, f"b64 T={T}")
+    ek, ev = oracle.kv_append_multi(wl.bits(kn), wl.bits(vn), k_pre, v_pre, sl, block_table=bt)
+    assert np.array_equal(wl.bits(pool.k_cache), ek) and np.array_equal(wl.bits(pool.v_cache), ev)
+
+
+def test_workspace_reuse_across_shapes():
+    """A call with few (sequence, head, row-block) groups and many splits writes split
+    partials; a following call with more groups must still find its arrival counters at
+    zero (the counters live in a region of their own)."""
+    few = Multi(875, 64, 8, [9000, 4000], [4, 2], 4)        # 16 groups, many splits
+    run_paged(few, 0)
+    lens = [int(x) for x in np.random.default_rng(5).integers(600, 2000, size=48)]
+    many = Multi(876, 64, 8, lens, [4] * 48, 4)              # 384 groups, a few splits each
+    run_paged(many, 0)
+    run_paged(few, 0)
+    run_paged(many, 0)
