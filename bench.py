@@ -38,24 +38,28 @@ HBM_BUS_BITS = 8192  # 8 HBM3e stacks x 1024 bits
 
 
 # ---------------------------------------------------------------- bytes the method must move
-def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W, kv="bf16"):
-    """Per call: cached K+V of the attended tokens (except the new one), k_new/v_new read
-    and written, q read, out written, block-table entries read, seq_lens, sinks. A cached
-    token costs 2*2*D bytes per KV head in bf16, or 2*D codes + two fp32 scales in fp8."""
+def algorithmic_bytes(lens, kind, Hq, Hkv, D, P, W, kv="bf16", q_tokens=1):
+    """Per call: cached K+V of the attended positions (each read once per sequence and KV
+    head, however many query tokens see it), the n = q_tokens new tokens' k/v read and
+    written into the cache, q read and out written for the n rows, block-table entries
+    read, seq_lens, sinks. A cached token costs 2*2*D bytes per KV head in bf16, or 2*D
+    codes + two fp32 scales in fp8."""
     tok = 4 * D if kv == "bf16" else 2 * D + 8
     total = 0
     for L in lens:
         if L <= 0:
             continue
+        n = min(q_tokens, L)
+        base = L - n
         if kind == "paged_full":
-            n, tiles = L, math.ceil(L / P)
+            cached, tiles = base, math.ceil(L / P)
         elif kind == "paged_window":
-            lo = max(0, L - W)
-            n, tiles = L - lo, (L - 1) // P - lo // P + 1
-        else:  # ring
-            n, tiles = min(L, W), 0
-        total += (n - 1) * tok * Hkv + 2 * 2 * Hkv * D + tok * Hkv + 2 * Hq * D \
-            + 2 * Hq * D + 4 * tiles
+            lo = max(0, base - W + 1)
+            cached, tiles = base - lo, (L - 1) // P - lo // P + 1
+        else:  # ring: the union of the n windows reaches W - 1 positions behind the first
+            cached, tiles = min(base, W - 1), 0
+        total += cached * tok * Hkv + n * (2 * 2 * Hkv * D + tok * Hkv) + 2 * Hq * D * n \
+            + 2 * Hq * D * n + 4 * tiles
     return total + 4 * len(lens) + 4 * Hq
 
 
@@ -192,11 +196,13 @@ def cpu_cores():
 class StepInputs:
     """One independent copy of a step's inputs and caches on the device."""
 
-    def __init__(self, name, device, seed_offset=0, batch_limit=None, kv="bf16"):
+    def __init__(self, name, device, seed_offset=0, batch_limit=None, kv="bf16", q_tokens=1):
         import torch
         from paged_decode_attention_kv_gb300 import workloads as wl
         cfg = wl.config(name)
-        self.lens = wl.seq_lens(name)[:batch_limit]
+        # T new tokens per sequence behind the same cached history as the 1-token step
+        self.T = q_tokens
+        self.lens = [L + q_tokens - 1 if L > 0 else 0 for L in wl.seq_lens(name)[:batch_limit]]
         cfg["B"] = len(self.lens)
         self.cfg = cfg
         seed = cfg["seed"] + seed_offset
@@ -220,9 +226,13 @@ class StepInputs:
             self.pool = wl.draw_fp8_paged_pool(npages, Hkv, P, D, vgen, device=device)
             self.ring = wl.draw_fp8_ring_pool(B, Hkv, W, D, vgen, device=device)
         d = lambda t: t.to(device).contiguous()
+        if q_tokens > 1:  # [B, T, heads, D] rows instead
+            self.inp.q = wl.randn_bf16((B, q_tokens, Hq, D), gen)
+            self.inp.k_new = wl.randn_bf16((B, q_tokens, Hkv, D), gen)
+            self.inp.v_new = wl.randn_bf16((B, q_tokens, Hkv, D), gen)
         self.q, self.k_new, self.v_new = d(self.inp.q), d(self.inp.k_new), d(self.inp.v_new)
         self.seq_lens, self.sinks = d(self.inp.seq_lens), d(self.inp.sinks)
-        self.out_full = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.out_full = torch.empty(tuple(self.q.shape), dtype=torch.bfloat16, device=device)
         self.out_ring = torch.empty_like(self.out_full)
         cs, sn = wl.rope_tables(max(self.lens) + 1, D)
         self.rope_cos = torch.from_numpy(cs).to(device)
@@ -245,7 +255,10 @@ def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=
     bt = s.block_table if bt is None else bt
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
-    if s.kv == "fp8":
+    if s.T > 1:
+        da.decode_attn_paged_multi(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks, 0,
+                                   s.inp.scale, s.out_full)
+    elif s.kv == "fp8":
         da.decode_attn_paged_fp8(q, k_new, v_new, s.pool, bt, sl, sinks, 0, s.inp.scale, s.out_full)
     elif rope:
         da.decode_attn_paged_rope(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks,
@@ -262,7 +275,10 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
     v_new = s.v_new if v_new is None else v_new
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
-    if s.kv == "fp8":
+    if s.T > 1:
+        da.decode_attn_ring_multi(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
+                                  s.inp.scale, s.out_ring)
+    elif s.kv == "fp8":
         da.decode_attn_ring_fp8(q, k_new, v_new, s.ring, sl, sinks, s.inp.scale, s.out_ring)
     elif rope:
         da.decode_attn_ring_rope(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
@@ -272,12 +288,12 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
                             s.inp.scale, s.out_ring)
 
 
-def step_bytes(name, lens, kv="bf16"):
+def step_bytes(name, lens, kv="bf16", q_tokens=1):
     from paged_decode_attention_kv_gb300 import workloads as wl
     c = wl.config(name)
     args = (c["Hq"], c["Hkv"], c["D"], c["page_size"], c["window"])
-    return (algorithmic_bytes(lens, "paged_full", *args, kv=kv),
-            algorithmic_bytes(lens, "ring", *args, kv=kv))
+    return (algorithmic_bytes(lens, "paged_full", *args, kv=kv, q_tokens=q_tokens),
+            algorithmic_bytes(lens, "ring", *args, kv=kv, q_tokens=q_tokens))
 
 
 # ---------------------------------------------------------------- the CPU oracle on a sample
@@ -306,7 +322,13 @@ def oracle_sample(name, s: "StepInputs", budget_s):
         for b in order:
             items = [(b, h) for h in range(Hq)]
             t0 = time.perf_counter()
-            if s.kv == "fp8":
+            if s.T > 1:
+                one = slice(b, b + 1)
+                oracle.decode_multi(q[one], kn[one], vn[one], kp, vp, lens[one], sinks, 0,
+                                    s.inp.scale, block_table=bt[one], nthreads=cores)
+                oracle.decode_multi(q[one], kn[one], vn[one], rk[one], rv[one], lens[one], sinks,
+                                    W, s.inp.scale, nthreads=cores)
+            elif s.kv == "fp8":
                 oracle.decode_paged_fp8(q, kn, vn, pool8, bt, lens, sinks, 0, s.inp.scale,
                                         items=items, nthreads=cores)
                 oracle.decode_ring_fp8(q, kn, vn, ring8, lens, sinks, W, s.inp.scale,
@@ -323,14 +345,15 @@ def oracle_sample(name, s: "StepInputs", budget_s):
                 oracle.decode_ring(q, kn, vn, rk, rv, lens, sinks, W, s.inp.scale, items=items,
                                    nthreads=cores)
             elapsed += time.perf_counter() - t0
-            pb, rb = step_bytes(name, [int(lens[b])], s.kv)
+            pb, rb = step_bytes(name, [int(lens[b])], s.kv, s.T)
             done_bytes += pb + rb
             seqs += 1
             if elapsed >= budget_s:
                 break
         passes += 1
     desc = (f"{seqs} sequence-steps ({passes} pass(es) over the {len(order)} active sequences), "
-            f"all {Hq} heads, full + ring layer; {elapsed:.1f} s on {cores} threads")
+            f"all {Hq} heads" + (f" x {s.T} query tokens" if s.T > 1 else "") +
+            f", full + ring layer; {elapsed:.1f} s on {cores} threads")
     return done_bytes / elapsed / 1e9, cores, desc
 
 
@@ -341,7 +364,8 @@ def run_reference(args, rank, world):
         return None
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    s = StepInputs(args.workload, device, batch_limit=args.batch_limit, kv=args.kv)
+    s = StepInputs(args.workload, device, batch_limit=args.batch_limit, kv=args.kv,
+                   q_tokens=args.q_tokens)
     s.rope = args.rope
     # each step is a bounded sample: calibrate so that warmup+steps fit ~90 s
     per_step = max(0.02, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
@@ -353,7 +377,7 @@ def run_reference(args, rank, world):
         vals.append(v)
         descs.append(desc)
     value = statistics.median(vals)
-    pbytes, rbytes = step_bytes(args.workload, s.lens, args.kv)
+    pbytes, rbytes = step_bytes(args.workload, s.lens, args.kv, args.q_tokens)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -377,6 +401,7 @@ def workload_config(name, s):
             "layers_per_step": ["paged full attention", f"ring window {c['window']}"],
             "rope": bool(getattr(s, "rope", False)),
             "kv_cache": "bf16" if s.kv == "bf16" else "fp8 e4m3 codes + per-token fp32 scales",
+            "q_tokens": s.T,
             "parallelism": "replicas", **({"note": c["workload_note"]} if "workload_note" in c else {})}
 
 
@@ -391,7 +416,8 @@ def run_ours(args, rank, world, local_rank):
     # their own caches); more sets rotate when one step's inputs would fit in L2
     def make_set(k):
         return [StepInputs(args.workload, dev, seed_offset=k * 10007 + 101 * li,
-                           batch_limit=args.batch_limit, kv=args.kv) for li in range(args.layers)]
+                           batch_limit=args.batch_limit, kv=args.kv, q_tokens=args.q_tokens)
+                for li in range(args.layers)]
     sets = [make_set(0)]
     first = sets[0][0]
     first.rope = args.rope
@@ -401,7 +427,7 @@ def run_ours(args, rank, world, local_rank):
     cfg = first.cfg
     B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
     da.decode_attn_reserve(da.decode_attn_workspace_bytes(B, Hq, Hkv, D))
-    pbytes, rbytes = step_bytes(args.workload, first.lens, args.kv)
+    pbytes, rbytes = step_bytes(args.workload, first.lens, args.kv, args.q_tokens)
     pbytes_call, rbytes_call = pbytes, rbytes
     pbytes, rbytes = pbytes * args.layers, rbytes * args.layers
     if args.batch_limit is not None:
@@ -477,7 +503,8 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_hbm_peak()
     nominal = nominal_hbm_peak()
     achieved = pbytes_call / (paged_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload, "paged" if args.kv == "bf16" else "paged_fp8")
+    traffic = recorded_traffic(args.workload, ("paged" if args.kv == "bf16" else "paged_fp8")
+                               if args.q_tokens == 1 else f"paged_multi{args.q_tokens}")
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -496,12 +523,14 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "traffic": traffic,
-                     "kernel": "decode_attn_kernel (paged, full attention%s)" % (
-                         "" if args.kv == "bf16" else ", fp8 cache"),
+                     "kernel": ("decode_attn_kernel (paged, full attention%s)" % (
+                         "" if args.kv == "bf16" else ", fp8 cache")) if args.q_tokens == 1 else
+                     ("multi_attn_kernel + kv_append_multi_kernel (paged, full attention, "
+                      "%d query tokens; one bracket around both)" % args.q_tokens),
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
-        "gpu_launches": 2 * args.layers * args.steps,
+        "gpu_launches": (2 if args.q_tokens == 1 else 4) * args.layers * args.steps,
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
                    "events around every launch in a second pass (includes the launch gap)"),
         "clocks": clocks,
@@ -562,6 +591,9 @@ def main():
                     help="fuse the rotary embedding of position L-1 (q and the new key) into both calls")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="cache storage: bf16, or e4m3 codes with per-token scales (quantised on append)")
+    ap.add_argument("--q-tokens", type=int, default=1,
+                    help="new tokens per sequence per step (speculative verification / chunked "
+                         "prefill): > 1 runs the multi-token calls")
     ap.add_argument("--batch-limit", type=int, default=None,
                     help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()
@@ -569,6 +601,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.kv == "fp8" and args.rope:
         ap.error("--rope is not available with --kv fp8")
+    if args.q_tokens > 1 and (args.rope or args.kv == "fp8" or args.graph):
+        ap.error("--q-tokens > 1 runs the bf16 multi-token calls without --rope, --kv fp8, --graph")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -80,6 +80,9 @@ __host__ __device__ constexpr int stages_for() {
 #ifndef DA_PAR_ISSUE_BF16
 #define DA_PAR_ISSUE_BF16 0
 #endif
+#ifndef DA_MULTI_CTAS_PER_SM  // multi-token calls: key splits aim at this many CTAs per SM
+#define DA_MULTI_CTAS_PER_SM 4
+#endif
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
 #endif
@@ -1688,14 +1691,15 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     MultiPlan m;
     const int G = s.num_q_heads / s.num_kv_heads;
     const long long TG = static_cast<long long>(T) * G;
-    m.nw = static_cast<int>(std::min<long long>(kMWarps, (TG + 15) / 16));
-    m.rows = 16 * m.nw;
+    m.nw = static_cast<int>(std::min<long long>(kMWarps, (TG + kMRowsPerWarp - 1) / kMRowsPerWarp));
+    m.rows = kMRowsPerWarp * m.nw;
     m.row_blocks = static_cast<int>((TG + m.rows - 1) / m.rows);
     const long long cached = ring ? (window + kPage - 1) / kPage : (max_seq_len + kPage - 1) / kPage;
     const long long max_tiles = cached + (T + kPage - 1) / kPage + 1;
     const long long groups = static_cast<long long>(s.batch) * s.num_kv_heads * m.row_blocks;
-    const long long target = 4LL * sms;  // two CTAs per SM, two waves
+    const long long target = static_cast<long long>(DA_MULTI_CTAS_PER_SM) * sms;
     long long sp = std::max<long long>(1, (target + groups - 1) / std::max<long long>(1, groups));
+    sp = std::max(sp, (max_tiles + kMMaxChunk - 1) / kMMaxChunk);  // a CTA's pages fit its smem
     sp = std::min(sp, max_tiles);
     m.chunk = static_cast<int>((max_tiles + sp - 1) / sp);
     m.splits = static_cast<int>((max_tiles + m.chunk - 1) / m.chunk);
@@ -1809,6 +1813,9 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     auto kern = ring ? multi_attn_kernel<true> : multi_attn_kernel<false>;
     if (!g_dev[dev].multi_attr_set[ring ? 1 : 0]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMSmem);
+        if (e == cudaSuccess)  // room for as many resident CTAs as the registers allow
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return set_cuda_error(e);
         g_dev[dev].multi_attr_set[ring ? 1 : 0] = true;
     }

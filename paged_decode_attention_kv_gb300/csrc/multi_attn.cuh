@@ -16,15 +16,26 @@
 // Included into decode_attn.cu (inside its anonymous namespace): one translation unit,
 // sharing the PTX helpers, the status word and the online-softmax state.
 //
-// Work split: one CTA per (sequence b, KV head g, block of 16 * warps query rows, key
+// Work split: one CTA per (sequence b, KV head g, block of 8 * warps query rows, key
 // split). Query rows of (b, g) are ordered (t, head): row r = t * G + (h - g * G). Each warp
-// owns 16 rows (two 8-row n-tiles of the same mma.sync shapes as the decode kernel). The
+// owns 8 rows (one 8-row n-tile of the same mma.sync shapes as the decode kernel). The
 // CTA streams the key tiles of its split through one TMA pipeline that every warp reads:
 // cached tiles first (pages, or 16-cell groups of the ring), then tiles of 16 new tokens
 // copied straight out of k_new / v_new by a 4-D tensor map. Splits of the same rows leave
 // fp32 partials; the CTA that takes the last ticket combines them with the sink.
 
-constexpr int kMWarps = 4;                        // query-row warps per CTA at most
+#ifndef DA_MULTI_NT
+#define DA_MULTI_NT 1
+#endif
+#ifndef DA_MULTI_WARPS
+#define DA_MULTI_WARPS 4
+#endif
+#ifndef DA_MULTI_MIN_BLOCKS  // resident CTAs per SM the register budget is cut for
+#define DA_MULTI_MIN_BLOCKS 4
+#endif
+constexpr int kMNT = DA_MULTI_NT;                 // 8-row n-tiles per warp (8 query rows each)
+constexpr int kMRowsPerWarp = 8 * kMNT;
+constexpr int kMWarps = DA_MULTI_WARPS;           // query-row warps per CTA at most
 constexpr int kMStages = 8;                       // K/V tile pairs in flight per CTA
 constexpr int kMStageBytes = 2 * kTileBytes;      // K tile, then V tile
 constexpr int kMSmem = 1024 + kMStages * kMStageBytes + 2 * kMStages * 8;
@@ -32,6 +43,7 @@ constexpr int kMSlotFloats = 4 + kD;              // per query row: m, l (log2 u
 constexpr int kMAccOff = 4;                       // acc starts 16-byte aligned
 constexpr int kMMaxTokens = 4096;                 // query tokens per sequence per call
 constexpr int kMMaxGroups = 1 << 18;              // (b, g, row block) counters: a fixed 1 MiB
+constexpr int kMMaxChunk = 1024;                  // key tiles per CTA at most (page indices in smem)
 
 struct MultiParams {
     const __nv_bfloat16 *q, *k_new, *v_new;  // [B][T][Hq][64], [B][T][Hkv][64]
@@ -59,7 +71,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 template <bool RING>
-__global__ void __launch_bounds__(kMWarps * 32, 2)
+__global__ void __launch_bounds__(kMWarps * 32, DA_MULTI_MIN_BLOCKS)
     multi_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ CUtensorMap tnk, const __grid_constant__ CUtensorMap tnv,
                       const MultiParams p) {
@@ -71,10 +83,11 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kMStages);
     __shared__ int s_ticket;
     __shared__ int s_failed;
+    __shared__ int s_page[kMMaxChunk];  // this CTA's page indices (paged cache), -1 = bad
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int nw = blockDim.x >> 5;
-    const int RB = nw * 16;  // query rows per CTA
+    const int RB = nw * kMRowsPerWarp;  // query rows per CTA
     const int split = blockIdx.x % p.splits, rb = blockIdx.x / p.splits;
     const int g = blockIdx.y, b = blockIdx.z;
 
@@ -111,12 +124,14 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
     const int t0 = r0 / p.G;                             // first query token of the block
     const int t1 = min(n - 1, (r_end - 1) / p.G);         // last valid one (< t0: none)
     int ncache = 0, pt_lo = 0, nvalid = 0, nt_base = 0, ntiles = 0;
+    int ring_off = 0;  // ring: position of cell c = c + ring_off, less W past the newest cell
     if (t1 >= t0) {
         const int lo_min = W > 0 ? max(0, base + t0 - W + 1) : 0;
         if (base > lo_min) {  // cached keys
             if (RING) {
                 nvalid = min(base, W);
                 ncache = (nvalid + kPage - 1) / kPage;
+                ring_off = base - 1 - (base - 1) % W;
             } else {
                 pt_lo = lo_min / kPage;
                 ncache = (base - 1) / kPage - pt_lo + 1;
@@ -141,6 +156,17 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
         return;
     }
     const int cnt = ke - kb;
+    if (!RING) {  // the pages of the CTA's cached tiles, read once
+        for (int i2 = tid; i2 < cnt && kb + i2 < ncache; i2 += blockDim.x) {
+            int page = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pt_lo + kb + i2);
+            if (page < 0 || page >= p.num_pages) {
+                flag_status(DA_STATUS_BAD_PAGE);
+                page = -1;  // out of the map: the copy reads zeros
+            }
+            s_page[i2] = page;
+        }
+        __syncthreads();
+    }
 
     // ---- producer (thread 0): tile k into stage s
     const uint64_t policy = evict_first_policy();
@@ -153,11 +179,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
                 tma_load_3d(dk, &tmk, 0, k * kPage, static_cast<int>(bg), fb, policy);
                 tma_load_3d(dv, &tmv, 0, k * kPage, static_cast<int>(bg), fb, policy);
             } else {
-                int page = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pt_lo + k);
-                if (page < 0 || page >= p.num_pages) {
-                    flag_status(DA_STATUS_BAD_PAGE);
-                    page = -1;  // out of the map: the copy reads zeros
-                }
+                const int page = s_page[k - kb];
                 tma_load_3d(dk, &tmk, 0, 0, page * p.Hkv + g, fb, policy);
                 tma_load_3d(dv, &tmv, 0, 0, page * p.Hkv + g, fb, policy);
             }
@@ -172,14 +194,14 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
         for (; issued < cnt && issued < kMStages; ++issued) issue(kb + issued, issued);
     }
 
-    // ---- this lane's query rows: n-tile j, column c -> row r0 + 16 warp + 8 j + 2 (lane % 4) + c
-    int rp[2][2], rlo[2][2];  // position and window start of the row (invalid row: no key passes)
-    float sig[2][2];
+    // ---- this lane's query rows: n-tile j, column c -> row r0 + RW warp + 8 j + 2 (lane % 4) + c
+    int rp[kMNT][2], rlo[kMNT][2];  // position and window start of the row (invalid: no key passes)
+    float sig[kMNT][2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < kMNT; ++j)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int r = r0 + 16 * warp + 8 * j + 2 * (lane & 3) + c;
+            const int r = r0 + kMRowsPerWarp * warp + 8 * j + 2 * (lane & 3) + c;
             const int t = r / p.G;
             const bool ok = r < r_end && t < n;
             rp[j][c] = ok ? base + t : -1;
@@ -187,11 +209,11 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
             const int h = g * p.G + (r - t * p.G);
             sig[j][c] = ok && p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
         }
-    // query fragments (B operand): row r0 + 16 warp + 8 j + lane / 4, d = 16 ks + 2 (lane % 4) (+ 8)
-    uint32_t qf[2][4][2];
+    // query fragments (B operand): row r0 + RW warp + 8 j + lane / 4, d = 16 ks + 2 (lane % 4) (+ 8)
+    uint32_t qf[kMNT][4][2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int r = r0 + 16 * warp + 8 * j + (lane >> 2);
+    for (int j = 0; j < kMNT; ++j) {
+        const int r = r0 + kMRowsPerWarp * warp + 8 * j + (lane >> 2);
         const int t = r / p.G;
         const bool ok = r < r_end && t < n;
 #pragma unroll
@@ -219,7 +241,8 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
             if (RING) {
                 const int c = k * kPage + kr;
                 if (c >= nvalid) return false;
-                j = base - 1 - (base - 1 - c) % W;  // the newest cached position in cell c
+                j = c + ring_off;  // the newest cached position in cell c
+                if (j >= base) j -= W;
                 return true;
             }
             j = (pt_lo + k) * kPage + kr;
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
         return tn < n;
     };
 
-    SegState<2> st;
+    SegState<kMNT> st;
     state_reset(st);
     bool failed = false;
     int s = 0;
@@ -282,9 +305,9 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
                 va[mt][3] &= vm1;
             }
         }
-        uint32_t pb[2][2];
+        uint32_t pb[kMNT][2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kMNT; ++j) {
             float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
             mma_bf16(sc, ka[0][0], ka[0][1], ka[0][2], ka[0][3], qf[j][0][0], qf[j][0][1]);
             mma_bf16(sd, ka[1][0], ka[1][1], ka[1][2], ka[1][3], qf[j][1][0], qf[j][1][1]);
@@ -326,7 +349,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < kMNT; ++j)
                 mma_bf16(st.acc[j][mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb[j][0], pb[j][1]);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -357,10 +380,10 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
     };
     if (nsplit == 1) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < kMNT; ++j)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const int r = r0 + 16 * warp + 8 * j + 2 * (lane & 3) + c;
+                const int r = r0 + kMRowsPerWarp * warp + 8 * j + 2 * (lane & 3) + c;
                 if (r >= r_end) continue;
                 float f = 0.f;
                 if (rp[j][c] >= 0) finish_row(st.m[j][c], st.l[j][c], sig[j][c], f);
@@ -376,10 +399,10 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
     const size_t slot0 = ((bg * p.row_blocks + rb) * p.splits) * static_cast<size_t>(RB);
     float *mine = p.part + (slot0 + static_cast<size_t>(split) * RB) * kMSlotFloats;
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < kMNT; ++j)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int rl = 16 * warp + 8 * j + 2 * (lane & 3) + c;
+            const int rl = kMRowsPerWarp * warp + 8 * j + 2 * (lane & 3) + c;
             float *o = mine + static_cast<size_t>(rl) * kMSlotFloats;
             if (lane < 4) {
                 o[0] = st.m[j][c];
@@ -398,47 +421,48 @@ __global__ void __launch_bounds__(kMWarps * 32, 2)
     __syncthreads();
     if (s_ticket != nsplit - 1) return;
     __threadfence();
-    // the last split: rows x 16 quarter-rows of 4 outputs
+    // the last split: one warp per query row, lanes striding over the splits for the
+    // maximum and the denominator, and holding two of the 64 outputs each
     const float *all = p.part + slot0 * kMSlotFloats;
-    for (int idx = tid; idx < RB * (kD / 4); idx += blockDim.x) {
-        const int rl = idx / (kD / 4), d0 = (idx % (kD / 4)) * 4;
+    for (int rl = warp; rl < RB; rl += nw) {
         const int r = r0 + rl;
-        if (r >= r_end) continue;
+        if (r >= r_end) break;
         const int t = r / p.G;
-        __nv_bfloat16 *o = out_row(r) + d0;
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        float o0 = 0.f, o1 = 0.f;
         if (t < n) {
             const int h = g * p.G + (r - t * p.G);
             const float sg = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+            auto slot = [&](int sp) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
             float M = sg;
-            for (int sp = 0; sp < nsplit; ++sp)
-                M = fmaxf(M, __ldcg(all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats));
+            for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, __ldcg(slot(sp)));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
             if (M != -INFINITY) {
-                float den = sg == -INFINITY ? 0.f : exp2f(sg - M);
+                float den = 0.f;
+                for (int sp = lane; sp < nsplit; sp += 32) {
+                    const float m = __ldcg(slot(sp));
+                    if (m != -INFINITY) den += __ldcg(slot(sp) + 1) * exp2f(m - M);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+                if (sg != -INFINITY) den += exp2f(sg - M);
+#pragma unroll 4
                 for (int sp = 0; sp < nsplit; ++sp) {
-                    const float *src = all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats;
-                    const float m = __ldcg(src);
-                    if (m == -INFINITY) continue;
-                    const float w = exp2f(m - M);
-                    den += __ldcg(src + 1) * w;
-                    const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + kMAccOff + d0));
-                    acc4[0] += a.x * w;
-                    acc4[1] += a.y * w;
-                    acc4[2] += a.z * w;
-                    acc4[3] += a.w * w;
+                    const float m = __ldcg(slot(sp));
+                    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+                    const float2 a2 = __ldcg(reinterpret_cast<const float2 *>(slot(sp) + kMAccOff) + lane);
+                    o0 += a2.x * w;
+                    o1 += a2.y * w;
                 }
                 const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc4[e] *= inv;
+                o0 *= inv;
+                o1 *= inv;
             }
         }
-        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc4[0], acc4[1]);
-        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc4[2], acc4[3]);
-        uint2 v;
-        v.x = *reinterpret_cast<const uint32_t *>(&lo2);
-        v.y = *reinterpret_cast<const uint32_t *>(&hi2);
-        *reinterpret_cast<uint2 *>(o) = v;
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o0, o1);
+        *reinterpret_cast<__nv_bfloat162 *>(out_row(r) + 2 * lane) = v2;
     }
+    __syncthreads();
     if (tid == 0) *ctr = 0;  // ready for the next call
 }
 
