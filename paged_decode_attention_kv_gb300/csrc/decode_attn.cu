@@ -1348,6 +1348,7 @@ __global__ void kv_append_kernel(const __nv_bfloat16 *__restrict__ k_new,
 
 // ------------------------------------------------------------------ several query tokens
 #include "multi_attn.cuh"
+#include "multi_tc.cuh"
 
 // ------------------------------------------------------------------ host side
 thread_local char t_err[256];
@@ -1438,7 +1439,7 @@ struct DeviceState {
     size_t ws_multi_bytes = 0;
     int sm_count = 0;
     bool attr_set[16] = {};
-    bool multi_attr_set[2] = {};
+    bool multi_attr_set[4] = {};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -1682,24 +1683,49 @@ bool make_new_map(CUtensorMap *map, const void *base, int Hkv, int T, int B) {
 // split. A function of the shape, T, the window or longest sequence and the SM count only
 // (never of the lengths), so the workspace can be sized ahead and the call captured.
 struct MultiPlan {
+    bool tc;           // the tcgen05 kernel (128 query rows per CTA) or the mma.sync one
     long long groups;  // (sequence, KV head, query-row block) triples, one counter each
     int nw, rows, row_blocks, splits, chunk;
     size_t counter_bytes, part_bytes;
 };
 
+// Paged calls with at least this many query rows per (sequence, KV head) run on tcgen05
+// (measured: from 64 rows on it beats the mma.sync kernel; the ring's few keys per row block
+// do not fill its pipeline, so ring calls stay on mma.sync).
+#ifndef DA_MULTI_TC_MIN_ROWS
+#define DA_MULTI_TC_MIN_ROWS 64
+#endif
+#ifndef DA_MULTI_TC_CTAS_PER_SM  // tcgen05 calls: key splits aim at this many CTAs per SM
+#define DA_MULTI_TC_CTAS_PER_SM 2
+#endif
+// Key tiles per CTA of the mma.sync kernel at most: a long sequence is split however many
+// groups there are (the host knows only the longest possible length; CTAs past a shorter
+// sequence's end exit at once). Not for tcgen05 CTAs, whose set-up (TMEM, staged queries)
+// makes more, shorter CTAs slower (measured).
+#ifndef DA_MULTI_MAX_CHUNK
+#define DA_MULTI_MAX_CHUNK 128
+#endif
+
 MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_seq_len, int sms) {
     MultiPlan m;
     const int G = s.num_q_heads / s.num_kv_heads;
     const long long TG = static_cast<long long>(T) * G;
-    m.nw = static_cast<int>(std::min<long long>(kMWarps, (TG + kMRowsPerWarp - 1) / kMRowsPerWarp));
-    m.rows = kMRowsPerWarp * m.nw;
+    m.tc = !ring && TG >= DA_MULTI_TC_MIN_ROWS;
+    if (m.tc) {
+        m.nw = kTcWarps;
+        m.rows = kTcRows;
+    } else {
+        m.nw = static_cast<int>(std::min<long long>(kMWarps, (TG + kMRowsPerWarp - 1) / kMRowsPerWarp));
+        m.rows = kMRowsPerWarp * m.nw;
+    }
     m.row_blocks = static_cast<int>((TG + m.rows - 1) / m.rows);
     const long long cached = ring ? (window + kPage - 1) / kPage : (max_seq_len + kPage - 1) / kPage;
     const long long max_tiles = cached + (T + kPage - 1) / kPage + 1;
     const long long groups = static_cast<long long>(s.batch) * s.num_kv_heads * m.row_blocks;
-    const long long target = static_cast<long long>(DA_MULTI_CTAS_PER_SM) * sms;
+    const long long target = static_cast<long long>(m.tc ? DA_MULTI_TC_CTAS_PER_SM : DA_MULTI_CTAS_PER_SM) * sms;
     long long sp = std::max<long long>(1, (target + groups - 1) / std::max<long long>(1, groups));
     sp = std::max(sp, (max_tiles + kMMaxChunk - 1) / kMMaxChunk);  // a CTA's pages fit its smem
+    if (!m.tc) sp = std::max(sp, (max_tiles + DA_MULTI_MAX_CHUNK - 1) / DA_MULTI_MAX_CHUNK);
     sp = std::min(sp, max_tiles);
     m.chunk = static_cast<int>((max_tiles + sp - 1) / sp);
     m.splits = static_cast<int>((max_tiles + m.chunk - 1) / m.chunk);
@@ -1810,20 +1836,23 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
         return DA_ERR_CUDA;
     }
-    auto kern = ring ? multi_attn_kernel<true> : multi_attn_kernel<false>;
-    if (!g_dev[dev].multi_attr_set[ring ? 1 : 0]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMSmem);
+    auto kern = m.tc ? (ring ? multi_tc_kernel<true> : multi_tc_kernel<false>)
+                     : (ring ? multi_attn_kernel<true> : multi_attn_kernel<false>);
+    const int smem = m.tc ? kTcSmem : kMSmem;
+    const int aidx = (ring ? 1 : 0) + (m.tc ? 2 : 0);
+    if (!g_dev[dev].multi_attr_set[aidx]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)  // room for as many resident CTAs as the registers allow
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return set_cuda_error(e);
-        g_dev[dev].multi_attr_set[ring ? 1 : 0] = true;
+        g_dev[dev].multi_attr_set[aidx] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(m.splits * m.row_blocks), static_cast<unsigned>(s.num_kv_heads),
                        static_cast<unsigned>(s.batch));
     cfg.blockDim = dim3(32 * m.nw);
-    cfg.dynamicSmemBytes = kMSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

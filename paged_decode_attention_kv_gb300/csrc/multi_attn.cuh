@@ -70,6 +70,52 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// The last split of a row block folds every split's partial (m, l, acc per row) into the
+// output, with the sink: one warp per query row, lanes striding over the splits for the
+// maximum and the denominator and holding two of the 64 outputs each.
+__device__ __noinline__ void multi_combine_rows(const MultiParams &p, const float *all, int RB, int r0, int r_end,
+                                                int n, int b, int g, int nsplit, int warp, int nw, int lane) {
+    for (int rl = warp; rl < RB; rl += nw) {
+        const int r = r0 + rl;
+        if (r >= r_end) break;
+        const int t = r / p.G;
+        const int hl = r - t * p.G;
+        float o0 = 0.f, o1 = 0.f;
+        if (t < n) {
+            const int h = g * p.G + hl;
+            const float sg = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+            auto slot = [&](int sp) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
+            float M = sg;
+            for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, __ldcg(slot(sp)));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            if (M != -INFINITY) {
+                float den = 0.f;
+                for (int sp = lane; sp < nsplit; sp += 32) {
+                    const float m = __ldcg(slot(sp));
+                    if (m != -INFINITY) den += __ldcg(slot(sp) + 1) * exp2f(m - M);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+                if (sg != -INFINITY) den += exp2f(sg - M);
+#pragma unroll 8
+                for (int sp = 0; sp < nsplit; ++sp) {
+                    const float m = __ldcg(slot(sp));
+                    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+                    const float2 a2 = __ldcg(reinterpret_cast<const float2 *>(slot(sp) + kMAccOff) + lane);
+                    o0 += a2.x * w;
+                    o1 += a2.y * w;
+                }
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+                o0 *= inv;
+                o1 *= inv;
+            }
+        }
+        __nv_bfloat16 *o = p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + g * p.G + hl) * kD;
+        *reinterpret_cast<__nv_bfloat162 *>(o + 2 * lane) = __floats2bfloat162_rn(o0, o1);
+    }
+}
+
 template <bool RING>
 __global__ void __launch_bounds__(kMWarps * 32, DA_MULTI_MIN_BLOCKS)
     multi_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -421,47 +467,7 @@ __global__ void __launch_bounds__(kMWarps * 32, DA_MULTI_MIN_BLOCKS)
     __syncthreads();
     if (s_ticket != nsplit - 1) return;
     __threadfence();
-    // the last split: one warp per query row, lanes striding over the splits for the
-    // maximum and the denominator, and holding two of the 64 outputs each
-    const float *all = p.part + slot0 * kMSlotFloats;
-    for (int rl = warp; rl < RB; rl += nw) {
-        const int r = r0 + rl;
-        if (r >= r_end) break;
-        const int t = r / p.G;
-        float o0 = 0.f, o1 = 0.f;
-        if (t < n) {
-            const int h = g * p.G + (r - t * p.G);
-            const float sg = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
-            auto slot = [&](int sp) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
-            float M = sg;
-            for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, __ldcg(slot(sp)));
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            if (M != -INFINITY) {
-                float den = 0.f;
-                for (int sp = lane; sp < nsplit; sp += 32) {
-                    const float m = __ldcg(slot(sp));
-                    if (m != -INFINITY) den += __ldcg(slot(sp) + 1) * exp2f(m - M);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-                if (sg != -INFINITY) den += exp2f(sg - M);
-#pragma unroll 4
-                for (int sp = 0; sp < nsplit; ++sp) {
-                    const float m = __ldcg(slot(sp));
-                    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-                    const float2 a2 = __ldcg(reinterpret_cast<const float2 *>(slot(sp) + kMAccOff) + lane);
-                    o0 += a2.x * w;
-                    o1 += a2.y * w;
-                }
-                const float inv = den > 0.f ? 1.f / den : 0.f;
-                o0 *= inv;
-                o1 *= inv;
-            }
-        }
-        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o0, o1);
-        *reinterpret_cast<__nv_bfloat162 *>(out_row(r) + 2 * lane) = v2;
-    }
+    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, RB, r0, r_end, n, b, g, nsplit, warp, nw, lane);
     __syncthreads();
     if (tid == 0) *ctr = 0;  // ready for the next call
 }

@@ -189,3 +189,25 @@ def test_workspace_reuse_across_shapes():
     run_paged(many, 0)
     run_paged(few, 0)
     run_paged(many, 0)
+
+
+def ramp_keys(m, top):
+    """Scale key j of every sequence by 1 + (top - 1) j / Tmax (rounded to bf16): scores grow
+    along the sequence, so later key blocks raise the running maximum by many octaves."""
+    from cases import bf16_to_f64, f64_to_bf16_bits
+    hk = bf16_to_f64(m.c.hist_k)
+    Tmax = hk.shape[1]
+    hk = hk * (1.0 + (top - 1.0) * np.arange(Tmax) / Tmax)[None, :, None, None]
+    m.c.hist_k = f64_to_bf16_bits(hk)
+    for b in range(m.c.B):
+        for t in range(int(m.n[b])):
+            m.k_new[b, t] = m.c.hist_k[b, m.base[b] + t]
+
+
+@pytest.mark.parametrize("T", [4, 16])
+def test_growing_scores_force_rescales(T):
+    m = Multi(877, 64, 8, [900, 300, 2000], [T, T, T], T)
+    ramp_keys(m, 12.0)
+    run_paged(m, 0)
+    run_paged(m, 200)
+    run_ring(m, 128)
