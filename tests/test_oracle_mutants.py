@@ -1,7 +1,9 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check
 that at least one pin in test_oracle.py catches each of them. This is what
 makes the pins trustworthy: a dropped term, a wrong sign, a wrong index or a
-transposed operand anywhere in the oracle must fail something."""
+transposed operand anywhere in the oracle must fail something. Every planted
+mistake keeps its reads and writes inside the arrays (one that wrote outside
+would corrupt this process instead of failing a pin)."""
 import os
 import subprocess
 
@@ -61,12 +63,12 @@ MUTANTS = [
      "v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d * P + slot]);"),
     ("fp8_scales_swapped", "const double sk = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)slot);",
      "const double sk = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)(P + slot));"),
-    ("fp8_ring_block", "return ((long long)b * Hkv + g) * (W / P) + cell / P;",
-     "return ((long long)g * 64 + b) * (W / P) + cell / P;"),
+    ("fp8_ring_slot", "*slot = cell % P;\n    return ((long long)b * Hkv + g) * (W / P) + cell / P;",
+     "*slot = (cell + 1) % P;\n    return ((long long)b * Hkv + g) * (W / P) + cell / P;"),
     ("fp8_scale_rule", "amax / 448.0f", "amax / 447.0f"),
     ("multi_not_causal_self", "const int cnt = p - lo + 1;", "const int cnt = p - lo;"),
     ("multi_position_shift", "const int p = L - n + t;", "const int p = L - n + t - 1;"),
-    ("multi_new_token_index", "const int t = j - base;", "const int t = j - base + 1;"),
+    ("multi_new_token_index", "const int t = j - base;", "const int t = (j - base + 1) % pr->T;"),
     ("multi_window_one_long", "const int lo = (W > 0 && p - W + 1 > 0) ? p - W + 1 : 0;",
      "const int lo = (W > 0 && p - W > 0) ? p - W : 0;"),
     ("multi_q_lens_ignored", "static int q_count(const int32_t *q_lens, int T, int b) { return q_lens ? q_lens[b] : T; }",
