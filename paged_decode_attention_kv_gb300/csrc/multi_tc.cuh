@@ -363,39 +363,46 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 tmem_ld32(sc, raw[0]);
                 tmem_ld32(sc + 32, raw[1]);
                 tmem_wait_ld();
+                // raw dot products; a key this row must not see becomes -inf
                 float x[64];
-                float mb = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < kTcTilesPerBlock; ++u) {
-                    const int k = k0 + u;
-                    // keys of tile u this row sees: kr in [a, e)
-                    int a = 0, e = 0;
-                    if (k < ke) {
-                        if (!RING || k >= ncache) {
+                for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(raw[c >> 5][c & 31]);
+                // a block whose 64 keys are consecutive positions, all present and all inside
+                // the row's window [lor, pr] needs no per-key mask (most blocks of a long sequence)
+                int jf = 0, jl = 0;
+                const bool okf = key_at(k0, 0, jf);
+                const bool okl = k0 + kTcTilesPerBlock - 1 < ke && key_at(k0 + kTcTilesPerBlock - 1, kPage - 1, jl);
+                const bool interior = valid && okf && okl && jl - jf == kTcKeys - 1 && jf >= lor && jl <= pr;
+                if (!interior) {
+#pragma unroll
+                    for (int u = 0; u < kTcTilesPerBlock; ++u) {
+                        const int k = k0 + u;
+                        // keys of tile u this row sees: kr in [a, e)
+                        int a = 0, e = 0;
+                        if (k < ke && (!RING || k >= ncache)) {
                             int j0;
                             key_at(k, 0, j0);  // first position of the tile (consecutive positions)
-                            int cntk;          // keys that exist in the tile
-                            if (k < ncache) cntk = min(kPage, base - j0);
-                            else cntk = min(kPage, n - (j0 - base));
+                            const int cntk = k < ncache ? min(kPage, base - j0) : min(kPage, n - (j0 - base));
                             a = max(0, lor - j0);
                             e = min(cntk, pr - j0 + 1);
                         }
-                    }
 #pragma unroll
-                    for (int kr = 0; kr < kPage; ++kr) {
-                        const int c = u * kPage + kr;
-                        bool keep;
-                        if (RING && k < ncache && k < ke) {
-                            int jp;
-                            keep = key_at(k, kr, jp) && jp >= lor && jp <= pr;
-                        } else {
-                            keep = kr >= a && kr < e;
+                        for (int kr = 0; kr < kPage; ++kr) {
+                            bool keep;
+                            if (RING && k < ncache && k < ke) {
+                                int jp;
+                                keep = key_at(k, kr, jp) && jp >= lor && jp <= pr;
+                            } else {
+                                keep = kr >= a && kr < e;
+                            }
+                            if (!keep) x[u * kPage + kr] = -INFINITY;
                         }
-                        const float v = __uint_as_float(raw[c >> 5][c & 31]) * p.scale_log2;
-                        x[c] = keep ? v : -INFINITY;
-                        mb = fmaxf(mb, x[c]);
                     }
                 }
+                float mraw = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mraw = fmaxf(mraw, x[c]);
+                const float mb = mraw * p.scale_log2;  // the scale is positive
                 const bool need = valid && mb > m_ref + kTcRescale;
                 const float m_new = need ? mb : m_ref;
                 // PV_{j-1} is waited for at every block, so that the parity of o_done never
@@ -432,7 +439,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float p0 = fast_exp2(x[32 * h + 2 * c] - mr), p1 = fast_exp2(x[32 * h + 2 * c + 1] - mr);
+                        const float p0 = fast_exp2(fmaf(x[32 * h + 2 * c], p.scale_log2, -mr));
+                        const float p1 = fast_exp2(fmaf(x[32 * h + 2 * c + 1], p.scale_log2, -mr));
                         ls += p0 + p1;
                         hi[c] = pack_bf16(p0, p1);
                         const float2 r2 = unpack_bf16(hi[c]);
