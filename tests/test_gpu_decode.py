@@ -358,3 +358,15 @@ def test_cuda_graph_capture_and_replay_with_new_lengths():
     assert_close(np.stack([got[b, h] for b, h in items]), ref, "graph ring")
     for b in np.nonzero(new_lens == 0)[0][:4]:
         assert torch.all(out_p[b] == 0) and torch.all(out_r[b] == 0)
+
+
+def test_maximum_batch():
+    """1024 slots (the largest batch the library takes), a quarter of them inactive, the rest
+    short with a few long ones, 16 query heads over 2 KV heads: the device-side prefix over
+    every slot, thousands of segments, the append into every active slot."""
+    rng = np.random.default_rng(8)
+    lens = [0 if rng.random() < 0.25 else int(rng.integers(1, 48)) for _ in range(1024)]
+    lens[5], lens[700] = 600, 900
+    c = make_case(340, len(lens), 16, 2, 64, lens)
+    check_paged(c, 0, seed=4)
+    check_ring(c, 32)

@@ -131,3 +131,11 @@ def test_full_size_fp8(name):
     want = oracle.kv_append_fp8(wl.bits(inp.k_new), wl.bits(inp.v_new), before, sl,
                                 block_table=bt.numpy())
     assert_blocks_equal(from_dev(pool), want)
+
+
+def test_paged_fp8_maximum_batch():
+    rng = np.random.default_rng(9)
+    lens = [0 if rng.random() < 0.25 else int(rng.integers(1, 48)) for _ in range(1024)]
+    lens[3] = 700
+    c = make_case(743, len(lens), 16, 2, 64, lens)
+    check_paged_fp8(c, 0, seed=9)

@@ -211,3 +211,14 @@ def test_growing_scores_force_rescales(T):
     run_paged(m, 0)
     run_paged(m, 200)
     run_ring(m, 128)
+
+
+def test_multi_many_slots():
+    """256 slots, a quarter inactive, 8 query tokens each (counts from 0 to 8): the tcgen05
+    kernel on the paged layer, many groups and splits."""
+    rng = np.random.default_rng(10)
+    lens = [0 if rng.random() < 0.25 else int(rng.integers(8, 400)) for _ in range(256)]
+    n = [0 if L == 0 else int(rng.integers(0, 9)) for L in lens]
+    m = Multi(878, 64, 8, lens, n, 8)
+    run_paged(m, 0)
+    run_ring(m, 128)
