@@ -139,3 +139,55 @@ def test_paged_fp8_maximum_batch():
     lens[3] = 700
     c = make_case(743, len(lens), 16, 2, 64, lens)
     check_paged_fp8(c, 0, seed=9)
+
+
+def test_fp8_cuda_graph_capture_and_replay():
+    """The fp8 paged and ring calls captured once and replayed after lengths, block table
+    and inputs changed in place."""
+    lens = [30, 500, 17, 0, 260]
+    c = make_case(744, len(lens), 64, 8, 64, lens)
+    kp, vp, bt = paged_identity(c, pre(c))
+    kp, vp, bt = shuffle_pages(kp, vp, bt, 3, spare=4)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c),
+                               oracle.Fp8Cache.empty_paged(kp.shape[0], c.Hkv, 16, c.D), block_table=bt)
+    ring = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c), oracle.Fp8Cache.empty_ring(c.B, c.Hkv, 128, c.D),
+                              window=128)
+    kv, rv = to_dev(cache), to_dev(ring)
+    q, kn, vn, sl, sk, btd = dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), dev(c.lens), dev(c.sinks), dev(bt)
+    out_p = torch.empty((c.B, c.Hq, c.D), dtype=torch.bfloat16, device=DEV)
+    out_r = torch.empty_like(out_p)
+    da.decode_attn_reserve(da.decode_attn_workspace_bytes(c.B, c.Hq, c.Hkv, c.D))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture
+        da.decode_attn_paged_fp8(q, kn, vn, kv.clone(), btd, sl, sk, 0, c.scale, out_p)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            da.decode_attn_paged_fp8(q, kn, vn, kv, btd, sl, sk, 0, c.scale, out_p)
+            da.decode_attn_ring_fp8(q, kn, vn, rv, sl, sk, c.scale, out_r)
+    torch.cuda.synchronize()
+    lens2 = [31, 100, 0, 45, 261]
+    c2 = make_case(745, len(lens2), 64, 8, 64, lens2)
+    kp2, vp2, bt2 = paged_identity(c2, pre(c2))
+    kp2, vp2, bt2 = shuffle_pages(kp2, vp2, bt2, 3, spare=kp.shape[0] - kp2.shape[0])  # captured pool size
+    assert kp2.shape == kp.shape and bt2.shape[0] == bt.shape[0]
+    bt2 = np.pad(bt2, ((0, 0), (0, bt.shape[1] - bt2.shape[1])), constant_values=-1)
+    cache2 = oracle.scatter_fp8(c2.hist_k, c2.hist_v, pre(c2),
+                                oracle.Fp8Cache.empty_paged(kp.shape[0], c.Hkv, 16, c.D), block_table=bt2)
+    ring2 = oracle.scatter_fp8(c2.hist_k, c2.hist_v, pre(c2), oracle.Fp8Cache.empty_ring(c.B, c.Hkv, 128, c.D),
+                               window=128)
+    kv.copy_(to_dev(cache2)); rv.copy_(to_dev(ring2))
+    for dst, src in ((q, c2.q), (kn, c2.k_new), (vn, c2.v_new)):
+        dst.copy_(dev_bits(src))
+    sl.copy_(dev(c2.lens)); btd.copy_(dev(bt2)); sk.copy_(dev(c2.sinks))
+    g.replay()
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref_p = oracle.decode_paged_fp8(c2.q, c2.k_new, c2.v_new, cache2, bt2, c2.lens, c2.sinks, 0, c.scale)
+    ref_r = oracle.decode_ring_fp8(c2.q, c2.k_new, c2.v_new, ring2, c2.lens, c2.sinks, 128, c.scale)
+    assert_close(out_p.double().cpu().numpy(), ref_p, "graph fp8 paged")
+    assert_close(out_r.double().cpu().numpy(), ref_r, "graph fp8 ring")
+    assert_blocks_equal(from_dev(kv), oracle.kv_append_fp8(c2.k_new, c2.v_new, cache2, c2.lens, block_table=bt2))
+    assert_blocks_equal(from_dev(rv), oracle.kv_append_fp8(c2.k_new, c2.v_new, ring2, c2.lens, window=128))

@@ -222,3 +222,60 @@ def test_multi_many_slots():
     m = Multi(878, 64, 8, lens, n, 8)
     run_paged(m, 0)
     run_ring(m, 128)
+
+
+@pytest.mark.parametrize("T", [4, 16])
+def test_cuda_graph_capture_and_replay(T):
+    """A multi-token step captured once in a CUDA graph (workspace reserved ahead, nothing on
+    the host depends on lengths) and replayed after the lengths, the counts and the inputs
+    changed in place: both layers against the oracle, both appends bit-exact."""
+    lens = [300, 40, 1200, 0, 77, 900]
+    m = Multi(879, 64, 8, lens, [T, 1, T, 0, 3, T], T)
+    kp, vp, bt = m.paged(5)
+    kr, vr = m.ring(128)
+    kd, vd, krd, vrd = dev_bits(kp), dev_bits(vp), dev_bits(kr), dev_bits(vr)
+    q, kn, vn = dev_bits(m.q), dev_bits(m.k_new), dev_bits(m.v_new)
+    sl, ql, sk, btd = dev(m.lens), dev(m.n), dev(m.sinks), dev(bt)
+    B, Hq, D = m.c.B, m.c.Hq, m.c.D
+    out_p = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=DEV)
+    out_r = torch.empty_like(out_p)
+    need = max(da.decode_attn_multi_workspace_bytes(B, Hq, 8, T, 0, bt.shape[1] * 16),
+               da.decode_attn_multi_workspace_bytes(B, Hq, 8, T, 128, 0))
+    da.decode_attn_multi_reserve(need)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture (the caches are rewritten below)
+        da.decode_attn_paged_multi(q, kn, vn, kd, vd, btd, sl, sk, 0, m.c.scale, out_p, q_lens=ql)
+        da.decode_attn_ring_multi(q, kn, vn, krd, vrd, sl, sk, m.c.scale, out_r, q_lens=ql)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            da.decode_attn_paged_multi(q, kn, vn, kd, vd, btd, sl, sk, 0, m.c.scale, out_p, q_lens=ql)
+            da.decode_attn_ring_multi(q, kn, vn, krd, vrd, sl, sk, m.c.scale, out_r, q_lens=ql)
+    torch.cuda.synchronize()
+    # a new step in place: other lengths and counts, new queries and new tokens
+    m2 = Multi(880, 64, 8, [250, 45, 1100, 60, 0, 800], [T, 2, 1, T, 0, T], T)
+    kp2, vp2, bt2 = m2.paged(5, total_pages=kp.shape[0], table_width=bt.shape[1])  # the captured sizes
+    kr2, vr2 = m2.ring(128)
+    assert kp2.shape == kp.shape and bt2.shape == bt.shape
+    for dst, src in ((kd, kp2), (vd, vp2), (krd, kr2), (vrd, vr2), (q, m2.q), (kn, m2.k_new),
+                     (vn, m2.v_new)):
+        dst.copy_(dev_bits(src))
+    for dst, src in ((sl, m2.lens), (ql, m2.n), (btd, bt2), (sk, m2.sinks)):
+        dst.copy_(dev(src))
+    g.replay()
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref_p = oracle.decode_multi(m2.q, m2.k_new, m2.v_new, kp2, vp2, m2.lens, m2.sinks, 0, m2.c.scale,
+                                block_table=bt2, q_lens=m2.n)
+    ref_r = oracle.decode_multi(m2.q, m2.k_new, m2.v_new, kr2, vr2, m2.lens, m2.sinks, 128, m2.c.scale,
+                                q_lens=m2.n)
+    assert_close(out_p.double().cpu().numpy(), ref_p, "graph multi paged")
+    assert_close(out_r.double().cpu().numpy(), ref_r, "graph multi ring")
+    ek, ev = oracle.kv_append_multi(m2.k_new, m2.v_new, kp2, vp2, m2.lens, block_table=bt2, q_lens=m2.n)
+    np.testing.assert_array_equal(wl.bits(kd), ek)
+    np.testing.assert_array_equal(wl.bits(vd), ev)
+    ek, ev = oracle.kv_append_multi(m2.k_new, m2.v_new, kr2, vr2, m2.lens, window=128, q_lens=m2.n)
+    np.testing.assert_array_equal(wl.bits(krd), ek)
+    np.testing.assert_array_equal(wl.bits(vrd), ev)

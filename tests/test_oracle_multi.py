@@ -35,9 +35,15 @@ class Multi:
                 self.v_new[b, t] = c.hist_v[b, self.base[b] + t]
         self.sinks = c.sinks
 
-    def paged(self, seed=1, after=False):
+    def paged(self, seed=1, after=False, total_pages=None, table_width=None):
+        """Pools of the history (before the step, or after its append) behind a shuffled
+        block table; optionally exactly total_pages pages and table_width table columns."""
         kp, vp, bt = paged_identity(self.c, self.lens if after else self.base)
-        return shuffle_pages(kp, vp, bt, seed, spare=3)
+        spare = 3 if total_pages is None else total_pages - kp.shape[0]
+        kp, vp, bt = shuffle_pages(kp, vp, bt, seed, spare=spare)
+        if table_width is not None:
+            bt = np.pad(bt, ((0, 0), (0, table_width - bt.shape[1])), constant_values=-1)
+        return kp, vp, bt
 
     def ring(self, W, after=False):
         return ring_from_history(self.c, self.lens if after else self.base, W)
