@@ -1736,6 +1736,9 @@ struct MultiPlan {
 #ifndef DA_MULTI_MAX_CHUNK
 #define DA_MULTI_MAX_CHUNK 128
 #endif
+#ifndef DA_MULTI_TC_MAX_CHUNK  // the same cap for tcgen05 CTAs, whose set-up is heavier
+#define DA_MULTI_TC_MAX_CHUNK 1024
+#endif
 
 MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_seq_len, int sms) {
     MultiPlan m;
@@ -1756,7 +1759,8 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     const long long target = static_cast<long long>(m.tc ? DA_MULTI_TC_CTAS_PER_SM : DA_MULTI_CTAS_PER_SM) * sms;
     long long sp = std::max<long long>(1, (target + groups - 1) / std::max<long long>(1, groups));
     sp = std::max(sp, (max_tiles + kMMaxChunk - 1) / kMMaxChunk);  // a CTA's pages fit its smem
-    if (!m.tc) sp = std::max(sp, (max_tiles + DA_MULTI_MAX_CHUNK - 1) / DA_MULTI_MAX_CHUNK);
+    const long long cap = m.tc ? DA_MULTI_TC_MAX_CHUNK : DA_MULTI_MAX_CHUNK;
+    sp = std::max(sp, (max_tiles + cap - 1) / cap);
     sp = std::min(sp, max_tiles);
     m.chunk = static_cast<int>((max_tiles + sp - 1) / sp);
     m.splits = static_cast<int>((max_tiles + m.chunk - 1) / m.chunk);
