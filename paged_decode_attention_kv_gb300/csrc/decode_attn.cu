@@ -13,7 +13,8 @@
 //     units are ordered (b, g, tile), so a "segment" (b, g) is a contiguous
 //     run of units. Every CTA recomputes the prefix of units over b from
 //     seq_lens in shared memory.
-//   * the grid is one CTA per SM, 8 warps each; every warp is a worker that
+//   * the grid is one CTA per SM (two for the fp8 cache with 8-head groups,
+//     whose instruction chains need the extra warps), 8 warps each; every warp is a worker that
 //     takes an equal contiguous share of all units (split-KV with perfect
 //     balance, whatever the length mix). A warp streams its tiles through a
 //     private TMA/mbarrier pipeline and keeps an online-softmax state (running
@@ -61,10 +62,25 @@ constexpr int kThreads = kWarps * 32;
 #ifndef DA_STAGES_G16
 #define DA_STAGES_G16 4
 #endif
-template <int NT, bool ROPE, bool KV8>
+// CPS = CTAs resident per SM (1 or 2). On large calls the fp8 kernel with 8-head groups is
+// bound by the latency of its per-warp convert / MMA / softmax chain, not by HBM: two CTAs
+// (16 warps, 128 registers each, 3 stages per warp) hide it better than one CTA with 7
+// stages. Small calls, whose warps own a few tiles each, are bound by the first tiles'
+// arrival and keep the deeper single-CTA pipeline. The host picks CPS per call from an
+// upper bound of the call's tiles.
+#ifndef DA_STAGES_FP8_2CTA
+#define DA_STAGES_FP8_2CTA 3
+#endif
+#ifndef DA_FP8_2CTA_MIN_TILES
+#define DA_FP8_2CTA_MIN_TILES 16384
+#endif
+constexpr int kMaxCtasPerSm = 2;
+template <int NT, bool ROPE, bool KV8, int CPS>
 __host__ __device__ constexpr int stages_for() {
-    // fp8 tiles are half the size: more of them in flight for the same bytes
-    return KV8 ? (NT == 1 ? 7 : 6) : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16);
+    // fp8 tiles are half the size: more of them in flight for the same bytes; with two
+    // CTAs per SM each gets half the shared memory
+    return KV8 ? (NT == 1 ? (CPS > 1 ? DA_STAGES_FP8_2CTA : 7) : 6)
+               : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16);
 }
 #ifndef DA_PAIR_BF16
 #define DA_PAIR_BF16 1
@@ -448,12 +464,12 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 // cover the four consecutive tokens 4t..4t+3 that one 32-bit word of a V^T row holds.
 __device__ __forceinline__ int fp8_row_token(int g) { return 4 * (g >> 1) + (g & 1); }
 
-// Shared-memory layout of decode_attn_kernel<NT, ., ROPE>: byte offsets from a 1024-byte
+// Shared-memory layout of decode_attn_kernel<NT, ., ROPE, KV8, CPS>: byte offsets from a 1024-byte
 // aligned base. The kernel carves its buffers from these offsets and the launch
 // requests `bytes`, so the two cannot drift apart.
-template <int NT, bool ROPE, bool KV8>
+template <int NT, bool ROPE, bool KV8, int CPS>
 struct SmemLayout {
-    static constexpr int kStages = stages_for<NT, ROPE, KV8>();
+    static constexpr int kStages = stages_for<NT, ROPE, KV8, CPS>();
     static constexpr int GP = NT * 8;
     // a stage holds a K and a V tile (bf16: 2 KiB each, kept 1024-byte aligned for the
     // 128-byte swizzle; all K tiles first, then all V tiles) or one fp8 block
@@ -475,14 +491,16 @@ struct SmemLayout {
     static_assert(kWarpTileBytes % 16 == 0 && kStageBytes % 16 == 0, "bulk copies need 16-byte alignment");
     static_assert(kQBytes % 16 == 0 && meta % 16 == 0, "bulk copies and int4 need 16-byte alignment");
     static_assert(bytes <= kMaxSmem, "shared memory budget");
+    // every resident CTA also takes 1 KiB of reserved shared memory (228 KiB per SM)
+    static_assert(CPS == 1 || CPS * (bytes + 1024) <= 233472, "shared memory budget of the CTAs on one SM");
 };
 
 // ------------------------------------------------------------------ the kernel
-template <int NT, bool RING, bool ROPE, bool KV8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NT, bool RING, bool ROPE, bool KV8, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
-    using Lay = SmemLayout<NT, ROPE, KV8>;
+    using Lay = SmemLayout<NT, ROPE, KV8, CPS>;
     constexpr int kTileB = KV8 ? kBlk8V : kTileBytes;  // bytes of one K (or V) tile
     constexpr int kStages = Lay::kStages;
     constexpr int GP = Lay::GP;
@@ -1469,7 +1487,7 @@ struct DeviceState {
     void *ws_multi = nullptr;  // multi-token calls: counters + split partials
     size_t ws_multi_bytes = 0;
     int sm_count = 0;
-    bool attr_set[16] = {};
+    bool attr_set[32] = {};
     bool multi_attr_set[4] = {};
 };
 DeviceState g_dev[kMaxDevices];
@@ -1496,7 +1514,10 @@ size_t slot_floats(int G) {
     return static_cast<size_t>(2 * gp + gp * kD);
 }
 
-size_t workspace_for(int G, int ctas) {
+// Counters and two partial slots per CTA of the largest grid a decode call of group size G
+// may launch.
+size_t workspace_for(int G, int sms) {
+    const int ctas = sms * (G <= 8 ? kMaxCtasPerSm : 1);  // two CTAs per SM: fp8, 8-head groups
     return kCounterBytes + static_cast<size_t>(ctas) * 2 * slot_floats(G) * sizeof(float);
 }
 
@@ -1535,12 +1556,13 @@ int check_shape(const da_shape &s) {
     return DA_OK;
 }
 
-template <int NT, bool RING, bool ROPE, bool KV8 = false>
+template <int NT, bool RING, bool ROPE, bool KV8 = false, int CPS = 1>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
-    const size_t smem = SmemLayout<NT, ROPE, KV8>::bytes;
+    static_assert(CPS == 1 || (KV8 && NT == 1), "two CTAs per SM: fp8 kernel with 8-head groups only");
+    const size_t smem = SmemLayout<NT, ROPE, KV8, CPS>::bytes;
     const size_t smem_max = smem;
-    auto kern = decode_attn_kernel<NT, RING, ROPE, KV8>;
-    const int idx = (NT - 1) * 8 + (RING ? 4 : 0) + (ROPE ? 2 : 0) + (KV8 ? 1 : 0);
+    auto kern = decode_attn_kernel<NT, RING, ROPE, KV8, CPS>;
+    const int idx = (CPS - 1) * 16 + (NT - 1) * 8 + (RING ? 4 : 0) + (ROPE ? 2 : 0) + (KV8 ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
@@ -1551,7 +1573,7 @@ int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm,
     // while the previous kernel of the stream drains; it waits for that kernel before
     // touching memory (griddepcontrol.wait).
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sm_count(dev));
+    cfg.gridDim = dim3(sm_count(dev) * CPS);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1654,9 +1676,22 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
         }
     }
     if (kv8) {
-        if (G <= 8)
+        if (G <= 8) {
+            // an upper bound of the call's tiles, from shapes only (seq_lens stay on the device)
+            long long per_seq;
+            if (ring) {
+                per_seq = window / kPage;
+            } else {
+                const int span = window > 0 ? std::min(window, max_seq_len) : max_seq_len;
+                per_seq = (span + kPage - 1) / kPage + 1;
+            }
+            const bool two = static_cast<long long>(s.batch) * s.num_kv_heads * per_seq >= DA_FP8_2CTA_MIN_TILES;
+            if (two)
+                return ring ? launch_attn<1, true, false, true, 2>(mk, mv, prm, dev, stream)
+                            : launch_attn<1, false, false, true, 2>(mk, mv, prm, dev, stream);
             return ring ? launch_attn<1, true, false, true>(mk, mv, prm, dev, stream)
                         : launch_attn<1, false, false, true>(mk, mv, prm, dev, stream);
+        }
         return ring ? launch_attn<2, true, false, true>(mk, mv, prm, dev, stream)
                     : launch_attn<2, false, false, true>(mk, mv, prm, dev, stream);
     }

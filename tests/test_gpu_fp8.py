@@ -133,6 +133,51 @@ def test_full_size_fp8(name):
     assert_blocks_equal(from_dev(pool), want)
 
 
+@pytest.mark.parametrize("max_seq_len", [None, 1 << 20])
+def test_paged_fp8_grid_choice(max_seq_len):
+    """The host sizes the fp8 grid (one or two CTAs per SM) from an upper bound of the
+    call's tiles, which grows with max_seq_len; a tight and a very loose bound give the
+    two grids on the same sequences."""
+    lens = [1000, 17, 0, 512, 999, 1, 300, 64, 16, 800, 33, 700, 5, 950, 128, 640]
+    c = make_case(746, len(lens), 64, 8, 64, lens)
+    kp, vp, bt = paged_identity(c, pre(c))
+    kp, vp, bt = shuffle_pages(kp, vp, bt, 11, spare=4)
+    width = bt.shape[1] if max_seq_len is None else max_seq_len // 16
+    bt = np.pad(bt, ((0, 0), (0, width - bt.shape[1])), constant_values=-1)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c),
+                               oracle.Fp8Cache.empty_paged(kp.shape[0], c.Hkv, 16, c.D), block_table=bt)
+    kv = to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_paged_fp8(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kv, dev(bt),
+                             dev(c.lens), dev(c.sinks), 0, c.scale, out,
+                             max_seq_len=max(lens) if max_seq_len is None else max_seq_len)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_paged_fp8(c.q, c.k_new, c.v_new, cache, bt, c.lens, c.sinks, 0, c.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"paged fp8 max_seq_len={max_seq_len}")
+    assert_blocks_equal(from_dev(kv), oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, block_table=bt))
+
+
+@pytest.mark.parametrize("W", [256, 512])
+def test_ring_fp8_many_slots(W):
+    """64 slots of 8 KV heads: at W = 512 the ring call is large enough for the two-CTA grid."""
+    rng = np.random.default_rng(W)
+    lens = [0 if rng.random() < 0.1 else int(rng.integers(1, 3 * W)) for _ in range(64)]
+    lens[:4] = [W - 1, W, W + 1, 1]
+    c = make_case(747 + W, len(lens), 64, 8, 64, lens)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c), oracle.Fp8Cache.empty_ring(c.B, c.Hkv, W, c.D),
+                               window=W)
+    kv = to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_ring_fp8(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kv,
+                            dev(c.lens), dev(c.sinks), c.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_ring_fp8(c.q, c.k_new, c.v_new, cache, c.lens, c.sinks, W, c.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"ring fp8 many slots W={W}")
+    assert_blocks_equal(from_dev(kv), oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, window=W))
+
+
 def test_paged_fp8_maximum_batch():
     rng = np.random.default_rng(9)
     lens = [0 if rng.random() < 0.25 else int(rng.integers(1, 48)) for _ in range(1024)]
