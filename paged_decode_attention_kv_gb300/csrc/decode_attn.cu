@@ -1488,7 +1488,7 @@ struct DeviceState {
     size_t ws_multi_bytes = 0;
     int sm_count = 0;
     bool attr_set[32] = {};
-    bool multi_attr_set[4] = {};
+    bool multi_attr_set[8] = {};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -1906,10 +1906,12 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
         return DA_ERR_CUDA;
     }
+    const bool small = !m.tc && m.nw <= 2;
     auto kern = m.tc ? (ring ? multi_tc_kernel<true> : multi_tc_kernel<false>)
-                     : (ring ? multi_attn_kernel<true> : multi_attn_kernel<false>);
-    const int smem = m.tc ? kTcSmem : kMSmem;
-    const int aidx = (ring ? 1 : 0) + (m.tc ? 2 : 0);
+                     : small ? (ring ? multi_attn_kernel<true, 2> : multi_attn_kernel<false, 2>)
+                             : (ring ? multi_attn_kernel<true, kMWarps> : multi_attn_kernel<false, kMWarps>);
+    const int smem = m.tc ? kTcSmem : small ? MultiShape<2>::kSmem : MultiShape<kMWarps>::kSmem;
+    const int aidx = (ring ? 1 : 0) + (m.tc ? 2 : 0) + (small ? 4 : 0);
     if (!g_dev[dev].multi_attr_set[aidx]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)  // room for as many resident CTAs as the registers allow

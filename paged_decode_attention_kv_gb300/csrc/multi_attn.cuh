@@ -30,15 +30,34 @@
 #ifndef DA_MULTI_WARPS
 #define DA_MULTI_WARPS 4
 #endif
-#ifndef DA_MULTI_MIN_BLOCKS  // resident CTAs per SM the register budget is cut for
+// Two CTA shapes, by the warps a call needs: up to 2 (at most 16 query rows per sequence and
+// KV head: one or two tokens at 8 heads per group) and up to 4. Small CTAs gain most from
+// residency (many CTAs per SM with 4 stages each), 4-warp CTAs from deep pipelines (8 stages
+// at 4 CTAs per SM): measured on both shapes.
+#ifndef DA_MULTI_MIN_BLOCKS  // resident 4-warp CTAs per SM the register budget is cut for
 #define DA_MULTI_MIN_BLOCKS 4
+#endif
+#ifndef DA_MULTI_MIN_BLOCKS_SMALL  // the same for 1- and 2-warp CTAs
+#define DA_MULTI_MIN_BLOCKS_SMALL 10
+#endif
+#ifndef DA_MULTI_STAGES
+#define DA_MULTI_STAGES 8
+#endif
+#ifndef DA_MULTI_STAGES_SMALL
+#define DA_MULTI_STAGES_SMALL 4
 #endif
 constexpr int kMNT = DA_MULTI_NT;                 // 8-row n-tiles per warp (8 query rows each)
 constexpr int kMRowsPerWarp = 8 * kMNT;
 constexpr int kMWarps = DA_MULTI_WARPS;           // query-row warps per CTA at most
-constexpr int kMStages = 8;                       // K/V tile pairs in flight per CTA
 constexpr int kMStageBytes = 2 * kTileBytes;      // K tile, then V tile
-constexpr int kMSmem = 1024 + kMStages * kMStageBytes + 2 * kMStages * 8;
+// the shape of a CTA of at most NW warps: K/V tile pairs in flight, dynamic shared memory,
+// resident CTAs per SM for the register budget
+template <int NW>
+struct MultiShape {
+    static constexpr int kStages = NW <= 2 ? DA_MULTI_STAGES_SMALL : DA_MULTI_STAGES;
+    static constexpr int kSmem = 1024 + kStages * kMStageBytes + 2 * kStages * 8;
+    static constexpr int kMinBlocks = NW <= 2 ? DA_MULTI_MIN_BLOCKS_SMALL : DA_MULTI_MIN_BLOCKS;
+};
 constexpr int kMSlotFloats = 4 + kD;              // per query row: m, l (log2 units), 2 pad, acc[64]
 constexpr int kMAccOff = 4;                       // acc starts 16-byte aligned
 constexpr int kMMaxTokens = 4096;                 // query tokens per sequence per call
@@ -116,11 +135,12 @@ __device__ __noinline__ void multi_combine_rows(const MultiParams &p, const floa
     }
 }
 
-template <bool RING>
-__global__ void __launch_bounds__(kMWarps * 32, DA_MULTI_MIN_BLOCKS)
+template <bool RING, int NW>
+__global__ void __launch_bounds__(NW * 32, MultiShape<NW>::kMinBlocks)
     multi_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ CUtensorMap tnk, const __grid_constant__ CUtensorMap tnv,
                       const MultiParams p) {
+    constexpr int kMStages = MultiShape<NW>::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
