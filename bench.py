@@ -247,8 +247,9 @@ class StepInputs:
         return sum(t.numel() * t.element_size() for t in self.cache_tensors())
 
 
-def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=None):
+def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=None, out=None):
     import paged_decode_attention_kv_gb300 as da
+    out = s.out_full if out is None else out
     q = s.q if q is None else q
     k_new = s.k_new if k_new is None else k_new
     v_new = s.v_new if v_new is None else v_new
@@ -257,19 +258,20 @@ def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=
     sinks = s.sinks if sinks is None else sinks
     if s.T > 1:
         da.decode_attn_paged_multi(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks, 0,
-                                   s.inp.scale, s.out_full)
+                                   s.inp.scale, out)
     elif s.kv == "fp8":
-        da.decode_attn_paged_fp8(q, k_new, v_new, s.pool, bt, sl, sinks, 0, s.inp.scale, s.out_full)
+        da.decode_attn_paged_fp8(q, k_new, v_new, s.pool, bt, sl, sinks, 0, s.inp.scale, out)
     elif rope:
         da.decode_attn_paged_rope(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks,
-                                  s.rope_cos, s.rope_sin, 0, s.inp.scale, s.out_full)
+                                  s.rope_cos, s.rope_sin, 0, s.inp.scale, out)
     else:
         da.decode_attn_paged(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks, 0,
-                             s.inp.scale, s.out_full)
+                             s.inp.scale, out)
 
 
-def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
+def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None, out=None):
     import paged_decode_attention_kv_gb300 as da
+    out = s.out_ring if out is None else out
     q = s.q if q is None else q
     k_new = s.k_new if k_new is None else k_new
     v_new = s.v_new if v_new is None else v_new
@@ -277,15 +279,15 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None):
     sinks = s.sinks if sinks is None else sinks
     if s.T > 1:
         da.decode_attn_ring_multi(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
-                                  s.inp.scale, s.out_ring)
+                                  s.inp.scale, out)
     elif s.kv == "fp8":
-        da.decode_attn_ring_fp8(q, k_new, v_new, s.ring, sl, sinks, s.inp.scale, s.out_ring)
+        da.decode_attn_ring_fp8(q, k_new, v_new, s.ring, sl, sinks, s.inp.scale, out)
     elif rope:
         da.decode_attn_ring_rope(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
-                                 s.rope_cos, s.rope_sin, s.inp.scale, s.out_ring)
+                                 s.rope_cos, s.rope_sin, s.inp.scale, out)
     else:
         da.decode_attn_ring(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
-                            s.inp.scale, s.out_ring)
+                            s.inp.scale, out)
 
 
 def step_bytes(name, lens, kv="bf16", q_tokens=1):
@@ -542,28 +544,48 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-def run_e2e(args, s, step_bytes_total, dev):
-    """Per step: H2D of q, k_new, v_new, seq_lens, block table, sinks from pinned host
-    memory; both layer calls; D2H of both outputs. Wall clock around the whole loop."""
+def packed(tensors, dev=None, pin=False):
+    """One byte buffer holding the given tensors back to back (each at a 256-byte aligned
+    offset) and a view of each one into it, so that a step moves them in one copy."""
     import torch
-    import paged_decode_attention_kv_gb300 as da
-    host = {k: getattr(s, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "seq_lens", "sinks")}
-    host["block_table"] = s.block_table.cpu().pin_memory()
-    outs = [torch.empty(s.out_full.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    dst = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off += -(-t.numel() * t.element_size() // 256) * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    if pin:
+        buf = buf.pin_memory()
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    return buf, views
+
+
+def run_e2e(args, s, step_bytes_total, dev):
+    """Per step: one H2D copy of q, k_new, v_new, seq_lens, block table and sinks, staged
+    back to back in one pinned host buffer (as a serving loop stages a step's inputs); both
+    layer calls; one D2H copy of both outputs, which the calls write into one device buffer.
+    Wall clock around the whole loop."""
+    import torch
+    names = ("q", "k_new", "v_new", "seq_lens", "sinks", "block_table")
+    src = [getattr(s, k) for k in names]
+    host_in, host_views = packed(src, pin=True)
+    for v, t in zip(host_views, src):
+        v.copy_(t.cpu())
+    dev_in, dev_views = packed(src, dev=dev)
+    dst = dict(zip(names, dev_views))
+    dev_out, (out_full, out_ring) = packed([s.out_full, s.out_ring], dev=dev)
+    host_out = torch.empty_like(dev_out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in src)
+    d2h = s.out_full.numel() * s.out_full.element_size() + s.out_ring.numel() * s.out_ring.element_size()
     n = max(3, min(args.steps, args.e2e_steps))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(n):
-        for k, v in host.items():
-            dst[k].copy_(v, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         call_paged(s, args.rope, dst["q"], dst["k_new"], dst["v_new"], dst["block_table"],
-                   dst["seq_lens"], dst["sinks"])
-        call_ring(s, args.rope, dst["q"], dst["k_new"], dst["v_new"], dst["seq_lens"], dst["sinks"])
-        outs[0].copy_(s.out_full, non_blocking=True)
-        outs[1].copy_(s.out_ring, non_blocking=True)
+                   dst["seq_lens"], dst["sinks"], out=out_full)
+        call_ring(s, args.rope, dst["q"], dst["k_new"], dst["v_new"], dst["seq_lens"], dst["sinks"],
+                  out=out_ring)
+        host_out.copy_(dev_out, non_blocking=True)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     return {"value": round(step_bytes_total * n / dt / 1e9, 2), "unit": UNIT,
