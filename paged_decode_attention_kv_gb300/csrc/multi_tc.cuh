@@ -405,16 +405,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 const float mb = mraw * p.scale_log2;  // the scale is positive
                 const bool need = valid && mb > m_ref + kTcRescale;
                 const float m_new = need ? mb : m_ref;
-                // PV_{j-1} is waited for at every block, so that the parity of o_done never
-                // aliases an older phase (it is normally done by now)
-                if (j > 0) {
+                // P_j goes over S_j, whose buffer PV_{j-2} read: the MMA warp waited for PV_{j-2}
+                // before it wrote S_j. Only a rescale of O needs PV_{j-1} done, and the last
+                // block waits for it too so that the final wait below is for PV_{nblk-1} alone.
+                // A parity wait is exact only while the barrier is at most one phase behind or
+                // ahead of the awaited phase: here PV_{j-2} is complete (S_j exists) and PV_j
+                // cannot be issued before this block's P, so o_done stands at PV_{j-1} or one
+                // phase before it.
+                const bool resc = j > 0 && __any_sync(0xffffffffu, need);
+                if (j > 0 && (resc || j == nblk - 1)) {
                     if (__any_sync(0xffffffffu, !mbar_wait_bounded(o_done, (j - 1) & 1))) {
                         failed = true;
                         break;
                     }
                     tc_fence_after();
                 }
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                if (resc) {
                     // O holds PV_0 .. PV_{j-1}: rescale the rows that need it
                     const float f = need ? exp2f(m_ref - m_new) : 1.f;  // m_ref = -inf: 0 (O and l are 0)
                     uint32_t o[32];
@@ -476,6 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // ---- finish this thread's row: O (after the last PV) -> output or partial
         float o[64];
         bool have = false;
+        // the last PV (PV_{nblk-2} was waited for in the last block)
         if (!failed && warp_active && !__any_sync(0xffffffffu, !mbar_wait_bounded(o_done, (nblk - 1) & 1))) {
             tc_fence_after();
             uint32_t raw[2][32];
