@@ -399,9 +399,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         }
                     }
                 }
-                float mraw = -INFINITY;
+                // maximum as a pairwise tree (6 dependent steps instead of 64)
+                float mx[32];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mraw = fmaxf(mraw, x[c]);
+                for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
+#pragma unroll
+                for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+                    for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+                const float mraw = mx[0];
                 const float mb = mraw * p.scale_log2;  // the scale is positive
                 const bool need = valid && mb > m_ref + kTcRescale;
                 const float m_new = need ? mb : m_ref;
@@ -439,7 +445,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     m_ref = m_new;
                 }
                 const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-                float ls = 0.f;
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {  // keys 32h .. 32h + 31: hi and lo, 16 columns each
                     uint32_t hi[16], lo[16];
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     for (int c = 0; c < 16; ++c) {
                         const float p0 = fast_exp2(fmaf(x[32 * h + 2 * c], p.scale_log2, -mr));
                         const float p1 = fast_exp2(fmaf(x[32 * h + 2 * c + 1], p.scale_log2, -mr));
-                        ls += p0 + p1;
+                        ls4[c & 3] += p0 + p1;
                         hi[c] = pack_bf16(p0, p1);
                         const float2 r2 = unpack_bf16(hi[c]);
                         lo[c] = pack_bf16(p0 - r2.x, p1 - r2.y);
@@ -456,7 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     tmem_st16(tm + lanes + kTcColS + 64 * (j & 1) + 32 + 16 * h, lo);
                     tmem_wait_st();
                 }
-                l += ls;
+                l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             }
             if (warp == 0) {  // V rows of keys that do not exist may hold anything: zero them
                 uint8_t *vb = sKV + (j % kTcStages) * kTcStageBytes + kTcBlockBytes;
