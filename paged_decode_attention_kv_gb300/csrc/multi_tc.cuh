@@ -23,7 +23,10 @@
 constexpr int kTcRows = 128;                               // query rows per CTA (MMA M)
 constexpr int kTcKeys = 64;                                // keys per block (MMA N of S)
 constexpr int kTcTilesPerBlock = kTcKeys / kPage;          // 4
-constexpr int kTcStages = 4;                               // key blocks in flight
+#ifndef DA_TC_STAGES
+#define DA_TC_STAGES 5
+#endif
+constexpr int kTcStages = DA_TC_STAGES;                    // key blocks in flight
 constexpr int kTcBlockBytes = kTcTilesPerBlock * kTileBytes;  // 8 KiB of K (or V)
 constexpr int kTcStageBytes = 2 * kTcBlockBytes;           // K block, then V block
 constexpr int kTcQBytes = kTcRows * kD * 2;                // 16 KiB
