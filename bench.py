@@ -527,8 +527,11 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic,
                      "kernel": ("decode_attn_kernel (paged, full attention%s)" % (
                          "" if args.kv == "bf16" else ", fp8 cache")) if args.q_tokens == 1 else
-                     ("multi_attn_kernel + kv_append_multi_kernel (paged, full attention, "
-                      "%d query tokens; one bracket around both)" % args.q_tokens),
+                     ("%s + kv_append_multi_kernel (paged, full attention, "
+                      "%d query tokens; one bracket around both)" % (
+                          # the library runs 64+ query rows per KV head on tcgen05
+                          "multi_tc_kernel" if args.q_tokens * first.cfg["Hq"] // first.cfg["Hkv"] >= 64
+                          else "multi_attn_kernel", args.q_tokens)),
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
