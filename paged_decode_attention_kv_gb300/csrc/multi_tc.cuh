@@ -9,16 +9,17 @@
 //   warp 5     lane 0 issues the MMAs:  S_j = Q K_j^T  (M 128, N 64, K 64; A = Q, B = K, both
 //              K-major in shared memory, 128-byte swizzle)  and  O += P_j V_j  (M 128, N 64,
 //              K 64; A = P_j in TMEM as bf16, B = V_j with d contiguous)
-// TMEM: S_0 columns [0, 64), S_1 [64, 128), O [128, 192). P_j overwrites S_{j%2} as two bf16
-// parts, P = hi + lo (hi = P rounded to bf16 in columns [0, 32), lo = the rest in [32, 64)),
+// TMEM: S buffers b = 0 .. kTcSBufs - 1 at columns [64 b, 64 b + 64), O after them. Block j
+// uses buffer j % kTcSBufs; P_j overwrites S_j there as two bf16 parts, P = hi + lo (hi = P rounded to bf16 in columns [0, 32), lo = the rest in [32, 64)),
 // and the PV product runs on both: about 16 significant bits on every probability, so a
 // sharply peaked softmax loses nothing to the bf16 operand. The softmax keeps a per-row
 // reference maximum and
 // rescales O (in TMEM) only when a block's maximum exceeds it by more than 2^8, so the
 // probabilities stay below 256 and O is rarely touched; O and l share the reference, so the
 // final O / l is exact.
-// Barriers: kv_full / kv_empty per stage (TMA <-> MMA), s_full / p_full per S buffer
-// (MMA <-> softmax), o_done (every PV), drain (all MMAs before TMEM is freed).
+// Barriers: kv_full / kv_empty per stage (TMA <-> MMA); s_full / p_full / o_done per S buffer
+// (S_j written, P_j written, PV_j done: one phase per use of the buffer, so every parity wait
+// below is at most one phase behind its barrier); drain (all MMAs before TMEM is freed).
 
 constexpr int kTcRows = 128;                               // query rows per CTA (MMA M)
 constexpr int kTcKeys = 64;                                // keys per block (MMA N of S)
@@ -30,12 +31,19 @@ constexpr int kTcStages = DA_TC_STAGES;                    // key blocks in flig
 constexpr int kTcBlockBytes = kTcTilesPerBlock * kTileBytes;  // 8 KiB of K (or V)
 constexpr int kTcStageBytes = 2 * kTcBlockBytes;           // K block, then V block
 constexpr int kTcQBytes = kTcRows * kD * 2;                // 16 KiB
-constexpr int kTcBars = 2 * kTcStages + 2 + 2 + 1 + 1;
+// S / P buffers in TMEM: S_j waits for PV_{j-kTcSBufs}. A third buffer (TMEM has the room)
+// measured no faster: the row warps' softmax, not the MMA hand-off, sets the pace.
+#ifndef DA_TC_SBUFS
+#define DA_TC_SBUFS 2
+#endif
+constexpr int kTcSBufs = DA_TC_SBUFS;
+constexpr int kTcBars = 2 * kTcStages + 3 * kTcSBufs + 1;
 constexpr int kTcSmem = 1024 + kTcQBytes + kTcStages * kTcStageBytes + kTcBars * 8;
 constexpr int kTcWarps = 6;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr uint32_t kTcTmemCols = 256;
-constexpr uint32_t kTcColS = 0, kTcColO = 128;             // S_b at kTcColS + 64 b
+constexpr uint32_t kTcColS = 0, kTcColO = 64 * kTcSBufs;  // S_b at kTcColS + 64 b
+static_assert(kTcColO + 64 <= kTcTmemCols, "S buffers and O fit the TMEM allocation");
 constexpr float kTcRescale = 8.f;                          // log2 of the largest probability
 
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte offsets (16-byte
@@ -122,8 +130,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint8_t *sKV = smem + kTcQBytes;                     // [stage][K block | V block]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sKV + kTcStages * kTcStageBytes);
     const uint32_t kv_full = smem_addr(bars), kv_empty = kv_full + 8 * kTcStages;
-    const uint32_t s_full = kv_empty + 8 * kTcStages, p_full = s_full + 16;
-    const uint32_t o_done = p_full + 16, drain = o_done + 8;
+    const uint32_t s_full = kv_empty + 8 * kTcStages, p_full = s_full + 8 * kTcSBufs;
+    const uint32_t o_done = p_full + 8 * kTcSBufs, drain = o_done + 8 * kTcSBufs;
     __shared__ int s_page[kMMaxChunk];
     __shared__ uint32_t s_tmem;
     __shared__ int s_ticket, s_failed;
@@ -141,11 +149,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_init(kv_full + 8 * s, 1);
             mbar_init(kv_empty + 8 * s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kTcSBufs; ++s) {
             mbar_init(s_full + 8 * s, 1);
             mbar_init(p_full + 8 * s, 4);  // the four row warps
+            mbar_init(o_done + 8 * s, 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_failed = 0;
@@ -306,8 +314,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         failed = true;
                         break;
                     }
-                    // S_{j%2} last held P_{j-2}: its PV must be done (only PV_{j-2} can be pending)
-                    if (j >= 2 && !mbar_wait_bounded(o_done, (j - 2) & 1)) {
+                    // buffer j % kTcSBufs last held P_{j-kTcSBufs}: its PV must be done
+                    const int sb = j % kTcSBufs;
+                    if (j >= kTcSBufs && !mbar_wait_bounded(o_done + 8 * sb, ((j / kTcSBufs) - 1) & 1)) {
                         failed = true;
                         break;
                     }
@@ -315,13 +324,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const uint32_t k_s = smem_addr(sKV + s * kTcStageBytes);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk)
-                        umma_bf16_ss(tm + kTcColS + 64 * (j & 1), umma_sdesc(q_s + 32 * kk, 16, 1024),
+                        umma_bf16_ss(tm + kTcColS + 64 * sb, umma_sdesc(q_s + 32 * kk, 16, 1024),
                                      umma_sdesc(k_s + 32 * kk, 16, 1024), id_qk, kk > 0);
-                    umma_commit(s_full + 8 * (j & 1));
+                    umma_commit(s_full + 8 * sb);
                 }
                 if (j >= 1) {
-                    const int jj = j - 1, s = jj % kTcStages;
-                    if (!mbar_wait_bounded(p_full + 8 * (jj & 1), (jj >> 1) & 1)) {
+                    const int jj = j - 1, s = jj % kTcStages, pb = jj % kTcSBufs;
+                    if (!mbar_wait_bounded(p_full + 8 * pb, (jj / kTcSBufs) & 1)) {
                         failed = true;
                         break;
                     }
@@ -331,10 +340,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     for (int part = 0; part < 2; ++part)  // P = hi + lo
 #pragma unroll
                         for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                            umma_bf16_ts(tm + kTcColO, tm + kTcColS + 64 * (jj & 1) + 32 * part + 8 * kk,
+                            umma_bf16_ts(tm + kTcColO, tm + kTcColS + 64 * pb + 32 * part + 8 * kk,
                                          umma_sdesc(v_s + 2048 * kk, 2048, 1024), id_pv,
                                          (jj > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(o_done);
+                    umma_commit(o_done + 8 * pb);
                     umma_commit(kv_empty + 8 * s);
                 }
             }
@@ -355,13 +364,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // every row warp waits for S_j, rows or not, so that no warp's arrival on p_full
             // can run ahead into a later phase (a give-up is taken by the whole warp: the TMEM
             // accesses below are warp-wide)
-            if (__any_sync(0xffffffffu, !mbar_wait_bounded(s_full + 8 * (j & 1), (j >> 1) & 1))) {
+            const int sb = j % kTcSBufs;
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(s_full + 8 * sb, (j / kTcSBufs) & 1))) {
                 failed = true;
                 break;
             }
             if (warp_active) {
                 tc_fence_after();
-                const uint32_t sc = tm + lanes + kTcColS + 64 * (j & 1);
+                const uint32_t sc = tm + lanes + kTcColS + 64 * sb;
                 uint32_t raw[2][32];
                 tmem_ld32(sc, raw[0]);
                 tmem_ld32(sc + 32, raw[1]);
@@ -414,22 +424,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 const float mb = mraw * p.scale_log2;  // the scale is positive
                 const bool need = valid && mb > m_ref + kTcRescale;
                 const float m_new = need ? mb : m_ref;
-                // P_j goes over S_j, whose buffer PV_{j-2} read: the MMA warp waited for PV_{j-2}
-                // before it wrote S_j. Only a rescale of O needs PV_{j-1} done, and the last
-                // block waits for it too so that the final wait below is for PV_{nblk-1} alone.
-                // A parity wait is exact only while the barrier is at most one phase behind or
-                // ahead of the awaited phase: here PV_{j-2} is complete (S_j exists) and PV_j
-                // cannot be issued before this block's P, so o_done stands at PV_{j-1} or one
-                // phase before it.
+                // P_j goes over S_j, whose buffer PV_{j-kTcSBufs} read: the MMA warp waited for
+                // that PV before it wrote S_j. Only a rescale of O needs PV_{j-1} done. Its
+                // buffer's o_done is exact for that wait: the buffer's previous PV
+                // (PV_{j-1-kTcSBufs}) is complete since S_{j-1} exists, and its next one
+                // cannot be issued before P_{j-1+kTcSBufs}.
                 const bool resc = j > 0 && __any_sync(0xffffffffu, need);
-                if (j > 0 && (resc || j == nblk - 1)) {
-                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(o_done, (j - 1) & 1))) {
+                if (resc) {
+                    const int jb = (j - 1) % kTcSBufs;
+                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(o_done + 8 * jb, ((j - 1) / kTcSBufs) & 1))) {
                         failed = true;
                         break;
                     }
                     tc_fence_after();
-                }
-                if (resc) {
                     // O holds PV_0 .. PV_{j-1}: rescale the rows that need it
                     const float f = need ? exp2f(m_ref - m_new) : 1.f;  // m_ref = -inf: 0 (O and l are 0)
                     uint32_t o[32];
@@ -461,8 +468,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         const float2 r2 = unpack_bf16(hi[c]);
                         lo[c] = pack_bf16(p0 - r2.x, p1 - r2.y);
                     }
-                    tmem_st16(tm + lanes + kTcColS + 64 * (j & 1) + 16 * h, hi);
-                    tmem_st16(tm + lanes + kTcColS + 64 * (j & 1) + 32 + 16 * h, lo);
+                    tmem_st16(tm + lanes + kTcColS + 64 * sb + 16 * h, hi);
+                    tmem_st16(tm + lanes + kTcColS + 64 * sb + 32 + 16 * h, lo);
                     tmem_wait_st();
                 }
                 l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
@@ -486,13 +493,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + 8 * (j & 1));
+            if (lane == 0) mbar_arrive(p_full + 8 * sb);
         }
         // ---- finish this thread's row: O (after the last PV) -> output or partial
         float o[64];
         bool have = false;
-        // the last PV (PV_{nblk-2} was waited for in the last block)
-        if (!failed && warp_active && !__any_sync(0xffffffffu, !mbar_wait_bounded(o_done, (nblk - 1) & 1))) {
+        // the last PV (its buffer's previous PV is complete: S_{nblk-1} exists); the PVs
+        // complete in issue order, so O then holds all of them
+        const int lb = (nblk - 1) % kTcSBufs;
+        if (!failed && warp_active &&
+            !__any_sync(0xffffffffu, !mbar_wait_bounded(o_done + 8 * lb, ((nblk - 1) / kTcSBufs) & 1))) {
             tc_fence_after();
             uint32_t raw[2][32];
             tmem_ld32(tm + lanes + kTcColO, raw[0]);
