@@ -111,13 +111,38 @@ def nominal_hbm_peak():
     return mhz * 1e6 * 2 * HBM_BUS_BITS / 8 / 1e9
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its // and /* */ comments (string and character literals kept),
+    so that editing a comment does not change what the code hash identifies."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # a literal: copy through its closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def source_hash():
-    """sha256[:16] of the kernel sources (every .cu / .cuh of csrc, in name order)."""
+    """sha256[:16] of the kernel sources' code (every .cu / .cuh of csrc, in name order,
+    comments removed)."""
     h = hashlib.sha256()
     csrc = os.path.dirname(KERNEL_SRC)
     for name in sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,7 +13,7 @@
 //     units are ordered (b, g, tile), so a "segment" (b, g) is a contiguous
 //     run of units. Every CTA recomputes the prefix of units over b from
 //     seq_lens in shared memory.
-//   * the grid is one CTA per SM (two for the fp8 cache with 8-head groups,
+//   * the grid is one CTA per SM (two on large fp8 calls with 8-head groups,
 //     whose instruction chains need the extra warps), 8 warps each; every warp is a worker that
 //     takes an equal contiguous share of all units (split-KV with perfect
 //     balance, whatever the length mix). A warp streams its tiles through a

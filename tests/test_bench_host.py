@@ -62,3 +62,12 @@ def test_recorded_traffic_is_ignored_for_another_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("b64", "paged") is None
     monkeypatch.setattr(bench, "TRAFFIC_FILE", os.path.join(str(tmp_path), "missing.txt"))
     assert bench.recorded_traffic("b64", "paged") is None
+
+
+def test_the_code_hash_ignores_comments_only():
+    src = 'int a = 1; // one\nconst char *s = "// kept /* kept */"; /* two\nlines */ char c = \'"\';'
+    out = bench.strip_comments(src)
+    assert "one" not in out and "two" not in out and "lines" not in out
+    assert '"// kept /* kept */"' in out and "char c = '\"';" in out and "int a = 1;" in out
+    assert bench.strip_comments(src.replace("// one", "// another")) == out
+    assert bench.strip_comments(src.replace("a = 1", "a = 2")) != out
