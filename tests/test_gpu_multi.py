@@ -90,6 +90,17 @@ def test_ring_multi_matches_oracle(W, T):
     run_ring(m, W)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (16, 1)])
+def test_one_token_through_the_multi_calls(Hq, Hkv):
+    """T = 1 (one warp per CTA at G = 8, two at G = 16): the multi-token calls reduce to
+    the single-token step, paged and ring, with and without the token counts."""
+    lens = [1, 16, 17, 300, 0, 129]
+    m = Multi(860 + Hq, Hq, Hkv, lens, [1 if L > 0 else 0 for L in lens], 1)
+    run_paged(m, 0)
+    run_paged(m, 100, q_lens=False)
+    run_ring(m, 128)
+
+
 def test_all_rows_new_without_q_lens_and_no_sinks():
     m = Multi(870, 64, 8, [8, 40, 300], [8, 8, 8], 8)
     run_paged(m, 0, q_lens=False)
