@@ -315,6 +315,21 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None, out=
                             s.inp.scale, out)
 
 
+def decode_route(q_tokens, cfg):
+    """Whether the library runs a paged multi-token call in the decode kernel (one or two
+    query tokens, at most 16 query rows per KV head), append fused."""
+    return 1 < q_tokens <= 2 and q_tokens * cfg["Hq"] // cfg["Hkv"] <= 16
+
+
+def launches_per_step(q_tokens, cfg):
+    """Kernel launches of one step (a paged and a ring layer): one per layer for a single
+    query token; for several, the ring layer's attention and append, and the paged layer's
+    one (decode route) or two."""
+    if q_tokens == 1:
+        return 2
+    return 2 + (1 if decode_route(q_tokens, cfg) else 2)
+
+
 def step_bytes(name, lens, kv="bf16", q_tokens=1):
     from paged_decode_attention_kv_gb300 import workloads as wl
     c = wl.config(name)
@@ -552,7 +567,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic,
                      "kernel": ("decode_attn_kernel (paged, full attention%s)" % (
                          "" if args.kv == "bf16" else ", fp8 cache")) if args.q_tokens == 1 else
-                     ("%s + kv_append_multi_kernel (paged, full attention, "
+                     (("decode_attn_kernel (paged, full attention, %d query tokens, fused append)"
+                       % args.q_tokens) if decode_route(args.q_tokens, first.cfg) else
+                      "%s + kv_append_multi_kernel (paged, full attention, "
                       "%d query tokens; one bracket around both)" % (
                           # the library runs 64+ query rows per KV head on tcgen05
                           "multi_tc_kernel" if args.q_tokens * first.cfg["Hq"] // first.cfg["Hkv"] >= 64
@@ -560,7 +577,7 @@ def run_ours(args, rank, world, local_rank):
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
-        "gpu_launches": (2 if args.q_tokens == 1 else 4) * args.layers * args.steps,
+        "gpu_launches": launches_per_step(args.q_tokens, first.cfg) * args.layers * args.steps,
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
                    "events around every launch in a second pass (includes the launch gap)"),
         "clocks": clocks,

@@ -145,6 +145,10 @@ struct Params {
     const float *rope_cos;  // [max_position][D/2] fp32, or null: no rotary embedding
     const float *rope_sin;
     int max_position;
+    // several query tokens (the MT kernel): q / out [B][T][Hq][D], k_new / v_new
+    // [B][T][Hkv][D]; the n = q_lens[b] (T if null) newest positions are new tokens
+    int T;
+    const int *q_lens;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -426,6 +430,40 @@ __device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&s
     }
 }
 
+// The same for several query tokens: column r = t G + h of the group goes to
+// out[b][t][g G + h]; rows t >= n (no query token) are written as zeros.
+template <int NT>
+__device__ __forceinline__ void state_write_out_mt(SegState<NT> &s, const float (&sig)[NT][2], __nv_bfloat16 *out,
+                                                   int b, int g, int T, int G, int Hq, int nq, int lane) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        float f[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float M = fmaxf(s.m[n][j], sig[n][j]);
+            if (M == -INFINITY) {  // a column that saw no key and has no sink (not a query row)
+                f[j] = 0.f;
+                continue;
+            }
+            const float a = fast_exp2(s.m[n][j] - M);
+            const float den = s.l[n][j] * a + fast_exp2(sig[n][j] - M);
+            f[j] = a / den;
+        }
+        const int r = n * 8 + (lane >> 2), t = r / G, h = r - t * G;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            uint32_t lo = movmatrix_t(pack_bf16(s.acc[n][mt][0] * f[0], s.acc[n][mt][1] * f[1]));
+            uint32_t hi = movmatrix_t(pack_bf16(s.acc[n][mt][2] * f[0], s.acc[n][mt][3] * f[1]));
+            if (r < T * G) {
+                if (t >= nq) lo = hi = 0u;
+                uint32_t *row = reinterpret_cast<uint32_t *>(out + ((static_cast<size_t>(b) * T + t) * Hq + g * G + h) * kD);
+                row[(mt * 16 + (lane & 3) * 2) >> 1] = lo;
+                row[(mt * 16 + 8 + (lane & 3) * 2) >> 1] = hi;
+            }
+        }
+    }
+}
+
 // ---- fp8 (e4m3) helpers
 // Four e4m3 codes (bytes 0..3 of w) to two fp16 pairs: bytes 0,1 -> lo, bytes 2,3 -> hi
 // (lower byte to the lower half). Exact: every e4m3 value is an fp16 value.
@@ -467,9 +505,9 @@ __device__ __forceinline__ int fp8_row_token(int g) { return 4 * (g >> 1) + (g &
 // Shared-memory layout of decode_attn_kernel<NT, ., ROPE, KV8, CPS>: byte offsets from a 1024-byte
 // aligned base. The kernel carves its buffers from these offsets and the launch
 // requests `bytes`, so the two cannot drift apart.
-template <int NT, bool ROPE, bool KV8, int CPS>
+template <int NT, bool ROPE, bool KV8, int CPS, bool MT = false>
 struct SmemLayout {
-    static constexpr int kStages = stages_for<NT, ROPE, KV8, CPS>();
+    static constexpr int kStages = stages_for<NT, ROPE || MT, KV8, CPS>();  // MT: the RoPE build's room
     static constexpr int GP = NT * 8;
     // a stage holds a K and a V tile (bf16: 2 KiB each, kept 1024-byte aligned for the
     // 128-byte swizzle; all K tiles first, then all V tiles) or one fp8 block
@@ -477,9 +515,10 @@ struct SmemLayout {
     // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin
     // rows, the fp8 tile's K and V scale rows
     static constexpr int kRopeOff = GP * kD * 2 + 2 * kD * 2;
-    static constexpr int kQBytes = kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
+    // several query tokens: the rows of all T (<= 2) tokens, then their new k rows and v rows
+    static constexpr int kQBytes = MT ? GP * kD * 2 + 2 * 2 * kD * 2 : kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
     static constexpr int kWarpTileBytes = kStages * kStageBytes;  // the tiles of one warp
-    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8;
+    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8 + (MT ? kMaxBatch : 0);
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
     static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
     static constexpr size_t meta = bars + static_cast<size_t>(kWarps) * kStages * 8;
@@ -496,11 +535,16 @@ struct SmemLayout {
 };
 
 // ------------------------------------------------------------------ the kernel
-template <int NT, bool RING, bool ROPE, bool KV8, int CPS>
+// MT: several query tokens per sequence (paged, bf16, T <= 2, T * G <= 16): the query rows
+// of a KV head are (token t, head h) pairs r = t G + h, one column of the products each; row
+// t sees the positions lo_t .. base + t (base = L - n, lo_t its window start), the n new
+// tokens are appended in the same pass, rows t >= n are zero.
+template <int NT, bool RING, bool ROPE, bool KV8, int CPS, bool MT = false>
 __global__ void __launch_bounds__(kThreads, CPS)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const Params p) {
-    using Lay = SmemLayout<NT, ROPE, KV8, CPS>;
+    static_assert(!MT || (!RING && !ROPE && !KV8 && CPS == 1), "several query tokens: paged bf16 only");
+    using Lay = SmemLayout<NT, ROPE, KV8, CPS, MT>;
     constexpr int kTileB = KV8 ? kBlk8V : kTileBytes;  // bytes of one K (or V) tile
     constexpr int kStages = Lay::kStages;
     constexpr int GP = Lay::GP;
@@ -525,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
     int *s_winfo = s_wsum + kWarps;                                   // [kWarps][kWinfo]
     int *s_flag = s_winfo + kWarps * kWinfo;                          // [8]
+    int *s_n = s_flag + 8;                                            // [B] new tokens (MT)
     float *s_sink = reinterpret_cast<float *>(smem + Lay::sinks);     // [Hq], log2 units
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
@@ -552,18 +597,29 @@ __global__ void __launch_bounds__(kThreads, CPS)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int b = tid * 4 + k;
-            int L = 0;
+            int L = 0, nq = 1;
             if (b < B) {
                 L = __ldg(p.seq_lens + b);
                 bool bad = L < 0;
                 if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
+                if constexpr (MT) {
+                    nq = p.q_lens != nullptr ? __ldg(p.q_lens + b) : p.T;
+                    bad = bad || nq < 0 || nq > p.T || (L > 0 && nq > L);
+                }
                 if (bad) {
                     if (blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
                     L = 0;
                 }
+                if (MT && nq == 0) L = 0;  // no query row: an inactive slot
                 s_len[b] = L;
+                if constexpr (MT) s_n[b] = nq;
             }
-            v[k] = tiles_of<RING>(L, p.window) * Hkv;
+            if constexpr (MT) {  // positions lo_0 .. L - 1, lo_0 the first query token's window start
+                const int lo0 = (p.window > 0 && L > 0) ? max(0, L - nq - p.window + 1) : 0;
+                v[k] = (L > 0 ? (L - 1) / kPage - lo0 / kPage + 1 : 0) * Hkv;
+            } else {
+                v[k] = tiles_of<RING>(L, p.window) * Hkv;
+            }
             tsum += v[k];
         }
         int incl = tsum;
@@ -591,8 +647,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
     // ---- 2. inactive slots get a zero output
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         if (s_len[b] != 0) continue;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(b) * p.Hq * kD);
-        const int n16 = p.Hq * kD * 2 / 16;
+        const int rows_b = MT ? p.T : 1;  // query tokens per slot
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(b) * rows_b * p.Hq * kD);
+        const int n16 = rows_b * p.Hq * kD * 2 / 16;
         for (int i = tid; i < n16; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
     }
     if (U == 0) return;
@@ -654,7 +711,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 ot = r - og * tiles;
                 if (!RING) {
                     const int L = s_len[b];
-                    const int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+                    const int lo = MT ? ((p.window > 0) ? max(0, L - s_n[b] - p.window + 1) : 0)
+                                      : ((p.window > 0 && L > p.window) ? L - p.window : 0);
                     op = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + lo / kPage + ot);
                 }
             }
@@ -694,10 +752,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const bool newseg = (j == 0) || (tt == 0);
                 wmeta[stg] = make_int4(tb, tg, tt, tp);
                 const uint32_t bar = bar0 + 8 * stg;
-                const bool rows = newseg && p.k_new != nullptr;
+                const bool rows = !MT && newseg && p.k_new != nullptr;
                 const bool rope = ROPE && newseg;
-                mbar_expect_tx(bar, Lay::kStageBytes + (newseg ? p.G * kD * 2 : 0) + (rows ? 4 * kD : 0) +
-                                        (rope ? 4 * kD : 0));
+                const int qrows = MT ? p.T * p.G : p.G;  // query rows of the group
+                mbar_expect_tx(bar, Lay::kStageBytes + (newseg ? qrows * kD * 2 : 0) + (rows ? 4 * kD : 0) +
+                                        (rope ? 4 * kD : 0) + ((MT && newseg) ? p.T * 4 * kD : 0));
                 if constexpr (KV8) {  // the whole block in one copy (a bad page reads block 0)
                     const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
                                             : static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg;
@@ -710,10 +769,23 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
                     tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
                 }
-                if (newseg)
-                    bulk_load(q_tile(stg),
-                              p.q + (static_cast<size_t>(tb) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
-                              p.G * kD * 2, bar);
+                if (newseg) {
+                    if constexpr (MT) {  // rows t G .. t G + G - 1 of the slot: token t's heads of group tg;
+                                         // then the new tokens' k rows and v rows (2 each at most)
+                        for (int t = 0; t < p.T; ++t) {
+                            bulk_load(q_tile(stg) + t * p.G * kD * 2,
+                                      p.q + ((static_cast<size_t>(tb) * p.T + t) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
+                                      p.G * kD * 2, bar);
+                            const size_t off = ((static_cast<size_t>(tb) * p.T + t) * Hkv + tg) * kD;
+                            bulk_load(q_tile(stg) + GP * kD * 2 + t * kD * 2, p.k_new + off, kD * 2, bar);
+                            bulk_load(q_tile(stg) + GP * kD * 2 + (2 + t) * kD * 2, p.v_new + off, kD * 2, bar);
+                        }
+                    } else {
+                        bulk_load(q_tile(stg),
+                                  p.q + (static_cast<size_t>(tb) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
+                                  p.G * kD * 2, bar);
+                    }
+                }
                 if (rows) {
                     const size_t off = (static_cast<size_t>(tb) * Hkv + tg) * kD;
                     bulk_load(q_tile(stg) + GP * kD * 2, p.k_new + off, kD * 2, bar);
@@ -742,6 +814,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
         int sb = -1, sgk = -1;  // current segment (b, g)
         int seg_first_unit = 0, seg_end_unit = 0;
         int L = 0, lo = 0, ft = 0, nvalid = 0, app_tile = -1, app_row = 0;
+        // several query tokens: the segment's new-token count and first new position, the
+        // tightest bounds over its rows (tiles inside [lo_max, hi_min) need no mask), the new
+        // tokens' k/v (bf16 pairs of this lane), and this lane's columns' ranges [lo_c, hi_c)
+        int nq_seg = 1, base = 0, lo_max = 0, hi_min = 0;
+        uint32_t knew2[2] = {0u, 0u}, vnew2[2] = {0u, 0u};
         uint32_t knew = 0, vnew = 0;           // new token's k/v (bf16 pair, or 2 e4m3 codes)
         float knew_scale = 1.f, vnew_scale = 1.f;  // fp8: their scales
         const bool do_append = p.k_new != nullptr;
@@ -772,8 +849,29 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const int stg = stgs[u], tt = tts[u], tp = tps[u];
                 uint8_t *gK = wbase + k_off(stg);
                 uint8_t *gV = wbase + v_off(stg);
+                if constexpr (MT) {  // fused append of the new tokens this tile holds
+                    bool any = false;
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2) {
+                        const int pos = base + i2;
+                        if (i2 < nq_seg && pos / kPage - ft == tt) {
+                            const int row = pos % kPage;
+                            const uint32_t off = row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) + (lane & 3) * 4;
+                            const uint32_t kn = knew2[i2], vn = vnew2[i2];
+                            *reinterpret_cast<uint32_t *>(gK + off) = kn;
+                            *reinterpret_cast<uint32_t *>(gV + off) = vn;
+                            if (tp >= 0) {
+                                const size_t c = (static_cast<size_t>(tp) * Hkv + sgk) * kPage + row;
+                                reinterpret_cast<uint32_t *>(p.k_cache + c * kD)[lane] = kn;
+                                reinterpret_cast<uint32_t *>(p.v_cache + c * kD)[lane] = vn;
+                            }
+                            any = true;
+                        }
+                    }
+                    if (any) __syncwarp();
+                }
                 // fused append: this tile holds position p = L - 1
-                if (do_append && tt == app_tile) {
+                if (!MT && do_append && tt == app_tile) {
                     size_t slice, cell;  // (KV head) slice of the cache and the token's cell in it
                     bool ok = true;
                     if (RING) {
@@ -828,7 +926,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     ok_lo[u] = ok_hi[u] = true;
                 } else {
                     t0[u] = (RING ? tts[u] : ft + tts[u]) * kPage;
-                    partial[u] = (t0[u] < lo_v) || (t0[u] + kPage > hi_v);
+                    // several tokens: a tile is whole only inside every row's range
+                    partial[u] = MT ? (t0[u] < lo_max) || (t0[u] + kPage > hi_min)
+                                    : (t0[u] < lo_v) || (t0[u] + kPage > hi_v);
                     const int r0 = t0[u] + row_tok;
                     const int r8 = r0 + (KV8 ? 2 : 8);
                     ok_lo[u] = r0 >= lo_v && r0 < hi_v;
@@ -910,8 +1010,21 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     sv[u][2] = (sc[2] + sd[2]) * sl_hi;
                     sv[u][3] = (sc[3] + sd[3]) * sl_hi;
                     if (partial[u]) {
-                        if (!ok_lo[u]) sv[u][0] = sv[u][1] = -INFINITY;
-                        if (!ok_hi[u]) sv[u][2] = sv[u][3] = -INFINITY;
+                        if constexpr (MT) {  // key rows t0 + lane/4 and + 8 against each column's range
+                            const int kl = t0[u] + (lane >> 2), kh = kl + 8;
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const int r = n * 8 + (lane & 3) * 2 + j, t = r / p.G;
+                                const bool ok = r < p.T * p.G && t < nq_seg;
+                                const int lc = ok ? (p.window > 0 ? max(0, base + t - p.window + 1) : 0) : (1 << 30);
+                                const int hc = ok ? base + t + 1 : 0;
+                                if (!(kl >= lc && kl < hc)) sv[u][j] = -INFINITY;
+                                if (!(kh >= lc && kh < hc)) sv[u][2 + j] = -INFINITY;
+                            }
+                        } else {
+                            if (!ok_lo[u]) sv[u][0] = sv[u][1] = -INFINITY;
+                            if (!ok_hi[u]) sv[u][2] = sv[u][3] = -INFINITY;
+                        }
                     }
                 }
                 float mx0 = fmaxf(sv[0][0], sv[0][2]), mx1 = fmaxf(sv[0][1], sv[0][3]);
@@ -927,12 +1040,16 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
                 const float mn0 = fmaxf(st.m[n][0], mx0), mn1 = fmaxf(st.m[n][1], mx1);
-                const float a0 = fast_exp2(st.m[n][0] - mn0), a1 = fast_exp2(st.m[n][1] - mn1);
+                // several tokens: a column may have seen no key yet (m = -inf); subtract 0 then
+                // (every term is 0) instead of forming -inf - -inf
+                const float mr0 = (MT && mn0 == -INFINITY) ? 0.f : mn0;
+                const float mr1 = (MT && mn1 == -INFINITY) ? 0.f : mn1;
+                const float a0 = fast_exp2(st.m[n][0] - mr0), a1 = fast_exp2(st.m[n][1] - mr1);
                 float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
                 for (int u = 0; u < UT; ++u) {
-                    const float p0 = fast_exp2(sv[u][0] - mn0), p1 = fast_exp2(sv[u][1] - mn1);
-                    const float p2 = fast_exp2(sv[u][2] - mn0), p3 = fast_exp2(sv[u][3] - mn1);
+                    const float p0 = fast_exp2(sv[u][0] - mr0), p1 = fast_exp2(sv[u][1] - mr1);
+                    const float p2 = fast_exp2(sv[u][2] - mr0), p3 = fast_exp2(sv[u][3] - mr1);
                     ls0 += p0 + p2;
                     ls1 += p1 + p3;
                     if constexpr (KV8) {  // probabilities times the tokens' V scales, fp16
@@ -1024,6 +1141,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         head_seg = sb * Hkv + sgk;
                         head_s0 = seg_first_unit;
                         head_s1 = seg_end_unit;
+                    } else if constexpr (MT) {
+                        state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, lane);
                     } else {
                         state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD,
                                         p.G, lane);
@@ -1039,6 +1158,22 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     const int cell = (L - 1) % p.window;
                     app_tile = cell / kPage;
                     app_row = cell % kPage;
+                } else if constexpr (MT) {
+                    nq_seg = s_n[sb];
+                    base = L - nq_seg;
+                    lo = p.window > 0 ? max(0, base - p.window + 1) : 0;
+                    ft = lo / kPage;
+                    lo_max = p.window > 0 ? max(0, L - p.window) : 0;  // the last row's window start
+                    hi_min = base + 1;                                  // the first row's end
+                    // the new tokens' k/v rows arrived with this tile: into registers now, since
+                    // the slot may take the next segment's rows before this one's last tile
+                    const uint8_t *nrow = wq + stg * kQBytes + GP * kD * 2;
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2)
+                        if (i2 < nq_seg) {
+                            knew2[i2] = reinterpret_cast<const uint32_t *>(nrow + i2 * kD * 2)[lane];
+                            vnew2[i2] = reinterpret_cast<const uint32_t *>(nrow + (2 + i2) * kD * 2)[lane];
+                        }
                 } else {
                     lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
                     ft = lo / kPage;
@@ -1047,16 +1182,17 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 }
                 // Q fragments (B operand): q[head = lane/4][d = 16ks + 2(lane%4) (+8)]
                 const uint8_t *qs = wq + stg * kQBytes;
-                if (do_append) {  // the new token's k/v rows arrived with this tile
+                if (!MT && do_append) {  // the new token's k/v rows arrived with this tile
                     knew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2)[lane];
                     vnew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2 + kD * 2)[lane];
                 }
+                const int qrows = MT ? p.T * p.G : p.G;  // query rows (columns) of the group
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     const int hq = n * 8 + (lane >> 2);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        if (hq < p.G) {
+                        if (hq < qrows) {
                             const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + hq * kD * 2);
                             if constexpr (KV8) {
                                 // fp16 operands; k-step ks takes d = 16t + 4ks .. +3, the bytes
@@ -1074,7 +1210,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int hs = n * 8 + (lane & 3) * 2 + j;
-                        sig[n][j] = hs < p.G ? s_sink[sgk * p.G + hs] : -INFINITY;
+                        sig[n][j] = hs < qrows ? s_sink[sgk * p.G + (MT ? hs % p.G : hs)] : -INFINITY;
                     }
                 }
                 if constexpr (ROPE) {
@@ -1127,12 +1263,16 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     }
                     // both tiles whole and neither the append tile: the fast pass
                     auto whole = [&](int t) {
+                        if constexpr (MT) {  // before every new token and inside every row's window
+                            const int f = (ft + t) * kPage;
+                            return f >= lo_max && f + kPage <= base;
+                        }
                         if (do_append && t == app_tile) return false;
                         if (RING) return t * kPage + kPage <= nvalid;
                         const int f = (ft + t) * kPage;
                         return f >= lo && f + kPage <= L;
                     };
-                    if ((KV8 ? DA_FAST_PASS_FP8 : DA_FAST_PASS_BF16) && whole(tt) && whole(tt + 1))
+                    if ((MT || (KV8 ? DA_FAST_PASS_FP8 : DA_FAST_PASS_BF16)) && whole(tt) && whole(tt + 1))
                         tiles_step(std::integral_constant<int, 2>{}, std::true_type{}, stg, stg1);
                     else
                         tiles_step(std::integral_constant<int, 2>{}, std::false_type{}, stg, stg1);
@@ -1143,7 +1283,15 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     continue;
                 }
             }
-            tiles_step(std::integral_constant<int, 1>{}, std::false_type{}, stg, stg);
+            if constexpr (MT) {  // several tokens: the masks only on the tiles at the rows' edges
+                const int f = (ft + tt) * kPage;
+                if (f >= lo_max && f + kPage <= base)
+                    tiles_step(std::integral_constant<int, 1>{}, std::true_type{}, stg, stg);
+                else
+                    tiles_step(std::integral_constant<int, 1>{}, std::false_type{}, stg, stg);
+            } else {
+                tiles_step(std::integral_constant<int, 1>{}, std::false_type{}, stg, stg);
+            }
             i += 1;
             stg = stg1;
             ph = ph1;
@@ -1164,6 +1312,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
             tail_seg = sb * Hkv + sgk;
             tail_s0 = seg_first_unit;
             tail_s1 = seg_end_unit;
+        } else if constexpr (MT) {
+            state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, lane);
         } else {
             state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD, p.G, lane);
         }
@@ -1215,25 +1365,27 @@ __global__ void __launch_bounds__(kThreads, CPS)
                                          ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
                     M = fmaxf(M, sl->m[n]);
                 }
-                const float sg = (internal && n < p.G) ? s_sink[g * p.G + n] : -INFINITY;
+                const int qrows = MT ? p.T * p.G : p.G;  // valid columns of the group
+                const float sg = (internal && n < qrows) ? s_sink[g * p.G + (MT ? n % p.G : n)] : -INFINITY;
                 const float Mf = internal ? fmaxf(M, sg) : M;
-                float den = internal ? fast_exp2(sg - Mf) : 0.f;
+                float den = (internal && sg != -INFINITY) ? fast_exp2(sg - Mf) : 0.f;
                 float acc[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) acc[j] = 0.f;
                 for (int w = warp; w <= w_end; ++w) {
                     const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
                                          ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
-                    const float wgt = fast_exp2(sl->m[n] - Mf);
+                    const float wgt = sl->m[n] == -INFINITY ? 0.f : fast_exp2(sl->m[n] - Mf);  // no key: weight 0
                     den += sl->l[n] * wgt;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] += sl->acc[n][d0 + j] * wgt;
                 }
                 if (internal) {
-                    if (n < p.G) {
-                        const float inv = 1.f / den;
+                    if (n < qrows) {
+                        const int t = MT ? n / p.G : 0, h = MT ? n - t * p.G : n;
+                        const float inv = (MT && t >= s_n[b]) ? 0.f : 1.f / den;  // no query token: zeros
                         uint4 *dst = reinterpret_cast<uint4 *>(
-                            p.out + (static_cast<size_t>(b) * p.Hq + g * p.G + n) * kD + d0);
+                            p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD + d0);
                         uint4 o0, o1;
                         o0.x = pack_bf16(acc[0] * inv, acc[1] * inv);
                         o0.y = pack_bf16(acc[2] * inv, acc[3] * inv);
@@ -1326,26 +1478,28 @@ __global__ void __launch_bounds__(kThreads, CPS)
             float Mn = M;
 #pragma unroll
             for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mc[j]);
-            const float a = fast_exp2(M - Mn);  // 0 on the first batch (M = -inf)
+            const float a = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // 0 on the first batch (M = -inf)
             den *= a;
 #pragma unroll
             for (int t = 0; t < kPer; ++t) acc[t] *= a;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float w = fast_exp2(mc[j] - Mn);  // 0 for the padding entries
+                const float w = mc[j] == -INFINITY ? 0.f : fast_exp2(mc[j] - Mn);  // 0: padding, or no key
                 den += lc[j] * w;
 #pragma unroll
                 for (int t = 0; t < kPer; ++t) acc[t] += v[j][t] * w;
             }
             M = Mn;
         }
-        const float sg = cn < p.G ? s_sink[g * p.G + cn] : -INFINITY;
+        const int qrows = MT ? p.T * p.G : p.G;
+        const float sg = cn < qrows ? s_sink[g * p.G + (MT ? cn % p.G : cn)] : -INFINITY;
         const float Mf = fmaxf(M, sg);
-        const float a = fast_exp2(M - Mf);
-        den = den * a + fast_exp2(sg - Mf);
-        const float f = a / den;
-        if (cn < p.G) {
-            __nv_bfloat16 *dst = p.out + (static_cast<size_t>(b) * p.Hq + g * p.G + cn) * kD + cd0;
+        const float a = M == -INFINITY ? 0.f : fast_exp2(M - Mf);
+        den = den * a + (sg == -INFINITY ? 0.f : fast_exp2(sg - Mf));
+        const int ct = MT ? cn / p.G : 0, ch = MT ? cn - ct * p.G : cn;
+        const float f = (den > 0.f && !(MT && ct >= s_n[b])) ? a / den : 0.f;  // no query token: zeros
+        if (cn < qrows) {
+            __nv_bfloat16 *dst = p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + ct) * p.Hq + g * p.G + ch) * kD + cd0;
 #pragma unroll
             for (int t = 0; t < kPer; t += 2)
                 *reinterpret_cast<uint32_t *>(dst + t) = pack_bf16(acc[t] * f, acc[t + 1] * f);
@@ -1487,7 +1641,7 @@ struct DeviceState {
     void *ws_multi = nullptr;  // multi-token calls: counters + split partials
     size_t ws_multi_bytes = 0;
     int sm_count = 0;
-    bool attr_set[32] = {};
+    bool attr_set[64] = {};
     bool multi_attr_set[8] = {};
 };
 DeviceState g_dev[kMaxDevices];
@@ -1556,13 +1710,13 @@ int check_shape(const da_shape &s) {
     return DA_OK;
 }
 
-template <int NT, bool RING, bool ROPE, bool KV8 = false, int CPS = 1>
+template <int NT, bool RING, bool ROPE, bool KV8 = false, int CPS = 1, bool MT = false>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
     static_assert(CPS == 1 || (KV8 && NT == 1), "two CTAs per SM: fp8 kernel with 8-head groups only");
-    const size_t smem = SmemLayout<NT, ROPE, KV8, CPS>::bytes;
+    const size_t smem = SmemLayout<NT, ROPE, KV8, CPS, MT>::bytes;
     const size_t smem_max = smem;
-    auto kern = decode_attn_kernel<NT, RING, ROPE, KV8, CPS>;
-    const int idx = (CPS - 1) * 16 + (NT - 1) * 8 + (RING ? 4 : 0) + (ROPE ? 2 : 0) + (KV8 ? 1 : 0);
+    auto kern = decode_attn_kernel<NT, RING, ROPE, KV8, CPS, MT>;
+    const int idx = (MT ? 32 : 0) + (CPS - 1) * 16 + (NT - 1) * 8 + (RING ? 4 : 0) + (ROPE ? 2 : 0) + (KV8 ? 1 : 0);
     if (!g_dev[dev].attr_set[idx]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
@@ -1659,6 +1813,8 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.rope_cos = rope_cos;
     prm.rope_sin = rope_sin;
     prm.max_position = max_position;
+    prm.T = 1;
+    prm.q_lens = nullptr;
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
@@ -1749,6 +1905,7 @@ bool make_new_map(CUtensorMap *map, const void *base, int Hkv, int T, int B) {
 // split. A function of the shape, T, the window or longest sequence and the SM count only
 // (never of the lengths), so the workspace can be sized ahead and the call captured.
 struct MultiPlan {
+    bool dec;          // the decode kernel's several-token form (paged, T <= 2, T G <= 16)
     bool tc;           // the tcgen05 kernel (128 query rows per CTA) or the mma.sync one
     long long groups;  // (sequence, KV head, query-row block) triples, one counter each
     int nw, rows, row_blocks, splits, chunk;
@@ -1760,6 +1917,9 @@ struct MultiPlan {
 // do not fill its pipeline, so ring calls stay on mma.sync).
 #ifndef DA_MULTI_TC_MIN_ROWS
 #define DA_MULTI_TC_MIN_ROWS 64
+#endif
+#ifndef DA_MULTI_DECODE_ROUTE  // 0: every multi-token call on the row-block kernels
+#define DA_MULTI_DECODE_ROUTE 1
 #endif
 #ifndef DA_MULTI_TC_CTAS_PER_SM  // tcgen05 calls: key splits aim at this many CTAs per SM
 #define DA_MULTI_TC_CTAS_PER_SM 2
@@ -1779,6 +1939,22 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     MultiPlan m;
     const int G = s.num_q_heads / s.num_kv_heads;
     const long long TG = static_cast<long long>(T) * G;
+    // One or two query tokens of at most 16 rows per KV head on a paged cache take the decode
+    // kernel's device-balanced split (measured faster than the row-block kernel; the ring keeps
+    // the row-block kernel, whose separate append leaves the cells the earlier tokens read).
+    m.dec = !ring && T <= 2 && TG <= 16 && DA_MULTI_DECODE_ROUTE;
+    if (m.dec) {  // counters in the fixed region, then one pair of partial slots per CTA
+        m.tc = false;
+        m.nw = kWarps;
+        m.rows = TG <= 8 ? 8 : 16;
+        m.row_blocks = 1;
+        m.splits = 1;
+        m.chunk = 0;
+        m.groups = static_cast<long long>(s.batch) * s.num_kv_heads;
+        m.counter_bytes = static_cast<size_t>(kMMaxGroups) * sizeof(int);
+        m.part_bytes = static_cast<size_t>(sms) * 2 * slot_floats(static_cast<int>(TG)) * sizeof(float);
+        return m;
+    }
     m.tc = !ring && TG >= DA_MULTI_TC_MIN_ROWS;
     if (m.tc) {
         m.nw = kTcWarps;
@@ -1870,6 +2046,42 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
             rc = reserve_multi_locked(dev, need);
             if (rc != DA_OK) return rc;
         }
+    }
+    if (m.dec) {  // the decode kernel's several-token form, on this workspace
+        Params dp;
+        dp.q = static_cast<const __nv_bfloat16 *>(q);
+        dp.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+        dp.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+        dp.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+        dp.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
+        dp.block_table = block_table;
+        dp.seq_lens = seq_lens;
+        dp.sinks = sinks;
+        dp.out = static_cast<__nv_bfloat16 *>(out);
+        dp.counters = static_cast<int *>(g_dev[dev].ws_multi);
+        dp.part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws_multi) + m.counter_bytes);
+        dp.B = s.batch;
+        dp.Hq = s.num_q_heads;
+        dp.Hkv = s.num_kv_heads;
+        dp.G = s.num_q_heads / s.num_kv_heads;
+        dp.window = window;
+        dp.max_pages = max_pages;
+        dp.num_pages = num_pages;
+        dp.max_seq_len = max_seq_len;
+        dp.scale_log2 = scale * kLog2e;
+        dp.rope_cos = nullptr;
+        dp.rope_sin = nullptr;
+        dp.max_position = 0;
+        dp.T = T;
+        dp.q_lens = q_lens;
+        CUtensorMap mk, mv;
+        const uint64_t slices = static_cast<uint64_t>(num_pages) * s.num_kv_heads;
+        if (!make_kv_map(&mk, k_cache, kPage, slices) || !make_kv_map(&mv, v_cache, kPage, slices)) {
+            snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
+            return DA_ERR_CUDA;
+        }
+        return T * dp.G <= 8 ? launch_attn<1, false, false, false, 1, true>(mk, mv, dp, dev, stream)
+                             : launch_attn<2, false, false, false, 1, true>(mk, mv, dp, dev, stream);
     }
     MultiParams prm;
     prm.q = static_cast<const __nv_bfloat16 *>(q);
@@ -2026,6 +2238,8 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.rope_cos = nullptr;
     prm.rope_sin = nullptr;
     prm.max_position = 0;
+    prm.T = 1;
+    prm.q_lens = nullptr;
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call

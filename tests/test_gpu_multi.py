@@ -90,6 +90,17 @@ def test_ring_multi_matches_oracle(W, T):
     run_ring(m, W)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (32, 8)])
+def test_segments_spanning_whole_pipelines(Hq, Hkv):
+    """Sequences whose key tiles fill a warp's stage ring exactly (4, 5, 8, 10, 12, 15, 16,
+    20 tiles): the next sequence's first tile then lands in the stage that held this one's
+    new-token rows before this one's last tile is processed."""
+    lens = [64, 80, 128, 160, 192, 240, 256, 320, 63, 65, 2, 17]
+    m = Multi(865 + Hq, Hq, Hkv, lens, [2] * len(lens), 2)
+    run_paged(m, 0)
+    run_paged(m, 48)
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(64, 8), (16, 1)])
 def test_one_token_through_the_multi_calls(Hq, Hkv):
     """T = 1 (one warp per CTA at G = 8, two at G = 16): the multi-token calls reduce to
@@ -155,7 +166,7 @@ def test_bad_counts_are_reported_not_faulted():
     assert torch.all(out[0].float() == 0)                          # treated as inactive
 
 
-@pytest.mark.parametrize("T", [4, 8])
+@pytest.mark.parametrize("T", [2, 4, 8])
 def test_full_size_speculative_step(T):
     """The batch-64 workload with T draft tokens per sequence (lengths from the benchmark
     recipe, random pools): a sample of sequences against the oracle, the append
