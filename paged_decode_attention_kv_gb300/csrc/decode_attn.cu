@@ -1934,6 +1934,11 @@ struct MultiPlan {
 #ifndef DA_MULTI_TC_MAX_CHUNK  // the same cap for tcgen05 CTAs, whose set-up is heavier
 #define DA_MULTI_TC_MAX_CHUNK 1024
 #endif
+// Key tiles per split at least, where the SM target alone would cut finer: a split of fewer
+// keys saves less than its partial and the combine cost (a 128-token window is never split)
+#ifndef DA_MULTI_MIN_CHUNK
+#define DA_MULTI_MIN_CHUNK 16
+#endif
 
 MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_seq_len, int sms) {
     MultiPlan m;
@@ -1969,6 +1974,7 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     const long long groups = static_cast<long long>(s.batch) * s.num_kv_heads * m.row_blocks;
     const long long target = static_cast<long long>(m.tc ? DA_MULTI_TC_CTAS_PER_SM : DA_MULTI_CTAS_PER_SM) * sms;
     long long sp = std::max<long long>(1, (target + groups - 1) / std::max<long long>(1, groups));
+    sp = std::min(sp, std::max<long long>(1, max_tiles / DA_MULTI_MIN_CHUNK));
     sp = std::max(sp, (max_tiles + kMMaxChunk - 1) / kMMaxChunk);  // a CTA's pages fit its smem
     const long long cap = m.tc ? DA_MULTI_TC_MAX_CHUNK : DA_MULTI_MAX_CHUNK;
     sp = std::max(sp, (max_tiles + cap - 1) / cap);

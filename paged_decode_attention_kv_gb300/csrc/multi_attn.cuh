@@ -91,48 +91,108 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // The last split of a row block folds every split's partial (m, l, acc per row) into the
-// output, with the sink: one warp per query row, lanes striding over the splits for the
-// maximum and the denominator and holding two of the 64 outputs each.
+// output, with the sink. A warp takes kCombRows of the block's rows at a time, so that their
+// loads are in flight together (rows one after another left a chain of dependent L2 round
+// trips in the CTA that finishes last). First pass: lanes stride over the splits and merge
+// (m, l) online, then across the warp. Second pass: lane = (split phase s = lane / 8, output
+// octet q = lane % 8) sums the weighted acc[8 q .. 8 q + 7] of splits s, s + 4, ..., and the four
+// phases are added across the warp.
+constexpr int kCombRows = 4;
 __device__ __noinline__ void multi_combine_rows(const MultiParams &p, const float *all, int RB, int r0, int r_end,
                                                 int n, int b, int g, int nsplit, int warp, int nw, int lane) {
-    for (int rl = warp; rl < RB; rl += nw) {
-        const int r = r0 + rl;
-        if (r >= r_end) break;
-        const int t = r / p.G;
-        const int hl = r - t * p.G;
-        float o0 = 0.f, o1 = 0.f;
-        if (t < n) {
-            const int h = g * p.G + hl;
-            const float sg = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
-            auto slot = [&](int sp) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
-            float M = sg;
-            for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, __ldcg(slot(sp)));
+    auto slot = [&](int sp, int rl) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
+    const int phase = lane >> 3, q = lane & 7;
+    for (int rl0 = warp; rl0 < RB; rl0 += kCombRows * nw) {
+        int rl[kCombRows];
+        bool row[kCombRows];   // an output row of this block
+        bool live[kCombRows];  // a query row (t < n); the other output rows are zeros
+        float sg[kCombRows], M[kCombRows], den[kCombRows];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            if (M != -INFINITY) {
-                float den = 0.f;
-                for (int sp = lane; sp < nsplit; sp += 32) {
-                    const float m = __ldcg(slot(sp));
-                    if (m != -INFINITY) den += __ldcg(slot(sp) + 1) * exp2f(m - M);
-                }
+        for (int i = 0; i < kCombRows; ++i) {
+            rl[i] = rl0 + i * nw;
+            const int r = r0 + rl[i];
+            const int t = r / p.G;
+            row[i] = rl[i] < RB && r < r_end;
+            live[i] = row[i] && t < n;
+            sg[i] = live[i] && p.sinks != nullptr ? __ldg(p.sinks + g * p.G + (r - t * p.G)) * kLog2e : -INFINITY;
+            M[i] = -INFINITY;
+            den[i] = 0.f;
+        }
+        for (int sp = lane; sp < nsplit; sp += 32) {
+            float2 ml[kCombRows];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-                if (sg != -INFINITY) den += exp2f(sg - M);
-#pragma unroll 8
-                for (int sp = 0; sp < nsplit; ++sp) {
-                    const float m = __ldcg(slot(sp));
-                    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-                    const float2 a2 = __ldcg(reinterpret_cast<const float2 *>(slot(sp) + kMAccOff) + lane);
-                    o0 += a2.x * w;
-                    o1 += a2.y * w;
-                }
-                const float inv = den > 0.f ? 1.f / den : 0.f;
-                o0 *= inv;
-                o1 *= inv;
+            for (int i = 0; i < kCombRows; ++i)
+                ml[i] = live[i] ? __ldcg(reinterpret_cast<const float2 *>(slot(sp, rl[i]))) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int i = 0; i < kCombRows; ++i) {
+                if (ml[i].x == -INFINITY) continue;  // a split that saw no key of the row
+                const float Mn = fmaxf(M[i], ml[i].x);
+                den[i] = den[i] * exp2f(M[i] - Mn) + ml[i].y * exp2f(ml[i].x - Mn);
+                M[i] = Mn;
             }
         }
-        __nv_bfloat16 *o = p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + g * p.G + hl) * kD;
-        *reinterpret_cast<__nv_bfloat162 *>(o + 2 * lane) = __floats2bfloat162_rn(o0, o1);
+        float Mf[kCombRows], inv[kCombRows];
+#pragma unroll
+        for (int i = 0; i < kCombRows; ++i) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float Mo = __shfl_xor_sync(0xffffffffu, M[i], off);
+                const float Do = __shfl_xor_sync(0xffffffffu, den[i], off);
+                const float Mn = fmaxf(M[i], Mo);
+                den[i] = Mn == -INFINITY ? 0.f : den[i] * exp2f(M[i] - Mn) + Do * exp2f(Mo - Mn);
+                M[i] = Mn;
+            }
+            // the sink joins the denominator; no key and no sink: a zero row
+            Mf[i] = fmaxf(M[i], sg[i]);
+            inv[i] = 0.f;
+            if (Mf[i] != -INFINITY) {
+                const float d = den[i] * exp2f(M[i] - Mf[i]) + (sg[i] == -INFINITY ? 0.f : exp2f(sg[i] - Mf[i]));
+                inv[i] = d > 0.f ? 1.f / d : 0.f;
+            }
+        }
+        float o[kCombRows][8];
+#pragma unroll
+        for (int i = 0; i < kCombRows; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[i][k] = 0.f;
+        for (int sp = phase; sp < nsplit; sp += 4) {
+#pragma unroll
+            for (int i = 0; i < kCombRows; ++i) {
+                if (Mf[i] == -INFINITY) continue;  // the same on every lane: M is an exact maximum
+                const float *s = slot(sp, rl[i]);
+                const float m = __ldcg(s);
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(s + kMAccOff) + 2 * q);
+                const float4 c = __ldcg(reinterpret_cast<const float4 *>(s + kMAccOff) + 2 * q + 1);
+                const float w = m == -INFINITY ? 0.f : exp2f(m - Mf[i]);
+                o[i][0] += a.x * w;
+                o[i][1] += a.y * w;
+                o[i][2] += a.z * w;
+                o[i][3] += a.w * w;
+                o[i][4] += c.x * w;
+                o[i][5] += c.y * w;
+                o[i][6] += c.z * w;
+                o[i][7] += c.w * w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCombRows; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                o[i][k] += __shfl_xor_sync(0xffffffffu, o[i][k], 8);
+                o[i][k] += __shfl_xor_sync(0xffffffffu, o[i][k], 16);
+            }
+        if (phase == 0) {
+#pragma unroll
+            for (int i = 0; i < kCombRows; ++i) {
+                if (!row[i]) continue;
+                const int r = r0 + rl[i], t = r / p.G, hl = r - t * p.G;
+                const float f = inv[i];
+                const uint4 v = make_uint4(pack_bf16(o[i][0] * f, o[i][1] * f), pack_bf16(o[i][2] * f, o[i][3] * f),
+                                           pack_bf16(o[i][4] * f, o[i][5] * f), pack_bf16(o[i][6] * f, o[i][7] * f));
+                *reinterpret_cast<uint4 *>(p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + g * p.G + hl) * kD +
+                                           8 * q) = v;
+            }
+        }
     }
 }
 

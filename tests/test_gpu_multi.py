@@ -81,9 +81,11 @@ def test_paged_multi_matches_oracle(Hq, Hkv, T, window):
     run_paged(m, window, seed=T + 1)
 
 
-@pytest.mark.parametrize("W", [16, 128])
+@pytest.mark.parametrize("W", [16, 128, 1024])
 @pytest.mark.parametrize("T", [3, 16, 40])
 def test_ring_multi_matches_oracle(W, T):
+    """Windows of one and eight tiles run unsplit; a 1024-token window splits its keys over
+    several CTAs at 3 and 16 tokens, whose partials the last one combines."""
     lens = [1, 15, 16, 17, W - 1, W, W + 1, 3 * W + 5, 60, 0]
     n = counts(T, lens, W + T)
     m = Multi(850 + W + T, 64, 8, lens, n, T)
