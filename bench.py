@@ -316,9 +316,9 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None, out=
 
 
 def decode_route(q_tokens, cfg):
-    """Whether the library runs a paged multi-token call in the decode kernel (one or two
-    query tokens, at most 16 query rows per KV head), append fused."""
-    return 1 < q_tokens <= 2 and q_tokens * cfg["Hq"] // cfg["Hkv"] <= 16
+    """Whether the library runs a paged multi-token call in the decode kernel (up to four
+    query tokens, at most 32 query rows per KV head), append fused."""
+    return 1 < q_tokens <= 4 and q_tokens * cfg["Hq"] // cfg["Hkv"] <= 32
 
 
 def launches_per_step(q_tokens, cfg):

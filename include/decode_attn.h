@@ -202,8 +202,8 @@ DA_API int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_
  *   caches, block_table, sinks, page_size, max_pages_per_seq, num_pages, max_seq_len:
  *                 as in decode_attn_paged / decode_attn_ring (the ring's W >= 16).
  * Two kernels on `stream`: the attention, then the append (the ring's early query tokens
- * still read the cells the later new tokens overwrite); paged calls of one or two tokens
- * with T * G <= 16 run one kernel with the append fused (a paged cell of a new token is
+ * still read the cells the later new tokens overwrite); paged calls of up to four tokens
+ * with T * G <= 32 run one kernel with the append fused (a paged cell of a new token is
  * read only through the tile its own kernel pass patches). Split partials and counters live
  * in a second library workspace (decode_attn_multi_workspace_bytes / _reserve); it is
  * allocated on first use outside graph capture, else DA_ERR_WORKSPACE. T <= 4096.

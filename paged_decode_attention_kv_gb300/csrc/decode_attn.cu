@@ -120,6 +120,7 @@ constexpr int kBlk8Bytes = kBlk8S + 8 * kPage;  // 2176
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxSegments = 65536;         // B * Hkv
 constexpr int kMaxQHeads = 1024;
+constexpr int kMaxNewMT = 4;   // query tokens per sequence of the MT kernel at most
 constexpr int kWinfo = 12;     // ints of per-warp bookkeeping in shared memory
 constexpr int kCounterBytes = kMaxSegments * 4;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s of SM clock per tile wait
@@ -149,6 +150,10 @@ struct Params {
     // [B][T][Hkv][D]; the n = q_lens[b] (T if null) newest positions are new tokens
     int T;
     const int *q_lens;
+    // query-row groups of the MT kernel: CTA c takes rows [16 (c % ngrp), + 16) of every
+    // (sequence, KV head) over the units of CTA c / ngrp of a grid of gridDim.x / ngrp (the
+    // CTAs of one unit range read the same tiles, all but the first from L2); 1 otherwise
+    int ngrp;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -430,11 +435,11 @@ __device__ __forceinline__ void state_write_out(SegState<NT> &s, const float (&s
     }
 }
 
-// The same for several query tokens: column r = t G + h of the group goes to
-// out[b][t][g G + h]; rows t >= n (no query token) are written as zeros.
+// The same for several query tokens: column c holds query row r = r0 + c = t G + h of the
+// group, which goes to out[b][t][g G + h]; rows t >= n (no query token) are written as zeros.
 template <int NT>
 __device__ __forceinline__ void state_write_out_mt(SegState<NT> &s, const float (&sig)[NT][2], __nv_bfloat16 *out,
-                                                   int b, int g, int T, int G, int Hq, int nq, int lane) {
+                                                   int b, int g, int T, int G, int Hq, int nq, int r0, int lane) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
         float f[2];
@@ -449,7 +454,7 @@ __device__ __forceinline__ void state_write_out_mt(SegState<NT> &s, const float 
             const float den = s.l[n][j] * a + fast_exp2(sig[n][j] - M);
             f[j] = a / den;
         }
-        const int r = n * 8 + (lane >> 2), t = r / G, h = r - t * G;
+        const int r = r0 + n * 8 + (lane >> 2), t = r / G, h = r - t * G;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
             uint32_t lo = movmatrix_t(pack_bf16(s.acc[n][mt][0] * f[0], s.acc[n][mt][1] * f[1]));
@@ -515,8 +520,9 @@ struct SmemLayout {
     // per stage: the group's q rows, the new token's k and v rows, the rotary cos and sin
     // rows, the fp8 tile's K and V scale rows
     static constexpr int kRopeOff = GP * kD * 2 + 2 * kD * 2;
-    // several query tokens: the rows of all T (<= 2) tokens, then their new k rows and v rows
-    static constexpr int kQBytes = MT ? GP * kD * 2 + 2 * 2 * kD * 2 : kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
+    // several query tokens: the GP query rows of this CTA's row group (the new tokens' k/v
+    // rows go to registers straight from global memory)
+    static constexpr int kQBytes = MT ? GP * kD * 2 : kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
     static constexpr int kWarpTileBytes = kStages * kStageBytes;  // the tiles of one warp
     static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8 + (MT ? kMaxBatch : 0);
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
@@ -535,10 +541,11 @@ struct SmemLayout {
 };
 
 // ------------------------------------------------------------------ the kernel
-// MT: several query tokens per sequence (paged, bf16, T <= 2, T * G <= 16): the query rows
-// of a KV head are (token t, head h) pairs r = t G + h, one column of the products each; row
-// t sees the positions lo_t .. base + t (base = L - n, lo_t its window start), the n new
-// tokens are appended in the same pass, rows t >= n are zero.
+// MT: several query tokens per sequence (paged, bf16, T <= kMaxNewMT): the query rows of a
+// KV head are (token t, head h) pairs r = t G + h, one column of the products each; row t
+// sees the positions lo_t .. base + t (base = L - n, lo_t its window start), the n new tokens
+// are appended in the same pass, rows t >= n are zero. With more than 16 rows per KV head the
+// rows are cut into groups of 16 (p.ngrp), one per CTA of a pair that covers the same units.
 template <int NT, bool RING, bool ROPE, bool KV8, int CPS, bool MT = false>
 __global__ void __launch_bounds__(kThreads, CPS)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -561,6 +568,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    // the unit split runs over ncta CTAs; this CTA is number cta of row group rgrp, whose
+    // columns are the query rows r0g .. r0g + GP - 1 of each (sequence, KV head)
+    const int ngrp = MT ? p.ngrp : 1;
+    const int rgrp = MT ? static_cast<int>(blockIdx.x) % ngrp : 0;
+    const int cta = MT ? static_cast<int>(blockIdx.x) / ngrp : static_cast<int>(blockIdx.x);
+    const int ncta = MT ? static_cast<int>(gridDim.x) / ngrp : static_cast<int>(gridDim.x);
+    const int r0g = rgrp * GP;
     uint8_t *qarea = smem + Lay::qarea;  // [kWarps][kStages] q / k_new / v_new / cos / sin slots
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bars);
     int4 *meta = reinterpret_cast<int4 *>(smem + Lay::meta);
@@ -656,10 +670,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
 
     // ---- 3. workers and their unit ranges
     const long long nwork =
-        min(static_cast<long long>(gridDim.x) * kWarps,
+        min(static_cast<long long>(ncta) * kWarps,
             static_cast<long long>((U + kMinTilesPerWorker - 1) / kMinTilesPerWorker));
-    if (static_cast<long long>(blockIdx.x) * kWarps >= nwork) return;  // whole CTA idle
-    const long long wid = static_cast<long long>(blockIdx.x) * kWarps + warp;
+    if (static_cast<long long>(cta) * kWarps >= nwork) return;  // whole CTA idle
+    const long long wid = static_cast<long long>(cta) * kWarps + warp;
     const bool active = wid < nwork;
     const int ua = active ? wstart(wid, U, nwork) : 0;
     const int ue = active ? wstart(wid + 1, U, nwork) : 0;
@@ -754,9 +768,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = !MT && newseg && p.k_new != nullptr;
                 const bool rope = ROPE && newseg;
-                const int qrows = MT ? p.T * p.G : p.G;  // query rows of the group
+                // query rows this CTA stages: its row group's share of the T G (MT), or G
+                const int qrows = MT ? min(GP, max(0, p.T * p.G - r0g)) : p.G;
                 mbar_expect_tx(bar, Lay::kStageBytes + (newseg ? qrows * kD * 2 : 0) + (rows ? 4 * kD : 0) +
-                                        (rope ? 4 * kD : 0) + ((MT && newseg) ? p.T * 4 * kD : 0));
+                                        (rope ? 4 * kD : 0));
                 if constexpr (KV8) {  // the whole block in one copy (a bad page reads block 0)
                     const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
                                             : static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg;
@@ -770,15 +785,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
                 }
                 if (newseg) {
-                    if constexpr (MT) {  // rows t G .. t G + G - 1 of the slot: token t's heads of group tg;
-                                         // then the new tokens' k rows and v rows (2 each at most)
-                        for (int t = 0; t < p.T; ++t) {
-                            bulk_load(q_tile(stg) + t * p.G * kD * 2,
-                                      p.q + ((static_cast<size_t>(tb) * p.T + t) * p.Hq + static_cast<size_t>(tg) * p.G) * kD,
-                                      p.G * kD * 2, bar);
-                            const size_t off = ((static_cast<size_t>(tb) * p.T + t) * Hkv + tg) * kD;
-                            bulk_load(q_tile(stg) + GP * kD * 2 + t * kD * 2, p.k_new + off, kD * 2, bar);
-                            bulk_load(q_tile(stg) + GP * kD * 2 + (2 + t) * kD * 2, p.v_new + off, kD * 2, bar);
+                    if constexpr (MT) {  // rows r0g .. r0g + qrows - 1: for each token t the heads of
+                                         // group tg whose row t G + h falls in that range
+                        for (int t = r0g / p.G; t < p.T && t * p.G < r0g + qrows; ++t) {
+                            const int h0 = max(0, r0g - t * p.G), h1 = min(p.G, r0g + qrows - t * p.G);
+                            bulk_load(q_tile(stg) + (t * p.G + h0 - r0g) * kD * 2,
+                                      p.q + ((static_cast<size_t>(tb) * p.T + t) * p.Hq + static_cast<size_t>(tg) * p.G + h0) * kD,
+                                      (h1 - h0) * kD * 2, bar);
                         }
                     } else {
                         bulk_load(q_tile(stg),
@@ -818,7 +831,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
         // tightest bounds over its rows (tiles inside [lo_max, hi_min) need no mask), the new
         // tokens' k/v (bf16 pairs of this lane), and this lane's columns' ranges [lo_c, hi_c)
         int nq_seg = 1, base = 0, lo_max = 0, hi_min = 0;
-        uint32_t knew2[2] = {0u, 0u}, vnew2[2] = {0u, 0u};
+        uint32_t knewm[kMaxNewMT], vnewm[kMaxNewMT];
+#pragma unroll
+        for (int i2 = 0; i2 < kMaxNewMT; ++i2) knewm[i2] = vnewm[i2] = 0u;
         uint32_t knew = 0, vnew = 0;           // new token's k/v (bf16 pair, or 2 e4m3 codes)
         float knew_scale = 1.f, vnew_scale = 1.f;  // fp8: their scales
         const bool do_append = p.k_new != nullptr;
@@ -849,18 +864,19 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const int stg = stgs[u], tt = tts[u], tp = tps[u];
                 uint8_t *gK = wbase + k_off(stg);
                 uint8_t *gV = wbase + v_off(stg);
-                if constexpr (MT) {  // fused append of the new tokens this tile holds
+                if constexpr (MT) {  // fused append of the new tokens this tile holds (into the
+                                     // cache by row group 0 only; every group patches its copy)
                     bool any = false;
 #pragma unroll
-                    for (int i2 = 0; i2 < 2; ++i2) {
+                    for (int i2 = 0; i2 < kMaxNewMT; ++i2) {
                         const int pos = base + i2;
                         if (i2 < nq_seg && pos / kPage - ft == tt) {
                             const int row = pos % kPage;
                             const uint32_t off = row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) + (lane & 3) * 4;
-                            const uint32_t kn = knew2[i2], vn = vnew2[i2];
+                            const uint32_t kn = knewm[i2], vn = vnewm[i2];
                             *reinterpret_cast<uint32_t *>(gK + off) = kn;
                             *reinterpret_cast<uint32_t *>(gV + off) = vn;
-                            if (tp >= 0) {
+                            if (tp >= 0 && rgrp == 0) {
                                 const size_t c = (static_cast<size_t>(tp) * Hkv + sgk) * kPage + row;
                                 reinterpret_cast<uint32_t *>(p.k_cache + c * kD)[lane] = kn;
                                 reinterpret_cast<uint32_t *>(p.v_cache + c * kD)[lane] = vn;
@@ -1014,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                             const int kl = t0[u] + (lane >> 2), kh = kl + 8;
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
-                                const int r = n * 8 + (lane & 3) * 2 + j, t = r / p.G;
+                                const int r = r0g + n * 8 + (lane & 3) * 2 + j, t = r / p.G;
                                 const bool ok = r < p.T * p.G && t < nq_seg;
                                 const int lc = ok ? (p.window > 0 ? max(0, base + t - p.window + 1) : 0) : (1 << 30);
                                 const int hc = ok ? base + t + 1 : 0;
@@ -1142,7 +1158,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         head_s0 = seg_first_unit;
                         head_s1 = seg_end_unit;
                     } else if constexpr (MT) {
-                        state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, lane);
+                        state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, r0g, lane);
                     } else {
                         state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD,
                                         p.G, lane);
@@ -1165,14 +1181,14 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     ft = lo / kPage;
                     lo_max = p.window > 0 ? max(0, L - p.window) : 0;  // the last row's window start
                     hi_min = base + 1;                                  // the first row's end
-                    // the new tokens' k/v rows arrived with this tile: into registers now, since
-                    // the slot may take the next segment's rows before this one's last tile
-                    const uint8_t *nrow = wq + stg * kQBytes + GP * kD * 2;
+                    // the new tokens' k/v rows (this lane's bf16 pair of each): loaded now, used
+                    // at the segment's last tiles, so the load latency hides behind the loop
 #pragma unroll
-                    for (int i2 = 0; i2 < 2; ++i2)
+                    for (int i2 = 0; i2 < kMaxNewMT; ++i2)
                         if (i2 < nq_seg) {
-                            knew2[i2] = reinterpret_cast<const uint32_t *>(nrow + i2 * kD * 2)[lane];
-                            vnew2[i2] = reinterpret_cast<const uint32_t *>(nrow + (2 + i2) * kD * 2)[lane];
+                            const size_t off = ((static_cast<size_t>(sb) * p.T + i2) * Hkv + sgk) * kD;
+                            knewm[i2] = __ldg(reinterpret_cast<const uint32_t *>(p.k_new + off) + lane);
+                            vnewm[i2] = __ldg(reinterpret_cast<const uint32_t *>(p.v_new + off) + lane);
                         }
                 } else {
                     lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
@@ -1189,10 +1205,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const int qrows = MT ? p.T * p.G : p.G;  // query rows (columns) of the group
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
-                    const int hq = n * 8 + (lane >> 2);
+                    const int hq = n * 8 + (lane >> 2);  // slot row; query row r0g + hq
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        if (hq < qrows) {
+                        if (r0g + hq < qrows) {
                             const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + hq * kD * 2);
                             if constexpr (KV8) {
                                 // fp16 operands; k-step ks takes d = 16t + 4ks .. +3, the bytes
@@ -1209,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     }
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const int hs = n * 8 + (lane & 3) * 2 + j;
+                        const int hs = r0g + n * 8 + (lane & 3) * 2 + j;
                         sig[n][j] = hs < qrows ? s_sink[sgk * p.G + (MT ? hs % p.G : hs)] : -INFINITY;
                     }
                 }
@@ -1313,7 +1329,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
             tail_s0 = seg_first_unit;
             tail_s1 = seg_end_unit;
         } else if constexpr (MT) {
-            state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, lane);
+            state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, r0g, lane);
         } else {
             state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD, p.G, lane);
         }
@@ -1331,13 +1347,19 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 4. merge segments shared between warps of this CTA (all threads take part)
-    const long long cta_w0 = static_cast<long long>(blockIdx.x) * kWarps;
+    const long long cta_w0 = static_cast<long long>(cta) * kWarps;
     const long long cta_w1 = min(cta_w0 + kWarps, nwork);
     const int R0 = wstart(cta_w0, U, nwork), R1 = wstart(cta_w1, U, nwork);
     const int nw_cta = static_cast<int>(cta_w1 - cta_w0);
     // Segments shared by several warps: the first warp of this CTA touching one merges it
     // (warps merge their segments concurrently). A segment that also crosses into another
     // CTA becomes this CTA's fp32 partial; slot 0 if it holds the CTA's first unit, else 1.
+    // fp32 partial slot k of the CTA with effective index c in this row group; the row
+    // groups count their tickets apart
+    auto part_slot = [&](int c, int k) {
+        return p.part + ((static_cast<size_t>(c) * ngrp + rgrp) * 2 + k) * kSlotFloats;
+    };
+    int *const counters = p.counters + static_cast<size_t>(rgrp) * B * Hkv;
     bool wrote_partial = false;
     if (warp < nw_cta) {
         const int *wi = s_winfo + warp * kWinfo;
@@ -1365,8 +1387,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
                                          ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
                     M = fmaxf(M, sl->m[n]);
                 }
-                const int qrows = MT ? p.T * p.G : p.G;  // valid columns of the group
-                const float sg = (internal && n < qrows) ? s_sink[g * p.G + (MT ? n % p.G : n)] : -INFINITY;
+                const int qrows = MT ? p.T * p.G : p.G;  // valid query rows of the group
+                const int rn = r0g + n;                  // column n's query row
+                const float sg = (internal && rn < qrows) ? s_sink[g * p.G + (MT ? rn % p.G : rn)] : -INFINITY;
                 const float Mf = internal ? fmaxf(M, sg) : M;
                 float den = (internal && sg != -INFINITY) ? fast_exp2(sg - Mf) : 0.f;
                 float acc[16];
@@ -1381,8 +1404,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     for (int j = 0; j < 16; ++j) acc[j] += sl->acc[n][d0 + j] * wgt;
                 }
                 if (internal) {
-                    if (n < qrows) {
-                        const int t = MT ? n / p.G : 0, h = MT ? n - t * p.G : n;
+                    if (rn < qrows) {
+                        const int t = MT ? rn / p.G : 0, h = MT ? rn - t * p.G : rn;
                         const float inv = (MT && t >= s_n[b]) ? 0.f : 1.f / den;  // no query token: zeros
                         uint4 *dst = reinterpret_cast<uint4 *>(
                             p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD + d0);
@@ -1399,7 +1422,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         dst[1] = o1;
                     }
                 } else {
-                    float *gp = p.part + (static_cast<size_t>(blockIdx.x) * 2 + slot_k) * kSlotFloats;
+                    float *gp = part_slot(cta, slot_k);
                     if (d0 == 0) {
                         gp[n] = M;
                         gp[GP + n] = den;
@@ -1420,8 +1443,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (tid == 0) {
         const int cand0 = s_flag[2], cand1 = s_flag[3];
         // both tickets in flight together
-        const int t0 = cand0 >= 0 ? atomicAdd(p.counters + cand0, 1) : 0;
-        const int t1 = cand1 >= 0 ? atomicAdd(p.counters + cand1, 1) : 0;
+        const int t0 = cand0 >= 0 ? atomicAdd(counters + cand0, 1) : 0;
+        const int t1 = cand1 >= 0 ? atomicAdd(counters + cand1, 1) : 0;
         auto last_of = [&](int seg, int ticket, int s0, int s1) {
             if (seg < 0) return -1;
             const int c_lo = worker_of(s0, U, nwork) / kWarps;
@@ -1462,8 +1485,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 for (int t = 0; t < kPer; ++t) v[j][t] = 0.f;
                 if (c0 + j < nc) {
                     const int c = c0 + j;
-                    const float *gp =
-                        p.part + (static_cast<size_t>(c_lo + c) * 2 + (c == 0 ? lo_slot : 0)) * kSlotFloats;
+                    const float *gp = part_slot(c_lo + c, c == 0 ? lo_slot : 0);
                     mc[j] = __ldcg(gp + cn);
                     lc[j] = __ldcg(gp + GP + cn);
                     if constexpr (kPer == 2) {
@@ -1492,19 +1514,20 @@ __global__ void __launch_bounds__(kThreads, CPS)
             M = Mn;
         }
         const int qrows = MT ? p.T * p.G : p.G;
-        const float sg = cn < qrows ? s_sink[g * p.G + (MT ? cn % p.G : cn)] : -INFINITY;
+        const int rc = r0g + cn;  // column cn's query row
+        const float sg = rc < qrows ? s_sink[g * p.G + (MT ? rc % p.G : rc)] : -INFINITY;
         const float Mf = fmaxf(M, sg);
         const float a = M == -INFINITY ? 0.f : fast_exp2(M - Mf);
         den = den * a + (sg == -INFINITY ? 0.f : fast_exp2(sg - Mf));
-        const int ct = MT ? cn / p.G : 0, ch = MT ? cn - ct * p.G : cn;
+        const int ct = MT ? rc / p.G : 0, ch = MT ? rc - ct * p.G : rc;
         const float f = (den > 0.f && !(MT && ct >= s_n[b])) ? a / den : 0.f;  // no query token: zeros
-        if (cn < qrows) {
+        if (rc < qrows) {
             __nv_bfloat16 *dst = p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + ct) * p.Hq + g * p.G + ch) * kD + cd0;
 #pragma unroll
             for (int t = 0; t < kPer; t += 2)
                 *reinterpret_cast<uint32_t *>(dst + t) = pack_bf16(acc[t] * f, acc[t + 1] * f);
         }
-        if (tid == 0) p.counters[seg] = 0;  // ready for the next call
+        if (tid == 0) counters[seg] = 0;  // ready for the next call
     }
 }
 
@@ -1727,7 +1750,8 @@ int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm,
     // while the previous kernel of the stream drains; it waits for that kernel before
     // touching memory (griddepcontrol.wait).
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sm_count(dev) * CPS);
+    // the row groups of a several-token call split the grid evenly
+    cfg.gridDim = dim3(sm_count(dev) * CPS / prm.ngrp * prm.ngrp);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1815,6 +1839,7 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.max_position = max_position;
     prm.T = 1;
     prm.q_lens = nullptr;
+    prm.ngrp = 1;
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
@@ -1905,7 +1930,7 @@ bool make_new_map(CUtensorMap *map, const void *base, int Hkv, int T, int B) {
 // split. A function of the shape, T, the window or longest sequence and the SM count only
 // (never of the lengths), so the workspace can be sized ahead and the call captured.
 struct MultiPlan {
-    bool dec;          // the decode kernel's several-token form (paged, T <= 2, T G <= 16)
+    bool dec;          // the decode kernel's several-token form (paged, T <= 4, T G <= 32)
     bool tc;           // the tcgen05 kernel (128 query rows per CTA) or the mma.sync one
     long long groups;  // (sequence, KV head, query-row block) triples, one counter each
     int nw, rows, row_blocks, splits, chunk;
@@ -1920,6 +1945,9 @@ struct MultiPlan {
 #endif
 #ifndef DA_MULTI_DECODE_ROUTE  // 0: every multi-token call on the row-block kernels
 #define DA_MULTI_DECODE_ROUTE 1
+#endif
+#ifndef DA_MULTI_DECODE_MAX_ROWS  // query rows per KV head the decode kernel takes (16 or 32)
+#define DA_MULTI_DECODE_MAX_ROWS 32
 #endif
 #ifndef DA_MULTI_TC_CTAS_PER_SM  // tcgen05 calls: key splits aim at this many CTAs per SM
 #define DA_MULTI_TC_CTAS_PER_SM 2
@@ -1944,18 +1972,20 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     MultiPlan m;
     const int G = s.num_q_heads / s.num_kv_heads;
     const long long TG = static_cast<long long>(T) * G;
-    // One or two query tokens of at most 16 rows per KV head on a paged cache take the decode
-    // kernel's device-balanced split (measured faster than the row-block kernel; the ring keeps
-    // the row-block kernel, whose separate append leaves the cells the earlier tokens read).
-    m.dec = !ring && T <= 2 && TG <= 16 && DA_MULTI_DECODE_ROUTE;
-    if (m.dec) {  // counters in the fixed region, then one pair of partial slots per CTA
+    // Up to kMaxNewMT query tokens of at most 32 rows per KV head on a paged cache take the
+    // decode kernel's device-balanced split (measured faster than the row-block kernel; the
+    // ring keeps the row-block kernel, whose separate append leaves the cells the earlier
+    // tokens read). Over 16 rows, two row groups of 16: pairs of CTAs on the same units.
+    m.dec = !ring && T <= kMaxNewMT && TG <= DA_MULTI_DECODE_MAX_ROWS && DA_MULTI_DECODE_ROUTE;
+    if (m.dec) {  // counters (one set per row group) in the fixed region, then one pair of
+                  // partial slots per CTA
         m.tc = false;
         m.nw = kWarps;
         m.rows = TG <= 8 ? 8 : 16;
-        m.row_blocks = 1;
+        m.row_blocks = static_cast<int>((TG + 15) / 16);
         m.splits = 1;
         m.chunk = 0;
-        m.groups = static_cast<long long>(s.batch) * s.num_kv_heads;
+        m.groups = static_cast<long long>(s.batch) * s.num_kv_heads * m.row_blocks;
         m.counter_bytes = static_cast<size_t>(kMMaxGroups) * sizeof(int);
         m.part_bytes = static_cast<size_t>(sms) * 2 * slot_floats(static_cast<int>(TG)) * sizeof(float);
         return m;
@@ -2080,6 +2110,7 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         dp.max_position = 0;
         dp.T = T;
         dp.q_lens = q_lens;
+        dp.ngrp = m.row_blocks;
         CUtensorMap mk, mv;
         const uint64_t slices = static_cast<uint64_t>(num_pages) * s.num_kv_heads;
         if (!make_kv_map(&mk, k_cache, kPage, slices) || !make_kv_map(&mv, v_cache, kPage, slices)) {
@@ -2246,6 +2277,7 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.max_position = 0;
     prm.T = 1;
     prm.q_lens = nullptr;
+    prm.ngrp = 1;
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call

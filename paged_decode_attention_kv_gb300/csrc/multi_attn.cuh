@@ -11,8 +11,8 @@
 //   rest come from the cache, which holds the history before the step. Rows t >= n and
 //   inactive slots are zero. The new tokens are appended by a second kernel after the
 //   attention: in a W-cell ring the early query tokens still read the cells that the later
-//   new tokens overwrite. (Paged calls of one or two tokens with T G <= 16 run in the decode
-//   kernel instead, append fused: see decode_attn_kernel's MT form.)
+//   new tokens overwrite. (Paged calls of up to four tokens with T G <= 32 run in the
+//   decode kernel instead, append fused: see decode_attn_kernel's MT form.)
 //
 // Included into decode_attn.cu (inside its anonymous namespace): one translation unit,
 // sharing the PTX helpers, the status word and the online-softmax state.

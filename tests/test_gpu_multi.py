@@ -73,9 +73,12 @@ def counts(T, lens, seed):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(64, 8), (8, 8), (16, 1), (32, 4)])
-@pytest.mark.parametrize("T", [2, 5, 16])
+@pytest.mark.parametrize("T", [2, 3, 4, 5, 16])
 @pytest.mark.parametrize("window", [0, 7, 100])
 def test_paged_multi_matches_oracle(Hq, Hkv, T, window):
+    """Up to 4 tokens and 32 query rows per KV head run in the decode kernel (over 16 rows:
+    two row groups, e.g. G = 8 at T = 3 and 4, G = 16 at T = 2), more on the row-block or
+    tcgen05 kernels."""
     n = counts(T, LENS, Hq + T + window)
     m = Multi(800 + Hq + T + window, Hq, Hkv, LENS, n, T)
     run_paged(m, window, seed=T + 1)
@@ -92,13 +95,14 @@ def test_ring_multi_matches_oracle(W, T):
     run_ring(m, W)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (32, 8)])
-def test_segments_spanning_whole_pipelines(Hq, Hkv):
+@pytest.mark.parametrize("Hq,Hkv,T", [(64, 8, 2), (32, 8, 2), (64, 8, 4), (128, 8, 2)])
+def test_segments_spanning_whole_pipelines(Hq, Hkv, T):
     """Sequences whose key tiles fill a warp's stage ring exactly (4, 5, 8, 10, 12, 15, 16,
-    20 tiles): the next sequence's first tile then lands in the stage that held this one's
-    new-token rows before this one's last tile is processed."""
+    20 tiles): the next sequence's first tile then lands in the stage whose slot held this
+    one's query rows before this one's last tiles (which hold the new tokens) are processed.
+    Two and four tokens, 16 and 32 query rows per KV head (one and two row groups)."""
     lens = [64, 80, 128, 160, 192, 240, 256, 320, 63, 65, 2, 17]
-    m = Multi(865 + Hq, Hq, Hkv, lens, [2] * len(lens), 2)
+    m = Multi(865 + Hq + T, Hq, Hkv, lens, [min(T, L) for L in lens], T)
     run_paged(m, 0)
     run_paged(m, 48)
 
@@ -130,10 +134,12 @@ def test_chunked_prefill_sized_step():
     run_ring(m, 128)
 
 
-def test_long_history_uses_many_splits():
-    """One sequence of 20k tokens and 4 draft tokens: the keys are split over many CTAs
-    and the last one combines."""
-    m = Multi(872, 64, 8, [20000, 3000], [4, 3], 4)
+@pytest.mark.parametrize("T", [4, 6, 16])
+def test_long_history_uses_many_splits(T):
+    """One sequence of 20k tokens: its keys are split over many CTAs and the last one
+    combines the partials (the decode kernel's row groups at 4 tokens, the row-block kernel
+    at 6, tcgen05 at 16)."""
+    m = Multi(872 + T, 64, 8, [20000, 3000], [T, T - 1], T)
     run_paged(m, 0)
     run_paged(m, 1000)
 
@@ -202,14 +208,15 @@ def test_full_size_speculative_step(T):
     assert np.array_equal(wl.bits(pool.k_cache), ek) and np.array_equal(wl.bits(pool.v_cache), ev)
 
 
-def test_workspace_reuse_across_shapes():
+@pytest.mark.parametrize("T", [4, 6])
+def test_workspace_reuse_across_shapes(T):
     """A call with few (sequence, head, row-block) groups and many splits writes split
     partials; a following call with more groups must still find its arrival counters at
     zero (the counters live in a region of their own)."""
-    few = Multi(875, 64, 8, [9000, 4000], [4, 2], 4)        # 16 groups, many splits
+    few = Multi(875, 64, 8, [9000, 4000], [T, 2], T)        # few groups, many splits
     run_paged(few, 0)
     lens = [int(x) for x in np.random.default_rng(5).integers(600, 2000, size=48)]
-    many = Multi(876, 64, 8, lens, [4] * 48, 4)              # 384 groups, a few splits each
+    many = Multi(876, 64, 8, lens, [T] * 48, T)              # many groups, a few splits each
     run_paged(many, 0)
     run_paged(few, 0)
     run_paged(many, 0)
