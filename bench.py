@@ -321,13 +321,18 @@ def decode_route(q_tokens, cfg):
     return 1 < q_tokens <= 4 and q_tokens * cfg["Hq"] // cfg["Hkv"] <= 32
 
 
-def launches_per_step(q_tokens, cfg):
+def launches_per_step(q_tokens, cfg, max_pages):
     """Kernel launches of one step (a paged and a ring layer): one per layer for a single
-    query token; for several, the ring layer's attention and append, and the paged layer's
-    one (decode route) or two."""
+    query token; for several, what the library reports for each layer's call (the attention,
+    the append unless fused, and a kernel that folds many key splits' partials)."""
     if q_tokens == 1:
         return 2
-    return 2 + (1 if decode_route(q_tokens, cfg) else 2)
+    import paged_decode_attention_kv_gb300 as da
+    n = [da.decode_attn_multi_launches(cfg["B"], cfg["Hq"], cfg["Hkv"], q_tokens, 0, max_pages * cfg["page_size"]),
+         da.decode_attn_multi_launches(cfg["B"], cfg["Hq"], cfg["Hkv"], q_tokens, cfg["window"], 0)]
+    if min(n) <= 0:
+        raise RuntimeError("the library reported no launch count for this shape")
+    return sum(n)
 
 
 def step_bytes(name, lens, kv="bf16", q_tokens=1):
@@ -577,7 +582,8 @@ def run_ours(args, rank, world, local_rank):
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(args.q_tokens, first.cfg) * args.layers * args.steps,
+        "gpu_launches": launches_per_step(args.q_tokens, first.cfg, first.block_table.shape[1])
+                        * args.layers * args.steps,
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
                    "events around every launch in a second pass (includes the launch gap)"),
         "clocks": clocks,

@@ -204,7 +204,8 @@ DA_API int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_
  * Two kernels on `stream`: the attention, then the append (the ring's early query tokens
  * still read the cells the later new tokens overwrite); paged calls of up to four tokens
  * with T * G <= 32 run one kernel with the append fused (a paged cell of a new token is
- * read only through the tile its own kernel pass patches). Split partials and counters live
+ * read only through the tile its own kernel pass patches); calls with many key splits add a
+ * kernel that folds the splits' partials. Split partials and counters live
  * in a second library workspace (decode_attn_multi_workspace_bytes / _reserve); it is
  * allocated on first use outside graph capture, else DA_ERR_WORKSPACE. T <= 4096.
  * Bad lengths (n_b > T, n_b > L, L beyond the block table) set DA_STATUS_BAD_SEQ_LEN and
@@ -225,6 +226,11 @@ DA_API int decode_attn_ring_multi(const void *q, const void *k_new, const void *
 DA_API size_t decode_attn_multi_workspace_bytes(da_shape s, int q_tokens, int ring_window,
                                                 int max_seq_len);
 DA_API int decode_attn_multi_reserve(size_t bytes);
+/* Kernel launches one such call makes, for the same arguments as
+ * decode_attn_multi_workspace_bytes: 1 when the append is fused into the attention kernel;
+ * else the attention and the append, plus a kernel that folds the key splits' partials when
+ * a sequence's keys are cut into many splits. 0 for invalid arguments or without a device. */
+DA_API int decode_attn_multi_launches(da_shape s, int q_tokens, int ring_window, int max_seq_len);
 
 /*
  * kv_append -- the append alone: bit-copies k_new/v_new [B, Hkv, D] of every

@@ -30,7 +30,7 @@ __all__ = [
     "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT", "DA_STATUS_BAD_POSITION",
     "decode_attn_paged_rope", "decode_attn_ring_rope", "decode_attn_paged_fp8", "decode_attn_ring_fp8",
     "decode_attn_paged_multi", "decode_attn_ring_multi", "decode_attn_multi_workspace_bytes",
-    "decode_attn_multi_reserve",
+    "decode_attn_multi_reserve", "decode_attn_multi_launches",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +98,8 @@ def load_library():
                                            vp, da_shape, c_int, vp]
     lib.decode_attn_multi_workspace_bytes.argtypes = [da_shape, c_int, c_int, c_int]
     lib.decode_attn_multi_workspace_bytes.restype = ctypes.c_size_t
+    lib.decode_attn_multi_launches.argtypes = [da_shape, c_int, c_int, c_int]
+    lib.decode_attn_multi_launches.restype = c_int
     lib.decode_attn_multi_reserve.argtypes = [ctypes.c_size_t]
     lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
@@ -279,6 +281,14 @@ def decode_attn_ring_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, s
 def decode_attn_multi_workspace_bytes(batch, num_q_heads, num_kv_heads, q_tokens, ring_window=0,
                                       max_seq_len=0, head_dim=64):
     return int(load_library().decode_attn_multi_workspace_bytes(
+        da_shape(batch, num_q_heads, num_kv_heads, head_dim), int(q_tokens), int(ring_window),
+        int(max_seq_len)))
+
+
+def decode_attn_multi_launches(batch, num_q_heads, num_kv_heads, q_tokens, ring_window=0,
+                               max_seq_len=0, head_dim=64):
+    """Kernel launches of one multi-token call of this shape (0: invalid, or no device)."""
+    return int(load_library().decode_attn_multi_launches(
         da_shape(batch, num_q_heads, num_kv_heads, head_dim), int(q_tokens), int(ring_window),
         int(max_seq_len)))
 

@@ -1932,6 +1932,7 @@ bool make_new_map(CUtensorMap *map, const void *base, int Hkv, int T, int B) {
 struct MultiPlan {
     bool dec;          // the decode kernel's several-token form (paged, T <= 4, T G <= 32)
     bool tc;           // the tcgen05 kernel (128 query rows per CTA) or the mma.sync one
+    bool defer;        // many key splits: multi_combine_kernel folds the partials
     long long groups;  // (sequence, KV head, query-row block) triples, one counter each
     int nw, rows, row_blocks, splits, chunk;
     size_t counter_bytes, part_bytes;
@@ -1948,6 +1949,11 @@ struct MultiPlan {
 #endif
 #ifndef DA_MULTI_DECODE_MAX_ROWS  // query rows per KV head the decode kernel takes (16 or 32)
 #define DA_MULTI_DECODE_MAX_ROWS 32
+#endif
+// Key splits from which the partials are folded by a kernel of their own (spread over many
+// SMs) rather than by the last CTA of each row block
+#ifndef DA_MULTI_DEFER_SPLITS
+#define DA_MULTI_DEFER_SPLITS 8
 #endif
 #ifndef DA_MULTI_TC_CTAS_PER_SM  // tcgen05 calls: key splits aim at this many CTAs per SM
 #define DA_MULTI_TC_CTAS_PER_SM 2
@@ -1980,6 +1986,7 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     if (m.dec) {  // counters (one set per row group) in the fixed region, then one pair of
                   // partial slots per CTA
         m.tc = false;
+        m.defer = false;
         m.nw = kWarps;
         m.rows = TG <= 8 ? 8 : 16;
         m.row_blocks = static_cast<int>((TG + 15) / 16);
@@ -2011,6 +2018,7 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     sp = std::min(sp, max_tiles);
     m.chunk = static_cast<int>((max_tiles + sp - 1) / sp);
     m.splits = static_cast<int>((max_tiles + m.chunk - 1) / m.chunk);
+    m.defer = m.splits >= DA_MULTI_DEFER_SPLITS;
     // the counters sit in a fixed region: a later call with more groups must find zeros
     // there, not the partials of an earlier call with fewer
     m.groups = groups;
@@ -2144,6 +2152,7 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     prm.chunk = m.chunk;
     prm.counters = static_cast<int *>(g_dev[dev].ws_multi);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws_multi) + m.counter_bytes);
+    prm.defer = m.defer ? 1 : 0;
 
     CUtensorMap mk, mv, nk, nv;
     const uint64_t rows = ring ? static_cast<uint64_t>(window) : static_cast<uint64_t>(kPage);
@@ -2183,6 +2192,19 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mk, mv, nk, nv, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e);
+    if (m.defer) {  // the fold of the split partials, over (16-row slices, KV heads, sequences)
+        cudaLaunchConfig_t cc = {};
+        cc.gridDim = dim3(static_cast<unsigned>(m.row_blocks * ((m.rows + kCombSliceRows - 1) / kCombSliceRows)),
+                          static_cast<unsigned>(s.num_kv_heads), static_cast<unsigned>(s.batch));
+        cc.blockDim = dim3(128);
+        cc.dynamicSmemBytes = 0;
+        cc.stream = stream;
+        cc.attrs = attr;
+        cc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cc, multi_combine_kernel, prm, m.rows, ring ? 1 : 0);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return set_cuda_error(e);
+    }
     // the append, after every read of the cache (an ordinary launch: it waits for the kernel)
     kv_append_multi_kernel<<<s.batch, 256, 0, stream>>>(
         prm.k_new, prm.v_new, static_cast<__nv_bfloat16 *>(k_cache), static_cast<__nv_bfloat16 *>(v_cache),
@@ -2405,6 +2427,15 @@ size_t decode_attn_multi_workspace_bytes(da_shape s, int q_tokens, int ring_wind
     if (current_device(&dev) != DA_OK) return 0;
     const MultiPlan m = multi_plan(s, q_tokens, ring_window > 0, ring_window, max_seq_len, sm_count(dev));
     return m.counter_bytes + m.part_bytes;
+}
+
+int decode_attn_multi_launches(da_shape s, int q_tokens, int ring_window, int max_seq_len) {
+    if (check_shape(s) != DA_OK || q_tokens <= 0 || q_tokens > kMMaxTokens || max_seq_len < 0 || ring_window < 0)
+        return 0;
+    int dev;
+    if (current_device(&dev) != DA_OK) return 0;
+    const MultiPlan m = multi_plan(s, q_tokens, ring_window > 0, ring_window, max_seq_len, sm_count(dev));
+    return m.dec ? 1 : 2 + (m.defer ? 1 : 0);
 }
 
 int decode_attn_multi_reserve(size_t bytes) {

@@ -75,7 +75,48 @@ struct MultiParams {
     int row_blocks, splits, chunk;  // query-row blocks per (b, g); key splits; tiles per split
     float *part;                    // [B * Hkv * row_blocks][splits][rows per CTA][kMSlotFloats]
     int *counters;                  // [B * Hkv * row_blocks], zero at rest
+    int defer;                      // 1: the split partials are left for multi_combine_kernel
 };
+
+// The key tiles of the block of query rows r0 .. r_end - 1 of sequence b: the cached tiles
+// (pages pt_lo .. pt_lo + ncache - 1, or the ring's 16-cell groups) come first, then tiles of
+// 16 new tokens from nt_base on.
+struct MultiKeys {
+    int L, n, base;  // length, new tokens (rows t >= n are empty), first new position L - n
+    int ncache, pt_lo, nvalid, nt_base, ntiles;
+    int ring_off;    // ring: position of cell c = c + ring_off, less W past the newest cell
+    bool bad;        // counts out of range: the slot is treated as inactive
+};
+__device__ __forceinline__ MultiKeys multi_keys(const MultiParams &p, bool ring, int b, int r0, int r_end) {
+    MultiKeys k;
+    k.L = __ldg(p.seq_lens + b);
+    k.n = p.q_lens != nullptr ? __ldg(p.q_lens + b) : p.T;
+    k.bad = k.L < 0 || k.n < 0 || k.n > p.T || (k.L > 0 && k.n > k.L);
+    if (!ring) k.bad = k.bad || k.L > p.max_seq_len || k.L > p.max_pages * kPage;
+    if (k.bad) k.L = 0;
+    if (k.L == 0) k.n = 0;
+    k.base = k.L - k.n;
+    const int W = p.window;
+    const int t0 = r0 / p.G;                        // first query token of the block
+    const int t1 = min(k.n - 1, (r_end - 1) / p.G);  // last valid one (< t0: none)
+    k.ncache = k.pt_lo = k.nvalid = k.nt_base = k.ntiles = k.ring_off = 0;
+    if (t1 >= t0) {
+        const int lo_min = W > 0 ? max(0, k.base + t0 - W + 1) : 0;
+        if (k.base > lo_min) {  // cached keys
+            if (ring) {
+                k.nvalid = min(k.base, W);
+                k.ncache = (k.nvalid + kPage - 1) / kPage;
+                k.ring_off = k.base - 1 - (k.base - 1) % W;
+            } else {
+                k.pt_lo = lo_min / kPage;
+                k.ncache = (k.base - 1) / kPage - k.pt_lo + 1;
+            }
+        }
+        k.nt_base = max(0, lo_min - k.base) / kPage;  // first tile of new tokens (16 per tile)
+        k.ntiles = k.ncache + t1 / kPage - k.nt_base + 1;
+    }
+    return k;
+}
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
                                             int c3, uint32_t bar, uint64_t policy) {
@@ -90,8 +131,8 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// The last split of a row block folds every split's partial (m, l, acc per row) into the
-// output, with the sink. A warp takes kCombRows of the block's rows at a time, so that their
+// The last split of a row block (or multi_combine_kernel) folds every split's partial (m, l,
+// acc per row) of the block's rows rl_lo .. rl_hi - 1 into the output, with the sink. A warp takes kCombRows of the block's rows at a time, so that their
 // loads are in flight together (rows one after another left a chain of dependent L2 round
 // trips in the CTA that finishes last). First pass: lanes stride over the splits and merge
 // (m, l) online, then across the warp. Second pass: lane = (split phase s = lane / 8, output
@@ -99,10 +140,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 // phases are added across the warp.
 constexpr int kCombRows = 4;
 __device__ __noinline__ void multi_combine_rows(const MultiParams &p, const float *all, int RB, int r0, int r_end,
-                                                int n, int b, int g, int nsplit, int warp, int nw, int lane) {
+                                                int n, int b, int g, int nsplit, int rl_lo, int rl_hi, int warp,
+                                                int nw, int lane) {
     auto slot = [&](int sp, int rl) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
     const int phase = lane >> 3, q = lane & 7;
-    for (int rl0 = warp; rl0 < RB; rl0 += kCombRows * nw) {
+    for (int rl0 = rl_lo + warp; rl0 < rl_hi; rl0 += kCombRows * nw) {
         int rl[kCombRows];
         bool row[kCombRows];   // an output row of this block
         bool live[kCombRows];  // a query row (t < n); the other output rows are zeros
@@ -112,7 +154,7 @@ __device__ __noinline__ void multi_combine_rows(const MultiParams &p, const floa
             rl[i] = rl0 + i * nw;
             const int r = r0 + rl[i];
             const int t = r / p.G;
-            row[i] = rl[i] < RB && r < r_end;
+            row[i] = rl[i] < rl_hi && r < r_end;
             live[i] = row[i] && t < n;
             sg[i] = live[i] && p.sinks != nullptr ? __ldg(p.sinks + g * p.G + (r - t * p.G)) * kLog2e : -INFINITY;
             M[i] = -INFINITY;
@@ -234,39 +276,15 @@ __global__ void __launch_bounds__(NW * 32, MultiShape<NW>::kMinBlocks)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- this sequence's counts and the block's key tiles
-    int L = __ldg(p.seq_lens + b);
-    int n = p.q_lens != nullptr ? __ldg(p.q_lens + b) : p.T;
-    bool bad = L < 0 || n < 0 || n > p.T || (L > 0 && n > L);
-    if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
-    if (bad) {
-        if (tid == 0 && g == 0 && blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
-        L = 0;
-    }
-    if (L == 0) n = 0;
-    const int base = L - n;
     const int W = p.window;
     const int TG = p.T * p.G;
     const int r0 = rb * RB;
     const int r_end = min(r0 + RB, TG);
-    const int t0 = r0 / p.G;                             // first query token of the block
-    const int t1 = min(n - 1, (r_end - 1) / p.G);         // last valid one (< t0: none)
-    int ncache = 0, pt_lo = 0, nvalid = 0, nt_base = 0, ntiles = 0;
-    int ring_off = 0;  // ring: position of cell c = c + ring_off, less W past the newest cell
-    if (t1 >= t0) {
-        const int lo_min = W > 0 ? max(0, base + t0 - W + 1) : 0;
-        if (base > lo_min) {  // cached keys
-            if (RING) {
-                nvalid = min(base, W);
-                ncache = (nvalid + kPage - 1) / kPage;
-                ring_off = base - 1 - (base - 1) % W;
-            } else {
-                pt_lo = lo_min / kPage;
-                ncache = (base - 1) / kPage - pt_lo + 1;
-            }
-        }
-        nt_base = max(0, lo_min - base) / kPage;  // first tile of new tokens (16 per tile)
-        ntiles = ncache + t1 / kPage - nt_base + 1;
-    }
+    const MultiKeys keys = multi_keys(p, RING, b, r0, r_end);
+    if (keys.bad && tid == 0 && g == 0 && blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+    const int n = keys.n, base = keys.base;
+    const int ncache = keys.ncache, pt_lo = keys.pt_lo, nvalid = keys.nvalid, nt_base = keys.nt_base;
+    const int ntiles = keys.ntiles, ring_off = keys.ring_off;
     const int kb = split * p.chunk;
     const int ke = min(kb + p.chunk, ntiles);
     const int nsplit = (ntiles + p.chunk - 1) / p.chunk;
@@ -541,6 +559,7 @@ __global__ void __launch_bounds__(NW * 32, MultiShape<NW>::kMinBlocks)
                 o[kMAccOff + mt * 16 + (lane >> 2) + 8] = st.acc[j][mt][c + 2];
             }
         }
+    if (p.defer) return;  // multi_combine_kernel follows
     __threadfence();
     __syncthreads();
     int *ctr = p.counters + bg * p.row_blocks + rb;
@@ -548,9 +567,31 @@ __global__ void __launch_bounds__(NW * 32, MultiShape<NW>::kMinBlocks)
     __syncthreads();
     if (s_ticket != nsplit - 1) return;
     __threadfence();
-    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, RB, r0, r_end, n, b, g, nsplit, warp, nw, lane);
+    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, RB, r0, r_end, n, b, g, nsplit, 0, RB, warp, nw, lane);
     __syncthreads();
     if (tid == 0) *ctr = 0;  // ready for the next call
+}
+
+// Calls whose row blocks are split over many CTAs fold the partials in a kernel of their own,
+// after the attention kernel: one CTA of 4 warps per 16 rows of a row block, so the fold runs
+// on many SMs at once instead of in the one CTA per row block that arrives last (which would
+// read every split's partial of all the block's rows alone).
+constexpr int kCombSliceRows = 16;
+__global__ void __launch_bounds__(128) multi_combine_kernel(const MultiParams p, int RB, int ring) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials of the attention kernel
+    const int slices = (RB + kCombSliceRows - 1) / kCombSliceRows;
+    const int rb = blockIdx.x / slices, sl = blockIdx.x - rb * slices;
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int r0 = rb * RB, r_end = min(r0 + RB, p.T * p.G);
+    const int rl_lo = sl * kCombSliceRows;
+    if (r0 + rl_lo >= r_end) return;
+    const MultiKeys k = multi_keys(p, ring != 0, b, r0, r_end);
+    const int nsplit = (k.ntiles + p.chunk - 1) / p.chunk;
+    if (nsplit <= 1) return;  // the attention kernel wrote these rows (or their zeros)
+    const size_t bg = static_cast<size_t>(b) * p.Hkv + g;
+    const size_t slot0 = ((bg * p.row_blocks + rb) * p.splits) * static_cast<size_t>(RB);
+    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, RB, r0, r_end, k.n, b, g, nsplit, rl_lo,
+                       min(RB, rl_lo + kCombSliceRows), threadIdx.x >> 5, blockDim.x >> 5, threadIdx.x & 31);
 }
 
 // The append of a multi-token step: new token t < n of b goes to position L - n + t. In a

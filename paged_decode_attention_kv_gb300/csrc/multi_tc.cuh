@@ -162,38 +162,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- counts and the key tiles of this row block (as in multi_attn_kernel)
-    int L = __ldg(p.seq_lens + b);
-    int n = p.q_lens != nullptr ? __ldg(p.q_lens + b) : p.T;
-    bool bad = L < 0 || n < 0 || n > p.T || (L > 0 && n > L);
-    if (!RING) bad = bad || L > p.max_seq_len || L > p.max_pages * kPage;
-    if (bad) {
-        if (tid == 0 && g == 0 && blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
-        L = 0;
-    }
-    if (L == 0) n = 0;
-    const int base = L - n;
     const int W = p.window;
     const int TG = p.T * p.G;
     const int r0 = rb * kTcRows;
     const int r_end = min(r0 + kTcRows, TG);
-    const int t0 = r0 / p.G;
-    const int t1 = min(n - 1, (r_end - 1) / p.G);
-    int ncache = 0, pt_lo = 0, nvalid = 0, nt_base = 0, ntiles = 0, ring_off = 0;
-    if (t1 >= t0) {
-        const int lo_min = W > 0 ? max(0, base + t0 - W + 1) : 0;
-        if (base > lo_min) {
-            if (RING) {
-                nvalid = min(base, W);
-                ncache = (nvalid + kPage - 1) / kPage;
-                ring_off = base - 1 - (base - 1) % W;
-            } else {
-                pt_lo = lo_min / kPage;
-                ncache = (base - 1) / kPage - pt_lo + 1;
-            }
-        }
-        nt_base = max(0, lo_min - base) / kPage;
-        ntiles = ncache + t1 / kPage - nt_base + 1;
-    }
+    const MultiKeys keys = multi_keys(p, RING, b, r0, r_end);
+    if (keys.bad && tid == 0 && g == 0 && blockIdx.x == 0) flag_status(DA_STATUS_BAD_SEQ_LEN);
+    const int n = keys.n, base = keys.base;
+    const int ncache = keys.ncache, pt_lo = keys.pt_lo, nvalid = keys.nvalid, nt_base = keys.nt_base;
+    const int ntiles = keys.ntiles, ring_off = keys.ring_off;
     const int kb = split * p.chunk;
     const int ke = min(kb + p.chunk, ntiles);
     const int nsplit = (ntiles + p.chunk - 1) / p.chunk;
@@ -565,7 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(kTcTmemCols));
     }
-    if (nsplit == 1) return;
+    if (nsplit == 1 || p.defer) return;  // p.defer: multi_combine_kernel follows
     __threadfence();
     __syncthreads();
     int *ctr = p.counters + bg * p.row_blocks + rb;
@@ -574,7 +551,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (s_ticket != nsplit - 1) return;
     __threadfence();
     const size_t slot0 = ((bg * p.row_blocks + rb) * p.splits) * static_cast<size_t>(kTcRows);
-    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, kTcRows, r0, r_end, n, b, g, nsplit, warp, kTcWarps, lane);
+    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, kTcRows, r0, r_end, n, b, g, nsplit, 0, kTcRows, warp,
+                       kTcWarps, lane);
     __syncthreads();
     if (tid == 0) *ctr = 0;  // ready for the next call
 }

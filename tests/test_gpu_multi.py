@@ -208,6 +208,23 @@ def test_full_size_speculative_step(T):
     assert np.array_equal(wl.bits(pool.k_cache), ek) and np.array_equal(wl.bits(pool.v_cache), ev)
 
 
+@pytest.mark.parametrize("T", [6, 16])
+@pytest.mark.parametrize("B,deferred", [(24, False), (2, True)])
+def test_split_combine_in_kernel_and_deferred(T, B, deferred):
+    """Few key splits per row block are folded by the row block's last CTA; many by a
+    kernel of their own after the attention (three launches in all). Both paths, on the
+    row-block kernel (6 tokens) and on tcgen05 (16)."""
+    rng = np.random.default_rng(880 + T + B)
+    lens = [int(x) for x in rng.integers(700, 3000, size=B)]
+    lens[0] = 2900  # at 2 sequences: over 8 splits of at least 16 tiles
+    m = Multi(880 + T + B, 64, 8, lens, [T] * B, T)
+    _, _, bt = m.paged(1)
+    launches = da.decode_attn_multi_launches(B, 64, 8, T, 0, bt.shape[1] * 16)
+    assert launches == (3 if deferred else 2)
+    run_paged(m, 0)
+    run_paged(m, 300)
+
+
 @pytest.mark.parametrize("T", [4, 6])
 def test_workspace_reuse_across_shapes(T):
     """A call with few (sequence, head, row-block) groups and many splits writes split
