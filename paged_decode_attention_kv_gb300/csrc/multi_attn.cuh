@@ -23,7 +23,7 @@
 // CTA streams the key tiles of its split through one TMA pipeline that every warp reads:
 // cached tiles first (pages, or 16-cell groups of the ring), then tiles of 16 new tokens
 // copied straight out of k_new / v_new by a 4-D tensor map. Splits of the same rows leave
-// fp32 partials; the CTA that takes the last ticket combines them with the sink.
+// fp32 partials; the CTA with the last ticket (many splits: multi_combine_kernel) folds them with the sink.
 
 #ifndef DA_MULTI_NT
 #define DA_MULTI_NT 1
@@ -32,7 +32,7 @@
 #define DA_MULTI_WARPS 4
 #endif
 // Two CTA shapes, by the warps a call needs: up to 2 (at most 16 query rows per sequence and
-// KV head: one or two tokens at 8 heads per group) and up to 4. Small CTAs gain most from
+// KV head: ring calls of one or two tokens at 8 heads per group) and up to 4. Small CTAs gain most from
 // residency (many CTAs per SM with 4 stages each), 4-warp CTAs from deep pipelines (8 stages
 // at 4 CTAs per SM): measured on both shapes.
 #ifndef DA_MULTI_MIN_BLOCKS  // resident 4-warp CTAs per SM the register budget is cut for
