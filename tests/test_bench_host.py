@@ -71,3 +71,22 @@ def test_the_code_hash_ignores_comments_only():
     assert '"// kept /* kept */"' in out and "char c = '\"';" in out and "int a = 1;" in out
     assert bench.strip_comments(src.replace("// one", "// another")) == out
     assert bench.strip_comments(src.replace("a = 1", "a = 2")) != out
+
+
+def test_launch_count_sums_the_library_answer_per_layer(monkeypatch):
+    import paged_decode_attention_kv_gb300 as da
+    cfg = {"B": 64, "Hq": 64, "Hkv": 8, "page_size": 16, "window": 128}
+    seen = []
+
+    def fake(B, Hq, Hkv, T, ring_window, max_seq_len):
+        seen.append((B, Hq, Hkv, T, ring_window, max_seq_len))
+        return 1 if ring_window == 0 else 2  # paged call fused, ring call attention + append
+
+    monkeypatch.setattr(da, "decode_attn_multi_launches", fake)
+    assert bench.launches_per_step(1, cfg, 495) == 2  # one token: one launch per layer
+    assert seen == []
+    assert bench.launches_per_step(4, cfg, 495) == 3
+    assert seen == [(64, 64, 8, 4, 0, 495 * 16), (64, 64, 8, 4, 128, 0)]
+    monkeypatch.setattr(da, "decode_attn_multi_launches", lambda *a: 0)
+    with pytest.raises(RuntimeError):
+        bench.launches_per_step(4, cfg, 495)
