@@ -24,7 +24,7 @@ _FUNCS = ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
           "oracle_decode_ring_rope", "oracle_e4m3_decode", "oracle_e4m3_encode",
           "oracle_quantise_rows", "oracle_decode_paged_fp8", "oracle_decode_ring_fp8",
           "oracle_kv_append_fp8", "oracle_scatter_fp8", "oracle_decode_multi",
-          "oracle_kv_append_multi")
+          "oracle_kv_append_multi", "oracle_decode_paged_fp8_rope", "oracle_decode_ring_fp8_rope")
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -74,6 +74,12 @@ def _load():
             _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
         lib.oracle_decode_ring_fp8.argtypes = [
             _u16p, _u16p, _u16p, _u8p, _i32p, _f32p, c_int, c_double, _f64p,
+            c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_decode_paged_fp8_rope.argtypes = [
+            _u16p, _u16p, _u16p, _u8p, _i32p, _i32p, _f32p, _f32p, _f32p, c_int, c_int, c_double,
+            _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
+        lib.oracle_decode_ring_fp8_rope.argtypes = [
+            _u16p, _u16p, _u16p, _u8p, _i32p, _f32p, _f32p, _f32p, c_int, c_int, c_double, _f64p,
             c_int, c_int, c_int, c_int, _i32p, c_int, c_int]
         lib.oracle_kv_append_fp8.argtypes = [
             _u16p, _u16p, _u8p, _i32p, _i32p, c_int, c_int, c_int, c_int, c_int, c_int, c_int]
@@ -519,6 +525,45 @@ def decode_ring_fp8(q, k_new, v_new, cache, seq_lens, sinks, window, scale, item
         _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), cache.ptr(), _ptr(sl, _i32p),
         _ptr(sk, _f32p), int(window), float(scale), _ptr(out, _f64p), B, Hq, Hkv, D,
         _ptr(it, _i32p), n_items, nthreads or default_threads()), "decode_ring_fp8")
+    return out
+
+
+def decode_paged_fp8_rope(q, k_new, v_new, cache, block_table, seq_lens, sinks, rope_cos, rope_sin,
+                          window, scale, items=None, nthreads=None):
+    """decode_paged_fp8 with q and k_new rotated to position L - 1 first (the new key is
+    rotated as stored in bf16, then quantised on append)."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    num_pages, Hkv = cache.blocks.shape[:2]
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_paged_fp8_rope(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), cache.ptr(), _ptr(bt, _i32p),
+        _ptr(sl, _i32p), _ptr(sk, _f32p), _ptr(c, _f32p), _ptr(sn, _f32p), maxpos, int(window),
+        float(scale), _ptr(out, _f64p), B, Hq, Hkv, D, cache.P, bt.shape[1], num_pages,
+        _ptr(it, _i32p), n_items, nthreads or default_threads()), "decode_paged_fp8_rope")
+    return out
+
+
+def decode_ring_fp8_rope(q, k_new, v_new, cache, seq_lens, sinks, rope_cos, rope_sin, window, scale,
+                         items=None, nthreads=None):
+    """decode_ring_fp8 with q and k_new rotated to position L - 1 first."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    sl, sk = _i32(seq_lens), _f32(sinks)
+    B, Hq, D = q.shape
+    Hkv = cache.blocks.shape[1]
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    it, n_items = _items(items)
+    out = np.zeros((n_items, D) if it is not None else (B, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_ring_fp8_rope(
+        _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), cache.ptr(), _ptr(sl, _i32p),
+        _ptr(sk, _f32p), _ptr(c, _f32p), _ptr(sn, _f32p), maxpos, int(window), float(scale),
+        _ptr(out, _f64p), B, Hq, Hkv, D, _ptr(it, _i32p), n_items, nthreads or default_threads()),
+        "decode_ring_fp8_rope")
     return out
 
 

@@ -608,6 +608,7 @@ typedef struct {
     int B, Hq, Hkv, D, P, max_pages, num_pages;
     const int32_t *items; int n_items;
     double *out;
+    const double *q64;           /* rotated queries [B][Hq][D] in fp64 (the RoPE steps), or NULL */
 } problem8;
 
 /* dequantised key and value rows of position j (cache or, for j = L-1, the quantised new token) */
@@ -648,13 +649,14 @@ static int attend_one8(const problem8 *pr, int b, int h, double *out) {
     double *kv = (double *)malloc(sizeof(double) * 2 * (size_t)D);
     if (!s || !kv) { free(s); free(kv); return OR_NOMEM; }
     const uint16_t *qrow = pr->q + ((size_t)b * pr->Hq + h) * D;
+    const double *q64 = pr->q64 ? pr->q64 + ((size_t)b * pr->Hq + h) * D : NULL;
     const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;
     double M = sigma;
     int st = OR_OK;
     for (int i = 0; i < n && st == OR_OK; ++i) {
         st = token_rows8(pr, b, g, lo + i, kv, kv + D);
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * kv[d];
+        for (int d = 0; d < D; ++d) dot += (q64 ? q64[d] : bf16_to_f64(qrow[d])) * kv[d];
         s[i] = pr->scale * dot;
         if (s[i] > M) M = s[i];
     }
@@ -729,6 +731,56 @@ int oracle_decode_ring_fp8(const uint16_t *q, const uint16_t *k_new, const uint1
     problem8 pr = {1, q, k_new, v_new, blocks, NULL, seq_lens, sinks,
                    window, scale, B, Hq, Hkv, D, 16, 0, 0, items, n_items, out};
     return run8(&pr, nthreads);
+}
+
+/* fp8 cache with the fused RoPE: q is rotated to position L - 1 exactly (fp64) and the new
+ * key is rotated as it is stored (bf16, rope_row_bf16) BEFORE it is quantised; then the step
+ * is oracle_decode_paged_fp8 / oracle_decode_ring_fp8 on those inputs. */
+static int decode_fp8_rope(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                           const uint8_t *blocks, const int32_t *block_table, const int32_t *seq_lens,
+                           const float *sinks, const float *rope_cos, const float *rope_sin,
+                           int max_position, int window, double scale, double *out, int B, int Hq, int Hkv,
+                           int D, int page_size, int max_pages, int num_pages, const int32_t *items,
+                           int n_items, int nthreads) {
+    double *q64 = NULL;
+    uint16_t *krot = NULL;
+    int st = rope_inputs(q, k_new, seq_lens, rope_cos, rope_sin, max_position, B, Hq, Hkv, D, &q64, &krot);
+    if (st == OR_OK) {
+        problem8 pr = {ring, q, krot, v_new, blocks, block_table, seq_lens, sinks,
+                       window, scale, B, Hq, Hkv, D, page_size, max_pages, num_pages, items, n_items, out,
+                       q64};
+        st = run8(&pr, nthreads);
+    }
+    free(q64);
+    free(krot);
+    return st;
+}
+
+int oracle_decode_paged_fp8_rope(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                 const uint8_t *blocks, const int32_t *block_table, const int32_t *seq_lens,
+                                 const float *sinks, const float *rope_cos, const float *rope_sin,
+                                 int max_position, int window, double scale, double *out, int B, int Hq,
+                                 int Hkv, int D, int page_size, int max_pages, int num_pages,
+                                 const int32_t *items, int n_items, int nthreads) {
+    if (!q || !blocks || !block_table || !seq_lens || !out || page_size <= 0 || max_pages <= 0 ||
+        num_pages <= 0 || window < 0 || ((k_new == NULL) != (v_new == NULL)))
+        return OR_BAD_ARG;
+    return decode_fp8_rope(0, q, k_new, v_new, blocks, block_table, seq_lens, sinks, rope_cos, rope_sin,
+                           max_position, window, scale, out, B, Hq, Hkv, D, page_size, max_pages, num_pages,
+                           items, n_items, nthreads);
+}
+
+int oracle_decode_ring_fp8_rope(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                const uint8_t *blocks, const int32_t *seq_lens, const float *sinks,
+                                const float *rope_cos, const float *rope_sin, int max_position, int window,
+                                double scale, double *out, int B, int Hq, int Hkv, int D,
+                                const int32_t *items, int n_items, int nthreads) {
+    if (!q || !blocks || !seq_lens || !out || window <= 0 || window % 16 != 0 ||
+        ((k_new == NULL) != (v_new == NULL)))
+        return OR_BAD_ARG;
+    return decode_fp8_rope(1, q, k_new, v_new, blocks, NULL, seq_lens, sinks, rope_cos, rope_sin,
+                           max_position, window, scale, out, B, Hq, Hkv, D, 16, 0, 0, items, n_items,
+                           nthreads);
 }
 
 /* Write token rows (bf16 [n][Hkv][D] per sequence b at positions pos[b] .. ) quantised into an

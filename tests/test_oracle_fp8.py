@@ -162,3 +162,77 @@ def test_block_layout_byte_by_byte():
     np.testing.assert_array_equal(rb[4 * 64:5 * 64], kc[0])
     np.testing.assert_array_equal(rb[1024 + np.arange(64) * 16 + 4], vc[0])
     assert rb[2064:2068].view(np.float32)[0] == ksc[0] and rb[2128:2132].view(np.float32)[0] == vsc[0]
+
+
+# ---------------------------------------------------------------- fp8 cache with the fused RoPE
+def _rope_tables(kind, maxpos, D=64):
+    if kind == "identity":
+        return np.ones((maxpos, D // 2), np.float32), np.zeros((maxpos, D // 2), np.float32)
+    if kind == "quarter":   # cos 0, sin 1: (x1, x2) -> (-x2, x1), exact on bf16 patterns
+        return np.zeros((maxpos, D // 2), np.float32), np.ones((maxpos, D // 2), np.float32)
+    return wl.rope_tables(maxpos, D)
+
+
+def _half_swap(x):
+    h = x.shape[-1] // 2
+    return np.concatenate([x[..., h:] ^ np.uint16(0x8000), x[..., :h]], axis=-1)
+
+
+def _fp8_rope_case(seed):
+    lens = [1, 16, 17, 40]
+    c = make_case(seed, 4, 8, 2, 64, lens)
+    kp, vp, bt = shuffle_pages(*paged_identity(c, pre(c)), 3)
+    paged = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c),
+                               oracle.Fp8Cache.empty_paged(kp.shape[0], 2, 16, 64), block_table=bt)
+    ring = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c), oracle.Fp8Cache.empty_ring(4, 2, 32, 64),
+                              window=32)
+    return c, bt, paged, ring
+
+
+def test_fp8_rope_with_identity_tables_is_the_fp8_step():
+    c, bt, paged, ring = _fp8_rope_case(611)
+    cs, sn = _rope_tables("identity", 64)
+    np.testing.assert_array_equal(
+        oracle.decode_paged_fp8_rope(c.q, c.k_new, c.v_new, paged, bt, c.lens, c.sinks, cs, sn, 0, c.scale),
+        oracle.decode_paged_fp8(c.q, c.k_new, c.v_new, paged, bt, c.lens, c.sinks, 0, c.scale))
+    np.testing.assert_array_equal(
+        oracle.decode_ring_fp8_rope(c.q, c.k_new, c.v_new, ring, c.lens, c.sinks, cs, sn, 32, c.scale),
+        oracle.decode_ring_fp8(c.q, c.k_new, c.v_new, ring, c.lens, c.sinks, 32, c.scale))
+
+
+def test_fp8_rope_quarter_turn_is_the_step_on_half_swapped_inputs():
+    """A quarter turn rotates q and the new key into their signed half swaps exactly; the
+    quantised new key of the swapped row is then the swapped codes (same amax, same scale)."""
+    c, bt, paged, ring = _fp8_rope_case(612)
+    cs, sn = _rope_tables("quarter", 64)
+    qs, ks = _half_swap(c.q), _half_swap(c.k_new)
+    np.testing.assert_array_equal(
+        oracle.decode_paged_fp8_rope(c.q, c.k_new, c.v_new, paged, bt, c.lens, c.sinks, cs, sn, 0, c.scale),
+        oracle.decode_paged_fp8(qs, ks, c.v_new, paged, bt, c.lens, c.sinks, 0, c.scale))
+    np.testing.assert_array_equal(
+        oracle.decode_ring_fp8_rope(c.q, c.k_new, c.v_new, ring, c.lens, c.sinks, cs, sn, 32, c.scale),
+        oracle.decode_ring_fp8(qs, ks, c.v_new, ring, c.lens, c.sinks, 32, c.scale))
+
+
+def test_fp8_rope_rotates_the_new_key_before_quantising_it():
+    """At generic angles the fused step equals: store quantise(rotate(k_new)) first (the
+    bf16 rotation of the RoPE pins, the quantisation of the fp8 pins), then attend with the
+    rotated query and the token read back from the cache. Quantising first and rotating
+    the codes would store different values."""
+    c, bt, paged, ring = _fp8_rope_case(613)
+    cs, sn = _rope_tables("plain", 64)
+    krot = oracle.rope_k(c.k_new, c.lens, cs, sn)
+    fused = oracle.decode_paged_fp8_rope(c.q, c.k_new, c.v_new, paged, bt, c.lens, c.sinks, cs, sn, 0,
+                                         c.scale)
+    app = oracle.kv_append_fp8(krot, c.v_new, paged, c.lens, block_table=bt)
+    after = oracle.decode_paged_fp8_rope(c.q, None, None, app, bt, c.lens, c.sinks, cs, sn, 0, c.scale)
+    np.testing.assert_array_equal(fused, after)
+    wrong = oracle.decode_paged_fp8_rope(c.q, None, None,
+                                         oracle.kv_append_fp8(c.k_new, c.v_new, paged, c.lens,
+                                                              block_table=bt),
+                                         bt, c.lens, c.sinks, cs, sn, 0, c.scale)
+    assert np.abs(wrong - fused).max() > 1e-3
+    fr = oracle.decode_ring_fp8_rope(c.q, c.k_new, c.v_new, ring, c.lens, c.sinks, cs, sn, 32, c.scale)
+    ar = oracle.kv_append_fp8(krot, c.v_new, ring, c.lens, window=32)
+    np.testing.assert_array_equal(
+        fr, oracle.decode_ring_fp8_rope(c.q, None, None, ar, c.lens, c.sinks, cs, sn, 32, c.scale))
