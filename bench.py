@@ -284,6 +284,9 @@ def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=
     if s.T > 1:
         da.decode_attn_paged_multi(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks, 0,
                                    s.inp.scale, out)
+    elif s.kv == "fp8" and rope:
+        da.decode_attn_paged_fp8_rope(q, k_new, v_new, s.pool, bt, sl, sinks, s.rope_cos, s.rope_sin, 0,
+                                      s.inp.scale, out)
     elif s.kv == "fp8":
         da.decode_attn_paged_fp8(q, k_new, v_new, s.pool, bt, sl, sinks, 0, s.inp.scale, out)
     elif rope:
@@ -305,6 +308,9 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None, out=
     if s.T > 1:
         da.decode_attn_ring_multi(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
                                   s.inp.scale, out)
+    elif s.kv == "fp8" and rope:
+        da.decode_attn_ring_fp8_rope(q, k_new, v_new, s.ring, sl, sinks, s.rope_cos, s.rope_sin,
+                                     s.inp.scale, out)
     elif s.kv == "fp8":
         da.decode_attn_ring_fp8(q, k_new, v_new, s.ring, sl, sinks, s.inp.scale, out)
     elif rope:
@@ -375,6 +381,12 @@ def oracle_sample(name, s: "StepInputs", budget_s):
                                     s.inp.scale, block_table=bt[one], nthreads=cores)
                 oracle.decode_multi(q[one], kn[one], vn[one], rk[one], rv[one], lens[one], sinks,
                                     W, s.inp.scale, nthreads=cores)
+            elif s.kv == "fp8" and getattr(s, "rope", False):
+                cs, sn = s.rope_cos.cpu().numpy(), s.rope_sin.cpu().numpy()
+                oracle.decode_paged_fp8_rope(q, kn, vn, pool8, bt, lens, sinks, cs, sn, 0, s.inp.scale,
+                                             items=items, nthreads=cores)
+                oracle.decode_ring_fp8_rope(q, kn, vn, ring8, lens, sinks, cs, sn, W, s.inp.scale,
+                                            items=items, nthreads=cores)
             elif s.kv == "fp8":
                 oracle.decode_paged_fp8(q, kn, vn, pool8, bt, lens, sinks, 0, s.inp.scale,
                                         items=items, nthreads=cores)
@@ -536,6 +548,10 @@ def run_ours(args, rank, world, local_rank):
         call_ring(s, args.rope)
         ev_r1[i].record(stream)
     torch.cuda.synchronize()
+    per_config = None
+    if args.per_config == "on" or (args.per_config == "auto" and args.q_tokens == 1 and not args.rope
+                                   and args.layers == 1):
+        per_config = per_config_block(args, dev, l2, measured_hbm_peak()[0], nominal_hbm_peak())
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     paged_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p0, ev_p1)) / args.steps
@@ -588,11 +604,111 @@ def run_ours(args, rank, world, local_rank):
                    "events around every launch in a second pass (includes the launch gap)"),
         "clocks": clocks,
     }
+    if per_config is not None:
+        result["per_config"] = per_config
+        result["per_config_timing"] = (
+            "per workload, the paged (full attention) and the ring (window 128) call of the "
+            "step, 128 timed calls of each kind: 16 batches of 8 calls of one kind queued back "
+            "to back (input sets rotating, > 2x L2), CUDA events around each batch, every batch "
+            "queued behind a GPU spin so the host never starves the device; us = the per-call "
+            "mean of a batch (median, p10, p90 over the 16 batches); direct = launches through "
+            "the public API, graph = the replay of a CUDA graph holding the batch's 8 calls")
     if world == 1 and not args.no_cpu_baseline:
         v, cores, desc = oracle_sample(args.workload, first, args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores,
                                   "kind": "oracle", "sample": desc}
     return result
+
+
+# ---------------------------------------------------------------- every config, per call
+PER_CONFIG = ("b1", "b64", "long1", "long8", "serve")
+
+
+def quantiles(xs):
+    """Median, 10th and 90th percentile (nearest rank) of a list of floats."""
+    ys = sorted(xs)
+    at = lambda f: ys[min(len(ys) - 1, max(0, int(round(f * (len(ys) - 1)))))]
+    return at(0.5), at(0.1), at(0.9)
+
+
+def timed_batches(n_sets, fn, n_batches, per_batch, gate_cycles):
+    """Device µs per call of one kind of call: n_batches batches of per_batch calls queued
+    back to back (rotating over n_sets input sets), CUDA events on the current stream around
+    each batch, each batch queued behind a timed spin of the GPU (torch.cuda._sleep) so that
+    the host's launch rate never starves the device. fn(i, k) launches the k-th call of
+    batch i (or, for graphs, the whole batch at k == 0). Returns the per-call mean of every
+    batch."""
+    import torch
+    stream = torch.cuda.current_stream()
+    out = []
+    for i in range(n_batches):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(gate_cycles)
+        e0.record(stream)
+        fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / per_batch)
+    return out
+
+
+def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
+    """µs per call (median, p10 and p90 over n_batches batches of per_batch calls, each batch
+    queued back to back: n_batches * per_batch >= 100 timed calls), algorithmic GB/s and the
+    fractions of the measured and nominal HBM peaks for the paged and the ring call of every
+    workload, by direct launch and by the replay of a CUDA graph holding one batch. Inputs
+    are larger than L2 per call or rotate over sets totalling more than twice L2."""
+    import torch
+    import paged_decode_attention_kv_gb300 as da
+    from paged_decode_attention_kv_gb300.graph import DecodeStepGraph
+    gate = int(3e-3 * 2.07e9)  # about 3 ms of spin ahead of each batch
+    out = {}
+    for name in PER_CONFIG:
+        first = StepInputs(name, dev, kv=args.kv)
+        set_bytes = first.nbytes() + sum(t.numel() * t.element_size() for t in
+                                         (first.q, first.k_new, first.v_new, first.out_full, first.out_ring))
+        n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
+        sets = [first] + [StepInputs(name, dev, seed_offset=k * 10007, kv=args.kv) for k in range(1, n_sets)]
+        c = first.cfg
+        shape = (c["B"], c["Hq"], c["Hkv"], c["D"])
+        da.decode_attn_reserve(da.decode_attn_workspace_bytes(*shape))
+        pb, rb = step_bytes(name, first.lens, args.kv)
+        entry = {"timed_calls": n_batches * per_batch, "input_sets": n_sets,
+                 "algorithmic_bytes": {"paged_full": pb, "ring": rb},
+                 "max_len": max(first.lens), "active": sum(1 for L in first.lens if L > 0)}
+        for kind, nbytes, call in (("paged_full", pb, call_paged), ("ring", rb, call_ring)):
+            for k in range(2 * n_sets + 3):  # warm-up, module and attribute set-up before capture
+                call(sets[k % n_sets], False)
+            torch.cuda.synchronize()
+
+            def direct(i):
+                for k in range(per_batch):
+                    call(sets[(i * per_batch + k) % n_sets], False)
+            # one graph per distinct run of per_batch sets
+            n_graphs = n_sets // math.gcd(n_sets, per_batch) if n_sets > 1 else 1
+            graphs = [DecodeStepGraph([lambda s=sets[(g * per_batch + k) % n_sets]: call(s, False)
+                                       for k in range(per_batch)], shape, dev).capture()
+                      for g in range(n_graphs)]
+            res = {"direct": timed_batches(n_sets, direct, n_batches, per_batch, gate),
+                   "graph": timed_batches(n_sets, lambda i: graphs[i % n_graphs].replay(), n_batches,
+                                          per_batch, gate)}
+            e = {}
+            for mode, xs in res.items():
+                med, p10, p90 = quantiles(xs)
+                gbs = nbytes / (med * 1e-6) / 1e9
+                e[mode] = {"us_median": round(med, 2), "us_p10": round(p10, 2), "us_p90": round(p90, 2),
+                           "gb_s": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                           "frac_of_nominal": round(gbs / nominal, 4) if nominal else None}
+            entry[kind] = e
+            del graphs
+        torch.cuda.synchronize()
+        status = da.decode_attn_device_status()
+        if status != 0:
+            raise RuntimeError(f"{name}: device status {status}")
+        out[name] = entry
+        del sets, first
+        torch.cuda.empty_cache()
+    return out
 
 
 def packed(tensors, dev=None, pin=False):
@@ -667,13 +783,14 @@ def main():
     ap.add_argument("--q-tokens", type=int, default=1,
                     help="new tokens per sequence per step (speculative verification / chunked "
                          "prefill): > 1 runs the multi-token calls")
+    ap.add_argument("--per-config", default="auto", choices=["auto", "on", "off"],
+                    help="time the paged and ring calls of every workload (b1, b64, long1, long8, "
+                         "serve) per call; auto: on for one-token steps without --rope")
     ap.add_argument("--batch-limit", type=int, default=None,
                     help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.kv == "fp8" and args.rope:
-        ap.error("--rope is not available with --kv fp8")
     if args.q_tokens > 1 and (args.rope or args.kv == "fp8" or args.graph):
         ap.error("--q-tokens > 1 runs the bf16 multi-token calls without --rope, --kv fp8, --graph")
 

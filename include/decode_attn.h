@@ -168,8 +168,7 @@ DA_API int decode_attn_ring_rope(const void *q, const void *k_new, const void *v
  * the row is all zero), code_d = the e4m3 value nearest to x_d / scale (fp32 division),
  * ties to even, saturating at +-448; its K row, V column and both scales are written.
  * Scores and the PV product run in fp16 on tensor cores: |q| must stay below 65504.
- * No rotary embedding on this path yet (DA_ERR_UNSUPPORTED). Other arguments, the status
- * and the error behaviour as in decode_attn_paged / _ring.
+ * Other arguments, the status and the error behaviour as in decode_attn_paged / _ring.
  */
 DA_API int decode_attn_paged_fp8(const void *q, const void *k_new, const void *v_new,
                                  void *kv_cache, const int32_t *block_table,
@@ -180,6 +179,28 @@ DA_API int decode_attn_paged_fp8(const void *q, const void *k_new, const void *v
 DA_API int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_new,
                                 void *kv_cache, const int32_t *seq_lens, const float *sinks,
                                 int window, float scale, void *out, da_shape s, void *stream);
+
+/*
+ * decode_attn_paged_fp8_rope / decode_attn_ring_fp8_rope -- the fp8 steps with the rotary
+ * embedding fused in (SimpleLLM README, changes table, rows "RoPE as one fused kernel at
+ * every batch size" and "one decode-attention kernel for sinks, sliding window, GQA and the
+ * KV append"): q and the new key are rotated to position p = L - 1 exactly as in
+ * decode_attn_paged_rope (the new key in fp32, rounded to bf16 nearest even), and the
+ * rotated key is then quantised and appended as in decode_attn_paged_fp8. The rotated
+ * query is rounded to bf16, then converted to fp16 for the products. rope_cos, rope_sin and
+ * max_position as in decode_attn_paged_rope; the other arguments as in the fp8 calls.
+ */
+DA_API int decode_attn_paged_fp8_rope(const void *q, const void *k_new, const void *v_new,
+                                      void *kv_cache, const int32_t *block_table,
+                                      const int32_t *seq_lens, const float *sinks,
+                                      const float *rope_cos, const float *rope_sin, int max_position,
+                                      int window, float scale, void *out, da_shape s, int page_size,
+                                      int max_pages_per_seq, int num_pages, int max_seq_len,
+                                      void *stream);
+DA_API int decode_attn_ring_fp8_rope(const void *q, const void *k_new, const void *v_new,
+                                     void *kv_cache, const int32_t *seq_lens, const float *sinks,
+                                     const float *rope_cos, const float *rope_sin, int max_position,
+                                     int window, float scale, void *out, da_shape s, void *stream);
 
 /*
  * decode_attn_paged_multi / decode_attn_ring_multi -- several query tokens per sequence in
@@ -257,7 +278,8 @@ DA_API int kv_append(const void *k_new, const void *v_new, void *k_cache, void *
  *   - Limits: batch * num_kv_heads <= 4096 and a GPU with at most 160 SMs; beyond
  *     that it returns DA_ERR_SCRATCH_LIMIT and launches nothing.
  *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current); make that first call before any stream capture. A first call made while
+ *     `stream` is capturing returns DA_ERR_WORKSPACE and launches nothing.
  *   - Every call on a device shares the one array (it clears the arrival counters it
  *     needs at the start of each call), so calls that overlap on the GPU, e.g. on two
  *     streams at once, race and give wrong results. Serialise them.
@@ -275,6 +297,18 @@ DA_API size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len);
 /* Make sure the current device's workspace holds at least `bytes` (allocates
  * and zeroes synchronously). Call before capturing a CUDA graph. */
 DA_API int decode_attn_reserve(size_t bytes);
+
+/*
+ * decode_attn_test_expire_wait -- a testing aid for the bounded-wait failure path. It arms a
+ * one-shot: in the next one-token attention call (decode_attn_paged / _ring and their
+ * _rope / _fp8 forms), the first worker gives up at its first tile wait from its tile
+ * `tile` on (0-based, counted over that worker's share of the tiles), after that tile has
+ * landed, exactly as if the bounded wait had expired. The call then records
+ * DA_STATUS_TIMEOUT, its output is garbage, no copy is left in flight, and the library's
+ * arrival counters are back at zero for the next call. tile < 0 disarms. No GPU fault,
+ * trap or hang is involved. Returns DA_OK.
+ */
+DA_API int decode_attn_test_expire_wait(int tile);
 
 /* Wait for `stream`, then return the device status word (DA_STATUS_* bits, 0
  * if clean) of the current device and clear it; negative DA_ERR_CUDA on

@@ -30,7 +30,8 @@ __all__ = [
     "DA_STATUS_BAD_SEQ_LEN", "DA_STATUS_BAD_PAGE", "DA_STATUS_TIMEOUT", "DA_STATUS_BAD_POSITION",
     "decode_attn_paged_rope", "decode_attn_ring_rope", "decode_attn_paged_fp8", "decode_attn_ring_fp8",
     "decode_attn_paged_multi", "decode_attn_ring_multi", "decode_attn_multi_workspace_bytes",
-    "decode_attn_multi_reserve", "decode_attn_multi_launches",
+    "decode_attn_multi_reserve", "decode_attn_multi_launches", "decode_attn_test_expire_wait",
+    "decode_attn_paged_fp8_rope", "decode_attn_ring_fp8_rope",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -91,6 +92,11 @@ def load_library():
                                           da_shape, c_int, c_int, c_int, c_int, vp]
     lib.decode_attn_ring_fp8.argtypes = [vp, vp, vp, vp, i32p, f32p, c_int, c_float, vp, da_shape,
                                          vp]
+    lib.decode_attn_paged_fp8_rope.argtypes = [vp, vp, vp, vp, i32p, i32p, f32p, f32p, f32p,
+                                               c_int, c_int, c_float, vp, da_shape, c_int, c_int,
+                                               c_int, c_int, vp]
+    lib.decode_attn_ring_fp8_rope.argtypes = [vp, vp, vp, vp, i32p, f32p, f32p, f32p, c_int, c_int,
+                                              c_float, vp, da_shape, vp]
     lib.decode_attn_paged_multi.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, i32p, f32p, c_int,
                                             c_float, vp, da_shape, c_int, c_int, c_int, c_int,
                                             c_int, vp]
@@ -105,12 +111,15 @@ def load_library():
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
     lib.decode_attn_device_status.argtypes = [vp]
+    lib.decode_attn_test_expire_wait.argtypes = [c_int]
     lib.decode_attn_error_string.argtypes = [c_int]
     lib.decode_attn_error_string.restype = ctypes.c_char_p
     for fn in (lib.decode_attn_paged, lib.decode_attn_ring, lib.kv_append, lib.decode_attn_reserve,
                lib.decode_attn_device_status, lib.decode_attn_paged_rope, lib.decode_attn_ring_rope,
                lib.decode_attn_paged_fp8, lib.decode_attn_ring_fp8, lib.decode_attn_paged_multi,
-               lib.decode_attn_ring_multi, lib.decode_attn_multi_reserve):
+               lib.decode_attn_ring_multi, lib.decode_attn_multi_reserve,
+               lib.decode_attn_test_expire_wait, lib.decode_attn_paged_fp8_rope,
+               lib.decode_attn_ring_fp8_rope):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -232,6 +241,39 @@ def decode_attn_ring_fp8(q, k_new, v_new, kv_cache, seq_lens, sinks, scale, out,
     return out
 
 
+def decode_attn_paged_fp8_rope(q, k_new, v_new, kv_cache, block_table, seq_lens, sinks, rope_cos,
+                               rope_sin, window, scale, out, max_seq_len=None, stream=None):
+    """decode_attn_paged_fp8 with the rotary embedding of position L - 1 applied to q and
+    k_new first (the key before it is quantised); rope_cos/rope_sin fp32 [max_position, 32]."""
+    num_pages, Hkv, nb = kv_cache.shape
+    if nb != FP8_BLOCK_BYTES:
+        raise ValueError(f"kv_cache blocks must be {FP8_BLOCK_BYTES} bytes, got {nb}")
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * 16
+    lib = load_library()
+    _check(lib.decode_attn_paged_fp8_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(sinks), _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]), int(window),
+        float(scale), _ptr(out), _shape(q, Hkv), 16, max_pages, num_pages, int(max_seq_len),
+        _stream(stream)))
+    return out
+
+
+def decode_attn_ring_fp8_rope(q, k_new, v_new, kv_cache, seq_lens, sinks, rope_cos, rope_sin, scale,
+                              out, stream=None):
+    """decode_attn_ring_fp8 with the rotary embedding of position L - 1 applied first."""
+    B, Hkv, nblk, nb = kv_cache.shape
+    if nb != FP8_BLOCK_BYTES:
+        raise ValueError(f"kv_cache blocks must be {FP8_BLOCK_BYTES} bytes, got {nb}")
+    lib = load_library()
+    _check(lib.decode_attn_ring_fp8_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _ptr(seq_lens), _ptr(sinks),
+        _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]), int(nblk * 16), float(scale),
+        _ptr(out), _shape(q, Hkv), _stream(stream)))
+    return out
+
+
 def kv_append(k_new, v_new, k_cache, v_cache, seq_lens, block_table=None, stream=None):
     """Append alone: paged when block_table is given, else ring [B, Hkv, W, D]."""
     B, Hkv, D = k_new.shape
@@ -312,3 +354,9 @@ def decode_attn_device_status(stream=None) -> int:
     if rc < 0:
         _check(rc)
     return rc
+
+
+def decode_attn_test_expire_wait(tile: int):
+    """Testing aid: the next one-token attention call gives up at its first worker's tile
+    wait number `tile` (after the tile landed) as if the wait had expired; < 0 disarms."""
+    _check(load_library().decode_attn_test_expire_wait(int(tile)))

@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 #include <stdio.h>
@@ -79,7 +80,7 @@ template <int NT, bool ROPE, bool KV8, int CPS>
 __host__ __device__ constexpr int stages_for() {
     // fp8 tiles are half the size: more of them in flight for the same bytes; with two
     // CTAs per SM each gets half the shared memory
-    return KV8 ? (NT == 1 ? (CPS > 1 ? DA_STAGES_FP8_2CTA : 7) : 6)
+    return KV8 ? (NT == 1 ? (CPS > 1 ? DA_STAGES_FP8_2CTA : 7) : (ROPE ? 5 : 6))
                : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16);
 }
 #ifndef DA_PAIR_BF16
@@ -110,6 +111,11 @@ __host__ __device__ constexpr int stages_for() {
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
 #endif
+// The first kStages copies of a warp issued by several lanes at once
+#ifndef DA_PAR_FILL
+#define DA_PAR_FILL 0
+#endif
+
 constexpr int kMinTilesPerWorker = DA_MIN_TILES;
 constexpr int kTileBytes = kPage * kD * 2;  // 2048 B of K (or V) per tile
 // fp8 cache block: 16 tokens of one KV head, K codes [16][64], V codes transposed [64][16],
@@ -154,6 +160,9 @@ struct Params {
     // (sequence, KV head) over the units of CTA c / ngrp of a grid of gridDim.x / ngrp (the
     // CTAs of one unit range read the same tiles, all but the first from L2); 1 otherwise
     int ngrp;
+    // testing aid: worker 0 gives up at its first tile wait from this tile on (after the tile
+    // has landed), as if the wait had expired; -1 = never
+    int expire_at;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -323,10 +332,8 @@ __device__ __forceinline__ int find_seq(const int *pre, int B, int x) {
     return lo;
 }
 
-// Worker boundaries: worker w owns units [wstart(w), wstart(w+1)).
-__device__ __forceinline__ int wstart(long long w, long long U, long long nw) {
-    return static_cast<int>((w * U) / nw);
-}
+// Worker boundaries: worker w owns units [floor(w U / nw), floor((w + 1) U / nw)); the
+// worker owning unit x:
 __device__ __forceinline__ int worker_of(long long x, long long U, long long nw) {
     return static_cast<int>(((x + 1) * nw - 1) / U);
 }
@@ -524,7 +531,7 @@ struct SmemLayout {
     // rows go to registers straight from global memory)
     static constexpr int kQBytes = MT ? GP * kD * 2 : kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
     static constexpr int kWarpTileBytes = kStages * kStageBytes;  // the tiles of one warp
-    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 8 + (MT ? kMaxBatch : 0);
+    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 16 + (MT ? kMaxBatch : 0);
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
     static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
     static constexpr size_t meta = bars + static_cast<size_t>(kWarps) * kStages * 8;
@@ -582,8 +589,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
     int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
     int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
     int *s_winfo = s_wsum + kWarps;                                   // [kWarps][kWinfo]
-    int *s_flag = s_winfo + kWarps * kWinfo;                          // [8]
-    int *s_n = s_flag + 8;                                            // [B] new tokens (MT)
+    int *s_flag = s_winfo + kWarps * kWinfo;                          // [16]
+    int *s_n = s_flag + 16;                                           // [B] new tokens (MT)
     float *s_sink = reinterpret_cast<float *>(smem + Lay::sinks);     // [Hq], log2 units
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
@@ -675,8 +682,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (static_cast<long long>(cta) * kWarps >= nwork) return;  // whole CTA idle
     const long long wid = static_cast<long long>(cta) * kWarps + warp;
     const bool active = wid < nwork;
-    const int ua = active ? wstart(wid, U, nwork) : 0;
-    const int ue = active ? wstart(wid + 1, U, nwork) : 0;
+    // worker w starts at floor(w U / nwork) = w q + floor(w r / nwork) with U = q nwork + r:
+    // 32-bit arithmetic (w r < nwork^2 < 2^23)
+    const int nw32 = static_cast<int>(nwork);
+    const int q_nw = U / nw32, r_nw = U - q_nw * nw32;
+    auto wst = [&](int w) { return w * q_nw + (w * r_nw) / nw32; };
+    const int ua = active ? wst(static_cast<int>(wid)) : 0;
+    const int ue = active ? wst(static_cast<int>(wid) + 1) : 0;
     const int n_tiles = ue - ua;
 
     uint8_t *wbase = smem + warp * kWarpBytes;
@@ -706,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     int head_seg = -1, tail_seg = -1;
     int head_s0 = 0, head_s1 = 0, tail_s0 = 0, tail_s1 = 0;  // unit ranges of those segments
     bool failed = false;
+    bool slots_ok = true;  // false: a copy may still land in this warp's area (never read it)
 
     if (active) {
         __syncwarp();
@@ -817,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
             }
         };
 
-        if (kParIssue) {
+        if (kParIssue || DA_PAR_FILL) {
             issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0);
         } else {
             for (int j = 0; j < n_tiles && j < kStages; ++j) issue_n(j, 1, j);
@@ -1140,8 +1153,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
 
         int stg = 0;       // stage of tile i
         uint32_t ph = 0;   // parity of its barrier phase
+        const int expire_at = wid == 0 ? p.expire_at : -1;
         while (i < n_tiles) {
-            if (!mbar_wait_bounded(bar0 + 8 * stg, ph)) {
+            // the lanes decide together: a lane whose wait expired takes the whole warp out
+            const bool landed = mbar_wait_bounded(bar0 + 8 * stg, ph);
+            if (__any_sync(0xffffffffu, !landed) || (expire_at >= 0 && i >= expire_at)) {
                 failed = true;
                 break;
             }
@@ -1203,6 +1219,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     vnew = reinterpret_cast<const uint32_t *>(qs + GP * kD * 2 + kD * 2)[lane];
                 }
                 const int qrows = MT ? p.T * p.G : p.G;  // query rows (columns) of the group
+                // rotary cos / sin rows of the new token's position (staged with the segment)
+                const float *cr = reinterpret_cast<const float *>(qs + GP * kD * 2 + 4 * kD);
+                const float *sr = cr + kD / 2;
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     const int hq = n * 8 + (lane >> 2);  // slot row; query row r0g + hq
@@ -1213,8 +1232,18 @@ __global__ void __launch_bounds__(kThreads, CPS)
                             if constexpr (KV8) {
                                 // fp16 operands; k-step ks takes d = 16t + 4ks .. +3, the bytes
                                 // one lane reads from an fp8 K row (see the QK product)
-                                qf[n][ks][0] = bf16x2_to_f16x2(row[8 * (lane & 3) + 2 * ks]);
-                                qf[n][ks][1] = bf16x2_to_f16x2(row[8 * (lane & 3) + 2 * ks + 1]);
+                                const int wq = 8 * (lane & 3) + 2 * ks;  // word of elements 2wq, 2wq + 1
+                                uint32_t w0 = row[wq], w1 = row[wq + 1];
+                                if constexpr (ROPE) {
+                                    // rotated in bf16 before the conversion: the rotate-half partner
+                                    // of element e is e +- 32, the word 16 away in the same row
+                                    const int i0 = (2 * wq) & 31;
+                                    const bool first = wq < 16;
+                                    w0 = rope_half(w0, row[wq ^ 16], cr + i0, sr + i0, first);
+                                    w1 = rope_half(w1, row[(wq ^ 16) + 1], cr + i0 + 2, sr + i0 + 2, first);
+                                }
+                                qf[n][ks][0] = bf16x2_to_f16x2(w0);
+                                qf[n][ks][1] = bf16x2_to_f16x2(w1);
                             } else {
                                 qf[n][ks][0] = row[ks * 8 + (lane & 3)];
                                 qf[n][ks][1] = row[ks * 8 + 4 + (lane & 3)];
@@ -1232,19 +1261,20 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 if constexpr (ROPE) {
                     // rotary embedding of the new token (rotate-half pairs (i, i + 32)); each
                     // product and the sum/difference rounded to fp32, then to bf16 (nearest even)
-                    const float *cr = reinterpret_cast<const float *>(qs + GP * kD * 2 + 4 * kD);
-                    const float *sr = cr + kD / 2;
-                    // queries: the partner of element d (< 32) is d + 32, two k-steps further
+                    if constexpr (!KV8) {  // (fp8 tiles: the queries were rotated above)
+                        // queries: the partner of element d (< 32) is d + 32, two k-steps further
 #pragma unroll
-                    for (int n = 0; n < NT; ++n)
+                        for (int n = 0; n < NT; ++n)
 #pragma unroll
-                        for (int ks = 0; ks < 2; ++ks)
+                            for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
-                            for (int r = 0; r < 2; ++r) {
-                                const int d = ks * 16 + r * 8 + (lane & 3) * 2;
-                                rope_pair(qf[n][ks][r], qf[n][ks + 2][r], cr + d, sr + d);
-                            }
-                    if (do_append) {  // the new key: element 2*lane pairs with lane ^ 16
+                                for (int r = 0; r < 2; ++r) {
+                                    const int d = ks * 16 + r * 8 + (lane & 3) * 2;
+                                    rope_pair(qf[n][ks][r], qf[n][ks + 2][r], cr + d, sr + d);
+                                }
+                    }
+                    // the new key, rotated before it is stored (and, for fp8, quantised):
+                    if (do_append) {  // element 2*lane pairs with lane ^ 16
                         const uint32_t other = __shfl_xor_sync(0xffffffffu, knew, 16);
                         const int d = (2 * lane) & 31;
                         knew = rope_half(knew, other, cr + d, sr + d, lane < 16);
@@ -1273,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
             if (stg1 == kStages) { stg1 = 0; ph1 ^= 1u; }
             if constexpr (kPair) {
                 if (i + 1 < n_tiles && ua + i + 1 < seg_end_unit) {
-                    if (!mbar_wait_bounded(bar0 + 8 * stg1, ph1)) {
+                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar0 + 8 * stg1, ph1))) {
                         failed = true;
                         break;
                     }
@@ -1314,9 +1344,31 @@ __global__ void __launch_bounds__(kThreads, CPS)
         }
         if (failed) {
             flag_status(DA_STATUS_TIMEOUT);
-            // let the copies still in flight land before the buffers are reused
-            for (int j = i + 1; j < n_tiles && j < i + kStages; ++j)
-                mbar_wait_bounded(bar0 + 8 * (j % kStages), (j / kStages) & 1);
+            // let the copies still in flight (tiles i .. i + kStages - 1) land before the
+            // buffers are reused; if one of them never lands, the area is left alone
+            for (int j = i; j < n_tiles && j < i + kStages; ++j)
+                if (!mbar_wait_bounded(bar0 + 8 * (j % kStages), (j / kStages) & 1)) slots_ok = false;
+            // The call's output is garbage now, but the segments at both ends of this warp's
+            // range are still published (with empty states) exactly as a finished loop would
+            // publish them, so that every ticket is taken and the counters return to zero.
+            state_reset(st);
+            head = st;
+            auto seg_at = [&](int x, int &first, int &end) {
+                const int b = find_seq(s_pre, B, x);
+                const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
+                const int g = (x - s_pre[b]) / tiles;
+                first = s_pre[b] + g * tiles;
+                end = first + tiles;
+                return b * Hkv + g;
+            };
+            int f0, e0;
+            const int s_head = seg_at(ua, f0, e0);
+            const int s_tail = seg_at(ue - 1, seg_first_unit, seg_end_unit);
+            head_seg = (s_head != s_tail && f0 < ua) ? s_head : -1;
+            head_s0 = f0;
+            head_s1 = e0;
+            sb = s_tail / Hkv;
+            sgk = s_tail - sb * Hkv;
         }
         __syncwarp();
 
@@ -1335,13 +1387,14 @@ __global__ void __launch_bounds__(kThreads, CPS)
         }
         // partial states -> this warp's (drained) buffer area
         Slot<NT> *slots = reinterpret_cast<Slot<NT> *>(wbase);
-        if (head_seg >= 0) state_to_slot(head, &slots[0], lane);
-        if (tail_seg >= 0) state_to_slot(st, &slots[1], lane);
+        if (slots_ok && head_seg >= 0) state_to_slot(head, &slots[0], lane);
+        if (slots_ok && tail_seg >= 0) state_to_slot(st, &slots[1], lane);
     }
     if (lane == 0) {
         int *wi = s_winfo + warp * kWinfo;
         wi[0] = ua; wi[1] = ue; wi[2] = head_seg; wi[3] = tail_seg; wi[4] = active ? 1 : 0;
         wi[5] = head_s0; wi[6] = head_s1; wi[7] = tail_s0; wi[8] = tail_s1;
+        wi[9] = slots_ok ? 1 : 0;
     }
     __syncthreads();
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1349,10 +1402,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
     // ---- 4. merge segments shared between warps of this CTA (all threads take part)
     const long long cta_w0 = static_cast<long long>(cta) * kWarps;
     const long long cta_w1 = min(cta_w0 + kWarps, nwork);
-    const int R0 = wstart(cta_w0, U, nwork), R1 = wstart(cta_w1, U, nwork);
+    const int R0 = wst(static_cast<int>(cta_w0)), R1 = wst(static_cast<int>(cta_w1));
     const int nw_cta = static_cast<int>(cta_w1 - cta_w0);
-    // Segments shared by several warps: the first warp of this CTA touching one merges it
-    // (warps merge their segments concurrently). A segment that also crosses into another
+    // Segments shared by several warps: every warp of this CTA holding a state of one (warps
+    // wa .. wb, consecutive) merges a share of its columns, lane l taking dimensions 2l, 2l + 1
+    // of a column (conflict-free rows of the slots). A segment that also crosses into another
     // CTA becomes this CTA's fp32 partial; slot 0 if it holds the CTA's first unit, else 1.
     // fp32 partial slot k of the CTA with effective index c in this row group; the row
     // groups count their tickets apart
@@ -1360,99 +1414,108 @@ __global__ void __launch_bounds__(kThreads, CPS)
         return p.part + ((static_cast<size_t>(c) * ngrp + rgrp) * 2 + k) * kSlotFloats;
     };
     int *const counters = p.counters + static_cast<size_t>(rgrp) * B * Hkv;
-    bool wrote_partial = false;
     if (warp < nw_cta) {
         const int *wi = s_winfo + warp * kWinfo;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
             const int seg = wi[2 + which];
+            if (seg < 0) continue;
             const int s0 = wi[5 + 2 * which], s1 = wi[6 + 2 * which];
-            if (seg < 0 || !(warp == 0 || s0 >= wi[0])) continue;
-            int w_end = warp;
-            while (w_end + 1 < nw_cta && s_winfo[(w_end + 1) * kWinfo] < s1) ++w_end;
+            int wa = warp, wb = warp;  // ranges are contiguous: a neighbour holds seg iff it reaches past the boundary
+            while (wa > 0 && s_winfo[wa * kWinfo] > s0) --wa;
+            while (wb + 1 < nw_cta && s_winfo[(wb + 1) * kWinfo] < s1) ++wb;
+            const int k = wb - wa + 1, mine = warp - wa;
             const bool internal = s0 >= R0 && s1 <= R1;
             const int slot_k = s0 <= R0 ? 0 : 1;
             const int b = seg / Hkv, g = seg - b * Hkv;
-            if (!internal && lane == 0) {
+            if (!internal && warp == wa && lane == 0) {
                 s_flag[2 + slot_k] = seg;
                 s_flag[4 + 2 * slot_k] = s0;
                 s_flag[5 + 2 * slot_k] = s1;
             }
-            // lane -> (head n, 16 d values); the contributor loops issue independent loads
-            for (int item = lane; item < GP * 4; item += 32) {
-                const int n = item >> 2, d0 = (item & 3) * 16;
-                float M = -INFINITY;
-                for (int w = warp; w <= w_end; ++w) {
-                    const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
-                                         ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
-                    M = fmaxf(M, sl->m[n]);
-                }
-                const int qrows = MT ? p.T * p.G : p.G;  // valid query rows of the group
-                const int rn = r0g + n;                  // column n's query row
+            // lane c < k describes contributor wa + c: its slot (head or tail) and whether its
+            // area may be read (a warp whose copies never landed is skipped)
+            int my_off = 0;  // byte offset of the contributor's slot in shared memory
+            bool my_ok = false;
+            if (lane < k) {
+                const int w = wa + lane;
+                my_ok = s_winfo[w * kWinfo + 9] != 0;
+                my_off = w * kWarpBytes + ((s_winfo[w * kWinfo + 3] == seg) ? static_cast<int>(sizeof(Slot<NT>)) : 0);
+            }
+            const Slot<NT> *my_sl = reinterpret_cast<const Slot<NT> *>(smem + my_off);
+            const int qrows = MT ? p.T * p.G : p.G;  // valid query rows of the group
+#pragma unroll 1
+            for (int n = mine; n < GP; n += k) {
+                // (m, l) of every contributor at once, one per lane
+                const float mc = my_ok ? my_sl->m[n] : -INFINITY;
+                const float lc = my_ok ? my_sl->l[n] : 0.f;
+                float M = mc;  // (every lane ends with the maximum over the contributors)
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                const int rn = r0g + n;  // column n's query row
                 const float sg = (internal && rn < qrows) ? s_sink[g * p.G + (MT ? rn % p.G : rn)] : -INFINITY;
                 const float Mf = internal ? fmaxf(M, sg) : M;
-                float den = (internal && sg != -INFINITY) ? fast_exp2(sg - Mf) : 0.f;
-                float acc[16];
+                const float wc = mc == -INFINITY ? 0.f : fast_exp2(mc - Mf);  // no key: weight 0
+                float den = lc * wc;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-                for (int w = warp; w <= w_end; ++w) {
-                    const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + w * kWarpBytes) +
-                                         ((s_winfo[w * kWinfo + 3] == seg) ? 1 : 0);
-                    const float wgt = sl->m[n] == -INFINITY ? 0.f : fast_exp2(sl->m[n] - Mf);  // no key: weight 0
-                    den += sl->l[n] * wgt;
+                for (int off = 1; off < 32; off <<= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+                if (internal && sg != -INFINITY) den += fast_exp2(sg - Mf);
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[j] += sl->acc[n][d0 + j] * wgt;
+                for (int c = 0; c < kWarps; ++c) {
+                    const float w = __shfl_sync(0xffffffffu, wc, c);
+                    const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + __shfl_sync(0xffffffffu, my_off, c));
+                    if (c < k && w != 0.f) {
+                        const float2 a = *reinterpret_cast<const float2 *>(&sl->acc[n][2 * lane]);
+                        acc.x += a.x * w;
+                        acc.y += a.y * w;
+                    }
                 }
                 if (internal) {
                     if (rn < qrows) {
                         const int t = MT ? rn / p.G : 0, h = MT ? rn - t * p.G : rn;
                         const float inv = (MT && t >= s_n[b]) ? 0.f : 1.f / den;  // no query token: zeros
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD + d0);
-                        uint4 o0, o1;
-                        o0.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-                        o0.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-                        o0.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-                        o0.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-                        o1.x = pack_bf16(acc[8] * inv, acc[9] * inv);
-                        o1.y = pack_bf16(acc[10] * inv, acc[11] * inv);
-                        o1.z = pack_bf16(acc[12] * inv, acc[13] * inv);
-                        o1.w = pack_bf16(acc[14] * inv, acc[15] * inv);
-                        dst[0] = o0;
-                        dst[1] = o1;
+                        __nv_bfloat16 *dst =
+                            p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD;
+                        reinterpret_cast<uint32_t *>(dst)[lane] = pack_bf16(acc.x * inv, acc.y * inv);
                     }
                 } else {
                     float *gp = part_slot(cta, slot_k);
-                    if (d0 == 0) {
+                    if (lane == 0) {
                         gp[n] = M;
                         gp[GP + n] = den;
                     }
-                    float4 *ga = reinterpret_cast<float4 *>(gp + 2 * GP + n * kD + d0);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        ga[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-                    wrote_partial = true;
+                    reinterpret_cast<float2 *>(gp + 2 * GP + n * kD)[lane] = acc;
                 }
             }
         }
     }
-    if (wrote_partial) __threadfence();  // partials visible before the tickets below
+    // (no fence here: the ticket-taking thread's fence below publishes every thread's partials)
     __syncthreads();
 
     // ---- 5. segments shared with other CTAs: the last CTA to arrive combines them
     if (tid == 0) {
         const int cand0 = s_flag[2], cand1 = s_flag[3];
+        // the barrier above orders every thread's partial stores before this fence, which
+        // orders them (cumulatively, at GPU scope) before the tickets
+        if (cand0 >= 0 || cand1 >= 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
         // both tickets in flight together
         const int t0 = cand0 >= 0 ? atomicAdd(counters + cand0, 1) : 0;
         const int t1 = cand1 >= 0 ? atomicAdd(counters + cand1, 1) : 0;
-        auto last_of = [&](int seg, int ticket, int s0, int s1) {
+        // the CTAs contributing to segment k (first c_lo, count) and the slot of the first
+        // one, for the combine below: s_flag[8 + 3k ..]
+        auto last_of = [&](int k, int seg, int ticket, int s0, int s1) {
             if (seg < 0) return -1;
             const int c_lo = worker_of(s0, U, nwork) / kWarps;
             const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+            s_flag[8 + 3 * k] = c_lo;
+            s_flag[9 + 3 * k] = c_hi - c_lo + 1;
+            // the first contributing CTA may have started before this segment (its slot 1)
+            s_flag[10 + 3 * k] = wst(c_lo * kWarps) < s0 ? 1 : 0;
             return ticket == c_hi - c_lo ? seg : -1;
         };
-        s_flag[0] = last_of(cand0, t0, s_flag[4], s_flag[5]);
-        s_flag[1] = last_of(cand1, t1, s_flag[6], s_flag[7]);
+        s_flag[0] = last_of(0, cand0, t0, s_flag[4], s_flag[5]);
+        s_flag[1] = last_of(1, cand1, t1, s_flag[6], s_flag[7]);
         if (s_flag[0] >= 0 || s_flag[1] >= 0) __threadfence();
     }
     __syncthreads();
@@ -1464,12 +1527,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     for (int k = 0; k < 2; ++k) {
         const int seg = s_flag[k];
         if (seg < 0) continue;
-        const int s0 = s_flag[4 + 2 * k], s1 = s_flag[5 + 2 * k];
-        const int c_lo = worker_of(s0, U, nwork) / kWarps;
-        const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
-        const int nc = c_hi - c_lo + 1;
-        // the first contributing CTA may have started before this segment (its slot 1)
-        const int lo_slot = (wstart(static_cast<long long>(c_lo) * kWarps, U, nwork) < s0) ? 1 : 0;
+        const int c_lo = s_flag[8 + 3 * k], nc = s_flag[9 + 3 * k], lo_slot = s_flag[10 + 3 * k];
         const int b = seg / Hkv, g = seg - b * Hkv;
         float M = -INFINITY, den = 0.f, acc[kPer];
 #pragma unroll
@@ -1658,14 +1716,17 @@ bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices, i
 
 constexpr int kMaxDevices = 64;
 
+// Per-device state. The workspace pointers change only under g_mu; the SM count and the
+// "kernel attribute set" flags are caches that several host threads may fill at once (with
+// the same values), so they are atomics.
 struct DeviceState {
     void *ws = nullptr;
     size_t ws_bytes = 0;
     void *ws_multi = nullptr;  // multi-token calls: counters + split partials
     size_t ws_multi_bytes = 0;
-    int sm_count = 0;
-    bool attr_set[64] = {};
-    bool multi_attr_set[8] = {};
+    std::atomic<int> sm_count{0};
+    std::atomic<bool> attr_set[64] = {};
+    std::atomic<bool> multi_attr_set[8] = {};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -1678,12 +1739,12 @@ int current_device(int *dev) {
 }
 
 int sm_count(int dev) {
-    if (g_dev[dev].sm_count == 0) {
-        int n = 0;
+    int n = g_dev[dev].sm_count.load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-        g_dev[dev].sm_count = n;
+        g_dev[dev].sm_count.store(n, std::memory_order_relaxed);
     }
-    return g_dev[dev].sm_count;
+    return n;
 }
 
 size_t slot_floats(int G) {
@@ -1740,11 +1801,11 @@ int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm,
     const size_t smem_max = smem;
     auto kern = decode_attn_kernel<NT, RING, ROPE, KV8, CPS, MT>;
     const int idx = (MT ? 32 : 0) + (CPS - 1) * 16 + (NT - 1) * 8 + (RING ? 4 : 0) + (ROPE ? 2 : 0) + (KV8 ? 1 : 0);
-    if (!g_dev[dev].attr_set[idx]) {
+    if (!g_dev[dev].attr_set[idx].load(std::memory_order_acquire)) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
         if (e != cudaSuccess) return set_cuda_error(e);
-        g_dev[dev].attr_set[idx] = true;
+        g_dev[dev].attr_set[idx].store(true, std::memory_order_release);
     }
     // Programmatic dependent launch: the grid may start (and run its input-free set-up)
     // while the previous kernel of the stream drains; it waits for that kernel before
@@ -1782,6 +1843,10 @@ int prepare_workspace(int dev, int G, cudaStream_t stream, float **part, int **c
     return DA_OK;
 }
 
+// Testing aid (decode_attn_test_expire_wait): the tile wait at which the next one-token
+// call's first worker gives up; -1 = none. Taken (and cleared) by that call.
+std::atomic<int> g_expire_next{-1};
+
 int run_attention(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                   const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
                   float scale, void *out, const da_shape &s, int page_size, int max_pages, int num_pages,
@@ -1796,7 +1861,6 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
         return DA_ERR_INVALID_ARG;
     if (!(scale == scale)) return DA_ERR_INVALID_ARG;
     if ((rope_cos == nullptr) != (rope_sin == nullptr)) return DA_ERR_INVALID_ARG;
-    if (kv8 && rope_cos) return DA_ERR_UNSUPPORTED;
     if (kv8 && ring && window % kPage != 0) return DA_ERR_UNSUPPORTED;
     if (rope_cos && (max_position <= 0 || !aligned16(rope_cos) || !aligned16(rope_sin))) return DA_ERR_INVALID_ARG;
     const int G = s.num_q_heads / s.num_kv_heads;
@@ -1840,6 +1904,7 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.T = 1;
     prm.q_lens = nullptr;
     prm.ngrp = 1;
+    prm.expire_at = g_expire_next.exchange(-1);
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
@@ -1867,12 +1932,22 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
                 per_seq = (span + kPage - 1) / kPage + 1;
             }
             const bool two = static_cast<long long>(s.batch) * s.num_kv_heads * per_seq >= DA_FP8_2CTA_MIN_TILES;
+            if (rope_cos != nullptr) {
+                if (two)
+                    return ring ? launch_attn<1, true, true, true, 2>(mk, mv, prm, dev, stream)
+                                : launch_attn<1, false, true, true, 2>(mk, mv, prm, dev, stream);
+                return ring ? launch_attn<1, true, true, true>(mk, mv, prm, dev, stream)
+                            : launch_attn<1, false, true, true>(mk, mv, prm, dev, stream);
+            }
             if (two)
                 return ring ? launch_attn<1, true, false, true, 2>(mk, mv, prm, dev, stream)
                             : launch_attn<1, false, false, true, 2>(mk, mv, prm, dev, stream);
             return ring ? launch_attn<1, true, false, true>(mk, mv, prm, dev, stream)
                         : launch_attn<1, false, false, true>(mk, mv, prm, dev, stream);
         }
+        if (rope_cos != nullptr)
+            return ring ? launch_attn<2, true, true, true>(mk, mv, prm, dev, stream)
+                        : launch_attn<2, false, true, true>(mk, mv, prm, dev, stream);
         return ring ? launch_attn<2, true, false, true>(mk, mv, prm, dev, stream)
                     : launch_attn<2, false, false, true>(mk, mv, prm, dev, stream);
     }
@@ -2119,6 +2194,7 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         dp.T = T;
         dp.q_lens = q_lens;
         dp.ngrp = m.row_blocks;
+        dp.expire_at = -1;
         CUtensorMap mk, mv;
         const uint64_t slices = static_cast<uint64_t>(num_pages) * s.num_kv_heads;
         if (!make_kv_map(&mk, k_cache, kPage, slices) || !make_kv_map(&mv, v_cache, kPage, slices)) {
@@ -2170,13 +2246,13 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
                              : (ring ? multi_attn_kernel<true, kMWarps> : multi_attn_kernel<false, kMWarps>);
     const int smem = m.tc ? kTcSmem : small ? MultiShape<2>::kSmem : MultiShape<kMWarps>::kSmem;
     const int aidx = (ring ? 1 : 0) + (m.tc ? 2 : 0) + (small ? 4 : 0);
-    if (!g_dev[dev].multi_attr_set[aidx]) {
+    if (!g_dev[dev].multi_attr_set[aidx].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)  // room for as many resident CTAs as the registers allow
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return set_cuda_error(e);
-        g_dev[dev].multi_attr_set[aidx] = true;
+        g_dev[dev].multi_attr_set[aidx].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(m.splits * m.row_blocks), static_cast<unsigned>(s.num_kv_heads),
@@ -2192,11 +2268,11 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mk, mv, nk, nv, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e);
-    if (m.defer) {  // the fold of the split partials, over (16-row slices, KV heads, sequences)
+    if (m.defer) {  // the fold of the split partials: one warp per query row
         cudaLaunchConfig_t cc = {};
-        cc.gridDim = dim3(static_cast<unsigned>(m.row_blocks * ((m.rows + kCombSliceRows - 1) / kCombSliceRows)),
+        cc.gridDim = dim3(static_cast<unsigned>(m.row_blocks * ((m.rows + kCombWarps - 1) / kCombWarps)),
                           static_cast<unsigned>(s.num_kv_heads), static_cast<unsigned>(s.batch));
-        cc.blockDim = dim3(128);
+        cc.blockDim = dim3(kCombWarps * 32);
         cc.dynamicSmemBytes = 0;
         cc.stream = stream;
         cc.attrs = attr;
@@ -2235,10 +2311,15 @@ void *g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per 
 std::mutex g_noalloc_mu;
 
 // The array's name means nothing to host code; its device address is looked up once
-// per device, with that device current.
-int noalloc_scratch(int dev, void **addr) {
+// per device, with that device current. The lookup may load the module on the device, so
+// a first call made while `stream` is capturing a graph is refused (DA_ERR_WORKSPACE).
+int noalloc_scratch(int dev, cudaStream_t stream, void **addr) {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_addr[dev] == nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+        if (ce != cudaSuccess) return set_cuda_error(ce);
+        if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
         void *ptr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) return set_cuda_error(e);
@@ -2270,10 +2351,10 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     rc = current_device(&dev);
     if (rc != DA_OK) return rc;
     if (sm_count(dev) > kNoAllocMaxCtas) return DA_ERR_SCRATCH_LIMIT;
-    void *scratch = nullptr;
-    rc = noalloc_scratch(dev, &scratch);
-    if (rc != DA_OK) return rc;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    void *scratch = nullptr;
+    rc = noalloc_scratch(dev, stream, &scratch);
+    if (rc != DA_OK) return rc;
 
     Params prm;
     prm.q = static_cast<const __nv_bfloat16 *>(q);
@@ -2300,6 +2381,7 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.T = 1;
     prm.q_lens = nullptr;
     prm.ngrp = 1;
+    prm.expire_at = -1;
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call
@@ -2373,6 +2455,26 @@ int decode_attn_ring_fp8(const void *q, const void *k_new, const void *v_new, vo
                          da_shape s, void *stream) {
     return run_attention(true, q, k_new, v_new, kv_cache, nullptr, nullptr, seq_lens, sinks, window, scale, out,
                          s, kPage, 0, 0, 0, stream, nullptr, nullptr, 0, true);
+}
+
+int decode_attn_paged_fp8_rope(const void *q, const void *k_new, const void *v_new, void *kv_cache,
+                               const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                               const float *rope_cos, const float *rope_sin, int max_position, int window,
+                               float scale, void *out, da_shape s, int page_size, int max_pages_per_seq,
+                               int num_pages, int max_seq_len, void *stream) {
+    if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
+    return run_attention(false, q, k_new, v_new, kv_cache, nullptr, block_table, seq_lens, sinks, window, scale,
+                         out, s, page_size, max_pages_per_seq, num_pages, max_seq_len, stream, rope_cos, rope_sin,
+                         max_position, true);
+}
+
+int decode_attn_ring_fp8_rope(const void *q, const void *k_new, const void *v_new, void *kv_cache,
+                              const int32_t *seq_lens, const float *sinks, const float *rope_cos,
+                              const float *rope_sin, int max_position, int window, float scale, void *out,
+                              da_shape s, void *stream) {
+    if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
+    return run_attention(true, q, k_new, v_new, kv_cache, nullptr, nullptr, seq_lens, sinks, window, scale, out,
+                         s, kPage, 0, 0, 0, stream, rope_cos, rope_sin, max_position, true);
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, const int32_t *block_table,
@@ -2460,6 +2562,11 @@ int decode_attn_reserve(size_t bytes) {
     if (rc != DA_OK) return rc;
     std::lock_guard<std::mutex> lk(g_mu);
     return reserve_locked(dev, bytes);
+}
+
+int decode_attn_test_expire_wait(int tile) {
+    g_expire_next.store(tile < 0 ? -1 : tile);
+    return DA_OK;
 }
 
 int decode_attn_device_status(void *stream) {

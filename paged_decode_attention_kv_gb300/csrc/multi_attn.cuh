@@ -573,25 +573,92 @@ __global__ void __launch_bounds__(NW * 32, MultiShape<NW>::kMinBlocks)
 }
 
 // Calls whose row blocks are split over many CTAs fold the partials in a kernel of their own,
-// after the attention kernel: one CTA of 4 warps per 16 rows of a row block, so the fold runs
-// on many SMs at once instead of in the one CTA per row block that arrives last (which would
-// read every split's partial of all the block's rows alone).
-constexpr int kCombSliceRows = 16;
-__global__ void __launch_bounds__(128) multi_combine_kernel(const MultiParams p, int RB, int ring) {
+// after the attention kernel, so the fold runs on many SMs at once instead of in the one CTA
+// per row block that arrives last. One warp per query row, one lane per split (lanes take
+// splits l, l + 32, ...): each lane merges its splits' (m, l) online, the warp merges the
+// lanes' maxima and sums, then each lane adds up its splits' weighted accumulators (64
+// values) and the warp sums them over the lanes through shared memory (a padded 32 x 64
+// transpose), so a row costs about three dependent L2 round trips however many splits.
+constexpr int kCombWarps = 4;  // query rows per CTA
+__global__ void __launch_bounds__(kCombWarps * 32) multi_combine_kernel(const MultiParams p, int RB, int ring) {
+    __shared__ float s_sum[kCombWarps][32][kD + 1];
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials of the attention kernel
-    const int slices = (RB + kCombSliceRows - 1) / kCombSliceRows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slices = (RB + kCombWarps - 1) / kCombWarps;
     const int rb = blockIdx.x / slices, sl = blockIdx.x - rb * slices;
     const int g = blockIdx.y, b = blockIdx.z;
     const int r0 = rb * RB, r_end = min(r0 + RB, p.T * p.G);
-    const int rl_lo = sl * kCombSliceRows;
-    if (r0 + rl_lo >= r_end) return;
+    if (r0 + sl * kCombWarps >= r_end) return;
     const MultiKeys k = multi_keys(p, ring != 0, b, r0, r_end);
     const int nsplit = (k.ntiles + p.chunk - 1) / p.chunk;
     if (nsplit <= 1) return;  // the attention kernel wrote these rows (or their zeros)
+    const int rl = sl * kCombWarps + warp;  // this warp's row of the block
+    const int r = r0 + rl;
+    if (rl >= RB || r >= r_end) return;  // no barrier follows: warps leave on their own
+    const int t = r / p.G, hl = r - t * p.G;
+    __nv_bfloat16 *out = p.out + ((static_cast<size_t>(b) * p.T + t) * p.Hq + g * p.G + hl) * kD;
+    if (t >= k.n) {  // not a query row: zeros
+        reinterpret_cast<uint32_t *>(out)[lane] = 0u;
+        return;
+    }
     const size_t bg = static_cast<size_t>(b) * p.Hkv + g;
-    const size_t slot0 = ((bg * p.row_blocks + rb) * p.splits) * static_cast<size_t>(RB);
-    multi_combine_rows(p, p.part + slot0 * kMSlotFloats, RB, r0, r_end, k.n, b, g, nsplit, rl_lo,
-                       min(RB, rl_lo + kCombSliceRows), threadIdx.x >> 5, blockDim.x >> 5, threadIdx.x & 31);
+    const float *all = p.part + ((bg * p.row_blocks + rb) * p.splits) * static_cast<size_t>(RB) * kMSlotFloats;
+    auto slot = [&](int sp) { return all + (static_cast<size_t>(sp) * RB + rl) * kMSlotFloats; };
+    // (m, l) of this lane's splits, merged online
+    float M = -INFINITY, den = 0.f;
+    for (int sp = lane; sp < nsplit; sp += 32) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(slot(sp)));
+        if (ml.x == -INFINITY) continue;  // a split that saw no key of the row
+        const float Mn = fmaxf(M, ml.x);
+        den = den * exp2f(M - Mn) + ml.y * exp2f(ml.x - Mn);
+        M = Mn;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+        const float Do = __shfl_xor_sync(0xffffffffu, den, off);
+        const float Mn = fmaxf(M, Mo);
+        den = Mn == -INFINITY ? 0.f : den * exp2f(M - Mn) + Do * exp2f(Mo - Mn);
+        M = Mn;
+    }
+    const float sg = p.sinks != nullptr ? __ldg(p.sinks + g * p.G + hl) * kLog2e : -INFINITY;
+    const float Mf = fmaxf(M, sg);  // the same on every lane: an exact maximum
+    float inv = 0.f;
+    if (Mf != -INFINITY) {
+        const float d = den * exp2f(M - Mf) + (sg == -INFINITY ? 0.f : exp2f(sg - Mf));
+        inv = d > 0.f ? 1.f / d : 0.f;
+    }
+    // this lane's splits' weighted accumulators
+    float o[kD];
+#pragma unroll
+    for (int d = 0; d < kD; ++d) o[d] = 0.f;
+    if (Mf != -INFINITY) {
+        for (int sp = lane; sp < nsplit; sp += 32) {
+            const float *s = slot(sp);
+            const float m = __ldcg(s);
+            const float w = m == -INFINITY ? 0.f : exp2f(m - Mf);
+            const float4 *a4 = reinterpret_cast<const float4 *>(s + kMAccOff);
+#pragma unroll
+            for (int c = 0; c < kD / 4; ++c) {
+                const float4 a = __ldcg(a4 + c);
+                o[4 * c] += a.x * w;
+                o[4 * c + 1] += a.y * w;
+                o[4 * c + 2] += a.z * w;
+                o[4 * c + 3] += a.w * w;
+            }
+        }
+    }
+    // the sum over the lanes: lane l writes its 64 values as row l, then sums columns 2l, 2l + 1
+#pragma unroll
+    for (int d = 0; d < kD; ++d) s_sum[warp][lane][d] = o[d];
+    __syncwarp();
+    float x0 = 0.f, x1 = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+        x0 += s_sum[warp][j][2 * lane];
+        x1 += s_sum[warp][j][2 * lane + 1];
+    }
+    reinterpret_cast<uint32_t *>(out)[lane] = pack_bf16(x0 * inv, x1 * inv);
 }
 
 // The append of a multi-token step: new token t < n of b goes to position L - n + t. In a

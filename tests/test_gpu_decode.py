@@ -256,18 +256,6 @@ def full_workload(name, device=DEV):
     return cfg, lens, inp, pool, ring
 
 
-def sample_items(lens, Hq, n, seed):
-    rng = np.random.default_rng(seed)
-    active = [b for b, L in enumerate(lens) if L > 0]
-    items = {(int(b), int(h)) for b, h in zip(rng.choice(active, n), rng.integers(0, Hq, n))}
-    longest = int(np.argmax(lens))
-    items |= {(longest, h) for h in range(0, Hq, 7)}
-    inactive = [b for b, L in enumerate(lens) if L == 0]
-    if inactive:
-        items.add((inactive[0], 0))
-    return sorted(items)
-
-
 @pytest.mark.parametrize("name", ["b1", "b64", "long1", "long8", "serve"])
 def test_full_size_workload(name):
     cfg, lens, inp, pool, ring = full_workload(name)
@@ -280,12 +268,11 @@ def test_full_size_workload(name):
                          inp.scale, out)
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
-    items = sample_items(lens, Hq, 48, 11)
+    # every output row against the oracle (well under a second of host time per workload)
     ref = oracle.decode_paged(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), k_pre, v_pre,
                               pool.block_table.cpu().numpy(), np.asarray(lens, np.int32),
-                              inp.sinks.numpy(), 0, inp.scale, cfg["page_size"], items=items)
-    got = out.double().cpu().numpy()
-    assert_close(np.stack([got[b, h] for b, h in items]), ref, f"{name} paged")
+                              inp.sinks.numpy(), 0, inp.scale, cfg["page_size"])
+    assert_close(out.double().cpu().numpy(), ref, f"{name} paged")
     ek, ev = oracle.kv_append_paged(wl.bits(inp.k_new), wl.bits(inp.v_new), k_pre, v_pre,
                                     pool.block_table.cpu().numpy(), np.asarray(lens, np.int32))
     assert np.array_equal(wl.bits(pool.k_cache), ek) and np.array_equal(wl.bits(pool.v_cache), ev)
@@ -296,10 +283,8 @@ def test_full_size_workload(name):
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
     ref = oracle.decode_ring(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), rk_pre,
-                             rv_pre, np.asarray(lens, np.int32), inp.sinks.numpy(), W, inp.scale,
-                             items=items)
-    got = out.double().cpu().numpy()
-    assert_close(np.stack([got[b, h] for b, h in items]), ref, f"{name} ring")
+                             rv_pre, np.asarray(lens, np.int32), inp.sinks.numpy(), W, inp.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"{name} ring")
     ek, ev = oracle.kv_append_ring(wl.bits(inp.k_new), wl.bits(inp.v_new), rk_pre, rv_pre,
                                    np.asarray(lens, np.int32), W)
     assert np.array_equal(wl.bits(ring.k_cache), ek) and np.array_equal(wl.bits(ring.v_cache), ev)
@@ -346,16 +331,13 @@ def test_cuda_graph_capture_and_replay_with_new_lengths():
     g.replay()
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
-    items = sample_items(new_lens.tolist(), Hq, 48, 13)
     ref = oracle.decode_paged(wl.bits(new.q), wl.bits(new.k_new), wl.bits(new.v_new), k_pre,
                               v_pre, bt_new.numpy(), new_lens, inp.sinks.numpy(), 0, inp.scale,
-                              cfg["page_size"], items=items)
-    got = out_p.double().cpu().numpy()
-    assert_close(np.stack([got[b, h] for b, h in items]), ref, "graph paged")
+                              cfg["page_size"])
+    assert_close(out_p.double().cpu().numpy(), ref, "graph paged")
     ref = oracle.decode_ring(wl.bits(new.q), wl.bits(new.k_new), wl.bits(new.v_new), rk_pre,
-                             rv_pre, new_lens, inp.sinks.numpy(), W, inp.scale, items=items)
-    got = out_r.double().cpu().numpy()
-    assert_close(np.stack([got[b, h] for b, h in items]), ref, "graph ring")
+                             rv_pre, new_lens, inp.sinks.numpy(), W, inp.scale)
+    assert_close(out_r.double().cpu().numpy(), ref, "graph ring")
     for b in np.nonzero(new_lens == 0)[0][:4]:
         assert torch.all(out_p[b] == 0) and torch.all(out_r[b] == 0)
 

@@ -11,7 +11,7 @@ import oracle
 import paged_decode_attention_kv_gb300 as da
 from cases import make_case, paged_identity, shuffle_pages
 from paged_decode_attention_kv_gb300 import workloads as wl
-from test_gpu_decode import DEV, assert_close, dev, dev_bits, sample_items
+from test_gpu_decode import DEV, assert_close, dev, dev_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -104,7 +104,7 @@ def test_paged_fp8_many_segments_across_ctas():
 
 @pytest.mark.parametrize("name", ["b64", "long1"])
 def test_full_size_fp8(name):
-    """Benchmark-size fp8 pools of random codes and scales; sampled heads against the
+    """Benchmark-size fp8 pools of random codes and scales; every output row against the
     oracle, the appended rows and scales bit-exact."""
     cfg = wl.config(name)
     lens = wl.seq_lens(name)
@@ -123,11 +123,9 @@ def test_full_size_fp8(name):
                              dev(inp.sinks), 0, inp.scale, out)
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
-    items = sample_items(lens, Hq, 32, 13)
     ref = oracle.decode_paged_fp8(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), before,
-                                  bt.numpy(), sl, inp.sinks.numpy(), 0, inp.scale, items=items)
-    got = out.double().cpu().numpy()
-    assert_close(np.stack([got[b, h] for b, h in items]), ref, f"{name} paged fp8")
+                                  bt.numpy(), sl, inp.sinks.numpy(), 0, inp.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"{name} paged fp8")
     want = oracle.kv_append_fp8(wl.bits(inp.k_new), wl.bits(inp.v_new), before, sl,
                                 block_table=bt.numpy())
     assert_blocks_equal(from_dev(pool), want)
@@ -236,3 +234,80 @@ def test_fp8_cuda_graph_capture_and_replay():
     assert_close(out_r.double().cpu().numpy(), ref_r, "graph fp8 ring")
     assert_blocks_equal(from_dev(kv), oracle.kv_append_fp8(c2.k_new, c2.v_new, cache2, c2.lens, block_table=bt2))
     assert_blocks_equal(from_dev(rv), oracle.kv_append_fp8(c2.k_new, c2.v_new, ring2, c2.lens, window=128))
+
+
+# ---------------------------------------------------------------- fp8 cache with the fused RoPE
+def _tables(maxpos):
+    cs, sn = wl.rope_tables(maxpos, 64)
+    return cs, sn
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (64, 4), (8, 8)])
+@pytest.mark.parametrize("window", [0, 100])
+def test_paged_fp8_rope_matches_oracle(Hq, Hkv, window):
+    """q and the new key rotated to position L - 1, the key rotated before it is quantised;
+    the appended block bytes bit-exact against quantise(rope_k(k_new))."""
+    c = make_case(760 + Hq + Hkv + window, len(EDGE), Hq, Hkv, 64, EDGE)
+    kp, vp, bt = shuffle_pages(*paged_identity(c, pre(c)), window + 2, spare=4)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c),
+                               oracle.Fp8Cache.empty_paged(kp.shape[0], c.Hkv, 16, c.D), block_table=bt)
+    cs, sn = _tables(int(c.lens.max()) + 3)
+    kv = to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_paged_fp8_rope(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kv, dev(bt),
+                                  dev(c.lens), dev(c.sinks), dev(cs), dev(sn), window, c.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_paged_fp8_rope(c.q, c.k_new, c.v_new, cache, bt, c.lens, c.sinks, cs, sn,
+                                       window, c.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"paged fp8 rope window={window}")
+    krot = oracle.rope_k(c.k_new, c.lens, cs, sn)
+    assert_blocks_equal(from_dev(kv), oracle.kv_append_fp8(krot, c.v_new, cache, c.lens, block_table=bt))
+
+
+@pytest.mark.parametrize("W", [16, 128])
+def test_ring_fp8_rope_matches_oracle(W):
+    lens = [1, 15, 16, 17, W - 1, W, W + 1, 3 * W + 5, 0]
+    c = make_case(780 + W, len(lens), 64, 8, 64, lens)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, pre(c), oracle.Fp8Cache.empty_ring(c.B, c.Hkv, W, c.D),
+                               window=W)
+    cs, sn = _tables(int(c.lens.max()) + 1)
+    kv = to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_ring_fp8_rope(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), kv, dev(c.lens),
+                                 dev(c.sinks), dev(cs), dev(sn), c.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_ring_fp8_rope(c.q, c.k_new, c.v_new, cache, c.lens, c.sinks, cs, sn, W, c.scale)
+    assert_close(out.double().cpu().numpy(), ref, f"ring fp8 rope W={W}")
+    krot = oracle.rope_k(c.k_new, c.lens, cs, sn)
+    assert_blocks_equal(from_dev(kv), oracle.kv_append_fp8(krot, c.v_new, cache, c.lens, window=W))
+
+
+def test_full_size_fp8_rope_two_ctas_per_sm():
+    """The batch-64 workload on fp8 blocks with the RoPE: large enough for the two-CTA grid."""
+    name = "b64"
+    cfg = wl.config(name)
+    lens = wl.seq_lens(name)
+    gen = wl.cpu_generator(cfg["seed"] + 5)
+    vgen = torch.Generator(device=DEV)
+    vgen.manual_seed(cfg["seed"] + 5)
+    B, Hq, Hkv, D, P = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["page_size"]
+    inp = wl.draw_decode_inputs(B, Hq, Hkv, D, lens, gen)
+    npages = wl.pool_size(name, lens)
+    bt = wl.draw_block_table(lens, P, npages, wl.max_pages_per_seq(name, lens), gen)
+    pool = wl.draw_fp8_paged_pool(npages, Hkv, P, D, vgen, device=DEV)
+    before = from_dev(pool)
+    cs, sn = _tables(max(lens) + 1)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
+    sl = np.asarray(lens, np.int32)
+    da.decode_attn_paged_fp8_rope(dev(inp.q), dev(inp.k_new), dev(inp.v_new), pool, dev(bt), dev(sl),
+                                  dev(inp.sinks), dev(cs), dev(sn), 0, inp.scale, out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_paged_fp8_rope(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), before,
+                                       bt.numpy(), sl, inp.sinks.numpy(), cs, sn, 0, inp.scale)
+    assert_close(out.double().cpu().numpy(), ref, "b64 paged fp8 rope")
+    krot = oracle.rope_k(wl.bits(inp.k_new), sl, cs, sn)
+    assert_blocks_equal(from_dev(pool), oracle.kv_append_fp8(krot, wl.bits(inp.v_new), before, sl,
+                                                             block_table=bt.numpy()))

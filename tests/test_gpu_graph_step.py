@@ -9,7 +9,7 @@ import oracle
 from paged_decode_attention_kv_gb300 import decode_attn_paged, decode_attn_ring
 from paged_decode_attention_kv_gb300 import workloads as wl
 from paged_decode_attention_kv_gb300.graph import DecodeStepGraph
-from test_gpu_decode import DEV, assert_close, dev, sample_items
+from test_gpu_decode import DEV, assert_close, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -61,17 +61,15 @@ def test_one_graph_serves_every_active_slot_set():
         pre = [(wl.bits(kc), wl.bits(vc)) for _, kc, vc in layers]
         step.replay()
         torch.cuda.synchronize()
-        items = sample_items(lens.tolist(), Hq, 24, 100 + replay)
         for li, (kind, kc, vc) in enumerate(layers):
             kpre, vpre = pre[li]
             if kind == "full":
                 ref = oracle.decode_paged(wl.bits(new.q), wl.bits(new.k_new), wl.bits(new.v_new), kpre,
                                           vpre, bt_new.numpy(), lens, sinks.cpu().numpy(), 0, wl.SCALE,
-                                          P, items=items)
+                                          P)
             else:
                 ref = oracle.decode_ring(wl.bits(new.q), wl.bits(new.k_new), wl.bits(new.v_new), kpre,
-                                         vpre, lens, sinks.cpu().numpy(), W, wl.SCALE, items=items)
-            got = outs[li].double().cpu().numpy()
-            assert_close(np.stack([got[b, h] for b, h in items]), ref, f"replay {replay} layer {li}")
+                                         vpre, lens, sinks.cpu().numpy(), W, wl.SCALE)
+            assert_close(outs[li].double().cpu().numpy(), ref, f"replay {replay} layer {li}")
         for b in np.nonzero(lens == 0)[0][:3]:
             assert all(torch.all(o[b] == 0) for o in outs)

@@ -10,7 +10,7 @@ import oracle
 import paged_decode_attention_kv_gb300 as da
 from paged_decode_attention_kv_gb300 import workloads as wl
 from cases import make_case, paged_identity, ring_from_history, shuffle_pages
-from test_gpu_decode import DEV, assert_close, dev, dev_bits, full_workload, pre, sample_items
+from test_gpu_decode import DEV, assert_close, dev, dev_bits, full_workload, pre
 
 pytestmark = pytest.mark.gpu
 
@@ -107,13 +107,10 @@ def test_full_size_workload_with_rope(name):
                               dev(cs), dev(sn), 0, inp.scale, out)
     torch.cuda.synchronize()
     assert da.decode_attn_device_status() == 0
-    items = sample_items(lens, Hq, 32, 17)
     ref = oracle.decode_paged_rope(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), k_pre,
                                    v_pre, pool.block_table.cpu().numpy(), np.asarray(lens, np.int32),
-                                   inp.sinks.numpy(), cs, sn, 0, inp.scale, cfg["page_size"],
-                                   items=items)
-    got = out.double().cpu().numpy()
-    assert_close(np.stack([got[b, h] for b, h in items]), ref, f"{name} paged rope")
+                                   inp.sinks.numpy(), cs, sn, 0, inp.scale, cfg["page_size"])
+    assert_close(out.double().cpu().numpy(), ref, f"{name} paged rope")
     krot = oracle.rope_k(wl.bits(inp.k_new), np.asarray(lens, np.int32), cs, sn)
     ek, _ = oracle.kv_append_paged(krot, wl.bits(inp.v_new), k_pre, v_pre,
                                    pool.block_table.cpu().numpy(), np.asarray(lens, np.int32))

@@ -4,10 +4,13 @@ It exists for callers that cannot allocate device memory when they run decode
 attention (a runtime that hands out all GPU memory from its own pool, a plugin
 host that forbids cudaMalloc, code that must not risk the synchronisation an
 allocation can cause): its scratch lives in a fixed array inside the library.
-This test calls it through the C ABI and checks it against decode_attn_paged,
-which uses the library workspace, on two calls in a row (the second call finds
-the array as the first one left it). It is in a file of its own, named to be
-collected last, and it passes in a fresh process as well as after the others.
+These tests call it through the C ABI, twice in a row on the same inputs (the
+second call finds the array as the first one left it), and check every output
+row against the fp64 oracle and against decode_attn_paged, which uses the
+library workspace. The cases cover 8- and 16-head query groups, full attention
+and a 128-token window, and a shape exactly at the array's limit of 4096
+(sequence, KV head) pairs. The file is named to be collected last; it passes in a
+fresh process as well as after the other tests.
 """
 import ctypes
 
@@ -15,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_decode_attention_kv_gb300 as da
 from paged_decode_attention_kv_gb300 import workloads as wl
 
@@ -22,6 +26,7 @@ pytestmark = pytest.mark.gpu
 
 ATOL, RTOL = 4e-3, 1e-2
 DA_ERR_SCRATCH_LIMIT = -5
+P = 16
 
 
 def _entry():
@@ -40,48 +45,79 @@ def _p(t):
 
 def _call_noalloc(fn, q, kn, vn, kc, vc, bt, sl, sk, window, scale, out):
     B, Hq, D = q.shape
-    num_pages, Hkv, P, _ = kc.shape
+    num_pages, Hkv, page, _ = kc.shape
     maxp = bt.shape[1]
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return fn(_p(q), _p(kn), _p(vn), _p(kc), _p(vc), _p(bt), _p(sl), _p(sk), window, scale,
-              _p(out), da.da_shape(B, Hq, Hkv, D), P, maxp, num_pages, maxp * P, stream)
+              _p(out), da.da_shape(B, Hq, Hkv, D), page, maxp, num_pages, maxp * page, stream)
 
 
-def _inputs(lens, seed):
-    B, Hq, Hkv, D, P = len(lens), 64, 8, 64, 16
+def _inputs(lens, seed, Hq, Hkv, D=64):
+    B = len(lens)
     gen = wl.cpu_generator(seed)
     vgen = torch.Generator(device="cuda")
     vgen.manual_seed(seed)
     inp = wl.draw_decode_inputs(B, Hq, Hkv, D, lens, gen)
     npages = sum(wl.pages_needed(L, P) for L in lens) + 8
-    maxp = max(wl.pages_needed(L, P) for L in lens)
+    maxp = max(1, max(wl.pages_needed(L, P) for L in lens))
     pool = wl.draw_paged_pool(npages, Hkv, P, D, lens, maxp, gen, device="cuda", value_gen=vgen)
-    d = lambda t: t.to("cuda").contiguous()
-    return (d(inp.q), d(inp.k_new), d(inp.v_new), pool.k_cache, pool.v_cache, pool.block_table,
-            d(inp.seq_lens), d(inp.sinks), inp.scale)
+    return inp, pool
 
 
-def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
-    fn = _entry()
+def _close(got, want, what):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    excess = np.abs(got - want) - (ATOL + RTOL * np.abs(want))
+    assert excess.max() <= 0, f"{what}: worst excess {excess.max():.3e}"
+
+
+def _lens_mixed():
     # long sequences split across many CTAs (partials + tickets in the scratch), short ones
     # finished inside one warp, an inactive slot
-    lens = [3000, 17000, 40, 0, 9000, 1]
-    q, kn, vn, kc, vc, bt, sl, sk, scale = _inputs(lens, 7)
+    return [3000, 17000, 40, 0, 9000, 1]
+
+
+def _lens_at_limit():
+    # 512 slots x 8 KV heads = 4096 (sequence, KV head) pairs, the most the array holds
+    rng = np.random.default_rng(31)
+    lens = [int(x) for x in rng.integers(1, 300, size=512)]
+    lens[7], lens[300], lens[511] = 5000, 0, 2500
+    return lens
+
+
+@pytest.mark.parametrize("lens_fn,Hq,Hkv,window", [
+    (_lens_mixed, 64, 8, 0),
+    (_lens_mixed, 64, 8, 128),
+    (_lens_mixed, 64, 4, 0),      # 16 query heads per KV head: the widest partial slot
+    (_lens_mixed, 64, 4, 128),
+    (_lens_at_limit, 64, 8, 0),
+])
+def test_noalloc_matches_oracle_and_workspace_entry_on_two_calls(lens_fn, Hq, Hkv, window):
+    fn = _entry()
+    lens = lens_fn()
+    inp, pool = _inputs(lens, 7 + Hkv + window, Hq, Hkv)
+    d = lambda t: t.to("cuda").contiguous()
+    q, kn, vn, sl, sk = d(inp.q), d(inp.k_new), d(inp.v_new), d(inp.seq_lens), d(inp.sinks)
+    kc, vc, bt = pool.k_cache, pool.v_cache, pool.block_table
+    k_pre, v_pre = wl.bits(kc), wl.bits(vc)
+    bt_h, sl_h = bt.cpu().numpy(), np.asarray(lens, np.int32)
+    want = oracle.decode_paged(wl.bits(inp.q), wl.bits(inp.k_new), wl.bits(inp.v_new), k_pre, v_pre,
+                               bt_h, sl_h, inp.sinks.numpy(), window, inp.scale, P)
+    ek, ev = oracle.kv_append_paged(wl.bits(inp.k_new), wl.bits(inp.v_new), k_pre, v_pre, bt_h, sl_h)
+    # the workspace entry point on its own copy of the caches
     ref = torch.empty_like(q)
-    da.decode_attn_paged(q, kn, vn, kc, vc, bt, sl, sk, 0, scale, ref)
+    da.decode_attn_paged(q, kn, vn, kc.clone(), vc.clone(), bt, sl, sk, window, inp.scale, ref)
     torch.cuda.synchronize()
-    k_after, v_after = kc.clone(), vc.clone()
+    ref = ref.double().cpu().numpy()
     for call in range(2):
         out = torch.full_like(q, float("nan"))
-        rc = _call_noalloc(fn, q, kn, vn, kc, vc, bt, sl, sk, 0, scale, out)
+        rc = _call_noalloc(fn, q, kn, vn, kc, vc, bt, sl, sk, window, inp.scale, out)
         assert rc == 0, da.decode_attn_error_string(rc)
         torch.cuda.synchronize()
-        got, want = out.double().cpu().numpy(), ref.double().cpu().numpy()
-        assert np.all(np.isfinite(got)), f"call {call}: non-finite output"
-        excess = np.abs(got - want) - (ATOL + RTOL * np.abs(want))
-        assert excess.max() <= 0, f"call {call}: worst excess {excess.max():.3e}"
-        # the fused append wrote the same cells as the workspace entry point did
-        assert torch.equal(kc, k_after) and torch.equal(vc, v_after)
+        got = out.double().cpu().numpy()
+        _close(got, want, f"call {call} vs oracle")
+        _close(got, ref, f"call {call} vs decode_attn_paged")
+        # the fused append wrote exactly the oracle's cells (the second call rewrites them)
+        assert np.array_equal(wl.bits(kc), ek) and np.array_equal(wl.bits(vc), ev)
     assert da.decode_attn_device_status() == 0
 
 
