@@ -277,6 +277,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ void flag_status(unsigned bits) { atomicOr(&g_status, bits); }
 
+// Shared-memory loads by address (of data that is no longer written while they run)
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
 __device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v));
 }
@@ -330,6 +342,16 @@ __device__ __forceinline__ int find_seq(const int *pre, int B, int x) {
         if (pre[mid] <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// The segment (b Hkv + g) holding unit x and its unit range [first, end).
+__device__ __forceinline__ int segment_of_unit(const int *pre, int B, int Hkv, int x, int &first, int &end) {
+    const int b = find_seq(pre, B, x);
+    const int tiles = (pre[b + 1] - pre[b]) / Hkv;
+    const int g = (x - pre[b]) / tiles;
+    first = pre[b] + g * tiles;
+    end = first + tiles;
+    return b * Hkv + g;
 }
 
 // Worker boundaries: worker w owns units [floor(w U / nw), floor((w + 1) U / nw)); the
@@ -718,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     int head_seg = -1, tail_seg = -1;
     int head_s0 = 0, head_s1 = 0, tail_s0 = 0, tail_s1 = 0;  // unit ranges of those segments
     bool failed = false;
-    bool slots_ok = true;  // false: a copy may still land in this warp's area (never read it)
+    bool slots_ok = true;  // false after an expired wait: this warp's area is never read or written again
 
     if (active) {
         __syncwarp();
@@ -1344,31 +1366,14 @@ __global__ void __launch_bounds__(kThreads, CPS)
         }
         if (failed) {
             flag_status(DA_STATUS_TIMEOUT);
-            // let the copies still in flight (tiles i .. i + kStages - 1) land before the
-            // buffers are reused; if one of them never lands, the area is left alone
+            // let the copies still in flight (tiles i .. i + kStages - 1) land before the CTA
+            // moves on; the warp's area is then neither written nor read again (its states are
+            // left out of the merges: the call's output is garbage). The tickets do not depend
+            // on this warp: the CTA's boundary segments come from the unit prefix, so the
+            // counters still return to zero.
             for (int j = i; j < n_tiles && j < i + kStages; ++j)
-                if (!mbar_wait_bounded(bar0 + 8 * (j % kStages), (j / kStages) & 1)) slots_ok = false;
-            // The call's output is garbage now, but the segments at both ends of this warp's
-            // range are still published (with empty states) exactly as a finished loop would
-            // publish them, so that every ticket is taken and the counters return to zero.
-            state_reset(st);
-            head = st;
-            auto seg_at = [&](int x, int &first, int &end) {
-                const int b = find_seq(s_pre, B, x);
-                const int tiles = (s_pre[b + 1] - s_pre[b]) / Hkv;
-                const int g = (x - s_pre[b]) / tiles;
-                first = s_pre[b] + g * tiles;
-                end = first + tiles;
-                return b * Hkv + g;
-            };
-            int f0, e0;
-            const int s_head = seg_at(ua, f0, e0);
-            const int s_tail = seg_at(ue - 1, seg_first_unit, seg_end_unit);
-            head_seg = (s_head != s_tail && f0 < ua) ? s_head : -1;
-            head_s0 = f0;
-            head_s1 = e0;
-            sb = s_tail / Hkv;
-            sgk = s_tail - sb * Hkv;
+                mbar_wait_bounded(bar0 + 8 * (j % kStages), (j / kStages) & 1);
+            slots_ok = false;
         }
         __syncwarp();
 
@@ -1405,8 +1410,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int R0 = wst(static_cast<int>(cta_w0)), R1 = wst(static_cast<int>(cta_w1));
     const int nw_cta = static_cast<int>(cta_w1 - cta_w0);
     // Segments shared by several warps: every warp of this CTA holding a state of one (warps
-    // wa .. wb, consecutive) merges a share of its columns, lane l taking dimensions 2l, 2l + 1
-    // of a column (conflict-free rows of the slots). A segment that also crosses into another
+    // wa .. wb, consecutive) merges a share of it. A segment that also crosses into another
     // CTA becomes this CTA's fp32 partial; slot 0 if it holds the CTA's first unit, else 1.
     // fp32 partial slot k of the CTA with effective index c in this row group; the row
     // groups count their tickets apart
@@ -1421,74 +1425,128 @@ __global__ void __launch_bounds__(kThreads, CPS)
             const int seg = wi[2 + which];
             if (seg < 0) continue;
             const int s0 = wi[5 + 2 * which], s1 = wi[6 + 2 * which];
-            int wa = warp, wb = warp;  // ranges are contiguous: a neighbour holds seg iff it reaches past the boundary
-            while (wa > 0 && s_winfo[wa * kWinfo] > s0) --wa;
-            while (wb + 1 < nw_cta && s_winfo[(wb + 1) * kWinfo] < s1) ++wb;
+            // the warps of this CTA holding a state of seg, wa .. wb: ranges are contiguous and
+            // ordered, so warp w < warp holds it iff its range ends after s0, and w > warp iff
+            // its range starts before s1 (independent loads, no chain)
+            int wa = 0, wb = warp;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                if (w < warp && s_winfo[w * kWinfo + 1] <= s0) ++wa;
+                if (w > warp && w < nw_cta && s_winfo[w * kWinfo] < s1) ++wb;
+            }
             const int k = wb - wa + 1, mine = warp - wa;
             const bool internal = s0 >= R0 && s1 <= R1;
             const int slot_k = s0 <= R0 ? 0 : 1;
             const int b = seg / Hkv, g = seg - b * Hkv;
-            if (!internal && warp == wa && lane == 0) {
-                s_flag[2 + slot_k] = seg;
-                s_flag[4 + 2 * slot_k] = s0;
-                s_flag[5 + 2 * slot_k] = s1;
-            }
-            // lane c < k describes contributor wa + c: its slot (head or tail) and whether its
-            // area may be read (a warp whose copies never landed is skipped)
-            int my_off = 0;  // byte offset of the contributor's slot in shared memory
-            bool my_ok = false;
-            if (lane < k) {
-                const int w = wa + lane;
-                my_ok = s_winfo[w * kWinfo + 9] != 0;
-                my_off = w * kWarpBytes + ((s_winfo[w * kWinfo + 3] == seg) ? static_cast<int>(sizeof(Slot<NT>)) : 0);
-            }
-            const Slot<NT> *my_sl = reinterpret_cast<const Slot<NT> *>(smem + my_off);
+            // The segment's GP x 4 items (a column and 16 of its dimensions) are shared out over
+            // the lanes of its k warps; a lane loads its item from every contributor at once
+            // (contributor c is warp wa + c, its slot the head or the tail one; a warp whose
+            // copies never landed is skipped), four contributors per round.
+            const uint32_t slots_base = smem_addr(smem);
             const int qrows = MT ? p.T * p.G : p.G;  // valid query rows of the group
 #pragma unroll 1
-            for (int n = mine; n < GP; n += k) {
-                // (m, l) of every contributor at once, one per lane
-                const float mc = my_ok ? my_sl->m[n] : -INFINITY;
-                const float lc = my_ok ? my_sl->l[n] : 0.f;
-                float M = mc;  // (every lane ends with the maximum over the contributors)
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            for (int item = mine * 32 + lane; item < GP * 4; item += k * 32) {
+                const int n = item >> 2, d0 = (item & 3) * 16;
                 const int rn = r0g + n;  // column n's query row
                 const float sg = (internal && rn < qrows) ? s_sink[g * p.G + (MT ? rn % p.G : rn)] : -INFINITY;
-                const float Mf = internal ? fmaxf(M, sg) : M;
-                const float wc = mc == -INFINITY ? 0.f : fast_exp2(mc - Mf);  // no key: weight 0
-                float den = lc * wc;
+                float M = -INFINITY, den = 0.f;
+                float acc[16];
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-                if (internal && sg != -INFINITY) den += fast_exp2(sg - Mf);
-                float2 acc = make_float2(0.f, 0.f);
+                for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < k; c0 += 4) {
+                    float mc[4], lc[4];
+                    float4 a[4][4];
 #pragma unroll
-                for (int c = 0; c < kWarps; ++c) {
-                    const float w = __shfl_sync(0xffffffffu, wc, c);
-                    const Slot<NT> *sl = reinterpret_cast<const Slot<NT> *>(smem + __shfl_sync(0xffffffffu, my_off, c));
-                    if (c < k && w != 0.f) {
-                        const float2 a = *reinterpret_cast<const float2 *>(&sl->acc[n][2 * lane]);
-                        acc.x += a.x * w;
-                        acc.y += a.y * w;
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = c0 + u, w = wa + (c < k ? c : 0);
+                        const bool ok = c < k && s_winfo[w * kWinfo + 9] != 0;
+                        const uint32_t sl = slots_base + w * kWarpBytes +
+                                            ((s_winfo[w * kWinfo + 3] == seg) ? static_cast<uint32_t>(sizeof(Slot<NT>)) : 0u);
+                        mc[u] = ok ? lds_f32(sl + 4 * n) : -INFINITY;
+                        lc[u] = ok ? lds_f32(sl + 4 * (GP + n)) : 0.f;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            a[u][q] = ok ? lds_f32x4(sl + 4 * (2 * GP + n * Slot<NT>::LD + d0 + 4 * q))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
+                    float Mn = M;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) Mn = fmaxf(Mn, mc[u]);
+                    const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // rescale the rounds before
+                    den *= r;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] *= r;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float w = mc[u] == -INFINITY ? 0.f : fast_exp2(mc[u] - Mn);  // no key: weight 0
+                        den += lc[u] * w;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            acc[4 * q] += a[u][q].x * w;
+                            acc[4 * q + 1] += a[u][q].y * w;
+                            acc[4 * q + 2] += a[u][q].z * w;
+                            acc[4 * q + 3] += a[u][q].w * w;
+                        }
+                    }
+                    M = Mn;
                 }
-                if (internal) {
+                if (internal) {  // sink, normalise, bf16
+                    const float Mf = fmaxf(M, sg);
+                    const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mf);
+                    den = den * r + (sg == -INFINITY ? 0.f : fast_exp2(sg - Mf));
                     if (rn < qrows) {
                         const int t = MT ? rn / p.G : 0, h = MT ? rn - t * p.G : rn;
-                        const float inv = (MT && t >= s_n[b]) ? 0.f : 1.f / den;  // no query token: zeros
-                        __nv_bfloat16 *dst =
-                            p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD;
-                        reinterpret_cast<uint32_t *>(dst)[lane] = pack_bf16(acc.x * inv, acc.y * inv);
+                        const float inv = (MT && t >= s_n[b]) ? 0.f : r / den;  // no query token: zeros
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD + d0);
+                        uint4 o0, o1;
+                        o0.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                        o0.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                        o0.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+                        o0.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+                        o1.x = pack_bf16(acc[8] * inv, acc[9] * inv);
+                        o1.y = pack_bf16(acc[10] * inv, acc[11] * inv);
+                        o1.z = pack_bf16(acc[12] * inv, acc[13] * inv);
+                        o1.w = pack_bf16(acc[14] * inv, acc[15] * inv);
+                        dst[0] = o0;
+                        dst[1] = o1;
                     }
-                } else {
+                } else {  // this CTA's fp32 partial of the segment
                     float *gp = part_slot(cta, slot_k);
-                    if (lane == 0) {
+                    if (d0 == 0) {
                         gp[n] = M;
                         gp[GP + n] = den;
                     }
-                    reinterpret_cast<float2 *>(gp + 2 * GP + n * kD)[lane] = acc;
+                    float4 *ga = reinterpret_cast<float4 *>(gp + 2 * GP + n * kD + d0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        ga[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
                 }
             }
         }
+    }
+    // Meanwhile the last thread works out this CTA's segments shared with other CTAs from the
+    // unit prefix alone: the one holding its first unit (partial slot 0) and the one holding
+    // its last unit (slot 1), and for each the contributing CTAs (first, count) and the slot
+    // of the first one: s_flag[2..7] and s_flag[8 + 3k ..]
+    if (tid == kThreads - 1) {
+        int f, e;
+        const int sa = segment_of_unit(s_pre, B, Hkv, R0, f, e);
+        auto shared_seg = [&](int k, int seg, int s0, int s1) {
+            s_flag[2 + k] = seg;
+            s_flag[4 + 2 * k] = s0;
+            s_flag[5 + 2 * k] = s1;
+            const int c_lo = worker_of(s0, U, nwork) / kWarps;
+            const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+            s_flag[8 + 3 * k] = c_lo;
+            s_flag[9 + 3 * k] = c_hi - c_lo + 1;
+            // the first contributing CTA may have started before this segment (its slot 1)
+            s_flag[10 + 3 * k] = wst(c_lo * kWarps) < s0 ? 1 : 0;
+        };
+        if (f < R0 || e > R1) shared_seg(0, sa, f, e);
+        const int sz = segment_of_unit(s_pre, B, Hkv, R1 - 1, f, e);
+        if (sz != sa && e > R1) shared_seg(1, sz, f, e);
     }
     // (no fence here: the ticket-taking thread's fence below publishes every thread's partials)
     __syncthreads();
@@ -1502,26 +1560,18 @@ __global__ void __launch_bounds__(kThreads, CPS)
         // both tickets in flight together
         const int t0 = cand0 >= 0 ? atomicAdd(counters + cand0, 1) : 0;
         const int t1 = cand1 >= 0 ? atomicAdd(counters + cand1, 1) : 0;
-        // the CTAs contributing to segment k (first c_lo, count) and the slot of the first
-        // one, for the combine below: s_flag[8 + 3k ..]
-        auto last_of = [&](int k, int seg, int ticket, int s0, int s1) {
-            if (seg < 0) return -1;
-            const int c_lo = worker_of(s0, U, nwork) / kWarps;
-            const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
-            s_flag[8 + 3 * k] = c_lo;
-            s_flag[9 + 3 * k] = c_hi - c_lo + 1;
-            // the first contributing CTA may have started before this segment (its slot 1)
-            s_flag[10 + 3 * k] = wst(c_lo * kWarps) < s0 ? 1 : 0;
-            return ticket == c_hi - c_lo ? seg : -1;
-        };
-        s_flag[0] = last_of(0, cand0, t0, s_flag[4], s_flag[5]);
-        s_flag[1] = last_of(1, cand1, t1, s_flag[6], s_flag[7]);
-        if (s_flag[0] >= 0 || s_flag[1] >= 0) __threadfence();
+        // the CTA taking the last ticket of a segment combines it
+        s_flag[0] = (cand0 >= 0 && t0 == s_flag[9] - 1) ? cand0 : -1;
+        s_flag[1] = (cand1 >= 0 && t1 == s_flag[12] - 1) ? cand1 : -1;
+        // the other CTAs' partials, ordered before their tickets, are visible after this fence
+        if (s_flag[0] >= 0 || s_flag[1] >= 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
     __syncthreads();
     // One pass, no barrier: every thread owns kPer outputs of one head and folds the
-    // partials in batches of 8 contributors whose loads are all in flight together.
+    // partials in batches of kCombBatch contributors whose loads are all in flight together
+    // (a 131k-token sequence spread over every CTA has about 20 per KV head: one round trip).
     constexpr int kPer = GP * kD / kThreads;  // outputs per thread: 2 (G <= 8) or 4 (G = 16)
+    constexpr int kCombBatch = CPS > 1 ? 8 : 24;  // (the 128-register two-CTA kernel: 8)
     const int cn = tid / (kD / kPer), cd0 = (tid % (kD / kPer)) * kPer;
 #pragma unroll 1
     for (int k = 0; k < 2; ++k) {
@@ -1533,10 +1583,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
 #pragma unroll
         for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < nc; c0 += 8) {
-            float mc[8], lc[8], v[8][kPer];
+        for (int c0 = 0; c0 < nc; c0 += kCombBatch) {
+            float mc[kCombBatch], lc[kCombBatch], v[kCombBatch][kPer];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kCombBatch; ++j) {
                 mc[j] = -INFINITY;
                 lc[j] = 0.f;
 #pragma unroll
@@ -1557,13 +1607,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
             }
             float Mn = M;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mc[j]);
+            for (int j = 0; j < kCombBatch; ++j) Mn = fmaxf(Mn, mc[j]);
             const float a = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // 0 on the first batch (M = -inf)
             den *= a;
 #pragma unroll
             for (int t = 0; t < kPer; ++t) acc[t] *= a;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kCombBatch; ++j) {
                 const float w = mc[j] == -INFINITY ? 0.f : fast_exp2(mc[j] - Mn);  // 0: padding, or no key
                 den += lc[j] * w;
 #pragma unroll
