@@ -117,6 +117,12 @@ __host__ __device__ constexpr int stages_for() {
 #endif
 
 constexpr int kMinTilesPerWorker = DA_MIN_TILES;
+// CTA boundaries move to the nearer edge of a segment of at most this many units (and of at
+// most a worker's share), so that short segments are not split between CTAs
+#ifndef DA_SNAP_UNITS
+#define DA_SNAP_UNITS 32
+#endif
+constexpr int kSnapUnits = DA_SNAP_UNITS;
 constexpr int kTileBytes = kPage * kD * 2;  // 2048 B of K (or V) per tile
 // fp8 cache block: 16 tokens of one KV head, K codes [16][64], V codes transposed [64][16],
 // K scales [16] and V scales [16] (fp32)
@@ -594,8 +600,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
     constexpr bool kParIssue = KV8 ? DA_PAR_ISSUE_FP8 : DA_PAR_ISSUE_BF16;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    // the 1024-byte aligned base, derived from the shared array itself so that every access
+    // through it compiles to a shared-memory instruction (not a generic one)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     // the unit split runs over ncta CTAs; this CTA is number cta of row group rgrp, whose
     // columns are the query rows r0g .. r0g + GP - 1 of each (sequence, KV head)
@@ -703,14 +710,31 @@ __global__ void __launch_bounds__(kThreads, CPS)
             static_cast<long long>((U + kMinTilesPerWorker - 1) / kMinTilesPerWorker));
     if (static_cast<long long>(cta) * kWarps >= nwork) return;  // whole CTA idle
     const long long wid = static_cast<long long>(cta) * kWarps + warp;
-    const bool active = wid < nwork;
-    // worker w starts at floor(w U / nwork) = w q + floor(w r / nwork) with U = q nwork + r:
-    // 32-bit arithmetic (w r < nwork^2 < 2^23)
+    // Two levels. CTA c takes the units from cta_start(c): worker c kWarps's start in an even
+    // split over all nwork workers, floor(w U / nwork) = w q + floor(w r / nwork) with
+    // U = q nwork + r (32-bit: w r < nwork^2 < 2^23), moved to the nearer edge of the segment
+    // it falls in when that segment is at most a worker's share (and kSnapUnits) long: a
+    // segment that short is then never shared between CTAs, which would cost it a partial, a
+    // ticket and a combine (more than the few tiles of imbalance). The CTA's warps split its
+    // range evenly.
     const int nw32 = static_cast<int>(nwork);
     const int q_nw = U / nw32, r_nw = U - q_nw * nw32;
     auto wst = [&](int w) { return w * q_nw + (w * r_nw) / nw32; };
-    const int ua = active ? wst(static_cast<int>(wid)) : 0;
-    const int ue = active ? wst(static_cast<int>(wid) + 1) : 0;
+    const int snap_max = min(kSnapUnits, q_nw);
+    auto cta_start = [&](int c) {
+        const int x = wst(min(c * kWarps, nw32));
+        if (x <= 0 || x >= U) return x;
+        int f, e;
+        segment_of_unit(s_pre, B, Hkv, x, f, e);
+        if (x == f || e - f > snap_max) return x;
+        return (x - f <= e - x) ? f : e;
+    };
+    const int nw_cta = min(kWarps, nw32 - cta * kWarps);  // active warps of this CTA
+    const bool active = warp < nw_cta;
+    const int R0 = cta_start(cta), R1 = cta_start(cta + 1);  // this CTA's units
+    const int q_w = (R1 - R0) / nw_cta, r_w = (R1 - R0) - q_w * nw_cta;
+    const int ua = active ? R0 + warp * q_w + (warp * r_w) / nw_cta : 0;
+    const int ue = active ? R0 + (warp + 1) * q_w + ((warp + 1) * r_w) / nw_cta : 0;
     const int n_tiles = ue - ua;
 
     uint8_t *wbase = smem + warp * kWarpBytes;
@@ -1405,10 +1429,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 4. merge segments shared between warps of this CTA (all threads take part)
-    const long long cta_w0 = static_cast<long long>(cta) * kWarps;
-    const long long cta_w1 = min(cta_w0 + kWarps, nwork);
-    const int R0 = wst(static_cast<int>(cta_w0)), R1 = wst(static_cast<int>(cta_w1));
-    const int nw_cta = static_cast<int>(cta_w1 - cta_w0);
     // Segments shared by several warps: every warp of this CTA holding a state of one (warps
     // wa .. wb, consecutive) merges a share of it. A segment that also crosses into another
     // CTA becomes this CTA's fp32 partial; slot 0 if it holds the CTA's first unit, else 1.
@@ -1533,16 +1553,22 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (tid == kThreads - 1) {
         int f, e;
         const int sa = segment_of_unit(s_pre, B, Hkv, R0, f, e);
+        const int n_cta = (nw32 + kWarps - 1) / kWarps;  // CTAs with work
+        auto cta_of = [&](int x) {  // the CTA whose range holds unit x: near the even split's
+            int c = worker_of(x, U, nwork) / kWarps;
+            while (c > 0 && cta_start(c) > x) --c;
+            while (c + 1 < n_cta && cta_start(c + 1) <= x) ++c;
+            return c;
+        };
         auto shared_seg = [&](int k, int seg, int s0, int s1) {
             s_flag[2 + k] = seg;
             s_flag[4 + 2 * k] = s0;
             s_flag[5 + 2 * k] = s1;
-            const int c_lo = worker_of(s0, U, nwork) / kWarps;
-            const int c_hi = worker_of(s1 - 1, U, nwork) / kWarps;
+            const int c_lo = cta_of(s0), c_hi = cta_of(s1 - 1);
             s_flag[8 + 3 * k] = c_lo;
             s_flag[9 + 3 * k] = c_hi - c_lo + 1;
             // the first contributing CTA may have started before this segment (its slot 1)
-            s_flag[10 + 3 * k] = wst(c_lo * kWarps) < s0 ? 1 : 0;
+            s_flag[10 + 3 * k] = cta_start(c_lo) < s0 ? 1 : 0;
         };
         if (f < R0 || e > R1) shared_seg(0, sa, f, e);
         const int sz = segment_of_unit(s_pre, B, Hkv, R1 - 1, f, e);

@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(NW * 32, MultiShape<NW>::kMinBlocks)
                       const MultiParams p) {
     constexpr int kMStages = MultiShape<NW>::kStages;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    // the 1024-byte aligned base, derived from the shared array itself so that every access
+    // through it compiles to a shared-memory instruction (not a generic one)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t tiles_s = smem_addr(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kMStages * kMStageBytes);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kMStages);

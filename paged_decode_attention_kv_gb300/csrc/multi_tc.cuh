@@ -124,8 +124,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const __grid_constant__ CUtensorMap tnk, const __grid_constant__ CUtensorMap tnv,
                     const MultiParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    // the 1024-byte aligned base, derived from the shared array itself so that every access
+    // through it compiles to a shared-memory instruction (not a generic one)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;                                  // [128 rows][128 B], 128-byte swizzle
     uint8_t *sKV = smem + kTcQBytes;                     // [stage][K block | V block]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sKV + kTcStages * kTcStageBytes);

@@ -1,0 +1,136 @@
+"""CPU model of the one-token kernel's work split (host logic, no GPU), checked for the
+invariants the kernel relies on: the units (one 16-token tile of one (sequence, KV head)
+segment) are ordered (b, g, tile); CTA c takes [cta_start(c), cta_start(c + 1)), the even
+split's boundary moved to the nearer edge of a short segment; its warps split that range
+evenly. Every unit belongs to exactly one warp, every working CTA and warp has at least one
+unit, a segment of at most `snap` units never spans two CTAs, and the CTA found for a unit
+by searching near the even split is the CTA that owns it.
+
+The arithmetic mirrors the kernel's (32-bit integer formulas); the GPU parity tests run the
+kernel itself on the same kinds of length mixes."""
+import math
+
+import numpy as np
+import pytest
+
+WARPS, MIN_TILES, SNAP_UNITS, PAGE = 8, 4, 32, 16
+
+
+def units_prefix(lens, Hkv, window=0, ring=False):
+    tiles = []
+    for L in lens:
+        if L <= 0:
+            tiles.append(0)
+        elif ring:
+            tiles.append(math.ceil(min(L, window) / PAGE))
+        else:
+            lo = L - window if (window > 0 and L > window) else 0
+            tiles.append((L - 1) // PAGE - lo // PAGE + 1)
+    pre = np.concatenate([[0], np.cumsum(np.asarray(tiles) * Hkv)]).astype(np.int64)
+    return pre, tiles
+
+
+def segment_of_unit(pre, Hkv, x):
+    b = int(np.searchsorted(pre, x, side="right") - 1)
+    tiles = (pre[b + 1] - pre[b]) // Hkv
+    g = (x - pre[b]) // tiles
+    first = pre[b] + g * tiles
+    return b * Hkv + g, int(first), int(first + tiles)
+
+
+def split(pre, Hkv, ncta):
+    U = int(pre[-1])
+    nwork = min(ncta * WARPS, (U + MIN_TILES - 1) // MIN_TILES)
+    q, r = divmod(U, nwork)
+    wst = lambda w: w * q + (w * r) // nwork
+    snap_max = min(SNAP_UNITS, q)
+
+    def cta_start(c):
+        x = wst(min(c * WARPS, nwork))
+        if x <= 0 or x >= U:
+            return x
+        _, f, e = segment_of_unit(pre, Hkv, x)
+        if x == f or e - f > snap_max:
+            return x
+        return f if x - f <= e - x else e
+
+    n_cta = (nwork + WARPS - 1) // WARPS
+    warps = []
+    for c in range(n_cta):
+        R0, R1 = cta_start(c), cta_start(c + 1)
+        nw = min(WARPS, nwork - c * WARPS)
+        qw, rw = divmod(R1 - R0, nw)
+        for w in range(nw):
+            warps.append((c, R0 + w * qw + (w * rw) // nw, R0 + (w + 1) * qw + ((w + 1) * rw) // nw))
+
+    def cta_of(x):
+        c = (((x + 1) * nwork - 1) // U) // WARPS
+        while c > 0 and cta_start(c) > x:
+            c -= 1
+        while c + 1 < n_cta and cta_start(c + 1) <= x:
+            c += 1
+        return c
+
+    return U, n_cta, cta_start, warps, cta_of, snap_max
+
+
+LEN_MIXES = {
+    "b64": lambda rng: list(rng.integers(1024, 8193, 64)),
+    "b1": lambda rng: [4096],
+    "long1": lambda rng: [131072],
+    "serve": lambda rng: [0 if rng.random() < 0.25 else int(min(32768, max(1, math.ceil(
+        math.exp(math.log(2048) + rng.standard_normal()))))) for _ in range(256)],
+    "short_many": lambda rng: list(rng.integers(1, 70, 300)) + [1500, 700, 1],
+    "max_batch": lambda rng: [0 if rng.random() < 0.25 else int(rng.integers(1, 48)) for _ in range(1024)],
+}
+
+
+@pytest.mark.parametrize("mix", sorted(LEN_MIXES))
+@pytest.mark.parametrize("ring", [False, True])
+def test_split_invariants(mix, ring):
+    rng = np.random.default_rng(sum(map(ord, mix)) + ring)
+    lens = LEN_MIXES[mix](rng)
+    Hkv = 8 if mix != "short_many" else 2
+    pre, _ = units_prefix(lens, Hkv, window=128, ring=ring)
+    U = int(pre[-1])
+    if U == 0:
+        return
+    U2, n_cta, cta_start, warps, cta_of, snap_max = split(pre, Hkv, ncta=152)
+    # CTA boundaries strictly increasing from 0 to U: every working CTA has units
+    bounds = [cta_start(c) for c in range(n_cta + 1)]
+    assert bounds[0] == 0 and bounds[-1] == U
+    assert all(a < b for a, b in zip(bounds, bounds[1:]))
+    # warps tile [0, U) exactly, in order, each with at least one unit
+    at = 0
+    for c, ua, ue in warps:
+        assert ua == at and ue > ua and bounds[c] <= ua and ue <= bounds[c + 1]
+        at = ue
+    assert at == U
+    # a short segment never spans two CTAs; cta_of finds the owner
+    for c in range(1, n_cta):
+        x = bounds[c]
+        _, f, e = segment_of_unit(pre, Hkv, x)
+        if e - f <= snap_max:
+            assert x in (f, e)
+    for x in list(range(0, U, max(1, U // 500))) + [U - 1] + bounds[1:-1]:
+        c = cta_of(x)
+        assert bounds[c] <= x < bounds[c + 1]
+    # balance: no CTA is more than a worker's share (kSnapUnits at most) above the even split
+    share = U / (len(warps))
+    for c in range(n_cta):
+        nw = sum(1 for w in warps if w[0] == c)
+        assert bounds[c + 1] - bounds[c] <= nw * share + 2 * snap_max + 2
+
+
+def test_ring_segments_of_the_serving_mix_stay_in_one_cta():
+    """The window-128 ring layer of the serving mix: 8-tile segments and a worker share of
+    about 10 units, so every CTA boundary sits on a segment edge."""
+    rng = np.random.default_rng(4)
+    lens = LEN_MIXES["serve"](rng)
+    pre, _ = units_prefix(lens, 8, window=128, ring=True)
+    U, n_cta, cta_start, warps, cta_of, snap_max = split(pre, 8, ncta=152)
+    assert snap_max >= 8
+    for c in range(1, n_cta):
+        x = cta_start(c)
+        _, f, e = segment_of_unit(pre, 8, x)
+        assert x == f
