@@ -32,7 +32,8 @@
  *     launched when a code is returned.
  *   - Supported now: head_dim 64, page_size 16, query heads per KV head
  *     (G = Hq/Hkv) in {1, 2, 4, 8, 16}, batch <= 1024, Hq <= 1024, batch*Hkv <= 65536,
- *     ring capacity >= 16. Anything else returns DA_ERR_UNSUPPORTED.
+ *     ring capacity >= 16, a GPU with at most 160 SMs. Anything else returns
+ *     DA_ERR_UNSUPPORTED.
  *   - The attention entry points use a library-owned workspace per device
  *     (split partials and arrival counters). It is allocated on first use or
  *     by decode_attn_reserve(); during stream capture a call that would need

@@ -76,6 +76,7 @@ constexpr int kThreads = kWarps * 32;
 #define DA_FP8_2CTA_MIN_TILES 16384
 #endif
 constexpr int kMaxCtasPerSm = 2;
+constexpr int kMaxSms = 160;  // the one-token grid is one (or two) CTAs per SM, up to this many SMs
 template <int NT, bool ROPE, bool KV8, int CPS>
 __host__ __device__ constexpr int stages_for() {
     // fp8 tiles are half the size: more of them in flight for the same bytes; with two
@@ -559,7 +560,8 @@ struct SmemLayout {
     // rows go to registers straight from global memory)
     static constexpr int kQBytes = MT ? GP * kD * 2 : kRopeOff + (ROPE ? 2 * (kD / 2) * 4 : 0);
     static constexpr int kWarpTileBytes = kStages * kStageBytes;  // the tiles of one warp
-    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + kWarps + kWarps * kWinfo + 16 + (MT ? kMaxBatch : 0);
+    static constexpr int kInts = (kMaxBatch + 1) + kMaxBatch + 2 * kWarps + kWarps * kWinfo + 16 +
+                                 (kMaxCtasPerSm * kMaxSms + 1) + (MT ? kMaxBatch : 0);
     static constexpr size_t qarea = static_cast<size_t>(kWarps) * kWarpTileBytes;
     static constexpr size_t bars = qarea + static_cast<size_t>(kWarps) * kStages * kQBytes;
     static constexpr size_t meta = bars + static_cast<size_t>(kWarps) * kStages * 8;
@@ -617,9 +619,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
     int *s_pre = reinterpret_cast<int *>(smem + Lay::ints);  // [B + 1]
     int *s_len = s_pre + (kMaxBatch + 1);                             // [B]
     int *s_wsum = s_len + kMaxBatch;                                  // [kWarps]
-    int *s_winfo = s_wsum + kWarps;                                   // [kWarps][kWinfo]
+    int *s_wmin = s_wsum + kWarps;                                    // [kWarps]
+    int *s_winfo = s_wmin + kWarps;                                   // [kWarps][kWinfo]
     int *s_flag = s_winfo + kWarps * kWinfo;                          // [16]
-    int *s_n = s_flag + 16;                                           // [B] new tokens (MT)
+    int *s_bnd = s_flag + 16;                                         // [CTAs + 1] CTA boundaries
+    int *s_n = s_bnd + kMaxCtasPerSm * kMaxSms + 1;                   // [B] new tokens (MT)
     float *s_sink = reinterpret_cast<float *>(smem + Lay::sinks);     // [Hq], log2 units
 
     // Set-up that reads no input: it overlaps the previous kernel in the stream when this
@@ -643,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     {
         for (int h = tid; h < p.Hq; h += kThreads)
             s_sink[h] = p.sinks != nullptr ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
-        int v[4], tsum = 0;
+        int v[4], tsum = 0, tmin = 0x7fffffff;  // (tmin: the fewest units of a segment)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int b = tid * 4 + k;
@@ -671,14 +675,19 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 v[k] = tiles_of<RING>(L, p.window) * Hkv;
             }
             tsum += v[k];
+            if (v[k] > 0) tmin = min(tmin, v[k] / Hkv);
         }
         int incl = tsum;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += y;
+            tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, off));
         }
-        if (lane == 31) s_wsum[warp] = incl;
+        if (lane == 31) {
+            s_wsum[warp] = incl;
+            s_wmin[warp] = tmin;
+        }
         __syncthreads();
         int woff = 0;
         for (int w = 0; w < warp; ++w) woff += s_wsum[w];
@@ -721,14 +730,24 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int q_nw = U / nw32, r_nw = U - q_nw * nw32;
     auto wst = [&](int w) { return w * q_nw + (w * r_nw) / nw32; };
     const int snap_max = min(kSnapUnits, q_nw);
-    auto cta_start = [&](int c) {
-        const int x = wst(min(c * kWarps, nw32));
-        if (x <= 0 || x >= U) return x;
-        int f, e;
-        segment_of_unit(s_pre, B, Hkv, x, f, e);
-        if (x == f || e - f > snap_max) return x;
-        return (x - f <= e - x) ? f : e;
-    };
+    const int n_cta = (nw32 + kWarps - 1) / kWarps;  // CTAs with work
+    int min_seg = s_wmin[0];  // the shortest segment of the call, in units
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) min_seg = min(min_seg, s_wmin[w]);
+    const bool snapping = min_seg <= snap_max;  // (else no boundary can move)
+    if (snapping) {  // every CTA boundary of the call, one lookup per thread, into shared memory
+        for (int c = tid; c <= n_cta; c += kThreads) {
+            int x = wst(min(c * kWarps, nw32));
+            if (x > 0 && x < U) {
+                int f, e;
+                segment_of_unit(s_pre, B, Hkv, x, f, e);
+                if (x != f && e - f <= snap_max) x = (x - f <= e - x) ? f : e;
+            }
+            s_bnd[c] = x;
+        }
+        __syncthreads();
+    }
+    auto cta_start = [&](int c) { return snapping ? s_bnd[c] : wst(min(c * kWarps, nw32)); };
     const int nw_cta = min(kWarps, nw32 - cta * kWarps);  // active warps of this CTA
     const bool active = warp < nw_cta;
     const int R0 = cta_start(cta), R1 = cta_start(cta + 1);  // this CTA's units
@@ -831,18 +850,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const int qrows = MT ? min(GP, max(0, p.T * p.G - r0g)) : p.G;
                 mbar_expect_tx(bar, Lay::kStageBytes + (newseg ? qrows * kD * 2 : 0) + (rows ? 4 * kD : 0) +
                                         (rope ? 4 * kD : 0));
-                if constexpr (KV8) {  // the whole block in one copy (a bad page reads block 0)
-                    const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
-                                            : static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg;
-                    bulk_load_hint(k_tile(stg), reinterpret_cast<const uint8_t *>(p.k_cache) + blk * kBlk8Bytes,
-                                   kBlk8Bytes, bar, policy);
-                } else {
-                    int c1, c2;
-                    if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
-                    else { c1 = 0; c2 = tp * Hkv + tg; }
-                    tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
-                    tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
-                }
+                // a new segment's rows first: with several tiles issued at once, a stage's
+                // barrier then does not wait for them behind every tile's copies
                 if (newseg) {
                     if constexpr (MT) {  // rows r0g .. r0g + qrows - 1: for each token t the heads of
                                          // group tg whose row t G + h falls in that range
@@ -872,6 +881,18 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     const size_t row = static_cast<size_t>(pos) * (kD / 2);
                     bulk_load(q_tile(stg) + GP * kD * 2 + 4 * kD, p.rope_cos + row, kD * 2, bar);
                     bulk_load(q_tile(stg) + GP * kD * 2 + 6 * kD, p.rope_sin + row, kD * 2, bar);
+                }
+                if constexpr (KV8) {  // the whole block in one copy (a bad page reads block 0)
+                    const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
+                                            : static_cast<size_t>(tp < 0 ? 0 : tp) * Hkv + tg;
+                    bulk_load_hint(k_tile(stg), reinterpret_cast<const uint8_t *>(p.k_cache) + blk * kBlk8Bytes,
+                                   kBlk8Bytes, bar, policy);
+                } else {
+                    int c1, c2;
+                    if (RING) { c1 = tt * kPage; c2 = tb * Hkv + tg; }
+                    else { c1 = 0; c2 = tp * Hkv + tg; }
+                    tma_load_3d(k_tile(stg), &tmk, 0, c1, c2, bar, policy);
+                    tma_load_3d(v_tile(stg), &tmv, 0, c1, c2, bar, policy);
                 }
             }
         };
@@ -1553,7 +1574,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (tid == kThreads - 1) {
         int f, e;
         const int sa = segment_of_unit(s_pre, B, Hkv, R0, f, e);
-        const int n_cta = (nw32 + kWarps - 1) / kWarps;  // CTAs with work
         auto cta_of = [&](int x) {  // the CTA whose range holds unit x: near the even split's
             int c = worker_of(x, U, nwork) / kWarps;
             while (c > 0 && cta_start(c) > x) --c;
@@ -1872,6 +1892,7 @@ int check_shape(const da_shape &s) {
 
 template <int NT, bool RING, bool ROPE, bool KV8 = false, int CPS = 1, bool MT = false>
 int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm, int dev, cudaStream_t stream) {
+    if (sm_count(dev) > kMaxSms) return DA_ERR_UNSUPPORTED;  // the kernel keeps a boundary per CTA
     static_assert(CPS == 1 || (KV8 && NT == 1), "two CTAs per SM: fp8 kernel with 8-head groups only");
     const size_t smem = SmemLayout<NT, ROPE, KV8, CPS, MT>::bytes;
     const size_t smem_max = smem;
