@@ -304,10 +304,11 @@ DA_API int decode_attn_reserve(size_t bytes);
  * one-shot: in the next one-token attention call (decode_attn_paged / _ring and their
  * _rope / _fp8 forms), the first worker gives up at its first tile wait from its tile
  * `tile` on (0-based, counted over that worker's share of the tiles), after that tile has
- * landed, exactly as if the bounded wait had expired. The call then records
- * DA_STATUS_TIMEOUT, its output is garbage, no copy is left in flight, and the library's
- * arrival counters are back at zero for the next call. tile < 0 disarms. No GPU fault,
- * trap or hang is involved. Returns DA_OK.
+ * landed, exactly as if the bounded wait had expired (a worker takes its tiles two at a
+ * time, one wait per pass; if its share has no wait at or after `tile`, nothing happens).
+ * The call then records DA_STATUS_TIMEOUT, its output is garbage, no copy is left in
+ * flight, and the library's arrival counters are back at zero for the next call. tile < 0
+ * disarms. No GPU fault, trap or hang is involved. Returns DA_OK.
  */
 DA_API int decode_attn_test_expire_wait(int tile);
 

@@ -109,8 +109,13 @@ __host__ __device__ constexpr int stages_for() {
 #ifndef DA_FAST_PASS_BF16
 #define DA_FAST_PASS_BF16 0
 #endif
+// Tiles per worker at least: 4, or 2 for a call of at most two tiles per worker of the grid
+// (such a call cannot fill the grid anyway; two tiles are one loop pass)
 #ifndef DA_MIN_TILES
 #define DA_MIN_TILES 4
+#endif
+#ifndef DA_MIN_TILES_SMALL
+#define DA_MIN_TILES_SMALL 2
 #endif
 // The first kStages copies of a warp issued by several lanes at once
 #ifndef DA_PAR_FILL
@@ -118,6 +123,7 @@ __host__ __device__ constexpr int stages_for() {
 #endif
 
 constexpr int kMinTilesPerWorker = DA_MIN_TILES;
+constexpr int kMinTilesSmall = DA_MIN_TILES_SMALL;
 // CTA boundaries move to the nearer edge of a segment of at most this many units (and of at
 // most a worker's share), so that short segments are not split between CTAs
 #ifndef DA_SNAP_UNITS
@@ -361,11 +367,6 @@ __device__ __forceinline__ int segment_of_unit(const int *pre, int B, int Hkv, i
     return b * Hkv + g;
 }
 
-// Worker boundaries: worker w owns units [floor(w U / nw), floor((w + 1) U / nw)); the
-// worker owning unit x:
-__device__ __forceinline__ int worker_of(long long x, long long U, long long nw) {
-    return static_cast<int>(((x + 1) * nw - 1) / U);
-}
 
 template <int NT>
 struct SegState {
@@ -714,22 +715,25 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (U == 0) return;
 
     // ---- 3. workers and their unit ranges
-    const long long nwork =
-        min(static_cast<long long>(ncta) * kWarps,
-            static_cast<long long>((U + kMinTilesPerWorker - 1) / kMinTilesPerWorker));
+    // (whole CTAs of workers once there are eight or more: every CTA then holds 8 shares)
+    const int min_tiles = U <= 2 * ncta * kWarps ? kMinTilesSmall : kMinTilesPerWorker;
+    long long nwork = min(static_cast<long long>(ncta) * kWarps, static_cast<long long>((U + min_tiles - 1) / min_tiles));
+    if (nwork >= kWarps) nwork -= nwork % kWarps;
     if (static_cast<long long>(cta) * kWarps >= nwork) return;  // whole CTA idle
     const long long wid = static_cast<long long>(cta) * kWarps + warp;
     // Two levels. CTA c takes the units from cta_start(c): worker c kWarps's start in an even
     // split over all nwork workers, floor(w U / nwork) = w q + floor(w r / nwork) with
     // U = q nwork + r (32-bit: w r < nwork^2 < 2^23), moved to the nearer edge of the segment
-    // it falls in when that segment is at most a worker's share (and kSnapUnits) long: a
+    // it falls in when that segment is at most four workers' shares (and kSnapUnits) long: a
     // segment that short is then never shared between CTAs, which would cost it a partial, a
     // ticket and a combine (more than the few tiles of imbalance). The CTA's warps split its
     // range evenly.
     const int nw32 = static_cast<int>(nwork);
     const int q_nw = U / nw32, r_nw = U - q_nw * nw32;
     auto wst = [&](int w) { return w * q_nw + (w * r_nw) / nw32; };
-    const int snap_max = min(kSnapUnits, q_nw);
+    // a boundary moves by at most snap_max / 2 <= 2 q, and a CTA holds 8 shares of q (or is
+    // the only one): every CTA keeps units
+    const int snap_max = min(kSnapUnits, 4 * q_nw);
     const int n_cta = (nw32 + kWarps - 1) / kWarps;  // CTAs with work
     int min_seg = s_wmin[0];  // the shortest segment of the call, in units
 #pragma unroll
@@ -1574,8 +1578,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (tid == kThreads - 1) {
         int f, e;
         const int sa = segment_of_unit(s_pre, B, Hkv, R0, f, e);
-        auto cta_of = [&](int x) {  // the CTA whose range holds unit x: near the even split's
-            int c = worker_of(x, U, nwork) / kWarps;
+        auto cta_of = [&](int x) {  // the CTA whose range holds unit x: start from an estimate
+            int c = min(n_cta - 1, static_cast<int>(static_cast<float>(x) * (static_cast<float>(n_cta) / U)));
             while (c > 0 && cta_start(c) > x) --c;
             while (c + 1 < n_cta && cta_start(c + 1) <= x) ++c;
             return c;

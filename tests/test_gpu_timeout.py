@@ -48,7 +48,7 @@ def test_expired_wait_in_the_ring_and_many_segments_per_worker():
     c = make_case(390, len(lens), 16, 2, 64, lens)
     kr, vr = ring_from_history(c, pre(c), 128)
     out = torch.empty((c.B, c.Hq, c.D), dtype=torch.bfloat16, device=DEV)
-    da.decode_attn_test_expire_wait(2)
+    da.decode_attn_test_expire_wait(0)  # (the first worker's share may be two tiles: one pass)
     da.decode_attn_ring(dev_bits(c.q), dev_bits(c.k_new), dev_bits(c.v_new), dev_bits(kr),
                         dev_bits(vr), dev(c.lens), dev(c.sinks), c.scale, out)
     assert da.decode_attn_device_status() & da.DA_STATUS_TIMEOUT

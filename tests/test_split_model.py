@@ -13,7 +13,7 @@ import math
 import numpy as np
 import pytest
 
-WARPS, MIN_TILES, SNAP_UNITS, PAGE = 8, 4, 32, 16
+WARPS, MIN_TILES, MIN_TILES_SMALL, SNAP_UNITS, PAGE = 8, 4, 2, 32, 16
 
 
 def units_prefix(lens, Hkv, window=0, ring=False):
@@ -38,12 +38,16 @@ def segment_of_unit(pre, Hkv, x):
     return b * Hkv + g, int(first), int(first + tiles)
 
 
-def split(pre, Hkv, ncta):
+def split(pre, Hkv, ncta, min_tiles=None):
     U = int(pre[-1])
-    nwork = min(ncta * WARPS, (U + MIN_TILES - 1) // MIN_TILES)
+    if min_tiles is None:  # the kernel's rule: 2 tiles per worker for a call of <= 2 per grid worker
+        min_tiles = MIN_TILES_SMALL if U <= 2 * ncta * WARPS else MIN_TILES
+    nwork = min(ncta * WARPS, (U + min_tiles - 1) // min_tiles)
+    if nwork >= WARPS:
+        nwork -= nwork % WARPS
     q, r = divmod(U, nwork)
     wst = lambda w: w * q + (w * r) // nwork
-    snap_max = min(SNAP_UNITS, q)
+    snap_max = min(SNAP_UNITS, 4 * q)
 
     def cta_start(c):
         x = wst(min(c * WARPS, nwork))
@@ -63,8 +67,8 @@ def split(pre, Hkv, ncta):
         for w in range(nw):
             warps.append((c, R0 + w * qw + (w * rw) // nw, R0 + (w + 1) * qw + ((w + 1) * rw) // nw))
 
-    def cta_of(x):
-        c = (((x + 1) * nwork - 1) // U) // WARPS
+    def cta_of(x):  # an fp32 estimate, then the search
+        c = min(n_cta - 1, int(np.float32(x) * (np.float32(n_cta) / np.float32(U))))
         while c > 0 and cta_start(c) > x:
             c -= 1
         while c + 1 < n_cta and cta_start(c + 1) <= x:
@@ -87,7 +91,8 @@ LEN_MIXES = {
 
 @pytest.mark.parametrize("mix", sorted(LEN_MIXES))
 @pytest.mark.parametrize("ring", [False, True])
-def test_split_invariants(mix, ring):
+@pytest.mark.parametrize("min_tiles", [None, 2, 4])
+def test_split_invariants(mix, ring, min_tiles):
     rng = np.random.default_rng(sum(map(ord, mix)) + ring)
     lens = LEN_MIXES[mix](rng)
     Hkv = 8 if mix != "short_many" else 2
@@ -95,7 +100,7 @@ def test_split_invariants(mix, ring):
     U = int(pre[-1])
     if U == 0:
         return
-    U2, n_cta, cta_start, warps, cta_of, snap_max = split(pre, Hkv, ncta=152)
+    U2, n_cta, cta_start, warps, cta_of, snap_max = split(pre, Hkv, ncta=152, min_tiles=min_tiles)
     # CTA boundaries strictly increasing from 0 to U: every working CTA has units
     bounds = [cta_start(c) for c in range(n_cta + 1)]
     assert bounds[0] == 0 and bounds[-1] == U
@@ -115,11 +120,11 @@ def test_split_invariants(mix, ring):
     for x in list(range(0, U, max(1, U // 500))) + [U - 1] + bounds[1:-1]:
         c = cta_of(x)
         assert bounds[c] <= x < bounds[c + 1]
-    # balance: no CTA is more than a worker's share (kSnapUnits at most) above the even split
+    # balance: a CTA boundary moves by at most snap_max / 2 from the even split
     share = U / (len(warps))
     for c in range(n_cta):
         nw = sum(1 for w in warps if w[0] == c)
-        assert bounds[c + 1] - bounds[c] <= nw * share + 2 * snap_max + 2
+        assert bounds[c + 1] - bounds[c] <= nw * share + snap_max + 2
 
 
 def test_ring_segments_of_the_serving_mix_stay_in_one_cta():
