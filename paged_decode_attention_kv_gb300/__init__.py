@@ -31,7 +31,7 @@ __all__ = [
     "decode_attn_paged_rope", "decode_attn_ring_rope", "decode_attn_paged_fp8", "decode_attn_ring_fp8",
     "decode_attn_paged_multi", "decode_attn_ring_multi", "decode_attn_multi_workspace_bytes",
     "decode_attn_multi_reserve", "decode_attn_multi_launches", "decode_attn_test_expire_wait",
-    "decode_attn_paged_fp8_rope", "decode_attn_ring_fp8_rope",
+    "decode_attn_paged_fp8_rope", "decode_attn_ring_fp8_rope", "decode_attn_set_early_inputs",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -112,6 +112,7 @@ def load_library():
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
     lib.decode_attn_device_status.argtypes = [vp]
     lib.decode_attn_test_expire_wait.argtypes = [c_int]
+    lib.decode_attn_set_early_inputs.argtypes = [c_int]
     lib.decode_attn_error_string.argtypes = [c_int]
     lib.decode_attn_error_string.restype = ctypes.c_char_p
     for fn in (lib.decode_attn_paged, lib.decode_attn_ring, lib.kv_append, lib.decode_attn_reserve,
@@ -119,7 +120,7 @@ def load_library():
                lib.decode_attn_paged_fp8, lib.decode_attn_ring_fp8, lib.decode_attn_paged_multi,
                lib.decode_attn_ring_multi, lib.decode_attn_multi_reserve,
                lib.decode_attn_test_expire_wait, lib.decode_attn_paged_fp8_rope,
-               lib.decode_attn_ring_fp8_rope):
+               lib.decode_attn_ring_fp8_rope, lib.decode_attn_set_early_inputs):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -354,6 +355,14 @@ def decode_attn_device_status(stream=None) -> int:
     if rc < 0:
         _check(rc)
     return rc
+
+
+def decode_attn_set_early_inputs(on: bool) -> bool:
+    """Process-wide launch order of the attention kernels; returns the previous setting.
+    True: seq_lens, q_lens, block_table and sinks are read before waiting for the kernel
+    launched just before each call, so they must have been written before that kernel
+    started (host copies or earlier kernels). False (the default): every read waits."""
+    return bool(load_library().decode_attn_set_early_inputs(1 if on else 0))
 
 
 def decode_attn_test_expire_wait(tile: int):

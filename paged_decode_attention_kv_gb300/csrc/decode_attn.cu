@@ -176,6 +176,11 @@ struct Params {
     // testing aid: worker 0 gives up at its first tile wait from this tile on (after the tile
     // has landed), as if the wait had expired; -1 = never
     int expire_at;
+    // 1: seq_lens, q_lens, block_table and sinks were final before the previous kernel in the
+    // stream started, so the lengths, the split and the first block-table entries are read
+    // and worked out before waiting for that kernel (the rest, from the first query row and
+    // cache tile on, after the wait); 0: every input is read after the wait
+    int early;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -639,8 +644,16 @@ __global__ void __launch_bounds__(kThreads, CPS)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid < 4) s_flag[tid] = -1;  // [0,1] segments this CTA combines; [2,3] its boundary segments
-    // Inputs may come from the previous kernel: wait for it before the first read.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Inputs may come from the previous kernel: wait for it before the first read of one it
+    // may have written (at once, or after the split when the step's lengths and tables were
+    // final before it started). The next kernel may start its own set-up once this grid has
+    // waited: this kernel's inputs are then final.
+    auto wait_previous = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    };
+    const bool early = p.early != 0;
+    if (!early) wait_previous();
 
     const int B = p.B, Hkv = p.Hkv;
 
@@ -704,22 +717,33 @@ __global__ void __launch_bounds__(kThreads, CPS)
     }
     const int U = s_pre[B];
 
-    // ---- 2. inactive slots get a zero output
-    for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        if (s_len[b] != 0) continue;
-        const int rows_b = MT ? p.T : 1;  // query tokens per slot
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(b) * rows_b * p.Hq * kD);
-        const int n16 = rows_b * p.Hq * kD * 2 / 16;
-        for (int i = tid; i < n16; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
+    // ---- 2. inactive slots get a zero output (after the wait: the previous kernel may still
+    // use the output buffer)
+    auto zero_inactive = [&]() {
+        for (int b = blockIdx.x; b < B; b += gridDim.x) {
+            if (s_len[b] != 0) continue;
+            const int rows_b = MT ? p.T : 1;  // query tokens per slot
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(b) * rows_b * p.Hq * kD);
+            const int n16 = rows_b * p.Hq * kD * 2 / 16;
+            for (int i = tid; i < n16; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (U == 0) {
+        if (early) wait_previous();
+        zero_inactive();
+        return;
     }
-    if (U == 0) return;
 
     // ---- 3. workers and their unit ranges
     // (whole CTAs of workers once there are eight or more: every CTA then holds 8 shares)
     const int min_tiles = U <= 2 * ncta * kWarps ? kMinTilesSmall : kMinTilesPerWorker;
     long long nwork = min(static_cast<long long>(ncta) * kWarps, static_cast<long long>((U + min_tiles - 1) / min_tiles));
     if (nwork >= kWarps) nwork -= nwork % kWarps;
-    if (static_cast<long long>(cta) * kWarps >= nwork) return;  // whole CTA idle
+    if (static_cast<long long>(cta) * kWarps >= nwork) {  // whole CTA idle
+        if (early) wait_previous();
+        zero_inactive();
+        return;
+    }
     const long long wid = static_cast<long long>(cta) * kWarps + warp;
     // Two levels. CTA c takes the units from cta_start(c): worker c kWarps's start in an even
     // split over all nwork workers, floor(w U / nwork) = w q + floor(w r / nwork) with
@@ -789,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     bool failed = false;
     bool slots_ok = true;  // false after an expired wait: this warp's area is never read or written again
 
+    if (early && !active) wait_previous();
     if (active) {
         __syncwarp();
         const uint64_t policy = evict_first_policy();
@@ -816,6 +841,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
         load_batch(0, cb, cg, ct, cp);
         if (n_tiles > 32) load_batch(1, nb, ng, ntl, np);
         int cur_batch = 0;
+        if (early) wait_previous();  // query rows, new tokens and cache tiles from here on
 
         // Copies of tiles j0 .. j0 + cnt - 1 (cnt <= kStages, calls in increasing order): lane u
         // issues tile j0 + u into stage (stg0 + u) mod kStages, so several tiles go out at once.
@@ -1444,6 +1470,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
         if (slots_ok && head_seg >= 0) state_to_slot(head, &slots[0], lane);
         if (slots_ok && tail_seg >= 0) state_to_slot(st, &slots[1], lane);
     }
+    zero_inactive();
     if (lane == 0) {
         int *wi = s_winfo + warp * kWinfo;
         wi[0] = ua; wi[1] = ue; wi[2] = head_seg; wi[3] = tail_seg; wi[4] = active ? 1 : 0;
@@ -1451,7 +1478,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
         wi[9] = slots_ok ? 1 : 0;
     }
     __syncthreads();
-    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 4. merge segments shared between warps of this CTA (all threads take part)
     // Segments shared by several warps: every warp of this CTA holding a state of one (warps
@@ -1483,120 +1509,147 @@ __global__ void __launch_bounds__(kThreads, CPS)
             const bool internal = s0 >= R0 && s1 <= R1;
             const int slot_k = s0 <= R0 ? 0 : 1;
             const int b = seg / Hkv, g = seg - b * Hkv;
-            // The segment's GP x 4 items (a column and 16 of its dimensions) are shared out over
-            // the lanes of its k warps; a lane loads its item from every contributor at once
-            // (contributor c is warp wa + c, its slot the head or the tail one; a warp whose
-            // copies never landed is skipped), four contributors per round.
+            // The segment's items (a column and DPI of its dimensions, DPI 16, 8 or 4: the
+            // narrowest that gives every lane of its k warps at most one item, or two when a
+            // single warp holds the 16 columns of a 16-head group) are shared out over those
+            // lanes; a lane loads its item from every contributor at once (contributor c is
+            // warp wa + c, its slot the head or the tail one; a warp whose copies never landed
+            // is skipped), four contributors per round.
             const uint32_t slots_base = smem_addr(smem);
             const int qrows = MT ? p.T * p.G : p.G;  // valid query rows of the group
+            auto merge_items = [&](auto dpi_c) {
+                constexpr int DPI = decltype(dpi_c)::value;
+                constexpr int IPC = kD / DPI;  // items per column
 #pragma unroll 1
-            for (int item = mine * 32 + lane; item < GP * 4; item += k * 32) {
-                const int n = item >> 2, d0 = (item & 3) * 16;
-                const int rn = r0g + n;  // column n's query row
-                const float sg = (internal && rn < qrows) ? s_sink[g * p.G + (MT ? rn % p.G : rn)] : -INFINITY;
-                float M = -INFINITY, den = 0.f;
-                float acc[16];
+                for (int item = mine * 32 + lane; item < GP * IPC; item += k * 32) {
+                    const int n = item / IPC, d0 = (item % IPC) * DPI;
+                    const int rn = r0g + n;  // column n's query row
+                    const float sg = (internal && rn < qrows) ? s_sink[g * p.G + (MT ? rn % p.G : rn)] : -INFINITY;
+                    float M = -INFINITY, den = 0.f;
+                    float acc[DPI];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+                    for (int j = 0; j < DPI; ++j) acc[j] = 0.f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < k; c0 += 4) {
-                    float mc[4], lc[4];
-                    float4 a[4][4];
+                    for (int c0 = 0; c0 < k; c0 += 4) {
+                        float mc[4], lc[4];
+                        float4 a[4][DPI / 4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = c0 + u, w = wa + (c < k ? c : 0);
-                        const bool ok = c < k && s_winfo[w * kWinfo + 9] != 0;
-                        const uint32_t sl = slots_base + w * kWarpBytes +
-                                            ((s_winfo[w * kWinfo + 3] == seg) ? static_cast<uint32_t>(sizeof(Slot<NT>)) : 0u);
-                        mc[u] = ok ? lds_f32(sl + 4 * n) : -INFINITY;
-                        lc[u] = ok ? lds_f32(sl + 4 * (GP + n)) : 0.f;
+                        for (int u = 0; u < 4; ++u) {
+                            const int c = c0 + u, w = wa + (c < k ? c : 0);
+                            const bool ok = c < k && s_winfo[w * kWinfo + 9] != 0;
+                            const uint32_t sl = slots_base + w * kWarpBytes +
+                                                ((s_winfo[w * kWinfo + 3] == seg) ? static_cast<uint32_t>(sizeof(Slot<NT>)) : 0u);
+                            mc[u] = ok ? lds_f32(sl + 4 * n) : -INFINITY;
+                            lc[u] = ok ? lds_f32(sl + 4 * (GP + n)) : 0.f;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            a[u][q] = ok ? lds_f32x4(sl + 4 * (2 * GP + n * Slot<NT>::LD + d0 + 4 * q))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    float Mn = M;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) Mn = fmaxf(Mn, mc[u]);
-                    const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // rescale the rounds before
-                    den *= r;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[j] *= r;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float w = mc[u] == -INFINITY ? 0.f : fast_exp2(mc[u] - Mn);  // no key: weight 0
-                        den += lc[u] * w;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            acc[4 * q] += a[u][q].x * w;
-                            acc[4 * q + 1] += a[u][q].y * w;
-                            acc[4 * q + 2] += a[u][q].z * w;
-                            acc[4 * q + 3] += a[u][q].w * w;
+                            for (int q = 0; q < DPI / 4; ++q)
+                                a[u][q] = ok ? lds_f32x4(sl + 4 * (2 * GP + n * Slot<NT>::LD + d0 + 4 * q))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-                    }
-                    M = Mn;
-                }
-                if (internal) {  // sink, normalise, bf16
-                    const float Mf = fmaxf(M, sg);
-                    const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mf);
-                    den = den * r + (sg == -INFINITY ? 0.f : fast_exp2(sg - Mf));
-                    if (rn < qrows) {
-                        const int t = MT ? rn / p.G : 0, h = MT ? rn - t * p.G : rn;
-                        const float inv = (MT && t >= s_n[b]) ? 0.f : r / den;  // no query token: zeros
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD + d0);
-                        uint4 o0, o1;
-                        o0.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-                        o0.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-                        o0.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-                        o0.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-                        o1.x = pack_bf16(acc[8] * inv, acc[9] * inv);
-                        o1.y = pack_bf16(acc[10] * inv, acc[11] * inv);
-                        o1.z = pack_bf16(acc[12] * inv, acc[13] * inv);
-                        o1.w = pack_bf16(acc[14] * inv, acc[15] * inv);
-                        dst[0] = o0;
-                        dst[1] = o1;
-                    }
-                } else {  // this CTA's fp32 partial of the segment
-                    float *gp = part_slot(cta, slot_k);
-                    if (d0 == 0) {
-                        gp[n] = M;
-                        gp[GP + n] = den;
-                    }
-                    float4 *ga = reinterpret_cast<float4 *>(gp + 2 * GP + n * kD + d0);
+                        float Mn = M;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        ga[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                        for (int u = 0; u < 4; ++u) Mn = fmaxf(Mn, mc[u]);
+                        const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // rescale the rounds before
+                        den *= r;
+#pragma unroll
+                        for (int j = 0; j < DPI; ++j) acc[j] *= r;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float w = mc[u] == -INFINITY ? 0.f : fast_exp2(mc[u] - Mn);  // no key: weight 0
+                            den += lc[u] * w;
+#pragma unroll
+                            for (int q = 0; q < DPI / 4; ++q) {
+                                acc[4 * q] += a[u][q].x * w;
+                                acc[4 * q + 1] += a[u][q].y * w;
+                                acc[4 * q + 2] += a[u][q].z * w;
+                                acc[4 * q + 3] += a[u][q].w * w;
+                            }
+                        }
+                        M = Mn;
+                    }
+                    if (internal) {  // sink, normalise, bf16
+                        const float Mf = fmaxf(M, sg);
+                        const float r = M == -INFINITY ? 0.f : fast_exp2(M - Mf);
+                        den = den * r + (sg == -INFINITY ? 0.f : fast_exp2(sg - Mf));
+                        if (rn < qrows) {
+                            const int t = MT ? rn / p.G : 0, h = MT ? rn - t * p.G : rn;
+                            const float inv = (MT && t >= s_n[b]) ? 0.f : r / den;  // no query token: zeros
+                            __nv_bfloat16 *dst =
+                                p.out + ((static_cast<size_t>(b) * (MT ? p.T : 1) + t) * p.Hq + g * p.G + h) * kD + d0;
+                            uint32_t o[DPI / 2];
+#pragma unroll
+                            for (int j = 0; j < DPI / 2; ++j) o[j] = pack_bf16(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+                            if constexpr (DPI == 4) {
+                                *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < DPI / 8; ++j)
+                                    reinterpret_cast<uint4 *>(dst)[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                            }
+                        }
+                    } else {  // this CTA's fp32 partial of the segment
+                        float *gp = part_slot(cta, slot_k);
+                        if (d0 == 0) {
+                            gp[n] = M;
+                            gp[GP + n] = den;
+                        }
+                        float4 *ga = reinterpret_cast<float4 *>(gp + 2 * GP + n * kD + d0);
+#pragma unroll
+                        for (int q = 0; q < DPI / 4; ++q)
+                            ga[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    }
                 }
-            }
+            };
+            if (32 * k >= GP * 16)  // (GP * kD / 4 items of 4 dimensions)
+                merge_items(std::integral_constant<int, 4>{});
+            else if (32 * k >= GP * 8)
+                merge_items(std::integral_constant<int, 8>{});
+            else
+                merge_items(std::integral_constant<int, 16>{});
         }
     }
-    // Meanwhile the last thread works out this CTA's segments shared with other CTAs from the
+    // Meanwhile the last warp works out this CTA's segments shared with other CTAs from the
     // unit prefix alone: the one holding its first unit (partial slot 0) and the one holding
     // its last unit (slot 1), and for each the contributing CTAs (first, count) and the slot
-    // of the first one: s_flag[2..7] and s_flag[8 + 3k ..]
-    if (tid == kThreads - 1) {
-        int f, e;
-        const int sa = segment_of_unit(s_pre, B, Hkv, R0, f, e);
-        auto cta_of = [&](int x) {  // the CTA whose range holds unit x: start from an estimate
-            int c = min(n_cta - 1, static_cast<int>(static_cast<float>(x) * (static_cast<float>(n_cta) / U)));
+    // of the first one: s_flag[2..7] and s_flag[8 + 3k ..]. Lanes 0 and 1 find the two
+    // segments, lanes 0..3 the CTAs holding their first and last units, all at once.
+    if (warp == kWarps - 1) {
+        int f = 0, e = 0, sg = -1;
+        if (lane < 2) sg = segment_of_unit(s_pre, B, Hkv, lane == 0 ? R0 : R1 - 1, f, e);
+        const int sa = __shfl_sync(0xffffffffu, sg, 0), fa = __shfl_sync(0xffffffffu, f, 0),
+                  ea = __shfl_sync(0xffffffffu, e, 0);
+        const int sz = __shfl_sync(0xffffffffu, sg, 1), fz = __shfl_sync(0xffffffffu, f, 1),
+                  ez = __shfl_sync(0xffffffffu, e, 1);
+        const bool sh0 = fa < R0 || ea > R1;   // the first unit's segment crosses a CTA edge
+        const bool sh1 = sz != sa && ez > R1;  // the last unit's, when another one
+        int c = 0, cs = 0;  // lane j < 4: segment j / 2, its first (j even) or last unit
+        if (lane < 4 && ((lane >> 1) == 0 ? sh0 : sh1)) {
+            const int x = (lane >> 1) == 0 ? ((lane & 1) ? ea - 1 : fa) : ((lane & 1) ? ez - 1 : fz);
+            // the CTA whose range holds unit x: start from an estimate
+            c = min(n_cta - 1, static_cast<int>(static_cast<float>(x) * (static_cast<float>(n_cta) / U)));
             while (c > 0 && cta_start(c) > x) --c;
             while (c + 1 < n_cta && cta_start(c + 1) <= x) ++c;
-            return c;
-        };
-        auto shared_seg = [&](int k, int seg, int s0, int s1) {
-            s_flag[2 + k] = seg;
-            s_flag[4 + 2 * k] = s0;
-            s_flag[5 + 2 * k] = s1;
-            const int c_lo = cta_of(s0), c_hi = cta_of(s1 - 1);
-            s_flag[8 + 3 * k] = c_lo;
-            s_flag[9 + 3 * k] = c_hi - c_lo + 1;
-            // the first contributing CTA may have started before this segment (its slot 1)
-            s_flag[10 + 3 * k] = cta_start(c_lo) < s0 ? 1 : 0;
-        };
-        if (f < R0 || e > R1) shared_seg(0, sa, f, e);
-        const int sz = segment_of_unit(s_pre, B, Hkv, R1 - 1, f, e);
-        if (sz != sa && e > R1) shared_seg(1, sz, f, e);
+            cs = cta_start(c);
+        }
+        int cc[4], ccs[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            cc[j] = __shfl_sync(0xffffffffu, c, j);
+            ccs[j] = __shfl_sync(0xffffffffu, cs, j);
+        }
+        if (lane == 0) {
+            auto shared_seg = [&](int k, int seg, int s0, int s1) {
+                s_flag[2 + k] = seg;
+                s_flag[4 + 2 * k] = s0;
+                s_flag[5 + 2 * k] = s1;
+                s_flag[8 + 3 * k] = cc[2 * k];
+                s_flag[9 + 3 * k] = cc[2 * k + 1] - cc[2 * k] + 1;
+                // the first contributing CTA may have started before this segment (its slot 1)
+                s_flag[10 + 3 * k] = ccs[2 * k] < s0 ? 1 : 0;
+            };
+            if (sh0) shared_seg(0, sa, fa, ea);
+            if (sh1) shared_seg(1, sz, fz, ez);
+        }
     }
     // (no fence here: the ticket-taking thread's fence below publishes every thread's partials)
     __syncthreads();
@@ -1947,6 +2000,8 @@ int prepare_workspace(int dev, int G, cudaStream_t stream, float **part, int **c
 // Testing aid (decode_attn_test_expire_wait): the tile wait at which the next one-token
 // call's first worker gives up; -1 = none. Taken (and cleared) by that call.
 std::atomic<int> g_expire_next{-1};
+// decode_attn_set_early_inputs: 1 = the lengths and tables are read before the wait
+std::atomic<int> g_early_inputs{0};
 
 int run_attention(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                   const int32_t *block_table, const int32_t *seq_lens, const float *sinks, int window,
@@ -2006,6 +2061,7 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.q_lens = nullptr;
     prm.ngrp = 1;
     prm.expire_at = g_expire_next.exchange(-1);
+    prm.early = g_early_inputs.load();
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
 
@@ -2296,6 +2352,7 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         dp.q_lens = q_lens;
         dp.ngrp = m.row_blocks;
         dp.expire_at = -1;
+        dp.early = g_early_inputs.load();
         CUtensorMap mk, mv;
         const uint64_t slices = static_cast<uint64_t>(num_pages) * s.num_kv_heads;
         if (!make_kv_map(&mk, k_cache, kPage, slices) || !make_kv_map(&mv, v_cache, kPage, slices)) {
@@ -2483,6 +2540,7 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.q_lens = nullptr;
     prm.ngrp = 1;
     prm.expire_at = -1;
+    prm.early = g_early_inputs.load();
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
     // The array keeps whatever the previous call left: the arrival counters this call
@@ -2669,6 +2727,8 @@ int decode_attn_test_expire_wait(int tile) {
     g_expire_next.store(tile < 0 ? -1 : tile);
     return DA_OK;
 }
+
+int decode_attn_set_early_inputs(int on) { return g_early_inputs.exchange(on ? 1 : 0); }
 
 int decode_attn_device_status(void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
