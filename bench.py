@@ -469,7 +469,7 @@ def run_ours(args, rank, world, local_rank):
     import paged_decode_attention_kv_gb300 as da
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    da.decode_attn_set_early_inputs(args.early_inputs == "on")
+    da.decode_attn_set_early_inputs(args.early_inputs)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     # one set = the layer pairs of one step (each pair: a full layer and a ring layer with
@@ -604,10 +604,13 @@ def run_ours(args, rank, world, local_rank):
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
                    "events around every launch in a second pass (includes the launch gap)"),
         "clocks": clocks,
-        "launch": {"early_inputs": args.early_inputs == "on",
-                   "note": ("on: each attention kernel reads the lengths, block table and sinks "
-                            "and works out its split before waiting for the previous kernel; "
-                            "the step's lengths and tables are written before its kernels")},
+        "launch": {"early_inputs": args.early_inputs,
+                   "note": ("level 1: each attention kernel reads the lengths, block table and "
+                            "sinks and works out its split before waiting for the previous "
+                            "kernel; level 2: it also starts its first cache-tile copies. The "
+                            "step's lengths and tables are written before its kernels, and the "
+                            "kernel before each call (the other layer) writes neither them nor "
+                            "the cache the call reads")},
     }
     if per_config is not None:
         result["per_config"] = per_config
@@ -619,7 +622,7 @@ def run_ours(args, rank, world, local_rank):
             "mean of a batch (median, p10, p90 over the 16 batches); direct = launches through "
             "the public API, graph = the replay of a CUDA graph holding the batch's 8 calls, "
             "direct_wait_first = the direct launches with every input read after the wait for "
-            "the previous kernel (decode_attn_set_early_inputs off)")
+            "the previous kernel (decode_attn_set_early_inputs level 0)")
     if world == 1 and not args.no_cpu_baseline:
         v, cores, desc = oracle_sample(args.workload, first, args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores,
@@ -675,6 +678,10 @@ def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
         set_bytes = first.nbytes() + sum(t.numel() * t.element_size() for t in
                                          (first.q, first.k_new, first.v_new, first.out_full, first.out_ring))
         n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
+        # calls of one kind back to back: at level 2 no call may read the cache that the call
+        # just before it appended to, so the sets alternate
+        if args.early_inputs == 2:
+            n_sets = max(2, n_sets)
         sets = [first] + [StepInputs(name, dev, seed_offset=k * 10007, kv=args.kv) for k in range(1, n_sets)]
         c = first.cfg
         shape = (c["B"], c["Hq"], c["Hkv"], c["D"])
@@ -699,10 +706,10 @@ def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
             res = {"direct": timed_batches(n_sets, direct, n_batches, per_batch, gate),
                    "graph": timed_batches(n_sets, lambda i: graphs[i % n_graphs].replay(), n_batches,
                                           per_batch, gate)}
-            if args.early_inputs == "on":  # the same direct launches, every read after the wait
-                da.decode_attn_set_early_inputs(False)
+            if args.early_inputs > 0:  # the same direct launches, every read after the wait
+                da.decode_attn_set_early_inputs(0)
                 res["direct_wait_first"] = timed_batches(n_sets, direct, n_batches, per_batch, gate)
-                da.decode_attn_set_early_inputs(True)
+                da.decode_attn_set_early_inputs(args.early_inputs)
             e = {}
             for mode, xs in res.items():
                 med, p10, p90 = quantiles(xs)
@@ -797,10 +804,12 @@ def main():
     ap.add_argument("--per-config", default="auto", choices=["auto", "on", "off"],
                     help="time the paged and ring calls of every workload (b1, b64, long1, long8, "
                          "serve) per call; auto: on for one-token steps without --rope")
-    ap.add_argument("--early-inputs", default="on", choices=["on", "off"],
-                    help="launch order of the attention kernels: on = lengths, block tables and "
-                         "sinks are read before waiting for the previous kernel (they are written "
-                         "once per step, before its kernels), off = every read waits")
+    ap.add_argument("--early-inputs", type=int, default=2, choices=[0, 1, 2],
+                    help="what the attention kernels read before waiting for the previous kernel "
+                         "(decode_attn_set_early_inputs): 0 nothing, 1 lengths, block tables and "
+                         "sinks, 2 those and the first cache tiles. The step's lengths and tables "
+                         "are written before its kernels and no call reads a cache the kernel "
+                         "just before it wrote")
     ap.add_argument("--batch-limit", type=int, default=None,
                     help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()

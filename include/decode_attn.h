@@ -313,25 +313,29 @@ DA_API int decode_attn_reserve(size_t bytes);
 DA_API int decode_attn_test_expire_wait(int tile);
 
 /*
- * decode_attn_set_early_inputs -- the launch order of the attention kernels, process-wide.
- * Every attention kernel is launched as a programmatic dependent of the kernel before it in
- * the stream: it may start while that kernel is still running and waits for it before it
- * reads an input. With on = 0 (the default) it waits before its first read of anything.
- * With on = 1 it first reads seq_lens, q_lens, block_table and sinks, works out its split
- * of the keys and loads the block-table entries of its first tiles, and only then waits
- * (before reading q, k_new, v_new, the rotary tables or the cache, and before writing
- * anything): a small call then spends a few microseconds less between the previous
- * kernel's end and its first cache tile.
- * Set on = 1 only when, for every attention call, seq_lens, q_lens, block_table and sinks
- * were written before the kernel launched directly before that call started: by host
- * copies or earlier kernels, not by that kernel (an engine that uploads the step's lengths
- * and tables once and then runs its layers, each attention call preceded by a projection,
- * qualifies). If that kernel was itself launched as a programmatic dependent and lets its
- * own dependents start before it has waited for its predecessor, the same must hold for
- * the predecessor. The library's own kernels let the next kernel start only after their
- * wait. Returns the previous setting (0 or 1).
+ * decode_attn_set_early_inputs -- what the attention kernels read before they wait for the
+ * kernel launched just before them in the stream (process-wide). Every attention kernel is
+ * launched as a programmatic dependent of that kernel: it may start while it is still
+ * running and waits for it before reading anything the level below does not name.
+ *   level 0 (the default): nothing is read before the wait.
+ *   level 1: seq_lens, q_lens, block_table and sinks are read, the split of the keys is
+ *            worked out and the block-table entries of the first tiles are loaded before the
+ *            wait. Valid when those four were written before the previous kernel started
+ *            (by host copies or by earlier kernels), not by that kernel.
+ *   level 2: as level 1, and each worker also fetches its first cache tiles (up to its
+ *            pipeline depth) into L2 before the wait. Valid when, in addition, the cache
+ *            rows the call reads were not written by the previous kernel. The call's own
+ *            append is applied after the wait, as at every level.
+ * q, k_new, v_new and the rotary tables are always read, and the output and the cache always
+ * written, after the wait. An engine that uploads a step's lengths and tables before the
+ * step and then runs its layers, each attention call preceded by a projection or another
+ * layer's attention, meets level 2; so does a captured step replayed after the uploads. If the
+ * previous kernel was itself launched as a programmatic dependent and lets its dependents
+ * start before it has waited for its own predecessor, that predecessor must meet the same
+ * conditions (this library's kernels let the next kernel start only after their own wait).
+ * Returns the previous level, or DA_ERR_INVALID_ARG for a level outside 0..2 (unchanged).
  */
-DA_API int decode_attn_set_early_inputs(int on);
+DA_API int decode_attn_set_early_inputs(int level);
 
 /* Wait for `stream`, then return the device status word (DA_STATUS_* bits, 0
  * if clean) of the current device and clear it; negative DA_ERR_CUDA on

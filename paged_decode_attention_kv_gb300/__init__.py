@@ -357,12 +357,16 @@ def decode_attn_device_status(stream=None) -> int:
     return rc
 
 
-def decode_attn_set_early_inputs(on: bool) -> bool:
-    """Process-wide launch order of the attention kernels; returns the previous setting.
-    True: seq_lens, q_lens, block_table and sinks are read before waiting for the kernel
-    launched just before each call, so they must have been written before that kernel
-    started (host copies or earlier kernels). False (the default): every read waits."""
-    return bool(load_library().decode_attn_set_early_inputs(1 if on else 0))
+def decode_attn_set_early_inputs(level: int) -> int:
+    """Process-wide: what the attention kernels read before waiting for the kernel launched
+    just before each call; returns the previous level. 0 (default): nothing. 1: seq_lens,
+    q_lens, block_table and sinks (they must have been written before that kernel started).
+    2: as 1, and the first cache tiles of each worker are fetched into L2 (the cache rows
+    read must not have been written by that kernel either)."""
+    rc = load_library().decode_attn_set_early_inputs(int(level))
+    if rc < 0:
+        _check(rc)
+    return rc
 
 
 def decode_attn_test_expire_wait(tile: int):

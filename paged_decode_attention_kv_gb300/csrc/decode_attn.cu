@@ -179,7 +179,10 @@ struct Params {
     // 1: seq_lens, q_lens, block_table and sinks were final before the previous kernel in the
     // stream started, so the lengths, the split and the first block-table entries are read
     // and worked out before waiting for that kernel (the rest, from the first query row and
-    // cache tile on, after the wait); 0: every input is read after the wait
+    // cache tile on, after the wait); 2: as 1, and the cache rows the call reads were too,
+    // so each worker's first cache tiles are also fetched into L2 before the wait (into
+    // shared memory after it, with its query rows and new tokens); 0: every input is read
+    // after the wait
     int early;
 };
 
@@ -226,6 +229,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// L2 prefetches: no shared memory, no barrier
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
@@ -813,6 +828,52 @@ __global__ void __launch_bounds__(kThreads, CPS)
     bool failed = false;
     bool slots_ok = true;  // false after an expired wait: this warp's area is never read or written again
 
+    // The segments this CTA shares with other CTAs, from the unit prefix alone (so the tickets
+    // never depend on what the warps publish): the one holding its first unit (partial slot
+    // 0) and the one holding its last unit (slot 1), and for each the contributing CTAs
+    // (first, count) and the slot of the first one: s_flag[2..7] and s_flag[8 + 3k ..]. The
+    // last warp works them out once the split is known, off the merge's path (before the
+    // wait for the previous kernel when the split is worked out early); lanes 0 and 1 find
+    // the two segments, lanes 0..3 the CTAs holding their first and last units, at once.
+    auto find_boundary_segments = [&]() {
+        int f = 0, e = 0, sg = -1;
+        if (lane < 2) sg = segment_of_unit(s_pre, B, Hkv, lane == 0 ? R0 : R1 - 1, f, e);
+        const int sa = __shfl_sync(0xffffffffu, sg, 0), fa = __shfl_sync(0xffffffffu, f, 0),
+                  ea = __shfl_sync(0xffffffffu, e, 0);
+        const int sz = __shfl_sync(0xffffffffu, sg, 1), fz = __shfl_sync(0xffffffffu, f, 1),
+                  ez = __shfl_sync(0xffffffffu, e, 1);
+        const bool sh0 = fa < R0 || ea > R1;   // the first unit's segment crosses a CTA edge
+        const bool sh1 = sz != sa && ez > R1;  // the last unit's, when another one
+        int c = 0, cs = 0;  // lane j < 4: segment j / 2, its first (j even) or last unit
+        if (lane < 4 && ((lane >> 1) == 0 ? sh0 : sh1)) {
+            const int x = (lane >> 1) == 0 ? ((lane & 1) ? ea - 1 : fa) : ((lane & 1) ? ez - 1 : fz);
+            // the CTA whose range holds unit x: start from an estimate
+            c = min(n_cta - 1, static_cast<int>(static_cast<float>(x) * (static_cast<float>(n_cta) / U)));
+            while (c > 0 && cta_start(c) > x) --c;
+            while (c + 1 < n_cta && cta_start(c + 1) <= x) ++c;
+            cs = cta_start(c);
+        }
+        int cc[4], ccs[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            cc[j] = __shfl_sync(0xffffffffu, c, j);
+            ccs[j] = __shfl_sync(0xffffffffu, cs, j);
+        }
+        if (lane == 0) {
+            auto shared_seg = [&](int k, int seg, int s0, int s1) {
+                s_flag[2 + k] = seg;
+                s_flag[4 + 2 * k] = s0;
+                s_flag[5 + 2 * k] = s1;
+                s_flag[8 + 3 * k] = cc[2 * k];
+                s_flag[9 + 3 * k] = cc[2 * k + 1] - cc[2 * k] + 1;
+                // the first contributing CTA may have started before this segment (its slot 1)
+                s_flag[10 + 3 * k] = ccs[2 * k] < s0 ? 1 : 0;
+            };
+            if (sh0) shared_seg(0, sa, fa, ea);
+            if (sh1) shared_seg(1, sz, fz, ez);
+        }
+    };
+    if (!active && warp == kWarps - 1) find_boundary_segments();
     if (early && !active) wait_previous();
     if (active) {
         __syncwarp();
@@ -841,11 +902,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
         load_batch(0, cb, cg, ct, cp);
         if (n_tiles > 32) load_batch(1, nb, ng, ntl, np);
         int cur_batch = 0;
-        if (early) wait_previous();  // query rows, new tokens and cache tiles from here on
 
         // Copies of tiles j0 .. j0 + cnt - 1 (cnt <= kStages, calls in increasing order): lane u
         // issues tile j0 + u into stage (stg0 + u) mod kStages, so several tiles go out at once.
-        auto issue_n = [&](int j0, int cnt, int stg0) {
+        // prefetch_only: the cache tiles into L2, nothing else (no stage, barrier or status)
+        auto issue_n = [&](int j0, int cnt, int stg0, bool prefetch_only = false) {
             if ((j0 >> 5) != cur_batch) {  // advance to the next batch, prefetch the one after
                 cb = nb; cg = ng; ct = ntl; cp = np;
                 ++cur_batch;
@@ -865,19 +926,31 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 const int p2 = __shfl_sync(0xffffffffu, np, src);
                 if (nxt) { tb = b2; tg = g2; tt = t2; tp = p2; }
             }
-            if (lane < cnt) {
+            if (prefetch_only) {
+                if (lane < cnt && (RING || (tp >= 0 && tp < p.num_pages))) {
+                    if constexpr (KV8) {
+                        const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
+                                                : static_cast<size_t>(tp) * Hkv + tg;
+                        bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.k_cache) + blk * kBlk8Bytes, kBlk8Bytes);
+                    } else {
+                        const int c1 = RING ? tt * kPage : 0, c2 = RING ? tb * Hkv + tg : tp * Hkv + tg;
+                        tma_prefetch_3d(&tmk, 0, c1, c2);
+                        tma_prefetch_3d(&tmv, 0, c1, c2);
+                    }
+                }
+            } else if (lane < cnt) {
                 const int stg = stg0 + lane < kStages ? stg0 + lane : stg0 + lane - kStages;
                 if (!RING && (tp < 0 || tp >= p.num_pages)) {
                     flag_status(DA_STATUS_BAD_PAGE);
                     tp = -1;  // TMA reads zeros out of bounds
                 }
                 const bool newseg = (j == 0) || (tt == 0);
-                wmeta[stg] = make_int4(tb, tg, tt, tp);
                 const uint32_t bar = bar0 + 8 * stg;
                 const bool rows = !MT && newseg && p.k_new != nullptr;
                 const bool rope = ROPE && newseg;
                 // query rows this CTA stages: its row group's share of the T G (MT), or G
                 const int qrows = MT ? min(GP, max(0, p.T * p.G - r0g)) : p.G;
+                wmeta[stg] = make_int4(tb, tg, tt, tp);
                 mbar_expect_tx(bar, Lay::kStageBytes + (newseg ? qrows * kD * 2 : 0) + (rows ? 4 * kD : 0) +
                                         (rope ? 4 * kD : 0));
                 // a new segment's rows first: with several tiles issued at once, a stage's
@@ -927,10 +1000,27 @@ __global__ void __launch_bounds__(kThreads, CPS)
             }
         };
 
-        if (kParIssue || DA_PAR_FILL) {
-            issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0);
+        // the first copies of every stage (with early == 2 their cache tiles are first fetched
+        // into L2 before the wait for the previous kernel, all at once)
+        auto first_copies = [&]() {
+            if (kParIssue || DA_PAR_FILL) {
+                issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0);
+            } else {
+                for (int j = 0; j < n_tiles && j < kStages; ++j) issue_n(j, 1, j);
+            }
+        };
+        if (p.early == 2) {
+            issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0, true);
+            if (warp == kWarps - 1) find_boundary_segments();
+            wait_previous();
+            first_copies();
+        } else if (early) {
+            if (warp == kWarps - 1) find_boundary_segments();
+            wait_previous();  // query rows, new tokens and cache tiles from here on
+            first_copies();
         } else {
-            for (int j = 0; j < n_tiles && j < kStages; ++j) issue_n(j, 1, j);
+            first_copies();
+            if (warp == kWarps - 1) find_boundary_segments();  // while the first tiles land
         }
 
         // segment context
@@ -1608,49 +1698,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 merge_items(std::integral_constant<int, 16>{});
         }
     }
-    // Meanwhile the last warp works out this CTA's segments shared with other CTAs from the
-    // unit prefix alone: the one holding its first unit (partial slot 0) and the one holding
-    // its last unit (slot 1), and for each the contributing CTAs (first, count) and the slot
-    // of the first one: s_flag[2..7] and s_flag[8 + 3k ..]. Lanes 0 and 1 find the two
-    // segments, lanes 0..3 the CTAs holding their first and last units, all at once.
-    if (warp == kWarps - 1) {
-        int f = 0, e = 0, sg = -1;
-        if (lane < 2) sg = segment_of_unit(s_pre, B, Hkv, lane == 0 ? R0 : R1 - 1, f, e);
-        const int sa = __shfl_sync(0xffffffffu, sg, 0), fa = __shfl_sync(0xffffffffu, f, 0),
-                  ea = __shfl_sync(0xffffffffu, e, 0);
-        const int sz = __shfl_sync(0xffffffffu, sg, 1), fz = __shfl_sync(0xffffffffu, f, 1),
-                  ez = __shfl_sync(0xffffffffu, e, 1);
-        const bool sh0 = fa < R0 || ea > R1;   // the first unit's segment crosses a CTA edge
-        const bool sh1 = sz != sa && ez > R1;  // the last unit's, when another one
-        int c = 0, cs = 0;  // lane j < 4: segment j / 2, its first (j even) or last unit
-        if (lane < 4 && ((lane >> 1) == 0 ? sh0 : sh1)) {
-            const int x = (lane >> 1) == 0 ? ((lane & 1) ? ea - 1 : fa) : ((lane & 1) ? ez - 1 : fz);
-            // the CTA whose range holds unit x: start from an estimate
-            c = min(n_cta - 1, static_cast<int>(static_cast<float>(x) * (static_cast<float>(n_cta) / U)));
-            while (c > 0 && cta_start(c) > x) --c;
-            while (c + 1 < n_cta && cta_start(c + 1) <= x) ++c;
-            cs = cta_start(c);
-        }
-        int cc[4], ccs[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            cc[j] = __shfl_sync(0xffffffffu, c, j);
-            ccs[j] = __shfl_sync(0xffffffffu, cs, j);
-        }
-        if (lane == 0) {
-            auto shared_seg = [&](int k, int seg, int s0, int s1) {
-                s_flag[2 + k] = seg;
-                s_flag[4 + 2 * k] = s0;
-                s_flag[5 + 2 * k] = s1;
-                s_flag[8 + 3 * k] = cc[2 * k];
-                s_flag[9 + 3 * k] = cc[2 * k + 1] - cc[2 * k] + 1;
-                // the first contributing CTA may have started before this segment (its slot 1)
-                s_flag[10 + 3 * k] = ccs[2 * k] < s0 ? 1 : 0;
-            };
-            if (sh0) shared_seg(0, sa, fa, ea);
-            if (sh1) shared_seg(1, sz, fz, ez);
-        }
-    }
     // (no fence here: the ticket-taking thread's fence below publishes every thread's partials)
     __syncthreads();
 
@@ -2000,7 +2047,7 @@ int prepare_workspace(int dev, int G, cudaStream_t stream, float **part, int **c
 // Testing aid (decode_attn_test_expire_wait): the tile wait at which the next one-token
 // call's first worker gives up; -1 = none. Taken (and cleared) by that call.
 std::atomic<int> g_expire_next{-1};
-// decode_attn_set_early_inputs: 1 = the lengths and tables are read before the wait
+// decode_attn_set_early_inputs: what is read before the wait for the previous kernel
 std::atomic<int> g_early_inputs{0};
 
 int run_attention(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
@@ -2728,7 +2775,10 @@ int decode_attn_test_expire_wait(int tile) {
     return DA_OK;
 }
 
-int decode_attn_set_early_inputs(int on) { return g_early_inputs.exchange(on ? 1 : 0); }
+int decode_attn_set_early_inputs(int level) {
+    if (level < 0 || level > 2) return DA_ERR_INVALID_ARG;
+    return g_early_inputs.exchange(level);
+}
 
 int decode_attn_device_status(void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -1,6 +1,7 @@
-"""The early-inputs launch order (decode_attn_set_early_inputs): each attention kernel reads
-the lengths, block table and sinks and works out its split before it waits for the kernel
-launched just before it; the query rows, new tokens, cache and output come after the wait.
+"""The early-input levels (decode_attn_set_early_inputs): at level 1 each attention kernel
+reads the lengths, block table and sinks and works out its split before it waits for the
+kernel launched just before it, at level 2 it also fetches its first cache tiles into L2; the
+query rows, new tokens and output (and the append) come after the wait.
 
 Checked against the oracle: calls whose q / k_new / v_new and output buffer are written by
 the kernel launched directly before them (so a read or write on the wrong side of the wait
@@ -25,19 +26,21 @@ pytestmark = pytest.mark.gpu
 DEV = gd.DEV
 
 
-@pytest.fixture
-def early():
-    prev = da.decode_attn_set_early_inputs(True)
-    yield
+@pytest.fixture(params=[1, 2])
+def early(request):
+    prev = da.decode_attn_set_early_inputs(request.param)
+    yield request.param
     da.decode_attn_set_early_inputs(prev)
 
 
-def test_switch_returns_the_previous_setting():
-    prev = da.decode_attn_set_early_inputs(True)
+def test_switch_returns_the_previous_level():
+    prev = da.decode_attn_set_early_inputs(2)
     try:
-        assert da.decode_attn_set_early_inputs(True) is True
-        assert da.decode_attn_set_early_inputs(False) is True
-        assert da.decode_attn_set_early_inputs(False) is False
+        assert da.decode_attn_set_early_inputs(1) == 2
+        assert da.decode_attn_set_early_inputs(0) == 1
+        with pytest.raises(da.DecodeAttnError):
+            da.decode_attn_set_early_inputs(3)
+        assert da.decode_attn_set_early_inputs(0) == 0
     finally:
         da.decode_attn_set_early_inputs(prev)
 
@@ -111,21 +114,22 @@ def test_many_segments_and_one_long_sequence(early):
     gd.test_repeated_calls_are_identical()
 
 
-def test_same_bits_as_waiting_first():
+def test_same_bits_at_every_level():
     rng = np.random.default_rng(31)
     lens = [0] * 4 + list(rng.integers(1, 9000, size=40)) + [60000]
     c = make_case(920, len(lens), 64, 8, 64, lens)
     kp, vp, bt = gd.paged_setup(c, 13)
     outs = {}
-    for mode in (False, True):
-        prev = da.decode_attn_set_early_inputs(mode)
+    for level in (0, 1, 2):
+        prev = da.decode_attn_set_early_inputs(level)
         try:
-            outs[mode], _, _ = gd.run_paged(c, kp, vp, bt, 0)
+            outs[level], _, _ = gd.run_paged(c, kp, vp, bt, 0)
         finally:
             da.decode_attn_set_early_inputs(prev)
-    np.testing.assert_array_equal(outs[False], outs[True])
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
     ref = oracle.decode_paged(c.q, c.k_new, c.v_new, kp, vp, bt, c.lens, c.sinks, 0, c.scale, c.P)
-    gd.assert_close(outs[True], ref, "early inputs, mixed batch")
+    gd.assert_close(outs[2], ref, "early inputs, mixed batch")
 
 
 @pytest.mark.parametrize("T", [2, 4])
