@@ -1568,6 +1568,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
         wi[9] = slots_ok ? 1 : 0;
     }
     __syncthreads();
+    // the CTA's boundary segments (final before the loop) and their contributors, in registers
+    const int bseg0 = s_flag[2], bseg1 = s_flag[3];
+    const int bclo0 = s_flag[8], bnc0 = s_flag[9], blo0 = s_flag[10];
+    const int bclo1 = s_flag[11], bnc1 = s_flag[12], blo1 = s_flag[13];
 
     // ---- 4. merge segments shared between warps of this CTA (all threads take part)
     // Segments shared by several warps: every warp of this CTA holding a state of one (warps
@@ -1703,7 +1707,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
 
     // ---- 5. segments shared with other CTAs: the last CTA to arrive combines them
     if (tid == 0) {
-        const int cand0 = s_flag[2], cand1 = s_flag[3];
+        const int cand0 = bseg0, cand1 = bseg1;
         // the barrier above orders every thread's partial stores before this fence, which
         // orders them (cumulatively, at GPU scope) before the tickets
         if (cand0 >= 0 || cand1 >= 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
@@ -1711,8 +1715,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
         const int t0 = cand0 >= 0 ? atomicAdd(counters + cand0, 1) : 0;
         const int t1 = cand1 >= 0 ? atomicAdd(counters + cand1, 1) : 0;
         // the CTA taking the last ticket of a segment combines it
-        s_flag[0] = (cand0 >= 0 && t0 == s_flag[9] - 1) ? cand0 : -1;
-        s_flag[1] = (cand1 >= 0 && t1 == s_flag[12] - 1) ? cand1 : -1;
+        s_flag[0] = (cand0 >= 0 && t0 == bnc0 - 1) ? cand0 : -1;
+        s_flag[1] = (cand1 >= 0 && t1 == bnc1 - 1) ? cand1 : -1;
         // the other CTAs' partials, ordered before their tickets, are visible after this fence
         if (s_flag[0] >= 0 || s_flag[1] >= 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
@@ -1727,7 +1731,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     for (int k = 0; k < 2; ++k) {
         const int seg = s_flag[k];
         if (seg < 0) continue;
-        const int c_lo = s_flag[8 + 3 * k], nc = s_flag[9 + 3 * k], lo_slot = s_flag[10 + 3 * k];
+        const int c_lo = k == 0 ? bclo0 : bclo1, nc = k == 0 ? bnc0 : bnc1, lo_slot = k == 0 ? blo0 : blo1;
         const int b = seg / Hkv, g = seg - b * Hkv;
         float M = -INFINITY, den = 0.f, acc[kPer];
 #pragma unroll
