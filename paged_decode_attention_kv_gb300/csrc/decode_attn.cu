@@ -140,7 +140,7 @@ constexpr int kMaxBatch = 1024;
 constexpr int kMaxSegments = 65536;         // B * Hkv
 constexpr int kMaxQHeads = 1024;
 constexpr int kMaxNewMT = 4;   // query tokens per sequence of the MT kernel at most
-constexpr int kWinfo = 12;     // ints of per-warp bookkeeping in shared memory
+constexpr int kWinfo = 16;     // ints of per-warp bookkeeping in shared memory
 constexpr int kCounterBytes = kMaxSegments * 4;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s of SM clock per tile wait
 constexpr int kMaxSmem = 232448;                       // opt-in shared memory per block
@@ -799,6 +799,41 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int ue = active ? R0 + (warp + 1) * q_w + ((warp + 1) * r_w) / nw_cta : 0;
     const int n_tiles = ue - ua;
 
+    // The warp's merge plan, fixed by the split alone: its head segment (the first one, when
+    // it started before ua) and tail segment (the last one, when it goes on after ue; a single
+    // segment that crosses either edge counts as the tail), their unit ranges, and for each
+    // the warps of this CTA holding it (wa and their count: the warps whose ranges meet it,
+    // found by all lanes at once), in the warp's row of s_winfo: [2] head, [3] tail, [5..8]
+    // their ranges, [12..15] wa and count of each. Worked out before the loop (before the
+    // wait for the previous kernel at early levels), so the merges start at once.
+    if (active) {
+        int f = 0, e = 0, sg = -1;
+        if (lane < 2) sg = segment_of_unit(s_pre, B, Hkv, lane == 0 ? ua : ue - 1, f, e);
+        const int sF = __shfl_sync(0xffffffffu, sg, 0), fF = __shfl_sync(0xffffffffu, f, 0),
+                  eF = __shfl_sync(0xffffffffu, e, 0);
+        const int sL = __shfl_sync(0xffffffffu, sg, 1), fL = __shfl_sync(0xffffffffu, f, 1),
+                  eL = __shfl_sync(0xffffffffu, e, 1);
+        int hs = -1, ts = -1;
+        if (sF == sL) {
+            if (fF < ua || eL > ue) ts = sL;
+        } else {
+            if (fF < ua) hs = sF;
+            if (eL > ue) ts = sL;
+        }
+        // lane w < nw_cta: warp w's range [st, st1)
+        const int st0 = lane <= nw_cta ? R0 + lane * q_w + (lane * r_w) / nw_cta : R1;
+        const int st1 = __shfl_down_sync(0xffffffffu, st0, 1);
+        const uint32_t mh = __ballot_sync(0xffffffffu, lane < nw_cta && st0 < eF && st1 > fF);
+        const uint32_t mt = __ballot_sync(0xffffffffu, lane < nw_cta && st0 < eL && st1 > fL);
+        if (lane == 0) {
+            int *wi = s_winfo + warp * kWinfo;
+            wi[0] = ua; wi[1] = ue; wi[2] = hs; wi[3] = ts; wi[4] = 1;
+            wi[5] = fF; wi[6] = eF; wi[7] = fL; wi[8] = eL;
+            wi[12] = __ffs(static_cast<int>(mh)) - 1; wi[13] = __popc(mh);
+            wi[14] = __ffs(static_cast<int>(mt)) - 1; wi[15] = __popc(mt);
+        }
+    }
+
     uint8_t *wbase = smem + warp * kWarpBytes;
     const uint32_t wbase_s = smem_addr(wbase);
     // offsets of a stage's K tile, V tile and (fp8) scale rows in the warp's area
@@ -824,7 +859,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
     float sig[NT][2];      // sink logits (log2 units) of this lane's heads
     uint32_t qf[NT][4][2]; // Q as mma B operand
     int head_seg = -1, tail_seg = -1;
-    int head_s0 = 0, head_s1 = 0, tail_s0 = 0, tail_s1 = 0;  // unit ranges of those segments
     bool failed = false;
     bool slots_ok = true;  // false after an expired wait: this warp's area is never read or written again
 
@@ -1358,8 +1392,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     if (seg_first_unit < ua) {  // shared with earlier workers: keep for merge
                         head = st;
                         head_seg = sb * Hkv + sgk;
-                        head_s0 = seg_first_unit;
-                        head_s1 = seg_end_unit;
                     } else if constexpr (MT) {
                         state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, r0g, lane);
                     } else {
@@ -1548,8 +1580,6 @@ __global__ void __launch_bounds__(kThreads, CPS)
         const bool last_shared = failed || seg_first_unit < ua || seg_end_unit > ue;
         if (last_shared) {
             tail_seg = sb * Hkv + sgk;
-            tail_s0 = seg_first_unit;
-            tail_s1 = seg_end_unit;
         } else if constexpr (MT) {
             state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, r0g, lane);
         } else {
@@ -1561,12 +1591,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
         if (slots_ok && tail_seg >= 0) state_to_slot(st, &slots[1], lane);
     }
     zero_inactive();
-    if (lane == 0) {
-        int *wi = s_winfo + warp * kWinfo;
-        wi[0] = ua; wi[1] = ue; wi[2] = head_seg; wi[3] = tail_seg; wi[4] = active ? 1 : 0;
-        wi[5] = head_s0; wi[6] = head_s1; wi[7] = tail_s0; wi[8] = tail_s1;
-        wi[9] = slots_ok ? 1 : 0;
-    }
+    // (the states published in the slots are the plan's head and tail: a warp whose copies
+    // never landed is left out of the merges)
+    if (lane == 0) s_winfo[warp * kWinfo + 9] = slots_ok ? 1 : 0;
     __syncthreads();
     // the CTA's boundary segments (final before the loop) and their contributors, in registers
     const int bseg0 = s_flag[2], bseg1 = s_flag[3];
@@ -1590,16 +1617,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
             const int seg = wi[2 + which];
             if (seg < 0) continue;
             const int s0 = wi[5 + 2 * which], s1 = wi[6 + 2 * which];
-            // the warps of this CTA holding a state of seg, wa .. wb: ranges are contiguous and
-            // ordered, so warp w < warp holds it iff its range ends after s0, and w > warp iff
-            // its range starts before s1 (independent loads, no chain)
-            int wa = 0, wb = warp;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                if (w < warp && s_winfo[w * kWinfo + 1] <= s0) ++wa;
-                if (w > warp && w < nw_cta && s_winfo[w * kWinfo] < s1) ++wb;
-            }
-            const int k = wb - wa + 1, mine = warp - wa;
+            // the warps of this CTA holding a state of seg: wa .. wa + k - 1 (the plan)
+            const int wa = wi[12 + 2 * which], k = wi[13 + 2 * which], mine = warp - wa;
             const bool internal = s0 >= R0 && s1 <= R1;
             const int slot_k = s0 <= R0 ? 0 : 1;
             const int b = seg / Hkv, g = seg - b * Hkv;

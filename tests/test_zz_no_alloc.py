@@ -9,8 +9,10 @@ second call finds the array as the first one left it), and check every output
 row against the fp64 oracle and against decode_attn_paged, which uses the
 library workspace. The cases cover 8- and 16-head query groups, full attention
 and a 128-token window, and a shape exactly at the array's limit of 4096
-(sequence, KV head) pairs. The file is named to be collected last; it passes in a
-fresh process as well as after the other tests.
+(sequence, KV head) pairs, at early-input level 0 and, for the mixed lengths, level 2
+(lengths, tables and the first cache tiles read before the wait for the kernel just
+before the call, which in these tests never writes them). The file is named to be
+collected last; it passes in a fresh process as well as after the other tests.
 """
 import ctypes
 
@@ -84,14 +86,24 @@ def _lens_at_limit():
     return lens
 
 
-@pytest.mark.parametrize("lens_fn,Hq,Hkv,window", [
-    (_lens_mixed, 64, 8, 0),
-    (_lens_mixed, 64, 8, 128),
-    (_lens_mixed, 64, 4, 0),      # 16 query heads per KV head: the widest partial slot
-    (_lens_mixed, 64, 4, 128),
-    (_lens_at_limit, 64, 8, 0),
+@pytest.mark.parametrize("lens_fn,Hq,Hkv,window,level", [
+    (_lens_mixed, 64, 8, 0, 0),
+    (_lens_mixed, 64, 8, 128, 0),
+    (_lens_mixed, 64, 4, 0, 0),      # 16 query heads per KV head: the widest partial slot
+    (_lens_mixed, 64, 4, 128, 0),
+    (_lens_at_limit, 64, 8, 0, 0),
+    (_lens_mixed, 64, 8, 0, 2),
+    (_lens_mixed, 64, 4, 128, 2),
 ])
-def test_noalloc_matches_oracle_and_workspace_entry_on_two_calls(lens_fn, Hq, Hkv, window):
+def test_noalloc_matches_oracle_and_workspace_entry_on_two_calls(lens_fn, Hq, Hkv, window, level):
+    prev = da.decode_attn_set_early_inputs(level)
+    try:
+        _check_two_calls(lens_fn, Hq, Hkv, window)
+    finally:
+        da.decode_attn_set_early_inputs(prev)
+
+
+def _check_two_calls(lens_fn, Hq, Hkv, window):
     fn = _entry()
     lens = lens_fn()
     inp, pool = _inputs(lens, 7 + Hkv + window, Hq, Hkv)
