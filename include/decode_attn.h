@@ -322,10 +322,11 @@ DA_API int decode_attn_test_expire_wait(int tile);
  *            worked out and the block-table entries of the first tiles are loaded before the
  *            wait. Valid when those four were written before the previous kernel started
  *            (by host copies or by earlier kernels), not by that kernel.
- *   level 2: as level 1, and each worker also fetches its first cache tiles (up to its
- *            pipeline depth) into L2 before the wait. Valid when, in addition, the cache
- *            rows the call reads were not written by the previous kernel. The call's own
- *            append is applied after the wait, as at every level.
+ *   level 2: as level 1, and each worker whose share of the keys is longer than its
+ *            pipeline also fetches its first cache tiles into L2 before the wait. Valid
+ *            when, in addition, the cache rows the call reads were not written by the
+ *            previous kernel. The call's own append is applied after the wait, as at every
+ *            level.
  * q, k_new, v_new and the rotary tables are always read, and the output and the cache always
  * written, after the wait. An engine that uploads a step's lengths and tables before the
  * step and then runs its layers, each attention call preceded by a projection or another

@@ -961,15 +961,36 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 if (nxt) { tb = b2; tg = g2; tt = t2; tp = p2; }
             }
             if (prefetch_only) {
-                if (lane < cnt && (RING || (tp >= 0 && tp < p.num_pages))) {
+                if constexpr (RING) {
+                    // a (sequence, KV head) window is contiguous: one prefetch per run of the
+                    // lanes' tiles in one window (the run starts where the previous lane's
+                    // tile is not the one just before)
+                    const int pb = __shfl_up_sync(0xffffffffu, tb, 1), pg = __shfl_up_sync(0xffffffffu, tg, 1),
+                              pt = __shfl_up_sync(0xffffffffu, tt, 1);
+                    const bool start = lane < cnt && (lane == 0 || pb != tb || pg != tg || pt + 1 != tt);
+                    const uint32_t starts = __ballot_sync(0xffffffffu, start);
+                    if (start) {
+                        const uint32_t later = starts & ~((2u << lane) - 1u);
+                        const int len = (later ? __ffs(static_cast<int>(later)) - 1 : cnt) - lane;
+                        const size_t slice = static_cast<size_t>(tb) * Hkv + tg;
+                        if constexpr (KV8) {
+                            const size_t blk = slice * (p.window / kPage) + tt;
+                            bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.k_cache) + blk * kBlk8Bytes,
+                                             static_cast<uint32_t>(len) * kBlk8Bytes);
+                        } else {  // rows tt 16 .. up to the window's end, 128 bytes each
+                            const int r0 = tt * kPage, r1 = min((tt + len) * kPage, p.window);
+                            const size_t off = (slice * p.window + r0) * (kD * 2);
+                            bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.k_cache) + off, (r1 - r0) * kD * 2);
+                            bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.v_cache) + off, (r1 - r0) * kD * 2);
+                        }
+                    }
+                } else if (lane < cnt && tp >= 0 && tp < p.num_pages) {
                     if constexpr (KV8) {
-                        const size_t blk = RING ? (static_cast<size_t>(tb) * Hkv + tg) * (p.window / kPage) + tt
-                                                : static_cast<size_t>(tp) * Hkv + tg;
+                        const size_t blk = static_cast<size_t>(tp) * Hkv + tg;
                         bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.k_cache) + blk * kBlk8Bytes, kBlk8Bytes);
                     } else {
-                        const int c1 = RING ? tt * kPage : 0, c2 = RING ? tb * Hkv + tg : tp * Hkv + tg;
-                        tma_prefetch_3d(&tmk, 0, c1, c2);
-                        tma_prefetch_3d(&tmv, 0, c1, c2);
+                        tma_prefetch_3d(&tmk, 0, 0, tp * Hkv + tg);
+                        tma_prefetch_3d(&tmv, 0, 0, tp * Hkv + tg);
                     }
                 }
             } else if (lane < cnt) {
@@ -1034,8 +1055,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
             }
         };
 
-        // the first copies of every stage (with early == 2 their cache tiles are first fetched
-        // into L2 before the wait for the previous kernel, all at once)
+        // the first copies of every stage (with early == 2, for a warp with more tiles than
+        // stages, their cache tiles are first fetched into L2 before the wait for the previous
+        // kernel); one copy of this code serves every level (the short calls are sensitive to
+        // the kernel's instruction footprint)
         auto first_copies = [&]() {
             if (kParIssue || DA_PAR_FILL) {
                 issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0);
@@ -1043,19 +1066,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 for (int j = 0; j < n_tiles && j < kStages; ++j) issue_n(j, 1, j);
             }
         };
-        if (p.early == 2) {
-            issue_n(0, n_tiles < kStages ? n_tiles : kStages, 0, true);
-            if (warp == kWarps - 1) find_boundary_segments();
-            wait_previous();
-            first_copies();
-        } else if (early) {
+        if (p.early == 2 && n_tiles > kStages) issue_n(0, kStages, 0, true);
+        if (early) {
             if (warp == kWarps - 1) find_boundary_segments();
             wait_previous();  // query rows, new tokens and cache tiles from here on
-            first_copies();
-        } else {
-            first_copies();
-            if (warp == kWarps - 1) find_boundary_segments();  // while the first tiles land
         }
+        first_copies();
+        if (!early && warp == kWarps - 1) find_boundary_segments();  // while the first tiles land
 
         // segment context
         int sb = -1, sgk = -1;  // current segment (b, g)
