@@ -607,10 +607,10 @@ def run_ours(args, rank, world, local_rank):
         "launch": {"early_inputs": args.early_inputs,
                    "note": ("level 1: each attention kernel reads the lengths, block table and "
                             "sinks and works out its split before waiting for the previous "
-                            "kernel; level 2: it also starts its first cache-tile copies. The "
-                            "step's lengths and tables are written before its kernels, and the "
-                            "kernel before each call (the other layer) writes neither them nor "
-                            "the cache the call reads")},
+                            "kernel; level 2: it also starts L2 prefetches of its first cache "
+                            "tiles. The step's lengths and tables are written before its "
+                            "kernels; the kernel before each call (the other layer) does not "
+                            "write them")},
     }
     if per_config is not None:
         result["per_config"] = per_config
@@ -678,8 +678,8 @@ def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
         set_bytes = first.nbytes() + sum(t.numel() * t.element_size() for t in
                                          (first.q, first.k_new, first.v_new, first.out_full, first.out_ring))
         n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
-        # calls of one kind back to back: at level 2 no call may read the cache that the call
-        # just before it appended to, so the sets alternate
+        # calls of one kind back to back: at level 2 no call prefetches the cache that the
+        # call just before it is appending to (the sets alternate)
         if args.early_inputs == 2:
             n_sets = max(2, n_sets)
         sets = [first] + [StepInputs(name, dev, seed_offset=k * 10007, kv=args.kv) for k in range(1, n_sets)]
@@ -807,9 +807,8 @@ def main():
     ap.add_argument("--early-inputs", type=int, default=2, choices=[0, 1, 2],
                     help="what the attention kernels read before waiting for the previous kernel "
                          "(decode_attn_set_early_inputs): 0 nothing, 1 lengths, block tables and "
-                         "sinks, 2 those and the first cache tiles. The step's lengths and tables "
-                         "are written before its kernels and no call reads a cache the kernel "
-                         "just before it wrote")
+                         "sinks, 2 those and L2 prefetches of the first cache tiles. The step's "
+                         "lengths and tables are written before its kernels")
     ap.add_argument("--batch-limit", type=int, default=None,
                     help="keep only the first N sequences (smaller cases for profiler captures)")
     args = ap.parse_args()

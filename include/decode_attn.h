@@ -323,17 +323,19 @@ DA_API int decode_attn_test_expire_wait(int tile);
  *            wait. Valid when those four were written before the previous kernel started
  *            (by host copies or by earlier kernels), not by that kernel.
  *   level 2: as level 1, and each worker whose share of the keys is longer than its
- *            pipeline also fetches its first cache tiles into L2 before the wait. Valid
- *            when, in addition, the cache rows the call reads were not written by the
- *            previous kernel. The call's own append is applied after the wait, as at every
- *            level.
- * q, k_new, v_new and the rotary tables are always read, and the output and the cache always
- * written, after the wait. An engine that uploads a step's lengths and tables before the
- * step and then runs its layers, each attention call preceded by a projection or another
- * layer's attention, meets level 2; so does a captured step replayed after the uploads. If the
- * previous kernel was itself launched as a programmatic dependent and lets its dependents
- * start before it has waited for its own predecessor, that predecessor must meet the same
- * conditions (this library's kernels let the next kernel start only after their own wait).
+ *            pipeline also starts L2 prefetches of its first cache tiles before the wait.
+ *            A prefetch only warms the GPU-wide L2, where a later write by the previous
+ *            kernel still lands, so the cache is read for the attention after the wait as at
+ *            the other levels: the conditions are those of level 1. The call's own append
+ *            is applied after the wait, as at every level.
+ * q, k_new, v_new, the cache and the rotary tables are always read, and the output and the
+ * cache always written, after the wait. An engine that uploads a step's lengths and tables
+ * before the step and then runs its layers, each attention call preceded by a projection or
+ * another layer's attention, meets these conditions; so does a captured step replayed after
+ * the uploads. If the previous kernel was itself launched as a programmatic dependent and
+ * lets its dependents start before it has waited for its own predecessor, that predecessor
+ * must meet the same conditions (this library's kernels let the next kernel start only
+ * after their own wait).
  * Returns the previous level, or DA_ERR_INVALID_ARG for a level outside 0..2 (unchanged).
  */
 DA_API int decode_attn_set_early_inputs(int level);

@@ -361,8 +361,8 @@ def decode_attn_set_early_inputs(level: int) -> int:
     """Process-wide: what the attention kernels read before waiting for the kernel launched
     just before each call; returns the previous level. 0 (default): nothing. 1: seq_lens,
     q_lens, block_table and sinks (they must have been written before that kernel started).
-    2: as 1, and the first cache tiles of each worker are fetched into L2 (the cache rows
-    read must not have been written by that kernel either)."""
+    2: as 1, and the first cache tiles of each long worker share are prefetched into L2 (a
+    hint to the GPU-wide cache: the same conditions as level 1)."""
     rc = load_library().decode_attn_set_early_inputs(int(level))
     if rc < 0:
         _check(rc)
