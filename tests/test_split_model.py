@@ -4,7 +4,9 @@ segment) are ordered (b, g, tile); CTA c takes [cta_start(c), cta_start(c + 1)),
 split's boundary moved to the nearer edge of a short segment; its warps split that range
 evenly. Every unit belongs to exactly one warp, every working CTA and warp has at least one
 unit, a segment of at most `snap` units never spans two CTAs, and the CTA found for a unit
-by searching near the even split is the CTA that owns it.
+by searching near the even split is the CTA that owns it. The merge plan each warp works
+out before its loop (head and tail segment, the consecutive warps holding each) is checked
+against a walk over the warp's units, as the loop meets them.
 
 The arithmetic mirrors the kernel's (32-bit integer formulas); the GPU parity tests run the
 kernel itself on the same kinds of length mixes."""
@@ -139,3 +141,83 @@ def test_ring_segments_of_the_serving_mix_stay_in_one_cta():
         x = cta_start(c)
         _, f, e = segment_of_unit(pre, 8, x)
         assert x == f
+
+
+def merge_plan(pre, Hkv, ua, ue):
+    """The kernel's merge plan for a warp with units [ua, ue), from the split alone: its
+    head segment (the first one, when it starts before ua) and its tail segment (the last one,
+    when it goes on after ue; a single segment crossing either edge counts as the tail)."""
+    sF, fF, eF = segment_of_unit(pre, Hkv, ua)
+    sL, fL, eL = segment_of_unit(pre, Hkv, ue - 1)
+    head = tail = None
+    if sF == sL:
+        if fF < ua or eL > ue:
+            tail = (sL, fL, eL)
+    else:
+        if fF < ua:
+            head = (sF, fF, eF)
+        if eL > ue:
+            tail = (sL, fL, eL)
+    return head, tail
+
+
+def walked_plan(pre, Hkv, ua, ue):
+    """The same two segments as the main loop finds them, walking the warp's units in order:
+    a segment left at a switch is kept (the head) when it began before ua, and the segment open
+    at the end is kept (the tail) when it began before ua or goes on after ue."""
+    head = None
+    cur = None
+    for x in range(ua, ue):
+        seg, f, e = segment_of_unit(pre, Hkv, x)
+        if cur is None or seg != cur[0]:
+            if cur is not None and cur[1] < ua:
+                head = cur
+            cur = (seg, f, e)
+    tail = cur if (cur[1] < ua or cur[2] > ue) else None
+    return head, tail
+
+
+@pytest.mark.parametrize("mix", sorted(LEN_MIXES))
+@pytest.mark.parametrize("ring", [False, True])
+def test_merge_plan_matches_the_walk_and_holders_are_consecutive(mix, ring):
+    """The plan worked out before the loop names the same head and tail segments the loop's
+    walk keeps, every warp of a CTA holding a unit of a shared segment has it in its plan, and
+    the holders of each segment within a CTA are consecutive warps (first warp and count are
+    what the merge uses)."""
+    rng = np.random.default_rng(7 + sum(map(ord, mix)) + ring)
+    lens = LEN_MIXES[mix](rng)
+    Hkv = 8 if mix != "short_many" else 2
+    pre, _ = units_prefix(lens, Hkv, window=128, ring=ring)
+    if int(pre[-1]) == 0:
+        return
+    U, n_cta, cta_start, warps, cta_of, snap_max = split(pre, Hkv, ncta=152)
+    by_cta = {}
+    for c, ua, ue in warps:
+        by_cta.setdefault(c, []).append((ua, ue))
+    checked = 0
+    for c, ranges in by_cta.items():
+        if checked > 40 and mix in ("serve", "max_batch", "b64"):
+            break
+        checked += 1
+        plans = [merge_plan(pre, Hkv, ua, ue) for ua, ue in ranges]
+        for (ua, ue), plan in zip(ranges, plans):
+            assert plan == walked_plan(pre, Hkv, ua, ue)
+        # every segment a warp shares (with another warp or CTA) is in that warp's plan
+        for w, (ua, ue) in enumerate(ranges):
+            x = ua
+            while x < ue:
+                seg, f, e = segment_of_unit(pre, Hkv, x)
+                shared = f < ua or e > ue
+                in_plan = any(p is not None and p[0] == seg for p in plans[w])
+                assert in_plan == shared, (c, w, seg)
+                x = e
+        # holders: the warps whose ranges meet the segment, consecutive
+        for plan in plans:
+            for p in plan:
+                if p is None:
+                    continue
+                seg, f, e = p
+                holders = [w for w, (ua, ue) in enumerate(ranges) if ua < e and ue > f]
+                assert holders == list(range(holders[0], holders[-1] + 1))
+                for w in holders:
+                    assert any(q is not None and q[0] == seg for q in plans[w])
