@@ -549,10 +549,13 @@ def run_ours(args, rank, world, local_rank):
         call_ring(s, args.rope)
         ev_r1[i].record(stream)
     torch.cuda.synchronize()
-    per_config = None
+    per_config = per_config_fp8 = None
     if args.per_config == "on" or (args.per_config == "auto" and args.q_tokens == 1 and not args.rope
                                    and args.layers == 1):
         per_config = per_config_block(args, dev, l2, measured_hbm_peak()[0], nominal_hbm_peak())
+        if args.kv == "bf16":  # the fp8 cache on the two target shapes, the same way
+            per_config_fp8 = per_config_block(args, dev, l2, measured_hbm_peak()[0], nominal_hbm_peak(),
+                                              workloads=("b64", "long1"), kv="fp8")
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     paged_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p0, ev_p1)) / args.steps
@@ -614,6 +617,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if per_config is not None:
         result["per_config"] = per_config
+        if per_config_fp8 is not None:
+            result["per_config_fp8"] = per_config_fp8
         result["per_config_timing"] = (
             "per workload, the paged (full attention) and the ring (window 128) call of the "
             "step, 128 timed calls of each kind: 16 batches of 8 calls of one kind queued back "
@@ -662,7 +667,7 @@ def timed_batches(n_sets, fn, n_batches, per_batch, gate_cycles):
     return out
 
 
-def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
+def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8, workloads=PER_CONFIG, kv=None):
     """µs per call (median, p10 and p90 over n_batches batches of per_batch calls, each batch
     queued back to back: n_batches * per_batch >= 100 timed calls), algorithmic GB/s and the
     fractions of the measured and nominal HBM peaks for the paged and the ring call of every
@@ -673,8 +678,9 @@ def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
     from paged_decode_attention_kv_gb300.graph import DecodeStepGraph
     gate = int(3e-3 * 2.07e9)  # about 3 ms of spin ahead of each batch
     out = {}
-    for name in PER_CONFIG:
-        first = StepInputs(name, dev, kv=args.kv)
+    kv = kv or args.kv
+    for name in workloads:
+        first = StepInputs(name, dev, kv=kv)
         set_bytes = first.nbytes() + sum(t.numel() * t.element_size() for t in
                                          (first.q, first.k_new, first.v_new, first.out_full, first.out_ring))
         n_sets = 1 if set_bytes >= 2 * l2 else min(64, math.ceil(2 * l2 / set_bytes))
@@ -682,11 +688,11 @@ def per_config_block(args, dev, l2, peak, nominal, n_batches=16, per_batch=8):
         # call just before it is appending to (the sets alternate)
         if args.early_inputs == 2:
             n_sets = max(2, n_sets)
-        sets = [first] + [StepInputs(name, dev, seed_offset=k * 10007, kv=args.kv) for k in range(1, n_sets)]
+        sets = [first] + [StepInputs(name, dev, seed_offset=k * 10007, kv=kv) for k in range(1, n_sets)]
         c = first.cfg
         shape = (c["B"], c["Hq"], c["Hkv"], c["D"])
         da.decode_attn_reserve(da.decode_attn_workspace_bytes(*shape))
-        pb, rb = step_bytes(name, first.lens, args.kv)
+        pb, rb = step_bytes(name, first.lens, kv)
         entry = {"timed_calls": n_batches * per_batch, "input_sets": n_sets,
                  "algorithmic_bytes": {"paged_full": pb, "ring": rb},
                  "max_len": max(first.lens), "active": sum(1 for L in first.lens if L > 0)}
