@@ -145,3 +145,40 @@ def test_fp8(early):
 
 def test_captured_step(early):
     gg.test_one_graph_serves_every_active_slot_set()
+
+
+@pytest.mark.parametrize("W", [1000, 1024])
+def test_long_ring_windows_prefetched_by_runs(W):
+    """Level 2 on ring calls whose workers hold more tiles than their pipeline: each run of a
+    worker's tiles in one window is prefetched as one range, up to the window's end (W = 1000
+    ends inside a tile), then read as usual."""
+    rng = np.random.default_rng(W)
+    lens = [int(x) for x in rng.integers(W // 2, 3 * W, size=24)] + [0, W, W + 1]
+    c = make_case(940 + W, len(lens), 64, 8, 64, lens)
+    prev = da.decode_attn_set_early_inputs(2)
+    try:
+        gd.check_ring(c, W)
+    finally:
+        da.decode_attn_set_early_inputs(prev)
+
+
+def test_long_fp8_ring_windows_prefetched_by_runs():
+    W = 1024
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(W // 2, 3 * W, size=24)] + [0, W - 1]
+    c = make_case(960, len(lens), 64, 8, 64, lens)
+    blank = oracle.Fp8Cache.empty_ring(c.B, c.Hkv, W, c.D)
+    cache = oracle.scatter_fp8(c.hist_k, c.hist_v, gf.pre(c), blank, window=W)
+    kv = gf.to_dev(cache)
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    prev = da.decode_attn_set_early_inputs(2)
+    try:
+        da.decode_attn_ring_fp8(gd.dev_bits(c.q), gd.dev_bits(c.k_new), gd.dev_bits(c.v_new), kv,
+                                gd.dev(c.lens), gd.dev(c.sinks), c.scale, out)
+        torch.cuda.synchronize()
+    finally:
+        da.decode_attn_set_early_inputs(prev)
+    assert da.decode_attn_device_status() == 0
+    ref = oracle.decode_ring_fp8(c.q, c.k_new, c.v_new, cache, c.lens, c.sinks, W, c.scale)
+    gd.assert_close(out.double().cpu().numpy(), ref, "ring fp8 W=1024, level 2")
+    gf.assert_blocks_equal(gf.from_dev(kv), oracle.kv_append_fp8(c.k_new, c.v_new, cache, c.lens, window=W))
