@@ -39,7 +39,8 @@
  *     by decode_attn_reserve(); during stream capture a call that would need
  *     a larger workspace returns DA_ERR_WORKSPACE instead of allocating.
  *     Calls that run concurrently on different streams of one device share
- *     this workspace and must not overlap.
+ *     this workspace and must not overlap, unless each of those streams has a
+ *     workspace of its own (decode_attn_stream_reserve).
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H
@@ -298,6 +299,33 @@ DA_API size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len);
 /* Make sure the current device's workspace holds at least `bytes` (allocates
  * and zeroes synchronously). Call before capturing a CUDA graph. */
 DA_API int decode_attn_reserve(size_t bytes);
+
+/*
+ * decode_attn_stream_reserve -- give the attention calls issued on `stream` (a cudaStream_t
+ * of the current device, as void*) workspaces of their own, so that they may run at the
+ * same time as calls on other streams (two layers or two micro-batches in flight at once).
+ * The pages describe one stream of kernels; this is an interface choice of the library.
+ *   - `bytes` and `multi_bytes`: sizes to hold at least now, for one-token calls
+ *     (decode_attn_workspace_bytes) and several-token calls
+ *     (decode_attn_multi_workspace_bytes); 0 allocates nothing yet. The first call on the
+ *     stream outside a capture grows a workspace that is too small, as for the device's.
+ *   - Both are owned by the library, allocated and zeroed synchronously, and held until
+ *     decode_attn_stream_release(stream). Calls on streams without a reservation keep
+ *     using the device's workspace. Calls on one stream still run in order, so they
+ *     share its workspaces safely.
+ *   - Returns DA_ERR_WORKSPACE while `stream` is capturing, DA_ERR_INVALID_ARG if the
+ *     stream already has workspaces on another device, DA_ERR_CUDA if allocation fails.
+ */
+DA_API int decode_attn_stream_reserve(void *stream, size_t bytes, size_t multi_bytes);
+
+/*
+ * decode_attn_stream_release -- synchronise `stream` and free the workspaces that
+ * decode_attn_stream_reserve gave it; later calls on it use the device's workspace again.
+ * A graph captured on the stream keeps the freed addresses: do not launch it afterwards.
+ * Release before destroying the stream (a new stream may get the same handle). Returns
+ * DA_OK also when the stream has none, DA_ERR_WORKSPACE while it is capturing.
+ */
+DA_API int decode_attn_stream_release(void *stream);
 
 /*
  * decode_attn_test_expire_wait -- a testing aid for the bounded-wait failure path. It arms a

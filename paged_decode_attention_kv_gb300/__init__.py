@@ -32,6 +32,7 @@ __all__ = [
     "decode_attn_paged_multi", "decode_attn_ring_multi", "decode_attn_multi_workspace_bytes",
     "decode_attn_multi_reserve", "decode_attn_multi_launches", "decode_attn_test_expire_wait",
     "decode_attn_paged_fp8_rope", "decode_attn_ring_fp8_rope", "decode_attn_set_early_inputs",
+    "decode_attn_stream_reserve", "decode_attn_stream_release",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -110,6 +111,8 @@ def load_library():
     lib.decode_attn_workspace_bytes.argtypes = [da_shape, c_int]
     lib.decode_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_reserve.argtypes = [ctypes.c_size_t]
+    lib.decode_attn_stream_reserve.argtypes = [vp, ctypes.c_size_t, ctypes.c_size_t]
+    lib.decode_attn_stream_release.argtypes = [vp]
     lib.decode_attn_device_status.argtypes = [vp]
     lib.decode_attn_test_expire_wait.argtypes = [c_int]
     lib.decode_attn_set_early_inputs.argtypes = [c_int]
@@ -120,7 +123,8 @@ def load_library():
                lib.decode_attn_paged_fp8, lib.decode_attn_ring_fp8, lib.decode_attn_paged_multi,
                lib.decode_attn_ring_multi, lib.decode_attn_multi_reserve,
                lib.decode_attn_test_expire_wait, lib.decode_attn_paged_fp8_rope,
-               lib.decode_attn_ring_fp8_rope, lib.decode_attn_set_early_inputs):
+               lib.decode_attn_ring_fp8_rope, lib.decode_attn_set_early_inputs,
+               lib.decode_attn_stream_reserve, lib.decode_attn_stream_release):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -347,6 +351,18 @@ def decode_attn_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim=64, m
 
 def decode_attn_reserve(nbytes: int):
     _check(load_library().decode_attn_reserve(int(nbytes)))
+
+
+def decode_attn_stream_reserve(stream, nbytes: int = 0, multi_nbytes: int = 0):
+    """Workspaces of its own for the attention calls issued on `stream` (a torch.cuda.Stream
+    or a raw handle), so that they may overlap calls on other streams; held until
+    decode_attn_stream_release(stream)."""
+    _check(load_library().decode_attn_stream_reserve(_stream(stream), int(nbytes), int(multi_nbytes)))
+
+
+def decode_attn_stream_release(stream):
+    """Synchronise `stream` and free its own workspaces (no-op if it has none)."""
+    _check(load_library().decode_attn_stream_release(_stream(stream)))
 
 
 def decode_attn_device_status(stream=None) -> int:

@@ -40,6 +40,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -1959,20 +1960,34 @@ bool make_kv_map(CUtensorMap *map, void *base, uint64_t rows, uint64_t slices, i
 
 constexpr int kMaxDevices = 64;
 
+// A zeroed device buffer that only grows (its arrival counters are zero at rest).
+struct Workspace {
+    void *p = nullptr;
+    size_t bytes = 0;
+};
+
 // Per-device state. The workspace pointers change only under g_mu; the SM count and the
 // "kernel attribute set" flags are caches that several host threads may fill at once (with
 // the same values), so they are atomics.
 struct DeviceState {
-    void *ws = nullptr;
-    size_t ws_bytes = 0;
-    void *ws_multi = nullptr;  // multi-token calls: counters + split partials
-    size_t ws_multi_bytes = 0;
+    Workspace ws;        // one-token calls: counters + CTA partials
+    Workspace ws_multi;  // multi-token calls: counters + split partials
     std::atomic<int> sm_count{0};
     std::atomic<bool> attr_set[64] = {};
     std::atomic<bool> multi_attr_set[8] = {};
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+
+// Workspaces of their own for the calls issued on one stream (decode_attn_stream_reserve),
+// keyed by the stream handle, under g_mu; g_n_stream_ws lets calls skip the lookup when
+// there are none.
+struct StreamWorkspaces {
+    int dev;
+    Workspace ws, ws_multi;
+};
+std::unordered_map<cudaStream_t, StreamWorkspaces> g_stream_ws;
+std::atomic<int> g_n_stream_ws{0};
 
 int current_device(int *dev) {
     cudaError_t e = cudaGetDevice(dev);
@@ -2002,13 +2017,13 @@ size_t workspace_for(int G, int sms) {
     return kCounterBytes + static_cast<size_t>(ctas) * 2 * slot_floats(G) * sizeof(float);
 }
 
-int reserve_locked(int dev, size_t bytes) {
-    DeviceState &d = g_dev[dev];
-    if (d.ws_bytes >= bytes) return DA_OK;
-    if (d.ws) {
-        cudaError_t e = cudaFree(d.ws);
-        d.ws = nullptr;
-        d.ws_bytes = 0;
+// Grow w to at least `bytes` (synchronous: the old buffer is freed, the new one zeroed).
+int grow_locked(Workspace &w, size_t bytes) {
+    if (w.bytes >= bytes) return DA_OK;
+    if (w.p) {
+        cudaError_t e = cudaFree(w.p);
+        w.p = nullptr;
+        w.bytes = 0;
         if (e != cudaSuccess) return set_cuda_error(e);
     }
     void *p = nullptr;
@@ -2019,8 +2034,31 @@ int reserve_locked(int dev, size_t bytes) {
         cudaFree(p);
         return set_cuda_error(e);
     }
-    d.ws = p;
-    d.ws_bytes = bytes;
+    w.p = p;
+    w.bytes = bytes;
+    return DA_OK;
+}
+
+// The workspace a call on `stream` uses (the stream's own if it has one, else the
+// device's), grown to `need` unless the stream is capturing. Under g_mu.
+int workspace_locked(int dev, cudaStream_t stream, bool multi, size_t need, void **ptr) {
+    Workspace *w = multi ? &g_dev[dev].ws_multi : &g_dev[dev].ws;
+    if (g_n_stream_ws.load(std::memory_order_relaxed) > 0) {
+        auto it = g_stream_ws.find(stream);
+        if (it != g_stream_ws.end()) {
+            if (it->second.dev != dev) return DA_ERR_INVALID_ARG;  // the stream is another device's
+            w = multi ? &it->second.ws_multi : &it->second.ws;
+        }
+    }
+    if (w->bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
+        int rc = grow_locked(*w, need);
+        if (rc != DA_OK) return rc;
+    }
+    *ptr = w->p;
     return DA_OK;
 }
 
@@ -2073,17 +2111,14 @@ int launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Params &prm,
 
 int prepare_workspace(int dev, int G, cudaStream_t stream, float **part, int **counters) {
     const size_t need = workspace_for(G, sm_count(dev));
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_dev[dev].ws_bytes < need) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-        if (e != cudaSuccess) return set_cuda_error(e);
-        if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
-        int rc = reserve_locked(dev, need);
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int rc = workspace_locked(dev, stream, false, need, &ws);
         if (rc != DA_OK) return rc;
     }
-    *counters = static_cast<int *>(g_dev[dev].ws);
-    *part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws) + kCounterBytes);
+    *counters = static_cast<int *>(ws);
+    *part = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
     return DA_OK;
 }
 
@@ -2350,28 +2385,6 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     return m;
 }
 
-int reserve_multi_locked(int dev, size_t bytes) {
-    DeviceState &d = g_dev[dev];
-    if (d.ws_multi_bytes >= bytes) return DA_OK;
-    if (d.ws_multi) {
-        cudaError_t e = cudaFree(d.ws_multi);
-        d.ws_multi = nullptr;
-        d.ws_multi_bytes = 0;
-        if (e != cudaSuccess) return set_cuda_error(e);
-    }
-    void *ptr = nullptr;
-    cudaError_t e = cudaMalloc(&ptr, bytes);
-    if (e != cudaSuccess) return set_cuda_error(e);
-    e = cudaMemset(ptr, 0, bytes);
-    if (e != cudaSuccess) {
-        cudaFree(ptr);
-        return set_cuda_error(e);
-    }
-    d.ws_multi = ptr;
-    d.ws_multi_bytes = bytes;
-    return DA_OK;
-}
-
 int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
               const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens, const float *sinks,
               int window, float scale, void *out, const da_shape &s, int T, int page_size, int max_pages,
@@ -2401,17 +2414,11 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     const MultiPlan m = multi_plan(s, T, ring, window, max_seq_len, sm_count(dev));
     if (static_cast<long long>(m.splits) * m.row_blocks > 0x7fffffffLL || m.groups > kMMaxGroups)
         return DA_ERR_UNSUPPORTED;
+    void *ws = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        const size_t need = m.counter_bytes + m.part_bytes;
-        if (g_dev[dev].ws_multi_bytes < need) {
-            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-            cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-            if (e != cudaSuccess) return set_cuda_error(e);
-            if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
-            rc = reserve_multi_locked(dev, need);
-            if (rc != DA_OK) return rc;
-        }
+        rc = workspace_locked(dev, stream, true, m.counter_bytes + m.part_bytes, &ws);
+        if (rc != DA_OK) return rc;
     }
     if (m.dec) {  // the decode kernel's several-token form, on this workspace
         Params dp;
@@ -2424,8 +2431,8 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         dp.seq_lens = seq_lens;
         dp.sinks = sinks;
         dp.out = static_cast<__nv_bfloat16 *>(out);
-        dp.counters = static_cast<int *>(g_dev[dev].ws_multi);
-        dp.part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws_multi) + m.counter_bytes);
+        dp.counters = static_cast<int *>(ws);
+        dp.part = reinterpret_cast<float *>(static_cast<char *>(ws) + m.counter_bytes);
         dp.B = s.batch;
         dp.Hq = s.num_q_heads;
         dp.Hkv = s.num_kv_heads;
@@ -2474,8 +2481,8 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     prm.row_blocks = m.row_blocks;
     prm.splits = m.splits;
     prm.chunk = m.chunk;
-    prm.counters = static_cast<int *>(g_dev[dev].ws_multi);
-    prm.part = reinterpret_cast<float *>(static_cast<char *>(g_dev[dev].ws_multi) + m.counter_bytes);
+    prm.counters = static_cast<int *>(ws);
+    prm.part = reinterpret_cast<float *>(static_cast<char *>(ws) + m.counter_bytes);
     prm.defer = m.defer ? 1 : 0;
 
     CUtensorMap mk, mv, nk, nv;
@@ -2794,7 +2801,7 @@ int decode_attn_multi_reserve(size_t bytes) {
     int rc = current_device(&dev);
     if (rc != DA_OK) return rc;
     std::lock_guard<std::mutex> lk(g_mu);
-    return reserve_multi_locked(dev, bytes);
+    return grow_locked(g_dev[dev].ws_multi, bytes);
 }
 
 size_t decode_attn_workspace_bytes(da_shape s, int max_seq_len) {
@@ -2810,7 +2817,56 @@ int decode_attn_reserve(size_t bytes) {
     int rc = current_device(&dev);
     if (rc != DA_OK) return rc;
     std::lock_guard<std::mutex> lk(g_mu);
-    return reserve_locked(dev, bytes);
+    return grow_locked(g_dev[dev].ws, bytes);
+}
+
+int decode_attn_stream_reserve(void *stream_v, size_t bytes, size_t multi_bytes) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc != DA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_stream_ws.find(stream);
+    if (it == g_stream_ws.end()) {
+        it = g_stream_ws.emplace(stream, StreamWorkspaces{dev, {}, {}}).first;
+        g_n_stream_ws.fetch_add(1, std::memory_order_relaxed);
+    } else if (it->second.dev != dev) {
+        return DA_ERR_INVALID_ARG;
+    }
+    rc = grow_locked(it->second.ws, bytes);
+    if (rc == DA_OK) rc = grow_locked(it->second.ws_multi, multi_bytes);
+    return rc;
+}
+
+int decode_attn_stream_release(void *stream_v) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_stream_ws.find(stream);
+    if (it == g_stream_ws.end()) return DA_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (cs != cudaStreamCaptureStatusNone) return DA_ERR_WORKSPACE;
+    int prev = -1;
+    e = cudaGetDevice(&prev);
+    if (e == cudaSuccess && prev != it->second.dev) e = cudaSetDevice(it->second.dev);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);  // its calls are done with them
+    for (Workspace *w : {&it->second.ws, &it->second.ws_multi}) {
+        if (e == cudaSuccess && w->p) {
+            e = cudaFree(w->p);
+            w->p = nullptr;
+            w->bytes = 0;
+        }
+    }
+    if (prev >= 0 && prev != it->second.dev) cudaSetDevice(prev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    g_stream_ws.erase(it);
+    g_n_stream_ws.fetch_sub(1, std::memory_order_relaxed);
+    return DA_OK;
 }
 
 int decode_attn_test_expire_wait(int tile) {
