@@ -64,6 +64,15 @@ constexpr int kThreads = kWarps * 32;
 #ifndef DA_STAGES_G16
 #define DA_STAGES_G16 4
 #endif
+// several query tokens, 32 rows per KV head in one warp (four 8-row n-tiles): the tiles and
+// the 4 KiB of query rows per stage leave room for 3 stages
+#ifndef DA_STAGES_MT32
+#define DA_STAGES_MT32 3
+#endif
+// n-tiles up to which a warp holds its query rows' sink logits in registers through the loop
+#ifndef DA_SINKS_REGS_MAX_NT
+#define DA_SINKS_REGS_MAX_NT 2
+#endif
 // CPS = CTAs resident per SM (1 or 2). On large calls the fp8 kernel with 8-head groups is
 // bound by the latency of its per-warp convert / MMA / softmax chain, not by HBM: two CTAs
 // (16 warps, 128 registers each, 3 stages per warp) hide it better than one CTA with 7
@@ -83,7 +92,7 @@ __host__ __device__ constexpr int stages_for() {
     // fp8 tiles are half the size: more of them in flight for the same bytes; with two
     // CTAs per SM each gets half the shared memory
     return KV8 ? (NT == 1 ? (CPS > 1 ? DA_STAGES_FP8_2CTA : 7) : (ROPE ? 5 : 6))
-               : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : DA_STAGES_G16);
+               : (NT == 1 ? (ROPE ? DA_STAGES_G8_ROPE : DA_STAGES_G8) : NT == 2 ? DA_STAGES_G16 : DA_STAGES_MT32);
 }
 #ifndef DA_PAIR_BF16
 #define DA_PAIR_BF16 1
@@ -173,10 +182,14 @@ struct Params {
     // query-row groups of the MT kernel: CTA c takes rows [16 (c % ngrp), + 16) of every
     // (sequence, KV head) over the units of CTA c / ngrp of a grid of gridDim.x / ngrp (the
     // CTAs of one unit range read the same tiles, all but the first from L2); 1 otherwise
+    // (also for 32 rows in one warp's four n-tiles, the default)
     int ngrp;
     // testing aid: worker 0 gives up at its first tile wait from this tile on (after the tile
     // has landed), as if the wait had expired; -1 = never
     int expire_at;
+    // 32 query rows (four n-tiles): a warp's saved first-segment state goes here instead of
+    // registers, SegState<4> per warp of the grid (lane-interleaved); null otherwise
+    float *head_scratch;
     // 1: seq_lens, q_lens, block_table and sinks were final before the previous kernel in the
     // stream started, so the lengths, the split and the first block-table entries are read
     // and worked out before waiting for that kernel (the rest, from the first query row and
@@ -395,6 +408,21 @@ struct SegState {
     float m[NT][2];       // running max (log2 units) of heads 2(lane%4), +1
     float l[NT][2];       // running sum, this lane's token rows only until reduced
 };
+
+// A lane's state in global memory, value k of lane l at base[32 k + l] (coalesced per value).
+template <int NT>
+__device__ __forceinline__ void state_store_lanes(const SegState<NT> &s, float *base, int lane) {
+    const float *v = reinterpret_cast<const float *>(&s);
+#pragma unroll
+    for (int k = 0; k < static_cast<int>(sizeof(SegState<NT>) / 4); ++k) base[32 * k + lane] = v[k];
+}
+
+template <int NT>
+__device__ __forceinline__ void state_load_lanes(SegState<NT> &s, const float *base, int lane) {
+    float *v = reinterpret_cast<float *>(&s);
+#pragma unroll
+    for (int k = 0; k < static_cast<int>(sizeof(SegState<NT>) / 4); ++k) v[k] = base[32 * k + lane];
+}
 
 template <int NT>
 __device__ __forceinline__ void state_reset(SegState<NT> &s) {
@@ -616,7 +644,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
     constexpr int GP = Lay::GP;
     constexpr int kQBytes = Lay::kQBytes;
     constexpr int kWarpBytes = Lay::kWarpTileBytes;
-    static_assert(2 * sizeof(Slot<NT>) <= kWarpBytes, "merge slots must fit a drained warp area");
+    // a warp's two merge slots (head and tail states) go to its drained tile area, or, when
+    // they do not both fit there (32 rows), the tail slot to its drained query-row area
+    constexpr bool kSlotsInTiles = 2 * sizeof(Slot<NT>) <= kWarpBytes;
+    static_assert(kSlotsInTiles || (sizeof(Slot<NT>) <= kWarpBytes && sizeof(Slot<NT>) <= kStages * kQBytes),
+                  "merge slots must fit a drained warp area");
     constexpr int kSlotFloats = 2 * GP + GP * kD;  // global partial: m, l, acc
     // two tiles per loop pass (single 8-head n-tile only: the registers of two 16-head passes
     // would not fit)
@@ -859,7 +891,15 @@ __global__ void __launch_bounds__(kThreads, CPS)
 
     SegState<NT> st;       // running state of the current segment
     SegState<NT> head;     // saved state of the warp's first segment when shared
-    float sig[NT][2];      // sink logits (log2 units) of this lane's heads
+    // (32 query rows: saved to global memory instead, the registers are needed in the loop)
+    constexpr bool kHeadInRegs = NT < 4;
+    float *const head_mem = kHeadInRegs ? nullptr
+                            : p.head_scratch + (static_cast<size_t>(blockIdx.x) * kWarps + warp) * (sizeof(SegState<NT>) / 4) * 32;
+    // sink logits (log2 units) of this lane's query rows: held through the loop for up to
+    // DA_SINKS_REGS_MAX_NT n-tiles, read from shared memory when a segment's output is
+    // written for more (their registers are needed for the n-tiles)
+    constexpr bool kSinksInRegs = NT <= DA_SINKS_REGS_MAX_NT;
+    float sig_r[NT][2];
     uint32_t qf[NT][4][2]; // Q as mma B operand
     int head_seg = -1, tail_seg = -1;
     bool failed = false;
@@ -1085,12 +1125,26 @@ __global__ void __launch_bounds__(kThreads, CPS)
         // tightest bounds over its rows (tiles inside [lo_max, hi_min) need no mask), the new
         // tokens' k/v (bf16 pairs of this lane), and this lane's columns' ranges [lo_c, hi_c)
         int nq_seg = 1, base = 0, lo_max = 0, hi_min = 0;
+        constexpr bool kNewInRegs = NT < 4;
         uint32_t knewm[kMaxNewMT], vnewm[kMaxNewMT];
 #pragma unroll
         for (int i2 = 0; i2 < kMaxNewMT; ++i2) knewm[i2] = vnewm[i2] = 0u;
         uint32_t knew = 0, vnew = 0;           // new token's k/v (bf16 pair, or 2 e4m3 codes)
         float knew_scale = 1.f, vnew_scale = 1.f;  // fp8: their scales
         const bool do_append = p.k_new != nullptr;
+
+        // sink logits (log2 units) of this lane's query rows in the current segment
+        auto sinks_of = [&](float (&sg)[NT][2]) {
+            const int qrows = MT ? p.T * p.G : p.G;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int hs = r0g + n * 8 + (lane & 3) * 2 + j;
+                    sg[n][j] = kSinksInRegs ? sig_r[n][j]
+                                            : hs < qrows ? s_sink[sgk * p.G + (MT ? hs % p.G : hs)] : -INFINITY;
+                }
+        };
 
         int i = 0;  // first tile of the current pass
         // One pass over UT (1 or 2) consecutive tiles i .. i + UT - 1 of the current segment.
@@ -1127,7 +1181,15 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         if (i2 < nq_seg && pos / kPage - ft == tt) {
                             const int row = pos % kPage;
                             const uint32_t off = row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) + (lane & 3) * 4;
-                            const uint32_t kn = knewm[i2], vn = vnewm[i2];
+                            uint32_t kn, vn;
+                            if constexpr (kNewInRegs) {
+                                kn = knewm[i2];
+                                vn = vnewm[i2];
+                            } else {
+                                const size_t o = ((static_cast<size_t>(sb) * p.T + i2) * Hkv + sgk) * kD;
+                                kn = __ldg(reinterpret_cast<const uint32_t *>(p.k_new + o) + lane);
+                                vn = __ldg(reinterpret_cast<const uint32_t *>(p.v_new + o) + lane);
+                            }
                             *reinterpret_cast<uint32_t *>(gK + off) = kn;
                             *reinterpret_cast<uint32_t *>(gV + off) = vn;
                             if (tp >= 0 && rgrp == 0) {
@@ -1410,11 +1472,18 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     state_reduce_l(st);
                     if constexpr (KV8) state_scale_acc(st, 1.f / 256.f);
                     if (seg_first_unit < ua) {  // shared with earlier workers: keep for merge
-                        head = st;
+                        if constexpr (kHeadInRegs)
+                            head = st;
+                        else
+                            state_store_lanes(st, head_mem, lane);
                         head_seg = sb * Hkv + sgk;
                     } else if constexpr (MT) {
+                        float sig[NT][2];
+                        sinks_of(sig);
                         state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, r0g, lane);
                     } else {
+                        float sig[NT][2];
+                        sinks_of(sig);
                         state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD,
                                         p.G, lane);
                     }
@@ -1438,9 +1507,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     hi_min = base + 1;                                  // the first row's end
                     // the new tokens' k/v rows (this lane's bf16 pair of each): loaded now, used
                     // at the segment's last tiles, so the load latency hides behind the loop
+                    // (32 rows: loaded there, the registers are needed for the four n-tiles)
 #pragma unroll
                     for (int i2 = 0; i2 < kMaxNewMT; ++i2)
-                        if (i2 < nq_seg) {
+                        if (kNewInRegs && i2 < nq_seg) {
                             const size_t off = ((static_cast<size_t>(sb) * p.T + i2) * Hkv + sgk) * kD;
                             knewm[i2] = __ldg(reinterpret_cast<const uint32_t *>(p.k_new + off) + lane);
                             vnewm[i2] = __ldg(reinterpret_cast<const uint32_t *>(p.v_new + off) + lane);
@@ -1491,10 +1561,12 @@ __global__ void __launch_bounds__(kThreads, CPS)
                             qf[n][ks][0] = qf[n][ks][1] = 0u;
                         }
                     }
+                    if constexpr (kSinksInRegs) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int hs = r0g + n * 8 + (lane & 3) * 2 + j;
-                        sig[n][j] = hs < qrows ? s_sink[sgk * p.G + (MT ? hs % p.G : hs)] : -INFINITY;
+                        for (int j = 0; j < 2; ++j) {
+                            const int hs = r0g + n * 8 + (lane & 3) * 2 + j;
+                            sig_r[n][j] = hs < qrows ? s_sink[sgk * p.G + (MT ? hs % p.G : hs)] : -INFINITY;
+                        }
                     }
                 }
                 if constexpr (ROPE) {
@@ -1601,14 +1673,22 @@ __global__ void __launch_bounds__(kThreads, CPS)
         if (last_shared) {
             tail_seg = sb * Hkv + sgk;
         } else if constexpr (MT) {
+            float sig[NT][2];
+            sinks_of(sig);
             state_write_out_mt(st, sig, p.out, sb, sgk, p.T, p.G, p.Hq, nq_seg, r0g, lane);
         } else {
+            float sig[NT][2];
+            sinks_of(sig);
             state_write_out(st, sig, p.out + (static_cast<size_t>(sb) * p.Hq + sgk * p.G) * kD, p.G, lane);
         }
         // partial states -> this warp's (drained) buffer area
-        Slot<NT> *slots = reinterpret_cast<Slot<NT> *>(wbase);
-        if (slots_ok && head_seg >= 0) state_to_slot(head, &slots[0], lane);
-        if (slots_ok && tail_seg >= 0) state_to_slot(st, &slots[1], lane);
+        Slot<NT> *slot0 = reinterpret_cast<Slot<NT> *>(wbase);
+        Slot<NT> *slot1 = kSlotsInTiles ? slot0 + 1 : reinterpret_cast<Slot<NT> *>(wq);
+        if (slots_ok && head_seg >= 0) {
+            if constexpr (!kHeadInRegs) state_load_lanes(head, head_mem, lane);  // (own stores)
+            state_to_slot(head, slot0, lane);
+        }
+        if (slots_ok && tail_seg >= 0) state_to_slot(st, slot1, lane);
     }
     zero_inactive();
     // (the states published in the slots are the plan's head and tail: a warp whose copies
@@ -1649,7 +1729,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
             // lanes; a lane loads its item from every contributor at once (contributor c is
             // warp wa + c, its slot the head or the tail one; a warp whose copies never landed
             // is skipped), four contributors per round.
-            const uint32_t slots_base = smem_addr(smem);
+            const uint32_t slots_base = smem_addr(smem), tails_base = smem_addr(qarea);
             const int qrows = MT ? p.T * p.G : p.G;  // valid query rows of the group
             auto merge_items = [&](auto dpi_c) {
                 constexpr int DPI = decltype(dpi_c)::value;
@@ -1671,8 +1751,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         for (int u = 0; u < 4; ++u) {
                             const int c = c0 + u, w = wa + (c < k ? c : 0);
                             const bool ok = c < k && s_winfo[w * kWinfo + 9] != 0;
-                            const uint32_t sl = slots_base + w * kWarpBytes +
-                                                ((s_winfo[w * kWinfo + 3] == seg) ? static_cast<uint32_t>(sizeof(Slot<NT>)) : 0u);
+                            const bool tail = s_winfo[w * kWinfo + 3] == seg;
+                            const uint32_t sl = !tail ? slots_base + w * kWarpBytes
+                                                : kSlotsInTiles ? slots_base + w * kWarpBytes + static_cast<uint32_t>(sizeof(Slot<NT>))
+                                                                : tails_base + w * kStages * kQBytes;
                             mc[u] = ok ? lds_f32(sl + 4 * n) : -INFINITY;
                             lc[u] = ok ? lds_f32(sl + 4 * (GP + n)) : 0.f;
 #pragma unroll
@@ -1764,8 +1846,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
     // One pass, no barrier: every thread owns kPer outputs of one head and folds the
     // partials in batches of kCombBatch contributors whose loads are all in flight together
     // (a 131k-token sequence spread over every CTA has about 20 per KV head: one round trip).
-    constexpr int kPer = GP * kD / kThreads;  // outputs per thread: 2 (G <= 8) or 4 (G = 16)
-    constexpr int kCombBatch = CPS > 1 ? 8 : 24;  // (the 128-register two-CTA kernel: 8)
+    constexpr int kPer = GP * kD / kThreads;  // outputs per thread: 2 (8 rows), 4 (16) or 8 (32)
+    constexpr int kCombBatch = (CPS > 1 || kPer == 8) ? 8 : 24;  // (the 128-register two-CTA kernel: 8)
     const int cn = tid / (kD / kPer), cd0 = (tid % (kD / kPer)) * kPer;
 #pragma unroll 1
     for (int k = 0; k < 2; ++k) {
@@ -1794,8 +1876,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         const float2 t2 = __ldcg(reinterpret_cast<const float2 *>(gp + 2 * GP + cn * kD + cd0));
                         v[j][0] = t2.x; v[j][1] = t2.y;
                     } else {
-                        const float4 t4 = __ldcg(reinterpret_cast<const float4 *>(gp + 2 * GP + cn * kD + cd0));
-                        v[j][0] = t4.x; v[j][1] = t4.y; v[j][2] = t4.z; v[j][3] = t4.w;
+#pragma unroll
+                        for (int q4 = 0; q4 < kPer / 4; ++q4) {
+                            const float4 t4 = __ldcg(reinterpret_cast<const float4 *>(gp + 2 * GP + cn * kD + cd0) + q4);
+                            v[j][4 * q4] = t4.x; v[j][4 * q4 + 1] = t4.y; v[j][4 * q4 + 2] = t4.z; v[j][4 * q4 + 3] = t4.w;
+                        }
                     }
                 }
             }
@@ -2006,7 +2091,7 @@ int sm_count(int dev) {
 }
 
 size_t slot_floats(int G) {
-    const int gp = G <= 8 ? 8 : 16;
+    const int gp = G <= 8 ? 8 : G <= 16 ? 16 : 32;
     return static_cast<size_t>(2 * gp + gp * kD);
 }
 
@@ -2186,6 +2271,7 @@ int run_attention(bool ring, const void *q, const void *k_new, const void *v_new
     prm.q_lens = nullptr;
     prm.ngrp = 1;
     prm.expire_at = g_expire_next.exchange(-1);
+    prm.head_scratch = nullptr;
     prm.early = g_early_inputs.load();
     rc = prepare_workspace(dev, G, stream, &prm.part, &prm.counters);
     if (rc != DA_OK) return rc;
@@ -2307,6 +2393,11 @@ struct MultiPlan {
 #ifndef DA_MULTI_DECODE_MAX_ROWS  // query rows per KV head the decode kernel takes (16 or 32)
 #define DA_MULTI_DECODE_MAX_ROWS 32
 #endif
+// 17 to 32 rows per KV head: 1 = one warp takes all of them (four n-tiles), 0 = two row
+// groups of 16 on pairs of CTAs that cover the same units
+#ifndef DA_MULTI_DECODE_NT4
+#define DA_MULTI_DECODE_NT4 1
+#endif
 // Key splits from which the partials are folded by a kernel of their own (spread over many
 // SMs) rather than by the last CTA of each row block
 #ifndef DA_MULTI_DEFER_SPLITS
@@ -2338,20 +2429,24 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     // Up to kMaxNewMT query tokens of at most 32 rows per KV head on a paged cache take the
     // decode kernel's device-balanced split (measured faster than the row-block kernel; the
     // ring keeps the row-block kernel, whose separate append leaves the cells the earlier
-    // tokens read). Over 16 rows, two row groups of 16: pairs of CTAs on the same units.
+    // tokens read). Over 16 rows, one warp takes all 32 (four n-tiles), or (switch off) two
+    // row groups of 16 on pairs of CTAs that cover the same units.
     m.dec = !ring && T <= kMaxNewMT && TG <= DA_MULTI_DECODE_MAX_ROWS && DA_MULTI_DECODE_ROUTE;
     if (m.dec) {  // counters (one set per row group) in the fixed region, then one pair of
                   // partial slots per CTA
         m.tc = false;
         m.defer = false;
         m.nw = kWarps;
-        m.rows = TG <= 8 ? 8 : 16;
-        m.row_blocks = static_cast<int>((TG + 15) / 16);
+        const bool nt4 = DA_MULTI_DECODE_NT4 && TG > 16;
+        m.rows = TG <= 8 ? 8 : nt4 ? 32 : 16;
+        m.row_blocks = nt4 ? 1 : static_cast<int>((TG + 15) / 16);
         m.splits = 1;
         m.chunk = 0;
         m.groups = static_cast<long long>(s.batch) * s.num_kv_heads * m.row_blocks;
         m.counter_bytes = static_cast<size_t>(kMMaxGroups) * sizeof(int);
-        m.part_bytes = static_cast<size_t>(sms) * 2 * slot_floats(static_cast<int>(TG)) * sizeof(float);
+        // the CTAs' partial slots; with 32 rows also every warp's saved first-segment state
+        m.part_bytes = static_cast<size_t>(sms) * 2 * slot_floats(m.rows) * sizeof(float) +
+                       (m.rows == 32 ? static_cast<size_t>(sms) * kWarps * 32 * (4 * 16 + 4 * 4) * sizeof(float) : 0);
         return m;
     }
     m.tc = !ring && TG >= DA_MULTI_TC_MIN_ROWS;
@@ -2449,6 +2544,7 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
         dp.q_lens = q_lens;
         dp.ngrp = m.row_blocks;
         dp.expire_at = -1;
+        dp.head_scratch = m.rows == 32 ? dp.part + static_cast<size_t>(sm_count(dev)) * 2 * slot_floats(m.rows) : nullptr;
         dp.early = g_early_inputs.load();
         CUtensorMap mk, mv;
         const uint64_t slices = static_cast<uint64_t>(num_pages) * s.num_kv_heads;
@@ -2456,8 +2552,9 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
             snprintf(t_err, sizeof t_err, "CUDA error: tensor map encoding failed");
             return DA_ERR_CUDA;
         }
-        return T * dp.G <= 8 ? launch_attn<1, false, false, false, 1, true>(mk, mv, dp, dev, stream)
-                             : launch_attn<2, false, false, false, 1, true>(mk, mv, dp, dev, stream);
+        return m.rows == 8    ? launch_attn<1, false, false, false, 1, true>(mk, mv, dp, dev, stream)
+               : m.rows == 16 ? launch_attn<2, false, false, false, 1, true>(mk, mv, dp, dev, stream)
+                              : launch_attn<4, false, false, false, 1, true>(mk, mv, dp, dev, stream);
     }
     MultiParams prm;
     prm.q = static_cast<const __nv_bfloat16 *>(q);
@@ -2637,6 +2734,7 @@ int run_paged_noalloc(const void *q, const void *k_new, const void *v_new, void 
     prm.q_lens = nullptr;
     prm.ngrp = 1;
     prm.expire_at = -1;
+    prm.head_scratch = nullptr;
     prm.early = g_early_inputs.load();
     prm.counters = static_cast<int *>(scratch);
     prm.part = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocCounterBytes);
