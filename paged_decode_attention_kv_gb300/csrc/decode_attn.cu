@@ -119,6 +119,17 @@ __host__ __device__ constexpr int stages_for() {
 #ifndef DA_FAST_PASS_BF16
 #define DA_FAST_PASS_BF16 0
 #endif
+// Lazy softmax maximum (bf16 tiles): a column's reference maximum moves only when a score
+// exceeds it by more than 2^kLazyLog2 (one warp vote per n-tile and pass instead of the
+// three-round shuffle reduction and the accumulator rescale); the probabilities then stay
+// below 2^kLazyLog2, and m, l and O share the reference, so O / l is unchanged
+#ifndef DA_LAZY_MAX_MT
+#define DA_LAZY_MAX_MT 1
+#endif
+#ifndef DA_LAZY_MAX_BF16
+#define DA_LAZY_MAX_BF16 0
+#endif
+constexpr float kLazyLog2 = 8.f;
 // Tiles per worker at least: 4, or 2 for a call of at most two tiles per worker of the grid
 // (such a call cannot fill the grid anyway; two tiles are one loop pass)
 #ifndef DA_MIN_TILES
@@ -653,6 +664,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
     // two tiles per loop pass (single 8-head n-tile only: the registers of two 16-head passes
     // would not fit)
     constexpr bool kPair = NT == 1 && (KV8 ? DA_PAIR_FP8 : DA_PAIR_BF16);
+    // lazy softmax maximum: bf16 tiles only (the fp8 path's fp16 probabilities carry the V
+    // scales and a factor 2^8 already)
+    constexpr bool kLazy = !KV8 && (MT ? DA_LAZY_MAX_MT : DA_LAZY_MAX_BF16);
     constexpr bool kParIssue = KV8 ? DA_PAR_ISSUE_FP8 : DA_PAR_ISSUE_BF16;
 
     extern __shared__ uint8_t smem_raw[];
@@ -1364,6 +1378,49 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 for (int u = 1; u < UT; ++u) {
                     mx0 = fmaxf(mx0, fmaxf(sv[u][0], sv[u][2]));
                     mx1 = fmaxf(mx1, fmaxf(sv[u][1], sv[u][3]));
+                }
+                if constexpr (kLazy) {
+                    // the reference moves (to the exact maximum) only when a score of this
+                    // pass exceeds it by more than 2^kLazyLog2 in some lane
+                    const bool grow = mx0 > st.m[n][0] + kLazyLog2 || mx1 > st.m[n][1] + kLazyLog2;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 8));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 8));
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
+                        const float mn0 = fmaxf(st.m[n][0], mx0), mn1 = fmaxf(st.m[n][1], mx1);
+                        const float mr0 = mn0 == -INFINITY ? 0.f : mn0, mr1 = mn1 == -INFINITY ? 0.f : mn1;
+                        const float a0 = fast_exp2(st.m[n][0] - mr0), a1 = fast_exp2(st.m[n][1] - mr1);
+                        st.l[n][0] *= a0;
+                        st.l[n][1] *= a1;
+                        st.m[n][0] = mn0;
+                        st.m[n][1] = mn1;
+#pragma unroll
+                        for (int mt = 0; mt < 4; ++mt) {
+                            st.acc[n][mt][0] *= a0;
+                            st.acc[n][mt][1] *= a1;
+                            st.acc[n][mt][2] *= a0;
+                            st.acc[n][mt][3] *= a1;
+                        }
+                    }
+                    // (a column that has seen no key yet, m = -inf: subtract 0, every term is 0)
+                    const float mr0 = st.m[n][0] == -INFINITY ? 0.f : st.m[n][0];
+                    const float mr1 = st.m[n][1] == -INFINITY ? 0.f : st.m[n][1];
+                    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                    for (int u = 0; u < UT; ++u) {
+                        const float p0 = fast_exp2(sv[u][0] - mr0), p1 = fast_exp2(sv[u][1] - mr1);
+                        const float p2 = fast_exp2(sv[u][2] - mr0), p3 = fast_exp2(sv[u][3] - mr1);
+                        ls0 += p0 + p2;
+                        ls1 += p1 + p3;
+                        pb[u][n][0] = movmatrix_t(pack_bf16(p0, p1));
+                        pb[u][n][1] = movmatrix_t(pack_bf16(p2, p3));
+                    }
+                    st.l[n][0] += ls0;
+                    st.l[n][1] += ls1;
+                    continue;
                 }
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
