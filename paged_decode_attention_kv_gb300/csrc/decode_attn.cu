@@ -129,7 +129,13 @@ __host__ __device__ constexpr int stages_for() {
 #ifndef DA_LAZY_MAX_BF16
 #define DA_LAZY_MAX_BF16 0
 #endif
-constexpr float kLazyLog2 = 8.f;
+// fp8 tiles: the probabilities are multiplied by the tokens' V scales and a power of two
+// before the fp16 conversion; with the lazy maximum (probabilities below 2^4) that factor is
+// 2^4 instead of 2^8, so the largest product stays the same as with exact maxima
+#ifndef DA_LAZY_MAX_FP8
+#define DA_LAZY_MAX_FP8 1
+#endif
+constexpr float kLazyLog2 = 8.f, kLazyLog2Fp8 = 4.f;
 // Tiles per worker at least: 4, or 2 for a call of at most two tiles per worker of the grid
 // (such a call cannot fill the grid anyway; two tiles are one loop pass)
 #ifndef DA_MIN_TILES
@@ -664,9 +670,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
     // two tiles per loop pass (single 8-head n-tile only: the registers of two 16-head passes
     // would not fit)
     constexpr bool kPair = NT == 1 && (KV8 ? DA_PAIR_FP8 : DA_PAIR_BF16);
-    // lazy softmax maximum: bf16 tiles only (the fp8 path's fp16 probabilities carry the V
-    // scales and a factor 2^8 already)
-    constexpr bool kLazy = !KV8 && (MT ? DA_LAZY_MAX_MT : DA_LAZY_MAX_BF16);
+    constexpr bool kLazy = KV8 ? DA_LAZY_MAX_FP8 : (MT ? DA_LAZY_MAX_MT : DA_LAZY_MAX_BF16);
+    constexpr float kLazyT = KV8 ? kLazyLog2Fp8 : kLazyLog2;  // log2 of the largest probability
+    // fp8: the power of two the V scales carry (taken out when a segment closes)
+    constexpr float kV8Factor = kLazy ? 16.f : 256.f;
     constexpr bool kParIssue = KV8 ? DA_PAR_ISSUE_FP8 : DA_PAR_ISSUE_BF16;
 
     extern __shared__ uint8_t smem_raw[];
@@ -1312,10 +1319,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     const float *ssr = reinterpret_cast<const float *>(wbase + s_off(stgs[u]));
                     ks_lo[u] = ssr[row_tok];
                     ks_hi[u] = ssr[row_tok + 2];
-                    // V scales carry a factor 2^8 so that the fp16 probabilities stay normal;
-                    // it is taken out when the segment closes
-                    vs_lo[u] = ssr[kPage + row_tok] * 256.f;
-                    vs_hi[u] = ssr[kPage + row_tok + 2] * 256.f;
+                    // V scales carry a factor 2^8 (2^4 with the lazy maximum, whose
+                    // probabilities reach 2^4) so that the fp16 products stay normal; it is
+                    // taken out when the segment closes
+                    vs_lo[u] = ssr[kPage + row_tok] * kV8Factor;
+                    vs_hi[u] = ssr[kPage + row_tok + 2] * kV8Factor;
                     if (partial[u]) {  // a row outside the attended range may hold a garbage scale
                         vs_lo[u] = ok_lo[u] ? vs_lo[u] : 0.f;
                         vs_hi[u] = ok_hi[u] ? vs_hi[u] : 0.f;
@@ -1382,7 +1390,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 if constexpr (kLazy) {
                     // the reference moves (to the exact maximum) only when a score of this
                     // pass exceeds it by more than 2^kLazyLog2 in some lane
-                    const bool grow = mx0 > st.m[n][0] + kLazyLog2 || mx1 > st.m[n][1] + kLazyLog2;
+                    const bool grow = mx0 > st.m[n][0] + kLazyT || mx1 > st.m[n][1] + kLazyT;
                     if (__any_sync(0xffffffffu, grow)) {
                         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
                         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
@@ -1415,8 +1423,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         const float p2 = fast_exp2(sv[u][2] - mr0), p3 = fast_exp2(sv[u][3] - mr1);
                         ls0 += p0 + p2;
                         ls1 += p1 + p3;
-                        pb[u][n][0] = movmatrix_t(pack_bf16(p0, p1));
-                        pb[u][n][1] = movmatrix_t(pack_bf16(p2, p3));
+                        if constexpr (KV8) {
+                            pb[u][n][0] = movmatrix_t(pack_f16(p0 * vs_lo[u], p1 * vs_lo[u]));
+                            pb[u][n][1] = movmatrix_t(pack_f16(p2 * vs_hi[u], p3 * vs_hi[u]));
+                        } else {
+                            pb[u][n][0] = movmatrix_t(pack_bf16(p0, p1));
+                            pb[u][n][1] = movmatrix_t(pack_bf16(p2, p3));
+                        }
                     }
                     st.l[n][0] += ls0;
                     st.l[n][1] += ls1;
@@ -1527,7 +1540,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 // close the previous segment
                 if (i > 0) {
                     state_reduce_l(st);
-                    if constexpr (KV8) state_scale_acc(st, 1.f / 256.f);
+                    if constexpr (KV8) state_scale_acc(st, 1.f / kV8Factor);
                     if (seg_first_unit < ua) {  // shared with earlier workers: keep for merge
                         if constexpr (kHeadInRegs)
                             head = st;
@@ -1725,7 +1738,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
 
         // close the last segment
         state_reduce_l(st);
-        if constexpr (KV8) state_scale_acc(st, 1.f / 256.f);
+        if constexpr (KV8) state_scale_acc(st, 1.f / kV8Factor);
         const bool last_shared = failed || seg_first_unit < ua || seg_end_unit > ue;
         if (last_shared) {
             tail_seg = sb * Hkv + sgk;
