@@ -24,7 +24,8 @@ _FUNCS = ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
           "oracle_decode_ring_rope", "oracle_e4m3_decode", "oracle_e4m3_encode",
           "oracle_quantise_rows", "oracle_decode_paged_fp8", "oracle_decode_ring_fp8",
           "oracle_kv_append_fp8", "oracle_scatter_fp8", "oracle_decode_multi",
-          "oracle_kv_append_multi", "oracle_decode_paged_fp8_rope", "oracle_decode_ring_fp8_rope")
+          "oracle_kv_append_multi", "oracle_decode_paged_fp8_rope", "oracle_decode_ring_fp8_rope",
+          "oracle_rope_multi", "oracle_decode_multi_rope")
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -92,6 +93,13 @@ def _load():
         lib.oracle_kv_append_multi.argtypes = [
             c_int, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, c_int, c_int, c_int, c_int,
             c_int, c_int, c_int, c_int]
+        lib.oracle_rope_multi.argtypes = [
+            _u16p, _u16p, _i32p, _i32p, _f32p, _f32p, c_int, c_int, c_int, c_int, c_int, c_int,
+            _f64p, _u16p]
+        lib.oracle_decode_multi_rope.argtypes = [
+            c_int, _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _f32p, _f32p, _f32p,
+            c_int, c_int, c_double, _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+            c_int]
         for name in _FUNCS:
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -588,6 +596,48 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, window, sca
         int(window), float(scale), _ptr(out, _f64p), B, T, Hq, Hkv, D, page_size,
         0 if ring else bt.shape[1], 0 if ring else kc.shape[0], nthreads or default_threads()),
         "decode_multi")
+    return out
+
+
+def rope_multi(q, k_new, seq_lens, rope_cos, rope_sin, q_lens=None):
+    """Several-token rotary embedding: query row (t, h) and new key (t, g), t < n, rotated to
+    their own position L - n + t. Returns (q64 [B, T, Hq, D] float64, zero rows for t >= n;
+    k_rot [B, T, Hkv, D] uint16 as stored, rows t >= n copied)."""
+    lib = _load()
+    q, kn = _u16(q, "q"), _u16(k_new, "k_new")
+    sl, ql = _i32(seq_lens), _i32(q_lens)
+    B, T, Hq, D = q.shape
+    Hkv = kn.shape[2]
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    q64 = np.zeros((B, T, Hq, D), np.float64)
+    krot = np.zeros_like(kn)
+    _check(lib.oracle_rope_multi(_ptr(q, _u16p), _ptr(kn, _u16p), _ptr(sl, _i32p), _ptr(ql, _i32p),
+                                 _ptr(c, _f32p), _ptr(sn, _f32p), maxpos, B, T, Hq, Hkv, D,
+                                 _ptr(q64, _f64p), _ptr(krot, _u16p)), "rope_multi")
+    return q64, krot
+
+
+def decode_multi_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, rope_cos, rope_sin,
+                      window, scale, block_table=None, q_lens=None, page_size=16, nthreads=None):
+    """decode_multi with q and k_new rotated first (rope_multi): the several-token step of a
+    model whose keys are stored rotated. The append of the step stores the rotated keys
+    (kv_append_multi of rope_multi's k_rot)."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    kc, vc = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    sl, ql, sk = _i32(seq_lens), _i32(q_lens), _f32(sinks)
+    B, T, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    c, sn, maxpos = _tables(rope_cos, rope_sin, D)
+    ring = block_table is None
+    bt = None if ring else _i32(block_table)
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_multi_rope(
+        int(ring), _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), _ptr(kc, _u16p),
+        _ptr(vc, _u16p), _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(ql, _i32p), _ptr(sk, _f32p),
+        _ptr(c, _f32p), _ptr(sn, _f32p), maxpos, int(window), float(scale), _ptr(out, _f64p), B, T,
+        Hq, Hkv, D, page_size, 0 if ring else bt.shape[1], 0 if ring else kc.shape[0],
+        nthreads or default_threads()), "decode_multi_rope")
     return out
 
 

@@ -870,6 +870,7 @@ typedef struct {
     int window; double scale;
     int B, T, Hq, Hkv, D, P, max_pages, num_pages;
     double *out;
+    const double *q64;  /* rotated queries [B][T][Hq][D] in fp64, or NULL: q as given */
 } problemM;
 
 static int q_count(const int32_t *q_lens, int T, int b) { return q_lens ? q_lens[b] : T; }
@@ -903,14 +904,16 @@ static int attend_oneM(const problemM *pr, int b, int t, int h, double *out) {
     const int cnt = p - lo + 1;
     double *s = (double *)malloc(sizeof(double) * (size_t)cnt);
     if (!s) return OR_NOMEM;
-    const uint16_t *qrow = pr->q + (((size_t)b * pr->T + t) * pr->Hq + h) * D;
+    const size_t qoff = (((size_t)b * pr->T + t) * pr->Hq + h) * D;
+    const uint16_t *qrow = pr->q + qoff;
+    const double *q64 = pr->q64 ? pr->q64 + qoff : NULL;
     const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;
     double M = sigma;
     for (int i = 0; i < cnt; ++i) {
         const uint16_t *krow = rowM(pr, b, g, lo + i, 0);
         if (!krow) { free(s); return OR_BAD_INDEX; }
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+        for (int d = 0; d < D; ++d) dot += (q64 ? q64[d] : bf16_to_f64(qrow[d])) * bf16_to_f64(krow[d]);
         s[i] = pr->scale * dot;
         if (s[i] > M) M = s[i];
     }
@@ -948,18 +951,18 @@ static int check_counts(const int32_t *seq_lens, const int32_t *q_lens, int B, i
     return OR_OK;
 }
 
-int oracle_decode_multi(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
-                        const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_table,
-                        const int32_t *seq_lens, const int32_t *q_lens, const float *sinks, int window,
-                        double scale, double *out, int B, int T, int Hq, int Hkv, int D, int page_size,
-                        int max_pages, int num_pages, int nthreads) {
+static int decode_multi_q64(int ring, const uint16_t *q, const double *q64_in, const uint16_t *k_new,
+                            const uint16_t *v_new, const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                            const float *sinks, int window, double scale, double *out, int B, int T, int Hq,
+                            int Hkv, int D, int page_size, int max_pages, int num_pages, int nthreads) {
     if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !out || B < 0 || T <= 0 || Hq <= 0 ||
         Hkv <= 0 || Hq % Hkv || D <= 0 || window < 0 || (ring && window <= 0) ||
         (!ring && (!block_table || page_size <= 0 || max_pages <= 0 || num_pages <= 0)))
         return OR_BAD_ARG;
     if (check_counts(seq_lens, q_lens, B, T) != OR_OK) return OR_BAD_ARG;
     problemM pr = {ring, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks, window, scale,
-                   B, T, Hq, Hkv, D, page_size, max_pages, num_pages, out};
+                   B, T, Hq, Hkv, D, page_size, max_pages, num_pages, out, q64_in};
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     pthread_t th[256];
@@ -975,6 +978,74 @@ int oracle_decode_multi(int ring, const uint16_t *q, const uint16_t *k_new, cons
     for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
     for (int t = 0; t < nthreads; ++t) if (args[t].status != OR_OK) return args[t].status;
     return OR_OK;
+}
+
+int oracle_decode_multi(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                        const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_table,
+                        const int32_t *seq_lens, const int32_t *q_lens, const float *sinks, int window,
+                        double scale, double *out, int B, int T, int Hq, int Hkv, int D, int page_size,
+                        int max_pages, int num_pages, int nthreads) {
+    return decode_multi_q64(ring, q, NULL, k_new, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks,
+                            window, scale, out, B, T, Hq, Hkv, D, page_size, max_pages, num_pages, nthreads);
+}
+
+/* Several query tokens with the rotary embedding (the rotate-half form of the one-token
+ * steps above, at each new token's own position): query row (t, h) and new key (t, g),
+ * t < n, are rotated to position p = L - n + t -- the query in fp64, the key in fp32 and
+ * rounded to bf16 nearest even, as it is stored. Rows t >= n are left as they are (zero
+ * queries in q64; keys copied). */
+int oracle_rope_multi(const uint16_t *q, const uint16_t *k_new, const int32_t *seq_lens, const int32_t *q_lens,
+                      const float *rope_cos, const float *rope_sin, int max_position, int B, int T, int Hq,
+                      int Hkv, int D, double *q64, uint16_t *krot) {
+    if (!q || !seq_lens || !rope_cos || !rope_sin || !q64 || (k_new && !krot) || D % 2 || max_position <= 0 ||
+        B < 0 || T <= 0)
+        return OR_BAD_ARG;
+    if (check_counts(seq_lens, q_lens, B, T) != OR_OK) return OR_BAD_ARG;
+    const int h = D / 2;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b], n = q_count(q_lens, T, b);
+        for (int t = 0; t < T; ++t) {
+            const int active = L > 0 && t < n;
+            const int p = L - n + t;
+            if (active && p >= max_position) return OR_BAD_INDEX;
+            const size_t row = active ? (size_t)p * h : 0;
+            for (int hq = 0; hq < Hq; ++hq) {
+                const size_t off = (((size_t)b * T + t) * Hq + hq) * D;
+                if (active) rope_row_f64(q + off, rope_cos + row, rope_sin + row, D, q64 + off);
+                else for (int d = 0; d < D; ++d) q64[off + d] = 0.0;
+            }
+            if (!k_new) continue;
+            for (int g = 0; g < Hkv; ++g) {
+                const size_t off = (((size_t)b * T + t) * Hkv + g) * D;
+                if (active) rope_row_bf16(k_new + off, rope_cos + row, rope_sin + row, D, krot + off);
+                else memcpy(krot + off, k_new + off, sizeof(uint16_t) * (size_t)D);
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* The several-token step with the rotary embedding: rotate (oracle_rope_multi), then attend
+ * exactly as oracle_decode_multi with the rotated queries and keys. */
+int oracle_decode_multi_rope(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                             const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *q_lens, const float *sinks,
+                             const float *rope_cos, const float *rope_sin, int max_position, int window,
+                             double scale, double *out, int B, int T, int Hq, int Hkv, int D, int page_size,
+                             int max_pages, int num_pages, int nthreads) {
+    if (!k_new) return OR_BAD_ARG;
+    double *q64 = (double *)malloc(sizeof(double) * (size_t)B * T * Hq * D + 1);
+    uint16_t *krot = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)B * T * Hkv * D + 1);
+    int st = (q64 && krot) ? OR_OK : OR_NOMEM;
+    if (st == OR_OK)
+        st = oracle_rope_multi(q, k_new, seq_lens, q_lens, rope_cos, rope_sin, max_position, B, T, Hq, Hkv, D,
+                               q64, krot);
+    if (st == OR_OK)
+        st = decode_multi_q64(ring, q, q64, krot, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks,
+                              window, scale, out, B, T, Hq, Hkv, D, page_size, max_pages, num_pages, nthreads);
+    free(q64);
+    free(krot);
+    return st;
 }
 
 /* The append of a multi-token step: new token t < n of b goes to position L - n + t (paged:
