@@ -13,6 +13,7 @@ import oracle
 import test_oracle as pins
 import test_oracle_fp8 as fp8_pins
 import test_oracle_multi as multi_pins
+import test_oracle_multi_rope as multi_rope_pins
 import test_oracle_rope as rope_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -74,8 +75,10 @@ MUTANTS = [
     ("multi_q_lens_ignored", "static int q_count(const int32_t *q_lens, int T, int b) { return q_lens ? q_lens[b] : T; }",
      "static int q_count(const int32_t *q_lens, int T, int b) { (void)q_lens; (void)b; return T; }"),
     ("multi_append_shift", "const int pos = L - n + t;", "const int pos = L - n + t + 1;"),
-    ("multi_q_token_stride", "const uint16_t *qrow = pr->q + (((size_t)b * pr->T + t) * pr->Hq + h) * D;",
-     "const uint16_t *qrow = pr->q + (((size_t)t * pr->B + b) * pr->Hq + h) * D;"),
+    ("multi_q_token_stride", "const size_t qoff = (((size_t)b * pr->T + t) * pr->Hq + h) * D;",
+     "const size_t qoff = (((size_t)t * pr->B + b) * pr->Hq + h) * D;"),
+    ("multi_rope_position", "const int p = L - n + t;\n            if (active && p >= max_position)",
+     "const int p = L - 1;\n            if (active && p >= max_position)"),
     ("append_wrong_cell",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(L % page_size)) * D;"),
@@ -112,6 +115,10 @@ PIN_CALLS = [
     multi_pins.test_rows_beyond_q_lens_and_inactive_slots_are_zero,
     lambda: multi_pins.test_append_is_bit_exact_and_touches_only_the_new_cells(True),
     lambda: multi_pins.test_append_is_bit_exact_and_touches_only_the_new_cells(False),
+    multi_rope_pins.test_identity_tables_give_the_plain_step,
+    lambda: multi_rope_pins.test_one_new_token_is_the_one_token_step(0),
+    multi_rope_pins.test_each_token_is_rotated_at_its_own_position,
+    multi_rope_pins.test_stored_keys_round_as_fp32_then_bf16,
 ]
 
 
