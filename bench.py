@@ -281,7 +281,10 @@ def call_paged(s, rope, q=None, k_new=None, v_new=None, bt=None, sl=None, sinks=
     bt = s.block_table if bt is None else bt
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
-    if s.T > 1:
+    if s.T > 1 and rope:
+        da.decode_attn_paged_multi_rope(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks,
+                                        s.rope_cos, s.rope_sin, 0, s.inp.scale, out)
+    elif s.T > 1:
         da.decode_attn_paged_multi(q, k_new, v_new, s.pool.k_cache, s.pool.v_cache, bt, sl, sinks, 0,
                                    s.inp.scale, out)
     elif s.kv == "fp8" and rope:
@@ -305,7 +308,10 @@ def call_ring(s, rope, q=None, k_new=None, v_new=None, sl=None, sinks=None, out=
     v_new = s.v_new if v_new is None else v_new
     sl = s.seq_lens if sl is None else sl
     sinks = s.sinks if sinks is None else sinks
-    if s.T > 1:
+    if s.T > 1 and rope:
+        da.decode_attn_ring_multi_rope(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
+                                       s.rope_cos, s.rope_sin, s.inp.scale, out)
+    elif s.T > 1:
         da.decode_attn_ring_multi(q, k_new, v_new, s.ring.k_cache, s.ring.v_cache, sl, sinks,
                                   s.inp.scale, out)
     elif s.kv == "fp8" and rope:
@@ -327,10 +333,11 @@ def decode_route(q_tokens, cfg):
     return 1 < q_tokens <= 4 and q_tokens * cfg["Hq"] // cfg["Hkv"] <= 32
 
 
-def launches_per_step(q_tokens, cfg, max_pages):
+def launches_per_step(q_tokens, cfg, max_pages, rope=False):
     """Kernel launches of one step (a paged and a ring layer): one per layer for a single
     query token; for several, what the library reports for each layer's call (the attention,
-    the append unless fused, and a kernel that folds many key splits' partials)."""
+    the append unless fused, and a kernel that folds many key splits' partials), plus the
+    rotation kernel of each layer's call with the rotary embedding."""
     if q_tokens == 1:
         return 2
     import paged_decode_attention_kv_gb300 as da
@@ -338,7 +345,7 @@ def launches_per_step(q_tokens, cfg, max_pages):
          da.decode_attn_multi_launches(cfg["B"], cfg["Hq"], cfg["Hkv"], q_tokens, cfg["window"], 0)]
     if min(n) <= 0:
         raise RuntimeError("the library reported no launch count for this shape")
-    return sum(n)
+    return sum(n) + (2 if rope else 0)
 
 
 def step_bytes(name, lens, kv="bf16", q_tokens=1):
@@ -375,7 +382,14 @@ def oracle_sample(name, s: "StepInputs", budget_s):
         for b in order:
             items = [(b, h) for h in range(Hq)]
             t0 = time.perf_counter()
-            if s.T > 1:
+            if s.T > 1 and getattr(s, "rope", False):
+                one = slice(b, b + 1)
+                cs, sn = s.rope_cos.cpu().numpy(), s.rope_sin.cpu().numpy()
+                oracle.decode_multi_rope(q[one], kn[one], vn[one], kp, vp, lens[one], sinks, cs, sn, 0,
+                                         s.inp.scale, block_table=bt[one], nthreads=cores)
+                oracle.decode_multi_rope(q[one], kn[one], vn[one], rk[one], rv[one], lens[one], sinks,
+                                         cs, sn, W, s.inp.scale, nthreads=cores)
+            elif s.T > 1:
                 one = slice(b, b + 1)
                 oracle.decode_multi(q[one], kn[one], vn[one], kp, vp, lens[one], sinks, 0,
                                     s.inp.scale, block_table=bt[one], nthreads=cores)
@@ -602,7 +616,7 @@ def run_ours(args, rank, world, local_rank):
                      "nominal_peak": round(nominal, 1) if nominal else None,
                      "frac_of_nominal": round(achieved / nominal, 4) if nominal else None},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(args.q_tokens, first.cfg, first.block_table.shape[1])
+        "gpu_launches": launches_per_step(args.q_tokens, first.cfg, first.block_table.shape[1], args.rope)
                         * args.layers * args.steps,
         "timing": ("value: steps back to back, events at the ends; us_per_call and roofline: "
                    "events around every launch in a second pass (includes the launch gap)"),
@@ -820,8 +834,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.q_tokens > 1 and (args.rope or args.kv == "fp8" or args.graph):
-        ap.error("--q-tokens > 1 runs the bf16 multi-token calls without --rope, --kv fp8, --graph")
+    if args.q_tokens > 1 and (args.kv == "fp8" or args.graph):
+        ap.error("--q-tokens > 1 runs the bf16 multi-token calls (with or without --rope), not --kv fp8 or --graph")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

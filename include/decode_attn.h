@@ -244,8 +244,40 @@ DA_API int decode_attn_ring_multi(const void *q, const void *k_new, const void *
                                   void *k_cache, void *v_cache, const int32_t *seq_lens,
                                   const int32_t *q_lens, const float *sinks, int window,
                                   float scale, void *out, da_shape s, int q_tokens, void *stream);
+/*
+ * decode_attn_paged_multi_rope / decode_attn_ring_multi_rope -- the several-token steps
+ * above with the rotary embedding of decode_attn_paged_rope (the SimpleLLM README's changes
+ * table, row "RoPE as one fused kernel at every batch size", applied at each new token's
+ * own position): query row (t, h) and new key (t, g) of every new token t < n are rotated to
+ * position p = L - n + t before the append and the scores (rotate-half pairs, each product
+ * and the sum or difference in fp32, rounded to bf16 nearest even). Cached keys are expected
+ * to be stored rotated already; v is not rotated. Rows t >= n are used as given.
+ *   rope_cos, rope_sin, max_position: as in decode_attn_paged_rope (a position at or beyond
+ *     max_position sets DA_STATUS_BAD_POSITION and uses row 0).
+ *   The rotated q and k_new are written to the multi-token workspace (its size from
+ *     decode_attn_multi_workspace_bytes covers them) by a kernel launched ahead of the
+ *     attention, so the call makes one launch more than decode_attn_multi_launches says.
+ *     q and k_new themselves are not modified.
+ *   The other arguments, the results and the errors as in decode_attn_paged_multi /
+ *   decode_attn_ring_multi; null tables return DA_ERR_INVALID_ARG.
+ */
+DA_API int decode_attn_paged_multi_rope(const void *q, const void *k_new, const void *v_new,
+                                        void *k_cache, void *v_cache, const int32_t *block_table,
+                                        const int32_t *seq_lens, const int32_t *q_lens,
+                                        const float *sinks, const float *rope_cos,
+                                        const float *rope_sin, int max_position, int window,
+                                        float scale, void *out, da_shape s, int q_tokens,
+                                        int page_size, int max_pages_per_seq, int num_pages,
+                                        int max_seq_len, void *stream);
+DA_API int decode_attn_ring_multi_rope(const void *q, const void *k_new, const void *v_new,
+                                       void *k_cache, void *v_cache, const int32_t *seq_lens,
+                                       const int32_t *q_lens, const float *sinks,
+                                       const float *rope_cos, const float *rope_sin,
+                                       int max_position, int window, float scale, void *out,
+                                       da_shape s, int q_tokens, void *stream);
 /* Bytes of the multi-token workspace for a shape, T, the ring capacity (0 for paged calls)
- * and the longest sequence; decode_attn_multi_reserve allocates it (call before capture). */
+ * and the longest sequence (with room for the rotated q and k_new of the _rope forms);
+ * decode_attn_multi_reserve allocates it (call before capture). */
 DA_API size_t decode_attn_multi_workspace_bytes(da_shape s, int q_tokens, int ring_window,
                                                 int max_seq_len);
 DA_API int decode_attn_multi_reserve(size_t bytes);

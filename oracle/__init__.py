@@ -95,7 +95,7 @@ def _load():
             c_int, c_int, c_int, c_int]
         lib.oracle_rope_multi.argtypes = [
             _u16p, _u16p, _i32p, _i32p, _f32p, _f32p, c_int, c_int, c_int, c_int, c_int, c_int,
-            _f64p, _u16p]
+            _f64p, _u16p, _u16p]
         lib.oracle_decode_multi_rope.argtypes = [
             c_int, _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _f32p, _f32p, _f32p,
             c_int, c_int, c_double, _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
@@ -599,10 +599,12 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, window, sca
     return out
 
 
-def rope_multi(q, k_new, seq_lens, rope_cos, rope_sin, q_lens=None):
+def rope_multi(q, k_new, seq_lens, rope_cos, rope_sin, q_lens=None, with_q_bf16=False):
     """Several-token rotary embedding: query row (t, h) and new key (t, g), t < n, rotated to
-    their own position L - n + t. Returns (q64 [B, T, Hq, D] float64, zero rows for t >= n;
-    k_rot [B, T, Hkv, D] uint16 as stored, rows t >= n copied)."""
+    their own position L - n + t. Returns (q64 [B, T, Hq, D] float64, the exact rotation, zero
+    rows for t >= n; k_rot [B, T, Hkv, D] uint16 as stored, rows t >= n copied), and with
+    with_q_bf16 also q_rot [B, T, Hq, D] uint16: the query as the bf16 model holds it after
+    the rotation (rounded like the key; rows t >= n copied)."""
     lib = _load()
     q, kn = _u16(q, "q"), _u16(k_new, "k_new")
     sl, ql = _i32(seq_lens), _i32(q_lens)
@@ -610,17 +612,19 @@ def rope_multi(q, k_new, seq_lens, rope_cos, rope_sin, q_lens=None):
     Hkv = kn.shape[2]
     c, sn, maxpos = _tables(rope_cos, rope_sin, D)
     q64 = np.zeros((B, T, Hq, D), np.float64)
+    qrot = np.zeros_like(q)
     krot = np.zeros_like(kn)
     _check(lib.oracle_rope_multi(_ptr(q, _u16p), _ptr(kn, _u16p), _ptr(sl, _i32p), _ptr(ql, _i32p),
                                  _ptr(c, _f32p), _ptr(sn, _f32p), maxpos, B, T, Hq, Hkv, D,
-                                 _ptr(q64, _f64p), _ptr(krot, _u16p)), "rope_multi")
-    return q64, krot
+                                 _ptr(q64, _f64p), _ptr(qrot, _u16p), _ptr(krot, _u16p)), "rope_multi")
+    return (q64, krot, qrot) if with_q_bf16 else (q64, krot)
 
 
 def decode_multi_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, rope_cos, rope_sin,
                       window, scale, block_table=None, q_lens=None, page_size=16, nthreads=None):
-    """decode_multi with q and k_new rotated first (rope_multi): the several-token step of a
-    model whose keys are stored rotated. The append of the step stores the rotated keys
+    """decode_multi with q and k_new rotated first (rope_multi), both as the bf16 model holds
+    them (the query rounded to bf16 like the stored key): the several-token step of a model
+    whose keys are stored rotated. The append of the step stores the rotated keys
     (kv_append_multi of rope_multi's k_rot)."""
     lib = _load()
     q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")

@@ -991,12 +991,13 @@ int oracle_decode_multi(int ring, const uint16_t *q, const uint16_t *k_new, cons
 
 /* Several query tokens with the rotary embedding (the rotate-half form of the one-token
  * steps above, at each new token's own position): query row (t, h) and new key (t, g),
- * t < n, are rotated to position p = L - n + t -- the query in fp64, the key in fp32 and
- * rounded to bf16 nearest even, as it is stored. Rows t >= n are left as they are (zero
- * queries in q64; keys copied). */
+ * t < n, are rotated to position p = L - n + t. q64 gets the exact rotation of the query
+ * (fp64); qrot (if given) the query as the bf16 model holds it after the rotation, and krot
+ * the key as it is stored: fp32 products and sum or difference, rounded to bf16 nearest
+ * even. Rows t >= n are left as they are (zero in q64; copied into qrot and krot). */
 int oracle_rope_multi(const uint16_t *q, const uint16_t *k_new, const int32_t *seq_lens, const int32_t *q_lens,
                       const float *rope_cos, const float *rope_sin, int max_position, int B, int T, int Hq,
-                      int Hkv, int D, double *q64, uint16_t *krot) {
+                      int Hkv, int D, double *q64, uint16_t *qrot, uint16_t *krot) {
     if (!q || !seq_lens || !rope_cos || !rope_sin || !q64 || (k_new && !krot) || D % 2 || max_position <= 0 ||
         B < 0 || T <= 0)
         return OR_BAD_ARG;
@@ -1013,6 +1014,9 @@ int oracle_rope_multi(const uint16_t *q, const uint16_t *k_new, const int32_t *s
                 const size_t off = (((size_t)b * T + t) * Hq + hq) * D;
                 if (active) rope_row_f64(q + off, rope_cos + row, rope_sin + row, D, q64 + off);
                 else for (int d = 0; d < D; ++d) q64[off + d] = 0.0;
+                if (!qrot) continue;
+                if (active) rope_row_bf16(q + off, rope_cos + row, rope_sin + row, D, qrot + off);
+                else memcpy(qrot + off, q + off, sizeof(uint16_t) * (size_t)D);
             }
             if (!k_new) continue;
             for (int g = 0; g < Hkv; ++g) {
@@ -1026,7 +1030,8 @@ int oracle_rope_multi(const uint16_t *q, const uint16_t *k_new, const int32_t *s
 }
 
 /* The several-token step with the rotary embedding: rotate (oracle_rope_multi), then attend
- * exactly as oracle_decode_multi with the rotated queries and keys. */
+ * exactly as oracle_decode_multi with the rotated queries and keys, both as the bf16 model
+ * holds them (the query rounded to bf16 like the stored key). */
 int oracle_decode_multi_rope(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
                              const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_table,
                              const int32_t *seq_lens, const int32_t *q_lens, const float *sinks,
@@ -1035,15 +1040,18 @@ int oracle_decode_multi_rope(int ring, const uint16_t *q, const uint16_t *k_new,
                              int max_pages, int num_pages, int nthreads) {
     if (!k_new) return OR_BAD_ARG;
     double *q64 = (double *)malloc(sizeof(double) * (size_t)B * T * Hq * D + 1);
+    uint16_t *qrot = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)B * T * Hq * D + 1);
     uint16_t *krot = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)B * T * Hkv * D + 1);
-    int st = (q64 && krot) ? OR_OK : OR_NOMEM;
+    int st = (q64 && qrot && krot) ? OR_OK : OR_NOMEM;
     if (st == OR_OK)
         st = oracle_rope_multi(q, k_new, seq_lens, q_lens, rope_cos, rope_sin, max_position, B, T, Hq, Hkv, D,
-                               q64, krot);
+                               q64, qrot, krot);
     if (st == OR_OK)
-        st = decode_multi_q64(ring, q, q64, krot, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks,
-                              window, scale, out, B, T, Hq, Hkv, D, page_size, max_pages, num_pages, nthreads);
+        st = decode_multi_q64(ring, qrot, NULL, krot, v_new, k_cache, v_cache, block_table, seq_lens, q_lens,
+                              sinks, window, scale, out, B, T, Hq, Hkv, D, page_size, max_pages, num_pages,
+                              nthreads);
     free(q64);
+    free(qrot);
     free(krot);
     return st;
 }

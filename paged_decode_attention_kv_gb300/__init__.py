@@ -33,6 +33,7 @@ __all__ = [
     "decode_attn_multi_reserve", "decode_attn_multi_launches", "decode_attn_test_expire_wait",
     "decode_attn_paged_fp8_rope", "decode_attn_ring_fp8_rope", "decode_attn_set_early_inputs",
     "decode_attn_stream_reserve", "decode_attn_stream_release",
+    "decode_attn_paged_multi_rope", "decode_attn_ring_multi_rope",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -103,6 +104,11 @@ def load_library():
                                             c_int, vp]
     lib.decode_attn_ring_multi.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, f32p, c_int, c_float,
                                            vp, da_shape, c_int, vp]
+    lib.decode_attn_paged_multi_rope.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, i32p, f32p, f32p,
+                                                 f32p, c_int, c_int, c_float, vp, da_shape, c_int,
+                                                 c_int, c_int, c_int, c_int, vp]
+    lib.decode_attn_ring_multi_rope.argtypes = [vp, vp, vp, vp, vp, i32p, i32p, f32p, f32p, f32p,
+                                                c_int, c_int, c_float, vp, da_shape, c_int, vp]
     lib.decode_attn_multi_workspace_bytes.argtypes = [da_shape, c_int, c_int, c_int]
     lib.decode_attn_multi_workspace_bytes.restype = ctypes.c_size_t
     lib.decode_attn_multi_launches.argtypes = [da_shape, c_int, c_int, c_int]
@@ -124,7 +130,8 @@ def load_library():
                lib.decode_attn_ring_multi, lib.decode_attn_multi_reserve,
                lib.decode_attn_test_expire_wait, lib.decode_attn_paged_fp8_rope,
                lib.decode_attn_ring_fp8_rope, lib.decode_attn_set_early_inputs,
-               lib.decode_attn_stream_reserve, lib.decode_attn_stream_release):
+               lib.decode_attn_stream_reserve, lib.decode_attn_stream_release,
+               lib.decode_attn_paged_multi_rope, lib.decode_attn_ring_multi_rope):
         fn.restype = c_int
     _lib = lib
     return lib
@@ -322,6 +329,38 @@ def decode_attn_ring_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, s
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
         _ptr(q_lens), _ptr(sinks), int(W), float(scale), _ptr(out), da_shape(B, Hq, Hkv, D), T,
         _stream(stream)))
+    return out
+
+
+def decode_attn_paged_multi_rope(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, sinks,
+                                 rope_cos, rope_sin, window, scale, out, q_lens=None, max_seq_len=None,
+                                 stream=None):
+    """decode_attn_paged_multi with the rotary embedding: each new token's query rows and key
+    rotated to its own position (rope_cos / rope_sin fp32 [max_position, 32] device tables)."""
+    B, T, Hq, D = q.shape
+    num_pages, Hkv = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * 16
+    lib = load_library()
+    _check(lib.decode_attn_paged_multi_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(q_lens), _ptr(sinks), _ptr(rope_cos), _ptr(rope_sin),
+        int(rope_cos.shape[0]), int(window), float(scale), _ptr(out), da_shape(B, Hq, Hkv, D), T,
+        16, max_pages, num_pages, int(max_seq_len), _stream(stream)))
+    return out
+
+
+def decode_attn_ring_multi_rope(q, k_new, v_new, k_cache, v_cache, seq_lens, sinks, rope_cos,
+                                rope_sin, scale, out, q_lens=None, stream=None):
+    """decode_attn_ring_multi with the rotary embedding (see decode_attn_paged_multi_rope)."""
+    B, T, Hq, D = q.shape
+    Hkv, W = k_cache.shape[1], k_cache.shape[2]
+    lib = load_library()
+    _check(lib.decode_attn_ring_multi_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        _ptr(q_lens), _ptr(sinks), _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]), int(W),
+        float(scale), _ptr(out), da_shape(B, Hq, Hkv, D), T, _stream(stream)))
     return out
 
 

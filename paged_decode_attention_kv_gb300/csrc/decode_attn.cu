@@ -2550,13 +2550,25 @@ MultiPlan multi_plan(const da_shape &s, int T, bool ring, int window, int max_se
     return m;
 }
 
+// Bytes of the rotated q and k_new of a several-token call with the rotary embedding (they
+// follow the counters and partials in the multi-token workspace, 256-byte aligned).
+size_t rope_scratch_bytes(const da_shape &s, int T) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t rows = static_cast<size_t>(s.batch) * T;
+    return up(rows * s.num_q_heads * kD * 2) + up(rows * s.num_kv_heads * kD * 2);
+}
+
 int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
               const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens, const float *sinks,
               int window, float scale, void *out, const da_shape &s, int T, int page_size, int max_pages,
-              int num_pages, int max_seq_len, void *stream_v) {
+              int num_pages, int max_seq_len, void *stream_v, const float *rope_cos = nullptr,
+              const float *rope_sin = nullptr, int max_position = 0) {
     int rc = check_shape(s);
     if (rc != DA_OK) return rc;
     if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
+    const bool rope = rope_cos != nullptr || rope_sin != nullptr;
+    if (rope && (!rope_cos || !rope_sin || !aligned16(rope_cos) || !aligned16(rope_sin) || max_position <= 0))
+        return DA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
         !aligned16(out))
         return DA_ERR_INVALID_ARG;
@@ -2580,10 +2592,23 @@ int run_multi(bool ring, const void *q, const void *k_new, const void *v_new, vo
     if (static_cast<long long>(m.splits) * m.row_blocks > 0x7fffffffLL || m.groups > kMMaxGroups)
         return DA_ERR_UNSUPPORTED;
     void *ws = nullptr;
+    const size_t rope_off = (m.counter_bytes + m.part_bytes + 255) & ~static_cast<size_t>(255);
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        rc = workspace_locked(dev, stream, true, m.counter_bytes + m.part_bytes, &ws);
+        rc = workspace_locked(dev, stream, true, rope ? rope_off + rope_scratch_bytes(s, T) : m.counter_bytes + m.part_bytes,
+                              &ws);
         if (rc != DA_OK) return rc;
+    }
+    if (rope) {  // rotate q and k_new into the workspace; the attention reads them from there
+        __nv_bfloat16 *q_rot = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + rope_off);
+        __nv_bfloat16 *k_rot = q_rot + ((static_cast<size_t>(s.batch) * T * s.num_q_heads * kD + 127) & ~static_cast<size_t>(127));
+        rope_multi_kernel<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(s.batch)), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k_new), seq_lens, q_lens,
+            rope_cos, rope_sin, max_position, T, s.num_q_heads, s.num_kv_heads, q_rot, k_rot);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_cuda_error(e);
+        q = q_rot;
+        k_new = k_rot;
     }
     if (m.dec) {  // the decode kernel's several-token form, on this workspace
         Params dp;
@@ -2946,13 +2971,36 @@ int decode_attn_ring_multi(const void *q, const void *k_new, const void *v_new, 
                      s, q_tokens, kPage, 0, 0, 0, stream);
 }
 
+int decode_attn_paged_multi_rope(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                 void *v_cache, const int32_t *block_table, const int32_t *seq_lens,
+                                 const int32_t *q_lens, const float *sinks, const float *rope_cos,
+                                 const float *rope_sin, int max_position, int window, float scale, void *out,
+                                 da_shape s, int q_tokens, int page_size, int max_pages_per_seq, int num_pages,
+                                 int max_seq_len, void *stream) {
+    if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
+    return run_multi(false, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, q_lens, sinks, window, scale,
+                     out, s, q_tokens, page_size, max_pages_per_seq, num_pages, max_seq_len, stream, rope_cos,
+                     rope_sin, max_position);
+}
+
+int decode_attn_ring_multi_rope(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                void *v_cache, const int32_t *seq_lens, const int32_t *q_lens,
+                                const float *sinks, const float *rope_cos, const float *rope_sin,
+                                int max_position, int window, float scale, void *out, da_shape s, int q_tokens,
+                                void *stream) {
+    if (!rope_cos || !rope_sin) return DA_ERR_INVALID_ARG;
+    return run_multi(true, q, k_new, v_new, k_cache, v_cache, nullptr, seq_lens, q_lens, sinks, window, scale, out,
+                     s, q_tokens, kPage, 0, 0, 0, stream, rope_cos, rope_sin, max_position);
+}
+
 size_t decode_attn_multi_workspace_bytes(da_shape s, int q_tokens, int ring_window, int max_seq_len) {
     if (check_shape(s) != DA_OK || q_tokens <= 0 || q_tokens > kMMaxTokens || max_seq_len < 0 || ring_window < 0)
         return 0;
     int dev;
     if (current_device(&dev) != DA_OK) return 0;
     const MultiPlan m = multi_plan(s, q_tokens, ring_window > 0, ring_window, max_seq_len, sm_count(dev));
-    return m.counter_bytes + m.part_bytes;
+    // with room for the rotated q and k_new of the calls with the rotary embedding
+    return ((m.counter_bytes + m.part_bytes + 255) & ~static_cast<size_t>(255)) + rope_scratch_bytes(s, q_tokens);
 }
 
 int decode_attn_multi_launches(da_shape s, int q_tokens, int ring_window, int max_seq_len) {

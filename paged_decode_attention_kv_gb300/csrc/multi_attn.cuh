@@ -702,3 +702,44 @@ __global__ void kv_append_multi_kernel(const __nv_bfloat16 *__restrict__ k_new,
         *reinterpret_cast<uint4 *>(v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
     }
 }
+
+// The rotary embedding of a several-token step, ahead of its attention: query row (t, h) and
+// new key (t, g) of every new token t < n are rotated to their own position p = L - n + t
+// (rotate-half pairs (i, i + D/2); each product and the sum or difference rounded to fp32,
+// then to bf16 nearest even, as the one-token steps' fused rotation does) into q_rot / k_rot;
+// the rows of tokens t >= n and of inactive slots are copied as they are. One block per
+// (t, b). A position beyond the tables raises DA_STATUS_BAD_POSITION and uses row 0.
+__global__ void rope_multi_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+                                  const int *__restrict__ seq_lens, const int *__restrict__ q_lens,
+                                  const float *__restrict__ rope_cos, const float *__restrict__ rope_sin,
+                                  int max_position, int T, int Hq, int Hkv, __nv_bfloat16 *__restrict__ q_rot,
+                                  __nv_bfloat16 *__restrict__ k_rot) {
+    const int t = blockIdx.x, b = blockIdx.y;
+    const int L = __ldg(seq_lens + b);
+    const int n = q_lens != nullptr ? __ldg(q_lens + b) : T;
+    const bool active = L > 0 && t < n && n <= L;
+    int pos = L - n + t;
+    if (active && pos >= max_position) {
+        if (threadIdx.x == 0) flag_status(DA_STATUS_BAD_POSITION);
+        pos = 0;
+    }
+    constexpr int kHalf = kD / 2;
+    const size_t qrow0 = (static_cast<size_t>(b) * T + t) * Hq, krow0 = (static_cast<size_t>(b) * T + t) * Hkv;
+    const int pairs = (Hq + Hkv) * kHalf;
+    for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
+        const int r = i / kHalf, d = i % kHalf;  // rows 0 .. Hq - 1: queries, then keys
+        const __nv_bfloat16 *src = r < Hq ? q + (qrow0 + r) * kD : k_new + (krow0 + r - Hq) * kD;
+        __nv_bfloat16 *dst = r < Hq ? q_rot + (qrow0 + r) * kD : k_rot + (krow0 + r - Hq) * kD;
+        const __nv_bfloat16 x1 = src[d], x2 = src[d + kHalf];
+        if (!active) {
+            dst[d] = x1;
+            dst[d + kHalf] = x2;
+            continue;
+        }
+        const float c = __ldg(rope_cos + static_cast<size_t>(pos) * kHalf + d);
+        const float sn = __ldg(rope_sin + static_cast<size_t>(pos) * kHalf + d);
+        const float f1 = __bfloat162float(x1), f2 = __bfloat162float(x2);
+        dst[d] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(f1, c), __fmul_rn(f2, sn)));
+        dst[d + kHalf] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(f2, c), __fmul_rn(f1, sn)));
+    }
+}

@@ -118,7 +118,7 @@ PIN_CALLS = [
     multi_rope_pins.test_identity_tables_give_the_plain_step,
     lambda: multi_rope_pins.test_one_new_token_is_the_one_token_step(0),
     multi_rope_pins.test_each_token_is_rotated_at_its_own_position,
-    multi_rope_pins.test_stored_keys_round_as_fp32_then_bf16,
+    multi_rope_pins.test_rotated_rows_round_as_fp32_then_bf16,
 ]
 
 
