@@ -87,6 +87,8 @@ def test_launch_count_sums_the_library_answer_per_layer(monkeypatch):
     assert seen == []
     assert bench.launches_per_step(4, cfg, 495) == 3
     assert seen == [(64, 64, 8, 4, 0, 495 * 16), (64, 64, 8, 4, 128, 0)]
+    # with the rotary embedding each layer's call launches its rotation kernel first
+    assert bench.launches_per_step(4, cfg, 495, rope=True) == 5
     monkeypatch.setattr(da, "decode_attn_multi_launches", lambda *a: 0)
     with pytest.raises(RuntimeError):
         bench.launches_per_step(4, cfg, 495)
