@@ -354,7 +354,9 @@ DA_API int decode_attn_stream_reserve(void *stream, size_t bytes, size_t multi_b
  * decode_attn_stream_release -- synchronise `stream` and free the workspaces that
  * decode_attn_stream_reserve gave it; later calls on it use the device's workspace again.
  * A graph captured on the stream keeps the freed addresses: do not launch it afterwards.
- * Release before destroying the stream (a new stream may get the same handle). Returns
+ * Release before destroying the stream (a new stream may get the same handle). The
+ * library's lock is held while the stream synchronises, so attention calls made meanwhile
+ * from other host threads wait for it: release between steps, not inside one. Returns
  * DA_OK also when the stream has none, DA_ERR_WORKSPACE while it is capturing.
  */
 DA_API int decode_attn_stream_release(void *stream);
