@@ -25,7 +25,8 @@ _FUNCS = ("oracle_decode_paged", "oracle_decode_ring", "oracle_decode_contig",
           "oracle_quantise_rows", "oracle_decode_paged_fp8", "oracle_decode_ring_fp8",
           "oracle_kv_append_fp8", "oracle_scatter_fp8", "oracle_decode_multi",
           "oracle_kv_append_multi", "oracle_decode_paged_fp8_rope", "oracle_decode_ring_fp8_rope",
-          "oracle_rope_multi", "oracle_decode_multi_rope")
+          "oracle_rope_multi", "oracle_decode_multi_rope", "oracle_decode_multi_fp8",
+          "oracle_kv_append_multi_fp8")
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -96,6 +97,12 @@ def _load():
         lib.oracle_rope_multi.argtypes = [
             _u16p, _u16p, _i32p, _i32p, _f32p, _f32p, c_int, c_int, c_int, c_int, c_int, c_int,
             _f64p, _u16p, _u16p]
+        lib.oracle_decode_multi_fp8.argtypes = [
+            c_int, _u16p, _u16p, _u16p, _u8p, _i32p, _i32p, _i32p, _f32p, c_int, c_double, _f64p,
+            c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int]
+        lib.oracle_kv_append_multi_fp8.argtypes = [
+            c_int, _u16p, _u16p, _u8p, _i32p, _i32p, _i32p, c_int, c_int, c_int, c_int, c_int, c_int,
+            c_int, c_int]
         lib.oracle_decode_multi_rope.argtypes = [
             c_int, _u16p, _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _f32p, _f32p, _f32p,
             c_int, c_int, c_double, _f64p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
@@ -660,3 +667,43 @@ def kv_append_multi(k_new, v_new, k_cache, v_cache, seq_lens, window=0, block_ta
         _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(ql, _i32p), int(window), B, T, Hkv, D, page_size,
         0 if ring else bt.shape[1], 0 if ring else kc.shape[0]), "kv_append_multi")
     return kc, vc
+
+
+# ---------------------------------------------------------------- several query tokens, fp8 cache
+def decode_multi_fp8(q, k_new, v_new, cache, seq_lens, sinks, window, scale, block_table=None,
+                     q_lens=None, nthreads=None):
+    """decode_multi over an fp8 cache (Fp8Cache: paged when a block table is given, else the
+    ring of capacity `window`): history rows dequantised from their blocks, each new token
+    quantised as its append stores it. Returns out [B, T, Hq, D] float64."""
+    lib = _load()
+    q, k_new, v_new = _u16(q, "q"), _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    sl, ql, sk = _i32(seq_lens), _i32(q_lens), _f32(sinks)
+    B, T, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    ring = block_table is None
+    bt = None if ring else _i32(block_table)
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    _check(lib.oracle_decode_multi_fp8(
+        int(ring), _ptr(q, _u16p), _ptr(k_new, _u16p), _ptr(v_new, _u16p), cache.ptr(),
+        _ptr(bt, _i32p), _ptr(sl, _i32p), _ptr(ql, _i32p), _ptr(sk, _f32p), int(window),
+        float(scale), _ptr(out, _f64p), B, T, Hq, Hkv, D, cache.P,
+        0 if ring else bt.shape[1], 0 if ring else cache.blocks.shape[0],
+        nthreads or default_threads()), "decode_multi_fp8")
+    return out
+
+
+def kv_append_multi_fp8(k_new, v_new, cache, seq_lens, block_table=None, window=0, q_lens=None):
+    """A copy of the fp8 cache with the step's n = q_lens[b] (or T) new tokens quantised into
+    their blocks."""
+    lib = _load()
+    kn, vn = _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    sl, ql = _i32(seq_lens), _i32(q_lens)
+    out = cache.copy()
+    B, T, Hkv, D = kn.shape
+    ring = block_table is None
+    bt = None if ring else _i32(block_table)
+    _check(lib.oracle_kv_append_multi_fp8(
+        int(ring), _ptr(kn, _u16p), _ptr(vn, _u16p), out.ptr(), _ptr(bt, _i32p), _ptr(sl, _i32p),
+        _ptr(ql, _i32p), int(window), B, T, Hkv, D, out.P, 0 if ring else bt.shape[1],
+        0 if ring else out.blocks.shape[0]), "kv_append_multi_fp8")
+    return out

@@ -1089,3 +1089,147 @@ int oracle_kv_append_multi(int ring, const uint16_t *k_new, const uint16_t *v_ne
     }
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* Several query tokens per sequence over an fp8 cache: the several-token step above
+ * (positions, causal and window bounds, counts, zero rows) with every key and value row
+ * taken as the fp8 cache holds it -- history rows dequantised from their blocks, and the new
+ * token j - base quantised exactly as its append stores it (quantise_row) and dequantised. */
+typedef struct {
+    int ring;
+    const uint16_t *q, *k_new, *v_new;
+    const uint8_t *blocks;
+    const int32_t *block_table, *seq_lens, *q_lens;
+    const float *sinks;
+    int window; double scale;
+    int B, T, Hq, Hkv, D, P, max_pages, num_pages;
+    double *out;
+} problemM8;
+
+static int rowsM8(const problemM8 *pr, int b, int g, int j, double *k, double *v) {
+    const int L = pr->seq_lens[b], n = q_count(pr->q_lens, pr->T, b), base = L - n, D = pr->D, P = pr->P;
+    if (j >= base) {
+        uint8_t ck[256], cv[256];
+        float sk, sv;
+        const size_t src = (((size_t)b * pr->T + (j - base)) * pr->Hkv + g) * D;
+        quantise_row(pr->k_new + src, D, ck, &sk);
+        quantise_row(pr->v_new + src, D, cv, &sv);
+        for (int d = 0; d < D; ++d) { k[d] = e4m3_decode(ck[d]) * sk; v[d] = e4m3_decode(cv[d]) * sv; }
+        return OR_OK;
+    }
+    int slot = 0;
+    const long long bi = blk8_of(pr->ring, b, g, j, pr->Hkv, P, pr->window, pr->block_table, pr->max_pages,
+                                 pr->num_pages, &slot);
+    if (bi < 0) return OR_BAD_INDEX;
+    const uint8_t *blk = pr->blocks + (size_t)bi * blk8_bytes(P, D);
+    const double sk = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)slot);
+    const double sv = f32_at(blk + 2 * (size_t)P * D + 4 * (size_t)(P + slot));
+    for (int d = 0; d < D; ++d) {
+        k[d] = e4m3_decode(blk[(size_t)slot * D + d]) * sk;
+        v[d] = e4m3_decode(blk[(size_t)P * D + (size_t)d * P + slot]) * sv;
+    }
+    return OR_OK;
+}
+
+static int attend_oneM8(const problemM8 *pr, int b, int t, int h, double *out) {
+    const int D = pr->D, L = pr->seq_lens[b], n = q_count(pr->q_lens, pr->T, b);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (L <= 0 || t >= n) return OR_OK;
+    const int g = h / (pr->Hq / pr->Hkv);
+    const int p = L - n + t;
+    const int W = pr->window;
+    const int lo = (W > 0 && p - W + 1 > 0) ? p - W + 1 : 0;
+    const int cnt = p - lo + 1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)cnt);
+    double *kv = (double *)malloc(sizeof(double) * 2 * (size_t)D);
+    if (!s || !kv) { free(s); free(kv); return OR_NOMEM; }
+    const uint16_t *qrow = pr->q + (((size_t)b * pr->T + t) * pr->Hq + h) * D;
+    const double sigma = pr->sinks ? (double)pr->sinks[h] : -INFINITY;
+    double M = sigma;
+    int st = OR_OK;
+    for (int i = 0; i < cnt && st == OR_OK; ++i) {
+        st = rowsM8(pr, b, g, lo + i, kv, kv + D);
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * kv[d];
+        s[i] = pr->scale * dot;
+        if (s[i] > M) M = s[i];
+    }
+    double den = isinf(sigma) && sigma < 0 ? 0.0 : exp(sigma - M);
+    for (int i = 0; i < cnt && st == OR_OK; ++i) {
+        st = rowsM8(pr, b, g, lo + i, kv, kv + D);
+        const double w = exp(s[i] - M);
+        den += w;
+        for (int d = 0; d < D; ++d) out[d] += w * kv[D + d];
+    }
+    if (st == OR_OK) for (int d = 0; d < D; ++d) out[d] /= den;
+    free(s); free(kv);
+    return st;
+}
+
+typedef struct { problemM8 *pr; int tid, nthreads, status; } workerM8_arg;
+
+static void *workerM8(void *arg) {
+    workerM8_arg *a = (workerM8_arg *)arg;
+    problemM8 *pr = a->pr;
+    const long long total = (long long)pr->B * pr->T * pr->Hq;
+    for (long long w = a->tid; w < total; w += a->nthreads) {
+        const int h = (int)(w % pr->Hq), t = (int)((w / pr->Hq) % pr->T), b = (int)(w / ((long long)pr->Hq * pr->T));
+        const int st = attend_oneM8(pr, b, t, h, pr->out + (size_t)w * pr->D);
+        if (st != OR_OK && a->status == OR_OK) a->status = st;
+    }
+    return NULL;
+}
+
+int oracle_decode_multi_fp8(int ring, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                            const uint8_t *blocks, const int32_t *block_table, const int32_t *seq_lens,
+                            const int32_t *q_lens, const float *sinks, int window, double scale, double *out,
+                            int B, int T, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                            int nthreads) {
+    if (!q || !k_new || !v_new || !blocks || !seq_lens || !out || B < 0 || T <= 0 || Hq <= 0 || Hkv <= 0 ||
+        Hq % Hkv || D <= 0 || D > 256 || window < 0 || page_size <= 0 ||
+        (ring && (window <= 0 || window % page_size != 0)) ||
+        (!ring && (!block_table || max_pages <= 0 || num_pages <= 0)))
+        return OR_BAD_ARG;
+    if (check_counts(seq_lens, q_lens, B, T) != OR_OK) return OR_BAD_ARG;
+    problemM8 pr = {ring, q, k_new, v_new, blocks, block_table, seq_lens, q_lens, sinks, window, scale,
+                    B, T, Hq, Hkv, D, page_size, max_pages, num_pages, out};
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    workerM8_arg args[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) { args[t].pr = &pr; args[t].tid = t; args[t].nthreads = nthreads; args[t].status = OR_OK; }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, workerM8, &args[t]) != 0) break;
+        started = t;
+    }
+    for (int t = started + 1; t < nthreads; ++t) workerM8(&args[t]);
+    workerM8(&args[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    for (int t = 0; t < nthreads; ++t) if (args[t].status != OR_OK) return args[t].status;
+    return OR_OK;
+}
+
+/* The append of a several-token step into an fp8 cache: new token t < n of b, quantised, to
+ * position L - n + t (ring: cell (L - n + t) % W, written in order, so the last W survive). */
+int oracle_kv_append_multi_fp8(int ring, const uint16_t *k_new, const uint16_t *v_new, uint8_t *blocks,
+                               const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                               int window, int B, int T, int Hkv, int D, int page_size, int max_pages,
+                               int num_pages) {
+    if (!k_new || !v_new || !blocks || !seq_lens || D > 256 || page_size <= 0 ||
+        (ring && (window <= 0 || window % page_size != 0)) || (!ring && (!block_table || max_pages <= 0)))
+        return OR_BAD_ARG;
+    if (check_counts(seq_lens, q_lens, B, T) != OR_OK) return OR_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b], n = q_count(q_lens, T, b);
+        if (L <= 0) continue;
+        for (int t = 0; t < n; ++t)
+            for (int g = 0; g < Hkv; ++g) {
+                const size_t src = (((size_t)b * T + t) * Hkv + g) * D;
+                const int st = put8(ring, blocks, b, g, L - n + t, k_new + src, v_new + src, Hkv, D, page_size,
+                                    window, block_table, max_pages, num_pages);
+                if (st != OR_OK) return st;
+            }
+    }
+    return OR_OK;
+}
