@@ -14,6 +14,7 @@ import test_oracle as pins
 import test_oracle_fp8 as fp8_pins
 import test_oracle_multi as multi_pins
 import test_oracle_multi_rope as multi_rope_pins
+import test_oracle_multi_fp8 as multi_fp8_pins
 import test_oracle_rope as rope_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -79,6 +80,12 @@ MUTANTS = [
      "const size_t qoff = (((size_t)t * pr->B + b) * pr->Hq + h) * D;"),
     ("multi_rope_position", "const int p = L - n + t;\n            if (active && p >= max_position)",
      "const int p = L - 1;\n            if (active && p >= max_position)"),
+    ("multi_fp8_new_token_from_cache",
+     "const int L = pr->seq_lens[b], n = q_count(pr->q_lens, pr->T, b), base = L - n, D = pr->D, P = pr->P;\n    if (j >= base) {",
+     "const int L = pr->seq_lens[b], n = q_count(pr->q_lens, pr->T, b), base = L - n, D = pr->D, P = pr->P;\n    if (j > base) {"),
+    ("multi_fp8_append_order",
+     "const int st = put8(ring, blocks, b, g, L - n + t, k_new + src",
+     "const int st = put8(ring, blocks, b, g, L - 1 - t, k_new + src"),
     ("append_wrong_cell",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(p % page_size)) * D;",
      "size_t dst = (((size_t)page * Hkv + g) * page_size + (size_t)(L % page_size)) * D;"),
@@ -119,6 +126,9 @@ PIN_CALLS = [
     lambda: multi_rope_pins.test_one_new_token_is_the_one_token_step(0),
     multi_rope_pins.test_each_token_is_rotated_at_its_own_position,
     multi_rope_pins.test_rotated_rows_round_as_fp32_then_bf16,
+    lambda: multi_fp8_pins.test_one_new_token_is_the_one_token_fp8_step(0),
+    lambda: multi_fp8_pins.test_exact_values_give_the_bf16_step(0),
+    lambda: multi_fp8_pins.test_append_equals_quantising_the_whole_history(False),
 ]
 
 
